@@ -1,0 +1,355 @@
+/*
+ * spx_oracle.c -- CPU oracle for the Specter per-layer MoE expert path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, single-threaded
+ * restatement of what the path computes, used by the tests, by the smoke
+ * check and by the benchmark's CPU-baseline leg.  The CUDA library never
+ * links, includes or calls it, and it shares no code with the library.
+ *
+ * Arithmetic is IEEE binary64 throughout (the pages fix no precision for a
+ * reference); inputs arrive as fp16 bit patterns, int32 GPTQ words and fp32
+ * logits.  Where a floating-point value decides an integer (the top-k
+ * selection), the decision is taken on the fp32 value, as the kernels do.
+ *
+ * Sources, cited by page title and section:
+ *  [S1] ai.info, "Specter: Fast MoE Inference via Quantization-Enabled
+ *       Multi-Step Speculative Offloading" (AI summary): Key Contributions
+ *       items 1-4 and "Methodology in Plain English" -- INT4 copy of the
+ *       target's experts as draft, FP16 gates and shared experts, GPU-side
+ *       per-layer expert-activation counters (the Expert Lookahead Buffer),
+ *       tokens gathered by expert and computed in one fused draft launch,
+ *       expert-wise packing of verification tokens ("mathematically
+ *       identical").
+ *  [S2] richland.au, "Specter previews expert routing with an INT4 copy of
+ *       the model itself", section "What shipped" -- GPTQ INT4, group size
+ *       128, routers and shared experts reuse the target's FP16 tensors,
+ *       W4A16 kernels that dequantise INT4 tiles and compute in FP16.
+ *  Readings where the pages are silent (top-k key and tie order, renorm,
+ *  GPTQ nibble order and zero point, SwiGLU form, combine) are listed
+ *  beside each function and in the design notes.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* IEEE 754 binary16 <-> binary64                                       */
+/* ------------------------------------------------------------------ */
+
+/* Decode a binary16 bit pattern: sign, 5-bit biased exponent (bias 15),
+ * 10-bit fraction; exponent 0 = subnormal (fraction * 2^-24), 31 = inf/NaN. */
+double orc_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 0x1f;
+    int fr = h & 0x3ff;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)fr, -24);
+    else if (ex == 31)
+        v = fr ? NAN : INFINITY;
+    else
+        v = ldexp((double)(fr | 0x400), ex - 25);
+    return sign ? -v : v;
+}
+
+/* Encode to binary16 with round-to-nearest, ties-to-even. */
+uint16_t orc_double_to_half(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v))
+        return 0x7e00;
+    if (a >= 65520.0) /* halfway between 65504 and 2^16 rounds to even = inf */
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal: quantum 2^-24; rint() is ties-to-even in the default mode.
+         * A result of 1024 is the bit pattern of the smallest normal. */
+        double m = rint(ldexp(a, 24));
+        return sign | (uint16_t)m;
+    }
+    int e2;
+    frexp(a, &e2);           /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;          /* a in [2^E, 2^(E+1)) */
+    double m = rint(ldexp(a, 10 - E)); /* in [1024, 2048] */
+    if (m >= 2048.0) {
+        m = 1024.0;
+        E += 1;
+    }
+    if (E + 15 >= 31)
+        return sign | 0x7c00;
+    return sign | (uint16_t)(((E + 15) << 10) | ((int)m - 1024));
+}
+
+void orc_halves_to_doubles(const uint16_t *in, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_half_to_double(in[i]);
+}
+
+void orc_doubles_to_halves(const double *in, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_double_to_half(in[i]);
+}
+
+/* decode table, filled from orc_half_to_double on first use */
+static double g_half_tab[65536];
+static int g_half_tab_ready = 0;
+
+static const double *half_tab(void)
+{
+    if (!g_half_tab_ready) {
+        for (int i = 0; i < 65536; ++i)
+            g_half_tab[i] = orc_half_to_double((uint16_t)i);
+        g_half_tab_ready = 1;
+    }
+    return g_half_tab;
+}
+
+/* ------------------------------------------------------------------ */
+/* Router: logits, softmax, top-k, weights  [S1 Key Contributions 2;    */
+/* S2 What shipped: routers reuse the target's FP16 tensors]           */
+/* ------------------------------------------------------------------ */
+
+/* logits[t][e] = sum_h x[t][h] * wr[e][h], h ascending. */
+void orc_router_logits(const uint16_t *x, const uint16_t *wr, int T, int H, int E, double *logits)
+{
+    const double *tab = half_tab();
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += tab[x[(int64_t)t * H + h]] * tab[wr[(int64_t)e * H + h]];
+            logits[(int64_t)t * E + e] = acc;
+        }
+}
+
+/* Reading: the k experts with the largest logits (logits rounded to fp32,
+ * the precision the kernels decide in), ties to the lower expert index,
+ * listed in descending order; softmax over all E experts in fp64;
+ * weight = p[id], or p[id] / sum of the selected p when renorm != 0.
+ * probs (nullable) receives the full softmax [T][E]. */
+void orc_route_topk(const double *logits, int T, int E, int k, int renorm,
+                    int32_t *ids, double *w, double *probs)
+{
+    float *lf = (float *)malloc(sizeof(float) * (size_t)E);
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    int *order = (int *)malloc(sizeof(int) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e)
+            lf[e] = (float)logits[(int64_t)t * E + e];
+        /* softmax */
+        double m = -INFINITY;
+        for (int e = 0; e < E; ++e)
+            if ((double)lf[e] > m)
+                m = (double)lf[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) {
+            p[e] = exp((double)lf[e] - m);
+            z += p[e];
+        }
+        for (int e = 0; e < E; ++e)
+            p[e] /= z;
+        if (probs)
+            for (int e = 0; e < E; ++e)
+                probs[(int64_t)t * E + e] = p[e];
+        /* stable insertion sort of expert indices by descending fp32 logit;
+         * equal logits keep ascending index order (lower index first) */
+        for (int e = 0; e < E; ++e) {
+            int j = e;
+            while (j > 0 && lf[order[j - 1]] < lf[e]) {
+                order[j] = order[j - 1];
+                --j;
+            }
+            order[j] = e;
+        }
+        double sel = 0.0;
+        for (int j = 0; j < k; ++j)
+            sel += p[order[j]];
+        for (int j = 0; j < k; ++j) {
+            ids[(int64_t)t * k + j] = order[j];
+            w[(int64_t)t * k + j] = renorm ? p[order[j]] / sel : p[order[j]];
+        }
+    }
+    free(lf);
+    free(p);
+    free(order);
+}
+
+/* ------------------------------------------------------------------ */
+/* Expert Lookahead Buffer: layer-indexed activation counters           */
+/* [S1 Key Contributions 3; Methodology: counters tally how often each  */
+/* expert in each layer is selected as draft tokens are generated]      */
+/* ------------------------------------------------------------------ */
+
+/* elb is [L][E]; one increment per (token, slot) selection. */
+void orc_elb_accumulate(uint32_t *elb, int E, int layer, const int32_t *ids, int T, int k)
+{
+    for (int s = 0; s < T * k; ++s)
+        elb[(int64_t)layer * E + ids[s]] += 1u;
+}
+
+/* ------------------------------------------------------------------ */
+/* Gather tokens by expert [S1 Key Contributions 4: the fused draft     */
+/* kernel gathers tokens by expert; verification packs tokens routed    */
+/* to the same expert together]                                         */
+/* ------------------------------------------------------------------ */
+
+/* Counting sort of the flat slots s = t*k + j by expert id: counts[e];
+ * offsets = exclusive prefix sum (E+1 entries); sorted_slots lists slots
+ * in ascending expert, then ascending slot order; active lists the experts
+ * with count > 0 in ascending order, n_active of them. */
+void orc_gather_by_expert(const int32_t *ids, int T, int k, int E, int32_t *counts,
+                          int32_t *offsets, int32_t *sorted_slots, int32_t *active,
+                          int32_t *n_active)
+{
+    int n = T * k;
+    for (int e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int s = 0; s < n; ++s)
+        counts[ids[s]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e)
+        fill[e] = offsets[e];
+    for (int s = 0; s < n; ++s)
+        sorted_slots[fill[ids[s]]++] = s;
+    free(fill);
+    int a = 0;
+    for (int e = 0; e < E; ++e)
+        if (counts[e] > 0)
+            active[a++] = e;
+    for (int e = a; e < E; ++e)
+        active[e] = -1;
+    *n_active = a;
+}
+
+/* ------------------------------------------------------------------ */
+/* GPTQ INT4, group 128, zero point 8  [S2 What shipped]                */
+/* ------------------------------------------------------------------ */
+
+/* Reading: qweight is [K/8][N] int32, code of row kk at bits 4*(kk%8)..+3
+ * of word (kk/8, n), low nibble first; scales [K/128][N] fp16; no act-order
+ * permutation; W[kk][n] = (code - 8) * scale[kk/128][n]. */
+static inline double w4_at(const int32_t *q, const uint16_t *s, const double *tab, int N, int kk, int n)
+{
+    uint32_t word = (uint32_t)q[(int64_t)(kk / 8) * N + n];
+    int code = (int)((word >> (4 * (kk % 8))) & 15u);
+    return (double)(code - 8) * tab[s[(int64_t)(kk / 128) * N + n]];
+}
+
+/* out[kk][n] = W[kk][n] for the whole K x N matrix. */
+void orc_w4_dequant(const int32_t *q, const uint16_t *s, int K, int N, double *out)
+{
+    const double *tab = half_tab();
+    for (int kk = 0; kk < K; ++kk)
+        for (int n = 0; n < N; ++n)
+            out[(int64_t)kk * N + n] = w4_at(q, s, tab, N, kk, n);
+}
+
+/* ------------------------------------------------------------------ */
+/* Expert MLP: y = W_down ( silu(W_gate x) * (W_up x) )                 */
+/* Reading: SwiGLU, the MLP form of all three named models; silu(z) =   */
+/* z / (1 + exp(-z)); the intermediate h is kept in fp64.              */
+/* ------------------------------------------------------------------ */
+
+static inline double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* INT4 expert (GPTQ layout, gate/up K=H N=I, down K=I N=H) on one token. */
+void orc_swiglu_w4(const uint16_t *x, int H, int I,
+                   const int32_t *qg, const uint16_t *sg,
+                   const int32_t *qu, const uint16_t *su,
+                   const int32_t *qd, const uint16_t *sd,
+                   double *y, double *h_out)
+{
+    const double *tab = half_tab();
+    double *g = (double *)calloc((size_t)I, sizeof(double));
+    double *u = (double *)calloc((size_t)I, sizeof(double));
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    /* g[i] = sum_kk W_g[kk][i] x[kk], kk ascending for every i */
+    for (int kk = 0; kk < H; ++kk) {
+        double xk = tab[x[kk]];
+        for (int i = 0; i < I; ++i) {
+            g[i] += w4_at(qg, sg, tab, I, kk, i) * xk;
+            u[i] += w4_at(qu, su, tab, I, kk, i) * xk;
+        }
+    }
+    for (int i = 0; i < I; ++i)
+        h[i] = silu(g[i]) * u[i];
+    for (int n = 0; n < H; ++n)
+        y[n] = 0.0;
+    for (int i = 0; i < I; ++i)
+        for (int n = 0; n < H; ++n)
+            y[n] += w4_at(qd, sd, tab, H, i, n) * h[i];
+    if (h_out)
+        memcpy(h_out, h, sizeof(double) * (size_t)I);
+    free(g);
+    free(u);
+    free(h);
+}
+
+/* FP16 expert, PyTorch [out, in] layout: wg, wu [I][H]; wd [H][I]. */
+void orc_swiglu_f16(const uint16_t *x, int H, int I,
+                    const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,
+                    double *y, double *h_out)
+{
+    const double *tab = half_tab();
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        const uint16_t *rg = wg + (int64_t)i * H;
+        const uint16_t *ru = wu + (int64_t)i * H;
+        for (int kk = 0; kk < H; ++kk) {
+            double xk = tab[x[kk]];
+            g += tab[rg[kk]] * xk;
+            u += tab[ru[kk]] * xk;
+        }
+        h[i] = silu(g) * u;
+    }
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        const uint16_t *rd = wd + (int64_t)n * I;
+        for (int i = 0; i < I; ++i)
+            acc += tab[rd[i]] * h[i];
+        y[n] = acc;
+    }
+    if (h_out)
+        memcpy(h_out, h, sizeof(double) * (size_t)I);
+    free(h);
+}
+
+/* Sigmoid gate of a gated shared expert: 1 / (1 + exp(-x . w)). */
+double orc_shared_gate(const uint16_t *x, const uint16_t *wsg, int H)
+{
+    const double *tab = half_tab();
+    double z = 0.0;
+    for (int kk = 0; kk < H; ++kk)
+        z += tab[x[kk]] * tab[wsg[kk]];
+    return 1.0 / (1.0 + exp(-z));
+}
+
+/* ------------------------------------------------------------------ */
+/* Weighted scatter-combine                                             */
+/* Reading: out[t] = sum_j w[t][j] * y[t*k+j] + gamma[t] * sh[t], summed */
+/* in ascending j, then rounded once to fp16.                           */
+/* ------------------------------------------------------------------ */
+
+void orc_combine(int T, int H, int k, const double *w, const double *y_slot,
+                 const double *gamma, const double *sh, double *out, uint16_t *out_half)
+{
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j)
+                acc += w[(int64_t)t * k + j] * y_slot[((int64_t)t * k + j) * H + n];
+            if (sh)
+                acc += (gamma ? gamma[t] : 1.0) * sh[(int64_t)t * H + n];
+            out[(int64_t)t * H + n] = acc;
+            if (out_half)
+                out_half[(int64_t)t * H + n] = orc_double_to_half(acc);
+        }
+}

@@ -1,0 +1,348 @@
+"""Pins for the CPU oracle: each check ties an oracle step to something other
+than the oracle itself (a library routine, brute force, a closed form, an
+invariant, or a hand-derived fixture from the format's definition).
+Runs on CPU only."""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit, softmax
+
+import oracle
+import spx_workloads as W
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ fp16
+def test_half_decode_exhaustive_vs_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.half_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zeros survive
+    assert np.signbit(ours[0x8000]) and not np.signbit(ours[0])
+
+
+def test_half_encode_rne_vs_numpy():
+    rng = np.random.default_rng(7)
+    v = np.concatenate([
+        rng.standard_normal(200000) * np.exp(rng.uniform(-20, 12, 200000)),
+        # exact ties between neighbouring halves, normal and subnormal ranges
+        (np.arange(1, 4000, dtype=np.float64) + 0.5) * 2.0 ** -24,
+        (np.arange(1024, 3048, dtype=np.float64) + 0.5) * 2.0 ** -10,
+        np.array([65504.0, 65519.999, 65520.0, 1e9, -65520.0, 2.0 ** -25, 2.0 ** -26,
+                  3 * 2.0 ** -26, 0.0, -0.0, 6.1e-5, 2.0 ** -14 - 2.0 ** -26]),
+    ])
+    ours = oracle.double_to_half(v)
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------- routing
+def _brute_topk(v, k):
+    order = sorted(range(len(v)), key=lambda e: (-float(np.float32(v[e])), e))
+    return order[:k]
+
+
+def test_topk_all_permutations_tiny():
+    for perm in itertools.permutations([0.5, -1.0, 2.0, 0.25]):
+        lg = np.array([perm], np.float64)
+        for k in range(1, 5):
+            ids, _ = oracle.route_topk(lg, k, False)
+            assert list(ids[0]) == _brute_topk(perm, k)
+
+
+def test_topk_ties_lower_index_first_and_signed_zero():
+    lg = np.array([[1.0, 3.0, 3.0, -0.0, 0.0, 3.0, 0.0, -1.0]])
+    ids, _ = oracle.route_topk(lg, 6, False)
+    assert list(ids[0]) == [1, 2, 5, 0, 3, 4]
+
+
+def test_topk_random_vs_stable_argsort():
+    rng = np.random.default_rng(3)
+    for E, k in [(64, 6), (60, 4), (16, 2), (256, 8), (8, 8)]:
+        lg = rng.standard_normal((33, E)).astype(np.float32)
+        lg[:, ::7] = lg[:, :1]  # plant ties
+        ids, _ = oracle.route_topk(lg.astype(np.float64), k, False)
+        ref = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+        assert np.array_equal(ids, ref)
+
+
+def test_topk_decides_in_fp32():
+    # two logits that differ in fp64 but round to the same fp32 value tie
+    a = 1.0
+    b = 1.0 + 2.0 ** -30
+    ids, _ = oracle.route_topk(np.array([[a, b]]), 1, False)
+    assert ids[0, 0] == 0
+
+
+def test_softmax_and_weights_vs_scipy():
+    rng = np.random.default_rng(5)
+    lg = rng.standard_normal((9, 60)).astype(np.float32).astype(np.float64)
+    ids, w, p = oracle.route_topk(lg, 4, False, want_probs=True)
+    ref = softmax(lg, axis=1)
+    assert np.allclose(p, ref, rtol=1e-13, atol=0)
+    assert np.allclose(p.sum(1), 1.0, atol=1e-14)
+    assert np.allclose(w, np.take_along_axis(ref, ids, 1), rtol=1e-13)
+    ids2, w2 = oracle.route_topk(lg, 4, True)
+    assert np.array_equal(ids, ids2)
+    assert np.allclose(w2.sum(1), 1.0, atol=1e-14)
+    sel = np.take_along_axis(ref, ids, 1)
+    assert np.allclose(w2, sel / sel.sum(1, keepdims=True), rtol=1e-13)
+
+
+def test_renorm_with_k_equal_E_is_softmax():
+    rng = np.random.default_rng(6)
+    lg = rng.standard_normal((4, 8)).astype(np.float32).astype(np.float64)
+    ids, w, p = oracle.route_topk(lg, 8, True, want_probs=True)
+    assert np.allclose(w, np.take_along_axis(p, ids, 1), rtol=1e-14)
+
+
+# --------------------------------------------------------- ELB / gather
+def test_elb_counter_sum_and_depth1_golden():
+    g = json.load(open(os.path.join(GOLD, "elb_depth1.json")))
+    E, k = g["E"], g["k"]
+    rng = np.random.default_rng(11)
+    L = 3
+    elb = np.zeros((L, E), np.uint32)
+    expect = np.zeros(L, np.int64)
+    for layer in range(L):
+        for _ in range(5):
+            T = int(rng.integers(1, 18))
+            ids, _ = oracle.route_topk(rng.standard_normal((T, E)), k, False)
+            oracle.elb_accumulate(elb, layer, ids)
+            expect[layer] += T * k
+    # sum of increments per layer = (calls) * T * k
+    assert np.array_equal(elb.sum(1).astype(np.int64), expect)
+    # depth-1 draft step: exactly k distinct experts per layer (the pages' 6.0)
+    elb1 = np.zeros((1, E), np.uint32)
+    ids, _ = oracle.route_topk(rng.standard_normal((1, E)), k, False)
+    oracle.elb_accumulate(elb1, 0, ids)
+    assert float(np.count_nonzero(elb1[0])) == g["distinct_experts_per_layer"]
+    assert elb1.sum() == k
+
+
+def test_elb_matches_bincount():
+    rng = np.random.default_rng(12)
+    E, k, L = 64, 6, 4
+    elb = np.zeros((L, E), np.uint32)
+    ref = np.zeros((L, E), np.int64)
+    for _ in range(20):
+        layer = int(rng.integers(0, L))
+        T = int(rng.integers(1, 18))
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+        oracle.elb_accumulate(elb, layer, ids)
+        ref[layer] += np.bincount(ids.reshape(-1), minlength=E)
+    assert np.array_equal(elb.astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 6, 64), (17, 6, 64), (9, 4, 60), (17, 2, 16), (4, 2, 8), (3, 8, 8)])
+def test_gather_vs_stable_argsort(T, k, E):
+    rng = np.random.default_rng(T * 100 + k)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    g = oracle.gather_by_expert(ids, E)
+    flat = ids.reshape(-1)
+    assert np.array_equal(g["counts"], np.bincount(flat, minlength=E))
+    assert g["offsets"][0] == 0 and g["offsets"][E] == T * k
+    assert np.array_equal(np.diff(g["offsets"]), g["counts"])
+    assert np.array_equal(g["sorted_slots"], np.argsort(flat, kind="stable"))
+    act = np.nonzero(g["counts"])[0]
+    assert g["n_active"] == len(act)
+    assert np.array_equal(g["active"][:len(act)], act)
+    # scatter(gather(v)) is the identity
+    v = rng.standard_normal(T * k)
+    gathered = v[g["sorted_slots"]]
+    back = np.empty_like(v)
+    back[g["sorted_slots"]] = gathered
+    assert np.array_equal(back, v)
+    # each expert segment holds only that expert, in ascending slot order
+    for e in act:
+        seg = g["sorted_slots"][g["offsets"][e]:g["offsets"][e + 1]]
+        assert np.all(flat[seg] == e) and np.all(np.diff(seg) > 0)
+
+
+def test_gather_all_tokens_on_one_expert():
+    ids = np.array([[3], [3], [3], [3]], np.int32)
+    g = oracle.gather_by_expert(ids, 8)
+    assert g["n_active"] == 1 and g["active"][0] == 3
+    assert list(g["sorted_slots"]) == [0, 1, 2, 3]
+
+
+# ------------------------------------------------------------ dequant
+def test_dequant_hand_packed_golden():
+    gold = json.load(open(os.path.join(GOLD, "gptq_nibbles.json")))
+    for case in gold["cases"]:
+        q = np.array([[case["word"]]], np.int32)
+        s = np.array([[case["scale"]]], np.float16).view(np.uint16)
+        # one word covers rows 0..7; one group row of scales covers 128 rows
+        qq = np.zeros((16, 1), np.int32)
+        qq[0, 0] = q[0, 0]
+        out = oracle.w4_dequant(qq, s)
+        assert list(out[:8, 0]) == case["values"]
+
+
+def test_dequant_every_nibble_position_and_code():
+    K, N = 256, 16
+    codes = (np.arange(K)[:, None] * 7 + np.arange(N)[None, :] * 3) % 16
+    q = np.zeros((K // 8, N), np.uint32)
+    for kk in range(K):
+        q[kk // 8] |= (codes[kk].astype(np.uint32) << np.uint32(4 * (kk % 8)))
+    sc = (np.arange(2 * N, dtype=np.float64).reshape(2, N) + 1) / 64.0
+    s = sc.astype(np.float16)
+    out = oracle.w4_dequant(q.view(np.int32), s.view(np.uint16))
+    ref = (codes - 8) * np.repeat(s.astype(np.float64), 128, axis=0)
+    assert np.array_equal(out, ref)
+    assert set(np.unique(codes)) == set(range(16))
+
+
+# ---------------------------------------------------------------- MLP
+def _identity_w4(n):
+    q = np.full((n // 8, n), 0x88888888, np.uint32)
+    for i in range(n):
+        word = q[i // 8, i]
+        sh = np.uint32(4 * (i % 8))
+        q[i // 8, i] = (word & ~(np.uint32(15) << sh)) | (np.uint32(9) << sh)
+    s = np.ones((n // 128, n), np.float16).view(np.uint16)
+    return q.view(np.int32), s
+
+
+def test_identity_expert_closed_form():
+    n = 256
+    q, s = _identity_w4(n)
+    ex = dict(qw_gate=q, s_gate=s, qw_up=q, s_up=s, qw_down=q, s_down=s)
+    x = (np.random.default_rng(1).standard_normal(n) * 2).astype(np.float16)
+    xd = x.astype(np.float64)
+    ref = xd * expit(xd) * xd  # silu(x) * x through identity gate/up/down
+    y = oracle.swiglu_w4(x.view(np.uint16), ex)
+    assert np.allclose(y, ref, rtol=1e-14, atol=1e-300)
+    eye = np.eye(n).astype(np.float16).view(np.uint16)
+    y16 = oracle.swiglu_f16(x.view(np.uint16), dict(w_gate=eye, w_up=eye, w_down=eye))
+    assert np.allclose(y16, ref, rtol=1e-14, atol=1e-300)
+
+
+def test_f16_mlp_is_textbook_swiglu_via_matmul():
+    rng = np.random.default_rng(2)
+    H, I = 128, 96
+    wg = (rng.standard_normal((I, H)) * 0.1).astype(np.float16)
+    wu = (rng.standard_normal((I, H)) * 0.1).astype(np.float16)
+    wd = (rng.standard_normal((H, I)) * 0.1).astype(np.float16)
+    x = rng.standard_normal(H).astype(np.float16)
+    g = wg.astype(np.float64) @ x.astype(np.float64)
+    u = wu.astype(np.float64) @ x.astype(np.float64)
+    ref = wd.astype(np.float64) @ (g * expit(g) * u)
+    y = oracle.swiglu_f16(x.view(np.uint16), dict(w_gate=wg.view(np.uint16), w_up=wu.view(np.uint16),
+                                                  w_down=wd.view(np.uint16)))
+    assert np.allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_w4_mlp_matches_dequantised_matmul():
+    shape = W.scaled(W.CONFIGS["tiny"], H=256, I=384)
+    ex = W.gen_w4_expert(shape, 0, 0)
+    x = W.gen_x(shape, 1)[0]
+    Wg = oracle.w4_dequant(ex["qw_gate"], ex["s_gate"])   # [H, I]
+    Wu = oracle.w4_dequant(ex["qw_up"], ex["s_up"])
+    Wd = oracle.w4_dequant(ex["qw_down"], ex["s_down"])   # [I, H]
+    xd = x.view(np.float16).astype(np.float64)
+    g, u = xd @ Wg, xd @ Wu
+    ref = (g * expit(g) * u) @ Wd
+    y = oracle.swiglu_w4(x, ex)
+    assert np.allclose(y, ref, rtol=1e-10, atol=1e-10)
+
+
+def test_shared_gate_vs_expit():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(256).astype(np.float16)
+    w = (rng.standard_normal(256) * 0.05).astype(np.float16)
+    ref = expit(float(x.astype(np.float64) @ w.astype(np.float64)))
+    assert abs(oracle.shared_gate(x.view(np.uint16), w.view(np.uint16)) - ref) < 1e-15
+
+
+# ------------------------------------------------------------- combine
+def test_combine_closed_form_and_rounding():
+    rng = np.random.default_rng(8)
+    T, k, H = 3, 2, 16
+    w = rng.random((T, k))
+    y = rng.standard_normal((T, k, H))
+    sh = rng.standard_normal((T, H))
+    gam = rng.random(T)
+    out, outh = oracle.combine(w, y, gam, sh)
+    ref = w[:, 0, None] * y[:, 0] + w[:, 1, None] * y[:, 1] + gam[:, None] * sh
+    assert np.allclose(out, ref, rtol=1e-15, atol=1e-15)
+    assert np.array_equal(outh, out.astype(np.float16).view(np.uint16))
+    out2, _ = oracle.combine(w, y)
+    assert np.allclose(out2, ref - gam[:, None] * sh, rtol=1e-14, atol=1e-14)
+
+
+# --------------------------------------------------------------- layer
+def _tiny_layer(mode, relabel=None):
+    shape = W.CONFIGS["tiny"]
+    x = W.gen_x(shape, shape.T_draft)
+    wr = W.gen_router(shape)
+    perm = np.arange(shape.E) if relabel is None else relabel
+    wr_p = np.empty_like(wr)
+    wr_p[perm] = wr           # expert e is stored under label perm[e]
+    inv = np.argsort(perm)
+
+    def expert(lbl):
+        ex = W.gen_w4_expert(shape, 0, int(inv[lbl]))
+        return ex if mode == "draft" else oracle.f16_copy_of_w4(ex)
+    return oracle.moe_layer(mode, x, shape.k, shape.renorm, expert, shape.E, w_router=wr_p)
+
+
+def test_layer_invariant_under_expert_relabelling():
+    # expert-wise reordering is "mathematically identical": relabelling experts
+    # changes the gather order but not the output
+    base = _tiny_layer("draft")
+    perm = np.random.default_rng(9).permutation(W.CONFIGS["tiny"].E)
+    other = _tiny_layer("draft", perm)
+    assert np.array_equal(base["out_half"], other["out_half"])
+    assert np.array_equal(perm[base["ids"]], other["ids"])
+
+
+def test_single_expert_layer_is_plain_swiglu():
+    shape = W.scaled(W.CONFIGS["tiny"], E=1, k=1, I=256)
+    ex = W.gen_w4_expert(shape, 0, 0)
+    x = W.gen_x(shape, 3)
+    res = oracle.moe_layer("draft", x, 1, True, lambda e: ex, 1, logits=np.zeros((3, 1), np.float32))
+    Wg = oracle.w4_dequant(ex["qw_gate"], ex["s_gate"])
+    Wu = oracle.w4_dequant(ex["qw_up"], ex["s_up"])
+    Wd = oracle.w4_dequant(ex["qw_down"], ex["s_down"])
+    xd = x.view(np.float16).astype(np.float64)
+    g, u = xd @ Wg, xd @ Wu
+    ref = (g * expit(g) * u) @ Wd
+    assert np.allclose(res["out"], ref, rtol=1e-10, atol=1e-10)
+    assert np.all(res["w"] == 1.0)
+
+
+def test_tiny_draft_and_verify_agree_within_weight_rounding():
+    d = _tiny_layer("draft")
+    v = _tiny_layer("verify")
+    assert np.array_equal(d["ids"], v["ids"])
+    ref = d["out"]
+    err = np.abs(v["out"] - ref)
+    assert err.max() <= 1e-2 * np.abs(ref).max()
+    assert err.sum() / np.abs(ref).sum() <= 1e-3
+
+
+def test_gated_shared_expert_in_layer():
+    shape = W.scaled(W.CONFIGS["qwen15_moe"], H=256, I=128, E=8, k=2, I_s=256)
+    x = W.gen_x(shape, 2)
+    sh = W.gen_shared(shape)
+    lg = np.zeros((2, 8), np.float32)
+    lg[:, 0] = 5.0
+    lg[:, 1] = 4.0
+
+    def expert(e):
+        return W.gen_w4_expert(shape, 0, e)
+    res = oracle.moe_layer("draft", x, 2, False, expert, 8, logits=lg, shared=sh)
+    for t in range(2):
+        gam = expit(float(x[t].view(np.float16).astype(np.float64) @ sh["w_sgate"].view(np.float16).astype(np.float64)))
+        ys = [oracle.swiglu_w4(x[t], expert(e)) for e in (0, 1)]
+        ref = res["w"][t, 0] * ys[0] + res["w"][t, 1] * ys[1] + gam * oracle.swiglu_f16(x[t], sh)
+        assert np.allclose(res["out"][t], ref, rtol=1e-12, atol=1e-12)
