@@ -1,0 +1,452 @@
+"""Benchmark of the per-layer MoE expert hot path (libspx) on one GB300.
+
+One step = one draft layer (T = 1, fused INT4 experts) + one verify layer
+(T = K+1 = 17, expert-reordered FP16 experts), each the full chain route ->
+top-k -> counters -> gather -> experts -> shared expert -> combine, on the
+DeepSeek-V2-Lite-shaped layer (H 2048, I 1408, 64 experts top-6, 2 shared
+experts).  Weights are random (seeded, generated on the device); 8 weight sets
+(11.4 GB) are rotated so that no step finds its weights in the 126 MB L2.
+
+value = algorithmic HBM bytes of the step / device time of the step (GB/s):
+  routed INT4 bytes of the unique experts the draft token selects, routed FP16
+  bytes of the unique experts the 17 verify tokens select, the FP16 shared
+  expert twice, activations, logits and outputs.
+
+``--impl reference`` times the CPU oracle (test infrastructure, single core)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import spx_workloads as W  # noqa: E402
+
+METRIC = "MoE layer µs & achieved HBM GB/s vs GB300 peak, draft T=1 / verify T=K+1"
+NSETS = 8
+NINPUTS = 16
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ bytes --
+def w4_expert_bytes(s):
+    return 3 * s.H * s.I // 2 + 2 * (s.H // 128) * s.I * 2 + (s.I // 128) * s.H * 2
+
+
+def f16_expert_bytes(s, I=None):
+    I = s.I if I is None else I
+    return 3 * s.H * I * 2
+
+
+def layer_bytes(s, mode, T, n_unique):
+    b = n_unique * (w4_expert_bytes(s) if mode == "draft" else f16_expert_bytes(s))
+    if s.I_s:
+        b += f16_expert_bytes(s, s.I_s) + (s.H * 2 if s.shared_gate else 0)
+    if s.logits == "router":
+        b += s.E * s.H * 2
+    b += T * s.H * 2 * 2 + T * s.E * 4  # x in, out, logits
+    return b
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workload ----
+def make_weight_set(s, idx, torch, spx):
+    """Random canonical weights on the device (seeded), repacked for the kernels."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1_000_003 * (s.seed + 1) + idx)
+    E, H, I = s.E, s.H, s.I
+    dev = "cuda"
+
+    def codes(*shape):
+        return torch.randint(-2 ** 31, 2 ** 31, shape, dtype=torch.int32, device=dev, generator=g)
+
+    def scales(*shape):
+        return (torch.rand(shape, device=dev, generator=g) * 0.015 + 0.005).half()
+
+    def normal(*shape):
+        return (torch.randn(shape, device=dev, generator=g) * 0.02).half()
+
+    w4 = spx.spx_w4_repack(codes(E, H // 8, I), scales(E, H // 128, I), codes(E, H // 8, I),
+                           scales(E, H // 128, I), codes(E, I // 8, H), scales(E, I // 128, H), slice_cols=32)
+    f16 = spx.spx_f16_repack(normal(E, I, H), normal(E, I, H), normal(E, H, I))
+    sh = None
+    if s.I_s:
+        sh = spx.pack_shared(normal(s.I_s, H), normal(s.I_s, H), normal(H, s.I_s),
+                             normal(H) if s.shared_gate else None)
+    wr = normal(E, H) if s.logits == "router" else None
+    torch.cuda.synchronize()
+    return dict(w4=w4, f16=f16, shared=sh, w_router=wr)
+
+
+def make_inputs(s, i):
+    Td, Tv = s.T_draft, s.T_verify
+    d = dict(x_d=W.gen_x(s, Td, step=i, which=0), x_v=W.gen_x(s, Tv, step=i, which=1))
+    if s.logits != "router":
+        d["lg_d"] = W.gen_logits(s, Td, step=i, which=0)
+        d["lg_v"] = W.gen_logits(s, Tv, step=i, which=1)
+    return d
+
+
+def run_mine(args):
+    import torch
+    from quantized_expert_gb300 import build as spx_build
+    from quantized_expert_gb300 import spx
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        spx_build.build()
+    if world > 1:
+        dist.barrier()
+    spx.load()
+    s = W.CONFIGS[args.config]
+    Td, Tv = s.T_draft, s.T_verify
+
+    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
+    inputs = [make_inputs(s, i) for i in range(NINPUTS)]
+
+    def f16dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
+
+    dev_in = []
+    for d in inputs:
+        e = dict(x_d=f16dev(d["x_d"]), x_v=f16dev(d["x_v"]))
+        e["lg_d"] = torch.from_numpy(d["lg_d"]).cuda() if "lg_d" in d else torch.empty(Td, s.E, device="cuda")
+        e["lg_v"] = torch.from_numpy(d["lg_v"]).cuda() if "lg_v" in d else torch.empty(Tv, s.E, device="cuda")
+        dev_in.append(e)
+    L = s.layers
+    elb = torch.zeros(max(L, NSETS), s.E, dtype=torch.int32, device="cuda")
+    ws_d = spx.new_workspace(Td, s.H)
+    ws_v = spx.new_workspace(Tv, s.H)
+    r_d = spx.Routing.empty(Td, s.E, s.k)
+    r_v = spx.Routing.empty(Tv, s.E, s.k)
+    out_d = torch.empty(Td, s.H, dtype=torch.float16, device="cuda")
+    out_v = torch.empty(Tv, s.H, dtype=torch.float16, device="cuda")
+
+    def step_args(i):
+        st_d = sets[i % NSETS]
+        st_v = sets[(i + NSETS // 2) % NSETS]
+        inp = dev_in[i % NINPUTS]
+        ad, kd = spx.layer_args(0, inp["x_d"], s.E, s.k, s.renorm, inp["lg_d"], r_d, out_d, ws_d, w4=st_d["w4"],
+                                shared=st_d["shared"], w_router=st_d["w_router"], elb=elb, layer=i % NSETS)
+        av, kv = spx.layer_args(1, inp["x_v"], s.E, s.k, s.renorm, inp["lg_v"], r_v, out_v, ws_v, f16=st_v["f16"],
+                                shared=st_v["shared"], w_router=st_v["w_router"])
+        return ad, av, (kd, kv)
+
+    timed_keep = []
+
+    def step_args_timed(i, evd, evv):
+        st_d = sets[i % NSETS]
+        st_v = sets[(i + NSETS // 2) % NSETS]
+        inp = dev_in[i % NINPUTS]
+        ad, kd = spx.layer_args(0, inp["x_d"], s.E, s.k, s.renorm, inp["lg_d"], r_d, out_d, ws_d, w4=st_d["w4"],
+                                shared=st_d["shared"], w_router=st_d["w_router"], elb=elb, layer=i % NSETS,
+                                events=evd)
+        av, kv = spx.layer_args(1, inp["x_v"], s.E, s.k, s.renorm, inp["lg_v"], r_v, out_v, ws_v, f16=st_v["f16"],
+                                shared=st_v["shared"], w_router=st_v["w_router"], events=evv)
+        timed_keep.append((ad, av, kd, kv))
+        return ad, av
+
+    # unique experts per input (from the library's own routing) -> algorithmic bytes
+    nbytes = []
+    nd_list, nv_list = [], []
+    for i in range(NINPUTS):
+        ad, av, keep = step_args(i)
+        spx.spx_moe_layer(ad)
+        spx.spx_moe_layer(av)
+        torch.cuda.synchronize()
+        nd, nv = int(r_d.n_active.item()), int(r_v.n_active.item())
+        nd_list.append(nd)
+        nv_list.append(nv)
+        nbytes.append((layer_bytes(s, "draft", Td, nd), layer_bytes(s, "verify", Tv, nv)))
+
+    stream = torch.cuda.Stream()
+    nrot = NSETS * NINPUTS // int(np.gcd(NSETS, NINPUTS))
+    keeps = [step_args(i) for i in range(nrot)]
+
+    def sync_all():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+            torch.cuda.synchronize()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # pass 1: the timed region proper (eager launches; the host enqueues well
+    # ahead of the device, so launch overhead is off the clock)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            ad, av, _ = keeps[i % nrot]
+            spx.spx_moe_layer(ad, stream)
+            spx.spx_moe_layer(av, stream)
+    sync_all()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            for i in range(args.steps):
+                ad, av, _ = keeps[i % nrot]
+                spx.spx_moe_layer(ad, stream)
+                spx.spx_moe_layer(av, stream)
+            e1.record(stream)
+        sync_all()
+        ms_total = e0.elapsed_time(e1)
+        time.sleep(0.2)
+    clocks = clk.summary()
+
+    # pass 2: same steps with events between the layers and around each
+    # expert launch (per-layer and per-kernel durations for the roofline)
+    lay_ev, ker_ev = [], []
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            a, b, c = ev(), ev(), ev()
+            kd, kv = (ev(), ev()), (ev(), ev())
+            ad, ae = step_args_timed(i, kd, kv)
+            a.record(stream)
+            spx.spx_moe_layer(ad, stream)
+            b.record(stream)
+            spx.spx_moe_layer(ae, stream)
+            c.record(stream)
+            lay_ev.append((a, b, c))
+            ker_ev.append((kd, kv))
+    sync_all()
+    d_ms = [a.elapsed_time(b) for a, b, c in lay_ev]
+    v_ms = [b.elapsed_time(c) for a, b, c in lay_ev]
+    kd_ms = [k[0][0].elapsed_time(k[0][1]) for k in ker_ev]
+    kv_ms = [k[1][0].elapsed_time(k[1][1]) for k in ker_ev]
+
+    step_bytes = [nbytes[i % NINPUTS] for i in range(args.steps)]
+    tot_bytes = sum(d + v for d, v in step_bytes)
+    ms_step = ms_total / args.steps
+    t_max = ms_total
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    value = world * tot_bytes / (t_max * 1e-3) / 1e9
+
+    d_bytes = statistics.mean(b[0] for b in step_bytes)
+    v_bytes = statistics.mean(b[1] for b in step_bytes)
+    d_us = statistics.median(d_ms) * 1e3
+    v_us = statistics.median(v_ms) * 1e3
+    kd_us = statistics.mean(kd_ms) * 1e3
+    kv_us = statistics.mean(kv_ms) * 1e3
+    # expert-launch bytes: the layer's bytes minus what the routing launch reads
+    kv_bytes = v_bytes - Tv * s.E * 4 - (s.E * s.H * 2 if s.logits == "router" else 0)
+    kd_bytes = d_bytes - Td * s.E * 4 - (s.E * s.H * 2 if s.logits == "router" else 0)
+    peak, peak_src = measured_peaks()
+
+    # e2e: host buffers through the public API, copies inside the timed region
+    host_in = []
+    for d in inputs:
+        h = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.float16) if v.dtype == np.uint16 else v)).pin_memory()
+             for k, v in d.items()}
+        host_in.append(h)
+    host_out_d = torch.empty(Td, s.H, dtype=torch.float16).pin_memory()
+    host_out_v = torch.empty(Tv, s.H, dtype=torch.float16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values())
+    d2h = host_out_d.numel() * 2 + host_out_v.numel() * 2
+    sync_all()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                stream.synchronize()
+                t0 = time.perf_counter()
+            h = host_in[i % NINPUTS]
+            inp = dev_in[i % NINPUTS]
+            for k, v in h.items():
+                inp[k].copy_(v, non_blocking=True)
+            ad, av, _ = keeps[i % nrot]
+            spx.spx_moe_layer(ad, stream)
+            spx.spx_moe_layer(av, stream)
+            host_out_d.copy_(out_d, non_blocking=True)
+            host_out_v.copy_(out_v, non_blocking=True)
+        stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+    e2e_gbs = world * tot_bytes / e2e_s / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 (int4 draft weights, fp32 accumulate)",
+        "data": "synthetic (seeded random weights and activations; drawn Zipf(1.1) router logits)",
+        "config": {"workload": f"{s.name} layer: draft T={Td} + verify T={Tv}", "H": s.H, "I": s.I, "E": s.E,
+                   "k": s.k, "I_shared": s.I_s, "draft_T": Td, "verify_T": Tv,
+                   "l2": f"{NSETS} rotated weight sets ({NSETS * 1.43:.1f} GB) > L2; no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "unique_experts_draft": statistics.mean(nd_list), "unique_experts_verify": statistics.mean(nv_list)},
+        "layers": {"draft_us": round(d_us, 2), "draft_gbs": round(d_bytes / (d_us * 1e-6) / 1e9, 1),
+                   "draft_frac": round(d_bytes / (d_us * 1e-6) / 1e9 / peak, 3),
+                   "draft_tokens_per_s": round(Td / (d_us * 1e-6), 1),
+                   "verify_us": round(v_us, 2), "verify_gbs": round(v_bytes / (v_us * 1e-6) / 1e9, 1),
+                   "verify_frac": round(v_bytes / (v_us * 1e-6) / 1e9 / peak, 3),
+                   "verify_tokens_per_s": round(Tv / (v_us * 1e-6), 1),
+                   "draft_bytes": int(d_bytes), "verify_bytes": int(v_bytes)},
+        "roofline": {"bound": "hbm", "kernel": "engine_kernel<1,3> (verify expert launch)",
+                     "achieved": round(kv_bytes / (kv_us * 1e-6) / 1e9, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(kv_bytes / (kv_us * 1e-6) / 1e9 / peak, 3), "traffic": None,
+                     "launch_us": round(kv_us, 2), "bytes_per_launch": int(kv_bytes)},
+        "draft_roofline": {"bound": "hbm", "kernel": "engine_kernel<2,1> (draft expert launch)",
+                           "achieved": round(kd_bytes / (kd_us * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                           "frac": round(kd_bytes / (kd_us * 1e-6) / 1e9 / peak, 3), "launch_us": round(kd_us, 2),
+                           "bytes_per_launch": int(kd_bytes)},
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 4 * args.steps,
+    }
+    if rank == 0 and args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- oracle --
+def cpu_baseline(s, reps=1):
+    """The CPU oracle (single thread) on one draft + one verify layer."""
+    import oracle
+    oracle.build()
+    d = make_inputs(s, 0)
+    ids_d, _ = oracle.route_topk(d["lg_d"].astype(np.float64), s.k, s.renorm)
+    ids_v, _ = oracle.route_topk(d["lg_v"].astype(np.float64), s.k, s.renorm)
+    need_d = sorted(set(ids_d.reshape(-1).tolist()))
+    need_v = sorted(set(ids_v.reshape(-1).tolist()))
+    w4 = {e: W.gen_w4_expert(s, 0, e) for e in need_d}
+    f16 = {e: W.gen_f16_expert(s, 0, e) for e in need_v}
+    sh = W.gen_shared(s, 0)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.moe_layer("draft", d["x_d"], s.k, s.renorm, w4.__getitem__, s.E, logits=d["lg_d"], shared=sh)
+        oracle.moe_layer("verify", d["x_v"], s.k, s.renorm, f16.__getitem__, s.E, logits=d["lg_v"], shared=sh)
+    dt = (time.perf_counter() - t0) / reps
+    b = layer_bytes(s, "draft", s.T_draft, len(need_d)) + layer_bytes(s, "verify", s.T_verify, len(need_v))
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 draft (T={s.T_draft}) + 1 verify (T={s.T_verify}) layer of {s.name}, input set 0, "
+                      f"{reps} rep(s), {dt:.2f} s per step"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    s = W.CONFIGS[args.config]
+    times = []
+    cb = None
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(s)
+        if i >= args.warmup:
+            times.append(cb)
+    vals = [c["value"] for c in times]
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{s.name} layer: draft T={s.T_draft} + verify T={s.T_verify}"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--config", default="deepseek_v2_lite", choices=sorted(W.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if args.steps > 3:
+            args.steps = 3
+        if args.warmup > 1:
+            args.warmup = 1
+        run_reference(args)
+    else:
+        run_mine(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,255 @@
+/*
+ * spx.h -- C ABI of libspx, the GB300 (sm_103a) per-layer MoE expert path of
+ * Specter's Streamlined Execution Engine, for one decoding request.
+ *
+ * Sources, cited by page title and section:
+ *  [P1] ai.info summary, "Specter: Fast MoE Inference via Quantization-Enabled
+ *       Multi-Step Speculative Offloading": Key Contributions 2 (FP16 gates and
+ *       shared experts, INT4 routed experts), 3 (Expert Lookahead Buffer: GPU-
+ *       resident, layer-indexed expert-activation counters), 4 (fused multi-
+ *       expert INT4 draft kernel that gathers tokens by expert in one launch;
+ *       expert-wise verification reordering); "Methodology in Plain English".
+ *  [P2] richland.au, "Specter previews expert routing with an INT4 copy of the
+ *       model itself", section "What shipped": GPTQ INT4 with group size 128,
+ *       routers and shared experts reuse the target's FP16 tensors, W4A16
+ *       kernels that dequantise INT4 tiles and compute in FP16.
+ *
+ * Conventions (all entry points):
+ *  - fp16 values are passed as binary16 bit patterns (uint16_t); fp32 as float.
+ *  - Every pointer is caller-owned device memory unless stated otherwise; the
+ *    library allocates nothing and never synchronises.  Every call is
+ *    asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - Arguments are validated before any launch.  Return value: SPX_OK, or a
+ *    negative spx_status; on error nothing was enqueued.  Launch failures are
+ *    reported as SPX_ERR_CUDA (from cudaGetLastError).
+ *  - Supported shapes: 1 <= T <= 64 tokens, 1 <= k <= E <= 256, T*k <= 512,
+ *    H and I multiples of 128, H <= 8192.  Anything else: SPX_ERR_UNSUPPORTED.
+ *  - Device pointers passed to the expert calls must be 16-byte aligned.
+ *  - The library holds no state between calls: the counter table and the
+ *    workspace are the caller's buffers.  One workspace must not be used by
+ *    two calls that can run concurrently (e.g. on two streams).
+ */
+#ifndef SPX_H
+#define SPX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SPX_API __attribute__((visibility("default")))
+#else
+#define SPX_API
+#endif
+
+typedef struct CUstream_st *spx_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    SPX_OK = 0,
+    SPX_ERR_INVALID_ARG = -1, /* null pointer, negative size, k > E, ... */
+    SPX_ERR_UNSUPPORTED = -2, /* shape outside the supported range */
+    SPX_ERR_WORKSPACE = -3,   /* workspace missing, too small or misaligned */
+    SPX_ERR_CUDA = -4,        /* a CUDA call or kernel launch failed */
+    SPX_ERR_TIMEOUT = -5      /* a bounded device-side wait gave up (status word) */
+} spx_status;
+
+/* Static text for a status code (never NULL). */
+SPX_API const char *spx_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+SPX_API int spx_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Router: logits, softmax, top-k   [P1 Key Contributions 2; P2 What shipped] */
+/* ------------------------------------------------------------------------ */
+/* logits: [T][E] fp32.  If w_router != NULL (fp16 [E][H]) the call computes
+ *   logits[t][e] = sum_h x[t][h] * w_router[e][h] (fp32 accumulate) and writes
+ *   them; otherwise logits is read as given and x may be NULL.
+ * Selection: the k largest fp32 logits per token, ties to the lower expert
+ *   index, in descending order -> topk_ids [T][k] (int32).
+ * Weights: p = softmax over all E experts; topk_w[t][j] = p[id] (renorm == 0)
+ *   or p[id] / sum of the k selected p (renorm != 0) -> [T][k] fp32.
+ * ws: workspace of spx_workspace_size() bytes (holds the completion counter
+ *   of the multi-block router product). */
+SPX_API int spx_route_topk(const uint16_t *x, const uint16_t *w_router, float *logits,
+                   int T, int H, int E, int k, int renorm,
+                   int32_t *topk_ids, float *topk_w,
+                   void *ws, size_t ws_bytes, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert Lookahead Buffer counters  [P1 Key Contributions 3; Methodology]   */
+/* ------------------------------------------------------------------------ */
+/* elb: uint32 [L][E], layer-indexed expert-activation counters.
+ * accumulate: elb[layer][topk_ids[t][j]] += 1 for every t < T, j < k
+ *   (so each call adds exactly T*k to the layer's row). */
+SPX_API int spx_elb_accumulate(uint32_t *elb, int L, int E, int layer,
+                       const int32_t *topk_ids, int T, int k, spx_stream_t stream);
+/* read: asynchronous, non-destructive snapshot of all L*E counters into dst,
+ *   which may be device memory or page-locked host memory. */
+SPX_API int spx_elb_read(const uint32_t *elb, int L, int E, uint32_t *dst, spx_stream_t stream);
+/* reset: all L*E counters to zero. */
+SPX_API int spx_elb_reset(uint32_t *elb, int L, int E, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gather tokens by expert (counting sort)  [P1 Key Contributions 4]         */
+/* ------------------------------------------------------------------------ */
+/* Flat slots s = t*k + j.  counts [E]: assignments per expert; offsets [E+1]:
+ * exclusive prefix sum (offsets[E] = T*k); sorted_slots [T*k]: slots in
+ * ascending expert, then ascending slot order ("sorted position" p indexes
+ * this array); active [E]: experts with count > 0 in ascending order, the
+ * rest -1; n_active [1]: how many.  Bit-exact and deterministic. */
+SPX_API int spx_gather_by_expert(const int32_t *topk_ids, int T, int k, int E,
+                         int32_t *counts, int32_t *offsets, int32_t *sorted_slots,
+                         int32_t *active, int32_t *n_active, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert weight formats                                                      */
+/* ------------------------------------------------------------------------ */
+/* Canonical inputs (what a checkpoint holds):
+ *  INT4 draft experts [P2 What shipped: GPTQ INT4, group 128], zero point 8,
+ *   no act-order: qweight int32 [E][K/8][N], code of row kk at bits
+ *   4*(kk%8)..+3 of word (kk/8, n); scales fp16 [E][K/128][N];
+ *   W[kk][n] = (code - 8) * scale[kk/128][n].  gate/up: K = H, N = I;
+ *   down: K = I, N = H.
+ *  FP16 experts (verify, shared): PyTorch [out][in]: gate/up [E][I][H],
+ *   down [E][H][I].
+ *
+ * Packed (what the expert kernels stream).  The repack calls below rewrite a
+ * canonical tensor set once, at load time, into "units": one unit = one
+ * expert's I-slice of S intermediate columns (gate rows, up rows and the
+ * matching down columns), stored contiguously so that one unit is a few large
+ * bulk copies, and laid out in the register-fragment order of the
+ * m16n8k16 tensor-core instruction, so each lane reads its operands with
+ * sequential 16-byte shared-memory loads.  The INT4 codes are re-packed two
+ * fp16 lanes at a time for the magic-exponent dequantisation.  The byte order
+ * inside a unit is private to the library; only the sizes below are public.
+ *   INT4: S = 16 or 32 (slice_cols); unit bytes = 49*H*S/32; then the down
+ *         scales, copied unchanged ([E][I/128][H] fp16).
+ *   FP16: S = 16; unit bytes = 6*H*S.
+ */
+typedef struct {
+    const void *packed; /* spx_w4_packed_bytes() bytes, from spx_w4_repack() */
+    int E, H, I;        /* experts, hidden size, expert intermediate size */
+    int slice_cols;     /* S: 16 or 32 */
+} spx_w4_experts;
+
+typedef struct {
+    const void *packed; /* spx_f16_packed_bytes() bytes, from spx_f16_repack() */
+    int E, H, I;
+} spx_f16_experts;
+
+/* Shared expert(s): one FP16 MLP of intermediate size I_s (several shared
+ * experts concatenated along I are one MLP, as the intermediate sum splits).
+ * If w_sgate != NULL (fp16 [H]) its output is scaled per token by
+ * gamma_t = 1 / (1 + exp(-x_t . w_sgate)).  [P1 Key Contributions 2] */
+typedef struct {
+    const void *packed;      /* spx_f16_packed_bytes(1, H, I_s) bytes */
+    const uint16_t *w_sgate; /* nullable */
+    int H, I_s;
+} spx_shared;
+
+SPX_API size_t spx_w4_packed_bytes(int E, int H, int I, int slice_cols);
+SPX_API size_t spx_f16_packed_bytes(int E, int H, int I);
+
+/* Repack canonical GPTQ tensors (device memory, layouts above) into `packed`
+ * (device, spx_w4_packed_bytes() bytes, 16-byte aligned).  Deterministic. */
+SPX_API int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate,
+                  const int32_t *qw_up, const uint16_t *s_up,
+                  const int32_t *qw_down, const uint16_t *s_down,
+                  int E, int H, int I, int slice_cols, void *packed, spx_stream_t stream);
+
+/* Repack canonical FP16 [out][in] tensors into `packed` (spx_f16_packed_bytes). */
+SPX_API int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
+                   int E, int H, int I, void *packed, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Workspace                                                                  */
+/* ------------------------------------------------------------------------ */
+/* Bytes of workspace for calls with up to T tokens of hidden size H. */
+SPX_API size_t spx_workspace_size(int T, int H);
+/* Zero a workspace; required once before first use (kernels leave it zeroed
+ * again on exit) and after any call whose status word reported an error. */
+SPX_API int spx_workspace_init(void *ws, size_t ws_bytes, spx_stream_t stream);
+/* Asynchronously copy the workspace status word (SPX_OK or SPX_ERR_TIMEOUT)
+ * into *host_status (page-locked host memory or device memory). */
+SPX_API int spx_workspace_status(const void *ws, int32_t *host_status, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert MLPs   [P1 Key Contributions 4; P2 What shipped]                    */
+/* ------------------------------------------------------------------------ */
+/* For every assignment (t, e = topk_ids[t][j]):
+ *   y = W_down_e( silu(W_gate_e x_t) * (W_up_e x_t) ),  silu(z) = z/(1+e^-z),
+ * accumulated in fp32; the intermediate is rounded to fp16 before the down
+ * projection (W4A16: dequantised INT4 weights times fp16 activations).
+ * offsets/sorted_slots/active/n_active come from spx_gather_by_expert.
+ * Output: y_sorted fp32 [T*k][H], row p = the assignment sorted_slots[p]
+ * (zeroed by the call, then accumulated).
+ *
+ * draft: one fused launch over all active experts' INT4 units.
+ * verify: the same launch shape over FP16 experts; each active expert's
+ *   weights are read once for all of its n_e tokens (expert-wise reordering:
+ *   tokens of one expert form the columns of one tensor-core product). */
+SPX_API int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_experts *w, int k,
+                        const int32_t *offsets, const int32_t *sorted_slots,
+                        const int32_t *active, const int32_t *n_active,
+                        float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream);
+
+SPX_API int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_experts *w, int k,
+                        const int32_t *offsets, const int32_t *sorted_slots,
+                        const int32_t *active, const int32_t *n_active,
+                        float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream);
+
+/* Weighted scatter-combine plus shared expert:
+ *   out[t] = fp16( sum_j topk_w[t][j] * y_sorted[pos(t,j)] + gamma_t * sh_t )
+ * where pos(t,j) is the sorted position of slot t*k+j and sh_t the shared
+ * expert MLP of x_t (omitted when shared == NULL).  out: fp16 [T][H]. */
+SPX_API int spx_combine(const float *y_sorted, const int32_t *sorted_slots, const float *topk_w,
+                const uint16_t *x, const spx_shared *shared, int T, int H, int k,
+                uint16_t *out, void *ws, size_t ws_bytes, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Composite layer: route, top-k, counters, gather, experts, shared, combine  */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int mode;                  /* 0 = draft (INT4 routed experts), 1 = verify (FP16) */
+    int T, H, E, k, renorm;
+    const uint16_t *x;         /* [T][H] fp16 */
+    const uint16_t *w_router;  /* [E][H] fp16, or NULL: logits are given */
+    float *logits;             /* [T][E]: output if w_router, else input */
+    const spx_w4_experts *w4;  /* mode 0 */
+    const spx_f16_experts *f16;/* mode 1 */
+    const spx_shared *shared;  /* NULL = no shared expert */
+    uint32_t *elb;             /* [L][E] counters to update, or NULL */
+    int L, layer;
+    /* routing outputs (caller-owned, same meaning as the unit calls) */
+    int32_t *topk_ids;         /* [T][k] */
+    float *topk_w;             /* [T][k] */
+    int32_t *counts;           /* [E] */
+    int32_t *offsets;          /* [E+1] */
+    int32_t *sorted_slots;     /* [T*k] */
+    int32_t *active;           /* [E] */
+    int32_t *n_active;         /* [1] */
+    uint16_t *out;             /* [T][H] fp16 */
+    void *ws;
+    size_t ws_bytes;
+    /* Instrumentation, both nullable: cudaEvent_t handles recorded on the
+     * stream immediately before and after the expert launch (recording between
+     * the two launches removes their programmatic overlap). */
+    void *ev_experts_begin;
+    void *ev_experts_end;
+} spx_layer_args;
+
+/* Two launches: a routing launch (router product when w_router is given,
+ * softmax, top-k, counters, counting sort) and one persistent expert launch
+ * that streams the shared expert first (it does not depend on routing; the
+ * launch is made programmatically dependent so that this overlaps routing),
+ * then every active expert's units, and writes out[] from its last block. */
+SPX_API int spx_moe_layer(const spx_layer_args *args, spx_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPX_H */

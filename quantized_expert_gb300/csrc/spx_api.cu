@@ -1,0 +1,303 @@
+// spx_api.cu -- C ABI entry points of libspx for the expert path: argument
+// validation, workspace handling and launch sequencing.  Every numeric step
+// runs in the kernels of spx_route.cu, spx_engine.cu and the combine kernel
+// below; this file only checks arguments and enqueues launches.
+#include "spx_internal.cuh"
+
+#include <math.h>
+
+namespace spx {
+
+int device_sm_count() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int record_launch(cudaError_t e) { return e == cudaSuccess ? SPX_OK : SPX_ERR_CUDA; }
+
+// out[t][n] = fp16( sum_j w[t][j] * y_sorted[pos(t,j)][n] + acc[t][n] ); acc -> 0
+__global__ void __launch_bounds__(256) combine_kernel(const float *y_sorted, const int32_t *sorted_slots,
+                                                      const float *topk_w, float *acc, int T, int H, int k,
+                                                      __half *out) {
+    __shared__ int inv[kMaxSlots];
+    const int n = T * k;
+    for (int p = threadIdx.x; p < n; p += blockDim.x) {
+        const int s = sorted_slots[p];
+        if (s >= 0 && s < n) inv[s] = p;
+    }
+    __syncthreads();
+    const int t = blockIdx.y;
+    const int n4 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T || n4 * 4 >= H) return;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (acc) {
+        a = __ldcg(reinterpret_cast<const float4 *>(acc + (size_t)t * H) + n4);
+        __stcg(reinterpret_cast<float4 *>(acc + (size_t)t * H) + n4, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const float w = topk_w[t * k + j];
+        const float4 y = __ldg(reinterpret_cast<const float4 *>(y_sorted + (size_t)inv[t * k + j] * H) + n4);
+        r.x = fmaf(w, y.x, r.x);
+        r.y = fmaf(w, y.y, r.y);
+        r.z = fmaf(w, y.z, r.z);
+        r.w = fmaf(w, y.w, r.w);
+    }
+    __half2 lo = __floats2half2_rn(r.x + a.x, r.y + a.y), hi = __floats2half2_rn(r.z + a.z, r.w + a.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t *>(&lo);
+    o.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(out + (size_t)t * H)[n4] = o;
+}
+
+}  // namespace spx
+
+using namespace spx;
+
+static const uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s per bounded wait
+
+static bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+extern "C" const char *spx_status_string(int st) {
+    switch (st) {
+        case SPX_OK: return "ok";
+        case SPX_ERR_INVALID_ARG: return "invalid argument";
+        case SPX_ERR_UNSUPPORTED: return "unsupported shape";
+        case SPX_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case SPX_ERR_CUDA: return "CUDA error";
+        case SPX_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int spx_version(void) { return 100; }
+
+extern "C" size_t spx_workspace_size(int T, int H) {
+    if (T < 1 || H < 1 || T > kMaxT || H > kMaxH) return 0;
+    return ws_gamma_offset(T, H) + 256;
+}
+
+extern "C" int spx_workspace_init(void *ws, size_t ws_bytes, spx_stream_t stream) {
+    if (!ws || ws_bytes < sizeof(WsHeader)) return SPX_ERR_WORKSPACE;
+    return record_launch(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int spx_workspace_status(const void *ws, int32_t *host_status, spx_stream_t stream) {
+    if (!ws || !host_status) return SPX_ERR_INVALID_ARG;
+    const WsHeader *h = static_cast<const WsHeader *>(ws);
+    return record_launch(cudaMemcpyAsync(host_status, &h->status, sizeof(int32_t), cudaMemcpyDefault,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static int check_expert_common(const uint16_t *x, int T, int H, int E, int I, int k, const int32_t *offsets,
+                               const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
+                               void *ws, size_t ws_bytes) {
+    if (!x || !offsets || !sorted_slots || !active || !n_active) return SPX_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || E < 1 || k > E || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
+    if (T > kMaxT || E > kMaxE || T * k > kMaxSlots || H % 128 || I % 128 || H > kMaxH) return SPX_ERR_UNSUPPORTED;
+    if (!engine_fits(T, H)) return SPX_ERR_UNSUPPORTED;
+    if (!al16(x)) return SPX_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < spx_workspace_size(T, H) || !al16(ws)) return SPX_ERR_WORKSPACE;
+    return SPX_OK;
+}
+
+static EngineParams base_params(const uint16_t *x, int T, int H, void *ws) {
+    EngineParams p{};
+    p.x = reinterpret_cast<const __half *>(x);
+    p.T = T;
+    p.H = H;
+    p.hdr = static_cast<WsHeader *>(ws);
+    p.npad = 8 * ((T + 7) / 8);
+    p.wait_budget_ns = kWaitBudgetNs;
+    return p;
+}
+
+extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_experts *w, int k, const int32_t *offsets,
+                                   const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
+                                   float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
+    if (!w || !w->packed || !y_sorted) return SPX_ERR_INVALID_ARG;
+    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes);
+    if (st) return st;
+    if ((w->slice_cols != 16 && w->slice_cols != 32) || !al16(w->packed) || !al16(y_sorted)) return SPX_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    EngineParams p = base_params(x, T, w->H, ws);
+    p.routed = static_cast<const uint8_t *>(w->packed);
+    p.w4_sdown = reinterpret_cast<const __half *>(p.routed + w4_units_bytes(w->E, w->H, w->I, w->slice_cols));
+    p.routed_fmt = 0;
+    p.S = w->slice_cols;
+    p.E = w->E;
+    p.I = w->I;
+    p.k = k;
+    p.routed_enabled = 1;
+    p.offsets = offsets;
+    p.sorted_slots = sorted_slots;
+    p.active = active;
+    p.n_active = n_active;
+    p.mode = 0;  // sorted rows
+    p.yout = y_sorted;
+    if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
+    return launch_engine(p, s, false);
+}
+
+extern "C" int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_experts *w, int k, const int32_t *offsets,
+                                   const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
+                                   float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
+    if (!w || !w->packed || !y_sorted) return SPX_ERR_INVALID_ARG;
+    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes);
+    if (st) return st;
+    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    EngineParams p = base_params(x, T, w->H, ws);
+    p.routed = static_cast<const uint8_t *>(w->packed);
+    p.routed_fmt = 1;
+    p.S = kF16S;
+    p.E = w->E;
+    p.I = w->I;
+    p.k = k;
+    p.routed_enabled = 1;
+    p.offsets = offsets;
+    p.sorted_slots = sorted_slots;
+    p.active = active;
+    p.n_active = n_active;
+    p.mode = 0;
+    p.yout = y_sorted;
+    if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
+    return launch_engine(p, s, false);
+}
+
+static int check_shared(const spx_shared *sh, int H) {
+    if (!sh) return SPX_OK;
+    if (!sh->packed || sh->H != H || sh->I_s < kF16S || sh->I_s % kF16S) return SPX_ERR_INVALID_ARG;
+    if (!al16(sh->packed)) return SPX_ERR_INVALID_ARG;
+    if (sh->w_sgate && (reinterpret_cast<uintptr_t>(sh->w_sgate) & 3)) return SPX_ERR_INVALID_ARG;
+    return SPX_OK;
+}
+
+extern "C" int spx_combine(const float *y_sorted, const int32_t *sorted_slots, const float *topk_w, const uint16_t *x,
+                           const spx_shared *shared, int T, int H, int k, uint16_t *out, void *ws, size_t ws_bytes,
+                           spx_stream_t stream) {
+    if (!y_sorted || !sorted_slots || !topk_w || !out) return SPX_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || H < 1) return SPX_ERR_INVALID_ARG;
+    if (T > kMaxT || T * k > kMaxSlots || H % 128 || H > kMaxH) return SPX_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < spx_workspace_size(T, H) || !al16(ws)) return SPX_ERR_WORKSPACE;
+    if (!al16(y_sorted) || (reinterpret_cast<uintptr_t>(out) & 7)) return SPX_ERR_INVALID_ARG;
+    int st = check_shared(shared, H);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsAccOffset);
+    if (shared) {
+        if (!x || !al16(x)) return SPX_ERR_INVALID_ARG;
+        if (!engine_fits(T, H)) return SPX_ERR_UNSUPPORTED;
+        EngineParams p = base_params(x, T, H, ws);
+        p.routed_enabled = 0;
+        p.routed_fmt = 1;
+        p.S = kF16S;
+        p.I = kF16S;
+        p.E = 1;
+        p.k = k;
+        p.shared = static_cast<const uint8_t *>(shared->packed);
+        p.w_sgate = reinterpret_cast<const __half *>(shared->w_sgate);
+        p.I_s = shared->I_s;
+        p.mode = 1;  // accumulate gamma * sh into acc
+        p.yout = acc;
+        st = launch_engine(p, s, false);
+        if (st) return st;
+    }
+    dim3 grid((H / 4 + 255) / 256, T);
+    combine_kernel<<<grid, 256, 0, s>>>(y_sorted, sorted_slots, topk_w, shared ? acc : nullptr, T, H, k,
+                                        reinterpret_cast<__half *>(out));
+    return record_launch(cudaGetLastError());
+}
+
+extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
+    if (!a) return SPX_ERR_INVALID_ARG;
+    const int T = a->T, H = a->H, E = a->E, k = a->k;
+    int st = route_validate(a->x, a->w_router, a->logits, T, H, E, k, a->topk_ids, a->topk_w);
+    if (st) return st;
+    if (!a->x || !a->counts || !a->offsets || !a->sorted_slots || !a->active || !a->n_active || !a->out)
+        return SPX_ERR_INVALID_ARG;
+    if (a->mode != 0 && a->mode != 1) return SPX_ERR_INVALID_ARG;
+    if (a->elb && (a->layer < 0 || a->layer >= a->L)) return SPX_ERR_INVALID_ARG;
+    int I = 0;
+    const uint8_t *routed = nullptr;
+    int S = kF16S;
+    if (a->mode == 0) {
+        if (!a->w4 || !a->w4->packed || a->w4->E != E || a->w4->H != H) return SPX_ERR_INVALID_ARG;
+        if ((a->w4->slice_cols != 16 && a->w4->slice_cols != 32) || !al16(a->w4->packed)) return SPX_ERR_UNSUPPORTED;
+        I = a->w4->I;
+        S = a->w4->slice_cols;
+        routed = static_cast<const uint8_t *>(a->w4->packed);
+    } else {
+        if (!a->f16 || !a->f16->packed || a->f16->E != E || a->f16->H != H) return SPX_ERR_INVALID_ARG;
+        if (!al16(a->f16->packed)) return SPX_ERR_UNSUPPORTED;
+        I = a->f16->I;
+        routed = static_cast<const uint8_t *>(a->f16->packed);
+    }
+    st = check_expert_common(a->x, T, H, E, I, k, a->offsets, a->sorted_slots, a->active, a->n_active, a->ws,
+                             a->ws_bytes);
+    if (st) return st;
+    st = check_shared(a->shared, H);
+    if (st) return st;
+    if (reinterpret_cast<uintptr_t>(a->out) & 7) return SPX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    RouteParams rp{};
+    rp.x = reinterpret_cast<const __half *>(a->x);
+    rp.w_router = reinterpret_cast<const __half *>(a->w_router);
+    rp.logits = a->logits;
+    rp.T = T;
+    rp.H = H;
+    rp.E = E;
+    rp.k = k;
+    rp.renorm = a->renorm;
+    rp.topk_ids = a->topk_ids;
+    rp.topk_w = a->topk_w;
+    rp.elb = a->elb;
+    rp.layer = a->layer;
+    rp.counts = a->counts;
+    rp.offsets = a->offsets;
+    rp.sorted_slots = a->sorted_slots;
+    rp.active = a->active;
+    rp.n_active = a->n_active;
+    rp.hdr = static_cast<WsHeader *>(a->ws);
+    st = launch_route(rp, s);
+    if (st) return st;
+
+    EngineParams p = base_params(a->x, T, H, a->ws);
+    p.routed = routed;
+    p.routed_fmt = a->mode == 0 ? 0 : 1;
+    p.S = S;
+    if (a->mode == 0) p.w4_sdown = reinterpret_cast<const __half *>(routed + w4_units_bytes(E, H, I, S));
+    p.E = E;
+    p.I = I;
+    p.k = k;
+    p.routed_enabled = 1;
+    p.offsets = a->offsets;
+    p.sorted_slots = a->sorted_slots;
+    p.active = a->active;
+    p.n_active = a->n_active;
+    p.topk_w = a->topk_w;
+    if (a->shared) {
+        p.shared = static_cast<const uint8_t *>(a->shared->packed);
+        p.w_sgate = reinterpret_cast<const __half *>(a->shared->w_sgate);
+        p.I_s = a->shared->I_s;
+    }
+    p.mode = 2;  // layer: weighted accumulate, last block writes out
+    p.yout = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
+    p.out = reinterpret_cast<__half *>(a->out);
+    const bool timed = a->ev_experts_begin || a->ev_experts_end;
+    if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
+        return SPX_ERR_CUDA;
+    st = launch_engine(p, s, !timed);
+    if (st) return st;
+    if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
+        return SPX_ERR_CUDA;
+    return SPX_OK;
+}

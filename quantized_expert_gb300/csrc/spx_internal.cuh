@@ -1,0 +1,244 @@
+// spx_internal.cuh -- shared device helpers and packed-format geometry for libspx.
+// sm_103a only: inline PTX for mbarriers, bulk copies (TMA engine), the
+// m16n8k16 tensor-core instruction and LOP3; nothing here is portable on purpose.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spx.h"
+
+namespace spx {
+
+// ---------------------------------------------------------------- limits --
+constexpr int kMaxT = 64;          // tokens per call
+constexpr int kMaxE = 256;         // experts
+constexpr int kMaxSlots = 512;     // T * k
+constexpr int kMaxH = 8192;
+constexpr int kGroup = 128;        // GPTQ group size along K
+constexpr int kChunk = 16384;      // bytes per ring stage
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
+constexpr int kSmemLimit = 227 * 1024;
+
+// --------------------------------------------------------- workspace ---
+// Header of the caller's workspace (zeroed once; kernels leave it zeroed).
+struct WsHeader {
+    uint32_t work_counter;   // dynamic unit queue of the expert launch
+    uint32_t done_ticket;    // completed blocks of the expert launch
+    int32_t status;          // SPX_OK or SPX_ERR_TIMEOUT (sticky)
+    uint32_t route_ticket;   // completed blocks of the router product
+    uint32_t pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+constexpr size_t kWsAccOffset = 256;
+
+__host__ __device__ inline size_t ws_acc_bytes(int T, int H) {
+    return ((size_t)T * H * 4 + 255) / 256 * 256;
+}
+__host__ __device__ inline size_t ws_gamma_offset(int T, int H) { return kWsAccOffset + ws_acc_bytes(T, H); }
+
+// ----------------------------------------------------- packed geometry ---
+// INT4 unit (S = 16*MS columns of I):
+//   [gu scales: (H/128) x 2S fp16, gate cols then up cols]
+//   [gu codes : (H/16)/KB blocks of 512 B, KB = 2/MS k-steps per block;
+//               block = 32 lanes x 16 B, lane's 4 words = [ks_in][tile]]
+//   [down codes: (H/16)/MB blocks of 512 B, MB = 4/MS m-tiles per block;
+//               lane's 4 words = [tile_in][ks]]
+// then after all units: down scales [E][I/128][H] fp16 (canonical).
+__host__ __device__ inline size_t w4_unit_bytes(int H, int S) { return (size_t)49 * H * S / 32; }
+__host__ __device__ inline size_t w4_sc_bytes(int H, int S) { return (size_t)(H / 128) * 2 * S * 2; }
+__host__ __device__ inline size_t w4_gu_bytes(int H, int S) { return (size_t)H * S; }
+__host__ __device__ inline size_t w4_dn_bytes(int H, int S) { return (size_t)H * S / 2; }
+__host__ __device__ inline size_t w4_units_bytes(int E, int H, int I, int S) {
+    return (size_t)E * (I / S) * w4_unit_bytes(H, S);
+}
+// FP16 unit (S = 16):
+//   [gu  : H/16 blocks (one k-step each) of 2 tiles x 32 lanes x 16 B]
+//   [down: H/32 blocks (one m-tile pair each) of 2 tiles x 32 lanes x 16 B]
+constexpr int kF16S = 16;
+__host__ __device__ inline size_t f16_unit_bytes(int H) { return (size_t)6 * H * kF16S; }
+__host__ __device__ inline size_t f16_gu_bytes(int H) { return (size_t)4 * H * kF16S; }
+
+// Physical output column of row m (0..15) of down tile mt: tile pair P = mt/2
+// covers 32 columns; rows (g, g+8) of tile q land on columns 4g+2q, 4g+2q+1,
+// so one lane's C fragments of a pair are 4 consecutive columns of a token.
+__host__ __device__ inline int down_col(int mt, int m) {
+    return 32 * (mt >> 1) + 4 * (m & 7) + 2 * (mt & 1) + (m >> 3);
+}
+// Row/column of an m16k16 A-fragment element: lane (g = lane/4, c = lane%4),
+// register r (0..3), half h (0..1).
+__host__ __device__ inline int frag_row(int lane, int r) { return (lane >> 2) + 8 * (r & 1); }
+__host__ __device__ inline int frag_col(int lane, int r, int h) { return 2 * (lane & 3) + h + 8 * (r >> 1); }
+
+#if defined(__CUDACC__)
+// ------------------------------------------------------------- PTX ------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait: gives up after `budget_ns` of wall time (or at once when
+// *abort is already set), records SPX_ERR_TIMEOUT in the status word and
+// sets *abort so every later wait in the block returns immediately.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  int32_t *status, uint64_t budget_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (*abort) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > budget_ns) {
+            atomicCAS(status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+// Bulk copy (TMA engine, no tensor map): global -> shared, completion counted
+// on an mbarrier in bytes.  Both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+    return v;
+}
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// One packed INT4 word -> one m16k16 A fragment (4 x half2) holding code-8.
+// OR-ing a nibble into the mantissa of fp16 1024.0 (0x6400) gives 1024 + q
+// exactly; subtracting 1032 leaves q - 8.  The nibble in bits 4..7 of each
+// half gives 1024 + 16q; a fused (x/16 - 72) gives q - 8.  Nibble j of the word
+// is register (j & 3), half (j >> 2).
+__device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t (&a)[4]) {
+    const uint32_t kMagic = 0x64006400u, kLo = 0x000F000Fu, kHi = 0x00F000F0u;
+    const uint32_t w8 = w >> 8;
+    const __half2 sub = u32_as_h2(0x64086408u);   // (1032, 1032)
+    const __half2 mul = u32_as_h2(0x2C002C00u);   // (1/16, 1/16)
+    const __half2 add = u32_as_h2(0xD480D480u);   // (-72, -72)
+    a[0] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w, kLo, kMagic)), sub));
+    a[1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w, kHi, kMagic)), mul, add));
+    a[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w8, kLo, kMagic)), sub));
+    a[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w8, kHi, kMagic)), mul, add));
+}
+#endif  // __CUDACC__
+
+
+// ------------------------------------------------------- launch params --
+struct RouteParams {
+    const __half *x;
+    const __half *w_router;  // nullable: logits are given
+    float *logits;
+    int T, H, E, k, renorm;
+    int32_t *topk_ids;
+    float *topk_w;
+    uint32_t *elb;  // nullable
+    int layer;
+    int32_t *counts, *offsets, *sorted_slots, *active, *n_active;  // all or none
+    WsHeader *hdr;
+};
+
+struct EngineParams {
+    // routed experts (packed units)
+    const uint8_t *routed;
+    const __half *w4_sdown;  // INT4: down scales [E][I/128][H]
+    int routed_fmt;          // 0 INT4, 1 FP16
+    int S;                   // routed slice width (INT4: 16/32; FP16: 16)
+    int E, I, k;
+    int routed_enabled;
+    const int32_t *offsets, *sorted_slots, *active, *n_active;
+    const float *topk_w;
+    // shared expert (FP16, S = 16), nullable
+    const uint8_t *shared;
+    const __half *w_sgate;
+    int I_s;
+    // problem
+    const __half *x;
+    int T, H;
+    // output
+    int mode;      // 0 sorted rows, 1 accumulate (gamma-scaled), 2 layer (weighted, last block writes out)
+    float *yout;   // mode 0: y_sorted; otherwise the fp32 accumulator
+    __half *out;   // mode 2: final fp16 output
+    WsHeader *hdr;
+    // geometry
+    int nstages;
+    int npad;      // token columns of the shared scratch: 8 * ceil(T / 8)
+    uint64_t wait_budget_ns;
+};
+
+int launch_route(const RouteParams &p, cudaStream_t s);
+int route_validate(const uint16_t *x, const uint16_t *w_router, const float *logits, int T, int H, int E, int k,
+                   const int32_t *ids, const float *w);
+int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl);
+int engine_fits(int T, int H);
+
+// -------------------------------------------------------- host helpers --
+int device_sm_count();
+int record_launch(cudaError_t e);
+
+}  // namespace spx

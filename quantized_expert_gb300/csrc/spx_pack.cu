@@ -1,0 +1,198 @@
+// spx_pack.cu -- one-time repack of canonical expert tensors into the packed
+// units the expert launch streams (see spx_internal.cuh for the geometry).
+//
+// Canonical inputs: GPTQ INT4 with group size 128 and zero point 8 (richland.au
+// post, "What shipped"): qweight [K/8][N] int32 with code kk at bits
+// 4*(kk%8), scales [K/128][N] fp16; FP16 experts in PyTorch [out][in] layout.
+// The repack is a pure permutation of codes / values (scales are copied), so
+// it is bit-exact and deterministic.
+#include "spx_internal.cuh"
+
+namespace spx {
+
+__device__ __forceinline__ uint32_t gptq_code(const int32_t *q, int N, int kk, int n) {
+    const uint32_t w = static_cast<uint32_t>(q[(size_t)(kk >> 3) * N + n]);
+    return (w >> (4 * (kk & 7))) & 15u;
+}
+
+// Gate/up scales: unit (e, j) section [H/128][2S]: gate columns then up columns.
+__global__ void w4_pack_scales(const uint16_t *s_gate, const uint16_t *s_up, int E, int H, int I, int S,
+                               uint8_t *packed) {
+    const int spe = I / S, G = H / 128;
+    const size_t total = (size_t)E * spe * G * 2 * S;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int c2 = idx % (2 * S);
+        const int grp = (idx / (2 * S)) % G;
+        const size_t unit = idx / ((size_t)2 * S * G);
+        const int e = unit / spe, j = unit % spe;
+        const int i = j * S + (c2 % S);
+        const uint16_t *src = c2 < S ? s_gate : s_up;
+        uint16_t *dst = reinterpret_cast<uint16_t *>(packed + unit * w4_unit_bytes(H, S));
+        dst[grp * 2 * S + c2] = src[((size_t)e * G + grp) * I + i];
+    }
+}
+
+// Gate/up codes: block b holds KB = 2/MS k-steps; lane word w = [ki][tile],
+// tile t < MS gate columns 16t.., t >= MS up columns 16(t-MS)..; nibble j of a
+// word is fragment register (j & 3), half (j >> 2).
+__global__ void w4_pack_gu(const int32_t *qg, const int32_t *qu, int E, int H, int I, int S, uint8_t *packed) {
+    const int MS = S / 16, KB = 2 / MS, NTILE = 2 * MS, spe = I / S;
+    const int nblk = (H / 16) / KB;
+    const size_t total = (size_t)E * spe * nblk * 32 * 4;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int wi = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int b = (idx >> 7) % nblk;
+        const size_t unit = (idx >> 7) / nblk;
+        const int e = unit / spe, jsl = unit % spe;
+        const int ki = wi / NTILE, t = wi % NTILE;
+        const int ks = b * KB + ki;
+        const int32_t *q = (t < MS ? qg : qu) + (size_t)e * (H / 8) * I;
+        const int icol0 = jsl * S + 16 * (t % MS);
+        uint32_t word = 0;
+        for (int nib = 0; nib < 8; ++nib) {
+            const int r = nib & 3, hh = nib >> 2;
+            const int m = frag_row(lane, r), kc = frag_col(lane, r, hh);
+            word |= gptq_code(q, I, 16 * ks + kc, icol0 + m) << (4 * nib);
+        }
+        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * w4_unit_bytes(H, S) + w4_sc_bytes(H, S));
+        dst[(size_t)b * 128 + lane * 4 + wi] = word;
+    }
+}
+
+// Down codes: block b holds MB = 4/MS m-tiles; lane word w = [tile_in][ks];
+// A[m][kc] = code of W_down[i0 + 16 ks + kc][down_col(mt, m)].
+__global__ void w4_pack_down(const int32_t *qd, int E, int H, int I, int S, uint8_t *packed) {
+    const int MS = S / 16, MB = 4 / MS, spe = I / S;
+    const int nblk = (H / 16) / MB;
+    const size_t total = (size_t)E * spe * nblk * 32 * 4;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int wi = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int b = (idx >> 7) % nblk;
+        const size_t unit = (idx >> 7) / nblk;
+        const int e = unit / spe, jsl = unit % spe;
+        const int tin = wi / MS, ks = wi % MS;
+        const int mt = b * MB + tin;
+        const int32_t *q = qd + (size_t)e * (I / 8) * H;
+        uint32_t word = 0;
+        for (int nib = 0; nib < 8; ++nib) {
+            const int r = nib & 3, hh = nib >> 2;
+            const int m = frag_row(lane, r), kc = frag_col(lane, r, hh);
+            word |= gptq_code(q, H, jsl * S + 16 * ks + kc, down_col(mt, m)) << (4 * nib);
+        }
+        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * w4_unit_bytes(H, S) + w4_sc_bytes(H, S) +
+                                                     w4_gu_bytes(H, S));
+        dst[(size_t)b * 128 + lane * 4 + wi] = word;
+    }
+}
+
+// FP16 gate/up: block = k-step ks: [tile t (0 gate, 1 up)][lane] x 16 B; the
+// 16 B are the fragment registers r = 0..3, halves h = 0..1.
+__global__ void f16_pack_gu(const uint16_t *wg, const uint16_t *wu, int E, int H, int I, uint8_t *packed) {
+    const int spe = I / kF16S;
+    const size_t total = (size_t)E * spe * (H / 16) * 2 * 32 * 4;  // 32-bit words
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int r = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int t = (idx >> 7) & 1;
+        const int ks = (idx >> 8) % (H / 16);
+        const size_t unit = (idx >> 8) / (H / 16);
+        const int e = unit / spe, jsl = unit % spe;
+        const uint16_t *w = (t == 0 ? wg : wu) + (size_t)e * I * H;
+        const int i = jsl * kF16S + frag_row(lane, r);
+        uint32_t word = 0;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int kk = 16 * ks + frag_col(lane, r, hh);
+            word |= (uint32_t)w[(size_t)i * H + kk] << (16 * hh);
+        }
+        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * f16_unit_bytes(H));
+        dst[(((size_t)ks * 2 + t) * 32 + lane) * 4 + r] = word;
+    }
+}
+
+// FP16 down: block = m-tile pair P: [q][lane] x 16 B; A[m][kc] =
+// W_down[down_col(2P+q, m)][i0 + kc].
+__global__ void f16_pack_down(const uint16_t *wd, int E, int H, int I, uint8_t *packed) {
+    const int spe = I / kF16S;
+    const size_t total = (size_t)E * spe * (H / 32) * 2 * 32 * 4;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int r = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int q = (idx >> 7) & 1;
+        const int P = (idx >> 8) % (H / 32);
+        const size_t unit = (idx >> 8) / (H / 32);
+        const int e = unit / spe, jsl = unit % spe;
+        const uint16_t *w = wd + (size_t)e * H * I;
+        const int n = down_col(2 * P + q, frag_row(lane, r));
+        uint32_t word = 0;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int i = jsl * kF16S + frag_col(lane, r, hh);
+            word |= (uint32_t)w[(size_t)n * I + i] << (16 * hh);
+        }
+        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * f16_unit_bytes(H) + f16_gu_bytes(H));
+        dst[(((size_t)P * 2 + q) * 32 + lane) * 4 + r] = word;
+    }
+}
+
+static int grid_for(size_t total) {
+    size_t g = (total + 255) / 256;
+    if (g > 65535) g = 65535;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace spx
+
+using namespace spx;
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+extern "C" size_t spx_w4_packed_bytes(int E, int H, int I, int S) {
+    if (E < 1 || H < 128 || I < 128 || (S != 16 && S != 32) || H % 128 || I % 128) return 0;
+    return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
+}
+
+extern "C" size_t spx_f16_packed_bytes(int E, int H, int I) {
+    if (E < 1 || H < 128 || I < 16 || H % 128 || I % kF16S) return 0;
+    return (size_t)E * (I / kF16S) * f16_unit_bytes(H);
+}
+
+extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, const int32_t *qw_up,
+                             const uint16_t *s_up, const int32_t *qw_down, const uint16_t *s_down, int E, int H,
+                             int I, int S, void *packed, spx_stream_t stream) {
+    if (!qw_gate || !s_gate || !qw_up || !s_up || !qw_down || !s_down || !packed) return SPX_ERR_INVALID_ARG;
+    if (E < 1 || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
+    if ((S != 16 && S != 32) || H % 128 || I % 128 || H > kMaxH || E > kMaxE) return SPX_ERR_UNSUPPORTED;
+    if (!aligned16(packed)) return SPX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *out = static_cast<uint8_t *>(packed);
+    const int spe = I / S;
+    size_t tot = (size_t)E * spe * (H / 128) * 2 * S;
+    w4_pack_scales<<<grid_for(tot), 256, 0, s>>>(s_gate, s_up, E, H, I, S, out);
+    tot = (size_t)E * spe * ((H / 16) / (2 / (S / 16))) * 128;
+    w4_pack_gu<<<grid_for(tot), 256, 0, s>>>(qw_gate, qw_up, E, H, I, S, out);
+    tot = (size_t)E * spe * ((H / 16) / (4 / (S / 16))) * 128;
+    w4_pack_down<<<grid_for(tot), 256, 0, s>>>(qw_down, E, H, I, S, out);
+    int st = record_launch(cudaGetLastError());
+    if (st) return st;
+    cudaError_t e = cudaMemcpyAsync(out + w4_units_bytes(E, H, I, S), s_down, (size_t)E * (I / 128) * H * 2,
+                                    cudaMemcpyDeviceToDevice, s);
+    return record_launch(e);
+}
+
+extern "C" int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down, int E, int H,
+                              int I, void *packed, spx_stream_t stream) {
+    if (!w_gate || !w_up || !w_down || !packed) return SPX_ERR_INVALID_ARG;
+    if (E < 1 || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
+    if (H % 128 || I % kF16S || H > kMaxH || E > kMaxE) return SPX_ERR_UNSUPPORTED;
+    if (!aligned16(packed)) return SPX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *out = static_cast<uint8_t *>(packed);
+    const int spe = I / kF16S;
+    size_t tot = (size_t)E * spe * (H / 16) * 2 * 128;
+    f16_pack_gu<<<grid_for(tot), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
+    tot = (size_t)E * spe * (H / 32) * 2 * 128;
+    f16_pack_down<<<grid_for(tot), 256, 0, s>>>(w_down, E, H, I, out);
+    return record_launch(cudaGetLastError());
+}

@@ -1,0 +1,327 @@
+// spx_route.cu -- router product, softmax + top-k, Expert Lookahead Buffer
+// counters and the counting-sort gather, as one small launch.
+//
+// Method (ai.info summary of the Specter paper, Key Contributions 2-4 and
+// "Methodology in Plain English"; richland.au post, "What shipped"): the draft
+// shares the target's FP16 router; GPU-side counters tally per layer how often
+// each expert is selected by draft tokens; tokens are gathered by expert so
+// each expert's work is dispatched once.
+//
+// Layout of the launch: when a router weight is given, blocks compute the
+// [T][E] logits (one warp per expert row, fp32 accumulate), the last block to
+// finish (completion ticket in the workspace, no spin) selects; otherwise a
+// single block selects from the given logits.  Selection: one warp per token,
+// k rounds of a warp-wide (value desc, index asc) arg-max; softmax with expf.
+#include "spx_internal.cuh"
+
+#include <math.h>
+
+namespace spx {
+
+
+__device__ __forceinline__ float dot8_h(uint4 a, uint4 b, float acc) {
+    const __half2 *pa = reinterpret_cast<const __half2 *>(&a);
+    const __half2 *pb = reinterpret_cast<const __half2 *>(&b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 fa = __half22float2(pa[i]);
+        float2 fb = __half22float2(pb[i]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+    }
+    return acc;
+}
+
+// logits[t][e] for e handled by this warp; 16 tokens per pass.
+__device__ void router_rows(const RouteParams &p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    for (int e = blockIdx.x * wpb + warp; e < p.E; e += gridDim.x * wpb) {
+        const uint4 *wr = reinterpret_cast<const uint4 *>(p.w_router + (size_t)e * p.H);
+        for (int t0 = 0; t0 < p.T; t0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int h8 = lane; h8 < p.H / 8; h8 += 32) {
+                uint4 w = __ldg(wr + h8);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (t0 + i < p.T) {
+                        uint4 xv = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)(t0 + i) * p.H) + h8);
+                        acc[i] = dot8_h(xv, w, acc[i]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float v = acc[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0 && t0 + i < p.T) p.logits[(size_t)(t0 + i) * p.E + e] = v;
+            }
+        }
+    }
+}
+
+// Counting sort of the T*k slots held in s_ids (shared) into the caller's
+// gather arrays.  Whole block participates.
+__device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts, int32_t *offsets,
+                             int32_t *sorted_slots, int32_t *active, int32_t *n_active) {
+    __shared__ int s_cnt[kMaxE];
+    __shared__ int s_off[kMaxE + 1];
+    __shared__ int s_act[kMaxE];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    for (int s = tid; s < n; s += blockDim.x) atomicAdd(&s_cnt[s_ids[s]], 1);
+    __syncthreads();
+    if (tid < 32) {
+        // exclusive scans of counts and of (count > 0); each lane owns a run of 8
+        const int lane = tid;
+        int c[8], f[8];
+        int sc = 0, sf = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int e = lane * 8 + i;
+            c[i] = e < E ? s_cnt[e] : 0;
+            f[i] = c[i] > 0;
+            sc += c[i];
+            sf += f[i];
+        }
+        int ic = sc, jf = sf;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int a = __shfl_up_sync(0xffffffffu, ic, o);
+            int b = __shfl_up_sync(0xffffffffu, jf, o);
+            if (lane >= o) {
+                ic += a;
+                jf += b;
+            }
+        }
+        int run = ic - sc, runf = jf - sf;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int e = lane * 8 + i;
+            if (e < E) {
+                s_off[e] = run;
+                if (f[i]) s_act[runf] = e;
+            }
+            run += c[i];
+            runf += f[i];
+        }
+        if (lane == 31) {
+            s_off[E] = ic;
+            *n_active = jf;
+            for (int a = jf; a < E; ++a) s_act[a] = -1;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        counts[e] = s_cnt[e];
+        offsets[e] = s_off[e];
+        active[e] = s_act[e];
+    }
+    if (tid == 0) offsets[E] = s_off[E];
+    // stable placement: rank of slot s among earlier slots of the same expert
+    for (int s = tid; s < n; s += blockDim.x) {
+        const int e = s_ids[s];
+        int rank = 0;
+        for (int s2 = 0; s2 < s; ++s2) rank += (s_ids[s2] == e);
+        sorted_slots[s_off[e] + rank] = s;
+    }
+}
+
+// Softmax, top-k, weights, counters and gather; one block.
+__device__ void select_block(const RouteParams &p) {
+    __shared__ int32_t s_ids[kMaxSlots];
+    __shared__ float s_pw[kMaxSlots];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int nper = (p.E + 31) >> 5;  // <= 8
+    for (int t = warp; t < p.T; t += wpb) {
+        float v[8];
+        bool taken[8];
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            const bool ok = j < nper && e < p.E;
+            v[j] = ok ? __ldcg(p.logits + (size_t)t * p.E + e) : -INFINITY;
+            taken[j] = !ok;
+            if (ok) m = fmaxf(m, v[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (!taken[j]) z += expf(v[j] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        float psel = 0.f;
+        for (int r = 0; r < p.k; ++r) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = lane + 32 * j;
+                if (!taken[j] && (v[j] > bv || (v[j] == bv && e < be))) {
+                    bv = v[j];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j == (be >> 5)) taken[j] = true;
+            }
+            const float pr = expf(bv - m) / z;
+            psel += pr;
+            if (lane == 0) {
+                p.topk_ids[(size_t)t * p.k + r] = be;
+                s_ids[t * p.k + r] = be;
+                s_pw[t * p.k + r] = pr;
+                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * p.E + be, 1u);
+            }
+        }
+        if (lane == 0)
+            for (int r = 0; r < p.k; ++r)
+                p.topk_w[(size_t)t * p.k + r] = p.renorm ? s_pw[t * p.k + r] / psel : s_pw[t * p.k + r];
+    }
+    __syncthreads();
+    if (p.counts)
+        gather_block(s_ids, p.T * p.k, p.E, p.counts, p.offsets, p.sorted_slots, p.active, p.n_active);
+}
+
+__global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
+    // Let a programmatically dependent expert launch start its routing-
+    // independent work (shared expert) while this one runs.
+    griddep_launch_dependents();
+    if (p.w_router) {
+        router_rows(p);
+        __shared__ int s_last;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s_last = atomicAdd(&p.hdr->route_ticket, 1u) == gridDim.x - 1;
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (threadIdx.x == 0) p.hdr->route_ticket = 0;
+    }
+    select_block(p);
+}
+
+__global__ void __launch_bounds__(256) elb_kernel(uint32_t *elb, int E, int layer, const int32_t *ids, int n) {
+    for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) atomicAdd(elb + (size_t)layer * E + e, 1u);
+    }
+}
+
+__global__ void __launch_bounds__(256) gather_kernel(const int32_t *ids, int n, int E, int32_t *counts,
+                                                      int32_t *offsets, int32_t *sorted_slots, int32_t *active,
+                                                      int32_t *n_active) {
+    __shared__ int32_t s_ids[kMaxSlots];
+    for (int s = threadIdx.x; s < n; s += blockDim.x) {
+        const int e = ids[s];
+        s_ids[s] = (e >= 0 && e < E) ? e : 0;
+    }
+    __syncthreads();
+    gather_block(s_ids, n, E, counts, offsets, sorted_slots, active, n_active);
+}
+
+// ----------------------------------------------------------- launchers --
+static int check_route_shape(int T, int H, int E, int k) {
+    if (T < 1 || E < 1 || k < 1 || H < 0) return SPX_ERR_INVALID_ARG;
+    if (k > E) return SPX_ERR_INVALID_ARG;
+    if (T > kMaxT || E > kMaxE || T * k > kMaxSlots) return SPX_ERR_UNSUPPORTED;
+    return SPX_OK;
+}
+
+int launch_route(const RouteParams &p, cudaStream_t s) {
+    int grid = 1;
+    if (p.w_router) grid = (p.E + 7) / 8;
+    route_kernel<<<grid, 256, 0, s>>>(p);
+    return record_launch(cudaGetLastError());
+}
+
+int route_validate(const uint16_t *x, const uint16_t *w_router, const float *logits, int T, int H, int E, int k,
+                   const int32_t *ids, const float *w) {
+    int st = check_route_shape(T, H, E, k);
+    if (st) return st;
+    if (!logits || !ids || !w) return SPX_ERR_INVALID_ARG;
+    if (w_router) {
+        if (!x) return SPX_ERR_INVALID_ARG;
+        if (H % 128 || H > kMaxH || H < 128) return SPX_ERR_UNSUPPORTED;
+        if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router)) & 15) return SPX_ERR_INVALID_ARG;
+    }
+    return SPX_OK;
+}
+
+}  // namespace spx
+
+using namespace spx;
+
+extern "C" int spx_route_topk(const uint16_t *x, const uint16_t *w_router, float *logits, int T, int H, int E,
+                              int k, int renorm, int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes,
+                              spx_stream_t stream) {
+    int st = route_validate(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
+    if (st) return st;
+    if (w_router && (!ws || ws_bytes < sizeof(WsHeader))) return SPX_ERR_WORKSPACE;
+    RouteParams p{};
+    p.x = reinterpret_cast<const __half *>(x);
+    p.w_router = reinterpret_cast<const __half *>(w_router);
+    p.logits = logits;
+    p.T = T;
+    p.H = H;
+    p.E = E;
+    p.k = k;
+    p.renorm = renorm;
+    p.topk_ids = topk_ids;
+    p.topk_w = topk_w;
+    p.hdr = reinterpret_cast<WsHeader *>(ws);
+    return launch_route(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int spx_elb_accumulate(uint32_t *elb, int L, int E, int layer, const int32_t *topk_ids, int T, int k,
+                                  spx_stream_t stream) {
+    if (!elb || !topk_ids || L < 1 || E < 1 || T < 1 || k < 1 || layer < 0 || layer >= L || k > E)
+        return SPX_ERR_INVALID_ARG;
+    if (E > kMaxE || T > kMaxT || T * k > kMaxSlots) return SPX_ERR_UNSUPPORTED;
+    elb_kernel<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(elb, E, layer, topk_ids, T * k);
+    return record_launch(cudaGetLastError());
+}
+
+extern "C" int spx_elb_read(const uint32_t *elb, int L, int E, uint32_t *dst, spx_stream_t stream) {
+    if (!elb || !dst || L < 1 || E < 1) return SPX_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(dst, elb, sizeof(uint32_t) * (size_t)L * E, cudaMemcpyDefault,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    return record_launch(e);
+}
+
+extern "C" int spx_elb_reset(uint32_t *elb, int L, int E, spx_stream_t stream) {
+    if (!elb || L < 1 || E < 1) return SPX_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(elb, 0, sizeof(uint32_t) * (size_t)L * E, reinterpret_cast<cudaStream_t>(stream));
+    return record_launch(e);
+}
+
+extern "C" int spx_gather_by_expert(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                                    int32_t *sorted_slots, int32_t *active, int32_t *n_active, spx_stream_t stream) {
+    if (!topk_ids || !counts || !offsets || !sorted_slots || !active || !n_active) return SPX_ERR_INVALID_ARG;
+    int st = check_route_shape(T, 0, E, k);
+    if (st) return st;
+    gather_kernel<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(topk_ids, T * k, E, counts, offsets,
+                                                                         sorted_slots, active, n_active);
+    return record_launch(cudaGetLastError());
+}

@@ -1,0 +1,326 @@
+"""Thin Python binding of libspx (include/spx.h): argument marshalling only.
+
+Every function here takes torch tensors that already live on the GPU, passes
+their device pointers and the current CUDA stream to the C entry point of the
+same name, and raises ``SpxError`` on a non-zero status.  No arithmetic of
+the method happens in Python, and there is no fallback: if libspx.so is not
+built, importing the library fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+SPX_OK, SPX_ERR_INVALID_ARG, SPX_ERR_UNSUPPORTED, SPX_ERR_WORKSPACE, SPX_ERR_CUDA, SPX_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+
+
+class SpxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class W4Experts(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int), ("slice_cols", C.c_int)]
+
+
+class F16Experts(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int)]
+
+
+class Shared(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("w_sgate", C.c_void_p), ("H", C.c_int), ("I_s", C.c_int)]
+
+
+class LayerArgs(C.Structure):
+    _fields_ = [("mode", C.c_int), ("T", C.c_int), ("H", C.c_int), ("E", C.c_int), ("k", C.c_int),
+                ("renorm", C.c_int), ("x", C.c_void_p), ("w_router", C.c_void_p), ("logits", C.c_void_p),
+                ("w4", C.POINTER(W4Experts)), ("f16", C.POINTER(F16Experts)), ("shared", C.POINTER(Shared)),
+                ("elb", C.c_void_p), ("L", C.c_int), ("layer", C.c_int),
+                ("topk_ids", C.c_void_p), ("topk_w", C.c_void_p), ("counts", C.c_void_p),
+                ("offsets", C.c_void_p), ("sorted_slots", C.c_void_p), ("active", C.c_void_p),
+                ("n_active", C.c_void_p), ("out", C.c_void_p), ("ws", C.c_void_p), ("ws_bytes", C.c_size_t),
+                ("ev_experts_begin", C.c_void_p), ("ev_experts_end", C.c_void_p)]
+
+
+_SIGS = {
+    "spx_status_string": (C.c_char_p, [C.c_int]),
+    "spx_version": (C.c_int, []),
+    "spx_route_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "spx_elb_accumulate": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
+    "spx_elb_read": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "spx_elb_reset": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
+    "spx_gather_by_expert": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_void_p, C.c_void_p]),
+    "spx_w4_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "spx_f16_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "spx_w4_repack": (C.c_int, [C.c_void_p] * 6 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "spx_f16_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "spx_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
+    "spx_workspace_init": (C.c_int, [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "spx_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
+    "spx_moe_draft_w4a16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(W4Experts), C.c_int] + [C.c_void_p] * 5 +
+                            [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "spx_moe_verify_fp16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(F16Experts), C.c_int] + [C.c_void_p] * 5 +
+                            [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "spx_combine": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(Shared), C.c_int, C.c_int,
+                              C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "spx_moe_layer": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libspx.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise ImportError(f"libspx.so is not built ({p}); run quantized_expert_gb300.build.build() "
+                              "(or __graft_entry__.build()) first -- there is no fallback path")
+        L = C.CDLL(p)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGS)
+
+
+def status_string(st: int) -> str:
+    return load().spx_status_string(st).decode()
+
+
+def _chk(st: int, what: str):
+    if st != SPX_OK:
+        raise SpxError(st, what)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libspx takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libspx takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------------ API ----
+def spx_version() -> int:
+    return load().spx_version()
+
+
+def spx_workspace_size(T: int, H: int) -> int:
+    return load().spx_workspace_size(T, H)
+
+
+def new_workspace(T: int, H: int, device="cuda", stream=None) -> torch.Tensor:
+    """Allocate (through torch) and zero a workspace for up to T tokens."""
+    n = spx_workspace_size(T, H)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    spx_workspace_init(ws, stream)
+    return ws
+
+
+def spx_workspace_init(ws: torch.Tensor, stream=None):
+    _chk(load().spx_workspace_init(_p(ws), ws.numel(), _stream(stream)), "spx_workspace_init")
+
+
+def spx_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    out = torch.zeros(1, dtype=torch.int32, device=ws.device)
+    _chk(load().spx_workspace_status(_p(ws), _p(out), _stream(stream)), "spx_workspace_status")
+    return int(out.item())
+
+
+def spx_route_topk(x, w_router, logits, T, H, E, k, renorm, topk_ids, topk_w, ws, stream=None):
+    _chk(load().spx_route_topk(_p(x), _p(w_router), _p(logits), T, H, E, k, int(bool(renorm)), _p(topk_ids),
+                               _p(topk_w), _p(ws), ws.numel() if ws is not None else 0, _stream(stream)),
+         "spx_route_topk")
+
+
+def spx_elb_accumulate(elb, layer, topk_ids, stream=None):
+    L, E = elb.shape
+    T, k = topk_ids.shape
+    _chk(load().spx_elb_accumulate(_p(elb), L, E, layer, _p(topk_ids), T, k, _stream(stream)), "spx_elb_accumulate")
+
+
+def spx_elb_read(elb, dst, stream=None):
+    L, E = elb.shape
+    dptr = dst.data_ptr()
+    _chk(load().spx_elb_read(_p(elb), L, E, dptr, _stream(stream)), "spx_elb_read")
+
+
+def spx_elb_reset(elb, stream=None):
+    L, E = elb.shape
+    _chk(load().spx_elb_reset(_p(elb), L, E, _stream(stream)), "spx_elb_reset")
+
+
+def spx_gather_by_expert(topk_ids, E, counts, offsets, sorted_slots, active, n_active, stream=None):
+    T, k = topk_ids.shape
+    _chk(load().spx_gather_by_expert(_p(topk_ids), T, k, E, _p(counts), _p(offsets), _p(sorted_slots), _p(active),
+                                     _p(n_active), _stream(stream)), "spx_gather_by_expert")
+
+
+@dataclass
+class PackedW4:
+    buf: torch.Tensor
+    E: int
+    H: int
+    I: int
+    S: int
+
+    def cstruct(self) -> W4Experts:
+        return W4Experts(self.buf.data_ptr(), self.E, self.H, self.I, self.S)
+
+
+@dataclass
+class PackedF16:
+    buf: torch.Tensor
+    E: int
+    H: int
+    I: int
+
+    def cstruct(self) -> F16Experts:
+        return F16Experts(self.buf.data_ptr(), self.E, self.H, self.I)
+
+
+@dataclass
+class PackedShared:
+    buf: torch.Tensor
+    w_sgate: torch.Tensor | None
+    H: int
+    I_s: int
+
+    def cstruct(self) -> Shared:
+        return Shared(self.buf.data_ptr(), _p(self.w_sgate), self.H, self.I_s)
+
+
+def spx_w4_repack(qw_gate, s_gate, qw_up, s_up, qw_down, s_down, slice_cols=32, stream=None) -> PackedW4:
+    """Canonical GPTQ tensors ([E][K/8][N] int32, [E][K/128][N] fp16 as int16/uint16 bits) -> packed units."""
+    E, H8, I = qw_gate.shape
+    H = H8 * 8
+    n = load().spx_w4_packed_bytes(E, H, I, slice_cols)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_w4_packed_bytes")
+    buf = torch.empty(n, dtype=torch.uint8, device=qw_gate.device)
+    _chk(load().spx_w4_repack(_p(qw_gate), _p(s_gate), _p(qw_up), _p(s_up), _p(qw_down), _p(s_down), E, H, I,
+                              slice_cols, _p(buf), _stream(stream)), "spx_w4_repack")
+    return PackedW4(buf, E, H, I, slice_cols)
+
+
+def spx_f16_repack(w_gate, w_up, w_down, stream=None) -> PackedF16:
+    """Canonical [E][I][H], [E][I][H], [E][H][I] fp16 -> packed units."""
+    E, I, H = w_gate.shape
+    n = load().spx_f16_packed_bytes(E, H, I)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_f16_packed_bytes")
+    buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
+    _chk(load().spx_f16_repack(_p(w_gate), _p(w_up), _p(w_down), E, H, I, _p(buf), _stream(stream)), "spx_f16_repack")
+    return PackedF16(buf, E, H, I)
+
+
+def pack_shared(w_gate, w_up, w_down, w_sgate=None, stream=None) -> PackedShared:
+    """Shared expert [I_s][H], [I_s][H], [H][I_s] fp16 -> packed (one FP16 expert)."""
+    p = spx_f16_repack(w_gate[None], w_up[None], w_down[None], stream)
+    return PackedShared(p.buf, w_sgate, p.H, p.I)
+
+
+def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+    T = x.shape[0]
+    cs = w.cstruct()
+    _chk(load().spx_moe_draft_w4a16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
+                                    _p(n_active), _p(y_sorted), _p(ws), ws.numel(), _stream(stream)),
+         "spx_moe_draft_w4a16")
+
+
+def spx_moe_verify_fp16(x, w: PackedF16, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+    T = x.shape[0]
+    cs = w.cstruct()
+    _chk(load().spx_moe_verify_fp16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
+                                    _p(n_active), _p(y_sorted), _p(ws), ws.numel(), _stream(stream)),
+         "spx_moe_verify_fp16")
+
+
+def spx_combine(y_sorted, sorted_slots, topk_w, x, shared: PackedShared | None, T, H, k, out, ws, stream=None):
+    cs = shared.cstruct() if shared is not None else None
+    _chk(load().spx_combine(_p(y_sorted), _p(sorted_slots), _p(topk_w), _p(x), C.byref(cs) if cs else None, T, H, k,
+                            _p(out), _p(ws), ws.numel(), _stream(stream)), "spx_combine")
+
+
+@dataclass
+class Routing:
+    """Caller-owned routing buffers of one layer call."""
+    topk_ids: torch.Tensor
+    topk_w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    sorted_slots: torch.Tensor
+    active: torch.Tensor
+    n_active: torch.Tensor
+
+    @staticmethod
+    def empty(T, E, k, device="cuda") -> "Routing":
+        i32 = dict(dtype=torch.int32, device=device)
+        return Routing(torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=device),
+                       torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(T * k, **i32),
+                       torch.empty(E, **i32), torch.empty(1, **i32))
+
+
+def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: PackedW4 | None = None,
+               f16: PackedF16 | None = None, shared: PackedShared | None = None, w_router=None, elb=None,
+               layer=0, events=None):
+    """Build (and keep alive) the argument block of one spx_moe_layer call."""
+    T, H = x.shape
+    keep = []
+    a = LayerArgs()
+    a.mode, a.T, a.H, a.E, a.k, a.renorm = mode, T, H, E, k, int(bool(renorm))
+    a.x, a.w_router, a.logits = _p(x), _p(w_router), _p(logits)
+    if w4 is not None:
+        s4 = w4.cstruct()
+        keep.append(s4)
+        a.w4 = C.pointer(s4)
+    if f16 is not None:
+        s16 = f16.cstruct()
+        keep.append(s16)
+        a.f16 = C.pointer(s16)
+    if shared is not None:
+        ss = shared.cstruct()
+        keep.append(ss)
+        a.shared = C.pointer(ss)
+    if elb is not None:
+        a.elb, a.L, a.layer = _p(elb), elb.shape[0], layer
+    r = routing
+    a.topk_ids, a.topk_w, a.counts, a.offsets = _p(r.topk_ids), _p(r.topk_w), _p(r.counts), _p(r.offsets)
+    a.sorted_slots, a.active, a.n_active = _p(r.sorted_slots), _p(r.active), _p(r.n_active)
+    a.out, a.ws, a.ws_bytes = _p(out), _p(ws), ws.numel()
+    if events is not None:
+        a.ev_experts_begin, a.ev_experts_end = events[0].cuda_event, events[1].cuda_event
+        keep.append(events)
+    return a, keep
+
+
+def spx_moe_layer(args: LayerArgs, stream=None):
+    _chk(load().spx_moe_layer(C.byref(args), _stream(stream)), "spx_moe_layer")

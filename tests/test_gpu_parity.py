@@ -1,0 +1,315 @@
+"""GPU parity: every C-ABI call of libspx against the CPU oracle on the same
+seeded inputs.  Routing ids, counters and gathers must be bit-exact; fp32 /
+fp16 outputs within the tolerance in gpu_helpers (max err <= 1e-2 max|ref|,
+mean relative error <= 1e-3)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import spx_workloads as W  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from quantized_expert_gb300 import build, spx
+    build.build()
+    spx.load()
+    yield
+
+
+def _spx():
+    from quantized_expert_gb300 import spx
+    return spx
+
+
+def _gh():
+    import gpu_helpers
+    return gpu_helpers
+
+
+# ------------------------------------------------------------------ routing
+@pytest.mark.parametrize("E,k,T,renorm", [(64, 6, 17, False), (64, 6, 1, False), (60, 4, 9, False),
+                                          (16, 2, 17, True), (8, 2, 4, True), (8, 8, 3, True), (256, 8, 64, False),
+                                          (1, 1, 5, True)])
+def test_route_topk_given_logits(E, k, T, renorm):
+    spx, gh = _spx(), _gh()
+    rng = np.random.default_rng(E * 100 + T)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[:, ::5] = lg[:, :1]           # exact ties across experts
+    lg[0, :] = 0.0                    # an all-tie row
+    lg[min(1, T - 1), ::2] = -0.0     # signed zeros tie with +0.0
+    ids_ref, w_ref = oracle.route_topk(lg.astype(np.float64), k, renorm)
+    d_lg = gh.dev(lg)
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    ws = spx.new_workspace(T, 128)
+    spx.spx_route_topk(None, None, d_lg, T, 128, E, k, renorm, ids, w, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen15_moe"])
+def test_route_router_product(name):
+    spx, gh = _spx(), _gh()
+    s = W.CONFIGS[name]
+    wr = W.gen_router(s)
+    for T in sorted({s.T_draft, s.T_verify}):
+        x = W.gen_x(s, T)
+        lg_ref = oracle.router_logits(x, wr)
+        ids_ref, w_ref = oracle.route_topk(lg_ref, s.k, s.renorm)
+        lg = torch.empty(T, s.E, dtype=torch.float32, device="cuda")
+        ids = torch.empty(T, s.k, dtype=torch.int32, device="cuda")
+        w = torch.empty(T, s.k, dtype=torch.float32, device="cuda")
+        ws = spx.new_workspace(T, s.H)
+        for rep in range(2):  # the completion ticket must reset itself
+            spx.spx_route_topk(gh.dev_f16(x), gh.dev_f16(wr), lg, T, s.H, s.E, s.k, s.renorm, ids, w, ws)
+            torch.cuda.synchronize()
+            lg_g = lg.cpu().numpy().astype(np.float64)
+            assert np.allclose(lg_g, lg_ref, rtol=1e-5, atol=1e-5 * np.abs(lg_ref).max())
+            srt = np.sort(lg_ref.astype(np.float32), axis=1)[:, ::-1]
+            margin = (srt[:, s.k - 1] - srt[:, s.k]).min()
+            assert margin > 1e-4, "seeded inputs have a near-tie at the top-k boundary"
+            assert np.array_equal(ids.cpu().numpy(), ids_ref)
+            assert np.allclose(w.cpu().numpy(), w_ref, rtol=1e-5)
+
+
+def test_elb_and_gather_bit_exact():
+    spx, gh = _spx(), _gh()
+    rng = np.random.default_rng(21)
+    L, E, k = 26, 64, 6
+    elb = torch.zeros(L, E, dtype=torch.int32, device="cuda")
+    elb_ref = np.zeros((L, E), np.uint32)
+    for it in range(40):
+        layer = int(rng.integers(0, L))
+        T = int(rng.integers(1, 65))
+        kk = int(rng.integers(1, 9))
+        Ee = int(rng.integers(kk, 257))
+        ids_np = np.stack([rng.choice(Ee, kk, replace=False) for _ in range(T)]).astype(np.int32)
+        g_ref = oracle.gather_by_expert(ids_np, Ee)
+        ids = gh.dev(ids_np)
+        counts = torch.empty(Ee, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(Ee + 1, dtype=torch.int32, device="cuda")
+        ss = torch.empty(T * kk, dtype=torch.int32, device="cuda")
+        act = torch.empty(Ee, dtype=torch.int32, device="cuda")
+        na = torch.empty(1, dtype=torch.int32, device="cuda")
+        spx.spx_gather_by_expert(ids, Ee, counts, offsets, ss, act, na)
+        if Ee == E:
+            spx.spx_elb_accumulate(elb, layer, ids)
+            oracle.elb_accumulate(elb_ref, layer, ids_np)
+        torch.cuda.synchronize()
+        assert np.array_equal(counts.cpu().numpy(), g_ref["counts"])
+        assert np.array_equal(offsets.cpu().numpy(), g_ref["offsets"])
+        assert np.array_equal(ss.cpu().numpy(), g_ref["sorted_slots"])
+        assert int(na.item()) == g_ref["n_active"]
+        assert np.array_equal(act.cpu().numpy()[:g_ref["n_active"]], g_ref["active"][:g_ref["n_active"]])
+        assert np.all(act.cpu().numpy()[g_ref["n_active"]:] == -1)
+    assert np.array_equal(elb.cpu().numpy().astype(np.uint32), elb_ref)
+    # read (device and pinned host destinations) and reset
+    host = torch.empty(L, E, dtype=torch.int32).pin_memory()
+    spx.spx_elb_read(elb, host)
+    torch.cuda.synchronize()
+    assert np.array_equal(host.numpy().astype(np.uint32), elb_ref)
+    spx.spx_elb_reset(elb)
+    torch.cuda.synchronize()
+    assert int(elb.abs().sum().item()) == 0
+
+
+# ------------------------------------------------------------ expert calls
+def _routing_dev(ids_np, E):
+    gh = _gh()
+    g = oracle.gather_by_expert(ids_np, E)
+    return g, dict(offsets=gh.dev(g["offsets"]), sorted_slots=gh.dev(g["sorted_slots"]),
+                   active=gh.dev(g["active"].astype(np.int32)), n_active=gh.dev(np.array([g["n_active"]], np.int32)))
+
+
+def _small(name, **kw):
+    return W.scaled(W.CONFIGS[name], **kw)
+
+
+SMALL_CASES = [
+    # (shape, T, slice_cols): several tiles, ragged token tiles, both slice widths
+    (_small("tiny"), 4, 32),
+    (_small("tiny"), 4, 16),
+    (_small("deepseek_v2_lite", I=256, E=16), 1, 32),
+    (_small("deepseek_v2_lite", I=256, E=16), 17, 32),
+    (_small("qwen15_moe", I=384, E=12, I_s=512), 9, 16),
+    (_small("phi35_moe", H=1024, I=512), 17, 16),
+    (_small("phi35_moe", H=1024, I=512, k=2), 33, 32),   # > 24 tokens: second token block
+    (_small("deepseek_v2_lite", H=256, I=128, E=8, k=8), 64, 32),  # k = E, maximum T
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_CASES)))
+def test_draft_and_verify_unit_calls(case):
+    spx, gh = _spx(), _gh()
+    s, T, S = SMALL_CASES[case]
+    x = W.gen_x(s, T, step=case)
+    rng = np.random.default_rng(case)
+    lg = rng.standard_normal((T, s.E)).astype(np.float64)
+    ids, w = oracle.route_topk(lg, s.k, s.renorm)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), slice_cols=S)
+    g, r = _routing_dev(ids, s.E)
+    ws = spx.new_workspace(T, s.H)
+    dx = gh.dev_f16(x)
+    for mode in ("draft", "verify"):
+        mlp = oracle.swiglu_w4 if mode == "draft" else oracle.swiglu_f16
+        host = lay.w4_host if mode == "draft" else lay.f16_host
+        y_ref = np.stack([mlp(x[int(sl) // s.k], host[int(ids.reshape(-1)[sl])]) for sl in g["sorted_slots"]])
+        y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
+        for rep in range(2):  # queue counters and scratch must reset themselves
+            if mode == "draft":
+                spx.spx_moe_draft_w4a16(dx, lay.w4, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                                        r["n_active"], y, ws)
+            else:
+                spx.spx_moe_verify_fp16(dx, lay.f16, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                                        r["n_active"], y, ws)
+            torch.cuda.synchronize()
+            gh.check_close(y.cpu().numpy(), y_ref, f"{mode} case {case} rep {rep}")
+        assert spx.spx_workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_combine_with_shared(gated):
+    spx, gh = _spx(), _gh()
+    s = _small("qwen15_moe", I=256, E=8, I_s=512, shared_gate=gated)
+    T = 9
+    x = W.gen_x(s, T)
+    sh = W.gen_shared(s)
+    rng = np.random.default_rng(3)
+    ids, w = oracle.route_topk(rng.standard_normal((T, s.E)), s.k, False)
+    g = oracle.gather_by_expert(ids, s.E)
+    y_slot = rng.standard_normal((T * s.k, s.H))
+    gamma = np.array([oracle.shared_gate(x[t], sh["w_sgate"]) for t in range(T)]) if gated else None
+    shv = np.stack([oracle.swiglu_f16(x[t], sh) for t in range(T)])
+    _, ref = oracle.combine(w, y_slot.reshape(T, s.k, s.H), gamma, shv)
+    packed = spx.pack_shared(gh.dev_f16(sh["w_gate"]), gh.dev_f16(sh["w_up"]), gh.dev_f16(sh["w_down"]),
+                             gh.dev_f16(sh["w_sgate"]) if gated else None)
+    ysorted = gh.dev(y_slot[g["sorted_slots"]].astype(np.float32))
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(T, s.H)
+    for rep in range(2):
+        spx.spx_combine(ysorted, gh.dev(g["sorted_slots"]), gh.dev(w.astype(np.float32)), gh.dev_f16(x), packed,
+                        T, s.H, s.k, out, ws)
+        torch.cuda.synchronize()
+        gh.check_close(gh.f16_out(out), ref.view(np.float16).astype(np.float64), f"combine rep {rep}")
+    # without a shared expert the combine is the weighted sum alone
+    _, ref2 = oracle.combine(w, y_slot.reshape(T, s.k, s.H))
+    spx.spx_combine(ysorted, gh.dev(g["sorted_slots"]), gh.dev(w.astype(np.float32)), gh.dev_f16(x), None,
+                    T, s.H, s.k, out, ws)
+    torch.cuda.synchronize()
+    gh.check_close(gh.f16_out(out), ref2.view(np.float16).astype(np.float64), "combine no shared")
+
+
+# --------------------------------------------------------------- composite
+def _run_layer(lay, mode, x, logits, elb=None):
+    spx, gh = _spx(), _gh()
+    s = lay.shape
+    T = x.shape[0]
+    routing = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(T, s.H)
+    d_lg = gh.dev(np.asarray(logits, np.float32)) if logits is not None else torch.empty(
+        T, s.E, dtype=torch.float32, device="cuda")
+    args, keep = spx.layer_args(0 if mode == "draft" else 1, gh.dev_f16(x), s.E, s.k, s.renorm, d_lg, routing, out,
+                                ws, w4=lay.w4, f16=lay.f16, shared=lay.shared, w_router=lay.w_router, elb=elb,
+                                layer=lay.layer)
+    outs = []
+    for rep in range(2):
+        spx.spx_moe_layer(args, None)
+        torch.cuda.synchronize()
+        outs.append(gh.f16_out(out))
+    assert spx.spx_workspace_status(ws) == 0
+    return outs, routing, d_lg
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_v2_lite", "qwen15_moe", "phi35_moe"])
+@pytest.mark.parametrize("mode", ["draft", "verify"])
+def test_layer_full_size(name, mode):
+    """The five configurations' layer shapes at full size, through spx_moe_layer."""
+    gh = _gh()
+    s = W.CONFIGS[name]
+    T = s.T_draft if mode == "draft" else s.T_verify
+    if name == "tiny":
+        T = 4
+    x = W.gen_x(s, T, which=int(mode == "verify"))
+    logits = None if s.logits == "router" else W.gen_logits(s, T, which=int(mode == "verify"))
+    need = gh.needed_experts(s, [logits], [x])
+    lay = gh.Layer(s, needed=need, draft=(mode == "draft"), verify=(mode == "verify"))
+    ref = lay.oracle_layer(mode, x, logits=logits)
+    outs, routing, d_lg = _run_layer(lay, mode, x, logits)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    g = ref["gather"]
+    assert np.array_equal(routing.offsets.cpu().numpy(), g["offsets"])
+    assert np.array_equal(routing.sorted_slots.cpu().numpy(), g["sorted_slots"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{name} {mode} rep {rep}")
+
+
+def test_tiny_draft_matches_verify_on_gpu():
+    """Tiny layer: verify weights are FP16 copies of the dequantised draft
+    weights, so the two paths agree within the weights' fp16 rounding."""
+    gh = _gh()
+    s = W.CONFIGS["tiny"]
+    x = W.gen_x(s, 4)
+    lay = gh.Layer(s)
+    d, _, _ = _run_layer(lay, "draft", x, None)
+    v, _, _ = _run_layer(lay, "verify", x, None)
+    gh.check_close(v[0], d[0], "tiny draft vs verify")
+
+
+def test_layer_elb_counts_draft_steps():
+    spx, gh = _spx(), _gh()
+    s = _small("deepseek_v2_lite", I=128)
+    L = 3
+    elb = torch.zeros(L, s.E, dtype=torch.int32, device="cuda")
+    elb_ref = np.zeros((L, s.E), np.uint32)
+    lays = [gh.Layer(s, layer=l, needed=None, verify=False) for l in range(L)]
+    for step in range(1, 5):
+        for l in range(L):
+            x = W.gen_x(s, 1, layer=l, step=step)
+            lg = W.draft_logits(s, l, step)
+            ref = lays[l].oracle_layer("draft", x, logits=lg, elb=elb_ref)
+            routing = spx.Routing.empty(1, s.E, s.k)
+            out = torch.empty(1, s.H, dtype=torch.float16, device="cuda")
+            ws = spx.new_workspace(1, s.H)
+            args, keep = spx.layer_args(0, gh.dev_f16(x), s.E, s.k, s.renorm, gh.dev(lg), routing, out, ws,
+                                        w4=lays[l].w4, shared=lays[l].shared, elb=elb, layer=l)
+            spx.spx_moe_layer(args)
+            torch.cuda.synchronize()
+            gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), f"elb step {step}")
+    assert np.array_equal(elb.cpu().numpy().astype(np.uint32), elb_ref)
+    assert np.all(elb.cpu().numpy().sum(1) == 4 * s.k)
+
+
+def test_invalid_arguments_rejected():
+    spx, gh = _spx(), _gh()
+    from quantized_expert_gb300.spx import SpxError
+    ws = spx.new_workspace(4, 256)
+    lg = torch.zeros(4, 8, device="cuda")
+    ids = torch.empty(4, 9, dtype=torch.int32, device="cuda")
+    w = torch.empty(4, 9, device="cuda")
+    with pytest.raises(SpxError) as ei:
+        spx.spx_route_topk(None, None, lg, 4, 256, 8, 9, 0, ids, w, ws)   # k > E
+    assert ei.value.status == spx.SPX_ERR_INVALID_ARG
+    with pytest.raises(SpxError) as ei:
+        spx.spx_route_topk(None, None, lg, 65, 256, 8, 2, 0, ids, w, ws)  # T > 64
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
+    small_ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(4, 256, dtype=torch.float16, device="cuda")
+    y = torch.zeros(8, 256, device="cuda")
+    z = torch.zeros(9, dtype=torch.int32, device="cuda")
+    p = spx.PackedF16(torch.zeros(16, dtype=torch.uint8, device="cuda"), 8, 256, 512)
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_verify_fp16(x, p, 2, z, z, z, z, y, small_ws)
+    assert ei.value.status == spx.SPX_ERR_WORKSPACE
+    p_bad = spx.PackedF16(torch.zeros(16, dtype=torch.uint8, device="cuda"), 8, 200, 512)  # H % 128 != 0
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_verify_fp16(torch.zeros(4, 200, dtype=torch.float16, device="cuda"), p_bad, 2, z, z, z, z, y, ws)
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
