@@ -34,7 +34,7 @@ import numpy as np  # noqa: E402
 import spx_workloads as W  # noqa: E402
 
 METRIC = "MoE layer µs & achieved HBM GB/s vs GB300 peak, draft T=1 / verify T=K+1"
-NSETS = 8
+NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
 
 
@@ -279,6 +279,8 @@ def run_mine(args):
         for i in range(args.steps):
             a, b, c = ev(), ev(), ev()
             kd, kv = (ev(), ev()), (ev(), ev())
+            for e_ in kd + kv:  # create the event; libspx re-records it around the expert launch
+                e_.record(stream)
             ad, ae = step_args_timed(i, kd, kv)
             a.record(stream)
             spx.spx_moe_layer(ad, stream)
@@ -437,7 +439,9 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--config", default="deepseek_v2_lite", choices=sorted(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--sets", type=int, default=NSETS, help="rotated weight sets (8 defeat L2)")
     args = ap.parse_args()
+    globals()["NSETS"] = max(1, args.sets)
     if args.impl == "reference":
         if args.steps > 3:
             args.steps = 3

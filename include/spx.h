@@ -62,6 +62,10 @@ SPX_API const char *spx_status_string(int status);
 /* Library version as 10000*major + 100*minor + patch. */
 SPX_API int spx_version(void);
 
+/* Text of the last CUDA error this thread's calls turned into SPX_ERR_CUDA
+ * ("no error" if none); static storage, never NULL. */
+SPX_API const char *spx_last_cuda_error(void);
+
 /* ------------------------------------------------------------------------ */
 /* Router: logits, softmax, top-k   [P1 Key Contributions 2; P2 What shipped] */
 /* ------------------------------------------------------------------------ */

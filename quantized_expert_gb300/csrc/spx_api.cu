@@ -20,7 +20,13 @@ int device_sm_count() {
     return cache[dev];
 }
 
-int record_launch(cudaError_t e) { return e == cudaSuccess ? SPX_OK : SPX_ERR_CUDA; }
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int record_launch(cudaError_t e) {
+    if (e == cudaSuccess) return SPX_OK;
+    g_last_cuda_error = e;
+    return SPX_ERR_CUDA;
+}
 
 // out[t][n] = fp16( sum_j w[t][j] * y_sorted[pos(t,j)][n] + acc[t][n] ); acc -> 0
 __global__ void __launch_bounds__(256) combine_kernel(const float *y_sorted, const int32_t *sorted_slots,
@@ -79,9 +85,17 @@ extern "C" const char *spx_status_string(int st) {
 
 extern "C" int spx_version(void) { return 100; }
 
+extern "C" const char *spx_last_cuda_error(void) {
+    return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
+}
+
 extern "C" size_t spx_workspace_size(int T, int H) {
     if (T < 1 || H < 1 || T > kMaxT || H > kMaxH) return 0;
-    return ws_gamma_offset(T, H) + 256;
+    return ws_tables_offset(T, H) + (size_t)kMaxE * kTableBytes;
+}
+
+static TokTable *ws_tables(void *ws, int T, int H) {
+    return reinterpret_cast<TokTable *>(static_cast<uint8_t *>(ws) + ws_tables_offset(T, H));
 }
 
 extern "C" int spx_workspace_init(void *ws, size_t ws_bytes, spx_stream_t stream) {
@@ -98,11 +112,12 @@ extern "C" int spx_workspace_status(const void *ws, int32_t *host_status, spx_st
 
 static int check_expert_common(const uint16_t *x, int T, int H, int E, int I, int k, const int32_t *offsets,
                                const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
-                               void *ws, size_t ws_bytes) {
+                               void *ws, size_t ws_bytes, int fmt, int S) {
     if (!x || !offsets || !sorted_slots || !active || !n_active) return SPX_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || E < 1 || k > E || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
     if (T > kMaxT || E > kMaxE || T * k > kMaxSlots || H % 128 || I % 128 || H > kMaxH) return SPX_ERR_UNSUPPORTED;
-    if (!engine_fits(T, H)) return SPX_ERR_UNSUPPORTED;
+    if (fmt == 0 && S != 16 && S != 32) return SPX_ERR_UNSUPPORTED;
+    if (!engine_fits(T, H, fmt, S)) return SPX_ERR_UNSUPPORTED;
     if (!al16(x)) return SPX_ERR_INVALID_ARG;
     if (!ws || ws_bytes < spx_workspace_size(T, H) || !al16(ws)) return SPX_ERR_WORKSPACE;
     return SPX_OK;
@@ -123,9 +138,10 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
                                    const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
                                    float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
     if (!w || !w->packed || !y_sorted) return SPX_ERR_INVALID_ARG;
-    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes);
+    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes, 0,
+                                 w->slice_cols);
     if (st) return st;
-    if ((w->slice_cols != 16 && w->slice_cols != 32) || !al16(w->packed) || !al16(y_sorted)) return SPX_ERR_UNSUPPORTED;
+    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
     p.routed = static_cast<const uint8_t *>(w->packed);
@@ -136,13 +152,14 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     p.I = w->I;
     p.k = k;
     p.routed_enabled = 1;
-    p.offsets = offsets;
-    p.sorted_slots = sorted_slots;
     p.active = active;
     p.n_active = n_active;
+    p.tables = ws_tables(ws, T, w->H);
     p.mode = 0;  // sorted rows
     p.yout = y_sorted;
     if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
+    st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
+    if (st) return st;
     return launch_engine(p, s, false);
 }
 
@@ -150,9 +167,10 @@ extern "C" int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_exper
                                    const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
                                    float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
     if (!w || !w->packed || !y_sorted) return SPX_ERR_INVALID_ARG;
-    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes);
+    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes, 1,
+                                 kF16S);
     if (st) return st;
-    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_UNSUPPORTED;
+    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
     p.routed = static_cast<const uint8_t *>(w->packed);
@@ -162,13 +180,14 @@ extern "C" int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_exper
     p.I = w->I;
     p.k = k;
     p.routed_enabled = 1;
-    p.offsets = offsets;
-    p.sorted_slots = sorted_slots;
     p.active = active;
     p.n_active = n_active;
+    p.tables = ws_tables(ws, T, w->H);
     p.mode = 0;
     p.yout = y_sorted;
     if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
+    st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
+    if (st) return st;
     return launch_engine(p, s, false);
 }
 
@@ -194,7 +213,7 @@ extern "C" int spx_combine(const float *y_sorted, const int32_t *sorted_slots, c
     float *acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWsAccOffset);
     if (shared) {
         if (!x || !al16(x)) return SPX_ERR_INVALID_ARG;
-        if (!engine_fits(T, H)) return SPX_ERR_UNSUPPORTED;
+        if (!engine_fits(T, H, 1, kF16S)) return SPX_ERR_UNSUPPORTED;
         EngineParams p = base_params(x, T, H, ws);
         p.routed_enabled = 0;
         p.routed_fmt = 1;
@@ -230,18 +249,18 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     int S = kF16S;
     if (a->mode == 0) {
         if (!a->w4 || !a->w4->packed || a->w4->E != E || a->w4->H != H) return SPX_ERR_INVALID_ARG;
-        if ((a->w4->slice_cols != 16 && a->w4->slice_cols != 32) || !al16(a->w4->packed)) return SPX_ERR_UNSUPPORTED;
+        if (!al16(a->w4->packed)) return SPX_ERR_INVALID_ARG;
         I = a->w4->I;
         S = a->w4->slice_cols;
         routed = static_cast<const uint8_t *>(a->w4->packed);
     } else {
         if (!a->f16 || !a->f16->packed || a->f16->E != E || a->f16->H != H) return SPX_ERR_INVALID_ARG;
-        if (!al16(a->f16->packed)) return SPX_ERR_UNSUPPORTED;
+        if (!al16(a->f16->packed)) return SPX_ERR_INVALID_ARG;
         I = a->f16->I;
         routed = static_cast<const uint8_t *>(a->f16->packed);
     }
     st = check_expert_common(a->x, T, H, E, I, k, a->offsets, a->sorted_slots, a->active, a->n_active, a->ws,
-                             a->ws_bytes);
+                             a->ws_bytes, a->mode == 0 ? 0 : 1, S);
     if (st) return st;
     st = check_shared(a->shared, H);
     if (st) return st;
@@ -266,6 +285,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     rp.sorted_slots = a->sorted_slots;
     rp.active = a->active;
     rp.n_active = a->n_active;
+    rp.tables = ws_tables(a->ws, T, H);
     rp.hdr = static_cast<WsHeader *>(a->ws);
     st = launch_route(rp, s);
     if (st) return st;
@@ -279,11 +299,9 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     p.I = I;
     p.k = k;
     p.routed_enabled = 1;
-    p.offsets = a->offsets;
-    p.sorted_slots = a->sorted_slots;
     p.active = a->active;
     p.n_active = a->n_active;
-    p.topk_w = a->topk_w;
+    p.tables = ws_tables(a->ws, T, H);
     if (a->shared) {
         p.shared = static_cast<const uint8_t *>(a->shared->packed);
         p.w_sgate = reinterpret_cast<const __half *>(a->shared->w_sgate);

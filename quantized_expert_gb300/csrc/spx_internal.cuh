@@ -34,23 +34,19 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 constexpr size_t kWsAccOffset = 256;
 
-__host__ __device__ inline size_t ws_acc_bytes(int T, int H) {
-    return ((size_t)T * H * 4 + 255) / 256 * 256;
-}
-__host__ __device__ inline size_t ws_gamma_offset(int T, int H) { return kWsAccOffset + ws_acc_bytes(T, H); }
 
 // ----------------------------------------------------- packed geometry ---
 // INT4 unit (S = 16*MS columns of I):
-//   [gu scales: (H/128) x 2S fp16, gate cols then up cols]
-//   [gu codes : (H/16)/KB blocks of 512 B, KB = 2/MS k-steps per block;
-//               block = 32 lanes x 16 B, lane's 4 words = [ks_in][tile]]
-//   [down codes: (H/16)/MB blocks of 512 B, MB = 4/MS m-tiles per block;
-//               lane's 4 words = [tile_in][ks]]
+//   [gate/up: H/128 groups; group = 2S fp16 scales (gate cols, then up cols)
+//             followed by the group's 8 k-steps of codes as 512 B blocks of
+//             KB = 2/MS k-steps (32 lanes x 16 B; a lane's 4 words = [ks][tile])]
+//   [down   : (H/16)/MB blocks of 512 B, MB = 4/MS m-tiles per block
+//             (a lane's 4 words = [tile][ks])]
 // then after all units: down scales [E][I/128][H] fp16 (canonical).
-__host__ __device__ inline size_t w4_unit_bytes(int H, int S) { return (size_t)49 * H * S / 32; }
-__host__ __device__ inline size_t w4_sc_bytes(int H, int S) { return (size_t)(H / 128) * 2 * S * 2; }
-__host__ __device__ inline size_t w4_gu_bytes(int H, int S) { return (size_t)H * S; }
+__host__ __device__ inline size_t w4_group_bytes(int S) { return (size_t)132 * S; }
+__host__ __device__ inline size_t w4_gu_bytes(int H, int S) { return (size_t)(H / 128) * w4_group_bytes(S); }
 __host__ __device__ inline size_t w4_dn_bytes(int H, int S) { return (size_t)H * S / 2; }
+__host__ __device__ inline size_t w4_unit_bytes(int H, int S) { return w4_gu_bytes(H, S) + w4_dn_bytes(H, S); }
 __host__ __device__ inline size_t w4_units_bytes(int E, int H, int I, int S) {
     return (size_t)E * (I / S) * w4_unit_bytes(H, S);
 }
@@ -60,6 +56,25 @@ __host__ __device__ inline size_t w4_units_bytes(int E, int H, int I, int S) {
 constexpr int kF16S = 16;
 __host__ __device__ inline size_t f16_unit_bytes(int H) { return (size_t)6 * H * kF16S; }
 __host__ __device__ inline size_t f16_gu_bytes(int H) { return (size_t)4 * H * kF16S; }
+
+// Per-expert token table (workspace), written by the routing launch or by the
+// table launch of the unit calls, bulk-copied next to the expert's first chunk.
+struct TokEntry {
+    int32_t tok;    // row of x
+    int32_t row;    // output row (token, or sorted position)
+    float scale;    // output scale (gate weight, or 1)
+    int32_t pad;
+};
+struct TokTable {
+    int32_t n;
+    int32_t pad[3];
+    TokEntry e[kMaxT];
+};
+constexpr size_t kTableBytes = sizeof(TokTable);  // 16 + 64*16
+static_assert(kTableBytes % 16 == 0, "table is bulk-copied");
+__host__ __device__ inline size_t ws_tables_offset(int T, int H) {
+    return kWsAccOffset + ((size_t)T * H * 4 + 255) / 256 * 256;
+}
 
 // Physical output column of row m (0..15) of down tile mt: tile pair P = mt/2
 // covers 32 columns; rows (g, g+8) of tile q land on columns 4g+2q, 4g+2q+1,
@@ -200,6 +215,7 @@ struct RouteParams {
     uint32_t *elb;  // nullable
     int layer;
     int32_t *counts, *offsets, *sorted_slots, *active, *n_active;  // all or none
+    TokTable *tables;  // nullable: per-expert token tables (row = token, scale = weight)
     WsHeader *hdr;
 };
 
@@ -211,8 +227,8 @@ struct EngineParams {
     int S;                   // routed slice width (INT4: 16/32; FP16: 16)
     int E, I, k;
     int routed_enabled;
-    const int32_t *offsets, *sorted_slots, *active, *n_active;
-    const float *topk_w;
+    const int32_t *active, *n_active;
+    const TokTable *tables;  // per expert, in the workspace
     // shared expert (FP16, S = 16), nullable
     const uint8_t *shared;
     const __half *w_sgate;
@@ -235,7 +251,10 @@ int launch_route(const RouteParams &p, cudaStream_t s);
 int route_validate(const uint16_t *x, const uint16_t *w_router, const float *logits, int T, int H, int E, int k,
                    const int32_t *ids, const float *w);
 int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl);
-int engine_fits(int T, int H);
+int engine_fits(int T, int H, int fmt, int S);
+int engine_nt(int T);
+int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int32_t *active,
+                  const int32_t *n_active, int T, int k, int E, TokTable *tables, cudaStream_t s);
 
 // -------------------------------------------------------- host helpers --
 int device_sm_count();

@@ -15,7 +15,11 @@ __device__ __forceinline__ uint32_t gptq_code(const int32_t *q, int N, int kk, i
     return (w >> (4 * (kk & 7))) & 15u;
 }
 
-// Gate/up scales: unit (e, j) section [H/128][2S]: gate columns then up columns.
+// Gate/up section: H/128 groups, each = 2S fp16 scales (gate columns then up
+// columns) followed by 8 k-steps of codes in blocks of KB = 2/MS k-steps
+// (32 lanes x 16 B; lane word w = [ki][tile], tile t < MS gate columns
+// 16t.., t >= MS up columns 16(t-MS)..; nibble j of a word is fragment
+// register (j & 3), half (j >> 2)).
 __global__ void w4_pack_scales(const uint16_t *s_gate, const uint16_t *s_up, int E, int H, int I, int S,
                                uint8_t *packed) {
     const int spe = I / S, G = H / 128;
@@ -27,17 +31,15 @@ __global__ void w4_pack_scales(const uint16_t *s_gate, const uint16_t *s_up, int
         const int e = unit / spe, j = unit % spe;
         const int i = j * S + (c2 % S);
         const uint16_t *src = c2 < S ? s_gate : s_up;
-        uint16_t *dst = reinterpret_cast<uint16_t *>(packed + unit * w4_unit_bytes(H, S));
-        dst[grp * 2 * S + c2] = src[((size_t)e * G + grp) * I + i];
+        uint16_t *dst = reinterpret_cast<uint16_t *>(packed + unit * w4_unit_bytes(H, S) + grp * w4_group_bytes(S));
+        dst[c2] = src[((size_t)e * G + grp) * I + i];
     }
 }
 
-// Gate/up codes: block b holds KB = 2/MS k-steps; lane word w = [ki][tile],
-// tile t < MS gate columns 16t.., t >= MS up columns 16(t-MS)..; nibble j of a
-// word is fragment register (j & 3), half (j >> 2).
 __global__ void w4_pack_gu(const int32_t *qg, const int32_t *qu, int E, int H, int I, int S, uint8_t *packed) {
     const int MS = S / 16, KB = 2 / MS, NTILE = 2 * MS, spe = I / S;
-    const int nblk = (H / 16) / KB;
+    const int nblk = (H / 16) / KB;  // blocks per unit
+    const int bpg = 8 / KB;          // blocks per group
     const size_t total = (size_t)E * spe * nblk * 32 * 4;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
         const int wi = idx & 3;
@@ -55,8 +57,9 @@ __global__ void w4_pack_gu(const int32_t *qg, const int32_t *qu, int E, int H, i
             const int m = frag_row(lane, r), kc = frag_col(lane, r, hh);
             word |= gptq_code(q, I, 16 * ks + kc, icol0 + m) << (4 * nib);
         }
-        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * w4_unit_bytes(H, S) + w4_sc_bytes(H, S));
-        dst[(size_t)b * 128 + lane * 4 + wi] = word;
+        const int grp = b / bpg, ib = b % bpg;
+        uint8_t *gbase = packed + unit * w4_unit_bytes(H, S) + grp * w4_group_bytes(S) + 4 * S;
+        reinterpret_cast<uint32_t *>(gbase + ib * 512)[lane * 4 + wi] = word;
     }
 }
 
@@ -81,8 +84,7 @@ __global__ void w4_pack_down(const int32_t *qd, int E, int H, int I, int S, uint
             const int m = frag_row(lane, r), kc = frag_col(lane, r, hh);
             word |= gptq_code(q, H, jsl * S + 16 * ks + kc, down_col(mt, m)) << (4 * nib);
         }
-        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * w4_unit_bytes(H, S) + w4_sc_bytes(H, S) +
-                                                     w4_gu_bytes(H, S));
+        uint32_t *dst = reinterpret_cast<uint32_t *>(packed + unit * w4_unit_bytes(H, S) + w4_gu_bytes(H, S));
         dst[(size_t)b * 128 + lane * 4 + wi] = word;
     }
 }

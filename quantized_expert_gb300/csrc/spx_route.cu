@@ -66,7 +66,8 @@ __device__ void router_rows(const RouteParams &p) {
 // Counting sort of the T*k slots held in s_ids (shared) into the caller's
 // gather arrays.  Whole block participates.
 __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts, int32_t *offsets,
-                             int32_t *sorted_slots, int32_t *active, int32_t *n_active) {
+                             int32_t *sorted_slots, int32_t *active, int32_t *n_active, int k = 1,
+                             const float *s_w = nullptr, TokTable *tables = nullptr) {
     __shared__ int s_cnt[kMaxE];
     __shared__ int s_off[kMaxE + 1];
     __shared__ int s_act[kMaxE];
@@ -128,7 +129,19 @@ __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts
         int rank = 0;
         for (int s2 = 0; s2 < s; ++s2) rank += (s_ids[s2] == e);
         sorted_slots[s_off[e] + rank] = s;
+        if (tables) {
+            // token table of expert e, entry rank: token s/k, output row s/k, gate weight
+            TokEntry te;
+            te.tok = s / k;
+            te.row = s / k;
+            te.scale = s_w[s];
+            te.pad = 0;
+            tables[e].e[rank] = te;
+        }
     }
+    if (tables)
+        for (int e = tid; e < E; e += blockDim.x)
+            if (s_cnt[e] > 0) tables[e].n = s_cnt[e];
 }
 
 // Softmax, top-k, weights, counters and gather; one block.
@@ -194,12 +207,16 @@ __device__ void select_block(const RouteParams &p) {
             }
         }
         if (lane == 0)
-            for (int r = 0; r < p.k; ++r)
-                p.topk_w[(size_t)t * p.k + r] = p.renorm ? s_pw[t * p.k + r] / psel : s_pw[t * p.k + r];
+            for (int r = 0; r < p.k; ++r) {
+                const float wr = p.renorm ? s_pw[t * p.k + r] / psel : s_pw[t * p.k + r];
+                s_pw[t * p.k + r] = wr;
+                p.topk_w[(size_t)t * p.k + r] = wr;
+            }
     }
     __syncthreads();
     if (p.counts)
-        gather_block(s_ids, p.T * p.k, p.E, p.counts, p.offsets, p.sorted_slots, p.active, p.n_active);
+        gather_block(s_ids, p.T * p.k, p.E, p.counts, p.offsets, p.sorted_slots, p.active, p.n_active, p.k, s_pw,
+                     p.tables);
 }
 
 __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {

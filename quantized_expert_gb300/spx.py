@@ -53,6 +53,7 @@ class LayerArgs(C.Structure):
 _SIGS = {
     "spx_status_string": (C.c_char_p, [C.c_int]),
     "spx_version": (C.c_int, []),
+    "spx_last_cuda_error": (C.c_char_p, []),
     "spx_route_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                  C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_elb_accumulate": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
@@ -108,6 +109,8 @@ def status_string(st: int) -> str:
 
 def _chk(st: int, what: str):
     if st != SPX_OK:
+        if st == SPX_ERR_CUDA:
+            what = f"{what} [{load().spx_last_cuda_error().decode()}]"
         raise SpxError(st, what)
 
 

@@ -141,8 +141,8 @@ SMALL_CASES = [
     (_small("deepseek_v2_lite", I=256, E=16), 17, 32),
     (_small("qwen15_moe", I=384, E=12, I_s=512), 9, 16),
     (_small("phi35_moe", H=1024, I=512), 17, 16),
-    (_small("phi35_moe", H=1024, I=512, k=2), 33, 32),   # > 24 tokens: second token block
-    (_small("deepseek_v2_lite", H=256, I=128, E=8, k=8), 64, 32),  # k = E, maximum T
+    (_small("phi35_moe", H=1024, I=512, k=2), 33, 16),   # > 24 tokens: 64-token kernel
+    (_small("deepseek_v2_lite", H=256, I=128, E=8, k=8), 64, 16),  # k = E, maximum T
 ]
 
 
@@ -173,6 +173,23 @@ def test_draft_and_verify_unit_calls(case):
             torch.cuda.synchronize()
             gh.check_close(y.cpu().numpy(), y_ref, f"{mode} case {case} rep {rep}")
         assert spx.spx_workspace_status(ws) == 0
+
+
+def test_draft_wide_slices_reject_many_tokens():
+    """INT4 slices of 32 columns serve at most 24 tokens per expert; more is an
+    explicit SPX_ERR_UNSUPPORTED (pack with slice_cols=16 for such batches)."""
+    spx, gh = _spx(), _gh()
+    from quantized_expert_gb300.spx import SpxError
+    s = _small("phi35_moe", H=256, I=256, E=4, k=2)
+    T = 25
+    ids = np.array([[0, 1]] * T, np.int32)
+    lay = gh.Layer(s, needed=[0, 1], verify=False, slice_cols=32)
+    g, r = _routing_dev(ids, s.E)
+    y = torch.empty(T * s.k, s.H, device="cuda")
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_draft_w4a16(gh.dev_f16(W.gen_x(s, T)), lay.w4, s.k, r["offsets"], r["sorted_slots"],
+                                r["active"], r["n_active"], y, spx.new_workspace(T, s.H))
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("gated", [False, True])
