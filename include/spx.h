@@ -253,6 +253,23 @@ typedef struct {
  * then every active expert's units, and writes out[] from its last block. */
 SPX_API int spx_moe_layer(const spx_layer_args *args, spx_stream_t stream);
 
+/* The same layer for callers that cannot allocate device memory (code running
+ * inside an allocator or pool callback, runtimes that forbid device allocation
+ * after start-up, hosts that must not wait on the allocator).  The paper has no
+ * counterpart; it is a deployment convenience of this library.
+ * args->ws and args->ws_bytes are ignored: the scratch is a fixed 1 MiB array
+ * inside the library image, present on every GPU that loads the library until
+ * the process exits.  Shapes whose spx_workspace_size(T, H) exceeds 1 MiB are
+ * rejected with SPX_ERR_WORKSPACE (T*H up to about 195,000: T = 17 at H = 4096,
+ * T = 64 at H = 2048).  The call itself allocates nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array: the call clears the part that must
+ * start at zero, and calls that can overlap on the GPU (two streams, two host
+ * threads) race on it.  The device-side status word is cleared by each call and
+ * is not reported. */
+SPX_API int spx_moe_layer_noalloc(const spx_layer_args *args, spx_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,66 @@
+// spx_noalloc.cu -- the composite layer call for callers that cannot allocate
+// device memory.
+//
+// Some callers of this library cannot call cudaMalloc at the point where they
+// run a layer: code that runs inside a custom allocator or a memory-pool
+// callback, embedded runtimes that forbid device allocation after start-up,
+// or hosts that must never block on the allocator's device-wide
+// synchronisation.  They cannot provide the workspace that spx_moe_layer asks
+// for.  spx_moe_layer_noalloc runs the same layer with its scratch (queue
+// counter, completion ticket, status word, fp32 accumulator, token tables) in
+// a fixed array that is part of the library image on every GPU that loads it.
+#include "spx_internal.cuh"
+
+#include <mutex>
+
+namespace spx {
+
+// Scratch of spx_moe_layer_noalloc: 1 MiB, held by every GPU that loads the
+// library until the process exits.  Enough for spx_workspace_size(T, H) <= 1 MiB,
+// i.e. T*H up to about 195,000 (T = 17 at H = 4096, T = 64 at H = 2048).
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mutex;
+static void *g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array on the current device.  The host-side
+// name g_noalloc_scratch is only a stand-in for the symbol and must never be
+// passed to a kernel; the address comes from cudaGetSymbolAddress, looked up
+// once per device with that device current.
+static int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return record_launch(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SPX_OK;
+}
+
+}  // namespace spx
+
+using namespace spx;
+
+extern "C" int spx_moe_layer_noalloc(const spx_layer_args *args, spx_stream_t stream) {
+    if (!args) return SPX_ERR_INVALID_ARG;
+    const size_t need = spx_workspace_size(args->T, args->H);
+    if (need == 0) return SPX_ERR_UNSUPPORTED;
+    if (need > kNoAllocScratchBytes) return SPX_ERR_WORKSPACE;  // T*H beyond the fixed scratch
+    void *scratch = nullptr;
+    int st = noalloc_scratch(&scratch);
+    if (st) return st;
+    // The array keeps the previous call's contents: clear the header (queue
+    // counter, tickets, status) and the accumulator, which must start at zero.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, ws_tables_offset(args->T, args->H), s);
+    if (e != cudaSuccess) return record_launch(e);
+    spx_layer_args a = *args;
+    a.ws = scratch;
+    a.ws_bytes = kNoAllocScratchBytes;
+    return spx_moe_layer(&a, stream);
+}

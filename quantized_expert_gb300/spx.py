@@ -75,6 +75,7 @@ _SIGS = {
     "spx_combine": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(Shared), C.c_int, C.c_int,
                               C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_moe_layer": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
+    "spx_moe_layer_noalloc": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
 }
 
 
@@ -327,3 +328,9 @@ def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: Pac
 
 def spx_moe_layer(args: LayerArgs, stream=None):
     _chk(load().spx_moe_layer(C.byref(args), _stream(stream)), "spx_moe_layer")
+
+
+def spx_moe_layer_noalloc(args: LayerArgs, stream=None):
+    """The same layer with the library's fixed scratch instead of args.ws (for
+    callers that cannot allocate device memory); see include/spx.h."""
+    _chk(load().spx_moe_layer_noalloc(C.byref(args), _stream(stream)), "spx_moe_layer_noalloc")
