@@ -12,7 +12,10 @@
 //    routing, so it is queued first.
 //
 // GB300 design.  Persistent grid, one block per SM, each block = 8 consumer
-// warps + 1 producer warp.  Work is a dynamic queue of "units": one unit = one
+// warps + 1 producer warp.  The consumer warps form one or two groups; each
+// group has its own ring of stages and processes its own units, so one group's
+// gate/up -> down boundary (cross-warp reduction, SiLU) overlaps the other
+// group's streaming.  Work is a dynamic queue of "units": one unit = one
 // expert's slice of S intermediate columns, so the gate/up reduction over H
 // and the SiLU stay inside one block, and the down projection's partial sums
 // over slices are added into fp32 outputs with vector atomics (no grid-wide
@@ -57,15 +60,19 @@ struct SmemLayout {
     int red_rs;     // floats per red row
 };
 
-// red: per consumer warp, [2*smax][npad] fp32 partial sums of gate/up.
-__host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int nstages) {
+// G groups of 8/G consumer warps; nsg stages per group.
+// red: per group, per warp, [2*smax][npad] fp32 partial sums of gate/up;
+// hs : per group, [npad][kHsStride] fp16 intermediate; sd: per group, 2 x [H]
+// fp16 down-scale rows (INT4 only, double-buffered by unit parity).
+__host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg) {
     SmemLayout L;
+    const int nst = G * nsg;
     int o = 0;
     L.bars = o;
-    o += (2 * nstages + 1) * 8;
+    o += (2 * nst + G + 1) * 8;
     o = (o + 15) & ~15;
     L.hdrs = o;
-    o += nstages * (int)sizeof(ChunkHeader);
+    o += nst * (int)sizeof(ChunkHeader);
     L.gamma = o;
     o += kMaxT * 4;
     L.misc = o;
@@ -74,25 +81,37 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     L.red_rs = npad;
     o += kConsumerWarps * 2 * smax * npad * 4;
     L.hs = o;
-    o += npad * kHsStride * 2;
+    o += G * npad * kHsStride * 2;
     o = (o + 15) & ~15;
     L.sd = o;
-    if (w4) o += H * 2;
+    if (w4) o += G * 2 * H * 2;
     o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
     o += T * (H + 8) * 2;
     o = (o + 127) & ~127;
     L.ring = o;
-    o += nstages * kStageBytes;
+    o += nst * kStageBytes;
     L.total = o;
     return L;
 }
 
 // ------------------------------------------------------------- producer --
-__device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLayout &L) {
+// One lane feeds every group's ring.  Each group has its own unit stream:
+// units come from the block's share of the global dynamic queue (one unit is
+// dequeued ahead per group so its latency overlaps the copies), and chunks are
+// issued into whichever group's ring has a free stage.
+struct Stream {
+    int u, e, fmt, phase, b;
+    int next_u, next_e;
+    uint32_t it;
+    bool done;
+    const uint8_t *base;
+};
+
+__device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLayout &L, int G, int nsg) {
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.nstages;
+    uint64_t *empty = full + G * nsg;
     ChunkHeader *hdrs = reinterpret_cast<ChunkHeader *>(smem + L.hdrs);
     uint8_t *ring = smem + L.ring;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
@@ -101,27 +120,6 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     const int H = p.H;
     const int spe = p.I / p.S;
     int n_total = -1;
-    uint32_t it = 0;
-
-    // one stage: header, optional token table into the meta area, data
-    auto emit = [&](const ChunkHeader &h, const uint8_t *src, uint32_t bytes, const void *meta,
-                    uint32_t meta_bytes) -> bool {
-        const int st = it % p.nstages;
-        const uint32_t round = it / p.nstages;
-        if (!mbar_wait_bounded(&empty[st], (round & 1) ^ 1, abort_flag, &p.hdr->status, p.wait_budget_ns))
-            return false;
-        hdrs[st] = h;
-        uint8_t *dst = ring + (size_t)st * kStageBytes;
-        if (bytes + meta_bytes) {
-            mbar_arrive_expect_tx(&full[st], bytes + meta_bytes);
-            if (bytes) bulk_g2s(dst, src, bytes, &full[st], pol);
-            if (meta_bytes) bulk_g2s(dst + kChunk, meta, meta_bytes, &full[st], pol);
-        } else {
-            mbar_arrive(&full[st]);
-        }
-        ++it;
-        return true;
-    };
 
     auto total_units = [&]() -> int {
         if (n_total < 0) {
@@ -136,123 +134,165 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         }
         return n_total;
     };
-    // expert of a routed unit (global load, issued one unit ahead)
-    auto expert_of = [&](int u) -> int {
-        const int a = (u - n_sh) / spe;
-        return a < p.E ? __ldcg(p.active + a) : -1;
-    };
-
-    int u = (int)atomicAdd(&p.hdr->work_counter, 1u);
-    int e_cur = -1;
-    if (u >= n_sh && u < total_units()) e_cur = expert_of(u);
-    bool ok = true;
-    while (ok) {
-        if (u >= n_sh && u >= total_units()) break;
-        // dequeue the next unit now so its latency overlaps this unit's copies
-        const int u_next = (int)atomicAdd(&p.hdr->work_counter, 1u);
-        int e_next = -1;
-        if (u_next >= n_sh && u_next < total_units()) e_next = expert_of(u_next);
-
-        ChunkHeader h;
-        h.unit = u;
-        h.shared = u < n_sh;
-        bool valid = true;
-        const uint8_t *base;
-        const void *meta = nullptr;
-        uint32_t meta_bytes = 0;
-        int fmt;
-        if (h.shared) {
-            fmt = FMT_F16;
-            h.e = 0;
-            h.i0 = u * kF16S;
-            base = p.shared + (size_t)u * f16_unit_bytes(H);
-        } else {
-            const int j = (u - n_sh) % spe;
-            h.e = e_cur;
-            h.i0 = j * p.S;
-            valid = e_cur >= 0 && e_cur < p.E;
-            fmt = p.routed_fmt;
-            const size_t ub = fmt == FMT_W4 ? w4_unit_bytes(H, p.S) : f16_unit_bytes(H);
-            base = p.routed + ((size_t)(valid ? e_cur : 0) * spe + j) * ub;
-            meta = p.tables + (valid ? e_cur : 0);
-            meta_bytes = (uint32_t)(16 + 16 * p.T);  // table header + up to T entries
+    // dequeue one unit; e = its expert (routed units; global load issued now)
+    auto dequeue = [&](int &u, int &e) {
+        u = (int)atomicAdd(&p.hdr->work_counter, 1u);
+        e = -1;
+        if (u >= n_sh && u < total_units()) {
+            const int a = (u - n_sh) / spe;
+            e = a < p.E ? __ldcg(p.active + a) : -1;
         }
-        if (valid) {
-            if (fmt == FMT_W4) {
-                const int S = p.S;
-                const uint32_t gb = (uint32_t)w4_group_bytes(S);
-                const int ngr = H / 128;
-                const int gpc = kChunk / gb;  // whole groups per chunk
-                for (int b = 0; ok && b < ngr; b += gpc) {
-                    h.kind = HK_GU;
-                    h.b0 = b;
-                    h.nb = min(gpc, ngr - b);
-                    h.flags = (b == 0 ? HF_UNIT_START : 0) | (b + h.nb == ngr ? HF_GU_LAST : 0);
-                    ok = emit(h, base + (size_t)b * gb, h.nb * gb, b == 0 ? meta : nullptr, b == 0 ? meta_bytes : 0);
+    };
+    auto valid_unit = [&](int u) -> bool { return u < n_sh || u < total_units(); };
+
+    Stream s[2];
+    for (int g = 0; g < G; ++g) {
+        s[g].u = -1;
+        s[g].it = 0;
+        s[g].done = false;
+        dequeue(s[g].next_u, s[g].next_e);
+    }
+    const int W4GPC = kChunk / (int)w4_group_bytes(p.S);  // whole INT4 groups per chunk
+    long long t_prog = clock64();
+    const long long budget = (long long)p.wait_budget_ns * 2;  // cycles at ~2 GHz
+    bool aborted = false;
+    while (true) {
+        bool all_done = true, progressed = false;
+        for (int g = 0; g < G; ++g) {
+            Stream &S_ = s[g];
+            if (S_.done) continue;
+            all_done = false;
+            const int st = g * nsg + (int)(S_.it % nsg);
+            if (!mbar_try_wait(&empty[st], ((S_.it / nsg) & 1) ^ 1)) continue;
+            ChunkHeader h;
+            const uint8_t *src = nullptr;
+            uint32_t bytes = 0, meta_bytes = 0;
+            const void *meta = nullptr;
+            if (S_.u < 0) {
+                const int u = S_.next_u, e = S_.next_e;
+                if (!valid_unit(u)) {
+                    h = ChunkHeader{};
+                    h.kind = HK_DONE;
+                    hdrs[st] = h;
+                    mbar_arrive(&full[st]);
+                    S_.it++;
+                    S_.done = true;
+                    progressed = true;
+                    continue;
                 }
-                const uint8_t *dn = base + w4_gu_bytes(H, S);
-                const int nbd = (int)(w4_dn_bytes(H, S) / 512);
-                for (int b = 0; ok && b < nbd; b += kChunk / 512) {
-                    h.kind = HK_DOWN;
-                    h.b0 = b;
-                    h.nb = min(kChunk / 512, nbd - b);
-                    h.flags = 0;
-                    ok = emit(h, dn + (size_t)b * 512, h.nb * 512, nullptr, 0);
-                }
-            } else {
-                const int nbg = H / 16;  // one k-step (1 KB) per block
-                for (int b = 0; ok && b < nbg; b += kChunk / 1024) {
-                    h.kind = HK_GU;
-                    h.b0 = b;
-                    h.nb = min(kChunk / 1024, nbg - b);
-                    h.flags = (b == 0 ? HF_UNIT_START : 0) | (b + h.nb == nbg ? HF_GU_LAST : 0);
-                    ok = emit(h, base + (size_t)b * 1024, h.nb * 1024, b == 0 ? meta : nullptr,
-                              b == 0 ? meta_bytes : 0);
-                }
-                const uint8_t *dn = base + f16_gu_bytes(H);
-                const int nbd = H / 32;  // one m-tile pair (1 KB) per block
-                for (int b = 0; ok && b < nbd; b += kChunk / 1024) {
-                    h.kind = HK_DOWN;
-                    h.b0 = b;
-                    h.nb = min(kChunk / 1024, nbd - b);
-                    h.flags = 0;
-                    ok = emit(h, dn + (size_t)b * 1024, h.nb * 1024, nullptr, 0);
+                dequeue(S_.next_u, S_.next_e);
+                if (u >= n_sh && (e < 0 || e >= p.E)) continue;  // unusable routing entry: skip the unit
+                S_.u = u;
+                S_.e = u < n_sh ? 0 : e;
+                S_.fmt = u < n_sh ? FMT_F16 : p.routed_fmt;
+                S_.phase = 0;
+                S_.b = 0;
+                if (u < n_sh) {
+                    S_.base = p.shared + (size_t)u * f16_unit_bytes(H);
+                } else {
+                    const int j = (u - n_sh) % spe;
+                    const size_t ub = S_.fmt == FMT_W4 ? w4_unit_bytes(H, p.S) : f16_unit_bytes(H);
+                    S_.base = p.routed + ((size_t)e * spe + j) * ub;
                 }
             }
+            const bool shared = S_.u < n_sh;
+            h.unit = S_.u;
+            h.shared = shared;
+            h.e = S_.e;
+            h.i0 = shared ? S_.u * kF16S : ((S_.u - n_sh) % spe) * p.S;
+            h.flags = 0;
+            if (S_.fmt == FMT_W4) {
+                const int S = p.S;
+                const int ngr = H / 128;
+                const int nbd = (int)(w4_dn_bytes(H, S) / 512);
+                if (S_.phase == 0) {
+                    h.kind = HK_GU;
+                    h.b0 = S_.b;
+                    h.nb = min(W4GPC, ngr - S_.b);
+                    h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == ngr ? HF_GU_LAST : 0);
+                    src = S_.base + (size_t)S_.b * w4_group_bytes(S);
+                    bytes = h.nb * (uint32_t)w4_group_bytes(S);
+                    S_.b += h.nb;
+                    if (S_.b >= ngr) S_.phase = 1, S_.b = 0;
+                } else {
+                    h.kind = HK_DOWN;
+                    h.b0 = S_.b;
+                    h.nb = min(kChunk / 512, nbd - S_.b);
+                    src = S_.base + w4_gu_bytes(H, S) + (size_t)S_.b * 512;
+                    bytes = h.nb * 512;
+                    S_.b += h.nb;
+                    if (S_.b >= nbd) S_.u = -1;
+                }
+            } else {
+                const int nbg = H / 16, nbd = H / 32;
+                if (S_.phase == 0) {
+                    h.kind = HK_GU;
+                    h.b0 = S_.b;
+                    h.nb = min(kChunk / 1024, nbg - S_.b);
+                    h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == nbg ? HF_GU_LAST : 0);
+                    src = S_.base + (size_t)S_.b * 1024;
+                    bytes = h.nb * 1024;
+                    S_.b += h.nb;
+                    if (S_.b >= nbg) S_.phase = 1, S_.b = 0;
+                } else {
+                    h.kind = HK_DOWN;
+                    h.b0 = S_.b;
+                    h.nb = min(kChunk / 1024, nbd - S_.b);
+                    src = S_.base + f16_gu_bytes(H) + (size_t)S_.b * 1024;
+                    bytes = h.nb * 1024;
+                    S_.b += h.nb;
+                    if (S_.b >= nbd) S_.u = -1;
+                }
+            }
+            if ((h.flags & HF_UNIT_START) && !shared) {
+                meta = p.tables + h.e;
+                meta_bytes = (uint32_t)(16 + 16 * p.T);  // table header + up to T entries
+            }
+            hdrs[st] = h;
+            uint8_t *dst = ring + (size_t)st * kStageBytes;
+            mbar_arrive_expect_tx(&full[st], bytes + meta_bytes);
+            bulk_g2s(dst, src, bytes, &full[st], pol);
+            if (meta_bytes) bulk_g2s(dst + kChunk, meta, meta_bytes, &full[st], pol);
+            S_.it++;
+            progressed = true;
         }
-        u = u_next;
-        e_cur = e_next;
-    }
-    if (ok) {
-        ChunkHeader h{};
-        h.kind = HK_DONE;
-        emit(h, nullptr, 0, nullptr, 0);
+        if (all_done) break;
+        if (progressed) {
+            t_prog = clock64();
+        } else if (*abort_flag || clock64() - t_prog > budget) {
+            atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            *abort_flag = 1;
+            aborted = true;
+            break;
+        }
     }
     // Drain: every issued copy has been waited on by the consumers unless the
     // block aborted; in that case wait (bounded) for the copies in flight.
-    if (*abort_flag) {
-        const uint32_t first = it > (uint32_t)p.nstages ? it - p.nstages : 0;
-        for (uint32_t j = first; j < it; ++j) {
-            const int st = j % p.nstages;
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(&full[st], (j / p.nstages) & 1) && global_timer_ns() - t0 < 100000000ull) {
+    if (aborted) {
+        for (int g = 0; g < G; ++g) {
+            const uint32_t first = s[g].it > (uint32_t)nsg ? s[g].it - nsg : 0;
+            for (uint32_t j = first; j < s[g].it; ++j) {
+                const int st = g * nsg + (int)(j % nsg);
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&full[st], (j / nsg) & 1) && global_timer_ns() - t0 < 100000000ull) {
+                }
             }
         }
     }
 }
 
 // ------------------------------------------------------------ consumers --
-struct Cons {
-    uint64_t *csync;
-    volatile int *abort_flag;
-    uint32_t csync_phase;
+struct Sync {
+    uint64_t *bar;
+    uint32_t phase;
 };
 
-__device__ __forceinline__ void cons_sync(const EngineParams &p, Cons &c) {
+// All warps that share `bar` (initialised with their count) meet here.
+__device__ __forceinline__ void group_sync(const EngineParams &p, Sync &sy, volatile int *abort_flag) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(c.csync);
-    mbar_wait_bounded(c.csync, c.csync_phase & 1, c.abort_flag, &p.hdr->status, p.wait_budget_ns);
-    c.csync_phase ^= 1;
+    if ((threadIdx.x & 31) == 0) mbar_arrive(sy.bar);
+    mbar_wait_bounded(sy.bar, sy.phase & 1, abort_flag, &p.hdr->status, p.wait_budget_ns);
+    sy.phase ^= 1;
     __syncwarp();
 }
 
@@ -264,41 +304,45 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     extern __shared__ __align__(128) uint8_t smem[];
     const bool has_w4 = RFMT == FMT_W4 && p.routed_enabled;
     const int smax = has_w4 ? p.S : kF16S;
-    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, p.nstages);
+    const int G = p.groups, nsg = p.nstages;
+    const int gwarps = kConsumerWarps / G;
+    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.nstages;
-    uint64_t *csync = empty + p.nstages;
+    uint64_t *empty = full + G * nsg;
+    uint64_t *gbar = empty + G * nsg;  // one per group
+    uint64_t *allbar = gbar + G;       // all consumer warps
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.nstages; ++s) {
+        for (int s = 0; s < G * nsg; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], gwarps);
         }
-        mbar_init(csync, kConsumerWarps);
+        for (int q = 0; q < G; ++q) mbar_init(&gbar[q], gwarps);
+        mbar_init(allbar, kConsumerWarps);
         misc[0] = 0;  // abort flag
         misc[1] = 0;  // last-block flag
         fence_mbar_init();
     }
     __syncthreads();
     if (warp == kConsumerWarps) {
-        if (lane == 0) producer_loop(p, smem, L);
+        if (lane == 0) producer_loop(p, smem, L, G, nsg);
         return;
     }
-
-    Cons c;
-    c.csync = csync;
-    c.abort_flag = reinterpret_cast<volatile int *>(misc);
-    c.csync_phase = 0;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
+    const int grp_id = warp / gwarps, gw = warp % gwarps;
+    const int gtid = gw * 32 + lane;  // thread index within the group
+    Sync gs{&gbar[grp_id], 0};
+    Sync as{allbar, 0};
     const ChunkHeader *hdrs = reinterpret_cast<const ChunkHeader *>(smem + L.hdrs);
     const uint8_t *ring = smem + L.ring;
     float *gamma = reinterpret_cast<float *>(smem + L.gamma);
-    float *red = reinterpret_cast<float *>(smem + L.red);
-    __half *hs = reinterpret_cast<__half *>(smem + L.hs);
-    __half *sdm = reinterpret_cast<__half *>(smem + L.sd);
-    __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int xs_stride = L.xs_stride, rs = L.red_rs, npad = p.npad;
+    float *red = reinterpret_cast<float *>(smem + L.red) + (size_t)grp_id * gwarps * 2 * smax * rs;
+    __half *hs = reinterpret_cast<__half *>(smem + L.hs) + (size_t)grp_id * npad * kHsStride;
+    __half *sdg = reinterpret_cast<__half *>(smem + L.sd) + (size_t)grp_id * 2 * p.H;
+    __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int ctid = threadIdx.x;  // 0..255
     const int H = p.H;
 
@@ -308,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H) + h8);
         *reinterpret_cast<uint4 *>(xs + (size_t)t * xs_stride + h8 * 8) = v;
     }
-    cons_sync(p, c);
+    group_sync(p, as, abort_flag);
     // shared-expert gate per token: gamma = 1 / (1 + exp(-x . w_sgate)), else 1
     if (p.shared && p.w_sgate) {
         for (int t = warp; t < p.T; t += kConsumerWarps) {
@@ -326,19 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     } else {
         for (int t = ctid; t < p.T; t += kConsumerWarps * 32) gamma[t] = 1.0f;
     }
-    cons_sync(p, c);
+    group_sync(p, as, abort_flag);
 
     constexpr int NTW = 2 * MS4;  // INT4 gate+up tiles per k-step (FP16 units use 2)
     // per-warp state of the current unit
     int u_fmt = FMT_F16, u_S = kF16S, u_e = 0, u_i0 = 0, n_e = 0, nact = 0;
+    uint32_t ucount = 0;     // units started by this group (selects the down-scale buffer)
+    const __half *sdcur = sdg;
     int xoff[NT];
     int orow[NT][2];
     float oscl[NT][2];
     float run[NTW][NT][4];                // gate/up partial sums of this warp for the whole unit
     uint32_t hb0[MS4][NT], hb1[MS4][NT];  // h fragments for the down phase
-    uint4 sdv[4];                          // INT4: this thread's share of the down-scale row
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sdv[i] = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int ks = 0; ks < MS4; ++ks)
 #pragma unroll
@@ -346,9 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
 
     uint32_t it = 0;
     while (it < (1u << 30)) {
-        const int st = it % p.nstages;
-        if (!mbar_wait_bounded(&full[st], (it / p.nstages) & 1, c.abort_flag, &p.hdr->status, p.wait_budget_ns))
-            break;
+        const int st = grp_id * nsg + (int)(it % nsg);
+        if (!mbar_wait_bounded(&full[st], (it / nsg) & 1, abort_flag, &p.hdr->status, p.wait_budget_ns)) break;
         const ChunkHeader h = hdrs[st];
         if (h.kind == HK_DONE) break;
         const uint8_t *stage = ring + (size_t)st * kStageBytes;
@@ -399,16 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
 #pragma unroll
                     for (int r = 0; r < 4; ++r) run[t][nt][r] = 0.f;
             if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
-                // prefetch this unit's down-scale row; stored to shared memory
-                // at the gate/up -> down boundary
-                const uint4 *srow = reinterpret_cast<const uint4 *>(p.w4_sdown +
-                                                                    ((size_t)u_e * (p.I / 128) + u_i0 / 128) * H);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int idx = ctid + i * kConsumerWarps * 32;
-                    sdv[i] = idx < H / 8 ? __ldg(srow + idx) : make_uint4(0, 0, 0, 0);
-                }
+                // fetch this unit's down-scale row into the group's buffer for
+                // this unit's parity; waited for at the gate/up -> down boundary
+                __half *dst = sdg + (size_t)(ucount & 1) * H;
+                const __half *srow = p.w4_sdown + ((size_t)u_e * (p.I / 128) + u_i0 / 128) * H;
+                for (int idx = gtid; idx < H / 8; idx += gwarps * 32) cp_async16(dst + idx * 8, srow + idx * 8);
+                cp_async_commit();
+                sdcur = dst;
             }
+            ++ucount;
         }
         if (n_e > 0 && h.kind == HK_GU) {
             if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
@@ -417,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                 constexpr int BPG = 8 / KB;
                 const int gb = 132 * u_S;
                 const int nblk = h.nb * BPG;
-                const int per = (nblk + kConsumerWarps - 1) / kConsumerWarps;
-                const int bb = warp * per, be = min(bb + per, nblk);
+                const int per = (nblk + gwarps - 1) / gwarps;
+                const int bb = gw * per, be = min(bb + per, nblk);
                 float acc[NTW][NT][4];
                 float sA[NTW], sB[NTW];
                 int grp = -1;
@@ -487,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                 }
             } else {
                 const int nb = h.nb;
-                const int per = (nb + kConsumerWarps - 1) / kConsumerWarps;
-                const int bb = warp * per, be = min(bb + per, nb);
+                const int per = (nb + gwarps - 1) / gwarps;
+                const int bb = gw * per, be = min(bb + per, nb);
                 for (int b = bb; b < be; ++b) {
                     const int ks = h.b0 + b;
                     uint32_t bf0[NT], bf1[NT];
@@ -511,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             }
         } else if (n_e > 0 && h.kind == HK_DOWN) {
             const int nb = h.nb;
-            const int per = (nb + kConsumerWarps - 1) / kConsumerWarps;
-            const int bb = warp * per, be = min(bb + per, nb);
+            const int per = (nb + gwarps - 1) / gwarps;
+            const int bb = gw * per, be = min(bb + per, nb);
             for (int b = bb; b < be; ++b) {
                 if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
                     // block = 4/MS4 m-tiles (2/MS4 pairs), lane words [tile][ks]
@@ -528,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                             for (int ks = 0; ks < MS4; ++ks) dequant_frag(words[(2 * pr + q) * MS4 + ks], a[q][ks]);
                         const int mt0 = (h.b0 + b) * (4 / MS4) + 2 * pr;
                         const int n0 = 32 * (mt0 >> 1) + 4 * g;
-                        const uint2 sv = *reinterpret_cast<const uint2 *>(sdm + n0);
+                        const uint2 sv = *reinterpret_cast<const uint2 *>(sdcur + n0);
                         const float2 s01 = __half22float2(u32_as_h2(sv.x));
                         const float2 s23 = __half22float2(u32_as_h2(sv.y));
 #pragma unroll
@@ -597,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         if (h.flags & HF_GU_LAST) {
             // cross-warp reduction of the gate/up partial sums, SiLU, h -> fp16
             const int S = u_S;
-            float *myred = red + (size_t)warp * 2 * S * rs;
+            float *myred = red + (size_t)gw * 2 * S * rs;
 #pragma unroll
             for (int t = 0; t < NTW; ++t) {
                 if (t * 16 < 2 * S) {
@@ -614,26 +655,19 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                     }
                 }
             }
-            cons_sync(p, c);
-            if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int idx = ctid + i * kConsumerWarps * 32;
-                    if (idx < H / 8) reinterpret_cast<uint4 *>(sdm)[idx] = sdv[i];
-                }
-            }
-            for (int idx = ctid; idx < S * npad; idx += kConsumerWarps * 32) {
+            if (RFMT == FMT_W4) cp_async_wait_all();  // this thread's share of the down-scale row
+            group_sync(p, gs, abort_flag);
+            for (int idx = gtid; idx < S * npad; idx += gwarps * 32) {
                 const int i = idx / npad, col = idx - i * npad;
                 float gv = 0.f, uv = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
+                for (int w = 0; w < gwarps; ++w) {
                     gv += red[((size_t)w * 2 * S + i) * rs + col];
                     uv += red[((size_t)w * 2 * S + S + i) * rs + col];
                 }
                 const float hv = gv / (1.0f + __expf(-gv)) * uv;
                 hs[col * kHsStride + i] = __float2half_rn(col < n_e ? hv : 0.f);
             }
-            cons_sync(p, c);
+            group_sync(p, gs, abort_flag);
             const int kst = S / 16;
 #pragma unroll
             for (int ks = 0; ks < MS4; ++ks)
@@ -650,13 +684,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     }
 
     // completion ticket; the last block writes the fp16 output and resets
-    cons_sync(p, c);
+    group_sync(p, as, abort_flag);
     if (ctid == 0) {
         __threadfence();
         const uint32_t t = atomicAdd(&p.hdr->done_ticket, 1u);
         misc[1] = (t == gridDim.x - 1);
     }
-    cons_sync(p, c);
+    group_sync(p, as, abort_flag);
     if (misc[1]) {
         __threadfence();
         if (p.mode == MODE_LAYER) {
@@ -716,6 +750,21 @@ int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int
 // ------------------------------------------------------------ launching --
 int engine_nt(int T) { return T <= 8 ? 1 : (T <= 24 ? 3 : 8); }
 
+// Geometry: two consumer groups when each can get at least two stages,
+// otherwise one group; at most 12 stages in all.
+static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes) {
+    for (G = 2; G >= 1; --G) {
+        for (nsg = 12 / G; nsg >= 2; --nsg) {
+            const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg);
+            if (L.total <= kSmemLimit) {
+                bytes = L.total;
+                return true;
+            }
+        }
+    }
+    return false;
+}
+
 template <int RFMT, int MS4, int NT>
 static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     EngineParams p = p0;
@@ -723,11 +772,10 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     if (sms <= 0) return SPX_ERR_CUDA;
     const bool w4 = RFMT == FMT_W4 && p.routed_enabled;
     const int smax = w4 ? p.S : kF16S;
-    int nst = 12;
-    SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, w4, nst);
-    while (nst > 2 && L.total > kSmemLimit) L = smem_layout(p.T, p.H, p.npad, smax, w4, --nst);
-    if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
-    p.nstages = nst;
+    int G, nsg, bytes;
+    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes)) return SPX_ERR_UNSUPPORTED;
+    p.groups = G;
+    p.nstages = nsg;
     static int configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
@@ -740,7 +788,7 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L.total;
+    cfg.dynamicSmemBytes = bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -771,8 +819,8 @@ int engine_fits(int T, int H, int fmt, int S) {
     const int npad = 8 * ((T + 7) / 8);
     const bool w4 = fmt == FMT_W4;
     if (w4 && S == 32 && engine_nt(T) == 8) return 0;
-    const SmemLayout L = smem_layout(T, H, npad, w4 ? S : kF16S, w4, 2);
-    return L.total <= kSmemLimit;
+    int G, nsg, bytes;
+    return choose_geometry(T, H, npad, w4 ? S : kF16S, w4, G, nsg, bytes) ? 1 : 0;
 }
 
 }  // namespace spx

@@ -153,6 +153,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// 16-byte asynchronous global -> shared copy (completion: cp_async_wait_all
+// of the issuing thread).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -241,8 +248,9 @@ struct EngineParams {
     float *yout;   // mode 0: y_sorted; otherwise the fp32 accumulator
     __half *out;   // mode 2: final fp16 output
     WsHeader *hdr;
-    // geometry
-    int nstages;
+    // geometry (set by the launcher)
+    int groups;    // consumer warp groups (1 or 2)
+    int nstages;   // ring stages per group
     int npad;      // token columns of the shared scratch: 8 * ceil(T / 8)
     uint64_t wait_budget_ns;
 };
