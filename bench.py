@@ -193,8 +193,8 @@ def run_mine(args):
         dev_in.append(e)
     L = s.layers
     elb = torch.zeros(max(L, NSETS), s.E, dtype=torch.int32, device="cuda")
-    ws_d = spx.new_workspace(Td, s.H)
-    ws_v = spx.new_workspace(Tv, s.H)
+    ws_d = spx.new_workspace(Td, s.H, s.I, s.E, s.k, s.I_s)
+    ws_v = spx.new_workspace(Tv, s.H, s.I, s.E, s.k, s.I_s)
     r_d = spx.Routing.empty(Td, s.E, s.k)
     r_v = spx.Routing.empty(Tv, s.E, s.k)
     out_d = torch.empty(Td, s.H, dtype=torch.float16, device="cuda")

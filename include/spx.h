@@ -76,8 +76,8 @@ SPX_API const char *spx_last_cuda_error(void);
  *   index, in descending order -> topk_ids [T][k] (int32).
  * Weights: p = softmax over all E experts; topk_w[t][j] = p[id] (renorm == 0)
  *   or p[id] / sum of the k selected p (renorm != 0) -> [T][k] fp32.
- * ws: workspace of spx_workspace_size() bytes (holds the completion counter
- *   of the multi-block router product). */
+ * ws: workspace of spx_workspace_size(T, H, 0, E, k, 0) bytes or more (holds
+ *   the completion counter of the multi-block router product). */
 SPX_API int spx_route_topk(const uint16_t *x, const uint16_t *w_router, float *logits,
                    int T, int H, int E, int k, int renorm,
                    int32_t *topk_ids, float *topk_w,
@@ -131,7 +131,9 @@ SPX_API int spx_gather_by_expert(const int32_t *topk_ids, int T, int k, int E,
  * fp16 lanes at a time for the magic-exponent dequantisation.  The byte order
  * inside a unit is private to the library; only the sizes below are public.
  *   INT4: S = 16 or 32 (slice_cols); unit bytes = 49*H*S/32; then the down
- *         scales, copied unchanged ([E][I/128][H] fp16).
+ *         scales, copied unchanged ([E][I/128][H] fp16); then the down
+ *         weights once more in output-block order with their scales inline
+ *         (read by the draft launch, whose reduction over I stays in a block).
  *   FP16: S = 16; unit bytes = 6*H*S.
  */
 typedef struct {
@@ -150,13 +152,16 @@ typedef struct {
  * If w_sgate != NULL (fp16 [H]) its output is scaled per token by
  * gamma_t = 1 / (1 + exp(-x_t . w_sgate)).  [P1 Key Contributions 2] */
 typedef struct {
-    const void *packed;      /* spx_f16_packed_bytes(1, H, I_s) bytes */
+    const void *packed;      /* spx_shared_packed_bytes(H, I_s) bytes, from spx_shared_repack() */
     const uint16_t *w_sgate; /* nullable */
     int H, I_s;
 } spx_shared;
 
 SPX_API size_t spx_w4_packed_bytes(int E, int H, int I, int slice_cols);
 SPX_API size_t spx_f16_packed_bytes(int E, int H, int I);
+/* Shared expert pack: the FP16 units of one expert followed by its down
+ * weights once more in output-block order (read by the draft launch). */
+SPX_API size_t spx_shared_packed_bytes(int H, int I_s);
 
 /* Repack canonical GPTQ tensors (device memory, layouts above) into `packed`
  * (device, spx_w4_packed_bytes() bytes, 16-byte aligned).  Deterministic. */
@@ -165,6 +170,11 @@ SPX_API int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate,
                   const int32_t *qw_down, const uint16_t *s_down,
                   int E, int H, int I, int slice_cols, void *packed, spx_stream_t stream);
 
+/* Repack one canonical FP16 shared expert ([I_s][H], [I_s][H], [H][I_s]) into
+ * `packed` (device, spx_shared_packed_bytes() bytes, 16-byte aligned). */
+SPX_API int spx_shared_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
+                              int H, int I_s, void *packed, spx_stream_t stream);
+
 /* Repack canonical FP16 [out][in] tensors into `packed` (spx_f16_packed_bytes). */
 SPX_API int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
                    int E, int H, int I, void *packed, spx_stream_t stream);
@@ -172,8 +182,10 @@ SPX_API int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const u
 /* ------------------------------------------------------------------------ */
 /* Workspace                                                                  */
 /* ------------------------------------------------------------------------ */
-/* Bytes of workspace for calls with up to T tokens of hidden size H. */
-SPX_API size_t spx_workspace_size(int T, int H);
+/* Bytes of workspace for calls with up to T tokens of hidden size H, routed
+ * experts of intermediate size I (E of them, top-k) and a shared expert of
+ * intermediate size I_s (0 = none); 0 if the shape is outside the limits. */
+SPX_API size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s);
 /* Zero a workspace; required once before first use (kernels leave it zeroed
  * again on exit) and after any call whose status word reported an error. */
 SPX_API int spx_workspace_init(void *ws, size_t ws_bytes, spx_stream_t stream);
@@ -259,9 +271,9 @@ SPX_API int spx_moe_layer(const spx_layer_args *args, spx_stream_t stream);
  * counterpart; it is a deployment convenience of this library.
  * args->ws and args->ws_bytes are ignored: the scratch is a fixed 1 MiB array
  * inside the library image, present on every GPU that loads the library until
- * the process exits.  Shapes whose spx_workspace_size(T, H) exceeds 1 MiB are
- * rejected with SPX_ERR_WORKSPACE (T*H up to about 195,000: T = 17 at H = 4096,
- * T = 64 at H = 2048).  The call itself allocates nothing.
+ * the process exits.  Shapes whose spx_workspace_size(T, H, I, E, k, I_s)
+ * exceeds 1 MiB are rejected with SPX_ERR_WORKSPACE (the DeepSeek-V2-Lite-
+ * shaped layer fits at T = 1 and T = 17).  The call itself allocates nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  Every call shares the one array: the call clears the part that must

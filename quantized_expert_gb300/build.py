@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libspx.so")
-SOURCES = ["spx_route.cu", "spx_engine.cu", "spx_pack.cu", "spx_api.cu", "spx_noalloc.cu"]
+SOURCES = ["spx_route.cu", "spx_engine.cu", "spx_draft.cu", "spx_pack.cu", "spx_api.cu", "spx_noalloc.cu"]
 HEADERS = ["spx_internal.cuh", os.path.join("..", "..", "include", "spx.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

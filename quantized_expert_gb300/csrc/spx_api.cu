@@ -89,9 +89,14 @@ extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
-extern "C" size_t spx_workspace_size(int T, int H) {
-    if (T < 1 || H < 1 || T > kMaxT || H > kMaxH) return 0;
-    return ws_tables_offset(T, H) + (size_t)kMaxE * kTableBytes;
+static size_t ws_scratch_base(int T, int H) { return ws_tables_offset(T, H) + (size_t)kMaxE * kTableBytes; }
+
+extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
+    if (T < 1 || H < 1 || T > kMaxT || H > kMaxH || I < 0 || E < 1 || k < 1 || I_s < 0) return 0;
+    const size_t base = ws_scratch_base(T, H);
+    if (T > 8 || I % 128 || I_s % 16) return base;  // the split-K draft launch serves T <= 8 only
+    const int nact = E < T * k ? E : T * k;
+    return draft_scratch_end(base, T, H, I, I_s, nact);
 }
 
 static TokTable *ws_tables(void *ws, int T, int H) {
@@ -112,14 +117,14 @@ extern "C" int spx_workspace_status(const void *ws, int32_t *host_status, spx_st
 
 static int check_expert_common(const uint16_t *x, int T, int H, int E, int I, int k, const int32_t *offsets,
                                const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
-                               void *ws, size_t ws_bytes, int fmt, int S) {
+                               void *ws, size_t ws_bytes, int fmt, int S, int I_s = 0) {
     if (!x || !offsets || !sorted_slots || !active || !n_active) return SPX_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || E < 1 || k > E || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
     if (T > kMaxT || E > kMaxE || T * k > kMaxSlots || H % 128 || I % 128 || H > kMaxH) return SPX_ERR_UNSUPPORTED;
     if (fmt == 0 && S != 16 && S != 32) return SPX_ERR_UNSUPPORTED;
     if (!engine_fits(T, H, fmt, S)) return SPX_ERR_UNSUPPORTED;
     if (!al16(x)) return SPX_ERR_INVALID_ARG;
-    if (!ws || ws_bytes < spx_workspace_size(T, H) || !al16(ws)) return SPX_ERR_WORKSPACE;
+    if (!ws || ws_bytes < spx_workspace_size(T, H, I, E, k, I_s) || !al16(ws)) return SPX_ERR_WORKSPACE;
     return SPX_OK;
 }
 
@@ -160,6 +165,7 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
     st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
     if (st) return st;
+    if (draft_supported(T, w->H, w->I, w->slice_cols, 0)) return launch_draft(p, ws_scratch_base(T, w->H), false, s);
     return launch_engine(p, s, false);
 }
 
@@ -205,7 +211,7 @@ extern "C" int spx_combine(const float *y_sorted, const int32_t *sorted_slots, c
     if (!y_sorted || !sorted_slots || !topk_w || !out) return SPX_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || H < 1) return SPX_ERR_INVALID_ARG;
     if (T > kMaxT || T * k > kMaxSlots || H % 128 || H > kMaxH) return SPX_ERR_UNSUPPORTED;
-    if (!ws || ws_bytes < spx_workspace_size(T, H) || !al16(ws)) return SPX_ERR_WORKSPACE;
+    if (!ws || ws_bytes < spx_workspace_size(T, H, 0, 1, 1, 0) || !al16(ws)) return SPX_ERR_WORKSPACE;
     if (!al16(y_sorted) || (reinterpret_cast<uintptr_t>(out) & 7)) return SPX_ERR_INVALID_ARG;
     int st = check_shared(shared, H);
     if (st) return st;
@@ -259,8 +265,9 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         I = a->f16->I;
         routed = static_cast<const uint8_t *>(a->f16->packed);
     }
+    const int I_s = a->shared ? a->shared->I_s : 0;
     st = check_expert_common(a->x, T, H, E, I, k, a->offsets, a->sorted_slots, a->active, a->n_active, a->ws,
-                             a->ws_bytes, a->mode == 0 ? 0 : 1, S);
+                             a->ws_bytes, a->mode == 0 ? 0 : 1, S, I_s);
     if (st) return st;
     st = check_shared(a->shared, H);
     if (st) return st;
@@ -313,7 +320,10 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     const bool timed = a->ev_experts_begin || a->ev_experts_end;
     if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
         return SPX_ERR_CUDA;
-    st = launch_engine(p, s, !timed);
+    if (a->mode == 0 && draft_supported(T, H, I, S, I_s))
+        st = launch_draft(p, ws_scratch_base(T, H), !timed, s);
+    else
+        st = launch_engine(p, s, !timed);
     if (st) return st;
     if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
         return SPX_ERR_CUDA;

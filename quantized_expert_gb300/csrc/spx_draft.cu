@@ -1,0 +1,785 @@
+// spx_draft.cu -- the fused multi-expert INT4 draft launch (T <= 8 tokens).
+//
+// Method (ai.info summary of the Specter paper, Key Contributions 2 and 4;
+// richland.au post, "What shipped"): a draft step runs every selected INT4
+// (GPTQ, group 128) expert of a layer, plus the FP16 shared expert, in one
+// launch, dequantising the INT4 weights while multiplying them with fp16
+// activations; the expert MLP is SwiGLU, y = W_d (silu(W_g x) * (W_u x)).
+//
+// GB300 design.  At T = 1 a layer is ~60-90 MB of weights read once, ~10 us at
+// HBM speed, so balance and latency decide everything.  The work is cut into
+// ~16 KB items, each processed by ONE warp, with no block-level barriers:
+//   SG  shared gate/up   (16-column block, range of H)
+//   RG  routed gate/up   (S-column slice of an active expert, range of H)
+//   SD  shared down      (pair of output m-tiles = 32 outputs, range of I_s)
+//   RD  routed down      (32 outputs of an active expert, range of I)
+// Gate/up items add their partial sums into fp32 scratch; the warp whose item
+// completes a column block applies SiLU, writes the fp16 intermediate h in
+// mma B-fragment order and counts the block as ready.  Down items are issued
+// after every gate/up item (one global dynamic queue), their weights stream at
+// once, and the producer bulk-copies the h slice next to them as soon as the
+// slice is ready, so each output gets ~2 partial sums per expert, not one per
+// slice.  One producer warp streams items through a ring of stages (TMA bulk
+// copies + mbarriers); the 8 consumer warps take stages in order through a
+// shared-memory ticket, so a slow item never stalls the others.
+#include "spx_internal.cuh"
+
+#include <math.h>
+
+namespace spx {
+
+enum : int { DK_SG = 0, DK_RG = 1, DK_SD = 2, DK_RD = 3, DK_DONE = 4 };
+constexpr int kDkData = 16896;  // largest item: 4 INT4 groups of 32 columns (or 8 of 16)
+constexpr int kDkRdGroups = 7;  // INT4 down groups (of 128 rows of I) per RD item
+constexpr int kDkSdSteps = 16;  // k-steps of I_s per SD item
+
+struct __align__(16) DHeader {
+    int kind;
+    int a;    // active slot (routed items)
+    int e;    // expert (routed items)
+    int blk;  // SG: shared block; RG: slice; SD/RD: output pair
+    int r;    // range index
+    int k0;   // SG: first k-step of H; RG: first group of H; SD: first k-step of I_s; RD: first group of I
+    int n;    // SG/SD: k-steps; RG/RD: groups
+    int seq;  // ring sequence number of this stage fill
+};
+
+struct DkGeom {
+    int sg_cols, sg_nks, sg_nr;  // shared gate/up: blocks of 16 columns, k-steps per item, ranges
+    int sd_nr;                   // shared down ranges of kDkSdSteps k-steps
+    int rg_blocks, rg_gpi, rg_nr;
+    int rd_nr;
+};
+
+__host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s) {
+    DkGeom g;
+    g.sg_cols = I_s / 16;
+    g.sg_nks = ((H / 16) % 16 == 0) ? 16 : 8;
+    g.sg_nr = (H / 16) / g.sg_nks;
+    g.sd_nr = (I_s / 16 + kDkSdSteps - 1) / kDkSdSteps;
+    g.rg_blocks = I / S;
+    g.rg_gpi = S == 32 ? 4 : 8;
+    g.rg_nr = (H / 128 + g.rg_gpi - 1) / g.rg_gpi;
+    g.rd_nr = (I / 128 + kDkRdGroups - 1) / kDkRdGroups;
+    return g;
+}
+
+// Scratch in the workspace (after the token tables), 256-byte aligned parts.
+struct DkScratch {
+    size_t gu_s, gu_r, hf_s, hf_r, cnt_s, cnt_r, rdy_s, rdy_r, end;
+};
+__host__ __device__ inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+__host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I, int I_s, int nact_max) {
+    const DkGeom g = dk_geom(H, I, 16, I_s);
+    DkScratch s;
+    size_t o = al256(base);
+    s.gu_s = o;
+    o = al256(o + (size_t)2 * I_s * T * 4);
+    s.gu_r = o;
+    o = al256(o + (size_t)nact_max * 2 * I * T * 4);
+    s.hf_s = o;
+    o = al256(o + (size_t)(I_s / 16) * T * 32);
+    s.hf_r = o;
+    o = al256(o + (size_t)nact_max * (I / 16) * T * 32);
+    s.cnt_s = o;
+    o = al256(o + (size_t)(I_s / 16) * 4);
+    s.cnt_r = o;
+    o = al256(o + (size_t)nact_max * (I / 16) * 4);
+    s.rdy_s = o;
+    o = al256(o + (size_t)g.sd_nr * 4);
+    s.rdy_r = o;
+    o = al256(o + (size_t)nact_max * g.rd_nr * 4);
+    s.end = o;
+    return s;
+}
+
+struct DkLayout {
+    int bars, hdrs, misc, gamma, act, xs, ring, stage, hs_off, meta_off, total, xs_stride;
+};
+__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst) {
+    DkLayout L;
+    int o = 0;
+    L.bars = o;
+    o += (2 * nst + 1) * 8;
+    o = (o + 15) & ~15;
+    L.hdrs = o;
+    o += nst * (int)sizeof(DHeader);
+    L.misc = o;
+    o += 64;
+    L.gamma = o;
+    o += kMaxT * 4;
+    L.act = o;
+    o += kMaxE * 4;
+    o = (o + 15) & ~15;
+    L.xs = o;
+    L.xs_stride = H + 8;
+    o += T * (H + 8) * 2;
+    o = (o + 127) & ~127;
+    L.ring = o;
+    L.hs_off = kDkData;
+    const int hs_bytes = ((kDkRdGroups * 8 > kDkSdSteps ? kDkRdGroups * 8 : kDkSdSteps) * T * 32 + 127) & ~127;
+    L.meta_off = kDkData + hs_bytes;
+    L.stage = L.meta_off + ((16 + 16 * T + 127) & ~127);
+    o += nst * L.stage;
+    L.total = o;
+    return L;
+}
+
+struct DkParams {
+    const uint8_t *w4;      // packed INT4 experts
+    size_t w4_colblk;       // byte offset of the column-block-major down weights
+    int S;                  // INT4 slice width
+    const uint8_t *sh;      // shared pack (nullable)
+    const __half *w_sgate;  // nullable
+    int I_s;
+    int E, I, k, T, H;
+    const int32_t *active, *n_active;
+    const TokTable *tables;
+    const __half *x;
+    int mode;  // 0: rows of y_sorted, scale 1; 2: weighted into the fp32 accumulator, last block writes out
+    float *yout;
+    __half *out;
+    WsHeader *hdr;
+    float *gu_s, *gu_r;
+    uint2 *hf_s, *hf_r;
+    int *cnt_s, *cnt_r, *rdy_s, *rdy_r;
+    int nact_max, nstages;
+    uint64_t wait_budget_ns;
+};
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ void red_add(float *p, float v) { atomicAdd(p, v); }
+
+// ------------------------------------------------------------- producer --
+__device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L) {
+    const int nst = p.nstages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + nst;
+    DHeader *hdrs = reinterpret_cast<DHeader *>(smem + L.hdrs);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
+    int *act = reinterpret_cast<int *>(smem + L.act);
+    uint8_t *ring = smem + L.ring;
+    const uint64_t pol = policy_evict_first();
+    const int H = p.H, I = p.I, T = p.T;
+    const DkGeom g = dk_geom(H, I, p.S, p.I_s);
+    const int NQ = H / 32;
+    const long long nSG = p.sh ? (long long)g.sg_cols * g.sg_nr : 0;
+    const long long nSD = p.sh ? (long long)NQ * g.sd_nr : 0;
+    int na = -1;
+    auto n_act = [&]() -> int {
+        if (na < 0) {
+            griddep_wait();  // routing results of the preceding launch
+            int v = __ldcg(p.n_active);
+            na = v < 0 ? 0 : (v > p.E ? p.E : v);
+            for (int i = 0; i < na; ++i) cp_async4(act + i, p.active + i);
+            cp_async_commit();
+            cp_async_wait_all();
+        }
+        return na;
+    };
+    uint32_t it = 0;
+    bool ok = true;
+    auto wait_slot = [&]() -> int {
+        const int st = (int)(it % nst);
+        if (!mbar_wait_bounded(&empty[st], ((it / nst) & 1) ^ 1, abort_flag, &p.hdr->status, p.wait_budget_ns)) {
+            ok = false;
+            return -1;
+        }
+        return st;
+    };
+    long long u = (long long)atomicAdd(&p.hdr->work_counter, 1u);
+    while (ok) {
+        const long long u_next = (long long)atomicAdd(&p.hdr->work_counter, 1u);
+        DHeader h{};
+        const uint8_t *src = nullptr;
+        uint32_t bytes = 0, meta_bytes = 0, hs_bytes = 0;
+        const void *meta = nullptr;
+        const void *hsrc = nullptr;
+        const int *rdy = nullptr;
+        int rdy_target = 0;
+        long long v = u;
+        bool done = false;
+        if (v < nSG) {
+            h.kind = DK_SG;
+            h.blk = (int)(v / g.sg_nr);
+            h.r = (int)(v % g.sg_nr);
+            h.k0 = h.r * g.sg_nks;
+            h.n = g.sg_nks;
+            src = p.sh + (size_t)h.blk * f16_unit_bytes(H) + (size_t)h.k0 * 1024;
+            bytes = h.n * 1024;
+        } else {
+            v -= nSG;
+            const long long nRG = (long long)n_act() * g.rg_blocks * g.rg_nr;
+            if (v < nRG) {
+                h.kind = DK_RG;
+                h.a = (int)(v / ((long long)g.rg_blocks * g.rg_nr));
+                const int rem = (int)(v % ((long long)g.rg_blocks * g.rg_nr));
+                h.blk = rem / g.rg_nr;
+                h.r = rem % g.rg_nr;
+                h.e = act[h.a];
+                h.k0 = h.r * g.rg_gpi;
+                h.n = min(g.rg_gpi, H / 128 - h.k0);
+                const size_t unit = (size_t)h.e * g.rg_blocks + h.blk;
+                src = p.w4 + unit * w4_unit_bytes(H, p.S) + (size_t)h.k0 * w4_group_bytes(p.S);
+                bytes = h.n * (uint32_t)w4_group_bytes(p.S);
+                meta = p.tables + h.e;
+                meta_bytes = 16 + 16 * T;
+            } else {
+                v -= nRG;
+                if (v < nSD) {
+                    h.kind = DK_SD;
+                    h.r = (int)(v / NQ);
+                    h.blk = (int)(v % NQ);
+                    h.k0 = h.r * kDkSdSteps;
+                    h.n = min(kDkSdSteps, p.I_s / 16 - h.k0);
+                    src = p.sh + shared_pairdown_offset(H, p.I_s) + ((size_t)h.blk * (p.I_s / 16) + h.k0) * 1024;
+                    bytes = h.n * 1024;
+                    hsrc = p.hf_s + (size_t)h.k0 * T * 4;
+                    hs_bytes = h.n * T * 32;
+                    rdy = p.rdy_s + h.r;
+                    rdy_target = h.n;
+                } else {
+                    v -= nSD;
+                    const long long nRD = (long long)n_act() * NQ * g.rd_nr;
+                    if (v < nRD) {
+                        h.kind = DK_RD;
+                        h.a = (int)(v / ((long long)NQ * g.rd_nr));
+                        const int rem = (int)(v % ((long long)NQ * g.rd_nr));
+                        h.r = rem / NQ;
+                        h.blk = rem % NQ;
+                        h.e = act[h.a];
+                        h.k0 = h.r * kDkRdGroups;
+                        h.n = min(kDkRdGroups, I / 128 - h.k0);
+                        src = p.w4 + p.w4_colblk +
+                              (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * kW4ColGroupBytes;
+                        bytes = h.n * kW4ColGroupBytes;
+                        meta = p.tables + h.e;
+                        meta_bytes = 16 + 16 * T;
+                        hsrc = p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4;
+                        hs_bytes = h.n * 8 * T * 32;
+                        rdy = p.rdy_r + h.a * g.rd_nr + h.r;
+                        rdy_target = h.n * 8;
+                    } else {
+                        done = true;
+                    }
+                }
+            }
+        }
+        if (done) break;
+        if ((h.kind == DK_RG || h.kind == DK_RD) && (h.e < 0 || h.e >= p.E)) {  // unusable routing entry
+            u = u_next;
+            continue;
+        }
+        const int st = wait_slot();
+        if (st < 0) break;
+        h.seq = (int)it;
+        hdrs[st] = h;
+        uint8_t *dst = ring + (size_t)st * L.stage;
+        mbar_arrive_expect_tx(&full[st], bytes + meta_bytes + hs_bytes);
+        bulk_g2s(dst, src, bytes, &full[st], pol);
+        if (meta_bytes) bulk_g2s(dst + L.meta_off, meta, meta_bytes, &full[st], pol);
+        if (hs_bytes) {
+            // the intermediate slice must be complete before it is copied
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire(rdy) < rdy_target) {
+                if (*abort_flag || global_timer_ns() - t0 > p.wait_budget_ns) {
+                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+            fence_proxy_async_global();
+            bulk_g2s_plain(dst + L.hs_off, hsrc, hs_bytes, &full[st]);
+        }
+        ++it;
+        u = u_next;
+    }
+    if (ok) {
+        for (int w = 0; w < kConsumerWarps; ++w) {  // one end marker per consumer warp
+            const int st = wait_slot();
+            if (st < 0) break;
+            DHeader h{};
+            h.kind = DK_DONE;
+            h.seq = (int)it;
+            hdrs[st] = h;
+            mbar_arrive(&full[st]);
+            ++it;
+        }
+    }
+    if (!ok) {
+        // bounded wait for the copies in flight before the block may exit
+        const uint32_t first = it > (uint32_t)nst ? it - nst : 0;
+        for (uint32_t j = first; j <= it; ++j) {
+            const int st = (int)(j % nst);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&full[st], (j / nst) & 1) && global_timer_ns() - t0 < 100000000ull) {
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ consumers --
+// h = silu(g) * u for token column t and intermediate rows i0 + {2q, 2q+1,
+// 2q+8, 2q+9}, packed as one B fragment (two half2); the g/u sums are reset.
+__device__ __forceinline__ uint2 finalize_frag(float *gsum, float *usum, int T, int i0, int q4, int t) {
+    float hv[4];
+    const int off[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const size_t o = (size_t)(i0 + off[j]) * T + t;
+        const float gv = __ldcg(gsum + o), uv = __ldcg(usum + o);
+        __stcg(gsum + o, 0.f);
+        __stcg(usum + o, 0.f);
+        hv[j] = gv / (1.0f + __expf(-gv)) * uv;
+    }
+    uint2 r;
+    r.x = h2_as_u32(__floats2half2_rn(hv[0], hv[1]));
+    r.y = h2_as_u32(__floats2half2_rn(hv[2], hv[3]));
+    return r;
+}
+
+// INT4 draft kernel; MS = S/16 of the packed INT4 units.
+template <int MS>
+__global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nst = p.nstages;
+    const DkLayout L = dk_layout(p.T, p.H, nst);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q4 = lane & 3;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + nst;
+    uint64_t *allbar = empty + nst;
+    int *misc = reinterpret_cast<int *>(smem + L.misc);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(allbar, kConsumerWarps);
+        misc[0] = 0;  // abort flag
+        misc[1] = 0;  // last-block flag
+        misc[2] = 0;  // consumer stage ticket
+        DHeader *hw = reinterpret_cast<DHeader *>(smem + L.hdrs);
+        for (int st = 0; st < nst; ++st) hw[st].seq = -1;  // no fill yet (shared memory is not cleared)
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == kConsumerWarps) {
+        if (lane == 0) dk_producer(p, smem, L);
+        return;
+    }
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
+    uint32_t allphase = 0;
+    auto all_sync = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(allbar);
+        mbar_wait_bounded(allbar, allphase & 1, abort_flag, &p.hdr->status, p.wait_budget_ns);
+        allphase ^= 1;
+        __syncwarp();
+    };
+    const DHeader *hdrs = reinterpret_cast<const DHeader *>(smem + L.hdrs);
+    const uint8_t *ring = smem + L.ring;
+    float *gamma = reinterpret_cast<float *>(smem + L.gamma);
+    __half *xs = reinterpret_cast<__half *>(smem + L.xs);
+    const int H = p.H, I = p.I, T = p.T, xstr = L.xs_stride;
+    const int ctid = threadIdx.x;
+    const DkGeom geo = dk_geom(H, I, p.S, p.I_s);
+
+    for (int idx = ctid; idx < T * (H / 8); idx += kConsumerWarps * 32) {
+        const int t = idx / (H / 8), h8 = idx - t * (H / 8);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H) + h8);
+        *reinterpret_cast<uint4 *>(xs + (size_t)t * xstr + h8 * 8) = v;
+    }
+    all_sync();
+    if (p.sh && p.w_sgate) {
+        for (int t = warp; t < T; t += kConsumerWarps) {
+            float z = 0.f;
+            for (int hh = lane * 2; hh < H; hh += 64) {
+                const float2 xv = __half22float2(*reinterpret_cast<const __half2 *>(xs + (size_t)t * xstr + hh));
+                const float2 wv = __half22float2(__ldg(reinterpret_cast<const __half2 *>(p.w_sgate + hh)));
+                z = fmaf(xv.x, wv.x, z);
+                z = fmaf(xv.y, wv.y, z);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-z));
+        }
+    } else {
+        for (int t = ctid; t < T; t += kConsumerWarps * 32) gamma[t] = 1.0f;
+    }
+    all_sync();
+
+    constexpr int NTW = 2 * MS;  // INT4 gate+up tiles per k-step
+    constexpr int KB = 2 / MS;   // k-steps per 512 B block
+    constexpr int BPG = 8 / KB;  // blocks per group
+    const int gbytes = 132 * 16 * MS;
+    while (true) {
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(&misc[2], 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        const int st = idx % nst;
+        // Wait for fill number idx of stage st.  Consumers take stages by
+        // ticket, so this warp may wait for a stage whose previous fill has not
+        // landed yet; a parity wait cannot tell those two phases apart, so the
+        // fill is accepted only when its header carries this ticket.
+        bool got = false;
+        {
+            const uint32_t par = (uint32_t)(idx / nst) & 1;
+            const volatile int *seqp = &hdrs[st].seq;
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                if (mbar_try_wait(&full[st], par) && *seqp == idx) {
+                    got = true;
+                    break;
+                }
+                if (*abort_flag) break;
+                if (global_timer_ns() - t0 > p.wait_budget_ns) {
+                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        if (!got) break;
+        const DHeader h = hdrs[st];
+        if (h.kind == DK_DONE) {
+            // release it too: with fewer stages than warps the end markers reuse stages
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            break;
+        }
+        const uint8_t *stage = ring + (size_t)st * L.stage;
+        const TokTable *tb = reinterpret_cast<const TokTable *>(stage + L.meta_off);
+        const uint2 *hsl = reinterpret_cast<const uint2 *>(stage + L.hs_off);
+        int ready_slot = -1;  // completion counter hit by this item (gate/up)
+        if (h.kind == DK_SG) {
+            // shared gate/up: 16 columns (tiles: gate, up), k-steps [k0, k0+n) of H
+            float acc[2][2][4] = {};
+            const bool okx = g < T;
+            const __half *xr = xs + (okx ? g : 0) * xstr + 2 * q4;
+            for (int ks = 0; ks < h.n; ++ks) {
+                const uint32_t b0 = okx ? lds32(xr + 16 * (h.k0 + ks)) : 0u;
+                const uint32_t b1 = okx ? lds32(xr + 16 * (h.k0 + ks) + 8) : 0u;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const uint4 v = lds128(stage + ((size_t)ks * 2 + t) * 512 + lane * 16);
+                    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+                    mma_16816(acc[ks & 1][t], a, b0, b1);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                float *base = p.gu_s + (size_t)t * p.I_s * T;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int col = 2 * q4 + hf;
+                    if (col < T) {
+                        red_add(base + (size_t)(16 * h.blk + g) * T + col, acc[0][t][hf] + acc[1][t][hf]);
+                        red_add(base + (size_t)(16 * h.blk + g + 8) * T + col, acc[0][t][2 + hf] + acc[1][t][2 + hf]);
+                    }
+                }
+            }
+            __threadfence();  // this lane's partial sums before the block counter
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) old = atomicAdd(p.cnt_s + h.blk, 1);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == geo.sg_nr - 1) {
+                __threadfence();
+                const int t = lane >> 2;
+                if (t < T)
+                    p.hf_s[((size_t)h.blk * T + t) * 4 + q4] =
+                        finalize_frag(p.gu_s, p.gu_s + (size_t)p.I_s * T, T, 16 * h.blk, q4, t);
+                ready_slot = 0;
+            }
+        } else if (h.kind == DK_RG) {
+            // routed INT4 gate/up: slice of S = 16*MS columns, groups [k0, k0+n) of H
+            const int n_e = min(max(tb->n, 0), T);
+            const bool okx = g < n_e;
+            int tok = okx ? tb->e[g].tok : 0;
+            tok = (tok >= 0 && tok < T) ? tok : 0;
+            const __half *xr = xs + tok * xstr + 2 * q4;
+            float run[NTW][4] = {};
+            for (int gr = 0; gr < h.n; ++gr) {
+                const uint8_t *gp = stage + (size_t)gr * gbytes;
+                const __half *scp = reinterpret_cast<const __half *>(gp);
+                float acc[NTW][4] = {};
+#pragma unroll
+                for (int ib = 0; ib < BPG; ++ib) {
+                    const uint4 v = lds128(gp + 64 * MS + ib * 512 + lane * 16);
+                    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int ki = 0; ki < KB; ++ki) {
+                        const int ks = (h.k0 + gr) * 8 + ib * KB + ki;
+                        const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
+                        const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
+#pragma unroll
+                        for (int t = 0; t < NTW; ++t) {
+                            uint32_t a[4];
+                            dequant_frag(words[ki * NTW + t], a);
+                            mma_16816(acc[t], a, b0, b1);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < NTW; ++t) {
+                    const float sa = __half2float(scp[t * 16 + g]), sb = __half2float(scp[t * 16 + g + 8]);
+                    run[t][0] = fmaf(sa, acc[t][0], run[t][0]);
+                    run[t][1] = fmaf(sa, acc[t][1], run[t][1]);
+                    run[t][2] = fmaf(sb, acc[t][2], run[t][2]);
+                    run[t][3] = fmaf(sb, acc[t][3], run[t][3]);
+                }
+            }
+            const int S = 16 * MS;
+#pragma unroll
+            for (int t = 0; t < NTW; ++t) {
+                const int gu = t < MS ? 0 : 1;
+                const int i = h.blk * S + 16 * (t % MS) + g;
+                float *base = p.gu_r + ((size_t)h.a * 2 + gu) * I * T;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int col = 2 * q4 + hf;
+                    if (col < n_e) {
+                        red_add(base + (size_t)i * T + col, run[t][hf]);
+                        red_add(base + (size_t)(i + 8) * T + col, run[t][2 + hf]);
+                    }
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) old = atomicAdd(p.cnt_r + h.a * (I / 16) + h.blk, 1);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == geo.rg_nr - 1) {
+                __threadfence();
+                const int t = lane >> 2;
+                float *gs = p.gu_r + ((size_t)h.a * 2) * I * T;
+                if (t < T) {
+#pragma unroll
+                    for (int kk = 0; kk < MS; ++kk) {
+                        const int ks = h.blk * MS + kk;
+                        p.hf_r[(((size_t)h.a * (I / 16) + ks) * T + t) * 4 + q4] =
+                            finalize_frag(gs, gs + (size_t)I * T, T, 16 * ks, q4, t);
+                    }
+                }
+                ready_slot = 1;
+            }
+        } else if (h.kind == DK_SD) {
+            // shared down: output pair blk (32 outputs), k-steps [k0, k0+n) of I_s
+            float acc[2][2][4] = {};
+            const bool okb = g < T;
+            for (int ks = 0; ks < h.n; ++ks) {
+                uint2 bv = make_uint2(0u, 0u);
+                if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ks * T + g) * 4 + q4);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint4 v = lds128(stage + ((size_t)ks * 2 + q) * 512 + lane * 16);
+                    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+                    mma_16816(acc[ks & 1][q], a, bv.x, bv.y);
+                }
+            }
+            const int n0 = 32 * h.blk + 4 * g;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int col = 2 * q4 + hf;
+                if (col < T) {
+                    const float w = p.mode == 0 ? 1.f : gamma[col];
+                    float4 o;
+                    o.x = (acc[0][0][hf] + acc[1][0][hf]) * w;
+                    o.y = (acc[0][0][2 + hf] + acc[1][0][2 + hf]) * w;
+                    o.z = (acc[0][1][hf] + acc[1][1][hf]) * w;
+                    o.w = (acc[0][1][2 + hf] + acc[1][1][2 + hf]) * w;
+                    atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)col * H + n0), o);
+                }
+            }
+        } else if (h.kind == DK_RD) {
+            // routed INT4 down: output pair blk, groups [k0, k0+n) of I
+            const int n_e = min(max(tb->n, 0), T);
+            const bool okb = g < n_e;
+            float run[2][4] = {};
+            for (int gr = 0; gr < h.n; ++gr) {
+                const uint8_t *gp = stage + (size_t)gr * kW4ColGroupBytes;
+                const __half *scp = reinterpret_cast<const __half *>(gp);
+                float acc[2][4] = {};
+#pragma unroll
+                for (int ib = 0; ib < 4; ++ib) {
+                    const uint4 v = lds128(gp + 64 + ib * 512 + lane * 16);
+                    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int ki = 0; ki < 2; ++ki) {
+                        const int ksr = gr * 8 + ib * 2 + ki;  // k-step within the slice
+                        uint2 bv = make_uint2(0u, 0u);
+                        if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ksr * T + g) * 4 + q4);
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            uint32_t a[4];
+                            dequant_frag(words[ki * 2 + q], a);
+                            mma_16816(acc[q], a, bv.x, bv.y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float sa = __half2float(scp[q * 16 + g]), sb = __half2float(scp[q * 16 + g + 8]);
+                    run[q][0] = fmaf(sa, acc[q][0], run[q][0]);
+                    run[q][1] = fmaf(sa, acc[q][1], run[q][1]);
+                    run[q][2] = fmaf(sb, acc[q][2], run[q][2]);
+                    run[q][3] = fmaf(sb, acc[q][3], run[q][3]);
+                }
+            }
+            const int n0 = 32 * h.blk + 4 * g;
+            const int rmax = p.mode == 0 ? T * p.k : T;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int col = 2 * q4 + hf;
+                if (col < n_e) {
+                    const int row = tb->e[col].row;
+                    const float w = tb->e[col].scale;
+                    if (row >= 0 && row < rmax) {
+                        float4 o;
+                        o.x = run[0][hf] * w;
+                        o.y = run[0][2 + hf] * w;
+                        o.z = run[1][hf] * w;
+                        o.w = run[1][2 + hf] * w;
+                        atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)row * H + n0), o);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (ready_slot >= 0) {
+            // publish: the block's intermediate is complete; reset its counter
+            __threadfence();  // this lane's h fragments and cleared sums first
+            __syncwarp();
+            if (lane == 0) {
+                if (ready_slot == 0) {
+                    p.cnt_s[h.blk] = 0;
+                    __threadfence();
+                    atomicAdd(p.rdy_s + h.blk / kDkSdSteps, 1);
+                } else {
+                    p.cnt_r[h.a * (I / 16) + h.blk] = 0;
+                    __threadfence();
+                    atomicAdd(p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / kDkRdGroups, MS);
+                }
+            }
+        }
+    }
+
+    // completion ticket; the last block writes the fp16 output and resets
+    all_sync();
+    if (ctid == 0) {
+        __threadfence();
+        const uint32_t t = atomicAdd(&p.hdr->done_ticket, 1u);
+        misc[1] = (t == gridDim.x - 1);
+    }
+    all_sync();
+    if (misc[1]) {
+        __threadfence();
+        if (p.mode == 2) {
+            const int n4 = T * H / 4;
+            float4 *acc4 = reinterpret_cast<float4 *>(p.yout);
+            for (int idx = ctid; idx < n4; idx += kConsumerWarps * 32) {
+                const float4 v = __ldcg(acc4 + idx);
+                uint2 o;
+                o.x = h2_as_u32(__floats2half2_rn(v.x, v.y));
+                o.y = h2_as_u32(__floats2half2_rn(v.z, v.w));
+                reinterpret_cast<uint2 *>(p.out)[idx] = o;
+                __stcg(acc4 + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+            }
+        }
+        for (int i = ctid; i < geo.sd_nr; i += kConsumerWarps * 32) p.rdy_s[i] = 0;
+        for (int i = ctid; i < p.nact_max * geo.rd_nr; i += kConsumerWarps * 32) p.rdy_r[i] = 0;
+        if (ctid == 0) {
+            p.hdr->work_counter = 0;
+            p.hdr->done_ticket = 0;
+        }
+        __threadfence();
+    }
+}
+
+// ------------------------------------------------------------ launching --
+size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max) {
+    return dk_scratch(base, T, H, I, I_s, nact_max).end;
+}
+
+bool draft_supported(int T, int H, int I, int S, int I_s) {
+    if (T < 1 || T > 8 || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
+    if (I_s % 16) return false;
+    return dk_layout(T, H, 4).total <= kSmemLimit;
+}
+
+int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
+    DkParams p{};
+    p.w4 = e.routed;
+    p.S = e.S;
+    p.w4_colblk = w4_colblk_offset(e.E, e.H, e.I, e.S);
+    p.sh = e.shared;
+    p.w_sgate = e.w_sgate;
+    p.I_s = e.shared ? e.I_s : 0;
+    p.E = e.E;
+    p.I = e.I;
+    p.k = e.k;
+    p.T = e.T;
+    p.H = e.H;
+    p.active = e.active;
+    p.n_active = e.n_active;
+    p.tables = e.tables;
+    p.x = e.x;
+    p.mode = e.mode;
+    p.yout = e.yout;
+    p.out = e.out;
+    p.hdr = e.hdr;
+    p.wait_budget_ns = e.wait_budget_ns;
+    p.nact_max = e.E < e.T * e.k ? e.E : e.T * e.k;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(e.hdr);
+    const DkScratch sc = dk_scratch(ws_scratch_base, e.T, e.H, e.I, p.I_s, p.nact_max);
+    p.gu_s = reinterpret_cast<float *>(ws + sc.gu_s);
+    p.gu_r = reinterpret_cast<float *>(ws + sc.gu_r);
+    p.hf_s = reinterpret_cast<uint2 *>(ws + sc.hf_s);
+    p.hf_r = reinterpret_cast<uint2 *>(ws + sc.hf_r);
+    p.cnt_s = reinterpret_cast<int *>(ws + sc.cnt_s);
+    p.cnt_r = reinterpret_cast<int *>(ws + sc.cnt_r);
+    p.rdy_s = reinterpret_cast<int *>(ws + sc.rdy_s);
+    p.rdy_r = reinterpret_cast<int *>(ws + sc.rdy_r);
+    int nst = 12;
+    DkLayout L = dk_layout(e.T, e.H, nst);
+    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst);
+    if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
+    p.nstages = nst;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SPX_ERR_CUDA;
+    static int configured[2][64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
+    const int ms = e.S / 16;
+    if (!configured[ms - 1][dev]) {
+        cudaError_t err = ms == 2 ? cudaFuncSetAttribute(draft_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         kSmemLimit)
+                                  : cudaFuncSetAttribute(draft_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         kSmemLimit);
+        if (err != cudaSuccess) return record_launch(err);
+        configured[ms - 1][dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t err = ms == 2 ? cudaLaunchKernelEx(&cfg, draft_kernel<2>, p) : cudaLaunchKernelEx(&cfg, draft_kernel<1>, p);
+    return record_launch(err);
+}
+
+}  // namespace spx

@@ -50,12 +50,29 @@ __host__ __device__ inline size_t w4_unit_bytes(int H, int S) { return w4_gu_byt
 __host__ __device__ inline size_t w4_units_bytes(int E, int H, int I, int S) {
     return (size_t)E * (I / S) * w4_unit_bytes(H, S);
 }
+// INT4 down weights again, column-block-major (for the split-K draft launch):
+// per expert, per pair of output m-tiles (32 columns), per group of 128 rows
+// of I: 32 fp16 scales in tile-row order (tile q row m at q*16 + m) followed
+// by 4 blocks of 512 B, each 2 k-steps: lane words [ks][tile].
+constexpr int kW4ColGroupBytes = 64 + 4 * 512;
+__host__ __device__ inline size_t w4_colblk_bytes(int E, int H, int I) {
+    return (size_t)E * (H / 32) * (I / 128) * kW4ColGroupBytes;
+}
+__host__ __device__ inline size_t w4_colblk_offset(int E, int H, int I, int S) {
+    return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
+}
 // FP16 unit (S = 16):
 //   [gu  : H/16 blocks (one k-step each) of 2 tiles x 32 lanes x 16 B]
 //   [down: H/32 blocks (one m-tile pair each) of 2 tiles x 32 lanes x 16 B]
 constexpr int kF16S = 16;
 __host__ __device__ inline size_t f16_unit_bytes(int H) { return (size_t)6 * H * kF16S; }
 __host__ __device__ inline size_t f16_gu_bytes(int H) { return (size_t)4 * H * kF16S; }
+// Shared expert pack = FP16 units (one expert) followed by its down weights in
+// pair-major order: per m-tile pair P, per k-step of I: [tile][lane] x 16 B.
+__host__ __device__ inline size_t shared_pairdown_offset(int H, int I) { return (size_t)(I / kF16S) * f16_unit_bytes(H); }
+__host__ __device__ inline size_t shared_packed_bytes(int H, int I) {
+    return shared_pairdown_offset(H, I) + (size_t)(H / 32) * (I / 16) * 1024;
+}
 
 // Per-expert token table (workspace), written by the routing launch or by the
 // table launch of the unit calls, bulk-copied next to the expert's first chunk.
@@ -157,6 +174,16 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // of the issuing thread).
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Bulk copy without an L2 hint (data that other blocks read as well).
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -261,6 +288,9 @@ int route_validate(const uint16_t *x, const uint16_t *w_router, const float *log
 int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl);
 int engine_fits(int T, int H, int fmt, int S);
 int engine_nt(int T);
+bool draft_supported(int T, int H, int I, int S, int I_s);
+size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max);
+int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaStream_t s);
 int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int32_t *active,
                   const int32_t *n_active, int T, int k, int E, TokTable *tables, cudaStream_t s);
 

@@ -16,8 +16,9 @@
 namespace spx {
 
 // Scratch of spx_moe_layer_noalloc: 1 MiB, held by every GPU that loads the
-// library until the process exits.  Enough for spx_workspace_size(T, H) <= 1 MiB,
-// i.e. T*H up to about 195,000 (T = 17 at H = 4096, T = 64 at H = 2048).
+// library until the process exits.  Enough for any layer whose
+// spx_workspace_size(T, H, I, E, k, I_s) is at most 1 MiB (for example the
+// DeepSeek-V2-Lite-shaped layer at T = 1 and at T = 17).
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -48,16 +49,18 @@ using namespace spx;
 
 extern "C" int spx_moe_layer_noalloc(const spx_layer_args *args, spx_stream_t stream) {
     if (!args) return SPX_ERR_INVALID_ARG;
-    const size_t need = spx_workspace_size(args->T, args->H);
+    const int I = args->mode == 0 ? (args->w4 ? args->w4->I : 0) : (args->f16 ? args->f16->I : 0);
+    const int I_s = args->shared ? args->shared->I_s : 0;
+    const size_t need = spx_workspace_size(args->T, args->H, I, args->E, args->k, I_s);
     if (need == 0) return SPX_ERR_UNSUPPORTED;
     if (need > kNoAllocScratchBytes) return SPX_ERR_WORKSPACE;  // T*H beyond the fixed scratch
     void *scratch = nullptr;
     int st = noalloc_scratch(&scratch);
     if (st) return st;
-    // The array keeps the previous call's contents: clear the header (queue
-    // counter, tickets, status) and the accumulator, which must start at zero.
+    // The array keeps the previous call's contents: clear the part this shape
+    // uses (counters, tickets, status, accumulators), which must start at zero.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = cudaMemsetAsync(scratch, 0, ws_tables_offset(args->T, args->H), s);
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, need, s);
     if (e != cudaSuccess) return record_launch(e);
     spx_layer_args a = *args;
     a.ws = scratch;

@@ -137,6 +137,66 @@ __global__ void f16_pack_down(const uint16_t *wd, int E, int H, int I, uint8_t *
     }
 }
 
+// INT4 down, column-block-major: scales of (e, pair Q, group grp).
+__global__ void w4_pack_colblk_scales(const uint16_t *s_down, int E, int H, int I, uint8_t *region) {
+    const int NQ = H / 32, G = I / 128;
+    const size_t total = (size_t)E * NQ * G * 32;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int qm = idx % 32;
+        const size_t gi = idx / 32;  // (e * NQ + Q) * G + grp
+        const int grp = gi % G;
+        const int Q = (gi / G) % NQ;
+        const int e = gi / ((size_t)G * NQ);
+        const int n = down_col(2 * Q + (qm >> 4), qm & 15);
+        uint16_t *dst = reinterpret_cast<uint16_t *>(region + gi * kW4ColGroupBytes);
+        dst[qm] = s_down[((size_t)e * G + grp) * H + n];
+    }
+}
+
+// INT4 down, column-block-major: codes; block ib of a group holds k-steps
+// 8*grp + 2*ib + {0,1}; lane word w = [ks_in][tile].
+__global__ void w4_pack_colblk_codes(const int32_t *qd, int E, int H, int I, uint8_t *region) {
+    const int NQ = H / 32, G = I / 128;
+    const size_t total = (size_t)E * NQ * G * 4 * 128;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int wi = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int ib = (idx >> 7) & 3;
+        const size_t gi = idx >> 9;  // (e * NQ + Q) * G + grp
+        const int grp = gi % G;
+        const int Q = (gi / G) % NQ;
+        const int e = gi / ((size_t)G * NQ);
+        const int ks = grp * 8 + ib * 2 + (wi >> 1);
+        const int q = wi & 1;
+        const int32_t *qe = qd + (size_t)e * (I / 8) * H;
+        uint32_t word = 0;
+        for (int nib = 0; nib < 8; ++nib) {
+            const int r = nib & 3, hh = nib >> 2;
+            const int m = frag_row(lane, r), kc = frag_col(lane, r, hh);
+            word |= gptq_code(qe, H, 16 * ks + kc, down_col(2 * Q + q, m)) << (4 * nib);
+        }
+        reinterpret_cast<uint32_t *>(region + gi * kW4ColGroupBytes + 64 + ib * 512)[lane * 4 + wi] = word;
+    }
+}
+
+// Shared expert down, pair-major: [P][ks][tile q][lane] x 16 B;
+// A[m][kc] = W_down[down_col(2P+q, m)][16 ks + kc].
+__global__ void f16_pack_pairdown(const uint16_t *wd, int H, int I, uint8_t *region) {
+    const int NP = H / 32, NK = I / 16;
+    const size_t total = (size_t)NP * NK * 2 * 32 * 4;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int r = idx & 3;
+        const int lane = (idx >> 2) & 31;
+        const int q = (idx >> 7) & 1;
+        const size_t pk = idx >> 8;  // P * NK + ks
+        const int ks = pk % NK, P = pk / NK;
+        const int n = down_col(2 * P + q, frag_row(lane, r));
+        uint32_t word = 0;
+        for (int hh = 0; hh < 2; ++hh) word |= (uint32_t)wd[(size_t)n * I + 16 * ks + frag_col(lane, r, hh)] << (16 * hh);
+        reinterpret_cast<uint32_t *>(region)[((pk * 2 + q) * 32 + lane) * 4 + r] = word;
+    }
+}
+
 static int grid_for(size_t total) {
     size_t g = (total + 255) / 256;
     if (g > 65535) g = 65535;
@@ -152,7 +212,7 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 extern "C" size_t spx_w4_packed_bytes(int E, int H, int I, int S) {
     if (E < 1 || H < 128 || I < 128 || (S != 16 && S != 32) || H % 128 || I % 128) return 0;
-    return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
+    return w4_colblk_offset(E, H, I, S) + w4_colblk_bytes(E, H, I);
 }
 
 extern "C" size_t spx_f16_packed_bytes(int E, int H, int I) {
@@ -180,7 +240,29 @@ extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, con
     if (st) return st;
     cudaError_t e = cudaMemcpyAsync(out + w4_units_bytes(E, H, I, S), s_down, (size_t)E * (I / 128) * H * 2,
                                     cudaMemcpyDeviceToDevice, s);
-    return record_launch(e);
+    if (e != cudaSuccess) return record_launch(e);
+    uint8_t *cb = out + w4_colblk_offset(E, H, I, S);
+    tot = (size_t)E * (H / 32) * (I / 128) * 32;
+    w4_pack_colblk_scales<<<grid_for(tot), 256, 0, s>>>(s_down, E, H, I, cb);
+    tot = (size_t)E * (H / 32) * (I / 128) * 512;
+    w4_pack_colblk_codes<<<grid_for(tot), 256, 0, s>>>(qw_down, E, H, I, cb);
+    return record_launch(cudaGetLastError());
+}
+
+extern "C" size_t spx_shared_packed_bytes(int H, int I_s) {
+    if (H < 128 || I_s < 16 || H % 128 || I_s % kF16S || H > kMaxH) return 0;
+    return shared_packed_bytes(H, I_s);
+}
+
+extern "C" int spx_shared_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down, int H, int I_s,
+                                 void *packed, spx_stream_t stream) {
+    if (spx_shared_packed_bytes(H, I_s) == 0) return SPX_ERR_UNSUPPORTED;
+    int st = spx_f16_repack(w_gate, w_up, w_down, 1, H, I_s, packed, stream);
+    if (st) return st;
+    const size_t tot = (size_t)(H / 32) * (I_s / 16) * 256;
+    f16_pack_pairdown<<<grid_for(tot), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w_down, H, I_s, static_cast<uint8_t *>(packed) + shared_pairdown_offset(H, I_s));
+    return record_launch(cudaGetLastError());
 }
 
 extern "C" int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down, int E, int H,

@@ -65,7 +65,9 @@ _SIGS = {
     "spx_f16_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "spx_w4_repack": (C.c_int, [C.c_void_p] * 6 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_f16_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
-    "spx_workspace_size": (C.c_size_t, [C.c_int, C.c_int]),
+    "spx_workspace_size": (C.c_size_t, [C.c_int] * 6),
+    "spx_shared_packed_bytes": (C.c_size_t, [C.c_int, C.c_int]),
+    "spx_shared_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_workspace_init": (C.c_int, [C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "spx_moe_draft_w4a16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(W4Experts), C.c_int] + [C.c_void_p] * 5 +
@@ -135,13 +137,14 @@ def spx_version() -> int:
     return load().spx_version()
 
 
-def spx_workspace_size(T: int, H: int) -> int:
-    return load().spx_workspace_size(T, H)
+def spx_workspace_size(T: int, H: int, I: int = 0, E: int = 1, k: int = 1, I_s: int = 0) -> int:
+    return load().spx_workspace_size(T, H, I, E, k, I_s)
 
 
-def new_workspace(T: int, H: int, device="cuda", stream=None) -> torch.Tensor:
+def new_workspace(T: int, H: int, I: int = 0, E: int = 1, k: int = 1, I_s: int = 0, device="cuda",
+                  stream=None) -> torch.Tensor:
     """Allocate (through torch) and zero a workspace for up to T tokens."""
-    n = spx_workspace_size(T, H)
+    n = spx_workspace_size(T, H, I, E, k, I_s)
     if n == 0:
         raise SpxError(SPX_ERR_UNSUPPORTED, "spx_workspace_size")
     ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -247,9 +250,15 @@ def spx_f16_repack(w_gate, w_up, w_down, stream=None) -> PackedF16:
 
 
 def pack_shared(w_gate, w_up, w_down, w_sgate=None, stream=None) -> PackedShared:
-    """Shared expert [I_s][H], [I_s][H], [H][I_s] fp16 -> packed (one FP16 expert)."""
-    p = spx_f16_repack(w_gate[None], w_up[None], w_down[None], stream)
-    return PackedShared(p.buf, w_sgate, p.H, p.I)
+    """Shared expert [I_s][H], [I_s][H], [H][I_s] fp16 -> packed (spx_shared_repack)."""
+    I_s, H = w_gate.shape
+    n = load().spx_shared_packed_bytes(H, I_s)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_shared_packed_bytes")
+    buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
+    _chk(load().spx_shared_repack(_p(w_gate), _p(w_up), _p(w_down), H, I_s, _p(buf), _stream(stream)),
+         "spx_shared_repack")
+    return PackedShared(buf, w_sgate, H, I_s)
 
 
 def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):

@@ -42,11 +42,15 @@ def test_sizes_and_strings(lib):
     assert spx.status_string(0) == "ok"
     assert "timed out" in spx.status_string(-5)
     # INT4 unit = 49*H*S/32 bytes; down scales copied once per expert
-    assert lib.spx_w4_packed_bytes(64, 2048, 1408, 32) == 64 * 44 * (49 * 2048 * 32 // 32) + 64 * 11 * 2048 * 2
+    assert lib.spx_w4_packed_bytes(64, 2048, 1408, 32) == (64 * 44 * (49 * 2048 * 32 // 32) + 64 * 11 * 2048 * 2
+                                                           + 64 * 64 * 11 * (64 + 4 * 512))
+    assert lib.spx_shared_packed_bytes(2048, 2816) == 2816 // 16 * 6 * 2048 * 16 + 64 * 176 * 1024
     assert lib.spx_w4_packed_bytes(64, 2048, 1408, 24) == 0
     assert lib.spx_f16_packed_bytes(64, 2048, 1408) == 64 * 1408 * 2048 * 2 * 3
-    assert lib.spx_workspace_size(17, 2048) >= 256 + 17 * 2048 * 4
-    assert lib.spx_workspace_size(65, 2048) == 0
+    assert lib.spx_workspace_size(17, 2048, 1408, 64, 6, 2816) >= 256 + 17 * 2048 * 4
+    # the T <= 8 draft launch adds its split-K scratch
+    assert lib.spx_workspace_size(1, 2048, 1408, 64, 6, 2816) > lib.spx_workspace_size(1, 2048, 0, 64, 6, 0)
+    assert lib.spx_workspace_size(65, 2048, 1408, 64, 6, 0) == 0
 
 
 def test_validation_before_any_launch(lib):

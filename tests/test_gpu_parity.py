@@ -139,6 +139,7 @@ SMALL_CASES = [
     (_small("tiny"), 4, 16),
     (_small("deepseek_v2_lite", I=256, E=16), 1, 32),
     (_small("deepseek_v2_lite", I=256, E=16), 17, 32),
+    (_small("deepseek_v2_lite", I=256, E=16), 8, 16),    # draft launch with 8 tokens, 16-column slices
     (_small("qwen15_moe", I=384, E=12, I_s=512), 9, 16),
     (_small("phi35_moe", H=1024, I=512), 17, 16),
     (_small("phi35_moe", H=1024, I=512, k=2), 33, 16),   # > 24 tokens: 64-token kernel
@@ -156,7 +157,7 @@ def test_draft_and_verify_unit_calls(case):
     ids, w = oracle.route_topk(lg, s.k, s.renorm)
     lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), slice_cols=S)
     g, r = _routing_dev(ids, s.E)
-    ws = spx.new_workspace(T, s.H)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
     dx = gh.dev_f16(x)
     for mode in ("draft", "verify"):
         mlp = oracle.swiglu_w4 if mode == "draft" else oracle.swiglu_f16
@@ -188,7 +189,7 @@ def test_draft_wide_slices_reject_many_tokens():
     y = torch.empty(T * s.k, s.H, device="cuda")
     with pytest.raises(SpxError) as ei:
         spx.spx_moe_draft_w4a16(gh.dev_f16(W.gen_x(s, T)), lay.w4, s.k, r["offsets"], r["sorted_slots"],
-                                r["active"], r["n_active"], y, spx.new_workspace(T, s.H))
+                                r["active"], r["n_active"], y, spx.new_workspace(T, s.H, s.I, s.E, s.k))
     assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
 
 
@@ -231,7 +232,7 @@ def _run_layer(lay, mode, x, logits, elb=None):
     T = x.shape[0]
     routing = spx.Routing.empty(T, s.E, s.k)
     out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
-    ws = spx.new_workspace(T, s.H)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
     d_lg = gh.dev(np.asarray(logits, np.float32)) if logits is not None else torch.empty(
         T, s.E, dtype=torch.float32, device="cuda")
     args, keep = spx.layer_args(0 if mode == "draft" else 1, gh.dev_f16(x), s.E, s.k, s.renorm, d_lg, routing, out,
@@ -269,6 +270,22 @@ def test_layer_full_size(name, mode):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{name} {mode} rep {rep}")
 
 
+@pytest.mark.parametrize("T", [2, 8])
+def test_draft_layer_gated_shared_many_tokens(T):
+    """Draft layer through the split-K draft launch with T tokens, a gated
+    shared expert and a router product (Qwen-shaped, reduced sizes)."""
+    gh = _gh()
+    s = _small("qwen15_moe", I=384, E=12, I_s=768)
+    x = W.gen_x(s, T, step=T)
+    need = gh.needed_experts(s, None, [x])
+    lay = gh.Layer(s, needed=need, verify=False)
+    ref = lay.oracle_layer("draft", x)
+    outs, routing, _ = _run_layer(lay, "draft", x, None)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"draft T={T} rep {rep}")
+
+
 def test_tiny_draft_matches_verify_on_gpu():
     """Tiny layer: verify weights are FP16 copies of the dequantised draft
     weights, so the two paths agree within the weights' fp16 rounding."""
@@ -295,7 +312,7 @@ def test_layer_elb_counts_draft_steps():
             ref = lays[l].oracle_layer("draft", x, logits=lg, elb=elb_ref)
             routing = spx.Routing.empty(1, s.E, s.k)
             out = torch.empty(1, s.H, dtype=torch.float16, device="cuda")
-            ws = spx.new_workspace(1, s.H)
+            ws = spx.new_workspace(1, s.H, s.I, s.E, s.k, s.I_s)
             args, keep = spx.layer_args(0, gh.dev_f16(x), s.E, s.k, s.renorm, gh.dev(lg), routing, out, ws,
                                         w4=lays[l].w4, shared=lays[l].shared, elb=elb, layer=l)
             spx.spx_moe_layer(args)

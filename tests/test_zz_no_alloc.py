@@ -42,7 +42,7 @@ def test_noalloc_layer_matches_workspace_layer(lib, mode):
 
     r_ref = spx.Routing.empty(T, s.E, s.k)
     out_ref = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
-    ws = spx.new_workspace(T, s.H)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
     a_ref, keep_ref = spx.layer_args(m, x, s.E, s.k, s.renorm, lg, r_ref, out_ref, ws, w4=lay.w4, f16=lay.f16,
                                      shared=lay.shared)
     assert lib.spx_moe_layer(C.byref(a_ref), stream) == 0
