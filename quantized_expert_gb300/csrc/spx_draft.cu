@@ -8,20 +8,23 @@
 //
 // GB300 design.  At T = 1 a layer is ~60-90 MB of weights read once, ~10 us at
 // HBM speed, so balance and latency decide everything.  The work is cut into
-// ~16 KB items, each processed by ONE warp, with no block-level barriers:
+// ~16 KB items, each processed by ONE consumer warp, with no block barrier:
 //   SG  shared gate/up   (16-column block, range of H)
 //   RG  routed gate/up   (S-column slice of an active expert, range of H)
 //   SD  shared down      (pair of output m-tiles = 32 outputs, range of I_s)
 //   RD  routed down      (32 outputs of an active expert, range of I)
-// Gate/up items add their partial sums into fp32 scratch; the warp whose item
-// completes a column block applies SiLU, writes the fp16 intermediate h in
-// mma B-fragment order and counts the block as ready.  Down items are issued
-// after every gate/up item (one global dynamic queue), their weights stream at
-// once, and the producer bulk-copies the h slice next to them as soon as the
-// slice is ready, so each output gets ~2 partial sums per expert, not one per
-// slice.  One producer warp streams items through a ring of stages (TMA bulk
-// copies + mbarriers); the 8 consumer warps take stages in order through a
-// shared-memory ticket, so a slow item never stalls the others.
+// All gate/up items of one column block run on the SM that dequeued the
+// block: their partial sums meet in a shared-memory slot, and the warp that
+// completes the block applies SiLU, writes the fp16 intermediate h (mma
+// B-fragment order) to global memory and counts the block as ready.  So a
+// gate/up item costs no global atomics and no fence; only a block's last item
+// publishes.  Down items follow every gate/up block in one dynamic queue; their
+// weights stream at once, and a poller warp bulk-copies each down item's h
+// slice next to them as soon as that slice is complete, so each output gets
+// ~2 partial sums per expert, not one per slice.  The producer warp dequeues
+// whole blocks (or pairs of down items) with the next ticket already in
+// flight, and never waits on h.  Consumer warps take ring stages in order
+// through a shared-memory ticket, so a slow item never stalls the others.
 #include "spx_internal.cuh"
 
 #include <math.h>
@@ -29,23 +32,39 @@
 namespace spx {
 
 enum : int { DK_SG = 0, DK_RG = 1, DK_SD = 2, DK_RD = 3, DK_DONE = 4 };
-constexpr int kDkData = 16896;  // largest item: 4 INT4 groups of 32 columns (or 8 of 16)
-constexpr int kDkRdGroups = 7;  // INT4 down groups (of 128 rows of I) per RD item
-constexpr int kDkSdSteps = 16;  // k-steps of I_s per SD item
+constexpr int kDkData = 16896;    // largest item: 4 INT4 groups of 32 columns (or 8 of 16)
+constexpr int kDkRdGroups = 7;    // INT4 down groups (of 128 rows of I) per RD item
+constexpr int kDkSdSteps = 16;    // k-steps of I_s per SD item
+constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
+constexpr int kDkDBatch = 2;      // down items per queue ticket
+constexpr int kDkThreads = (kConsumerWarps + 2) * 32;  // + producer warp + poller warp
 
 struct __align__(16) DHeader {
     int kind;
-    int a;    // active slot (routed items)
-    int e;    // expert (routed items)
-    int blk;  // SG: shared block; RG: slice; SD/RD: output pair
-    int r;    // range index
-    int k0;   // SG: first k-step of H; RG: first group of H; SD: first k-step of I_s; RD: first group of I
-    int n;    // SG/SD: k-steps; RG/RD: groups
-    int seq;  // ring sequence number of this stage fill
+    int a;       // active slot (routed items)
+    int e;       // expert (routed items)
+    int blk;     // SG: shared block; RG: slice; SD/RD: output pair
+    int r;       // range index
+    int k0;      // SG: first k-step of H; RG: first group of H; SD: first k-step of I_s; RD: first group of I
+    int n;       // SG/SD: k-steps; RG/RD: groups
+    int seq;     // ring sequence number of this stage fill
+    int slot;    // gate/up: shared-memory slot of the column block
+    int nitems;  // gate/up: items of the column block
+    int bseq;    // gate/up: column-block sequence number on this SM
+    int pad;
+};
+
+// A down item's h slice that the poller copies once the slice is complete.
+struct DPend {
+    const void *src;
+    const int *rdy;
+    int target;
+    uint32_t bytes;
+    uint32_t pad[2];
 };
 
 struct DkGeom {
-    int sg_cols, sg_nks, sg_nr;  // shared gate/up: blocks of 16 columns, k-steps per item, ranges
+    int sg_cols, sg_nks, sg_nr;  // shared gate/up: blocks of 16 columns, k-steps per item, items per block
     int sd_nr;                   // shared down ranges of kDkSdSteps k-steps
     int rg_blocks, rg_gpi, rg_nr;
     int rd_nr;
@@ -64,27 +83,20 @@ __host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s) {
     return g;
 }
 
-// Scratch in the workspace (after the token tables), 256-byte aligned parts.
+// Scratch in the workspace (after the token tables), 256-byte aligned parts:
+// the intermediates h (B-fragment order) and the per-range ready counts.
 struct DkScratch {
-    size_t gu_s, gu_r, hf_s, hf_r, cnt_s, cnt_r, rdy_s, rdy_r, end;
+    size_t hf_s, hf_r, rdy_s, rdy_r, end;
 };
 __host__ __device__ inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I, int I_s, int nact_max) {
     const DkGeom g = dk_geom(H, I, 16, I_s);
     DkScratch s;
     size_t o = al256(base);
-    s.gu_s = o;
-    o = al256(o + (size_t)2 * I_s * T * 4);
-    s.gu_r = o;
-    o = al256(o + (size_t)nact_max * 2 * I * T * 4);
     s.hf_s = o;
     o = al256(o + (size_t)(I_s / 16) * T * 32);
     s.hf_r = o;
     o = al256(o + (size_t)nact_max * (I / 16) * T * 32);
-    s.cnt_s = o;
-    o = al256(o + (size_t)(I_s / 16) * 4);
-    s.cnt_r = o;
-    o = al256(o + (size_t)nact_max * (I / 16) * 4);
     s.rdy_s = o;
     o = al256(o + (size_t)g.sd_nr * 4);
     s.rdy_r = o;
@@ -93,8 +105,11 @@ __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I
     return s;
 }
 
+// Shared memory.  One gate/up slot per ring stage: a column block holds at
+// least one stage until it completes, so slots never run out before stages.
 struct DkLayout {
-    int bars, hdrs, misc, gamma, act, xs, ring, stage, hs_off, meta_off, total, xs_stride;
+    int bars, hdrs, misc, gamma, act, sfree, scnt, pstate, pend, sacc, xs, ring, stage, hs_off, meta_off, total,
+        xs_stride, slot_floats;
 };
 __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst) {
     DkLayout L;
@@ -110,6 +125,18 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst) {
     o += kMaxT * 4;
     L.act = o;
     o += kMaxE * 4;
+    L.sfree = o;
+    o += kDkMaxStages * 4;
+    L.scnt = o;
+    o += kDkMaxStages * 4;
+    L.pstate = o;
+    o += kDkMaxStages * 4;
+    o = (o + 15) & ~15;
+    L.pend = o;
+    o += kDkMaxStages * (int)sizeof(DPend);
+    L.sacc = o;
+    L.slot_floats = 2 * 32 * T;  // [gate|up][32 columns][T]
+    o += nst * L.slot_floats * 4;
     o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
@@ -140,35 +167,44 @@ struct DkParams {
     float *yout;
     __half *out;
     WsHeader *hdr;
-    float *gu_s, *gu_r;
     uint2 *hf_s, *hf_r;
-    int *cnt_s, *cnt_r, *rdy_s, *rdy_r;
+    int *rdy_s, *rdy_r;
     int nact_max, nstages;
     uint64_t wait_budget_ns;
 };
 
-__device__ __forceinline__ int ld_acquire(const int *p) {
+__device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
     int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-__device__ __forceinline__ void red_add(float *p, float v) { atomicAdd(p, v); }
+
+// misc words: [0] abort flag, [1] last-block flag, [2] consumer stage ticket,
+// [3] producer has registered its last h copy.
 
 // ------------------------------------------------------------- producer --
+// Queue tickets: [shared gate/up blocks][routed gate/up blocks][down items in
+// pairs].  Every gate/up block is dequeued before any down item, and a block's
+// items enter this SM's ring before anything it dequeues later, so h always
+// completes: the down items that wait for it never hold up a gate/up item.
 __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L) {
     const int nst = p.nstages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + nst;
     DHeader *hdrs = reinterpret_cast<DHeader *>(smem + L.hdrs);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + L.misc);
     int *act = reinterpret_cast<int *>(smem + L.act);
+    volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
+    volatile int *pstate = reinterpret_cast<volatile int *>(smem + L.pstate);
+    DPend *pend = reinterpret_cast<DPend *>(smem + L.pend);
     uint8_t *ring = smem + L.ring;
     const uint64_t pol = policy_evict_first();
     const int H = p.H, I = p.I, T = p.T;
     const DkGeom g = dk_geom(H, I, p.S, p.I_s);
     const int NQ = H / 32;
-    const long long nSG = p.sh ? (long long)g.sg_cols * g.sg_nr : 0;
+    const long long nSGb = p.sh ? g.sg_cols : 0;
     const long long nSD = p.sh ? (long long)NQ * g.sd_nr : 0;
     int na = -1;
     auto n_act = [&]() -> int {
@@ -182,129 +218,154 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         }
         return na;
     };
-    uint32_t it = 0;
     bool ok = true;
-    auto wait_slot = [&]() -> int {
+    uint32_t it = 0;
+    // One ring fill: weights (+ the expert's token table); a down item's h
+    // slice is left to the poller, which counts it on the same barrier.
+    auto issue = [&](DHeader &h, const uint8_t *src, uint32_t bytes, const void *meta, const void *hsrc,
+                     uint32_t hs_bytes, const int *rdy, int target) -> bool {
         const int st = (int)(it % nst);
-        if (!mbar_wait_bounded(&empty[st], ((it / nst) & 1) ^ 1, abort_flag, &p.hdr->status, p.wait_budget_ns)) {
+        if (!mbar_wait_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
             ok = false;
-            return -1;
+            return false;
         }
-        return st;
-    };
-    long long u = (long long)atomicAdd(&p.hdr->work_counter, 1u);
-    while (ok) {
-        const long long u_next = (long long)atomicAdd(&p.hdr->work_counter, 1u);
-        DHeader h{};
-        const uint8_t *src = nullptr;
-        uint32_t bytes = 0, meta_bytes = 0, hs_bytes = 0;
-        const void *meta = nullptr;
-        const void *hsrc = nullptr;
-        const int *rdy = nullptr;
-        int rdy_target = 0;
-        long long v = u;
-        bool done = false;
-        if (v < nSG) {
-            h.kind = DK_SG;
-            h.blk = (int)(v / g.sg_nr);
-            h.r = (int)(v % g.sg_nr);
-            h.k0 = h.r * g.sg_nks;
-            h.n = g.sg_nks;
-            src = p.sh + (size_t)h.blk * f16_unit_bytes(H) + (size_t)h.k0 * 1024;
-            bytes = h.n * 1024;
-        } else {
-            v -= nSG;
-            const long long nRG = (long long)n_act() * g.rg_blocks * g.rg_nr;
-            if (v < nRG) {
-                h.kind = DK_RG;
-                h.a = (int)(v / ((long long)g.rg_blocks * g.rg_nr));
-                const int rem = (int)(v % ((long long)g.rg_blocks * g.rg_nr));
-                h.blk = rem / g.rg_nr;
-                h.r = rem % g.rg_nr;
-                h.e = act[h.a];
-                h.k0 = h.r * g.rg_gpi;
-                h.n = min(g.rg_gpi, H / 128 - h.k0);
-                const size_t unit = (size_t)h.e * g.rg_blocks + h.blk;
-                src = p.w4 + unit * w4_unit_bytes(H, p.S) + (size_t)h.k0 * w4_group_bytes(p.S);
-                bytes = h.n * (uint32_t)w4_group_bytes(p.S);
-                meta = p.tables + h.e;
-                meta_bytes = 16 + 16 * T;
-            } else {
-                v -= nRG;
-                if (v < nSD) {
-                    h.kind = DK_SD;
-                    h.r = (int)(v / NQ);
-                    h.blk = (int)(v % NQ);
-                    h.k0 = h.r * kDkSdSteps;
-                    h.n = min(kDkSdSteps, p.I_s / 16 - h.k0);
-                    src = p.sh + shared_pairdown_offset(H, p.I_s) + ((size_t)h.blk * (p.I_s / 16) + h.k0) * 1024;
-                    bytes = h.n * 1024;
-                    hsrc = p.hf_s + (size_t)h.k0 * T * 4;
-                    hs_bytes = h.n * T * 32;
-                    rdy = p.rdy_s + h.r;
-                    rdy_target = h.n;
-                } else {
-                    v -= nSD;
-                    const long long nRD = (long long)n_act() * NQ * g.rd_nr;
-                    if (v < nRD) {
-                        h.kind = DK_RD;
-                        h.a = (int)(v / ((long long)NQ * g.rd_nr));
-                        const int rem = (int)(v % ((long long)NQ * g.rd_nr));
-                        h.r = rem / NQ;
-                        h.blk = rem % NQ;
-                        h.e = act[h.a];
-                        h.k0 = h.r * kDkRdGroups;
-                        h.n = min(kDkRdGroups, I / 128 - h.k0);
-                        src = p.w4 + p.w4_colblk +
-                              (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * kW4ColGroupBytes;
-                        bytes = h.n * kW4ColGroupBytes;
-                        meta = p.tables + h.e;
-                        meta_bytes = 16 + 16 * T;
-                        hsrc = p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4;
-                        hs_bytes = h.n * 8 * T * 32;
-                        rdy = p.rdy_r + h.a * g.rd_nr + h.r;
-                        rdy_target = h.n * 8;
-                    } else {
-                        done = true;
-                    }
-                }
-            }
-        }
-        if (done) break;
-        if ((h.kind == DK_RG || h.kind == DK_RD) && (h.e < 0 || h.e >= p.E)) {  // unusable routing entry
-            u = u_next;
-            continue;
-        }
-        const int st = wait_slot();
-        if (st < 0) break;
+        const uint32_t meta_bytes = meta ? 16 + 16 * T : 0;
         h.seq = (int)it;
         hdrs[st] = h;
         uint8_t *dst = ring + (size_t)st * L.stage;
         mbar_arrive_expect_tx(&full[st], bytes + meta_bytes + hs_bytes);
         bulk_g2s(dst, src, bytes, &full[st], pol);
-        if (meta_bytes) bulk_g2s(dst + L.meta_off, meta, meta_bytes, &full[st], pol);
+        if (meta) bulk_g2s_plain(dst + L.meta_off, meta, meta_bytes, &full[st]);
         if (hs_bytes) {
-            // the intermediate slice must be complete before it is copied
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire(rdy) < rdy_target) {
-                if (*abort_flag || global_timer_ns() - t0 > p.wait_budget_ns) {
-                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-            }
-            if (!ok) break;
-            fence_proxy_async_global();
-            bulk_g2s_plain(dst + L.hs_off, hsrc, hs_bytes, &full[st]);
+            pend[st].src = hsrc;
+            pend[st].rdy = rdy;
+            pend[st].target = target;
+            pend[st].bytes = hs_bytes;
+            __threadfence_block();
+            pstate[st] = 1;
         }
         ++it;
-        u = u_next;
+        return true;
+    };
+    int bseq = 0;
+    auto take_slot = [&](DHeader &h, int nitems) -> bool {
+        const int slot = bseq % nst;
+        if (sfree[slot] != bseq) {  // the slot's previous block is still being completed
+            const uint64_t t0 = global_timer_ns();
+            while (sfree[slot] != bseq) {
+                if (misc[0]) {
+                    ok = false;
+                    return false;
+                }
+                if (global_timer_ns() - t0 > p.wait_budget_ns) {
+                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    misc[0] = 1;
+                    ok = false;
+                    return false;
+                }
+            }
+        }
+        h.slot = slot;
+        h.nitems = nitems;
+        h.bseq = bseq++;
+        return true;
+    };
+    // Issues every item of ticket tk; false once the queue is exhausted (or on failure).
+    auto run_ticket = [&](uint32_t tk) -> bool {
+        if ((long long)tk < nSGb) {
+            DHeader h{};
+            h.kind = DK_SG;
+            h.blk = (int)tk;
+            if (!take_slot(h, g.sg_nr)) return false;
+            for (int r = 0; r < g.sg_nr; ++r) {
+                h.r = r;
+                h.k0 = r * g.sg_nks;
+                h.n = g.sg_nks;
+                const uint8_t *src = p.sh + (size_t)h.blk * f16_unit_bytes(H) + (size_t)h.k0 * 1024;
+                if (!issue(h, src, h.n * 1024, nullptr, nullptr, 0, nullptr, 0)) return false;
+            }
+            return true;
+        }
+        long long v = (long long)tk - nSGb;
+        const int nA = n_act();
+        const long long nRGb = (long long)nA * g.rg_blocks;
+        if (v < nRGb) {
+            DHeader h{};
+            h.kind = DK_RG;
+            h.a = (int)(v / g.rg_blocks);
+            h.blk = (int)(v % g.rg_blocks);
+            h.e = act[h.a];
+            if (h.e < 0 || h.e >= p.E) return true;  // unusable routing entry
+            if (!take_slot(h, g.rg_nr)) return false;
+            const size_t unit = (size_t)h.e * g.rg_blocks + h.blk;
+            for (int r = 0; r < g.rg_nr; ++r) {
+                h.r = r;
+                h.k0 = r * g.rg_gpi;
+                h.n = min(g.rg_gpi, H / 128 - h.k0);
+                const uint8_t *src = p.w4 + unit * w4_unit_bytes(H, p.S) + (size_t)h.k0 * w4_group_bytes(p.S);
+                if (!issue(h, src, h.n * (uint32_t)w4_group_bytes(p.S), p.tables + h.e, nullptr, 0, nullptr, 0))
+                    return false;
+            }
+            return true;
+        }
+        v -= nRGb;
+        const long long nRD = (long long)nA * NQ * g.rd_nr;
+        if (v * kDkDBatch >= nSD + nRD) return false;
+        for (int j = 0; j < kDkDBatch; ++j) {
+            long long d = v * kDkDBatch + j;
+            if (d >= nSD + nRD) break;
+            DHeader h{};
+            if (d < nSD) {
+                h.kind = DK_SD;
+                h.r = (int)(d / NQ);
+                h.blk = (int)(d % NQ);
+                h.k0 = h.r * kDkSdSteps;
+                h.n = min(kDkSdSteps, p.I_s / 16 - h.k0);
+                const uint8_t *src =
+                    p.sh + shared_pairdown_offset(H, p.I_s) + ((size_t)h.blk * (p.I_s / 16) + h.k0) * 1024;
+                if (!issue(h, src, h.n * 1024, nullptr, p.hf_s + (size_t)h.k0 * T * 4, h.n * T * 32,
+                           p.rdy_s + h.r, h.n))
+                    return false;
+            } else {
+                d -= nSD;
+                h.kind = DK_RD;
+                h.a = (int)(d / ((long long)NQ * g.rd_nr));
+                const int rem = (int)(d % ((long long)NQ * g.rd_nr));
+                h.r = rem / NQ;
+                h.blk = rem % NQ;
+                h.e = act[h.a];
+                if (h.e < 0 || h.e >= p.E) continue;  // unusable routing entry
+                h.k0 = h.r * kDkRdGroups;
+                h.n = min(kDkRdGroups, I / 128 - h.k0);
+                const uint8_t *src =
+                    p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * kW4ColGroupBytes;
+                if (!issue(h, src, h.n * kW4ColGroupBytes, p.tables + h.e,
+                           p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4, h.n * 8 * T * 32,
+                           p.rdy_r + h.a * g.rd_nr + h.r, h.n * 8))
+                    return false;
+            }
+        }
+        return true;
+    };
+    // Two tickets in flight: the next dequeue is issued a whole ticket ahead.
+    // The first ticket of each block is its index, so no dequeue waits at start.
+    uint32_t tkA = blockIdx.x;
+    uint32_t tkB = gridDim.x + atomicAdd(&p.hdr->work_counter, 1u);
+    while (true) {
+        if (!run_ticket(tkA)) break;
+        tkA = gridDim.x + atomicAdd(&p.hdr->work_counter, 1u);
+        if (!run_ticket(tkB)) break;
+        tkB = gridDim.x + atomicAdd(&p.hdr->work_counter, 1u);
     }
     if (ok) {
+        __threadfence_block();
+        misc[3] = 1;  // no more h copies to register
         for (int w = 0; w < kConsumerWarps; ++w) {  // one end marker per consumer warp
-            const int st = wait_slot();
-            if (st < 0) break;
+            const int st = (int)(it % nst);
+            if (!mbar_wait_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
+                ok = false;
+                break;
+            }
             DHeader h{};
             h.kind = DK_DONE;
             h.seq = (int)it;
@@ -316,7 +377,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     if (!ok) {
         // bounded wait for the copies in flight before the block may exit
         const uint32_t first = it > (uint32_t)nst ? it - nst : 0;
-        for (uint32_t j = first; j <= it; ++j) {
+        for (uint32_t j = first; j < it; ++j) {
             const int st = (int)(j % nst);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(&full[st], (j / nst) & 1) && global_timer_ns() - t0 < 100000000ull) {
@@ -325,29 +386,86 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     }
 }
 
-// ------------------------------------------------------------ consumers --
-// h = silu(g) * u for token column t and intermediate rows i0 + {2q, 2q+1,
-// 2q+8, 2q+9}, packed as one B fragment (two half2); the g/u sums are reset.
-__device__ __forceinline__ uint2 finalize_frag(float *gsum, float *usum, int T, int i0, int q4, int t) {
-    float hv[4];
-    const int off[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+// --------------------------------------------------------------- poller --
+// Copies each pending down item's h slice into its stage once the slice's
+// ready count reaches the item's target (a relaxed poll of all pending counts
+// at once, then an acquire fence and a proxy fence before the bulk copies).
+__device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
+    const int nst = p.nstages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + L.misc);
+    volatile int *pstate = reinterpret_cast<volatile int *>(smem + L.pstate);
+    const DPend *pend = reinterpret_cast<const DPend *>(smem + L.pend);
+    uint8_t *ring = smem + L.ring;
+    uint64_t t_last = global_timer_ns();
+    while (!misc[0]) {
+        const int fin = misc[3];
+        __threadfence_block();
+        uint32_t m = 0;
+        for (int j = 0; j < nst; ++j) m |= (pstate[j] == 1 ? 1u : 0u) << j;
+        if (!m) {
+            if (fin) return;
+            __nanosleep(100);
+            t_last = global_timer_ns();
+            continue;
+        }
+        __threadfence_block();
+        int v[kDkMaxStages];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const size_t o = (size_t)(i0 + off[j]) * T + t;
-        const float gv = __ldcg(gsum + o), uv = __ldcg(usum + o);
-        __stcg(gsum + o, 0.f);
-        __stcg(usum + o, 0.f);
-        hv[j] = gv / (1.0f + __expf(-gv)) * uv;
+        for (int j = 0; j < kDkMaxStages; ++j) v[j] = ((m >> j) & 1u) ? ld_relaxed_gpu(pend[j].rdy) : 0;
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < kDkMaxStages; ++j) {
+            if (((m >> j) & 1u) && v[j] >= pend[j].target) {
+                if (!any) {
+                    fence_acq_rel_gpu();         // the h stores counted by the ready count
+                    fence_proxy_async_global();  // ... are read through the bulk-copy proxy
+                    any = true;
+                }
+                bulk_g2s_plain(ring + (size_t)j * L.stage + L.hs_off, pend[j].src, pend[j].bytes, &full[j]);
+                pstate[j] = 0;
+            }
+        }
+        if (any) {
+            t_last = global_timer_ns();
+        } else if (global_timer_ns() - t_last > p.wait_budget_ns) {
+            atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            misc[0] = 1;
+            return;
+        }
     }
-    uint2 r;
-    r.x = h2_as_u32(__floats2half2_rn(hv[0], hv[1]));
-    r.y = h2_as_u32(__floats2half2_rn(hv[2], hv[3]));
-    return r;
+}
+
+// ------------------------------------------------------------ consumers --
+// Completes a column block whose partial sums are all in shared-memory slot
+// `sa` ([gate|up][32 columns][T]): h = silu(g) * u for token column t and the
+// block's k-steps kk (rows 16 kk + {2q, 2q+1, 2q+8, 2q+9}), packed as B
+// fragments (two half2) into hf[kk]; the slot is cleared on the way.
+__device__ __forceinline__ void finalize_block(float *sa, int T, int nk, int lane, uint2 *hf, size_t hf_kstride) {
+    const int t = lane >> 2, q4 = lane & 3;
+    if (t >= T) return;
+    const int off[4] = {2 * q4, 2 * q4 + 1, 2 * q4 + 8, 2 * q4 + 9};
+    for (int kk = 0; kk < nk; ++kk) {
+        float hv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            volatile float *gp = sa + (size_t)(16 * kk + off[j]) * T + t;
+            volatile float *up = gp + 32 * T;
+            const float gv = *gp, uv = *up;
+            *gp = 0.f;
+            *up = 0.f;
+            hv[j] = gv / (1.0f + __expf(-gv)) * uv;
+        }
+        uint2 r;
+        r.x = h2_as_u32(__floats2half2_rn(hv[0], hv[1]));
+        r.y = h2_as_u32(__floats2half2_rn(hv[2], hv[3]));
+        hf[(size_t)kk * hf_kstride + (size_t)t * 4 + q4] = r;
+    }
 }
 
 // INT4 draft kernel; MS = S/16 of the packed INT4 units.
 template <int MS>
-__global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
+__global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int nst = p.nstages;
     const DkLayout L = dk_layout(p.T, p.H, nst);
@@ -357,15 +475,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
     uint64_t *empty = full + nst;
     uint64_t *allbar = empty + nst;
     int *misc = reinterpret_cast<int *>(smem + L.misc);
+    int *scnt = reinterpret_cast<int *>(smem + L.scnt);
+    volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
+    float *sacc = reinterpret_cast<float *>(smem + L.sacc);
+    for (int i = threadIdx.x; i < nst * L.slot_floats; i += kDkThreads) sacc[i] = 0.f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(allbar, kConsumerWarps);
-        misc[0] = 0;  // abort flag
-        misc[1] = 0;  // last-block flag
-        misc[2] = 0;  // consumer stage ticket
+        for (int i = 0; i < 16; ++i) misc[i] = 0;
+        int *pstate = reinterpret_cast<int *>(smem + L.pstate);
+        for (int s = 0; s < kDkMaxStages; ++s) {
+            sfree[s] = s;  // slot s first takes block s
+            scnt[s] = 0;
+            pstate[s] = 0;
+        }
         DHeader *hw = reinterpret_cast<DHeader *>(smem + L.hdrs);
         for (int st = 0; st < nst; ++st) hw[st].seq = -1;  // no fill yet (shared memory is not cleared)
         fence_mbar_init();
@@ -373,6 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
     __syncthreads();
     if (warp == kConsumerWarps) {
         if (lane == 0) dk_producer(p, smem, L);
+        return;
+    }
+    if (warp == kConsumerWarps + 1) {
+        if (lane == 0) dk_poller(p, smem, L);
         return;
     }
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
@@ -416,6 +546,30 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
     }
     all_sync();
 
+    // Counts a gate/up item into its column block; the warp that completes the
+    // block finalizes it, frees the slot, and publishes h to the down items.
+    auto gu_done = [&](const DHeader &h, int nk, uint2 *hf, size_t hf_kstride, int *rdy, int amount) {
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) {
+            __threadfence_block();  // this warp's slot sums before the count
+            old = atomicAdd(scnt + h.slot, 1);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != h.nitems - 1) return;
+        __threadfence_block();  // every item's slot sums are visible past the count
+        finalize_block(sacc + (size_t)h.slot * L.slot_floats, T, nk, lane, hf, hf_kstride);
+        __syncwarp();
+        if (lane == 0) {
+            scnt[h.slot] = 0;
+            __threadfence_block();
+            sfree[h.slot] = h.bseq + nst;  // the slot's next block
+        }
+        __threadfence();  // this lane's h fragments before the ready count
+        __syncwarp();
+        if (lane == 0) atomicAdd(rdy, amount);
+    };
+
     constexpr int NTW = 2 * MS;  // INT4 gate+up tiles per k-step
     constexpr int KB = 2 / MS;   // k-steps per 512 B block
     constexpr int BPG = 8 / KB;  // blocks per group
@@ -449,16 +603,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
         }
         if (!got) break;
         const DHeader h = hdrs[st];
+        const uint8_t *stage = ring + (size_t)st * L.stage;
         if (h.kind == DK_DONE) {
             // release it too: with fewer stages than warps the end markers reuse stages
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
             break;
         }
-        const uint8_t *stage = ring + (size_t)st * L.stage;
         const TokTable *tb = reinterpret_cast<const TokTable *>(stage + L.meta_off);
         const uint2 *hsl = reinterpret_cast<const uint2 *>(stage + L.hs_off);
-        int ready_slot = -1;  // completion counter hit by this item (gate/up)
         if (h.kind == DK_SG) {
             // shared gate/up: 16 columns (tiles: gate, up), k-steps [k0, k0+n) of H
             float acc[2][2][4] = {};
@@ -474,32 +627,24 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
                     mma_16816(acc[ks & 1][t], a, b0, b1);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
+            float *sa = sacc + (size_t)h.slot * L.slot_floats;
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                float *base = p.gu_s + (size_t)t * p.I_s * T;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int col = 2 * q4 + hf;
                     if (col < T) {
-                        red_add(base + (size_t)(16 * h.blk + g) * T + col, acc[0][t][hf] + acc[1][t][hf]);
-                        red_add(base + (size_t)(16 * h.blk + g + 8) * T + col, acc[0][t][2 + hf] + acc[1][t][2 + hf]);
+                        atomicAdd(sa + (size_t)(32 * t + g) * T + col, acc[0][t][hf] + acc[1][t][hf]);
+                        atomicAdd(sa + (size_t)(32 * t + g + 8) * T + col, acc[0][t][2 + hf] + acc[1][t][2 + hf]);
                     }
                 }
             }
-            __threadfence();  // this lane's partial sums before the block counter
-            __syncwarp();
-            int old = 0;
-            if (lane == 0) old = atomicAdd(p.cnt_s + h.blk, 1);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == geo.sg_nr - 1) {
-                __threadfence();
-                const int t = lane >> 2;
-                if (t < T)
-                    p.hf_s[((size_t)h.blk * T + t) * 4 + q4] =
-                        finalize_frag(p.gu_s, p.gu_s + (size_t)p.I_s * T, T, 16 * h.blk, q4, t);
-                ready_slot = 0;
-            }
-        } else if (h.kind == DK_RG) {
+            gu_done(h, 1, p.hf_s + (size_t)h.blk * T * 4, 0, p.rdy_s + h.blk / kDkSdSteps, 1);
+            continue;
+        }
+        if (h.kind == DK_RG) {
             // routed INT4 gate/up: slice of S = 16*MS columns, groups [k0, k0+n) of H
             const int n_e = min(max(tb->n, 0), T);
             const bool okx = g < n_e;
@@ -537,41 +682,26 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
                     run[t][3] = fmaf(sb, acc[t][3], run[t][3]);
                 }
             }
-            const int S = 16 * MS;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
+            float *sa = sacc + (size_t)h.slot * L.slot_floats;
 #pragma unroll
             for (int t = 0; t < NTW; ++t) {
-                const int gu = t < MS ? 0 : 1;
-                const int i = h.blk * S + 16 * (t % MS) + g;
-                float *base = p.gu_r + ((size_t)h.a * 2 + gu) * I * T;
+                const int row = 32 * (t < MS ? 0 : 1) + 16 * (t % MS) + g;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int col = 2 * q4 + hf;
                     if (col < n_e) {
-                        red_add(base + (size_t)i * T + col, run[t][hf]);
-                        red_add(base + (size_t)(i + 8) * T + col, run[t][2 + hf]);
+                        atomicAdd(sa + (size_t)row * T + col, run[t][hf]);
+                        atomicAdd(sa + (size_t)(row + 8) * T + col, run[t][2 + hf]);
                     }
                 }
             }
-            __threadfence();
-            __syncwarp();
-            int old = 0;
-            if (lane == 0) old = atomicAdd(p.cnt_r + h.a * (I / 16) + h.blk, 1);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == geo.rg_nr - 1) {
-                __threadfence();
-                const int t = lane >> 2;
-                float *gs = p.gu_r + ((size_t)h.a * 2) * I * T;
-                if (t < T) {
-#pragma unroll
-                    for (int kk = 0; kk < MS; ++kk) {
-                        const int ks = h.blk * MS + kk;
-                        p.hf_r[(((size_t)h.a * (I / 16) + ks) * T + t) * 4 + q4] =
-                            finalize_frag(gs, gs + (size_t)I * T, T, 16 * ks, q4, t);
-                    }
-                }
-                ready_slot = 1;
-            }
-        } else if (h.kind == DK_SD) {
+            gu_done(h, MS, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.blk * MS) * T * 4, (size_t)T * 4,
+                    p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / kDkRdGroups, MS);
+            continue;
+        }
+        if (h.kind == DK_SD) {
             // shared down: output pair blk (32 outputs), k-steps [k0, k0+n) of I_s
             float acc[2][2][4] = {};
             const bool okb = g < T;
@@ -585,6 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
                     mma_16816(acc[ks & 1][q], a, bv.x, bv.y);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
             const int n0 = 32 * h.blk + 4 * g;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -599,8 +731,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
                     atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)col * H + n0), o);
                 }
             }
-        } else if (h.kind == DK_RD) {
-            // routed INT4 down: output pair blk, groups [k0, k0+n) of I
+            continue;
+        }
+        // DK_RD: routed INT4 down: output pair blk, groups [k0, k0+n) of I
+        {
             const int n_e = min(max(tb->n, 0), T);
             const bool okb = g < n_e;
             float run[2][4] = {};
@@ -634,40 +768,29 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const DkParams p) {
                     run[q][3] = fmaf(sb, acc[q][3], run[q][3]);
                 }
             }
-            const int n0 = 32 * h.blk + 4 * g;
-            const int rmax = p.mode == 0 ? T * p.k : T;
+            int row[2] = {-1, -1};
+            float w[2] = {0.f, 0.f};
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int col = 2 * q4 + hf;
                 if (col < n_e) {
-                    const int row = tb->e[col].row;
-                    const float w = tb->e[col].scale;
-                    if (row >= 0 && row < rmax) {
-                        float4 o;
-                        o.x = run[0][hf] * w;
-                        o.y = run[0][2 + hf] * w;
-                        o.z = run[1][hf] * w;
-                        o.w = run[1][2 + hf] * w;
-                        atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)row * H + n0), o);
-                    }
+                    row[hf] = tb->e[col].row;
+                    w[hf] = tb->e[col].scale;
                 }
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (ready_slot >= 0) {
-            // publish: the block's intermediate is complete; reset its counter
-            __threadfence();  // this lane's h fragments and cleared sums first
             __syncwarp();
-            if (lane == 0) {
-                if (ready_slot == 0) {
-                    p.cnt_s[h.blk] = 0;
-                    __threadfence();
-                    atomicAdd(p.rdy_s + h.blk / kDkSdSteps, 1);
-                } else {
-                    p.cnt_r[h.a * (I / 16) + h.blk] = 0;
-                    __threadfence();
-                    atomicAdd(p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / kDkRdGroups, MS);
+            if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
+            const int n0 = 32 * h.blk + 4 * g;
+            const int rmax = p.mode == 0 ? T * p.k : T;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                if (row[hf] >= 0 && row[hf] < rmax) {
+                    float4 o;
+                    o.x = run[0][hf] * w[hf];
+                    o.y = run[0][2 + hf] * w[hf];
+                    o.z = run[1][hf] * w[hf];
+                    o.w = run[1][2 + hf] * w[hf];
+                    atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)row[hf] * H + n0), o);
                 }
             }
         }
@@ -741,15 +864,11 @@ int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaSt
     p.nact_max = e.E < e.T * e.k ? e.E : e.T * e.k;
     uint8_t *ws = reinterpret_cast<uint8_t *>(e.hdr);
     const DkScratch sc = dk_scratch(ws_scratch_base, e.T, e.H, e.I, p.I_s, p.nact_max);
-    p.gu_s = reinterpret_cast<float *>(ws + sc.gu_s);
-    p.gu_r = reinterpret_cast<float *>(ws + sc.gu_r);
     p.hf_s = reinterpret_cast<uint2 *>(ws + sc.hf_s);
     p.hf_r = reinterpret_cast<uint2 *>(ws + sc.hf_r);
-    p.cnt_s = reinterpret_cast<int *>(ws + sc.cnt_s);
-    p.cnt_r = reinterpret_cast<int *>(ws + sc.cnt_r);
     p.rdy_s = reinterpret_cast<int *>(ws + sc.rdy_s);
     p.rdy_r = reinterpret_cast<int *>(ws + sc.rdy_r);
-    int nst = 12;
+    int nst = 12;  // <= kDkMaxStages
     DkLayout L = dk_layout(e.T, e.H, nst);
     while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst);
     if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
@@ -770,7 +889,7 @@ int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaSt
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kDkThreads);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
