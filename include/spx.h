@@ -153,7 +153,7 @@ typedef struct {
  * gamma_t = 1 / (1 + exp(-x_t . w_sgate)).  [P1 Key Contributions 2] */
 typedef struct {
     const void *packed;      /* spx_shared_packed_bytes(H, I_s) bytes, from spx_shared_repack() */
-    const uint16_t *w_sgate; /* nullable */
+    const uint16_t *w_sgate; /* nullable; 16-byte aligned */
     int H, I_s;
 } spx_shared;
 

@@ -165,7 +165,8 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
     st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
     if (st) return st;
-    if (draft_supported(T, w->H, w->I, w->slice_cols, 0)) return launch_draft(p, ws_scratch_base(T, w->H), false, s);
+    if (draft_supported(T, w->H, w->I, w->slice_cols, 0, w->E, k))
+        return launch_draft(p, nullptr, ws_scratch_base(T, w->H), false, s);
     return launch_engine(p, s, false);
 }
 
@@ -201,7 +202,7 @@ static int check_shared(const spx_shared *sh, int H) {
     if (!sh) return SPX_OK;
     if (!sh->packed || sh->H != H || sh->I_s < kF16S || sh->I_s % kF16S) return SPX_ERR_INVALID_ARG;
     if (!al16(sh->packed)) return SPX_ERR_INVALID_ARG;
-    if (sh->w_sgate && (reinterpret_cast<uintptr_t>(sh->w_sgate) & 3)) return SPX_ERR_INVALID_ARG;
+    if (sh->w_sgate && !al16(sh->w_sgate)) return SPX_ERR_INVALID_ARG;
     return SPX_OK;
 }
 
@@ -273,6 +274,52 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     if (st) return st;
     if (reinterpret_cast<uintptr_t>(a->out) & 7) return SPX_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool timed = a->ev_experts_begin || a->ev_experts_end;
+
+    if (a->mode == 0 && draft_supported(T, H, I, S, I_s, E, k)) {
+        // Draft layer: the draft launch routes its few tokens itself (no
+        // routing launch before it); with a router weight a small launch
+        // computes the logits first and the draft launch overlaps it.
+        if (a->w_router) {
+            st = launch_router_logits(reinterpret_cast<const __half *>(a->x),
+                                      reinterpret_cast<const __half *>(a->w_router), T, H, E, a->logits, s);
+            if (st) return st;
+        }
+        DraftRouting rt{};
+        rt.logits = a->logits;
+        rt.renorm = a->renorm;
+        rt.logits_dep = a->w_router ? 1 : 0;
+        rt.topk_ids = a->topk_ids;
+        rt.topk_w = a->topk_w;
+        rt.elb = a->elb;
+        rt.layer = a->layer;
+        rt.counts = a->counts;
+        rt.offsets = a->offsets;
+        rt.sorted_slots = a->sorted_slots;
+        rt.active = a->active;
+        rt.n_active = a->n_active;
+        EngineParams p = base_params(a->x, T, H, a->ws);
+        p.routed = routed;
+        p.S = S;
+        p.E = E;
+        p.I = I;
+        p.k = k;
+        if (a->shared) {
+            p.shared = static_cast<const uint8_t *>(a->shared->packed);
+            p.w_sgate = reinterpret_cast<const __half *>(a->shared->w_sgate);
+            p.I_s = a->shared->I_s;
+        }
+        p.mode = 2;
+        p.yout = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
+        p.out = reinterpret_cast<__half *>(a->out);
+        if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
+            return SPX_ERR_CUDA;
+        st = launch_draft(p, &rt, ws_scratch_base(T, H), a->w_router && !timed, s);
+        if (st) return st;
+        if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
+            return SPX_ERR_CUDA;
+        return SPX_OK;
+    }
 
     RouteParams rp{};
     rp.x = reinterpret_cast<const __half *>(a->x);
@@ -317,13 +364,9 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     p.mode = 2;  // layer: weighted accumulate, last block writes out
     p.yout = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
     p.out = reinterpret_cast<__half *>(a->out);
-    const bool timed = a->ev_experts_begin || a->ev_experts_end;
     if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
         return SPX_ERR_CUDA;
-    if (a->mode == 0 && draft_supported(T, H, I, S, I_s))
-        st = launch_draft(p, ws_scratch_base(T, H), !timed, s);
-    else
-        st = launch_engine(p, s, !timed);
+    st = launch_engine(p, s, !timed);
     if (st) return st;
     if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
         return SPX_ERR_CUDA;

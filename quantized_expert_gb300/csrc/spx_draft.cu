@@ -26,6 +26,7 @@
 // flight, and never waits on h.  Consumer warps take ring stages in order
 // through a shared-memory ticket, so a slow item never stalls the others.
 #include "spx_internal.cuh"
+#include "spx_routing.cuh"
 
 #include <math.h>
 
@@ -36,8 +37,15 @@ constexpr int kDkData = 16896;    // largest item: 4 INT4 groups of 32 columns (
 constexpr int kDkRdGroups = 7;    // INT4 down groups (of 128 rows of I) per RD item
 constexpr int kDkSdSteps = 16;    // k-steps of I_s per SD item
 constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
-constexpr int kDkDBatch = 2;      // down items per queue ticket
-constexpr int kDkThreads = (kConsumerWarps + 2) * 32;  // + producer warp + poller warp
+constexpr int kDkDBatch = 2;      // down items per queue unit
+constexpr int kDkShards = 8;      // independent queue counters (SM b uses shard b % kDkShards)
+constexpr uint32_t kDkSleepNs = 1000;  // longest sleep of a waiting warp inside one try_wait
+// Seven consumer warps, then the producer and the poller: warps share an SM
+// sub-partition by warp index mod 4, so the producer (warp 7) shares its
+// sub-partition with one consumer only and its dependent issue chain is not
+// starved by the dequantising warps.
+constexpr int kDkCons = 7;
+constexpr int kDkThreads = (kDkCons + 2) * 32;
 
 struct __align__(16) DHeader {
     int kind;
@@ -51,7 +59,7 @@ struct __align__(16) DHeader {
     int slot;    // gate/up: shared-memory slot of the column block
     int nitems;  // gate/up: items of the column block
     int bseq;    // gate/up: column-block sequence number on this SM
-    int pad;
+    int hpar;    // down items: phase parity of the stage's h-slice barrier for this fill
 };
 
 // A down item's h slice that the poller copies once the slice is complete.
@@ -86,13 +94,15 @@ __host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s) {
 // Scratch in the workspace (after the token tables), 256-byte aligned parts:
 // the intermediates h (B-fragment order) and the per-range ready counts.
 struct DkScratch {
-    size_t hf_s, hf_r, rdy_s, rdy_r, end;
+    size_t qctr, hf_s, hf_r, rdy_s, rdy_r, end;
 };
 __host__ __device__ inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I, int I_s, int nact_max) {
     const DkGeom g = dk_geom(H, I, 16, I_s);
     DkScratch s;
     size_t o = al256(base);
+    s.qctr = o;  // one 256-byte line per queue shard
+    o += (size_t)kDkShards * 256;
     s.hf_s = o;
     o = al256(o + (size_t)(I_s / 16) * T * 32);
     s.hf_r = o;
@@ -108,14 +118,14 @@ __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I
 // Shared memory.  One gate/up slot per ring stage: a column block holds at
 // least one stage until it completes, so slots never run out before stages.
 struct DkLayout {
-    int bars, hdrs, misc, gamma, act, sfree, scnt, pstate, pend, sacc, xs, ring, stage, hs_off, meta_off, total,
-        xs_stride, slot_floats;
+    int bars, hdrs, misc, gamma, act, sfree, scnt, pstate, pend, sacc, rids, rpw, rrank, rsv, stn, ste, sx, xs, ring,
+        stage, hs_off, total, xs_stride, slot_floats;
 };
-__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst) {
+__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E) {
     DkLayout L;
     int o = 0;
-    L.bars = o;
-    o += (2 * nst + 1) * 8;
+    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier
+    o += (3 * nst + 1) * 8;
     o = (o + 15) & ~15;
     L.hdrs = o;
     o += nst * (int)sizeof(DHeader);
@@ -137,6 +147,22 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst) {
     L.sacc = o;
     L.slot_floats = 2 * 32 * T;  // [gate|up][32 columns][T]
     o += nst * L.slot_floats * 4;
+    // routing of the launch's tokens: selections, counting sort, token tables
+    L.rids = o;
+    o += T * k * 4;
+    L.rpw = o;
+    o += T * k * 4;
+    L.rrank = o;
+    o += T * k * 4;
+    L.rsv = o;  // per selecting warp (one per token): the token's logits
+    o += T * E * 4;
+    L.stn = o;
+    o += nact_max * 4;
+    o = (o + 15) & ~15;
+    L.ste = o;
+    o += nact_max * T * (int)sizeof(TokEntry);
+    L.sx = o;  // [T][H/128] group sums of x (fp32)
+    o += T * (H / 128) * 4;
     o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
@@ -145,8 +171,7 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst) {
     L.ring = o;
     L.hs_off = kDkData;
     const int hs_bytes = ((kDkRdGroups * 8 > kDkSdSteps ? kDkRdGroups * 8 : kDkSdSteps) * T * 32 + 127) & ~127;
-    L.meta_off = kDkData + hs_bytes;
-    L.stage = L.meta_off + ((16 + 16 * T + 127) & ~127);
+    L.stage = kDkData + hs_bytes;
     o += nst * L.stage;
     L.total = o;
     return L;
@@ -164,14 +189,52 @@ struct DkParams {
     const TokTable *tables;
     const __half *x;
     int mode;  // 0: rows of y_sorted, scale 1; 2: weighted into the fp32 accumulator, last block writes out
+    // routing inside the launch (logits != nullptr) and its outputs (block 0)
+    const float *logits;
+    int renorm, logits_dep;
+    int32_t *topk_ids;
+    float *topk_w;
+    uint32_t *elb;
+    int layer;
+    int32_t *counts, *offsets, *sorted_slots, *active_out, *n_active_out;
     float *yout;
     __half *out;
     WsHeader *hdr;
+    uint32_t *qctr;  // queue shard s counter at qctr[64 * s]
     uint2 *hf_s, *hf_r;
     int *rdy_s, *rdy_r;
     int nact_max, nstages;
     uint64_t wait_budget_ns;
 };
+
+// Like mbar_try_wait, but the thread may sleep up to `ns` in the wait (it
+// wakes as soon as the phase completes), so waiting warps leave the issue
+// slots to the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                        int32_t *status, uint64_t budget_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (*abort) return false;
+        if (mbar_try_wait_sleep(bar, parity, kDkSleepNs)) return true;
+        if (global_timer_ns() - t0 > budget_ns) {
+            atomicCAS(status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
 
 __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
     int v;
@@ -182,7 +245,8 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // misc words: [0] abort flag, [1] last-block flag, [2] consumer stage ticket,
-// [3] producer has registered its last h copy.
+// [3] producer has registered its last h copy, [4] routing is in shared
+// memory, [5] number of active experts.
 
 // ------------------------------------------------------------- producer --
 // Queue tickets: [shared gate/up blocks][routed gate/up blocks][down items in
@@ -193,6 +257,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     const int nst = p.nstages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + nst;
+    uint64_t *hfull = empty + nst;
     DHeader *hdrs = reinterpret_cast<DHeader *>(smem + L.hdrs);
     volatile int *misc = reinterpret_cast<volatile int *>(smem + L.misc);
     int *act = reinterpret_cast<int *>(smem + L.act);
@@ -204,39 +269,48 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     const int H = p.H, I = p.I, T = p.T;
     const DkGeom g = dk_geom(H, I, p.S, p.I_s);
     const int NQ = H / 32;
-    const long long nSGb = p.sh ? g.sg_cols : 0;
-    const long long nSD = p.sh ? (long long)NQ * g.sd_nr : 0;
+    const int nSGb = p.sh ? g.sg_cols : 0;
+    const int nSD = p.sh ? NQ * g.sd_nr : 0;
+    bool ok = true;
     int na = -1;
+    // Active experts: the consumer warps route the launch's tokens into shared
+    // memory at start; routed work waits for that (shared gate/up does not).
     auto n_act = [&]() -> int {
         if (na < 0) {
-            griddep_wait();  // routing results of the preceding launch
-            int v = __ldcg(p.n_active);
-            na = v < 0 ? 0 : (v > p.E ? p.E : v);
-            for (int i = 0; i < na; ++i) cp_async4(act + i, p.active + i);
-            cp_async_commit();
-            cp_async_wait_all();
+            const uint64_t t0 = global_timer_ns();
+            while (!misc[4]) {
+                if (misc[0] || global_timer_ns() - t0 > p.wait_budget_ns) {
+                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    misc[0] = 1;
+                    ok = false;
+                    return na = 0;
+                }
+            }
+            __threadfence_block();
+            na = misc[5];
         }
         return na;
     };
-    bool ok = true;
     uint32_t it = 0;
-    // One ring fill: weights (+ the expert's token table); a down item's h
-    // slice is left to the poller, which counts it on the same barrier.
-    auto issue = [&](DHeader &h, const uint8_t *src, uint32_t bytes, const void *meta, const void *hsrc,
-                     uint32_t hs_bytes, const int *rdy, int target) -> bool {
+    uint32_t hpar_bits = 0;  // bit st: phase parity of hfull[st] for the stage's next down fill
+    // One ring fill: weights; a down item's h slice is left to the poller,
+    // which counts it on the same barrier.
+    auto issue = [&](DHeader &h, const uint8_t *src, uint32_t bytes, const void *hsrc, uint32_t hs_bytes,
+                     const int *rdy, int target) -> bool {
         const int st = (int)(it % nst);
-        if (!mbar_wait_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
+        if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
             ok = false;
             return false;
         }
-        const uint32_t meta_bytes = meta ? 16 + 16 * T : 0;
         h.seq = (int)it;
+        h.hpar = (int)((hpar_bits >> st) & 1u);
         hdrs[st] = h;
         uint8_t *dst = ring + (size_t)st * L.stage;
-        mbar_arrive_expect_tx(&full[st], bytes + meta_bytes + hs_bytes);
+        mbar_arrive_expect_tx(&full[st], bytes);
         bulk_g2s(dst, src, bytes, &full[st], pol);
-        if (meta) bulk_g2s_plain(dst + L.meta_off, meta, meta_bytes, &full[st]);
         if (hs_bytes) {
+            mbar_arrive_expect_tx(&hfull[st], hs_bytes);  // completed by the poller's copy
+            hpar_bits ^= 1u << st;
             pend[st].src = hsrc;
             pend[st].rdy = rdy;
             pend[st].target = target;
@@ -270,30 +344,31 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         h.bseq = bseq++;
         return true;
     };
-    // Issues every item of ticket tk; false once the queue is exhausted (or on failure).
-    auto run_ticket = [&](uint32_t tk) -> bool {
-        if ((long long)tk < nSGb) {
+    // Issues every item of queue unit u; false once the queue is exhausted (or on failure).
+    auto run_unit = [&](int u) -> bool {
+        if (u < nSGb) {
             DHeader h{};
             h.kind = DK_SG;
-            h.blk = (int)tk;
+            h.blk = u;
             if (!take_slot(h, g.sg_nr)) return false;
             for (int r = 0; r < g.sg_nr; ++r) {
                 h.r = r;
                 h.k0 = r * g.sg_nks;
                 h.n = g.sg_nks;
                 const uint8_t *src = p.sh + (size_t)h.blk * f16_unit_bytes(H) + (size_t)h.k0 * 1024;
-                if (!issue(h, src, h.n * 1024, nullptr, nullptr, 0, nullptr, 0)) return false;
+                if (!issue(h, src, h.n * 1024, nullptr, 0, nullptr, 0)) return false;
             }
             return true;
         }
-        long long v = (long long)tk - nSGb;
+        int v = u - nSGb;
         const int nA = n_act();
-        const long long nRGb = (long long)nA * g.rg_blocks;
+        if (!ok) return false;
+        const int nRGb = nA * g.rg_blocks;
         if (v < nRGb) {
             DHeader h{};
             h.kind = DK_RG;
-            h.a = (int)(v / g.rg_blocks);
-            h.blk = (int)(v % g.rg_blocks);
+            h.a = v / g.rg_blocks;
+            h.blk = v - h.a * g.rg_blocks;
             h.e = act[h.a];
             if (h.e < 0 || h.e >= p.E) return true;  // unusable routing entry
             if (!take_slot(h, g.rg_nr)) return false;
@@ -303,66 +378,70 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                 h.k0 = r * g.rg_gpi;
                 h.n = min(g.rg_gpi, H / 128 - h.k0);
                 const uint8_t *src = p.w4 + unit * w4_unit_bytes(H, p.S) + (size_t)h.k0 * w4_group_bytes(p.S);
-                if (!issue(h, src, h.n * (uint32_t)w4_group_bytes(p.S), p.tables + h.e, nullptr, 0, nullptr, 0))
-                    return false;
+                if (!issue(h, src, h.n * (uint32_t)w4_group_bytes(p.S), nullptr, 0, nullptr, 0)) return false;
             }
             return true;
         }
         v -= nRGb;
-        const long long nRD = (long long)nA * NQ * g.rd_nr;
+        const int nRD = nA * NQ * g.rd_nr;
         if (v * kDkDBatch >= nSD + nRD) return false;
         for (int j = 0; j < kDkDBatch; ++j) {
-            long long d = v * kDkDBatch + j;
+            int d = v * kDkDBatch + j;
             if (d >= nSD + nRD) break;
             DHeader h{};
             if (d < nSD) {
                 h.kind = DK_SD;
-                h.r = (int)(d / NQ);
-                h.blk = (int)(d % NQ);
+                h.r = d / NQ;
+                h.blk = d - h.r * NQ;
                 h.k0 = h.r * kDkSdSteps;
                 h.n = min(kDkSdSteps, p.I_s / 16 - h.k0);
                 const uint8_t *src =
                     p.sh + shared_pairdown_offset(H, p.I_s) + ((size_t)h.blk * (p.I_s / 16) + h.k0) * 1024;
-                if (!issue(h, src, h.n * 1024, nullptr, p.hf_s + (size_t)h.k0 * T * 4, h.n * T * 32,
-                           p.rdy_s + h.r, h.n))
+                if (!issue(h, src, h.n * 1024, p.hf_s + (size_t)h.k0 * T * 4, h.n * T * 32, p.rdy_s + h.r, h.n))
                     return false;
             } else {
                 d -= nSD;
                 h.kind = DK_RD;
-                h.a = (int)(d / ((long long)NQ * g.rd_nr));
-                const int rem = (int)(d % ((long long)NQ * g.rd_nr));
+                h.a = d / (NQ * g.rd_nr);
+                const int rem = d - h.a * (NQ * g.rd_nr);
                 h.r = rem / NQ;
-                h.blk = rem % NQ;
+                h.blk = rem - h.r * NQ;
                 h.e = act[h.a];
                 if (h.e < 0 || h.e >= p.E) continue;  // unusable routing entry
                 h.k0 = h.r * kDkRdGroups;
                 h.n = min(kDkRdGroups, I / 128 - h.k0);
                 const uint8_t *src =
                     p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * kW4ColGroupBytes;
-                if (!issue(h, src, h.n * kW4ColGroupBytes, p.tables + h.e,
-                           p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4, h.n * 8 * T * 32,
+                if (!issue(h, src, h.n * kW4ColGroupBytes, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4,
+                           h.n * 8 * T * 32,
                            p.rdy_r + h.a * g.rd_nr + h.r, h.n * 8))
                     return false;
             }
         }
         return true;
     };
-    // Two tickets in flight: the next dequeue is issued a whole ticket ahead.
-    // The first ticket of each block is its index, so no dequeue waits at start.
-    uint32_t tkA = blockIdx.x;
-    uint32_t tkB = gridDim.x + atomicAdd(&p.hdr->work_counter, 1u);
+    // The queue is split into kDkShards interleaved shards (unit u belongs to
+    // shard u % kDkShards) so that each counter serves a few SMs only.  Each
+    // block's first ticket in its shard is static; two tickets are in flight,
+    // so the next dequeue is issued a whole ticket ahead.
+    const int shard = (int)(blockIdx.x % kDkShards);
+    const uint32_t nsm = (gridDim.x - shard + kDkShards - 1) / kDkShards;  // blocks on this shard
+    uint32_t *ctr = p.qctr + 64 * shard;
+    uint32_t tkA = blockIdx.x / kDkShards;
+    uint32_t tkB = nsm + atomicAdd(ctr, 1u);
     while (true) {
-        if (!run_ticket(tkA)) break;
-        tkA = gridDim.x + atomicAdd(&p.hdr->work_counter, 1u);
-        if (!run_ticket(tkB)) break;
-        tkB = gridDim.x + atomicAdd(&p.hdr->work_counter, 1u);
+        if (!run_unit((int)tkA * kDkShards + shard)) break;
+        tkA = nsm + atomicAdd(ctr, 1u);
+        if (!run_unit((int)tkB * kDkShards + shard)) break;
+        tkB = nsm + atomicAdd(ctr, 1u);
     }
     if (ok) {
         __threadfence_block();
         misc[3] = 1;  // no more h copies to register
-        for (int w = 0; w < kConsumerWarps; ++w) {  // one end marker per consumer warp
+        for (int w = 0; w < kDkCons; ++w) {  // one end marker per consumer warp
             const int st = (int)(it % nst);
-            if (!mbar_wait_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
+            if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status,
+                                         p.wait_budget_ns)) {
                 ok = false;
                 break;
             }
@@ -392,13 +471,31 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
 // at once, then an acquire fence and a proxy fence before the bulk copies).
 __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
     const int nst = p.nstages;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *hfull = reinterpret_cast<uint64_t *>(smem + L.bars) + 2 * nst;
     volatile int *misc = reinterpret_cast<volatile int *>(smem + L.misc);
     volatile int *pstate = reinterpret_cast<volatile int *>(smem + L.pstate);
     const DPend *pend = reinterpret_cast<const DPend *>(smem + L.pend);
+    const DHeader *hdrs = reinterpret_cast<const DHeader *>(smem + L.hdrs);
     uint8_t *ring = smem + L.ring;
     uint64_t t_last = global_timer_ns();
-    while (!misc[0]) {
+    uint32_t issued = 0, ipar = 0;  // copies in flight (bit j) and their hfull phase parity
+    // On an abort the block exits early: wait (bounded) for this warp's copies first.
+    auto drain = [&]() {
+        for (int j = 0; j < nst; ++j) {
+            if (!((issued >> j) & 1u)) continue;
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&hfull[j], (ipar >> j) & 1u) && global_timer_ns() - t0 < 100000000ull) {
+            }
+        }
+    };
+    while (true) {
+        if (misc[0]) {
+            drain();
+            return;
+        }
+        // forget the copies that have landed
+        for (int j = 0; j < nst; ++j)
+            if (((issued >> j) & 1u) && mbar_try_wait(&hfull[j], (ipar >> j) & 1u)) issued &= ~(1u << j);
         const int fin = misc[3];
         __threadfence_block();
         uint32_t m = 0;
@@ -422,7 +519,9 @@ __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
                     fence_proxy_async_global();  // ... are read through the bulk-copy proxy
                     any = true;
                 }
-                bulk_g2s_plain(ring + (size_t)j * L.stage + L.hs_off, pend[j].src, pend[j].bytes, &full[j]);
+                bulk_g2s_plain(ring + (size_t)j * L.stage + L.hs_off, pend[j].src, pend[j].bytes, &hfull[j]);
+                issued |= 1u << j;
+                ipar = (ipar & ~(1u << j)) | ((uint32_t)hdrs[j].hpar << j);
                 pstate[j] = 0;
             }
         }
@@ -431,6 +530,7 @@ __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
         } else if (global_timer_ns() - t_last > p.wait_budget_ns) {
             atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
             misc[0] = 1;
+            drain();
             return;
         }
     }
@@ -463,17 +563,110 @@ __device__ __forceinline__ void finalize_block(float *sa, int T, int nk, int lan
     }
 }
 
+// Counting sort of the launch's T*k selections by expert, by one warp, into
+// shared memory (no shuffles: T*k is small, every lane scans the slot list):
+// the active experts in ascending order (act), each active expert's token
+// table (ste[a*T + rank]: token s/k, output row s/k, gate weight, in slot
+// order; stn[a] entries).  With out (block 0) the gather arrays of the routing
+// outputs are written as well.  Returns the number of active experts.
+__device__ int route_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane, bool out) {
+    const int E = p.E, k = p.k, T = p.T, n = T * k;
+    const int32_t *ids = reinterpret_cast<const int32_t *>(smem + L.rids);
+    const float *pw = reinterpret_cast<const float *>(smem + L.rpw);
+    int *rank = reinterpret_cast<int *>(smem + L.rrank);
+    int *act = reinterpret_cast<int *>(smem + L.act);
+    int *stn = reinterpret_cast<int *>(smem + L.stn);
+    TokEntry *ste = reinterpret_cast<TokEntry *>(smem + L.ste);
+    int nfirst = 0;
+    for (int s = lane; s < n; s += 32) {  // rank of slot s among the earlier slots of its expert
+        const int e = ids[s];
+        int r = 0;
+        for (int s2 = 0; s2 < s; ++s2) r += (ids[s2] == e);
+        rank[s] = r;
+        nfirst += (r == 0);
+    }
+    const int na = __reduce_add_sync(0xffffffffu, nfirst);
+    __syncwarp();
+    for (int s = lane; s < n; s += 32) {
+        const int e = ids[s], r = rank[s];
+        int a = 0, c = 0, below = 0;  // active experts below e, slots of e, slots of experts below e
+        for (int s2 = 0; s2 < n; ++s2) {
+            const int e2 = ids[s2];
+            a += (e2 < e && rank[s2] == 0);
+            c += (e2 == e);
+            below += (e2 < e);
+        }
+        TokEntry te;
+        te.tok = s / k;
+        te.row = s / k;
+        te.scale = pw[s];
+        te.pad = 0;
+        if (r < T) ste[a * T + r] = te;  // an expert holds at most one slot per token
+        if (r == 0) {
+            act[a] = e;
+            stn[a] = c;
+        }
+        if (out) p.sorted_slots[below + r] = s;
+    }
+    if (out) {
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) {
+            int c = 0, below = 0;
+            for (int s2 = 0; s2 < n; ++s2) {
+                c += (ids[s2] == e);
+                below += (ids[s2] < e);
+            }
+            p.counts[e] = c;
+            p.offsets[e] = below;
+            p.active_out[e] = e < na ? act[e] : -1;
+        }
+        if (lane == 0) {
+            p.offsets[E] = n;
+            *p.n_active_out = na;
+        }
+    }
+    return na;
+}
+
+// The unit call's routing: active experts and their token tables from global
+// memory (written by the preceding launches), into shared memory.
+__device__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane) {
+    const int T = p.T;
+    int *act = reinterpret_cast<int *>(smem + L.act);
+    int *stn = reinterpret_cast<int *>(smem + L.stn);
+    TokEntry *ste = reinterpret_cast<TokEntry *>(smem + L.ste);
+    griddep_wait();
+    const int v = __ldcg(p.n_active);
+    const int na = v < 0 ? 0 : (v > p.nact_max ? p.nact_max : v);
+    for (int a = lane; a < na; a += 32) act[a] = __ldcg(p.active + a);
+    __syncwarp();
+    for (int i = lane; i < na * T; i += 32) {
+        const int a = i / T, j = i - a * T;
+        const int e = act[a];
+        if (e < 0 || e >= p.E) continue;  // skipped by the producer
+        if (j == 0) stn[a] = min(max(__ldcg(&p.tables[e].n), 0), T);
+        TokEntry te;
+        te.tok = __ldcg(&p.tables[e].e[j].tok);
+        te.row = __ldcg(&p.tables[e].e[j].row);
+        te.scale = __ldcg(&p.tables[e].e[j].scale);
+        te.pad = 0;
+        ste[i] = te;
+    }
+    return na;
+}
+
 // INT4 draft kernel; MS = S/16 of the packed INT4 units.
 template <int MS>
 __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int nst = p.nstages;
-    const DkLayout L = dk_layout(p.T, p.H, nst);
+    const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + nst;
-    uint64_t *allbar = empty + nst;
+    uint64_t *hfull = empty + nst;
+    uint64_t *allbar = hfull + nst;
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     int *scnt = reinterpret_cast<int *>(smem + L.scnt);
     volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
@@ -483,8 +676,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&hfull[s], 1);
         }
-        mbar_init(allbar, kConsumerWarps);
+        mbar_init(allbar, kDkCons);
         for (int i = 0; i < 16; ++i) misc[i] = 0;
         int *pstate = reinterpret_cast<int *>(smem + L.pstate);
         for (int s = 0; s < kDkMaxStages; ++s) {
@@ -497,11 +691,11 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == kConsumerWarps) {
+    if (warp == kDkCons) {
         if (lane == 0) dk_producer(p, smem, L);
         return;
     }
-    if (warp == kConsumerWarps + 1) {
+    if (warp == kDkCons + 1) {
         if (lane == 0) dk_poller(p, smem, L);
         return;
     }
@@ -522,29 +716,120 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
     const int ctid = threadIdx.x;
     const DkGeom geo = dk_geom(H, I, p.S, p.I_s);
 
-    for (int idx = ctid; idx < T * (H / 8); idx += kConsumerWarps * 32) {
-        const int t = idx / (H / 8), h8 = idx - t * (H / 8);
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H) + h8);
-        *reinterpret_cast<uint4 *>(xs + (size_t)t * xstr + h8 * 8) = v;
+    // x into shared memory, and its sums over each group of 128 (16 chunks of
+    // 8 = one half-warp, as the stride is a multiple of 16 chunks)
+    float *sxs = reinterpret_cast<float *>(smem + L.sx);
+    for (int base = warp * 32; base < T * (H / 8); base += kDkCons * 32) {
+        const int idx = base + lane;
+        float sum = 0.f;
+        if (idx < T * (H / 8)) {
+            const int t = idx / (H / 8), h8 = idx - t * (H / 8);
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H) + h8);
+            *reinterpret_cast<uint4 *>(xs + (size_t)t * xstr + h8 * 8) = v;
+            const __half2 *vh = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __half22float2(vh[q]);
+                sum += f.x + f.y;
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if ((lane & 15) == 0 && idx < T * (H / 8)) sxs[idx / 16] = sum;  // [t][group]: idx/16 = t*(H/128) + group
     }
-    all_sync();
-    if (p.sh && p.w_sgate) {
-        for (int t = warp; t < T; t += kConsumerWarps) {
-            float z = 0.f;
-            for (int hh = lane * 2; hh < H; hh += 64) {
-                const float2 xv = __half22float2(*reinterpret_cast<const __half2 *>(xs + (size_t)t * xstr + hh));
-                const float2 wv = __half22float2(__ldg(reinterpret_cast<const __half2 *>(p.w_sgate + hh)));
-                z = fmaf(xv.x, wv.x, z);
-                z = fmaf(xv.y, wv.y, z);
+    all_sync();  // x is in shared memory
+    // Routing: warps t < T select token t (every block the same way; block 0
+    // also writes the routing outputs); the last of them builds the token
+    // tables and raises misc[4].  The other warps go straight to the shared
+    // expert's items, which need no routing.
+    auto publish_routing = [&](int na) {
+        __syncwarp();
+        if (lane == 0) {
+            misc[5] = na;
+            __threadfence_block();
+            *reinterpret_cast<volatile int *>(misc + 4) = 1;
+        }
+    };
+    if (p.logits) {
+        if (warp < T) {
+            if (p.logits_dep) griddep_wait();  // the logits come from the preceding launch
+            int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
+            float *rpw = reinterpret_cast<float *>(smem + L.rpw);
+            const int E = p.E, k = p.k;
+            int mine = 0;
+            for (int t = warp; t < T; t += kDkCons, ++mine) {
+                const float *lg = p.logits + (size_t)t * E;
+                select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k, rpw + t * k,
+                             reinterpret_cast<float *>(smem + L.rsv) + t * E);
+                if (blockIdx.x == 0 && lane == 0)
+                    for (int r = 0; r < k; ++r) {
+                        const int e = rids[t * k + r];
+                        p.topk_ids[(size_t)t * k + r] = e;
+                        p.topk_w[(size_t)t * k + r] = rpw[t * k + r];
+                        if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
+                    }
+            }
+            int done = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                done = atomicAdd(misc + 6, mine) + mine;
+            }
+            done = __shfl_sync(0xffffffffu, done, 0);
+            if (done == T) {  // every token is selected: build the tables
+                __threadfence_block();
+                publish_routing(route_tables_warp(p, L, smem, lane, blockIdx.x == 0));
+            }
+        }
+    } else if (warp == 0) {
+        publish_routing(load_tables_warp(p, L, smem, lane));
+    }
+    // shared-expert gate per token (only the shared down items use it; misc[7])
+    if (warp == kDkCons - 1) {
+        if (p.sh && p.w_sgate) {
+            // the gate row in chunks of 2048 halves: a lane's 8 loads of a chunk issued at once
+            float z[kMaxT < 8 ? kMaxT : 8] = {};
+            for (int c0 = 0; c0 < H; c0 += 2048) {
+                uint4 wv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (c0 + i * 256 + lane * 8 < H)
+                        wv[i] = __ldg(reinterpret_cast<const uint4 *>(p.w_sgate + c0) + i * 32 + lane);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    if (t >= T) break;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (c0 + i * 256 + lane * 8 >= H) break;
+                        const uint4 xv =
+                            *reinterpret_cast<const uint4 *>(xs + (size_t)t * xstr + c0 + i * 256 + lane * 8);
+                        const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+                        const __half2 *wh = reinterpret_cast<const __half2 *>(&wv[i]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 a = __half22float2(xh[q]), b = __half22float2(wh[q]);
+                            z[t] = fmaf(a.x, b.x, z[t]);
+                            z[t] = fmaf(a.y, b.y, z[t]);
+                        }
+                    }
+                }
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-            if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-z));
+            for (int t = 0; t < 8; ++t) {
+                if (t >= T) break;
+                float zt = z[t];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) zt += __shfl_xor_sync(0xffffffffu, zt, o);
+                if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-zt));
+            }
+        } else if (lane < T) {
+            gamma[lane] = 1.0f;
         }
-    } else {
-        for (int t = ctid; t < T; t += kConsumerWarps * 32) gamma[t] = 1.0f;
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile int *>(misc + 7) = 1;
+        }
     }
-    all_sync();
 
     // Counts a gate/up item into its column block; the warp that completes the
     // block finalizes it, frees the slot, and publishes h to the down items.
@@ -589,7 +874,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
             const volatile int *seqp = &hdrs[st].seq;
             const uint64_t t0 = global_timer_ns();
             while (true) {
-                if (mbar_try_wait(&full[st], par) && *seqp == idx) {
+                if (mbar_try_wait_sleep(&full[st], par, kDkSleepNs) && *seqp == idx) {
                     got = true;
                     break;
                 }
@@ -610,8 +895,14 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
             if (lane == 0) mbar_arrive(&empty[st]);
             break;
         }
-        const TokTable *tb = reinterpret_cast<const TokTable *>(stage + L.meta_off);
+        const int *stn = reinterpret_cast<const int *>(smem + L.stn);
+        const TokEntry *ste = reinterpret_cast<const TokEntry *>(smem + L.ste);
         const uint2 *hsl = reinterpret_cast<const uint2 *>(stage + L.hs_off);
+        if (h.kind == DK_SD || h.kind == DK_RD) {
+            // the intermediate slice lands after the weights (poller's copy)
+            if (!mbar_wait_sleep_bounded(&hfull[st], (uint32_t)h.hpar, abort_flag, &p.hdr->status, p.wait_budget_ns))
+                break;
+        }
         if (h.kind == DK_SG) {
             // shared gate/up: 16 columns (tiles: gate, up), k-steps [k0, k0+n) of H
             float acc[2][2][4] = {};
@@ -646,16 +937,35 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         }
         if (h.kind == DK_RG) {
             // routed INT4 gate/up: slice of S = 16*MS columns, groups [k0, k0+n) of H
-            const int n_e = min(max(tb->n, 0), T);
+            const int n_e = min(max(stn[h.a], 0), T);
             const bool okx = g < n_e;
-            int tok = okx ? tb->e[g].tok : 0;
+            int tok = okx ? ste[h.a * T + g].tok : 0;
             tok = (tok >= 0 && tok < T) ? tok : 0;
             const __half *xr = xs + tok * xstr + 2 * q4;
+            // Raw codes into the mma: rows m < 8 of a tile get 1024 + q, rows m >= 8
+            // get 1024 + 16 q (the magic-exponent fragments without their fix-up).
+            // Starting each group's accumulator at -1032 (resp. -1152) times the
+            // group's x sum leaves sum (q - 8) x (resp. 16 times it): the zero
+            // point and the x16 fold into the start value and the row scale.
+            const int ng = H / 128;
+            int tc0 = 2 * q4 < n_e ? ste[h.a * T + 2 * q4].tok : 0;
+            int tc1 = 2 * q4 + 1 < n_e ? ste[h.a * T + 2 * q4 + 1].tok : 0;
+            tc0 = (tc0 >= 0 && tc0 < T) ? tc0 : 0;
+            tc1 = (tc1 >= 0 && tc1 < T) ? tc1 : 0;
+            const float *sx0 = sxs + tc0 * ng, *sx1 = sxs + tc1 * ng;
             float run[NTW][4] = {};
             for (int gr = 0; gr < h.n; ++gr) {
                 const uint8_t *gp = stage + (size_t)gr * gbytes;
                 const __half *scp = reinterpret_cast<const __half *>(gp);
-                float acc[NTW][4] = {};
+                const float s0 = sx0[h.k0 + gr], s1 = sx1[h.k0 + gr];
+                float acc[NTW][4];
+#pragma unroll
+                for (int t = 0; t < NTW; ++t) {
+                    acc[t][0] = -1032.f * s0;
+                    acc[t][1] = -1032.f * s1;
+                    acc[t][2] = -1152.f * s0;
+                    acc[t][3] = -1152.f * s1;
+                }
 #pragma unroll
                 for (int ib = 0; ib < BPG; ++ib) {
                     const uint4 v = lds128(gp + 64 * MS + ib * 512 + lane * 16);
@@ -668,14 +978,15 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
 #pragma unroll
                         for (int t = 0; t < NTW; ++t) {
                             uint32_t a[4];
-                            dequant_frag(words[ki * NTW + t], a);
+                            codes_frag(words[ki * NTW + t], a);
                             mma_16816(acc[t], a, b0, b1);
                         }
                     }
                 }
 #pragma unroll
                 for (int t = 0; t < NTW; ++t) {
-                    const float sa = __half2float(scp[t * 16 + g]), sb = __half2float(scp[t * 16 + g + 8]);
+                    const float sa = __half2float(scp[t * 16 + g]);
+                    const float sb = __half2float(scp[t * 16 + g + 8]) * 0.0625f;
                     run[t][0] = fmaf(sa, acc[t][0], run[t][0]);
                     run[t][1] = fmaf(sa, acc[t][1], run[t][1]);
                     run[t][2] = fmaf(sb, acc[t][2], run[t][2]);
@@ -717,6 +1028,16 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
+            if (p.mode != 0 && !*reinterpret_cast<volatile int *>(misc + 7)) {  // the gate (set early on)
+                const uint64_t t0 = global_timer_ns();
+                while (!*reinterpret_cast<volatile int *>(misc + 7) && !*abort_flag) {
+                    if (global_timer_ns() - t0 > p.wait_budget_ns) {
+                        atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                }
+                __threadfence_block();
+            }
             const int n0 = 32 * h.blk + 4 * g;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -735,7 +1056,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         }
         // DK_RD: routed INT4 down: output pair blk, groups [k0, k0+n) of I
         {
-            const int n_e = min(max(tb->n, 0), T);
+            const int n_e = min(max(stn[h.a], 0), T);
             const bool okb = g < n_e;
             float run[2][4] = {};
             for (int gr = 0; gr < h.n; ++gr) {
@@ -774,8 +1095,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
             for (int hf = 0; hf < 2; ++hf) {
                 const int col = 2 * q4 + hf;
                 if (col < n_e) {
-                    row[hf] = tb->e[col].row;
-                    w[hf] = tb->e[col].scale;
+                    row[hf] = ste[h.a * T + col].row;
+                    w[hf] = ste[h.a * T + col].scale;
                 }
             }
             __syncwarp();
@@ -809,7 +1130,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         if (p.mode == 2) {
             const int n4 = T * H / 4;
             float4 *acc4 = reinterpret_cast<float4 *>(p.yout);
-            for (int idx = ctid; idx < n4; idx += kConsumerWarps * 32) {
+            for (int idx = ctid; idx < n4; idx += kDkCons * 32) {
                 const float4 v = __ldcg(acc4 + idx);
                 uint2 o;
                 o.x = h2_as_u32(__floats2half2_rn(v.x, v.y));
@@ -818,12 +1139,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
                 __stcg(acc4 + idx, make_float4(0.f, 0.f, 0.f, 0.f));
             }
         }
-        for (int i = ctid; i < geo.sd_nr; i += kConsumerWarps * 32) p.rdy_s[i] = 0;
-        for (int i = ctid; i < p.nact_max * geo.rd_nr; i += kConsumerWarps * 32) p.rdy_r[i] = 0;
-        if (ctid == 0) {
-            p.hdr->work_counter = 0;
-            p.hdr->done_ticket = 0;
-        }
+        for (int i = ctid; i < geo.sd_nr; i += kDkCons * 32) p.rdy_s[i] = 0;
+        for (int i = ctid; i < p.nact_max * geo.rd_nr; i += kDkCons * 32) p.rdy_r[i] = 0;
+        if (ctid < kDkShards) p.qctr[64 * ctid] = 0;
+        if (ctid == 0) p.hdr->done_ticket = 0;
         __threadfence();
     }
 }
@@ -833,13 +1152,13 @@ size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max
     return dk_scratch(base, T, H, I, I_s, nact_max).end;
 }
 
-bool draft_supported(int T, int H, int I, int S, int I_s) {
+bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k) {
     if (T < 1 || T > 8 || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
-    if (I_s % 16) return false;
-    return dk_layout(T, H, 4).total <= kSmemLimit;
+    if (I_s % 16 || E < 1 || k < 1 || E > kMaxE || T * k > kMaxSlots) return false;
+    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E).total <= kSmemLimit;
 }
 
-int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
+int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
     DkParams p{};
     p.w4 = e.routed;
     p.S = e.S;
@@ -862,15 +1181,30 @@ int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaSt
     p.hdr = e.hdr;
     p.wait_budget_ns = e.wait_budget_ns;
     p.nact_max = e.E < e.T * e.k ? e.E : e.T * e.k;
+    if (rt) {
+        p.logits = rt->logits;
+        p.renorm = rt->renorm;
+        p.logits_dep = rt->logits_dep;
+        p.topk_ids = rt->topk_ids;
+        p.topk_w = rt->topk_w;
+        p.elb = rt->elb;
+        p.layer = rt->layer;
+        p.counts = rt->counts;
+        p.offsets = rt->offsets;
+        p.sorted_slots = rt->sorted_slots;
+        p.active_out = rt->active;
+        p.n_active_out = rt->n_active;
+    }
     uint8_t *ws = reinterpret_cast<uint8_t *>(e.hdr);
     const DkScratch sc = dk_scratch(ws_scratch_base, e.T, e.H, e.I, p.I_s, p.nact_max);
+    p.qctr = reinterpret_cast<uint32_t *>(ws + sc.qctr);
     p.hf_s = reinterpret_cast<uint2 *>(ws + sc.hf_s);
     p.hf_r = reinterpret_cast<uint2 *>(ws + sc.hf_r);
     p.rdy_s = reinterpret_cast<int *>(ws + sc.rdy_s);
     p.rdy_r = reinterpret_cast<int *>(ws + sc.rdy_r);
     int nst = 12;  // <= kDkMaxStages
-    DkLayout L = dk_layout(e.T, e.H, nst);
-    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst);
+    DkLayout L = dk_layout(e.T, e.H, nst, e.k, p.nact_max, e.E);
+    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E);
     if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
     p.nstages = nst;
     const int sms = device_sm_count();

@@ -235,6 +235,18 @@ __device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t (&a)[4]) {
     a[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w8, kLo, kMagic)), sub));
     a[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w8, kHi, kMagic)), mul, add));
 }
+// One packed INT4 word -> the same fragment positions holding the raw
+// magic-exponent values: registers 0 and 2 (rows m < 8) get 1024 + q,
+// registers 1 and 3 (rows m >= 8) get 1024 + 16 q, all exact in fp16.  The
+// caller removes the 1024 (+8 zero point) and the factor 16 after the mma.
+__device__ __forceinline__ void codes_frag(uint32_t w, uint32_t (&a)[4]) {
+    const uint32_t kMagic = 0x64006400u, kLo = 0x000F000Fu, kHi = 0x00F000F0u;
+    const uint32_t w8 = w >> 8;
+    a[0] = lop3_and_or(w, kLo, kMagic);
+    a[1] = lop3_and_or(w, kHi, kMagic);
+    a[2] = lop3_and_or(w8, kLo, kMagic);
+    a[3] = lop3_and_or(w8, kHi, kMagic);
+}
 #endif  // __CUDACC__
 
 
@@ -288,9 +300,23 @@ int route_validate(const uint16_t *x, const uint16_t *w_router, const float *log
 int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl);
 int engine_fits(int T, int H, int fmt, int S);
 int engine_nt(int T);
-bool draft_supported(int T, int H, int I, int S, int I_s);
+// Routing done inside the draft launch (layer call): every block selects the
+// experts of the T tokens from the logits itself; block 0 writes the outputs.
+struct DraftRouting {
+    const float *logits;  // [T][E]
+    int renorm;
+    int logits_dep;       // 1: the logits come from the preceding launch (wait for it)
+    int32_t *topk_ids;
+    float *topk_w;
+    uint32_t *elb;        // nullable
+    int layer;
+    int32_t *counts, *offsets, *sorted_slots, *active, *n_active;
+};
+bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1);
 size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max);
-int launch_draft(const EngineParams &e, size_t ws_scratch_base, bool pdl, cudaStream_t s);
+// rt == nullptr: routing from e.active / e.n_active and the token tables e.tables.
+int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s);
+int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s);
 int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int32_t *active,
                   const int32_t *n_active, int T, int k, int E, TokTable *tables, cudaStream_t s);
 

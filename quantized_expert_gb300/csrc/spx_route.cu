@@ -13,6 +13,7 @@
 // single block selects from the given logits.  Selection: one warp per token,
 // k rounds of a warp-wide (value desc, index asc) arg-max; softmax with expf.
 #include "spx_internal.cuh"
+#include "spx_routing.cuh"
 
 #include <math.h>
 
@@ -148,69 +149,19 @@ __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts
 __device__ void select_block(const RouteParams &p) {
     __shared__ int32_t s_ids[kMaxSlots];
     __shared__ float s_pw[kMaxSlots];
+    __shared__ float s_sv[8][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
-    const int nper = (p.E + 31) >> 5;  // <= 8
     for (int t = warp; t < p.T; t += wpb) {
-        float v[8];
-        bool taken[8];
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane + 32 * j;
-            const bool ok = j < nper && e < p.E;
-            v[j] = ok ? __ldcg(p.logits + (size_t)t * p.E + e) : -INFINITY;
-            taken[j] = !ok;
-            if (ok) m = fmaxf(m, v[j]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (!taken[j]) z += expf(v[j] - m);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        float psel = 0.f;
-        for (int r = 0; r < p.k; ++r) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = lane + 32 * j;
-                if (!taken[j] && (v[j] > bv || (v[j] == bv && e < be))) {
-                    bv = v[j];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j == (be >> 5)) taken[j] = true;
-            }
-            const float pr = expf(bv - m) / z;
-            psel += pr;
-            if (lane == 0) {
-                p.topk_ids[(size_t)t * p.k + r] = be;
-                s_ids[t * p.k + r] = be;
-                s_pw[t * p.k + r] = pr;
-                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * p.E + be, 1u);
-            }
-        }
+        const float *lg = p.logits + (size_t)t * p.E;
+        select_token([&](int e) { return __ldcg(lg + e); }, p.E, p.k, p.renorm, lane, s_ids + t * p.k,
+                     s_pw + t * p.k, s_sv[warp]);
         if (lane == 0)
             for (int r = 0; r < p.k; ++r) {
-                const float wr = p.renorm ? s_pw[t * p.k + r] / psel : s_pw[t * p.k + r];
-                s_pw[t * p.k + r] = wr;
-                p.topk_w[(size_t)t * p.k + r] = wr;
+                const int be = s_ids[t * p.k + r];
+                p.topk_ids[(size_t)t * p.k + r] = be;
+                p.topk_w[(size_t)t * p.k + r] = s_pw[t * p.k + r];
+                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * p.E + be, 1u);
             }
     }
     __syncthreads();
@@ -237,6 +188,48 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
         if (threadIdx.x == 0) p.hdr->route_ticket = 0;
     }
     select_block(p);
+}
+
+// Router product for the draft layer call (T <= 8): one block per expert row,
+// every load of the block issued at once (a lane holds H / 2048 uint4 of the
+// row), fp32 accumulate, warp then block reduction.  A dependent launch may
+// start at once and waits for the logits with griddepcontrol.wait.
+__global__ void __launch_bounds__(256) router_logits_kernel(const __half *x, const __half *wr, int T, int H, int E,
+                                                            float *logits) {
+    griddep_launch_dependents();
+    __shared__ float red[8][8];
+    const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(wr + (size_t)e * H);
+    float acc[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+#pragma unroll 4
+    for (int h8 = threadIdx.x; h8 < H / 8; h8 += 256) {
+        const uint4 w = __ldg(w4 + h8);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            if (t < T) acc[t] = dot8_h(__ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H) + h8), w, acc[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[warp][t] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
+        logits[(size_t)threadIdx.x * E + e] = v;
+    }
+}
+
+int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s) {
+    if (T < 1 || T > 8) return SPX_ERR_UNSUPPORTED;
+    router_logits_kernel<<<E, 256, 0, s>>>(x, wr, T, H, E, logits);
+    return record_launch(cudaGetLastError());
 }
 
 __global__ void __launch_bounds__(256) elb_kernel(uint32_t *elb, int E, int layer, const int32_t *ids, int n) {
