@@ -905,17 +905,23 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         }
         if (h.kind == DK_SG) {
             // shared gate/up: 16 columns (tiles: gate, up), k-steps [k0, k0+n) of H
+            // two accumulator sets (even / odd k-steps) in registers: the k loop
+            // is unrolled by two so that no accumulator index is dynamic
             float acc[2][2][4] = {};
             const bool okx = g < T;
             const __half *xr = xs + (okx ? g : 0) * xstr + 2 * q4;
-            for (int ks = 0; ks < h.n; ++ks) {
-                const uint32_t b0 = okx ? lds32(xr + 16 * (h.k0 + ks)) : 0u;
-                const uint32_t b1 = okx ? lds32(xr + 16 * (h.k0 + ks) + 8) : 0u;
+            for (int ks = 0; ks < h.n; ks += 2) {
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const uint4 v = lds128(stage + ((size_t)ks * 2 + t) * 512 + lane * 16);
-                    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
-                    mma_16816(acc[ks & 1][t], a, b0, b1);
+                for (int u = 0; u < 2; ++u) {
+                    if (u == 1 && ks + 1 >= h.n) break;
+                    const uint32_t b0 = okx ? lds32(xr + 16 * (h.k0 + ks + u)) : 0u;
+                    const uint32_t b1 = okx ? lds32(xr + 16 * (h.k0 + ks + u) + 8) : 0u;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint4 v = lds128(stage + ((size_t)(ks + u) * 2 + t) * 512 + lane * 16);
+                        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+                        mma_16816(acc[u][t], a, b0, b1);
+                    }
                 }
             }
             __syncwarp();
@@ -1014,16 +1020,20 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
         }
         if (h.kind == DK_SD) {
             // shared down: output pair blk (32 outputs), k-steps [k0, k0+n) of I_s
-            float acc[2][2][4] = {};
+            float acc[2][2][4] = {};  // even / odd k-steps, as in the gate/up items
             const bool okb = g < T;
-            for (int ks = 0; ks < h.n; ++ks) {
-                uint2 bv = make_uint2(0u, 0u);
-                if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ks * T + g) * 4 + q4);
+            for (int ks = 0; ks < h.n; ks += 2) {
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint4 v = lds128(stage + ((size_t)ks * 2 + q) * 512 + lane * 16);
-                    const uint32_t a[4] = {v.x, v.y, v.z, v.w};
-                    mma_16816(acc[ks & 1][q], a, bv.x, bv.y);
+                for (int u = 0; u < 2; ++u) {
+                    if (u == 1 && ks + 1 >= h.n) break;
+                    uint2 bv = make_uint2(0u, 0u);
+                    if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)(ks + u) * T + g) * 4 + q4);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const uint4 v = lds128(stage + ((size_t)(ks + u) * 2 + q) * 512 + lane * 16);
+                        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+                        mma_16816(acc[u][q], a, bv.x, bv.y);
+                    }
                 }
             }
             __syncwarp();
@@ -1118,6 +1128,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) 
     }
 
     // completion ticket; the last block writes the fp16 output and resets
+    __threadfence();  // this thread's output additions, before the block counts as done
     all_sync();
     if (ctid == 0) {
         __threadfence();
