@@ -109,7 +109,10 @@ struct Stream {
     const uint8_t *base;
 };
 
-__device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLayout &L, int G, int nsg) {
+// G (groups) is a template parameter so that the per-group stream state
+// stays in registers (a loop over a runtime count would index it in memory).
+template <int G>
+__device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLayout &L, int nsg) {
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + G * nsg;
     ChunkHeader *hdrs = reinterpret_cast<ChunkHeader *>(smem + L.hdrs);
@@ -145,7 +148,8 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     };
     auto valid_unit = [&](int u) -> bool { return u < n_sh || u < total_units(); };
 
-    Stream s[2];
+    Stream s[G];
+#pragma unroll
     for (int g = 0; g < G; ++g) {
         s[g].u = -1;
         s[g].it = 0;
@@ -158,6 +162,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     bool aborted = false;
     while (true) {
         bool all_done = true, progressed = false;
+#pragma unroll
         for (int g = 0; g < G; ++g) {
             Stream &S_ = s[g];
             if (S_.done) continue;
@@ -269,6 +274,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     // Drain: every issued copy has been waited on by the consumers unless the
     // block aborted; in that case wait (bounded) for the copies in flight.
     if (aborted) {
+#pragma unroll
         for (int g = 0; g < G; ++g) {
             const uint32_t first = s[g].it > (uint32_t)nsg ? s[g].it - nsg : 0;
             for (uint32_t j = first; j < s[g].it; ++j) {
@@ -327,7 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     }
     __syncthreads();
     if (warp == kConsumerWarps) {
-        if (lane == 0) producer_loop(p, smem, L, G, nsg);
+        if (lane == 0) {
+            if (G == 2)
+                producer_loop<2>(p, smem, L, nsg);
+            else
+                producer_loop<1>(p, smem, L, nsg);
+        }
         return;
     }
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
