@@ -50,7 +50,8 @@ struct __align__(16) ChunkHeader {
 };
 
 constexpr int kMetaBytes = 1152;                  // >= kTableBytes, multiple of 128
-constexpr int kStageBytes = kChunk + kMetaBytes;  // data + token table
+// A stage holds one chunk of weights (kChunk or 2 kChunk bytes, chosen per
+// launch) followed by the token table area.
 static_assert(kTableBytes <= (size_t)kMetaBytes, "table fits the stage meta area");
 constexpr int kHsStride = 40;                     // halves per intermediate row (32 + 8 pad)
 
@@ -64,7 +65,8 @@ struct SmemLayout {
 // red: per group, per warp, [2*smax][npad] fp32 partial sums of gate/up;
 // hs : per group, [npad][kHsStride] fp16 intermediate; sd: per group, 2 x [H]
 // fp16 down-scale rows (INT4 only, double-buffered by unit parity).
-__host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg) {
+__host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg,
+                                                  int chunk) {
     SmemLayout L;
     const int nst = G * nsg;
     int o = 0;
@@ -91,7 +93,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     o += T * (H + 8) * 2;
     o = (o + 127) & ~127;
     L.ring = o;
-    o += nst * kStageBytes;
+    o += nst * (chunk + kMetaBytes);
     L.total = o;
     return L;
 }
@@ -156,7 +158,8 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         s[g].done = false;
         dequeue(s[g].next_u, s[g].next_e);
     }
-    const int W4GPC = kChunk / (int)w4_group_bytes(p.S);  // whole INT4 groups per chunk
+    const int chunk = p.chunk;
+    const int W4GPC = chunk / (int)w4_group_bytes(p.S);  // whole INT4 groups per chunk
     long long t_prog = clock64();
     const long long budget = (long long)p.wait_budget_ns * 2;  // cycles at ~2 GHz
     bool aborted = false;
@@ -222,7 +225,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 } else {
                     h.kind = HK_DOWN;
                     h.b0 = S_.b;
-                    h.nb = min(kChunk / 512, nbd - S_.b);
+                    h.nb = min(chunk / 512, nbd - S_.b);
                     src = S_.base + w4_gu_bytes(H, S) + (size_t)S_.b * 512;
                     bytes = h.nb * 512;
                     S_.b += h.nb;
@@ -233,7 +236,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 if (S_.phase == 0) {
                     h.kind = HK_GU;
                     h.b0 = S_.b;
-                    h.nb = min(kChunk / 1024, nbg - S_.b);
+                    h.nb = min(chunk / 1024, nbg - S_.b);
                     h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == nbg ? HF_GU_LAST : 0);
                     src = S_.base + (size_t)S_.b * 1024;
                     bytes = h.nb * 1024;
@@ -242,7 +245,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 } else {
                     h.kind = HK_DOWN;
                     h.b0 = S_.b;
-                    h.nb = min(kChunk / 1024, nbd - S_.b);
+                    h.nb = min(chunk / 1024, nbd - S_.b);
                     src = S_.base + f16_gu_bytes(H) + (size_t)S_.b * 1024;
                     bytes = h.nb * 1024;
                     S_.b += h.nb;
@@ -254,10 +257,10 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 meta_bytes = (uint32_t)(16 + 16 * p.T);  // table header + up to T entries
             }
             hdrs[st] = h;
-            uint8_t *dst = ring + (size_t)st * kStageBytes;
+            uint8_t *dst = ring + (size_t)st * (chunk + kMetaBytes);
             mbar_arrive_expect_tx(&full[st], bytes + meta_bytes);
             bulk_g2s(dst, src, bytes, &full[st], pol);
-            if (meta_bytes) bulk_g2s(dst + kChunk, meta, meta_bytes, &full[st], pol);
+            if (meta_bytes) bulk_g2s(dst + chunk, meta, meta_bytes, &full[st], pol);
             S_.it++;
             progressed = true;
         }
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     const int smax = has_w4 ? p.S : kF16S;
     const int G = p.groups, nsg = p.nstages;
     const int gwarps = kConsumerWarps / G;
-    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg);
+    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg, p.chunk);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -404,14 +407,14 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         if (!mbar_wait_bounded(&full[st], (it / nsg) & 1, abort_flag, &p.hdr->status, p.wait_budget_ns)) break;
         const ChunkHeader h = hdrs[st];
         if (h.kind == HK_DONE) break;
-        const uint8_t *stage = ring + (size_t)st * kStageBytes;
+        const uint8_t *stage = ring + (size_t)st * (p.chunk + kMetaBytes);
         if (h.flags & HF_UNIT_START) {
             // unit setup from the header and the token table in the meta area
             u_fmt = (h.shared || RFMT == FMT_F16) ? FMT_F16 : FMT_W4;
             u_S = h.shared ? kF16S : p.S;
             u_e = h.e;
             u_i0 = h.i0;
-            const TokTable *tb = reinterpret_cast<const TokTable *>(stage + kChunk);
+            const TokTable *tb = reinterpret_cast<const TokTable *>(stage + p.chunk);
             int n = h.shared ? p.T : tb->n;
             if (n < 0 || n > p.T || n > 8 * NT) n = 0;
             n_e = n;
@@ -761,15 +764,20 @@ int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int
 // ------------------------------------------------------------ launching --
 int engine_nt(int T) { return T <= 8 ? 1 : (T <= 24 ? 3 : 8); }
 
-// Geometry: two consumer groups when each can get at least two stages,
-// otherwise one group; at most 12 stages in all.
-static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes) {
-    for (G = 2; G >= 1; --G) {
-        for (nsg = 12 / G; nsg >= 2; --nsg) {
-            const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg);
-            if (L.total <= kSmemLimit) {
-                bytes = L.total;
-                return true;
+// Geometry: chunks of 2 kChunk bytes when at least four stages still fit
+// (half the producer steps per byte), else kChunk; two consumer groups when
+// each can get at least two stages, otherwise one group; at most 12 stages.
+static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes, int &chunk) {
+    for (chunk = 2 * kChunk; chunk >= kChunk; chunk /= 2) {
+        const int min_stages = chunk > kChunk ? 4 : 2;
+        for (G = 2; G >= 1; --G) {
+            for (nsg = 12 / G; nsg >= 2; --nsg) {
+                if (G * nsg < min_stages) continue;
+                const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk);
+                if (L.total <= kSmemLimit) {
+                    bytes = L.total;
+                    return true;
+                }
             }
         }
     }
@@ -783,10 +791,11 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     if (sms <= 0) return SPX_ERR_CUDA;
     const bool w4 = RFMT == FMT_W4 && p.routed_enabled;
     const int smax = w4 ? p.S : kF16S;
-    int G, nsg, bytes;
-    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes)) return SPX_ERR_UNSUPPORTED;
+    int G, nsg, bytes, chunk;
+    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk)) return SPX_ERR_UNSUPPORTED;
     p.groups = G;
     p.nstages = nsg;
+    p.chunk = chunk;
     static int configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
@@ -830,8 +839,8 @@ int engine_fits(int T, int H, int fmt, int S) {
     const int npad = 8 * ((T + 7) / 8);
     const bool w4 = fmt == FMT_W4;
     if (w4 && S == 32 && engine_nt(T) == 8) return 0;
-    int G, nsg, bytes;
-    return choose_geometry(T, H, npad, w4 ? S : kF16S, w4, G, nsg, bytes) ? 1 : 0;
+    int G, nsg, bytes, chunk;
+    return choose_geometry(T, H, npad, w4 ? S : kF16S, w4, G, nsg, bytes, chunk) ? 1 : 0;
 }
 
 }  // namespace spx

@@ -290,6 +290,7 @@ struct EngineParams {
     // geometry (set by the launcher)
     int groups;    // consumer warp groups (1 or 2)
     int nstages;   // ring stages per group
+    int chunk;     // weight bytes per stage
     int npad;      // token columns of the shared scratch: 8 * ceil(T / 8)
     uint64_t wait_budget_ns;
 };
