@@ -311,9 +311,12 @@ def run_mine(args):
     v_us = statistics.median(v_ms) * 1e3
     kd_us = statistics.mean(kd_ms) * 1e3
     kv_us = statistics.mean(kv_ms) * 1e3
-    # expert-launch bytes: the layer's bytes minus what the routing launch reads
+    # expert-launch bytes.  Verify: the layer's bytes minus what the routing
+    # launch reads.  Draft: the draft launch routes its token itself, so it
+    # reads everything the layer reads (a router product, where there is one,
+    # runs in a launch of its own before it).
     kv_bytes = v_bytes - Tv * s.E * 4 - (s.E * s.H * 2 if s.logits == "router" else 0)
-    kd_bytes = d_bytes - Td * s.E * 4 - (s.E * s.H * 2 if s.logits == "router" else 0)
+    kd_bytes = d_bytes - (s.E * s.H * 2 if s.logits == "router" else 0)
     peak, peak_src = measured_peaks()
 
     # e2e: host buffers through the public API, copies inside the timed region
@@ -362,19 +365,21 @@ def run_mine(args):
                    "verify_frac": round(v_bytes / (v_us * 1e-6) / 1e9 / peak, 3),
                    "verify_tokens_per_s": round(Tv / (v_us * 1e-6), 1),
                    "draft_bytes": int(d_bytes), "verify_bytes": int(v_bytes)},
-        "roofline": {"bound": "hbm", "kernel": "engine_kernel<1,3> (verify expert launch)",
+        "roofline": {"bound": "hbm", "kernel": "engine_kernel<1,1,3> (verify expert launch, FP16 experts)",
                      "achieved": round(kv_bytes / (kv_us * 1e-6) / 1e9, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(kv_bytes / (kv_us * 1e-6) / 1e9 / peak, 3), "traffic": None,
                      "launch_us": round(kv_us, 2), "bytes_per_launch": int(kv_bytes)},
-        "draft_roofline": {"bound": "hbm", "kernel": "engine_kernel<2,1> (draft expert launch)",
+        "draft_roofline": {"bound": "hbm", "kernel": "draft_kernel<2> (draft launch: routing + INT4 experts)",
                            "achieved": round(kd_bytes / (kd_us * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
                            "frac": round(kd_bytes / (kd_us * 1e-6) / 1e9 / peak, 3), "launch_us": round(kd_us, 2),
                            "bytes_per_launch": int(kd_bytes)},
         "clocks": clocks,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 4 * args.steps,
+        # per step: the draft launch (+ the router product when the layer has a
+        # router weight), the verify routing launch, the verify expert launch
+        "gpu_launches": (3 + (1 if s.logits == "router" else 0)) * args.steps,
     }
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s)
