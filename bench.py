@@ -436,6 +436,111 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cycle(args):
+    """The 26-layer draft-then-verify cycle: K draft steps at T = 1 through every
+    layer (Expert Lookahead Buffer counters on), then one verify pass at T = K+1;
+    independent weights per layer.  Prints one JSON line: device us per cycle,
+    achieved GB/s of the cycle's algorithmic bytes, ELB distinct experts per layer."""
+    import torch
+    from quantized_expert_gb300 import build as B, spx
+    import oracle
+    B.build()
+    spx.load()
+    s = W.CONFIGS["deepseek_v2_lite_x26"]
+    L, K, E, k, Tv = s.layers, s.K, s.E, s.k, s.T_verify
+    lays = [make_weight_set(s, l, torch, spx) for l in range(L)]
+
+    def f16dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
+    xd = {(st, l): f16dev(W.gen_x(s, 1, layer=l, step=st)) for st in range(1, K + 1) for l in range(L)}
+    lgd = {(st, l): torch.from_numpy(W.draft_logits(s, l, st)).cuda() for st in range(1, K + 1) for l in range(L)}
+    xv = [f16dev(W.gen_x(s, Tv, layer=l, step=K + 1, which=1)) for l in range(L)]
+    lgv = [torch.from_numpy(W.verify_logits(s, l)).cuda() for l in range(L)]
+    # algorithmic bytes of one cycle (unique experts of every call, from the drawn logits)
+    cyc_bytes = 0
+    for l in range(L):
+        for st in range(1, K + 1):
+            ids, _ = oracle.route_topk(W.draft_logits(s, l, st).astype(np.float64), k, s.renorm)
+            cyc_bytes += layer_bytes(s, "draft", 1, len(set(ids.reshape(-1).tolist())))
+        ids, _ = oracle.route_topk(W.verify_logits(s, l).astype(np.float64), k, s.renorm)
+        cyc_bytes += layer_bytes(s, "verify", Tv, len(set(ids.reshape(-1).tolist())))
+    elb = torch.zeros(L, E, dtype=torch.int32, device="cuda")
+    ws_d, ws_v = spx.new_workspace(1, s.H, s.I, E, k, s.I_s), spx.new_workspace(Tv, s.H, s.I, E, k, s.I_s)
+    r_d, r_v = spx.Routing.empty(1, E, k), spx.Routing.empty(Tv, E, k)
+    out_d = torch.empty(1, s.H, dtype=torch.float16, device="cuda")
+    out_v = torch.empty(Tv, s.H, dtype=torch.float16, device="cuda")
+    draft_args = [[spx.layer_args(0, xd[(st, l)], E, k, s.renorm, lgd[(st, l)], r_d, out_d, ws_d,
+                                  w4=lays[l]["w4"], shared=lays[l]["shared"], elb=elb, layer=l)
+                   for l in range(L)] for st in range(1, K + 1)]
+    verify_args = [spx.layer_args(1, xv[l], E, k, s.renorm, lgv[l], r_v, out_v, ws_v, f16=lays[l]["f16"],
+                                  shared=lays[l]["shared"]) for l in range(L)]
+    stream = torch.cuda.Stream()
+
+    def cycle():
+        spx.spx_elb_reset(elb, stream)
+        for st in range(K):
+            for l in range(L):
+                spx.spx_moe_layer(draft_args[st][l][0], stream)
+        for l in range(L):
+            spx.spx_moe_layer(verify_args[l][0], stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            cycle()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(1, args.steps)
+        e0.record(stream)
+        for _ in range(n):
+            cycle()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    got = elb.cpu().numpy()
+    distinct = (got > 0).sum(1)
+    peak, peak_src = measured_peaks()
+    gbs = cyc_bytes / (us * 1e-6) / 1e9
+    line = {"metric": "26-layer draft-then-verify cycle, device us per cycle", "value": round(us, 1), "unit": "us",
+            "higher_is_better": False, "n_gpus": 1, "steps": n, "warmup": max(1, args.warmup),
+            "data": "synthetic (independent seeded weights per layer; drawn Zipf(1.1) router logits)",
+            "config": {"workload": f"{s.name}: {K} draft steps (T=1) x {L} layers + verify (T={Tv}) x {L} layers",
+                       "layer_calls_per_cycle": (K + 1) * L},
+            "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3), "peak": peak,
+            "peak_source": peak_src, "bytes_per_cycle": int(cyc_bytes),
+            "elb_distinct_experts_per_layer": {"mean": round(float(distinct.mean()), 2), "min": int(distinct.min()),
+                                               "max": int(distinct.max())},
+            "elb_calls_per_layer": int(got.sum(1)[0]) // k}
+    print(json.dumps(line), flush=True)
+
+
+def run_loop(args):
+    """Profiling driver: --loop-n layer calls of one mode on --sets weight sets,
+    no timing (the command that ncu captures wrap)."""
+    import torch
+    from quantized_expert_gb300 import build as B, spx
+    B.build()
+    spx.load()
+    s = W.CONFIGS[args.config]
+    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
+    inp = make_inputs(s, 0)
+    draft = args.loop == "draft"
+    T = s.T_draft if draft else s.T_verify
+    xk, lk = ("x_d", "lg_d") if draft else ("x_v", "lg_v")
+    x = torch.from_numpy(np.ascontiguousarray(inp[xk]).view(np.float16)).cuda()
+    lg = torch.from_numpy(inp[lk]).cuda() if lk in inp else torch.empty(T, s.E, device="cuda")
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    r = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    keep = [spx.layer_args(0 if draft else 1, x, s.E, s.k, s.renorm, lg, r, out, ws,
+                           w4=st["w4"] if draft else None, f16=None if draft else st["f16"], shared=st["shared"],
+                           w_router=st["w_router"]) for st in sets]
+    for i in range(args.loop_n):
+        spx.spx_moe_layer(keep[i % len(keep)][0])
+    torch.cuda.synchronize()
+    assert spx.spx_workspace_status(ws) == 0
+    print(json.dumps({"loop": args.loop, "config": s.name, "calls": args.loop_n}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,9 +550,16 @@ def main():
     ap.add_argument("--config", default="deepseek_v2_lite", choices=sorted(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--sets", type=int, default=NSETS, help="rotated weight sets (8 defeat L2)")
+    ap.add_argument("--loop", choices=["draft", "verify"], help="profiling driver: layer calls only, no timing")
+    ap.add_argument("--cycle", action="store_true", help="the 26-layer draft-then-verify cycle (prints its own line)")
+    ap.add_argument("--loop-n", type=int, default=12)
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
-    if args.impl == "reference":
+    if args.loop:
+        run_loop(args)
+    elif args.cycle:
+        run_cycle(args)
+    elif args.impl == "reference":
         if args.steps > 3:
             args.steps = 3
         if args.warmup > 1:
