@@ -53,6 +53,8 @@ constexpr int kMetaBytes = 1152;                  // >= kTableBytes, multiple of
 // A stage holds one chunk of weights (kChunk or 2 kChunk bytes, chosen per
 // launch) followed by the token table area.
 static_assert(kTableBytes <= (size_t)kMetaBytes, "table fits the stage meta area");
+// The meta area a launch needs: the table header and T entries, in 128-byte units.
+__host__ __device__ inline int meta_bytes_for(int T) { return (16 + 16 * T + 127) & ~127; }
 constexpr int kHsStride = 40;                     // halves per intermediate row (32 + 8 pad)
 
 struct SmemLayout {
@@ -62,7 +64,7 @@ struct SmemLayout {
 };
 
 // G groups of 8/G consumer warps; nsg stages per group.
-// red: per group, per warp, [2*smax][npad] fp32 partial sums of gate/up;
+// red: per group, [2*smax][npad] fp32 gate/up sums (the group's warps add into it);
 // hs : per group, [npad][kHsStride] fp16 intermediate; sd: per group, 2 x [H]
 // fp16 down-scale rows (INT4 only, double-buffered by unit parity).
 __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg,
@@ -81,7 +83,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     o += 64;
     L.red = o;
     L.red_rs = npad;
-    o += kConsumerWarps * 2 * smax * npad * 4;
+    o += G * 2 * smax * npad * 4;
     L.hs = o;
     o += G * npad * kHsStride * 2;
     o = (o + 15) & ~15;
@@ -93,7 +95,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     o += T * (H + 8) * 2;
     o = (o + 127) & ~127;
     L.ring = o;
-    o += nst * (chunk + kMetaBytes);
+    o += nst * (chunk + meta_bytes_for(T));
     L.total = o;
     return L;
 }
@@ -257,7 +259,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 meta_bytes = (uint32_t)(16 + 16 * p.T);  // table header + up to T entries
             }
             hdrs[st] = h;
-            uint8_t *dst = ring + (size_t)st * (chunk + kMetaBytes);
+            uint8_t *dst = ring + (size_t)st * (chunk + meta_bytes_for(p.T));
             mbar_arrive_expect_tx(&full[st], bytes + meta_bytes);
             bulk_g2s(dst, src, bytes, &full[st], pol);
             if (meta_bytes) bulk_g2s(dst + chunk, meta, meta_bytes, &full[st], pol);
@@ -353,19 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     const uint8_t *ring = smem + L.ring;
     float *gamma = reinterpret_cast<float *>(smem + L.gamma);
     const int xs_stride = L.xs_stride, rs = L.red_rs, npad = p.npad;
-    float *red = reinterpret_cast<float *>(smem + L.red) + (size_t)grp_id * gwarps * 2 * smax * rs;
+    float *red = reinterpret_cast<float *>(smem + L.red) + (size_t)grp_id * 2 * smax * rs;
     __half *hs = reinterpret_cast<__half *>(smem + L.hs) + (size_t)grp_id * npad * kHsStride;
     __half *sdg = reinterpret_cast<__half *>(smem + L.sd) + (size_t)grp_id * 2 * p.H;
     __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int ctid = threadIdx.x;  // 0..255
     const int H = p.H;
 
-    // stage activations [T][H] -> shared rows of H+8 halves
+    // stage activations [T][H] -> shared rows of H+8 halves; zero the groups'
+    // gate/up reduction buffers
     for (int idx = ctid; idx < p.T * (H / 8); idx += kConsumerWarps * 32) {
         const int t = idx / (H / 8), h8 = idx - t * (H / 8);
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H) + h8);
         *reinterpret_cast<uint4 *>(xs + (size_t)t * xs_stride + h8 * 8) = v;
     }
+    for (int idx = ctid; idx < G * 2 * smax * rs; idx += kConsumerWarps * 32)
+        reinterpret_cast<float *>(smem + L.red)[idx] = 0.f;
     group_sync(p, as, abort_flag);
     // shared-expert gate per token: gamma = 1 / (1 + exp(-x . w_sgate)), else 1
     if (p.shared && p.w_sgate) {
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         if (!mbar_wait_bounded(&full[st], (it / nsg) & 1, abort_flag, &p.hdr->status, p.wait_budget_ns)) break;
         const ChunkHeader h = hdrs[st];
         if (h.kind == HK_DONE) break;
-        const uint8_t *stage = ring + (size_t)st * (p.chunk + kMetaBytes);
+        const uint8_t *stage = ring + (size_t)st * (p.chunk + meta_bytes_for(p.T));
         if (h.flags & HF_UNIT_START) {
             // unit setup from the header and the token table in the meta area
             u_fmt = (h.shared || RFMT == FMT_F16) ? FMT_F16 : FMT_W4;
@@ -650,21 +655,24 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (h.flags & HF_GU_LAST) {
-            // cross-warp reduction of the gate/up partial sums, SiLU, h -> fp16
+            // cross-warp reduction of the gate/up partial sums (shared-memory
+            // atomics into the group's buffer), SiLU, h -> fp16; the buffer is
+            // left zeroed for the group's next unit
             const int S = u_S;
-            float *myred = red + (size_t)gw * 2 * S * rs;
 #pragma unroll
             for (int t = 0; t < NTW; ++t) {
                 if (t * 16 < 2 * S) {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const int col = nt * 8 + 2 * q4;
-                        if (col < npad) {
+                        if (col < n_e) {
                             const int ra = t * 16 + g, rb = ra + 8;
-                            *reinterpret_cast<float2 *>(myred + ra * rs + col) =
-                                make_float2(run[t][nt][0], run[t][nt][1]);
-                            *reinterpret_cast<float2 *>(myred + rb * rs + col) =
-                                make_float2(run[t][nt][2], run[t][nt][3]);
+                            atomicAdd(red + ra * rs + col, run[t][nt][0]);
+                            atomicAdd(red + rb * rs + col, run[t][nt][2]);
+                            if (col + 1 < n_e) {
+                                atomicAdd(red + ra * rs + col + 1, run[t][nt][1]);
+                                atomicAdd(red + rb * rs + col + 1, run[t][nt][3]);
+                            }
                         }
                     }
                 }
@@ -673,11 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             group_sync(p, gs, abort_flag);
             for (int idx = gtid; idx < S * npad; idx += gwarps * 32) {
                 const int i = idx / npad, col = idx - i * npad;
-                float gv = 0.f, uv = 0.f;
-                for (int w = 0; w < gwarps; ++w) {
-                    gv += red[((size_t)w * 2 * S + i) * rs + col];
-                    uv += red[((size_t)w * 2 * S + S + i) * rs + col];
-                }
+                const float gv = red[(size_t)i * rs + col], uv = red[(size_t)(S + i) * rs + col];
+                red[(size_t)i * rs + col] = 0.f;
+                red[(size_t)(S + i) * rs + col] = 0.f;
                 const float hv = gv / (1.0f + __expf(-gv)) * uv;
                 hs[col * kHsStride + i] = __float2half_rn(col < n_e ? hv : 0.f);
             }
