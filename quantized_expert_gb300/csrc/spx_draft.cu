@@ -40,12 +40,13 @@ constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
 constexpr int kDkDBatch = 2;      // down items per queue unit
 constexpr int kDkShards = 8;      // independent queue counters (SM b uses shard b % kDkShards)
 constexpr uint32_t kDkSleepNs = 1000;  // longest sleep of a waiting warp inside one try_wait
-// Seven consumer warps, then the producer and the poller: warps share an SM
-// sub-partition by warp index mod 4, so the producer (warp 7) shares its
-// sub-partition with one consumer only and its dependent issue chain is not
-// starved by the dequantising warps.
-constexpr int kDkCons = 7;
+// Eleven consumer warps, then the producer and the poller (13 warps).  Warps
+// share an SM sub-partition by warp index mod 4, so four warps share one
+// sub-partition's 16K registers: a thread may use at most 128 (kDkMaxRegs).
+constexpr int kDkCons = 11;
 constexpr int kDkThreads = (kDkCons + 2) * 32;
+constexpr int kDkMaxRegs = 65536 / (((kDkCons + 2 + 3) / 4) * 4 * 32) / 8 * 8;
+static_assert(kDkMaxRegs >= 64, "registers per thread of the draft launch");
 
 struct __align__(16) DHeader {
     int kind;
@@ -657,7 +658,7 @@ __device__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *s
 
 // INT4 draft kernel; MS = S/16 of the packed INT4 units.
 template <int MS>
-__global__ void __launch_bounds__(kDkThreads, 1) draft_kernel(const DkParams p) {
+__global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int nst = p.nstages;
     const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E);
