@@ -34,8 +34,23 @@ import numpy as np  # noqa: E402
 import spx_workloads as W  # noqa: E402
 
 METRIC = "MoE layer µs & achieved HBM GB/s vs GB300 peak, draft T=1 / verify T=K+1"
+# DRAM bytes (read + write) of one launch in the ncu captures summarised in
+# profiles/ (bench.py --loop, input set 0), with that launch's algorithmic
+# bytes.  They describe the kernels as captured: set them to None when a
+# kernel changes until it is captured again.
+PROFILED_TRAFFIC = {
+    "verify": {"dram_bytes": 675_099_904 + 3_118_080, "algorithmic_bytes": 674_897_920,
+               "summary": "profiles/engine_kernel_deepseek_v2_lite_verify.md"},
+    "draft": {"dram_bytes": 61_521_152 + 217_600, "algorithmic_bytes": 61_374_720,
+              "summary": "profiles/draft_kernel_deepseek_v2_lite_draft.md"},
+}
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
+
+
+def traffic_of(which):
+    t = PROFILED_TRAFFIC.get(which)
+    return None if t is None else t["dram_bytes"]
 
 
 def measured_peaks():
@@ -368,12 +383,14 @@ def run_mine(args):
         "roofline": {"bound": "hbm", "kernel": "engine_kernel<1,1,3> (verify expert launch, FP16 experts)",
                      "achieved": round(kv_bytes / (kv_us * 1e-6) / 1e9, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(kv_bytes / (kv_us * 1e-6) / 1e9 / peak, 3), "traffic": None,
+                     "frac": round(kv_bytes / (kv_us * 1e-6) / 1e9 / peak, 3),
+                     "traffic": traffic_of("verify"), "traffic_capture": PROFILED_TRAFFIC["verify"],
                      "launch_us": round(kv_us, 2), "bytes_per_launch": int(kv_bytes)},
         "draft_roofline": {"bound": "hbm", "kernel": "draft_kernel<2> (draft launch: routing + INT4 experts)",
                            "achieved": round(kd_bytes / (kd_us * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
                            "frac": round(kd_bytes / (kd_us * 1e-6) / 1e9 / peak, 3), "launch_us": round(kd_us, 2),
-                           "bytes_per_launch": int(kd_bytes)},
+                           "bytes_per_launch": int(kd_bytes), "traffic": traffic_of("draft"),
+                           "traffic_capture": PROFILED_TRAFFIC["draft"]},
         "clocks": clocks,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
