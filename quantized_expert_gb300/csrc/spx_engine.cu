@@ -770,21 +770,29 @@ int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int
 // ------------------------------------------------------------ launching --
 int engine_nt(int T) { return T <= 8 ? 1 : (T <= 24 ? 3 : 8); }
 
-// Geometry: chunks of 2 kChunk bytes when at least four stages still fit
-// (half the producer steps per byte), else kChunk; two consumer groups when
-// each can get at least two stages, otherwise one group; at most 12 stages.
+// Geometry: two consumer groups of two stages each (two units in parallel,
+// each double-buffered), with the largest chunk (a multiple of 1 KB, at most
+// 4 kChunk) that shared memory holds: the bytes a block keeps in flight bound
+// the launch, and bigger chunks mean fewer producer steps.  Below kChunk per
+// chunk, one group with as many kChunk stages as fit (at least two).
 static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes, int &chunk) {
-    for (chunk = 2 * kChunk; chunk >= kChunk; chunk /= 2) {
-        const int min_stages = chunk > kChunk ? 4 : 2;
-        for (G = 2; G >= 1; --G) {
-            for (nsg = 12 / G; nsg >= 2; --nsg) {
-                if (G * nsg < min_stages) continue;
-                const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk);
-                if (L.total <= kSmemLimit) {
-                    bytes = L.total;
-                    return true;
-                }
-            }
+    G = 2;
+    nsg = 2;
+    const int base = smem_layout(T, H, npad, smax, w4, G, nsg, 0).total;
+    const int per_stage = (kSmemLimit - base) / (G * nsg) - meta_bytes_for(T);
+    chunk = per_stage / 1024 * 1024;
+    if (chunk > 4 * kChunk) chunk = 4 * kChunk;
+    if (chunk >= kChunk) {
+        bytes = smem_layout(T, H, npad, smax, w4, G, nsg, chunk).total;
+        return bytes <= kSmemLimit;
+    }
+    G = 1;
+    chunk = kChunk;
+    for (nsg = 12; nsg >= 2; --nsg) {
+        const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk);
+        if (L.total <= kSmemLimit) {
+            bytes = L.total;
+            return true;
         }
     }
     return false;
