@@ -7,11 +7,12 @@
 // each expert is selected by draft tokens; tokens are gathered by expert so
 // each expert's work is dispatched once.
 //
-// Layout of the launch: when a router weight is given, blocks compute the
-// [T][E] logits (one warp per expert row, fp32 accumulate), the last block to
-// finish (completion ticket in the workspace, no spin) selects; otherwise a
-// single block selects from the given logits.  Selection: one warp per token,
-// k rounds of a warp-wide (value desc, index asc) arg-max; softmax with expf.
+// Layout of the launch: when a router weight is given, one block per expert
+// row computes that row's logits for every token (fp32 accumulate) and the
+// last block to finish (completion ticket in the workspace, no spin) selects;
+// otherwise a single block selects from the given logits.  Selection: one
+// warp per token (rank of each expert in the order value descending, index
+// ascending; softmax with expf), then the counting sort by one block.
 #include "spx_internal.cuh"
 #include "spx_routing.cuh"
 
@@ -33,34 +34,42 @@ __device__ __forceinline__ float dot8_h(uint4 a, uint4 b, float acc) {
     return acc;
 }
 
-// logits[t][e] for e handled by this warp; 16 tokens per pass.
-__device__ void router_rows(const RouteParams &p) {
+// logits[t][e] of expert row e = blockIdx.x for every token t: a thread
+// holds every H/8 / blockDim-th uint4 of the row, its loads of the row issued
+// together; tokens in passes of 8, fp32 accumulate, warp then block
+// reduction.  Any block size that is a multiple of 32, at most 1024.
+__device__ void router_row_block(const __half *x, const __half *wr, int T, int H, int E, float *logits) {
+    __shared__ float red[32][8];
+    const int e = blockIdx.x, nthr = blockDim.x, nw = nthr >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wpb = blockDim.x >> 5;
-    for (int e = blockIdx.x * wpb + warp; e < p.E; e += gridDim.x * wpb) {
-        const uint4 *wr = reinterpret_cast<const uint4 *>(p.w_router + (size_t)e * p.H);
-        for (int t0 = 0; t0 < p.T; t0 += 16) {
-            float acc[16];
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(wr + (size_t)e * H);
+    const uint4 *x4 = reinterpret_cast<const uint4 *>(x);
+    const int H8 = H / 8;
+    for (int t0 = 0; t0 < T; t0 += 8) {
+        float acc[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-            for (int h8 = lane; h8 < p.H / 8; h8 += 32) {
-                uint4 w = __ldg(wr + h8);
+        for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+#pragma unroll 4
+        for (int h8 = threadIdx.x; h8 < H8; h8 += nthr) {
+            const uint4 w = __ldg(w4 + h8);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (t0 + i < p.T) {
-                        uint4 xv = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)(t0 + i) * p.H) + h8);
-                        acc[i] = dot8_h(xv, w, acc[i]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float v = acc[i];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0 && t0 + i < p.T) p.logits[(size_t)(t0 + i) * p.E + e] = v;
-            }
+            for (int t = 0; t < 8; ++t)
+                if (t0 + t < T) acc[t] = dot8_h(__ldg(x4 + (size_t)(t0 + t) * H8 + h8), w, acc[t]);
         }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            float v = acc[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[warp][t] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < 8 && t0 + (int)threadIdx.x < T) {
+            float v = 0.f;
+            for (int w = 0; w < nw; ++w) v += red[w][threadIdx.x];
+            logits[(size_t)(t0 + threadIdx.x) * E + e] = v;
+        }
+        __syncthreads();
     }
 }
 
@@ -149,7 +158,7 @@ __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts
 __device__ void select_block(const RouteParams &p) {
     __shared__ int32_t s_ids[kMaxSlots];
     __shared__ float s_pw[kMaxSlots];
-    __shared__ float s_sv[8][kMaxE];
+    __shared__ float s_sv[32][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     for (int t = warp; t < p.T; t += wpb) {
@@ -170,14 +179,13 @@ __device__ void select_block(const RouteParams &p) {
                      p.tables);
 }
 
-__global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
+__global__ void __launch_bounds__(1024) route_kernel(const RouteParams p) {
     // Let a programmatically dependent expert launch start its routing-
     // independent work (shared expert) while this one runs.
     griddep_launch_dependents();
     if (p.w_router) {
-        router_rows(p);
+        router_row_block(p.x, p.w_router, p.T, p.H, p.E, p.logits);
         __shared__ int s_last;
-        __syncthreads();
         if (threadIdx.x == 0) {
             __threadfence();
             s_last = atomicAdd(&p.hdr->route_ticket, 1u) == gridDim.x - 1;
@@ -190,40 +198,13 @@ __global__ void __launch_bounds__(256) route_kernel(const RouteParams p) {
     select_block(p);
 }
 
-// Router product for the draft layer call (T <= 8): one block per expert row,
-// every load of the block issued at once (a lane holds H / 2048 uint4 of the
-// row), fp32 accumulate, warp then block reduction.  A dependent launch may
-// start at once and waits for the logits with griddepcontrol.wait.
+// Router product for the draft layer call (T <= 8): one block per expert row.
+// A dependent launch may start at once and waits for the logits with
+// griddepcontrol.wait.
 __global__ void __launch_bounds__(256) router_logits_kernel(const __half *x, const __half *wr, int T, int H, int E,
                                                             float *logits) {
     griddep_launch_dependents();
-    __shared__ float red[8][8];
-    const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint4 *w4 = reinterpret_cast<const uint4 *>(wr + (size_t)e * H);
-    float acc[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-#pragma unroll 4
-    for (int h8 = threadIdx.x; h8 < H / 8; h8 += 256) {
-        const uint4 w = __ldg(w4 + h8);
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-            if (t < T) acc[t] = dot8_h(__ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H) + h8), w, acc[t]);
-    }
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        float v = acc[t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[warp][t] = v;
-    }
-    __syncthreads();
-    if (threadIdx.x < T) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
-        logits[(size_t)threadIdx.x * E + e] = v;
-    }
+    router_row_block(x, wr, T, H, E, logits);
 }
 
 int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s) {
@@ -259,10 +240,12 @@ static int check_route_shape(int T, int H, int E, int k) {
     return SPX_OK;
 }
 
+// One warp per token in the selecting block (at least 8 warps, at most 32);
+// with a router weight one block per expert row, the last to finish selects.
 int launch_route(const RouteParams &p, cudaStream_t s) {
-    int grid = 1;
-    if (p.w_router) grid = (p.E + 7) / 8;
-    route_kernel<<<grid, 256, 0, s>>>(p);
+    const int grid = p.w_router ? p.E : 1;
+    const int threads = 32 * (p.T < 8 ? 8 : (p.T > 32 ? 32 : p.T));
+    route_kernel<<<grid, threads, 0, s>>>(p);
     return record_launch(cudaGetLastError());
 }
 
