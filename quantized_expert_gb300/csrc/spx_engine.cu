@@ -16,9 +16,10 @@
 // group has its own ring of stages and processes its own units, so one group's
 // gate/up -> down boundary (cross-warp reduction, SiLU) overlaps the other
 // group's streaming.  Work is a dynamic queue of "units": one unit = one
-// expert's slice of S intermediate columns, so the gate/up reduction over H
-// and the SiLU stay inside one block, and the down projection's partial sums
-// over slices are added into fp32 outputs with vector atomics (no grid-wide
+// expert's slice of intermediate columns (an INT4 slice of S columns, or two
+// adjacent 16-column FP16 slices), so the gate/up reduction over H and the
+// SiLU stay inside one block, and the down projection's partial sums over
+// units are added into fp32 outputs with vector atomics (no grid-wide
 // barrier, no block waits on another block).  A unit is contiguous in HBM
 // (repacked once at load time: mma fragment order, GPTQ group scales in front
 // of each group's codes) and is streamed by the producer with bulk copies
@@ -34,7 +35,11 @@
 namespace spx {
 
 enum : int { HK_GU = 1, HK_DOWN = 2, HK_DONE = 3 };
-enum : int { HF_UNIT_START = 1, HF_GU_LAST = 2 };
+// HF_GU_LAST: last gate/up chunk of a (sub-)unit, whose partial sums are then
+// reduced; HF_GU_FINAL: last gate/up chunk of the unit (h is computed);
+// HF_SUB1: gate/up chunk of the second 16-column slice of an FP16 pair;
+// HF_PAIR: the unit is an FP16 pair (a down chunk holds both slices' blocks).
+enum : int { HF_UNIT_START = 1, HF_GU_LAST = 2, HF_GU_FINAL = 4, HF_SUB1 = 8, HF_PAIR = 16 };
 enum : int { MODE_SORTED = 0, MODE_ACC = 1, MODE_LAYER = 2 };
 enum : int { FMT_W4 = 0, FMT_F16 = 1 };
 
@@ -63,8 +68,11 @@ struct SmemLayout {
     int red_rs;     // floats per red row
 };
 
+// Widest unit a launch reduces: the INT4 slice width, at least an FP16 pair.
+__host__ __device__ inline int engine_smax(bool w4, int S) { return w4 && S > 2 * kF16S ? S : 2 * kF16S; }
+
 // G groups of 8/G consumer warps; nsg stages per group.
-// red: per group, [2*smax][npad] fp32 gate/up sums (the group's warps add into it);
+// red: per group, [2*smax][T] fp32 gate/up sums (the group's warps add into it);
 // hs : per group, [npad][kHsStride] fp16 intermediate; sd: per group, 2 x [H]
 // fp16 down-scale rows (INT4 only, double-buffered by unit parity).
 __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg,
@@ -82,8 +90,8 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     L.misc = o;
     o += 64;
     L.red = o;
-    L.red_rs = npad;
-    o += G * 2 * smax * npad * 4;
+    L.red_rs = T;  // token columns past T are never written
+    o += G * 2 * smax * T * 4;
     L.hs = o;
     o += G * npad * kHsStride * 2;
     o = (o + 15) & ~15;
@@ -106,7 +114,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
 // dequeued ahead per group so its latency overlaps the copies), and chunks are
 // issued into whichever group's ring has a free stage.
 struct Stream {
-    int u, e, fmt, phase, b;
+    int u, e, fmt, phase, b, nsub, i0;
     int next_u, next_e;
     uint32_t it;
     bool done;
@@ -123,9 +131,16 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     uint8_t *ring = smem + L.ring;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
     const uint64_t pol = policy_evict_first();
-    const int n_sh = p.shared ? p.I_s / kF16S : 0;
+    // FP16 units are pairs of adjacent 16-column slices (the last slice alone
+    // when the count is odd): the pair's down chunks hold both slices'
+    // blocks, so each output partial sum covers 32 intermediate columns and
+    // the fp32 output atomics halve.  Shared units are queued first.
+    const int nu_sh = p.shared ? p.I_s / kF16S : 0;
+    const int n_sh = (nu_sh + 1) / 2;
     const int H = p.H;
-    const int spe = p.I / p.S;
+    const bool rf16 = p.routed_fmt == FMT_F16;
+    const int nu_r = p.I / p.S;                      // routed slices per expert
+    const int spe = rf16 ? (nu_r + 1) / 2 : nu_r;    // routed units per expert
     int n_total = -1;
 
     auto total_units = [&]() -> int {
@@ -141,12 +156,20 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         }
         return n_total;
     };
+    // routed queue index -> active-expert index, first slice, slices
+    auto routed_slot = [&](int ur, int &a, int &i, int &nsub) {
+        a = ur / spe;
+        const int j = ur - a * spe;
+        i = rf16 ? 2 * j : j;
+        nsub = rf16 && i + 1 < nu_r ? 2 : 1;
+    };
     // dequeue one unit; e = its expert (routed units; global load issued now)
     auto dequeue = [&](int &u, int &e) {
         u = (int)atomicAdd(&p.hdr->work_counter, 1u);
         e = -1;
         if (u >= n_sh && u < total_units()) {
-            const int a = (u - n_sh) / spe;
+            int a, i, ns;
+            routed_slot(u - n_sh, a, i, ns);
             e = a < p.E ? __ldcg(p.active + a) : -1;
         }
     };
@@ -198,19 +221,24 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 S_.phase = 0;
                 S_.b = 0;
                 if (u < n_sh) {
-                    S_.base = p.shared + (size_t)u * f16_unit_bytes(H);
+                    S_.base = p.shared + (size_t)(2 * u) * f16_unit_bytes(H);
+                    S_.nsub = 2 * u + 1 < nu_sh ? 2 : 1;
                 } else {
-                    const int j = (u - n_sh) % spe;
+                    int a, i;
+                    routed_slot(u - n_sh, a, i, S_.nsub);
+                    S_.i0 = i * p.S;
                     const size_t ub = S_.fmt == FMT_W4 ? w4_unit_bytes(H, p.S) : f16_unit_bytes(H);
-                    S_.base = p.routed + ((size_t)e * spe + j) * ub;
+                    S_.base = p.routed + ((size_t)e * nu_r + i) * ub;
                 }
             }
             const bool shared = S_.u < n_sh;
             h.unit = S_.u;
             h.shared = shared;
             h.e = S_.e;
-            h.i0 = shared ? S_.u * kF16S : ((S_.u - n_sh) % spe) * p.S;
+            h.i0 = shared ? S_.u * 2 * kF16S : S_.i0;
             h.flags = 0;
+            const uint8_t *src2 = nullptr;  // second slice of an FP16 pair's down chunk
+            uint32_t bytes2 = 0;
             if (S_.fmt == FMT_W4) {
                 const int S = p.S;
                 const int ngr = H / 128;
@@ -219,7 +247,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                     h.kind = HK_GU;
                     h.b0 = S_.b;
                     h.nb = min(W4GPC, ngr - S_.b);
-                    h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == ngr ? HF_GU_LAST : 0);
+                    h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == ngr ? HF_GU_LAST | HF_GU_FINAL : 0);
                     src = S_.base + (size_t)S_.b * w4_group_bytes(S);
                     bytes = h.nb * (uint32_t)w4_group_bytes(S);
                     S_.b += h.nb;
@@ -234,22 +262,32 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                     if (S_.b >= nbd) S_.u = -1;
                 }
             } else {
+                // phase 0 / 1: gate/up of slice 0 / 1; phase 2: down of both
                 const int nbg = H / 16, nbd = H / 32;
-                if (S_.phase == 0) {
+                const int pair = S_.nsub == 2 ? HF_PAIR : 0;
+                if (S_.phase < 2) {
+                    const int sub = S_.phase;
+                    const bool last = S_.b + min(chunk / 1024, nbg - S_.b) == nbg;
                     h.kind = HK_GU;
                     h.b0 = S_.b;
                     h.nb = min(chunk / 1024, nbg - S_.b);
-                    h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == nbg ? HF_GU_LAST : 0);
-                    src = S_.base + (size_t)S_.b * 1024;
+                    h.flags = (sub == 0 && S_.b == 0 ? HF_UNIT_START : 0) | (last ? HF_GU_LAST : 0) |
+                              (last && sub + 1 == S_.nsub ? HF_GU_FINAL : 0) | (sub ? HF_SUB1 : 0) | pair;
+                    src = S_.base + (size_t)sub * f16_unit_bytes(H) + (size_t)S_.b * 1024;
                     bytes = h.nb * 1024;
                     S_.b += h.nb;
-                    if (S_.b >= nbg) S_.phase = 1, S_.b = 0;
+                    if (S_.b >= nbg) S_.phase = sub + 1 < S_.nsub ? sub + 1 : 2, S_.b = 0;
                 } else {
                     h.kind = HK_DOWN;
                     h.b0 = S_.b;
-                    h.nb = min(chunk / 1024, nbd - S_.b);
+                    h.nb = min(chunk / (1024 * S_.nsub), nbd - S_.b);
+                    h.flags = pair;
                     src = S_.base + f16_gu_bytes(H) + (size_t)S_.b * 1024;
                     bytes = h.nb * 1024;
+                    if (pair) {
+                        src2 = src + f16_unit_bytes(H);
+                        bytes2 = bytes;
+                    }
                     S_.b += h.nb;
                     if (S_.b >= nbd) S_.u = -1;
                 }
@@ -260,8 +298,9 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             }
             hdrs[st] = h;
             uint8_t *dst = ring + (size_t)st * (chunk + meta_bytes_for(p.T));
-            mbar_arrive_expect_tx(&full[st], bytes + meta_bytes);
+            mbar_arrive_expect_tx(&full[st], bytes + bytes2 + meta_bytes);
             bulk_g2s(dst, src, bytes, &full[st], pol);
+            if (bytes2) bulk_g2s(dst + bytes, src2, bytes2, &full[st], pol);
             if (meta_bytes) bulk_g2s(dst + chunk, meta, meta_bytes, &full[st], pol);
             S_.it++;
             progressed = true;
@@ -314,7 +353,7 @@ template <int RFMT, int MS4, int NT>
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const bool has_w4 = RFMT == FMT_W4 && p.routed_enabled;
-    const int smax = has_w4 ? p.S : kF16S;
+    const int smax = engine_smax(has_w4, p.S);
     const int G = p.groups, nsg = p.nstages;
     const int gwarps = kConsumerWarps / G;
     const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg, p.chunk);
@@ -392,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     group_sync(p, as, abort_flag);
 
     constexpr int NTW = 2 * MS4;  // INT4 gate+up tiles per k-step (FP16 units use 2)
+    constexpr int KH = MS4 > 2 ? MS4 : 2;  // k-steps of the down projection (an FP16 pair has 2)
     // per-warp state of the current unit
     int u_fmt = FMT_F16, u_S = kF16S, u_e = 0, u_i0 = 0, n_e = 0, nact = 0;
     uint32_t ucount = 0;     // units started by this group (selects the down-scale buffer)
@@ -400,9 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     int orow[NT][2];
     float oscl[NT][2];
     float run[NTW][NT][4];                // gate/up partial sums of this warp for the whole unit
-    uint32_t hb0[MS4][NT], hb1[MS4][NT];  // h fragments for the down phase
+    uint32_t hb0[KH][NT], hb1[KH][NT];  // h fragments for the down phase
 #pragma unroll
-    for (int ks = 0; ks < MS4; ++ks)
+    for (int ks = 0; ks < KH; ++ks)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) hb0[ks][nt] = hb1[ks][nt] = 0u;
 
@@ -416,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         if (h.flags & HF_UNIT_START) {
             // unit setup from the header and the token table in the meta area
             u_fmt = (h.shared || RFMT == FMT_F16) ? FMT_F16 : FMT_W4;
-            u_S = h.shared ? kF16S : p.S;
+            u_S = u_fmt == FMT_F16 ? kF16S * ((h.flags & HF_PAIR) ? 2 : 1) : p.S;
             u_e = h.e;
             u_i0 = h.i0;
             const TokTable *tb = reinterpret_cast<const TokTable *>(stage + p.chunk);
@@ -617,23 +657,31 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                         }
                     }
                 } else {
-                    // block = one m-tile pair: [q][lane] x 16 B
-                    uint32_t a[2][4];
+                    // block = one m-tile pair: [q][lane] x 16 B; a pair's second
+                    // slice has its block nb blocks further on (k-step 1)
+                    const bool two = (h.flags & HF_PAIR) != 0;
+                    uint32_t a[2][2][4];
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const uint4 v = lds128(stage + ((size_t)b * 2 + q) * 512 + lane * 16);
-                        a[q][0] = v.x;
-                        a[q][1] = v.y;
-                        a[q][2] = v.z;
-                        a[q][3] = v.w;
-                    }
+                    for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                            if (sl == 0 || two) v = lds128(stage + ((size_t)(sl * nb + b) * 2 + q) * 512 + lane * 16);
+                            a[sl][q][0] = v.x;
+                            a[sl][q][1] = v.y;
+                            a[sl][q][2] = v.z;
+                            a[sl][q][3] = v.w;
+                        }
                     const int n0 = 32 * (h.b0 + b) + 4 * g;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         if (nt < nact) {
                             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                            for (int q = 0; q < 2; ++q) mma_16816(acc[q], a[q], hb0[0][nt], hb1[0][nt]);
+                            for (int q = 0; q < 2; ++q) {
+                                mma_16816(acc[q], a[0][q], hb0[0][nt], hb1[0][nt]);
+                                if (two) mma_16816(acc[q], a[1][q], hb0[1][nt], hb1[1][nt]);
+                            }
 #pragma unroll
                             for (int hf = 0; hf < 2; ++hf) {
                                 const int col = nt * 8 + 2 * q4 + hf;
@@ -655,18 +703,20 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (h.flags & HF_GU_LAST) {
-            // cross-warp reduction of the gate/up partial sums (shared-memory
-            // atomics into the group's buffer), SiLU, h -> fp16; the buffer is
-            // left zeroed for the group's next unit
+            // cross-warp reduction of the (sub-)unit's gate/up partial sums
+            // (shared-memory atomics into the group's buffer: gate rows [0, S),
+            // up rows [S, 2S); an FP16 pair's second slice at row offset 16)
             const int S = u_S;
+            const bool f16u = u_fmt == FMT_F16;
+            const int roff = (h.flags & HF_SUB1) ? 16 : 0;
 #pragma unroll
             for (int t = 0; t < NTW; ++t) {
-                if (t * 16 < 2 * S) {
+                if (f16u ? t < 2 : t * 16 < 2 * S) {
+                    const int ra = (f16u ? t * S + roff : t * 16) + g, rb = ra + 8;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const int col = nt * 8 + 2 * q4;
                         if (col < n_e) {
-                            const int ra = t * 16 + g, rb = ra + 8;
                             atomicAdd(red + ra * rs + col, run[t][nt][0]);
                             atomicAdd(red + rb * rs + col, run[t][nt][2]);
                             if (col + 1 < n_e) {
@@ -674,23 +724,33 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                                 atomicAdd(red + rb * rs + col + 1, run[t][nt][3]);
                             }
                         }
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) run[t][nt][r] = 0.f;
                     }
                 }
             }
+        }
+        if (h.flags & HF_GU_FINAL) {
+            // SiLU, h -> fp16 fragments; the buffer is left zeroed for the
+            // group's next unit
+            const int S = u_S;
             if (RFMT == FMT_W4) cp_async_wait_all();  // this thread's share of the down-scale row
             group_sync(p, gs, abort_flag);
             for (int idx = gtid; idx < S * npad; idx += gwarps * 32) {
                 const int i = idx / npad, col = idx - i * npad;
-                const float gv = red[(size_t)i * rs + col], uv = red[(size_t)(S + i) * rs + col];
-                red[(size_t)i * rs + col] = 0.f;
-                red[(size_t)(S + i) * rs + col] = 0.f;
-                const float hv = gv / (1.0f + __expf(-gv)) * uv;
+                float hv = 0.f;
+                if (col < p.T) {
+                    const float gv = red[(size_t)i * rs + col], uv = red[(size_t)(S + i) * rs + col];
+                    red[(size_t)i * rs + col] = 0.f;
+                    red[(size_t)(S + i) * rs + col] = 0.f;
+                    hv = gv / (1.0f + __expf(-gv)) * uv;
+                }
                 hs[col * kHsStride + i] = __float2half_rn(col < n_e ? hv : 0.f);
             }
             group_sync(p, gs, abort_flag);
             const int kst = S / 16;
 #pragma unroll
-            for (int ks = 0; ks < MS4; ++ks)
+            for (int ks = 0; ks < KH; ++ks)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int col = nt * 8 + g;
@@ -804,7 +864,7 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
     const bool w4 = RFMT == FMT_W4 && p.routed_enabled;
-    const int smax = w4 ? p.S : kF16S;
+    const int smax = engine_smax(w4, p.S);
     int G, nsg, bytes, chunk;
     if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk)) return SPX_ERR_UNSUPPORTED;
     p.groups = G;
@@ -854,7 +914,7 @@ int engine_fits(int T, int H, int fmt, int S) {
     const bool w4 = fmt == FMT_W4;
     if (w4 && S == 32 && engine_nt(T) == 8) return 0;
     int G, nsg, bytes, chunk;
-    return choose_geometry(T, H, npad, w4 ? S : kF16S, w4, G, nsg, bytes, chunk) ? 1 : 0;
+    return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk) ? 1 : 0;
 }
 
 }  // namespace spx

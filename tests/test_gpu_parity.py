@@ -270,6 +270,23 @@ def test_layer_full_size(name, mode):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{name} {mode} rep {rep}")
 
 
+@pytest.mark.parametrize("T", [1, 9, 17])
+def test_verify_layer_odd_slice_count(T):
+    """Verify layer whose shared expert is an odd number of 16-column slices
+    (I_s = 272): the launch streams FP16 slices in pairs, so the shared
+    expert's last slice stands alone (routed widths are multiples of 128)."""
+    gh = _gh()
+    s = _small("qwen15_moe", H=512, I=384, E=6, k=2, I_s=272, shared_gate=True)
+    x = W.gen_x(s, T, step=T, which=1)
+    need = gh.needed_experts(s, None, [x])
+    lay = gh.Layer(s, needed=need, draft=False)
+    ref = lay.oracle_layer("verify", x)
+    outs, routing, _ = _run_layer(lay, "verify", x, None)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"odd slices T={T} rep {rep}")
+
+
 @pytest.mark.parametrize("T", [2, 8])
 def test_draft_layer_gated_shared_many_tokens(T):
     """Draft layer through the split-K draft launch with T tokens, a gated
