@@ -736,16 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             const int S = u_S;
             if (RFMT == FMT_W4) cp_async_wait_all();  // this thread's share of the down-scale row
             group_sync(p, gs, abort_flag);
-            for (int idx = gtid; idx < S * npad; idx += gwarps * 32) {
-                const int i = idx / npad, col = idx - i * npad;
-                float hv = 0.f;
-                if (col < p.T) {
-                    const float gv = red[(size_t)i * rs + col], uv = red[(size_t)(S + i) * rs + col];
-                    red[(size_t)i * rs + col] = 0.f;
-                    red[(size_t)(S + i) * rs + col] = 0.f;
-                    hv = gv / (1.0f + __expf(-gv)) * uv;
-                }
-                hs[col * kHsStride + i] = __float2half_rn(col < n_e ? hv : 0.f);
+            // only the unit's n_e token columns hold sums (the others stay
+            // zero); h columns past n_e feed output columns that are never
+            // stored, so they are left as they are
+            for (int idx = gtid; idx < S * n_e; idx += gwarps * 32) {
+                const int i = idx / n_e, col = idx - i * n_e;
+                const float gv = red[(size_t)i * rs + col], uv = red[(size_t)(S + i) * rs + col];
+                red[(size_t)i * rs + col] = 0.f;
+                red[(size_t)(S + i) * rs + col] = 0.f;
+                hs[col * kHsStride + i] = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
             }
             group_sync(p, gs, abort_flag);
             const int kst = S / 16;

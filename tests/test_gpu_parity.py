@@ -176,6 +176,29 @@ def test_draft_and_verify_unit_calls(case):
         assert spx.spx_workspace_status(ws) == 0
 
 
+def test_verify_unit_call_one_group():
+    """Wide activations (T = 20, H = 4096) leave room for one consumer group
+    only: FP16 slices then reduce through the shared-memory buffer."""
+    spx, gh = _spx(), _gh()
+    s = _small("phi35_moe", H=4096, I=256, E=4, k=2)
+    T = 20
+    x = W.gen_x(s, T, step=20)
+    lg = np.random.default_rng(20).standard_normal((T, s.E))
+    ids, w = oracle.route_topk(lg, s.k, s.renorm)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), draft=False)
+    g, r = _routing_dev(ids, s.E)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k)
+    y_ref = np.stack([oracle.swiglu_f16(x[int(sl) // s.k], lay.f16_host[int(ids.reshape(-1)[sl])])
+                      for sl in g["sorted_slots"]])
+    y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
+    for rep in range(2):
+        spx.spx_moe_verify_fp16(gh.dev_f16(x), lay.f16, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                                r["n_active"], y, ws)
+        torch.cuda.synchronize()
+        gh.check_close(y.cpu().numpy(), y_ref, f"one group rep {rep}")
+    assert spx.spx_workspace_status(ws) == 0
+
+
 def test_draft_wide_slices_reject_many_tokens():
     """INT4 slices of 32 columns serve at most 24 tokens per expert; more is an
     explicit SPX_ERR_UNSUPPORTED (pack with slice_cols=16 for such batches)."""
