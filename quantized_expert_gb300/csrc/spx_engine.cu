@@ -773,16 +773,29 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     if (misc[1]) {
         __threadfence();
         if (p.mode == MODE_LAYER) {
+            // the whole [T][H] sum is read in batches of 16 float4 per thread,
+            // all loads of a batch in flight before any store
             const int n4 = p.T * H / 4;
+            constexpr int kNth = kConsumerWarps * 32, kBatch = 16;
             float4 *acc4 = reinterpret_cast<float4 *>(p.yout);
-            for (int idx = ctid; idx < n4; idx += kConsumerWarps * 32) {
-                const float4 v = __ldcg(acc4 + idx);
-                const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
-                uint2 o;
-                o.x = h2_as_u32(lo);
-                o.y = h2_as_u32(hi);
-                reinterpret_cast<uint2 *>(p.out)[idx] = o;
-                __stcg(acc4 + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+            for (int i0 = ctid; i0 < n4; i0 += kNth * kBatch) {
+                float4 v[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = i0 + j * kNth;
+                    v[j] = idx < n4 ? __ldcg(acc4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = i0 + j * kNth;
+                    if (idx < n4) {
+                        uint2 o;
+                        o.x = h2_as_u32(__floats2half2_rn(v[j].x, v[j].y));
+                        o.y = h2_as_u32(__floats2half2_rn(v[j].z, v[j].w));
+                        reinterpret_cast<uint2 *>(p.out)[idx] = o;
+                        __stcg(acc4 + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+                    }
+                }
             }
         }
         if (ctid == 0) {
