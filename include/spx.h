@@ -28,6 +28,10 @@
  *  - The library holds no state between calls: the counter table and the
  *    workspace are the caller's buffers.  One workspace must not be used by
  *    two calls that can run concurrently (e.g. on two streams).
+ *  - The expert launches run one block per SM and some of their blocks wait
+ *    for others (finished work, intermediate results); every such wait is
+ *    bounded: if other work keeps SMs from this launch for longer than the
+ *    bound, the call's status word becomes SPX_ERR_TIMEOUT.
  */
 #ifndef SPX_H
 #define SPX_H

@@ -61,6 +61,7 @@ static_assert(kTableBytes <= (size_t)kMetaBytes, "table fits the stage meta area
 // The meta area a launch needs: the table header and T entries, in 128-byte units.
 __host__ __device__ inline int meta_bytes_for(int T) { return (16 + 16 * T + 127) & ~127; }
 constexpr int kHsStride = 40;                     // halves per intermediate row (32 + 8 pad)
+constexpr int kEpiBlocks = 16;                    // blocks sharing the fp16 output pass
 
 struct SmemLayout {
     int bars, hdrs, gamma, misc, red, hs, sd, xs, ring, total;
@@ -81,7 +82,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     const int nst = G * nsg;
     int o = 0;
     L.bars = o;
-    o += (2 * nst + G + 1) * 8;
+    o += (2 * nst + G + 2) * 8;  // full, empty, group, all-consumer, activation barriers
     o = (o + 15) & ~15;
     L.hdrs = o;
     o += nst * (int)sizeof(ChunkHeader);
@@ -131,6 +132,15 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     uint8_t *ring = smem + L.ring;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
     const uint64_t pol = policy_evict_first();
+    {
+        // the activation rows [T][H] -> shared rows of H + 8 halves, ahead of
+        // the weights (every block reads them: kept in L2)
+        uint64_t *xbar = full + 2 * G * nsg + G + 1;
+        const uint64_t keep = policy_evict_last();
+        mbar_arrive_expect_tx(xbar, (uint32_t)(p.T * p.H * 2));
+        for (int t = 0; t < p.T; ++t)
+            bulk_g2s(smem + L.xs + (size_t)t * L.xs_stride * 2, p.x + (size_t)t * p.H, (uint32_t)(p.H * 2), xbar, keep);
+    }
     // FP16 units are pairs of adjacent 16-column slices (the last slice alone
     // when the count is odd): the pair's down chunks hold both slices'
     // blocks, so each output partial sum covers 32 intermediate columns and
@@ -363,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     uint64_t *empty = full + G * nsg;
     uint64_t *gbar = empty + G * nsg;  // one per group
     uint64_t *allbar = gbar + G;       // all consumer warps
+    uint64_t *xbar = allbar + 1;       // activation rows landed
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     if (threadIdx.x == 0) {
         for (int s = 0; s < G * nsg; ++s) {
@@ -371,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         }
         for (int q = 0; q < G; ++q) mbar_init(&gbar[q], gwarps);
         mbar_init(allbar, kConsumerWarps);
+        mbar_init(xbar, 1);
         misc[0] = 0;  // abort flag
         misc[1] = 0;  // last-block flag
         fence_mbar_init();
@@ -401,15 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     const int ctid = threadIdx.x;  // 0..255
     const int H = p.H;
 
-    // stage activations [T][H] -> shared rows of H+8 halves; zero the groups'
-    // gate/up reduction buffers
-    for (int idx = ctid; idx < p.T * (H / 8); idx += kConsumerWarps * 32) {
-        const int t = idx / (H / 8), h8 = idx - t * (H / 8);
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H) + h8);
-        *reinterpret_cast<uint4 *>(xs + (size_t)t * xs_stride + h8 * 8) = v;
-    }
+    // zero the groups' gate/up reduction buffers; the activation rows come
+    // in by bulk copies the producer issues first
     for (int idx = ctid; idx < G * 2 * smax * rs; idx += kConsumerWarps * 32)
         reinterpret_cast<float *>(smem + L.red)[idx] = 0.f;
+    mbar_wait_bounded(xbar, 0, abort_flag, &p.hdr->status, p.wait_budget_ns);
     group_sync(p, as, abort_flag);
     // shared-expert gate per token: gamma = 1 / (1 + exp(-x . w_sgate)), else 1
     if (p.shared && p.w_sgate) {
@@ -762,33 +770,55 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         ++it;
     }
 
-    // completion ticket; the last block writes the fp16 output and resets
+    // Completion: the last kEpiBlocks blocks to finish wait until every block
+    // has (their own work is done; all blocks of the grid are resident) and
+    // each turns its share of the fp32 sums into the fp16 output and clears
+    // it; the last of them to leave resets the counters.
     group_sync(p, as, abort_flag);
     if (ctid == 0) {
         __threadfence();
-        const uint32_t t = atomicAdd(&p.hdr->done_ticket, 1u);
-        misc[1] = (t == gridDim.x - 1);
+        misc[1] = (int)atomicAdd(&p.hdr->done_ticket, 1u);
     }
     group_sync(p, as, abort_flag);
-    if (misc[1]) {
-        __threadfence();
-        if (p.mode == MODE_LAYER) {
-            // the whole [T][H] sum is read in batches of 16 float4 per thread,
+    const int nhelp = (int)gridDim.x < kEpiBlocks ? (int)gridDim.x : kEpiBlocks;
+    const int part = misc[1] - ((int)gridDim.x - nhelp);
+    if (part >= 0) {
+        if (ctid == 0) {
+            // bounded wait for the remaining blocks
+            const volatile uint32_t *dt = &p.hdr->done_ticket;
+            const uint64_t t0 = global_timer_ns();
+            bool ok = true;
+            while (*dt < gridDim.x) {
+                if (*abort_flag || global_timer_ns() - t0 > p.wait_budget_ns) {
+                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            misc[2] = ok;
+            __threadfence();
+        }
+        group_sync(p, as, abort_flag);
+        if (p.mode == MODE_LAYER && misc[2]) {
+            // rows of this part, read in batches of 16 float4 per thread with
             // all loads of a batch in flight before any store
             const int n4 = p.T * H / 4;
+            const int per = (n4 + nhelp - 1) / nhelp;
+            const int lo = part * per, hi = min(n4, lo + per);
             constexpr int kNth = kConsumerWarps * 32, kBatch = 16;
             float4 *acc4 = reinterpret_cast<float4 *>(p.yout);
-            for (int i0 = ctid; i0 < n4; i0 += kNth * kBatch) {
+            for (int i0 = lo + ctid; i0 < hi; i0 += kNth * kBatch) {
                 float4 v[kBatch];
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int idx = i0 + j * kNth;
-                    v[j] = idx < n4 ? __ldcg(acc4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[j] = idx < hi ? __ldcg(acc4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int idx = i0 + j * kNth;
-                    if (idx < n4) {
+                    if (idx < hi) {
                         uint2 o;
                         o.x = h2_as_u32(__floats2half2_rn(v[j].x, v[j].y));
                         o.y = h2_as_u32(__floats2half2_rn(v[j].z, v[j].w));
@@ -798,10 +828,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                 }
             }
         }
+        group_sync(p, as, abort_flag);
         if (ctid == 0) {
-            p.hdr->work_counter = 0;
-            p.hdr->done_ticket = 0;
             __threadfence();
+            if (atomicAdd(&p.hdr->exit_ticket, 1u) == (uint32_t)nhelp - 1) {
+                p.hdr->work_counter = 0;
+                p.hdr->done_ticket = 0;
+                p.hdr->exit_ticket = 0;
+                __threadfence();
+            }
         }
     }
 }

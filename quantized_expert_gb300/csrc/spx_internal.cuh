@@ -29,7 +29,8 @@ struct WsHeader {
     uint32_t done_ticket;    // completed blocks of the expert launch
     int32_t status;          // SPX_OK or SPX_ERR_TIMEOUT (sticky)
     uint32_t route_ticket;   // completed blocks of the router product
-    uint32_t pad[60];
+    uint32_t exit_ticket;    // blocks of the expert launch done with its output pass
+    uint32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 constexpr size_t kWsAccOffset = 256;
@@ -168,6 +169,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 // 16-byte asynchronous global -> shared copy (completion: cp_async_wait_all
