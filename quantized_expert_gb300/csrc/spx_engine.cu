@@ -116,7 +116,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
 // issued into whichever group's ring has a free stage.
 struct Stream {
     int u, e, fmt, phase, b, nsub, i0;
-    int next_u, next_e;
+    int next_u, next_e, pend_u;
     uint32_t it;
     bool done;
     const uint8_t *base;
@@ -173,14 +173,23 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         i = rf16 ? 2 * j : j;
         nsub = rf16 && i + 1 < nu_r ? 2 : 1;
     };
-    // dequeue one unit; e = its expert (routed units; global load issued now)
-    auto dequeue = [&](int &u, int &e) {
-        u = (int)atomicAdd(&p.hdr->work_counter, 1u);
+    // Queue: stream g of block b starts with unit b*G + g; later units come
+    // from the counter (offset by the stream count).  Each stream keeps two
+    // units ahead: the next one, whose expert id load was issued a unit
+    // earlier, and a counter value fetched a unit earlier, so the producer
+    // never waits on a queue round trip while streams are running.
+    const int nstreams = (int)gridDim.x * G;
+    auto fetch = [&]() -> int { return (int)atomicAdd(&p.hdr->work_counter, 1u) + nstreams; };
+    // expert id of unit u (routed units; the load is issued, not waited for)
+    auto resolve = [&](int u, int &e) {
         e = -1;
-        if (u >= n_sh && u < total_units()) {
+        if (u >= n_sh && p.routed_enabled) {
             int a, i, ns;
             routed_slot(u - n_sh, a, i, ns);
-            e = a < p.E ? __ldcg(p.active + a) : -1;
+            if (a < p.E) {
+                griddep_wait();  // routing results of the preceding launch
+                e = __ldcg(p.active + a);
+            }
         }
     };
     auto valid_unit = [&](int u) -> bool { return u < n_sh || u < total_units(); };
@@ -191,7 +200,9 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         s[g].u = -1;
         s[g].it = 0;
         s[g].done = false;
-        dequeue(s[g].next_u, s[g].next_e);
+        s[g].next_u = (int)blockIdx.x * G + g;
+        resolve(s[g].next_u, s[g].next_e);
+        s[g].pend_u = fetch();
     }
     const int chunk = p.chunk;
     const int W4GPC = chunk / (int)w4_group_bytes(p.S);  // whole INT4 groups per chunk
@@ -223,7 +234,9 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                     progressed = true;
                     continue;
                 }
-                dequeue(S_.next_u, S_.next_e);
+                S_.next_u = S_.pend_u;
+                resolve(S_.next_u, S_.next_e);
+                S_.pend_u = fetch();
                 if (u >= n_sh && (e < 0 || e >= p.E)) continue;  // unusable routing entry: skip the unit
                 S_.u = u;
                 S_.e = u < n_sh ? 0 : e;
