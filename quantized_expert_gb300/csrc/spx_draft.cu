@@ -125,8 +125,8 @@ struct DkLayout {
 __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E) {
     DkLayout L;
     int o = 0;
-    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier
-    o += (3 * nst + 1) * 8;
+    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer, logits
+    o += (3 * nst + 2) * 8;
     o = (o + 15) & ~15;
     L.hdrs = o;
     o += nst * (int)sizeof(DHeader);
@@ -155,6 +155,7 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int 
     o += T * k * 4;
     L.rrank = o;
     o += T * k * 4;
+    o = (o + 15) & ~15;
     L.rsv = o;  // per selecting warp (one per token): the token's logits
     o += T * E * 4;
     L.stn = o;
@@ -578,6 +579,43 @@ __device__ int route_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *
     int *act = reinterpret_cast<int *>(smem + L.act);
     int *stn = reinterpret_cast<int *>(smem + L.stn);
     TokEntry *ste = reinterpret_cast<TokEntry *>(smem + L.ste);
+    if (T == 1 && k <= 32) {
+        // one token: its k experts are distinct, one slot each; an expert's
+        // place in the active list = the selected experts below it
+        const int e = lane < k ? ids[lane] : 0x7fffffff;
+        int a = 0;
+        for (int s2 = 0; s2 < k; ++s2) a += __shfl_sync(0xffffffffu, e, s2) < e;
+        if (lane < k) {
+            TokEntry te;
+            te.tok = 0;
+            te.row = 0;
+            te.scale = pw[lane];
+            te.pad = 0;
+            ste[a] = te;
+            act[a] = e;
+            stn[a] = 1;
+            if (out) p.sorted_slots[a] = lane;
+        }
+        if (out) {
+            __syncwarp();
+            for (int e2 = lane; e2 < E; e2 += 32) {
+                int c = 0, below = 0;
+                for (int s2 = 0; s2 < k; ++s2) {
+                    const int es = ids[s2];
+                    c += es == e2;
+                    below += es < e2;
+                }
+                p.counts[e2] = c;
+                p.offsets[e2] = below;
+                p.active_out[e2] = e2 < k ? act[e2] : -1;
+            }
+            if (lane == 0) {
+                p.offsets[E] = k;
+                *p.n_active_out = k;
+            }
+        }
+        return k;
+    }
     int nfirst = 0;
     for (int s = lane; s < n; s += 32) {  // rank of slot s among the earlier slots of its expert
         const int e = ids[s];
@@ -672,6 +710,9 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     int *scnt = reinterpret_cast<int *>(smem + L.scnt);
     volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
     float *sacc = reinterpret_cast<float *>(smem + L.sacc);
+    // given logits whose bytes make whole 16-byte units come in by one bulk copy
+    const bool lg_bulk = p.logits && !p.logits_dep && ((p.T * p.E * 4) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
     for (int i = threadIdx.x; i < nst * L.slot_floats; i += kDkThreads) sacc[i] = 0.f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -689,7 +730,15 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         }
         DHeader *hw = reinterpret_cast<DHeader *>(smem + L.hdrs);
         for (int st = 0; st < nst; ++st) hw[st].seq = -1;  // no fill yet (shared memory is not cleared)
+        mbar_init(allbar + 1, 1);
         fence_mbar_init();
+        if (lg_bulk) {
+            // the launch's logits, ahead of every weight copy (a load issued
+            // behind the weight stream waits for it in the memory queues)
+            const uint32_t bytes = (uint32_t)(p.T * p.E * 4);
+            mbar_arrive_expect_tx(allbar + 1, bytes);
+            bulk_g2s(smem + L.rsv, p.logits, bytes, allbar + 1, policy_evict_last());
+        }
     }
     __syncthreads();
     if (warp == kDkCons) {
@@ -758,10 +807,15 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             float *rpw = reinterpret_cast<float *>(smem + L.rpw);
             const int E = p.E, k = p.k;
             int mine = 0;
+            if (lg_bulk) mbar_wait_bounded(allbar + 1, 0, abort_flag, &p.hdr->status, p.wait_budget_ns);
             for (int t = warp; t < T; t += kDkCons, ++mine) {
                 const float *lg = p.logits + (size_t)t * E;
-                select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k, rpw + t * k,
-                             reinterpret_cast<float *>(smem + L.rsv) + t * E);
+                float *sv = reinterpret_cast<float *>(smem + L.rsv) + t * E;
+                if (lg_bulk)
+                    select_token([&](int e) { return sv[e]; }, E, k, p.renorm, lane, rids + t * k, rpw + t * k, sv);
+                else
+                    select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k,
+                                 rpw + t * k, sv);
                 if (blockIdx.x == 0 && lane == 0)
                     for (int r = 0; r < k; ++r) {
                         const int e = rids[t * k + r];

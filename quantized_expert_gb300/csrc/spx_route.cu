@@ -158,13 +158,12 @@ __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts
 __device__ void select_block(const RouteParams &p) {
     __shared__ int32_t s_ids[kMaxSlots];
     __shared__ float s_pw[kMaxSlots];
-    __shared__ float s_sv[32][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     for (int t = warp; t < p.T; t += wpb) {
         const float *lg = p.logits + (size_t)t * p.E;
         select_token([&](int e) { return __ldcg(lg + e); }, p.E, p.k, p.renorm, lane, s_ids + t * p.k,
-                     s_pw + t * p.k, s_sv[warp]);
+                     s_pw + t * p.k, nullptr);
         if (lane == 0)
             for (int r = 0; r < p.k; ++r) {
                 const int be = s_ids[t * p.k + r];

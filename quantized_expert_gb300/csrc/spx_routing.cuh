@@ -14,28 +14,35 @@
 namespace spx {
 
 #if defined(__CUDACC__)
+// Order key of a logit: unsigned compare of keys = float compare of values
+// (-0 is taken as +0); 0 marks an expert already taken or absent.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // Warp-collective selection for one token.  lg(e) returns logit e (fp32, the
-// precision every decision is taken in); E <= 256, k <= E.  An expert's rank
-// is the number of experts before it in the order (value descending, index
-// ascending); the k experts of rank < k are the selection, listed by rank.
+// precision every decision is taken in); E <= 256, k <= E.  The experts are
+// taken in the order (value descending, index ascending): k rounds, each a
+// warp-wide maximum of the order keys, ties to the lowest expert index.
 // p = expf(v - max) / sum over all E of expf(v - max) (each lane sums its
 // experts e = lane + 32 j in j order, then a fixed xor-shuffle tree);
 // weight = p, or p / (sum of the k selected p, in rank order) when renorm.
-// sv is E floats of scratch in shared memory.  Lane 0 publishes nothing
-// itself: the lanes owning selected experts write ids[rank] and w[rank].
+// The lane owning the rank-r expert writes ids[r] and w[r]; sv (E floats of
+// shared scratch) is not used.
 template <int NPER, class Logit>
 __device__ __forceinline__ void select_token_n(Logit lg, int E, int k, int renorm, int lane, int32_t *ids, float *w,
                                                float *sv) {
+    (void)sv;
     float v[NPER];
+    uint32_t key[NPER];
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         const int e = lane + 32 * j;
         v[j] = e < E ? lg(e) : -INFINITY;
-        if (e < E) {
-            sv[e] = v[j];
-            m = fmaxf(m, v[j]);
-        }
+        key[j] = e < E ? logit_key(v[j]) : 0u;
+        if (e < E) m = fmaxf(m, v[j]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -45,22 +52,25 @@ __device__ __forceinline__ void select_token_n(Logit lg, int E, int k, int renor
         if (lane + 32 * j < E) z += expf(v[j] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    __syncwarp();
-    int rank[NPER];
+    for (int r = 0; r < k; ++r) {
+        uint32_t bk = 0u;
+        int bj = 0;
 #pragma unroll
-    for (int j = 0; j < NPER; ++j) rank[j] = 0;
-#pragma unroll 4
-    for (int e2 = 0; e2 < E; ++e2) {
-        const float u = sv[e2];
+        for (int j = 0; j < NPER; ++j)
+            if (key[j] > bk) {  // strict: the lowest j among equal keys
+                bk = key[j];
+                bj = j;
+            }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, (bk == mk && mk != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
+        if ((int)(win & 31u) == lane && win != 0xffffffffu) {
 #pragma unroll
-        for (int j = 0; j < NPER; ++j) rank[j] += (u > v[j] || (u == v[j] && e2 < lane + 32 * j)) ? 1 : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < NPER; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && rank[j] < k) {
-            ids[rank[j]] = e;
-            w[rank[j]] = expf(v[j] - m) / z;
+            for (int j = 0; j < NPER; ++j)
+                if (j == (int)(win >> 5)) {
+                    ids[r] = (int32_t)win;
+                    w[r] = expf(v[j] - m) / z;
+                    key[j] = 0u;
+                }
         }
     }
     __syncwarp();
