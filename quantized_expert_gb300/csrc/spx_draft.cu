@@ -348,6 +348,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     };
     // Issues every item of queue unit u; false once the queue is exhausted (or on failure).
     auto run_unit = [&](int u) -> bool {
+        if (u < 0) return false;  // a corrupted queue counter (workspace not zeroed): stop
         if (u < nSGb) {
             DHeader h{};
             h.kind = DK_SG;

@@ -192,7 +192,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             }
         }
     };
-    auto valid_unit = [&](int u) -> bool { return u < n_sh || u < total_units(); };
+    auto valid_unit = [&](int u) -> bool { return u >= 0 && (u < n_sh || u < total_units()); };
 
     Stream s[G];
 #pragma unroll
