@@ -282,7 +282,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         // computes the logits first and the draft launch overlaps it.
         if (a->w_router) {
             st = launch_router_logits(reinterpret_cast<const __half *>(a->x),
-                                      reinterpret_cast<const __half *>(a->w_router), T, H, E, a->logits, s);
+                                      reinterpret_cast<const __half *>(a->w_router), T, H, E, a->logits, s, !timed);
             if (st) return st;
         }
         DraftRouting rt{};
@@ -314,7 +314,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         p.out = reinterpret_cast<__half *>(a->out);
         if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
             return SPX_ERR_CUDA;
-        st = launch_draft(p, &rt, ws_scratch_base(T, H), a->w_router && !timed, s);
+        st = launch_draft(p, &rt, ws_scratch_base(T, H), !timed, s);
         if (st) return st;
         if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
             return SPX_ERR_CUDA;
@@ -341,7 +341,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     rp.n_active = a->n_active;
     rp.tables = ws_tables(a->ws, T, H);
     rp.hdr = static_cast<WsHeader *>(a->ws);
-    st = launch_route(rp, s);
+    st = launch_route(rp, s, !timed);
     if (st) return st;
 
     EngineParams p = base_params(a->x, T, H, a->ws);

@@ -125,8 +125,8 @@ struct DkLayout {
 __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E) {
     DkLayout L;
     int o = 0;
-    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer, logits
-    o += (3 * nst + 2) * 8;
+    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier
+    o += (3 * nst + 1) * 8;
     o = (o + 15) & ~15;
     L.hdrs = o;
     o += nst * (int)sizeof(DHeader);
@@ -430,13 +430,21 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     const int shard = (int)(blockIdx.x % kDkShards);
     const uint32_t nsm = (gridDim.x - shard + kDkShards - 1) / kDkShards;  // blocks on this shard
     uint32_t *ctr = p.qctr + 64 * shard;
+    // The static unit's items need no global memory but its weights (the
+    // routing and the ready counts are the consumers' and the poller's, who
+    // wait for the preceding launch themselves), so they are issued before
+    // this thread waits for it; the counters come after.
     uint32_t tkA = blockIdx.x / kDkShards;
-    uint32_t tkB = nsm + atomicAdd(ctr, 1u);
-    while (true) {
-        if (!run_unit((int)tkA * kDkShards + shard)) break;
-        tkA = nsm + atomicAdd(ctr, 1u);
-        if (!run_unit((int)tkB * kDkShards + shard)) break;
-        tkB = nsm + atomicAdd(ctr, 1u);
+    const bool more = run_unit((int)tkA * kDkShards + shard);
+    griddep_wait();
+    if (more) {
+        uint32_t tkB = nsm + atomicAdd(ctr, 1u);
+        while (true) {
+            tkA = nsm + atomicAdd(ctr, 1u);
+            if (!run_unit((int)tkB * kDkShards + shard)) break;
+            tkB = nsm + atomicAdd(ctr, 1u);
+            if (!run_unit((int)tkA * kDkShards + shard)) break;
+        }
     }
     if (ok) {
         __threadfence_block();
@@ -480,6 +488,7 @@ __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
     const DPend *pend = reinterpret_cast<const DPend *>(smem + L.pend);
     const DHeader *hdrs = reinterpret_cast<const DHeader *>(smem + L.hdrs);
     uint8_t *ring = smem + L.ring;
+    griddep_wait();  // the ready counts of the preceding launch's workspace use
     uint64_t t_last = global_timer_ns();
     uint32_t issued = 0, ipar = 0;  // copies in flight (bit j) and their hfull phase parity
     // On an abort the block exits early: wait (bounded) for this warp's copies first.
@@ -699,6 +708,9 @@ __device__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *s
 template <int MS>
 __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    // A launch that follows on the stream may be scheduled as SMs free up; it
+    // reads nothing of this one before its own griddepcontrol.wait.
+    griddep_launch_dependents();
     const int nst = p.nstages;
     const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -711,9 +723,6 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     int *scnt = reinterpret_cast<int *>(smem + L.scnt);
     volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
     float *sacc = reinterpret_cast<float *>(smem + L.sacc);
-    // given logits whose bytes make whole 16-byte units come in by one bulk copy
-    const bool lg_bulk = p.logits && !p.logits_dep && ((p.T * p.E * 4) & 15) == 0 &&
-                         (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
     for (int i = threadIdx.x; i < nst * L.slot_floats; i += kDkThreads) sacc[i] = 0.f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -731,15 +740,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         }
         DHeader *hw = reinterpret_cast<DHeader *>(smem + L.hdrs);
         for (int st = 0; st < nst; ++st) hw[st].seq = -1;  // no fill yet (shared memory is not cleared)
-        mbar_init(allbar + 1, 1);
         fence_mbar_init();
-        if (lg_bulk) {
-            // the launch's logits, ahead of every weight copy (a load issued
-            // behind the weight stream waits for it in the memory queues)
-            const uint32_t bytes = (uint32_t)(p.T * p.E * 4);
-            mbar_arrive_expect_tx(allbar + 1, bytes);
-            bulk_g2s(smem + L.rsv, p.logits, bytes, allbar + 1, policy_evict_last());
-        }
     }
     __syncthreads();
     if (warp == kDkCons) {
@@ -766,6 +767,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     const int H = p.H, I = p.I, T = p.T, xstr = L.xs_stride;
     const int ctid = threadIdx.x;
     const DkGeom geo = dk_geom(H, I, p.S, p.I_s);
+    griddep_wait();  // x, the logits and the workspace may come from the preceding launch
 
     // x into shared memory, and its sums over each group of 128 (16 chunks of
     // 8 = one half-warp, as the stride is a multiple of 16 chunks)
@@ -803,20 +805,14 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     };
     if (p.logits) {
         if (warp < T) {
-            if (p.logits_dep) griddep_wait();  // the logits come from the preceding launch
             int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
             float *rpw = reinterpret_cast<float *>(smem + L.rpw);
             const int E = p.E, k = p.k;
             int mine = 0;
-            if (lg_bulk) mbar_wait_bounded(allbar + 1, 0, abort_flag, &p.hdr->status, p.wait_budget_ns);
             for (int t = warp; t < T; t += kDkCons, ++mine) {
                 const float *lg = p.logits + (size_t)t * E;
-                float *sv = reinterpret_cast<float *>(smem + L.rsv) + t * E;
-                if (lg_bulk)
-                    select_token([&](int e) { return sv[e]; }, E, k, p.renorm, lane, rids + t * k, rpw + t * k, sv);
-                else
-                    select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k,
-                                 rpw + t * k, sv);
+                select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k, rpw + t * k,
+                             reinterpret_cast<float *>(smem + L.rsv) + t * E);
                 if (blockIdx.x == 0 && lane == 0)
                     for (int r = 0; r < k; ++r) {
                         const int e = rids[t * k + r];

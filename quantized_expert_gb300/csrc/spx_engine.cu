@@ -132,6 +132,11 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     uint8_t *ring = smem + L.ring;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.misc);
     const uint64_t pol = policy_evict_first();
+    // The activations, the routing and the workspace may all come from the
+    // launch this one follows (which may itself have started early): wait
+    // for it before anything else.  The consumers touch global memory only
+    // after the activation rows, which are copied after this wait.
+    griddep_wait();
     {
         // the activation rows [T][H] -> shared rows of H + 8 halves, ahead of
         // the weights (every block reads them: kept in L2)
@@ -375,6 +380,9 @@ __device__ __forceinline__ void group_sync(const EngineParams &p, Sync &sy, vola
 template <int RFMT, int MS4, int NT>
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    // A launch that follows on the stream may be scheduled as SMs free up; it
+    // reads nothing of this one before its own griddepcontrol.wait.
+    griddep_launch_dependents();
     const bool has_w4 = RFMT == FMT_W4 && p.routed_enabled;
     const int smax = engine_smax(has_w4, p.S);
     const int G = p.groups, nsg = p.nstages;

@@ -301,7 +301,7 @@ struct EngineParams {
     uint64_t wait_budget_ns;
 };
 
-int launch_route(const RouteParams &p, cudaStream_t s);
+int launch_route(const RouteParams &p, cudaStream_t s, bool pdl);
 int route_validate(const uint16_t *x, const uint16_t *w_router, const float *logits, int T, int H, int E, int k,
                    const int32_t *ids, const float *w);
 int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl);
@@ -323,7 +323,8 @@ bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1);
 size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max);
 // rt == nullptr: routing from e.active / e.n_active and the token tables e.tables.
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s);
-int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s);
+int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s,
+                         bool pdl);
 int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int32_t *active,
                   const int32_t *n_active, int T, int k, int E, TokTable *tables, cudaStream_t s);
 

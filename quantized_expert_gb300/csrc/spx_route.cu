@@ -180,8 +180,10 @@ __device__ void select_block(const RouteParams &p) {
 
 __global__ void __launch_bounds__(1024) route_kernel(const RouteParams p) {
     // Let a programmatically dependent expert launch start its routing-
-    // independent work (shared expert) while this one runs.
+    // independent work (shared expert) while this one runs; this one reads
+    // nothing before the launch it follows has completed.
     griddep_launch_dependents();
+    griddep_wait();
     if (p.w_router) {
         router_row_block(p.x, p.w_router, p.T, p.H, p.E, p.logits);
         __shared__ int s_last;
@@ -203,13 +205,30 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteParams p) {
 __global__ void __launch_bounds__(256) router_logits_kernel(const __half *x, const __half *wr, int T, int H, int E,
                                                             float *logits) {
     griddep_launch_dependents();
+    griddep_wait();
     router_row_block(x, wr, T, H, E, logits);
 }
 
-int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s) {
+// pdl: the launch may begin while the preceding one on the stream finishes
+// (programmatic dependent launch; the kernel waits for it before reading).
+static cudaLaunchConfig_t small_launch(dim3 grid, dim3 block, cudaStream_t s, bool pdl, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cfg;
+}
+
+int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E, float *logits, cudaStream_t s,
+                         bool pdl) {
     if (T < 1 || T > 8) return SPX_ERR_UNSUPPORTED;
-    router_logits_kernel<<<E, 256, 0, s>>>(x, wr, T, H, E, logits);
-    return record_launch(cudaGetLastError());
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = small_launch(dim3(E), dim3(256), s, pdl, attr);
+    return record_launch(cudaLaunchKernelEx(&cfg, router_logits_kernel, x, wr, T, H, E, logits));
 }
 
 __global__ void __launch_bounds__(256) elb_kernel(uint32_t *elb, int E, int layer, const int32_t *ids, int n) {
@@ -241,11 +260,12 @@ static int check_route_shape(int T, int H, int E, int k) {
 
 // One warp per token in the selecting block (at least 8 warps, at most 32);
 // with a router weight one block per expert row, the last to finish selects.
-int launch_route(const RouteParams &p, cudaStream_t s) {
+int launch_route(const RouteParams &p, cudaStream_t s, bool pdl) {
     const int grid = p.w_router ? p.E : 1;
     const int threads = 32 * (p.T < 8 ? 8 : (p.T > 32 ? 32 : p.T));
-    route_kernel<<<grid, threads, 0, s>>>(p);
-    return record_launch(cudaGetLastError());
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = small_launch(dim3(grid), dim3(threads), s, pdl, attr);
+    return record_launch(cudaLaunchKernelEx(&cfg, route_kernel, p));
 }
 
 int route_validate(const uint16_t *x, const uint16_t *w_router, const float *logits, int T, int H, int E, int k,
@@ -283,7 +303,7 @@ extern "C" int spx_route_topk(const uint16_t *x, const uint16_t *w_router, float
     p.topk_ids = topk_ids;
     p.topk_w = topk_w;
     p.hdr = reinterpret_cast<WsHeader *>(ws);
-    return launch_route(p, reinterpret_cast<cudaStream_t>(stream));
+    return launch_route(p, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" int spx_elb_accumulate(uint32_t *elb, int L, int E, int layer, const int32_t *topk_ids, int T, int k,
