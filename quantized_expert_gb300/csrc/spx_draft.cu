@@ -768,6 +768,10 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     const int ctid = threadIdx.x;
     const DkGeom geo = dk_geom(H, I, p.S, p.I_s);
     griddep_wait();  // x, the logits and the workspace may come from the preceding launch
+    // one token over at most 64 experts: every consumer warp ranks a share
+    const bool sel_all = p.logits && T == 1 && p.E <= 8 * kDkCons && p.E <= 64 && p.k <= 32;
+    float *sv0 = reinterpret_cast<float *>(smem + L.rsv);
+    if (sel_all && ctid < p.E) sv0[ctid] = __ldcg(p.logits + ctid);
 
     // x into shared memory, and its sums over each group of 128 (16 chunks of
     // 8 = one half-warp, as the stride is a multiple of 16 chunks)
@@ -803,7 +807,28 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             *reinterpret_cast<volatile int *>(misc + 4) = 1;
         }
     };
-    if (p.logits) {
+    if (sel_all) {
+        int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
+        float *rpw = reinterpret_cast<float *>(smem + L.rpw);
+        const int E = p.E, k = p.k;
+        if (warp < (E + 7) / 8) select_rank_warp(sv0, E, k, warp, lane, rids, rpw);
+        all_sync();  // every expert ranked
+        if (warp == 0) {
+            if (lane == 0 && p.renorm) {
+                float psel = 0.f;
+                for (int r = 0; r < k; ++r) psel += rpw[r];
+                for (int r = 0; r < k; ++r) rpw[r] = rpw[r] / psel;
+            }
+            __syncwarp();
+            if (blockIdx.x == 0 && lane < k) {
+                const int e = rids[lane];
+                p.topk_ids[lane] = e;
+                p.topk_w[lane] = rpw[lane];
+                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
+            }
+            publish_routing(route_tables_warp(p, L, smem, lane, blockIdx.x == 0));
+        }
+    } else if (p.logits) {
         if (warp < T) {
             int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
             float *rpw = reinterpret_cast<float *>(smem + L.rpw);

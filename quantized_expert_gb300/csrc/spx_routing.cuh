@@ -82,6 +82,48 @@ __device__ __forceinline__ void select_token_n(Logit lg, int E, int k, int renor
     __syncwarp();
 }
 
+// Selection for one token by several warps of a block (E <= 64): sv holds
+// the token's E logits in shared memory.  Each calling warp computes the
+// maximum and the softmax sum exactly as select_token_n does, and ranks eight
+// experts e = 8 w + lane/4 (four lanes per expert, each counting a quarter
+// of the others; rank = experts before e in the order value descending,
+// index ascending); the lane holding a rank-r expert (r < k) writes ids[r]
+// and its softmax weight w[r] (renormalisation is left to the caller, once
+// every warp is done).  Warps w >= E/8 have nothing to rank and may skip it.
+__device__ __forceinline__ void select_rank_warp(const float *sv, int E, int k, int w, int lane, int32_t *ids,
+                                                 float *wout) {
+    float v[2];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? sv[e] : -INFINITY;
+        if (e < E) m = fmaxf(m, v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        if (lane + 32 * j < E) z += expf(v[j] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const int e = 8 * w + (lane >> 2), q = lane & 3;
+    const float ve = e < E ? sv[e] : 0.f;
+    int rank = 0;
+    if (e < E)
+        for (int e2 = q; e2 < E; e2 += 4) {
+            const float u = sv[e2];
+            rank += (u > ve || (u == ve && e2 < e)) ? 1 : 0;
+        }
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    if (e < E && q == 0 && rank < k) {
+        ids[rank] = e;
+        wout[rank] = expf(ve - m) / z;
+    }
+}
+
 template <class Logit>
 __device__ __forceinline__ void select_token(Logit lg, int E, int k, int renorm, int lane, int32_t *ids, float *w,
                                              float *sv) {
