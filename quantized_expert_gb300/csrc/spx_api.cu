@@ -288,7 +288,6 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         DraftRouting rt{};
         rt.logits = a->logits;
         rt.renorm = a->renorm;
-        rt.logits_dep = a->w_router ? 1 : 0;
         rt.topk_ids = a->topk_ids;
         rt.topk_w = a->topk_w;
         rt.elb = a->elb;

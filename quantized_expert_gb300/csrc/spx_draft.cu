@@ -193,7 +193,7 @@ struct DkParams {
     int mode;  // 0: rows of y_sorted, scale 1; 2: weighted into the fp32 accumulator, last block writes out
     // routing inside the launch (logits != nullptr) and its outputs (block 0)
     const float *logits;
-    int renorm, logits_dep;
+    int renorm;
     int32_t *topk_ids;
     float *topk_w;
     uint32_t *elb;
@@ -1285,7 +1285,6 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     if (rt) {
         p.logits = rt->logits;
         p.renorm = rt->renorm;
-        p.logits_dep = rt->logits_dep;
         p.topk_ids = rt->topk_ids;
         p.topk_w = rt->topk_w;
         p.elb = rt->elb;

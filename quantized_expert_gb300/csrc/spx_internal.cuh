@@ -312,7 +312,6 @@ int engine_nt(int T);
 struct DraftRouting {
     const float *logits;  // [T][E]
     int renorm;
-    int logits_dep;       // 1: the logits come from the preceding launch (wait for it)
     int32_t *topk_ids;
     float *topk_w;
     uint32_t *elb;        // nullable
