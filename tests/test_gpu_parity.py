@@ -387,3 +387,44 @@ def test_invalid_arguments_rejected():
     with pytest.raises(SpxError) as ei:
         spx.spx_moe_verify_fp16(torch.zeros(4, 200, dtype=torch.float16, device="cuda"), p_bad, 2, z, z, z, z, y, ws)
     assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
+
+
+def test_chained_layer_calls_back_to_back():
+    """Layer calls back to back on one stream, each taking the previous call's
+    output as its activations and sharing its workspace (a launch may start
+    before the one it follows has finished, so it must not read activations,
+    routing or workspace before then).  Draft calls at T = 1 (draft launch)
+    and T = 9 (routing + expert launch), verify calls at T = 9; each call is
+    checked against the oracle on the input it was given, and the draft calls'
+    Expert Lookahead Buffer counts against the oracle's routing."""
+    spx, gh = _spx(), _gh()
+    s = _small("qwen15_moe", H=512, I=256, E=8, I_s=256)  # router product: routing follows x
+    lay = gh.Layer(s)
+    L = 2
+    elb = torch.zeros(L, s.E, dtype=torch.int32, device="cuda")
+    chains = [("draft", 1, 2), ("verify", 9, 2), ("draft", 9, 2), ("draft", 1, 2)]  # outputs shrink ~10x a layer
+    calls, keep = [], []
+    for mode, T, n in chains:
+        ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+        x = gh.dev_f16(W.gen_x(s, T, step=10 + T, which=int(mode == "verify")))
+        for j in range(n):
+            out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+            r = spx.Routing.empty(T, s.E, s.k)
+            lg = torch.empty(T, s.E, dtype=torch.float32, device="cuda")
+            args, kp = spx.layer_args(0 if mode == "draft" else 1, x, s.E, s.k, s.renorm, lg, r, out, ws,
+                                      w4=lay.w4, f16=lay.f16, shared=lay.shared, w_router=lay.w_router,
+                                      elb=elb if mode == "draft" else None, layer=j)
+            spx.spx_moe_layer(args)  # no synchronisation between the calls
+            calls.append((mode, T, j, x, out, r))
+            keep.append((args, kp, lg, ws))
+            x = out
+    torch.cuda.synchronize()
+    elb_ref = np.zeros((L, s.E), np.uint32)
+    for mode, T, j, x, out, r in calls:
+        xin = x.cpu().numpy().view(np.uint16)
+        ref = lay.oracle_layer(mode, xin)
+        assert np.array_equal(r.topk_ids.cpu().numpy(), ref["ids"]), (mode, T, j)
+        gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), f"chain {mode} T={T} #{j}")
+        if mode == "draft":
+            oracle.elb_accumulate(elb_ref, j, ref["ids"])
+    assert np.array_equal(elb.cpu().numpy().astype(np.uint32), elb_ref)
