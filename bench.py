@@ -601,6 +601,84 @@ def run_loop(args):
     print(json.dumps({"loop": args.loop, "config": s.name, "calls": args.loop_n}), flush=True)
 
 
+def run_cached(args):
+    """Cache-aware verify execution: the verify layer with its routed experts
+    queued resident first (resident = the experts the K draft steps before it
+    selected, i.e. the lookahead counters' nonzero entries) and a ready flag
+    per expert (all set), against the plain verify layer on the same inputs.
+    Prints one JSON line: device us per layer of both, and the share of the
+    verify's routed experts that were resident."""
+    import torch
+    from quantized_expert_gb300 import build as B, spx
+    B.build()
+    spx.load()
+    s = W.CONFIGS[args.config]
+    Tv = s.T_verify
+    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
+    inputs = [make_inputs(s, i) for i in range(NINPUTS)]
+    if "lg_d" not in inputs[0]:
+        print(json.dumps({"metric": "cache-aware verify", "unavailable": "shape computes its logits on the device"}))
+        return
+    # resident experts: union of the draft top-k of K = T_verify - 1 draft steps
+    K = Tv - 1
+    ids = [oracle_free_topk(inputs[i]["lg_d"], s.k) for i in range(K)]
+    res = np.zeros(s.E, np.uint8)
+    for x in ids:
+        res[x.reshape(-1)] = 1
+    resident = torch.from_numpy(res).cuda()
+    ready = torch.ones(s.E, dtype=torch.int32, device="cuda")
+    ws = spx.new_workspace(Tv, s.H, s.I, s.E, s.k, s.I_s)
+    r = spx.Routing.empty(Tv, s.E, s.k)
+    out = torch.empty(Tv, s.H, dtype=torch.float16, device="cuda")
+    dev = []
+    for d in inputs:
+        dev.append((torch.from_numpy(np.ascontiguousarray(d["x_v"]).view(np.float16)).cuda(),
+                    torch.from_numpy(d["lg_v"]).cuda()))
+    hits = []
+    for i in range(NINPUTS):
+        top = oracle_free_topk(inputs[i]["lg_v"], s.k)
+        u = np.unique(top)
+        hits.append(float(res[u].mean()))
+
+    def calls(cached):
+        return [spx.layer_args(1, dev[i % NINPUTS][0], s.E, s.k, s.renorm, dev[i % NINPUTS][1], r, out, ws,
+                               f16=sets[i % NSETS]["f16"], shared=sets[i % NSETS]["shared"],
+                               resident=resident if cached else None, ready=ready if cached else None)
+                for i in range(NSETS * NINPUTS)]
+
+    res_us = {}
+    stream = torch.cuda.Stream()
+    for name, cached in (("plain", False), ("cached", True)):
+        keep = calls(cached)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                spx.spx_moe_layer(keep[i % len(keep)][0], stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                spx.spx_moe_layer(keep[i % len(keep)][0], stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res_us[name] = e0.elapsed_time(e1) * 1e3 / args.steps
+    assert spx.spx_workspace_status(ws) == 0
+    line = {"metric": "cache-aware verify layer (resident first + ready flags) vs plain, device us per layer",
+            "config": {"workload": f"{s.name} verify T={Tv}", "resident": f"draft top-{s.k} of {K} steps",
+                       "resident_experts": int(res.sum())},
+            "plain_us": round(res_us["plain"], 2), "cached_us": round(res_us["cached"], 2),
+            "overhead_pct": round(100 * (res_us["cached"] / res_us["plain"] - 1), 2),
+            "verify_expert_hit_share": round(float(np.mean(hits)), 3), "steps": args.steps, "warmup": args.warmup}
+    print(json.dumps(line), flush=True)
+
+
+def oracle_free_topk(lg, k):
+    """Top-k expert ids of fp32 logits (value descending, index ascending), for
+    choosing the resident set; no method arithmetic beyond the ordering."""
+    lg = np.asarray(lg, np.float32)
+    order = np.lexsort((np.arange(lg.shape[-1])[None, :].repeat(lg.shape[0], 0), -lg), axis=-1)
+    return order[:, :k]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -613,10 +691,13 @@ def main():
     ap.add_argument("--loop", choices=["draft", "verify"], help="profiling driver: layer calls only, no timing")
     ap.add_argument("--cycle", action="store_true", help="the 26-layer draft-then-verify cycle (prints its own line)")
     ap.add_argument("--loop-n", type=int, default=12)
+    ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
     if args.loop:
         run_loop(args)
+    elif args.cached:
+        run_cached(args)
     elif args.cycle:
         run_cycle(args)
     elif args.impl == "reference":

@@ -260,13 +260,33 @@ typedef struct {
      * the two launches removes their programmatic overlap). */
     void *ev_experts_begin;
     void *ev_experts_end;
+    /* Cache-aware expert execution [P1 Key Contributions 3-4: experts the
+     * lookahead saw are cache hits and run first; misses wait for their
+     * weights].  Both nullable; when either is set the layer runs as a routing
+     * launch plus the expert launch (also for draft calls of T <= 8).
+     *   resident [E] uint8: nonzero = expert e's weights are resident; the
+     *     routed experts are queued resident first, then the others, each in
+     *     ascending expert order.  Only the order changes, not the result.
+     *   ready [E] uint32: before it streams expert e's weights the expert
+     *     launch waits until ready[e] is nonzero (the caller sets it once the
+     *     weights have landed, e.g. by a copy on another stream); a wait longer
+     *     than the bound below stops the launch with SPX_ERR_TIMEOUT in the
+     *     workspace status word (the output is then undefined). */
+    const uint8_t *resident;
+    const uint32_t *ready;
+    /* Bound of every device-side wait of the call in ns; 0 = 2 s. */
+    uint64_t wait_budget_ns;
 } spx_layer_args;
 
-/* Two launches: a routing launch (router product when w_router is given,
- * softmax, top-k, counters, counting sort) and one persistent expert launch
- * that streams the shared expert first (it does not depend on routing; the
- * launch is made programmatically dependent so that this overlaps routing),
- * then every active expert's units, and writes out[] from its last block. */
+/* One layer.  Draft calls with T <= 8 (and no cache-aware options) are one
+ * launch that routes its tokens in every block (after a router-product launch
+ * when w_router is given); other calls are a routing launch (router product,
+ * softmax, top-k, counters, counting sort, token tables) and one persistent
+ * expert launch that streams the shared expert first, then every active
+ * expert's units, and writes out[] from its last blocks.  Every launch of the
+ * call may begin while the one before it on the stream finishes (programmatic
+ * dependent launch): it reads nothing that launch writes before it has
+ * completed. */
 SPX_API int spx_moe_layer(const spx_layer_args *args, spx_stream_t stream);
 
 /* The same layer for callers that cannot allocate device memory (code running

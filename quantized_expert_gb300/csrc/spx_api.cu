@@ -83,13 +83,13 @@ extern "C" const char *spx_status_string(int st) {
     }
 }
 
-extern "C" int spx_version(void) { return 100; }
+extern "C" int spx_version(void) { return 101; }
 
 extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
-static size_t ws_scratch_base(int T, int H) { return ws_tables_offset(T, H) + (size_t)kMaxE * kTableBytes; }
+static size_t ws_scratch_base(int T, int H) { return ws_order_offset(T, H) + (size_t)kMaxE * 4; }
 
 extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
     if (T < 1 || H < 1 || T > kMaxT || H > kMaxH || I < 0 || E < 1 || k < 1 || I_s < 0) return 0;
@@ -275,8 +275,10 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     if (reinterpret_cast<uintptr_t>(a->out) & 7) return SPX_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool timed = a->ev_experts_begin || a->ev_experts_end;
+    const bool cache_aware = a->resident || a->ready;
+    const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
 
-    if (a->mode == 0 && draft_supported(T, H, I, S, I_s, E, k)) {
+    if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k)) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch
         // computes the logits first and the draft launch overlaps it.
@@ -311,6 +313,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         p.mode = 2;
         p.yout = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
         p.out = reinterpret_cast<__half *>(a->out);
+        p.wait_budget_ns = budget;
         if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
             return SPX_ERR_CUDA;
         st = launch_draft(p, &rt, ws_scratch_base(T, H), !timed, s);
@@ -339,6 +342,10 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     rp.active = a->active;
     rp.n_active = a->n_active;
     rp.tables = ws_tables(a->ws, T, H);
+    if (a->resident) {
+        rp.resident = a->resident;
+        rp.order = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a->ws) + ws_order_offset(T, H));
+    }
     rp.hdr = static_cast<WsHeader *>(a->ws);
     st = launch_route(rp, s, !timed);
     if (st) return st;
@@ -354,6 +361,9 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     p.routed_enabled = 1;
     p.active = a->active;
     p.n_active = a->n_active;
+    p.order = rp.order;
+    p.ready = a->ready;
+    p.wait_budget_ns = budget;
     p.tables = ws_tables(a->ws, T, H);
     if (a->shared) {
         p.shared = static_cast<const uint8_t *>(a->shared->packed);

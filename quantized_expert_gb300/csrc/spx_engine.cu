@@ -110,6 +110,12 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
 }
 
 // ------------------------------------------------------------- producer --
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // One lane feeds every group's ring.  Each group has its own unit stream:
 // units come from the block's share of the global dynamic queue (one unit is
 // dequeued ahead per group so its latency overlaps the copies), and chunks are
@@ -193,9 +199,28 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             routed_slot(u - n_sh, a, i, ns);
             if (a < p.E) {
                 griddep_wait();  // routing results of the preceding launch
-                e = __ldcg(p.active + a);
+                e = __ldcg((p.order ? p.order : p.active) + a);
             }
         }
+    };
+    // Cache-aware calls: expert e's weights may be read once ready[e] is set
+    // (bounded wait; on expiry the status word records SPX_ERR_TIMEOUT and the
+    // block stops).  The acquire orders the flag before the weights, the proxy
+    // fence before the bulk copies that read them.
+    auto ready_wait = [&](int e) -> bool {
+        if (ld_acquire_u32(p.ready + e) == 0u) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_u32(p.ready + e) == 0u) {
+                if (*abort_flag || global_timer_ns() - t0 > p.wait_budget_ns) {
+                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    return false;
+                }
+                __nanosleep(256);
+            }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        return true;
     };
     auto valid_unit = [&](int u) -> bool { return u >= 0 && (u < n_sh || u < total_units()); };
 
@@ -215,7 +240,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     const long long budget = (long long)p.wait_budget_ns * 2;  // cycles at ~2 GHz
     bool aborted = false;
     while (true) {
-        bool all_done = true, progressed = false;
+        bool all_done = true, progressed = false, stop = false;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             Stream &S_ = s[g];
@@ -243,6 +268,10 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                 resolve(S_.next_u, S_.next_e);
                 S_.pend_u = fetch();
                 if (u >= n_sh && (e < 0 || e >= p.E)) continue;  // unusable routing entry: skip the unit
+                if (p.ready && u >= n_sh && !ready_wait(e)) {
+                    stop = true;
+                    break;
+                }
                 S_.u = u;
                 S_.e = u < n_sh ? 0 : e;
                 S_.fmt = u < n_sh ? FMT_F16 : p.routed_fmt;
@@ -332,6 +361,10 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             if (meta_bytes) bulk_g2s(dst + chunk, meta, meta_bytes, &full[st], pol);
             S_.it++;
             progressed = true;
+        }
+        if (stop) {
+            aborted = true;
+            break;
         }
         if (all_done) break;
         if (progressed) {

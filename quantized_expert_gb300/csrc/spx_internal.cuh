@@ -93,6 +93,11 @@ static_assert(kTableBytes % 16 == 0, "table is bulk-copied");
 __host__ __device__ inline size_t ws_tables_offset(int T, int H) {
     return kWsAccOffset + ((size_t)T * H * 4 + 255) / 256 * 256;
 }
+// After the token tables: the expert launch's queue order of the active
+// experts (kMaxE ints; cache-aware calls).
+__host__ __device__ inline size_t ws_order_offset(int T, int H) {
+    return ws_tables_offset(T, H) + (size_t)kMaxE * kTableBytes;
+}
 
 // Physical output column of row m (0..15) of down tile mt: tile pair P = mt/2
 // covers 32 columns; rows (g, g+8) of tile q land on columns 4g+2q, 4g+2q+1,
@@ -268,6 +273,8 @@ struct RouteParams {
     int layer;
     int32_t *counts, *offsets, *sorted_slots, *active, *n_active;  // all or none
     TokTable *tables;  // nullable: per-expert token tables (row = token, scale = weight)
+    const uint8_t *resident;  // nullable (with order): resident experts are queued first
+    int32_t *order;           // nullable: queue order of the active experts (expert launch)
     WsHeader *hdr;
 };
 
@@ -280,6 +287,8 @@ struct EngineParams {
     int E, I, k;
     int routed_enabled;
     const int32_t *active, *n_active;
+    const int32_t *order;    // nullable: queue order of the active experts (else active)
+    const uint32_t *ready;   // nullable: wait for ready[e] != 0 before streaming expert e
     const TokTable *tables;  // per expert, in the workspace
     // shared expert (FP16, S = 16), nullable
     const uint8_t *shared;

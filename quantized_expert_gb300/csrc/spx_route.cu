@@ -77,10 +77,12 @@ __device__ void router_row_block(const __half *x, const __half *wr, int T, int H
 // gather arrays.  Whole block participates.
 __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts, int32_t *offsets,
                              int32_t *sorted_slots, int32_t *active, int32_t *n_active, int k = 1,
-                             const float *s_w = nullptr, TokTable *tables = nullptr) {
+                             const float *s_w = nullptr, TokTable *tables = nullptr,
+                             const uint8_t *resident = nullptr, int32_t *order = nullptr) {
     __shared__ int s_cnt[kMaxE];
     __shared__ int s_off[kMaxE + 1];
     __shared__ int s_act[kMaxE];
+    __shared__ int s_na;
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
     __syncthreads();
@@ -123,6 +125,7 @@ __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts
         if (lane == 31) {
             s_off[E] = ic;
             *n_active = jf;
+            s_na = jf;
             for (int a = jf; a < E; ++a) s_act[a] = -1;
         }
     }
@@ -152,6 +155,23 @@ __device__ void gather_block(const int32_t *s_ids, int n, int E, int32_t *counts
     if (tables)
         for (int e = tid; e < E; e += blockDim.x)
             if (s_cnt[e] > 0) tables[e].n = s_cnt[e];
+    if (order) {
+        // the expert launch's queue: resident experts first, then the others,
+        // each in ascending expert order (the active list's order)
+        __shared__ unsigned char s_res[kMaxE];
+        const int na = s_na;
+        for (int a = tid; a < na; a += blockDim.x) s_res[a] = resident[s_act[a]] != 0;
+        __syncthreads();
+        for (int a = tid; a < na; a += blockDim.x) {
+            const int r = s_res[a];
+            int before = 0, nres = 0;
+            for (int a2 = 0; a2 < na; ++a2) {
+                nres += s_res[a2];
+                before += (a2 < a && s_res[a2] == r) ? 1 : 0;
+            }
+            order[r ? before : nres + before] = s_act[a];
+        }
+    }
 }
 
 // Softmax, top-k, weights, counters and gather; one block.
@@ -175,7 +195,7 @@ __device__ void select_block(const RouteParams &p) {
     __syncthreads();
     if (p.counts)
         gather_block(s_ids, p.T * p.k, p.E, p.counts, p.offsets, p.sorted_slots, p.active, p.n_active, p.k, s_pw,
-                     p.tables);
+                     p.tables, p.resident, p.order);
 }
 
 __global__ void __launch_bounds__(1024) route_kernel(const RouteParams p) {

@@ -47,7 +47,8 @@ class LayerArgs(C.Structure):
                 ("topk_ids", C.c_void_p), ("topk_w", C.c_void_p), ("counts", C.c_void_p),
                 ("offsets", C.c_void_p), ("sorted_slots", C.c_void_p), ("active", C.c_void_p),
                 ("n_active", C.c_void_p), ("out", C.c_void_p), ("ws", C.c_void_p), ("ws_bytes", C.c_size_t),
-                ("ev_experts_begin", C.c_void_p), ("ev_experts_end", C.c_void_p)]
+                ("ev_experts_begin", C.c_void_p), ("ev_experts_end", C.c_void_p),
+                ("resident", C.c_void_p), ("ready", C.c_void_p), ("wait_budget_ns", C.c_uint64)]
 
 
 _SIGS = {
@@ -304,8 +305,11 @@ class Routing:
 
 def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: PackedW4 | None = None,
                f16: PackedF16 | None = None, shared: PackedShared | None = None, w_router=None, elb=None,
-               layer=0, events=None):
-    """Build (and keep alive) the argument block of one spx_moe_layer call."""
+               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0):
+    """Build (and keep alive) the argument block of one spx_moe_layer call.
+    resident (uint8 [E]) and ready (int32/uint32 [E]) are the optional
+    cache-aware expert order and ready flags; wait_budget_ns bounds every
+    device-side wait (0 = the library default)."""
     T, H = x.shape
     keep = []
     a = LayerArgs()
@@ -332,6 +336,7 @@ def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: Pac
     if events is not None:
         a.ev_experts_begin, a.ev_experts_end = events[0].cuda_event, events[1].cuda_event
         keep.append(events)
+    a.resident, a.ready, a.wait_budget_ns = _p(resident), _p(ready), int(wait_budget_ns)
     return a, keep
 
 

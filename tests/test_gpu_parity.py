@@ -428,3 +428,92 @@ def test_chained_layer_calls_back_to_back():
         if mode == "draft":
             oracle.elb_accumulate(elb_ref, j, ref["ids"])
     assert np.array_equal(elb.cpu().numpy().astype(np.uint32), elb_ref)
+
+
+def _cache_case(mode, T):
+    s = _small("deepseek_v2_lite", I=256, E=16, I_s=512)
+    x = W.gen_x(s, T, step=30 + T, which=int(mode == "verify"))
+    logits = W.gen_logits(s, T, step=30 + T, which=int(mode == "verify"))
+    need = _gh().needed_experts(s, [logits], [x])
+    lay = _gh().Layer(s, needed=need)
+    return s, x, logits, lay
+
+
+@pytest.mark.parametrize("mode,T", [("verify", 17), ("draft", 1), ("draft", 9)])
+def test_cache_aware_order_and_ready_flags(mode, T):
+    """Cache-aware calls (resident experts queued first, a ready flag per
+    expert, all set): the same routing outputs and layer output as the oracle
+    (the order changes no result); draft calls take the routing + expert
+    launch path."""
+    spx, gh = _spx(), _gh()
+    s, x, logits, lay = _cache_case(mode, T)
+    ref = lay.oracle_layer(mode, x, logits=logits)
+    rng = np.random.default_rng(T)
+    resident = torch.from_numpy((rng.random(s.E) < 0.5).astype(np.uint8)).cuda()
+    ready = torch.ones(s.E, dtype=torch.int32, device="cuda")
+    r = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    args, keep = spx.layer_args(0 if mode == "draft" else 1, gh.dev_f16(x), s.E, s.k, s.renorm, gh.dev(logits), r,
+                                out, ws, w4=lay.w4, f16=lay.f16, shared=lay.shared, resident=resident, ready=ready)
+    for rep in range(2):
+        spx.spx_moe_layer(args)
+        torch.cuda.synchronize()
+        assert np.array_equal(r.topk_ids.cpu().numpy(), ref["ids"])
+        assert np.array_equal(r.sorted_slots.cpu().numpy(), ref["gather"]["sorted_slots"])
+        gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), f"cache {mode} {rep}")
+    assert spx.spx_workspace_status(ws) == 0
+
+
+def test_cache_aware_ready_flags_set_late():
+    """Ready flags that land while the call runs (a host-to-device copy on
+    another stream, issued after the call, no kernel involved): the expert
+    launch waits for them and the result matches the oracle."""
+    import time
+    spx, gh = _spx(), _gh()
+    s, x, logits, lay = _cache_case("verify", 17)
+    ref = lay.oracle_layer("verify", x, logits=logits)
+    ready = torch.zeros(s.E, dtype=torch.int32, device="cuda")
+    ones = torch.ones(s.E, dtype=torch.int32).pin_memory()
+    r = spx.Routing.empty(17, s.E, s.k)
+    out = torch.empty(17, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(17, s.H, s.I, s.E, s.k, s.I_s)
+    args, keep = spx.layer_args(1, gh.dev_f16(x), s.E, s.k, s.renorm, gh.dev(logits), r, out, ws, f16=lay.f16,
+                                shared=lay.shared, ready=ready)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    spx.spx_moe_layer(args)
+    time.sleep(0.005)
+    with torch.cuda.stream(side):
+        ready.copy_(ones, non_blocking=True)
+    torch.cuda.synchronize()
+    assert spx.spx_workspace_status(ws) == 0
+    gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), "ready set late")
+
+
+def test_cache_aware_ready_flag_never_set_times_out():
+    """An active expert whose ready flag nothing sets: the expert launch gives
+    up after the call's wait bound with SPX_ERR_TIMEOUT in the status word, the
+    context stays usable, and a call on a re-zeroed workspace succeeds."""
+    spx, gh = _spx(), _gh()
+    s, x, logits, lay = _cache_case("verify", 17)
+    ref = lay.oracle_layer("verify", x, logits=logits)
+    missing = int(ref["ids"][0, 0])
+    ready = torch.ones(s.E, dtype=torch.int32, device="cuda")
+    ready[missing] = 0
+    r = spx.Routing.empty(17, s.E, s.k)
+    out = torch.empty(17, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(17, s.H, s.I, s.E, s.k, s.I_s)
+    dx, dl = gh.dev_f16(x), gh.dev(logits)
+    args, keep = spx.layer_args(1, dx, s.E, s.k, s.renorm, dl, r, out, ws, f16=lay.f16, shared=lay.shared,
+                                ready=ready, wait_budget_ns=20_000_000)
+    spx.spx_moe_layer(args)
+    torch.cuda.synchronize()
+    assert spx.spx_workspace_status(ws) == spx.SPX_ERR_TIMEOUT
+    assert np.array_equal(r.topk_ids.cpu().numpy(), ref["ids"])  # routing ran before the wait
+    spx.spx_workspace_init(ws)
+    args2, keep2 = spx.layer_args(1, dx, s.E, s.k, s.renorm, dl, r, out, ws, f16=lay.f16, shared=lay.shared)
+    spx.spx_moe_layer(args2)
+    torch.cuda.synchronize()
+    assert spx.spx_workspace_status(ws) == 0
+    gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), "after a timeout")
