@@ -671,6 +671,58 @@ def run_cached(args):
     print(json.dumps(line), flush=True)
 
 
+def run_draft_batch(args):
+    """Draft layers carrying T = 1, 2, 4, 8 tokens (one per request) in one
+    call: device us per layer, unique experts, algorithmic GB/s and draft
+    tokens/s.  Prints one JSON line."""
+    import torch
+    from quantized_expert_gb300 import build as B, spx
+    B.build()
+    spx.load()
+    s = W.CONFIGS[args.config]
+    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
+    peak, peak_src = measured_peaks()
+    rows = []
+    stream = torch.cuda.Stream()
+    for T in (1, 2, 4, 8):
+        xs = [torch.from_numpy(np.ascontiguousarray(W.gen_x(s, T, step=i)).view(np.float16)).cuda()
+              for i in range(NINPUTS)]
+        lgs = [torch.from_numpy(W.gen_logits(s, T, step=i)).cuda() if s.logits != "router"
+               else torch.empty(T, s.E, device="cuda") for i in range(NINPUTS)]
+        ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+        r = spx.Routing.empty(T, s.E, s.k)
+        out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+        keep = [spx.layer_args(0, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, out, ws,
+                               w4=sets[i % NSETS]["w4"], shared=sets[i % NSETS]["shared"],
+                               w_router=sets[i % NSETS]["w_router"]) for i in range(NSETS * NINPUTS)]
+        nb = []
+        for i in range(NINPUTS):
+            spx.spx_moe_layer(keep[i][0])
+            torch.cuda.synchronize()
+            nb.append((int(r.n_active.item()), layer_bytes(s, "draft", T, int(r.n_active.item()))))
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                spx.spx_moe_layer(keep[i % len(keep)][0], stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                spx.spx_moe_layer(keep[i % len(keep)][0], stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        ua = float(np.mean([a for a, _ in nb]))
+        byt = float(np.mean([b for _, b in nb]))
+        rows.append({"T": T, "layer_us": round(us, 2), "unique_experts": round(ua, 2),
+                     "gbs": round(byt / (us * 1e-6) / 1e9, 1), "frac": round(byt / (us * 1e-6) / 1e9 / peak, 3),
+                     "tokens_per_s": round(T / (us * 1e-6), 1)})
+        assert spx.spx_workspace_status(ws) == 0
+    line = {"metric": "draft layer with T requests' tokens per call, device us per layer",
+            "config": {"workload": f"{s.name} draft, T = 1, 2, 4, 8 (one token per request)"},
+            "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
+    print(json.dumps(line), flush=True)
+
+
 def oracle_free_topk(lg, k):
     """Top-k expert ids of fp32 logits (value descending, index ascending), for
     choosing the resident set; no method arithmetic beyond the ordering."""
@@ -692,12 +744,15 @@ def main():
     ap.add_argument("--cycle", action="store_true", help="the 26-layer draft-then-verify cycle (prints its own line)")
     ap.add_argument("--loop-n", type=int, default=12)
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
+    ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
     if args.loop:
         run_loop(args)
     elif args.cached:
         run_cached(args)
+    elif args.draft_batch:
+        run_draft_batch(args)
     elif args.cycle:
         run_cycle(args)
     elif args.impl == "reference":

@@ -517,3 +517,24 @@ def test_cache_aware_ready_flag_never_set_times_out():
     torch.cuda.synchronize()
     assert spx.spx_workspace_status(ws) == 0
     gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), "after a timeout")
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_batched_draft_full_size(T):
+    """Several requests' draft tokens in one draft call (DeepSeek-V2-Lite
+    shape, T = 4 and 8 tokens): one launch, each expert the tokens share read
+    once; routing outputs bit-exact and the layer output within tolerance."""
+    gh = _gh()
+    s = W.CONFIGS["deepseek_v2_lite"]
+    x = W.gen_x(s, T, step=40 + T)
+    logits = W.gen_logits(s, T, step=40 + T)
+    need = gh.needed_experts(s, [logits], [x])
+    lay = gh.Layer(s, needed=need, verify=False)
+    ref = lay.oracle_layer("draft", x, logits=logits)
+    outs, routing, _ = _run_layer(lay, "draft", x, logits)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    g = ref["gather"]
+    assert np.array_equal(routing.offsets.cpu().numpy(), g["offsets"])
+    assert np.array_equal(routing.sorted_slots.cpu().numpy(), g["sorted_slots"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"batched draft T={T} rep {rep}")
