@@ -20,14 +20,16 @@
 // adjacent 16-column FP16 slices), so the gate/up reduction over H and the
 // SiLU stay inside one block, and the down projection's partial sums over
 // units are added into fp32 outputs with vector atomics (no grid-wide
-// barrier, no block waits on another block).  A unit is contiguous in HBM
+// barrier; only the last 16 blocks to finish wait for the rest, to share the
+// fp16 output pass).  A unit is contiguous in HBM
 // (repacked once at load time: mma fragment order, GPTQ group scales in front
 // of each group's codes) and is streamed by the producer with bulk copies
 // (TMA engine) into a ring of shared-memory stages guarded by mbarriers.
 // The unit's expert id and slice travel in the stage header and its token
 // table is bulk-copied next to the first chunk, so consumers never wait on a
 // global load.  Consumers keep partial sums in registers for the whole
-// gate/up phase and reduce across warps once per unit with plain stores.
+// gate/up phase of a slice and reduce across warps once per slice with
+// shared-memory atomics.
 #include "spx_internal.cuh"
 
 #include <math.h>
@@ -55,8 +57,8 @@ struct __align__(16) ChunkHeader {
 };
 
 constexpr int kMetaBytes = 1152;                  // >= kTableBytes, multiple of 128
-// A stage holds one chunk of weights (kChunk or 2 kChunk bytes, chosen per
-// launch) followed by the token table area.
+// A stage holds one chunk of weights (a multiple of 1 KB chosen per launch,
+// see choose_geometry) followed by the token table area.
 static_assert(kTableBytes <= (size_t)kMetaBytes, "table fits the stage meta area");
 // The meta area a launch needs: the table header and T entries, in 128-byte units.
 __host__ __device__ inline int meta_bytes_for(int T) { return (16 + 16 * T + 127) & ~127; }
