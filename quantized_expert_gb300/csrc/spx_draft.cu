@@ -25,6 +25,11 @@
 // whole blocks (or pairs of down items) with the next ticket already in
 // flight, and never waits on h.  Consumer warps take ring stages in order
 // through a shared-memory ticket, so a slow item never stalls the others.
+// Every block routes the launch's tokens itself (softmax, top-k, the token
+// tables of the active experts) in shared memory; block 0 also writes the
+// routing outputs.  The launch may begin while the previous one on the stream
+// finishes: a block's first queue unit is static, so the producer issues its
+// weight copies before it waits for that launch; everything else waits.
 #include "spx_internal.cuh"
 #include "spx_routing.cuh"
 
