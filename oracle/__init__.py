@@ -70,6 +70,9 @@ def lib():
             L.orc_elb_accumulate.argtypes = [_u32, C.c_int, C.c_int, _i32, C.c_int, C.c_int]
             L.orc_gather_by_expert.argtypes = [_i32, C.c_int, C.c_int, C.c_int, _i32, _i32, _i32, _i32, _i32]
             L.orc_w4_dequant.argtypes = [_i32, _u16, C.c_int, C.c_int, _dp]
+            L.orc_w4z_dequant.argtypes = [_i32, _u16, C.c_void_p, C.c_int, C.c_int, _dp]
+            L.orc_swiglu_w4z.argtypes = [_u16, C.c_int, C.c_int, _i32, _u16, C.c_void_p, _i32, _u16, C.c_void_p,
+                                         _i32, _u16, C.c_void_p, _dp, C.c_void_p]
             L.orc_swiglu_w4.argtypes = [_u16, C.c_int, C.c_int, _i32, _u16, _i32, _u16, _i32, _u16, _dp, C.c_void_p]
             L.orc_swiglu_f16.argtypes = [_u16, C.c_int, C.c_int, _u16, _u16, _u16, _dp, C.c_void_p]
             L.orc_shared_gate.argtypes = [_u16, _u16, C.c_int]
@@ -142,25 +145,32 @@ def gather_by_expert(ids, E: int) -> dict:
 
 
 # ----------------------------------------------------------- experts --
-def w4_dequant(q, s) -> np.ndarray:
+def w4_dequant(q, s, qz=None) -> np.ndarray:
+    """W = (code - zero) * scale; qz [K/128][N/8] int32 zero points, or None
+    for zero point 8."""
     q = _c(q, np.int32)
     s = _c(s, np.uint16)
     K, N = q.shape[0] * 8, q.shape[1]
     out = np.empty((K, N), np.float64)
-    lib().orc_w4_dequant(q, s, K, N, out)
+    z = _c(qz, np.int32) if qz is not None else None
+    lib().orc_w4z_dequant(q, s, z.ctypes.data if z is not None else None, K, N, out)
     return out
 
 
 def swiglu_w4(x_row, ex: dict, want_h: bool = False):
+    """INT4 expert MLP on one token; ex may carry qz_gate / qz_up / qz_down
+    (per-group zero points), else zero point 8."""
     x_row = _c(x_row, np.uint16)
     H = x_row.shape[0]
     I = ex["qw_gate"].shape[1]
     y = np.empty(H, np.float64)
     h = np.empty(I, np.float64) if want_h else None
-    lib().orc_swiglu_w4(x_row, H, I, _c(ex["qw_gate"], np.int32), _c(ex["s_gate"], np.uint16),
-                        _c(ex["qw_up"], np.int32), _c(ex["s_up"], np.uint16),
-                        _c(ex["qw_down"], np.int32), _c(ex["s_down"], np.uint16), y,
-                        h.ctypes.data if want_h else None)
+    zs = [_c(ex[k], np.int32) if ex.get(k) is not None else None for k in ("qz_gate", "qz_up", "qz_down")]
+    zp = [z.ctypes.data if z is not None else None for z in zs]
+    lib().orc_swiglu_w4z(x_row, H, I, _c(ex["qw_gate"], np.int32), _c(ex["s_gate"], np.uint16), zp[0],
+                         _c(ex["qw_up"], np.int32), _c(ex["s_up"], np.uint16), zp[1],
+                         _c(ex["qw_down"], np.int32), _c(ex["s_down"], np.uint16), zp[2], y,
+                         h.ctypes.data if want_h else None)
     return (y, h) if want_h else y
 
 

@@ -242,13 +242,35 @@ static inline double w4_at(const int32_t *q, const uint16_t *s, const double *ta
     return (double)(code - 8) * tab[s[(int64_t)(kk / 128) * N + n]];
 }
 
-/* out[kk][n] = W[kk][n] for the whole K x N matrix. */
-void orc_w4_dequant(const int32_t *q, const uint16_t *s, int K, int N, double *out)
+/* Asymmetric INT4 (per-group zero points, the AWQ form of the same codes;
+ * [S1 Main Findings: drafts quantised by GPTQ, AWQ and GGUF]).  Reading: qzeros is
+ * [K/128][N/8] int32, the zero point of column n in group g at bits
+ * 4*(n%8)..+3 of word (g, n/8), low nibble first;
+ * W[kk][n] = (code - zero) * scale[kk/128][n].  qz == NULL: zero point 8. */
+static inline double w4z_at(const int32_t *q, const uint16_t *s, const int32_t *qz, const double *tab, int N,
+                            int kk, int n)
+{
+    if (!qz)
+        return w4_at(q, s, tab, N, kk, n);
+    uint32_t word = (uint32_t)q[(int64_t)(kk / 8) * N + n];
+    int code = (int)((word >> (4 * (kk % 8))) & 15u);
+    uint32_t zword = (uint32_t)qz[(int64_t)(kk / 128) * (N / 8) + n / 8];
+    int zero = (int)((zword >> (4 * (n % 8))) & 15u);
+    return (double)(code - zero) * tab[s[(int64_t)(kk / 128) * N + n]];
+}
+
+/* out[kk][n] = W[kk][n] for the whole K x N matrix (qz nullable). */
+void orc_w4z_dequant(const int32_t *q, const uint16_t *s, const int32_t *qz, int K, int N, double *out)
 {
     const double *tab = half_tab();
     for (int kk = 0; kk < K; ++kk)
         for (int n = 0; n < N; ++n)
-            out[(int64_t)kk * N + n] = w4_at(q, s, tab, N, kk, n);
+            out[(int64_t)kk * N + n] = w4z_at(q, s, qz, tab, N, kk, n);
+}
+
+void orc_w4_dequant(const int32_t *q, const uint16_t *s, int K, int N, double *out)
+{
+    orc_w4z_dequant(q, s, NULL, K, N, out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -259,12 +281,13 @@ void orc_w4_dequant(const int32_t *q, const uint16_t *s, int K, int N, double *o
 
 static inline double silu(double z) { return z / (1.0 + exp(-z)); }
 
-/* INT4 expert (GPTQ layout, gate/up K=H N=I, down K=I N=H) on one token. */
-void orc_swiglu_w4(const uint16_t *x, int H, int I,
-                   const int32_t *qg, const uint16_t *sg,
-                   const int32_t *qu, const uint16_t *su,
-                   const int32_t *qd, const uint16_t *sd,
-                   double *y, double *h_out)
+/* INT4 expert (GPTQ layout, gate/up K=H N=I, down K=I N=H) on one token;
+ * zg, zu, zd: per-group zero points (nullable: zero point 8). */
+void orc_swiglu_w4z(const uint16_t *x, int H, int I,
+                    const int32_t *qg, const uint16_t *sg, const int32_t *zg,
+                    const int32_t *qu, const uint16_t *su, const int32_t *zu,
+                    const int32_t *qd, const uint16_t *sd, const int32_t *zd,
+                    double *y, double *h_out)
 {
     const double *tab = half_tab();
     double *g = (double *)calloc((size_t)I, sizeof(double));
@@ -274,8 +297,8 @@ void orc_swiglu_w4(const uint16_t *x, int H, int I,
     for (int kk = 0; kk < H; ++kk) {
         double xk = tab[x[kk]];
         for (int i = 0; i < I; ++i) {
-            g[i] += w4_at(qg, sg, tab, I, kk, i) * xk;
-            u[i] += w4_at(qu, su, tab, I, kk, i) * xk;
+            g[i] += w4z_at(qg, sg, zg, tab, I, kk, i) * xk;
+            u[i] += w4z_at(qu, su, zu, tab, I, kk, i) * xk;
         }
     }
     for (int i = 0; i < I; ++i)
@@ -284,12 +307,21 @@ void orc_swiglu_w4(const uint16_t *x, int H, int I,
         y[n] = 0.0;
     for (int i = 0; i < I; ++i)
         for (int n = 0; n < H; ++n)
-            y[n] += w4_at(qd, sd, tab, H, i, n) * h[i];
+            y[n] += w4z_at(qd, sd, zd, tab, H, i, n) * h[i];
     if (h_out)
         memcpy(h_out, h, sizeof(double) * (size_t)I);
     free(g);
     free(u);
     free(h);
+}
+
+void orc_swiglu_w4(const uint16_t *x, int H, int I,
+                   const int32_t *qg, const uint16_t *sg,
+                   const int32_t *qu, const uint16_t *su,
+                   const int32_t *qd, const uint16_t *sd,
+                   double *y, double *h_out)
+{
+    orc_swiglu_w4z(x, H, I, qg, sg, NULL, qu, su, NULL, qd, sd, NULL, y, h_out);
 }
 
 /* FP16 expert, PyTorch [out, in] layout: wg, wu [I][H]; wd [H][I]. */

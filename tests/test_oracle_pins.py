@@ -201,6 +201,55 @@ def test_dequant_every_nibble_position_and_code():
     assert set(np.unique(codes)) == set(range(16))
 
 
+def _pack_zeros(z):
+    """[G][N] zero points -> [G][N/8] int32, column n at bits 4*(n%8), low nibble first."""
+    G, N = z.shape
+    qz = np.zeros((G, N // 8), np.uint32)
+    for n in range(N):
+        qz[:, n // 8] |= z[:, n].astype(np.uint32) << np.uint32(4 * (n % 8))
+    return qz.view(np.int32)
+
+
+def test_dequant_zero_points_closed_form():
+    """Asymmetric INT4: W = (code - zero) * scale for every nibble position of
+    the code word, every zero nibble position and every code / zero value."""
+    K, N = 256, 16
+    codes = (np.arange(K)[:, None] * 5 + np.arange(N)[None, :] * 3) % 16
+    q = np.zeros((K // 8, N), np.uint32)
+    for kk in range(K):
+        q[kk // 8] |= (codes[kk].astype(np.uint32) << np.uint32(4 * (kk % 8)))
+    zeros = (np.arange(2)[:, None] * 9 + np.arange(N)[None, :] * 7) % 16   # [K/128][N]
+    sc = ((np.arange(2 * N, dtype=np.float64).reshape(2, N) + 3) / 32.0).astype(np.float16)
+    out = oracle.w4_dequant(q.view(np.int32), sc.view(np.uint16), _pack_zeros(zeros))
+    ref = (codes - np.repeat(zeros, 128, axis=0)) * np.repeat(sc.astype(np.float64), 128, axis=0)
+    assert np.array_equal(out, ref)
+    assert set(np.unique(zeros)) == set(range(16)) and set(np.unique(codes)) == set(range(16))
+    # all zero points 8 is the symmetric format
+    eight = _pack_zeros(np.full((2, N), 8))
+    assert np.array_equal(oracle.w4_dequant(q.view(np.int32), sc.view(np.uint16), eight),
+                          oracle.w4_dequant(q.view(np.int32), sc.view(np.uint16)))
+
+
+def test_identity_expert_with_zero_points():
+    """Identity expert built on per-column zero points: code z+1 on the
+    diagonal, code z elsewhere, so W = I whatever the zero point."""
+    n = 256
+    z = (np.arange(n) * 5 % 15)[None, :].repeat(n // 128, 0)        # zero point per column, 0..14
+    codes = np.repeat(z, 128, axis=0).copy()
+    codes[np.arange(n), np.arange(n)] += 1
+    q = np.zeros((n // 8, n), np.uint32)
+    for kk in range(n):
+        q[kk // 8] |= (codes[kk].astype(np.uint32) << np.uint32(4 * (kk % 8)))
+    s = np.ones((n // 128, n), np.float16).view(np.uint16)
+    qz = _pack_zeros(z)
+    ex = dict(qw_gate=q.view(np.int32), s_gate=s, qz_gate=qz, qw_up=q.view(np.int32), s_up=s, qz_up=qz,
+              qw_down=q.view(np.int32), s_down=s, qz_down=qz)
+    x = (np.random.default_rng(5).standard_normal(n) * 2).astype(np.float16)
+    xd = x.astype(np.float64)
+    y = oracle.swiglu_w4(x.view(np.uint16), ex)
+    assert np.allclose(y, xd * expit(xd) * xd, rtol=1e-14, atol=1e-300)
+
+
 # ---------------------------------------------------------------- MLP
 def _identity_w4(n):
     q = np.full((n // 8, n), 0x88888888, np.uint32)
