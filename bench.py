@@ -72,8 +72,10 @@ def f16_expert_bytes(s, I=None):
     return 3 * s.H * I * 2
 
 
-def layer_bytes(s, mode, T, n_unique):
+def layer_bytes(s, mode, T, n_unique, zeros=False):
     b = n_unique * (w4_expert_bytes(s) if mode == "draft" else f16_expert_bytes(s))
+    if zeros:  # fp16 zero points: one per group of 128 rows and column, of the three matrices
+        b += n_unique * 2 * (3 * s.H * s.I // 128)
     if s.I_s:
         b += f16_expert_bytes(s, s.I_s) + (s.H * 2 if s.shared_gate else 0)
     if s.logits == "router":
@@ -681,6 +683,18 @@ def run_draft_batch(args):
     spx.load()
     s = W.CONFIGS[args.config]
     sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
+    if args.zeros:  # asymmetric INT4: seeded per-group zero points on every set
+        E, H, I = s.E, s.H, s.I
+        for i, st in enumerate(sets):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(2_000_003 * (s.seed + 1) + i)
+
+            def words(*shape):
+                return torch.randint(-2 ** 31, 2 ** 31, shape, dtype=torch.int32, device="cuda", generator=g)
+
+            st["w4"] = spx.spx_w4_zeros_repack(st["w4"], words(E, H // 128, I // 8), words(E, H // 128, I // 8),
+                                               words(E, I // 128, H // 8))
+        torch.cuda.synchronize()
     peak, peak_src = measured_peaks()
     rows = []
     stream = torch.cuda.Stream()
@@ -699,7 +713,7 @@ def run_draft_batch(args):
         for i in range(NINPUTS):
             spx.spx_moe_layer(keep[i][0])
             torch.cuda.synchronize()
-            nb.append((int(r.n_active.item()), layer_bytes(s, "draft", T, int(r.n_active.item()))))
+            nb.append((int(r.n_active.item()), layer_bytes(s, "draft", T, int(r.n_active.item()), args.zeros)))
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 spx.spx_moe_layer(keep[i % len(keep)][0], stream)
@@ -717,8 +731,9 @@ def run_draft_batch(args):
                      "gbs": round(byt / (us * 1e-6) / 1e9, 1), "frac": round(byt / (us * 1e-6) / 1e9 / peak, 3),
                      "tokens_per_s": round(T / (us * 1e-6), 1)})
         assert spx.spx_workspace_status(ws) == 0
+    zp = ", per-group zero points" if args.zeros else ""
     line = {"metric": "draft layer with T requests' tokens per call, device us per layer",
-            "config": {"workload": f"{s.name} draft, T = 1, 2, 4, 8 (one token per request)"},
+            "config": {"workload": f"{s.name} draft{zp}, T = 1, 2, 4, 8 (one token per request)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
     print(json.dumps(line), flush=True)
 
@@ -745,6 +760,7 @@ def main():
     ap.add_argument("--loop-n", type=int, default=12)
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
+    ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
     if args.loop:

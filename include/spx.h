@@ -144,6 +144,12 @@ typedef struct {
     const void *packed; /* spx_w4_packed_bytes() bytes, from spx_w4_repack() */
     int E, H, I;        /* experts, hidden size, expert intermediate size */
     int slice_cols;     /* S: 16 or 32 */
+    /* Per-group zero points (asymmetric INT4, the AWQ form: W = (code - zero)
+     * * scale) [P1 Main Findings: drafts quantised by GPTQ, AWQ and GGUF]:
+     * spx_w4_zeros_bytes() bytes from spx_w4_zeros_repack(), or NULL for zero
+     * point 8.  Served by draft calls of T <= 8 (the one-launch draft path);
+     * other calls with zero points return SPX_ERR_UNSUPPORTED. */
+    const void *zeros;
 } spx_w4_experts;
 
 typedef struct {
@@ -173,6 +179,15 @@ SPX_API int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate,
                   const int32_t *qw_up, const uint16_t *s_up,
                   const int32_t *qw_down, const uint16_t *s_down,
                   int E, int H, int I, int slice_cols, void *packed, spx_stream_t stream);
+
+/* Zero points of asymmetric INT4 experts: canonical qzeros [E][K/128][N/8]
+ * int32 per matrix (gate/up: K = H, N = I; down: K = I, N = H), the zero
+ * point of column n in group g at bits 4*(n%8)..+3 of word (g, n/8), low
+ * nibble first.  Repacked (device, 16-byte aligned) into the order the draft
+ * launch streams them, next to the packed scales' order; deterministic. */
+SPX_API size_t spx_w4_zeros_bytes(int E, int H, int I, int slice_cols);
+SPX_API int spx_w4_zeros_repack(const int32_t *qz_gate, const int32_t *qz_up, const int32_t *qz_down,
+                                int E, int H, int I, int slice_cols, void *zeros, spx_stream_t stream);
 
 /* Repack one canonical FP16 shared expert ([I_s][H], [I_s][H], [H][I_s]) into
  * `packed` (device, spx_shared_packed_bytes() bytes, 16-byte aligned). */

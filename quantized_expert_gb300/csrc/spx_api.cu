@@ -83,7 +83,7 @@ extern "C" const char *spx_status_string(int st) {
     }
 }
 
-extern "C" int spx_version(void) { return 101; }
+extern "C" int spx_version(void) { return 102; }
 
 extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
@@ -146,10 +146,13 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes, 0,
                                  w->slice_cols);
     if (st) return st;
-    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_INVALID_ARG;
+    if (!al16(w->packed) || !al16(y_sorted) || !al16(w->zeros)) return SPX_ERR_INVALID_ARG;
+    const bool draft = draft_supported(T, w->H, w->I, w->slice_cols, 0, w->E, k);
+    if (w->zeros && !draft) return SPX_ERR_UNSUPPORTED;  // zero points: the draft launch only
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
     p.routed = static_cast<const uint8_t *>(w->packed);
+    p.w4_zeros = static_cast<const uint8_t *>(w->zeros);
     p.w4_sdown = reinterpret_cast<const __half *>(p.routed + w4_units_bytes(w->E, w->H, w->I, w->slice_cols));
     p.routed_fmt = 0;
     p.S = w->slice_cols;
@@ -165,8 +168,7 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
     st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
     if (st) return st;
-    if (draft_supported(T, w->H, w->I, w->slice_cols, 0, w->E, k))
-        return launch_draft(p, nullptr, ws_scratch_base(T, w->H), false, s);
+    if (draft) return launch_draft(p, nullptr, ws_scratch_base(T, w->H), false, s);
     return launch_engine(p, s, false);
 }
 
@@ -256,7 +258,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     int S = kF16S;
     if (a->mode == 0) {
         if (!a->w4 || !a->w4->packed || a->w4->E != E || a->w4->H != H) return SPX_ERR_INVALID_ARG;
-        if (!al16(a->w4->packed)) return SPX_ERR_INVALID_ARG;
+        if (!al16(a->w4->packed) || !al16(a->w4->zeros)) return SPX_ERR_INVALID_ARG;
         I = a->w4->I;
         S = a->w4->slice_cols;
         routed = static_cast<const uint8_t *>(a->w4->packed);
@@ -278,6 +280,8 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     const bool cache_aware = a->resident || a->ready;
     const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
 
+    const bool zeros = a->mode == 0 && a->w4->zeros;
+    if (zeros && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k))) return SPX_ERR_UNSUPPORTED;
     if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k)) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch
@@ -301,6 +305,7 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         rt.n_active = a->n_active;
         EngineParams p = base_params(a->x, T, H, a->ws);
         p.routed = routed;
+        p.w4_zeros = static_cast<const uint8_t *>(a->w4->zeros);
         p.S = S;
         p.E = E;
         p.I = I;

@@ -40,6 +40,9 @@ namespace spx {
 enum : int { DK_SG = 0, DK_RG = 1, DK_SD = 2, DK_RD = 3, DK_DONE = 4 };
 constexpr int kDkData = 16896;    // largest item: 4 INT4 groups of 32 columns (or 8 of 16)
 constexpr int kDkRdGroups = 7;    // INT4 down groups (of 128 rows of I) per RD item
+// zero points of an RD item (32 per group) after its largest weight run
+constexpr int kDkRdZeroOff = kDkRdGroups * kW4ColGroupBytes;
+static_assert(kDkRdZeroOff % 16 == 0 && kDkRdZeroOff + kDkRdGroups * 64 <= kDkData, "RD zero points fit the stage");
 constexpr int kDkSdSteps = 16;    // k-steps of I_s per SD item
 constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
 constexpr int kDkDBatch = 2;      // down items per queue unit
@@ -186,6 +189,7 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int 
 
 struct DkParams {
     const uint8_t *w4;      // packed INT4 experts
+    const __half *zeros_gu, *zeros_dn;  // nullable: per-group zero points (else 8), repacked
     size_t w4_colblk;       // byte offset of the column-block-major down weights
     int S;                  // INT4 slice width
     const uint8_t *sh;      // shared pack (nullable)
@@ -303,7 +307,8 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     // One ring fill: weights; a down item's h slice is left to the poller,
     // which counts it on the same barrier.
     auto issue = [&](DHeader &h, const uint8_t *src, uint32_t bytes, const void *hsrc, uint32_t hs_bytes,
-                     const int *rdy, int target) -> bool {
+                     const int *rdy, int target, const void *zsrc = nullptr, uint32_t zbytes = 0,
+                     uint32_t zoff = 0) -> bool {
         const int st = (int)(it % nst);
         if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
             ok = false;
@@ -313,8 +318,9 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         h.hpar = (int)((hpar_bits >> st) & 1u);
         hdrs[st] = h;
         uint8_t *dst = ring + (size_t)st * L.stage;
-        mbar_arrive_expect_tx(&full[st], bytes);
+        mbar_arrive_expect_tx(&full[st], bytes + zbytes);
         bulk_g2s(dst, src, bytes, &full[st], pol);
+        if (zbytes) bulk_g2s(dst + zoff, zsrc, zbytes, &full[st], pol);
         if (hs_bytes) {
             mbar_arrive_expect_tx(&hfull[st], hs_bytes);  // completed by the poller's copy
             hpar_bits ^= 1u << st;
@@ -386,7 +392,11 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                 h.k0 = r * g.rg_gpi;
                 h.n = min(g.rg_gpi, H / 128 - h.k0);
                 const uint8_t *src = p.w4 + unit * w4_unit_bytes(H, p.S) + (size_t)h.k0 * w4_group_bytes(p.S);
-                if (!issue(h, src, h.n * (uint32_t)w4_group_bytes(p.S), nullptr, 0, nullptr, 0)) return false;
+                // zero points (2S per group, as the scales) in the stage's h area, unused by these items
+                const __half *zs = p.zeros_gu ? p.zeros_gu + (unit * (H / 128) + h.k0) * 2 * p.S : nullptr;
+                if (!issue(h, src, h.n * (uint32_t)w4_group_bytes(p.S), nullptr, 0, nullptr, 0, zs,
+                           zs ? h.n * 4u * p.S : 0u, (uint32_t)L.hs_off))
+                    return false;
             }
             return true;
         }
@@ -420,9 +430,11 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                 h.n = min(kDkRdGroups, I / 128 - h.k0);
                 const uint8_t *src =
                     p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * kW4ColGroupBytes;
+                const __half *zs =
+                    p.zeros_dn ? p.zeros_dn + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * 32 : nullptr;
                 if (!issue(h, src, h.n * kW4ColGroupBytes, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4,
-                           h.n * 8 * T * 32,
-                           p.rdy_r + h.a * g.rd_nr + h.r, h.n * 8))
+                           h.n * 8 * T * 32, p.rdy_r + h.a * g.rd_nr + h.r, h.n * 8, zs, zs ? h.n * 64u : 0u,
+                           (uint32_t)kDkRdZeroOff))
                     return false;
             }
         }
@@ -710,7 +722,7 @@ __device__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *s
 }
 
 // INT4 draft kernel; MS = S/16 of the packed INT4 units.
-template <int MS>
+template <int MS, bool ZP>
 __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
@@ -1049,10 +1061,18 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 float acc[NTW][4];
 #pragma unroll
                 for (int t = 0; t < NTW; ++t) {
-                    acc[t][0] = -1032.f * s0;
-                    acc[t][1] = -1032.f * s1;
-                    acc[t][2] = -1152.f * s0;
-                    acc[t][3] = -1152.f * s1;
+                    // with zero points z: start at -(1024 + z) and -(1024 + 16 z) times the sum
+                    float za = 8.f, zb = 8.f;
+                    if constexpr (ZP) {
+                        const __half *zp = reinterpret_cast<const __half *>(stage + L.hs_off) + gr * 32 * MS;
+                        za = __half2float(zp[t * 16 + g]);
+                        zb = __half2float(zp[t * 16 + g + 8]);
+                    }
+                    const float ca = -(1024.f + za), cb = -(1024.f + 16.f * zb);
+                    acc[t][0] = ca * s0;
+                    acc[t][1] = ca * s1;
+                    acc[t][2] = cb * s0;
+                    acc[t][3] = cb * s1;
                 }
 #pragma unroll
                 for (int ib = 0; ib < BPG; ++ib) {
@@ -1155,6 +1175,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 const uint8_t *gp = stage + (size_t)gr * kW4ColGroupBytes;
                 const __half *scp = reinterpret_cast<const __half *>(gp);
                 float acc[2][4] = {};
+                float hsum = 0.f;  // zero points: this lane's part of the group's h sum for token g
 #pragma unroll
                 for (int ib = 0; ib < 4; ++ib) {
                     const uint4 v = lds128(gp + 64 + ib * 512 + lane * 16);
@@ -1164,12 +1185,33 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                         const int ksr = gr * 8 + ib * 2 + ki;  // k-step within the slice
                         uint2 bv = make_uint2(0u, 0u);
                         if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ksr * T + g) * 4 + q4);
+                        if constexpr (ZP) {
+                            const float2 f0 = __half22float2(u32_as_h2(bv.x)), f1 = __half22float2(u32_as_h2(bv.y));
+                            hsum += (f0.x + f0.y) + (f1.x + f1.y);
+                        }
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
                             uint32_t a[4];
                             dequant_frag(words[ki * 2 + q], a);
                             mma_16816(acc[q], a, bv.x, bv.y);
                         }
+                    }
+                }
+                if constexpr (ZP) {
+                    // (q - z) = (q - 8) + (8 - z): add (8 - z) times the group's h sum of each token
+                    hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
+                    hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
+                    const float hc0 = __shfl_sync(0xffffffffu, hsum, 8 * q4);
+                    const float hc1 = __shfl_sync(0xffffffffu, hsum, 8 * q4 + 4);
+                    const __half *zp = reinterpret_cast<const __half *>(stage + kDkRdZeroOff) + gr * 32;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const float da = 8.f - __half2float(zp[q * 16 + g]);
+                        const float db = 8.f - __half2float(zp[q * 16 + g + 8]);
+                        acc[q][0] = fmaf(da, hc0, acc[q][0]);
+                        acc[q][1] = fmaf(da, hc1, acc[q][1]);
+                        acc[q][2] = fmaf(db, hc0, acc[q][2]);
+                        acc[q][3] = fmaf(db, hc1, acc[q][3]);
                     }
                 }
 #pragma unroll
@@ -1267,6 +1309,10 @@ bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k) {
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
     DkParams p{};
     p.w4 = e.routed;
+    if (e.w4_zeros) {
+        p.zeros_gu = reinterpret_cast<const __half *>(e.w4_zeros);
+        p.zeros_dn = reinterpret_cast<const __half *>(e.w4_zeros + w4_zeros_gu_bytes(e.E, e.H, e.I, e.S));
+    }
     p.S = e.S;
     p.w4_colblk = w4_colblk_offset(e.E, e.H, e.I, e.S);
     p.sh = e.shared;
@@ -1314,17 +1360,18 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.nstages = nst;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    static int configured[2][64] = {};
+    static int configured[4][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
     const int ms = e.S / 16;
-    if (!configured[ms - 1][dev]) {
-        cudaError_t err = ms == 2 ? cudaFuncSetAttribute(draft_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         kSmemLimit)
-                                  : cudaFuncSetAttribute(draft_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         kSmemLimit);
+    const bool zp = p.zeros_gu != nullptr;
+    void (*kern)(const DkParams) = ms == 2 ? (zp ? draft_kernel<2, true> : draft_kernel<2, false>)
+                                           : (zp ? draft_kernel<1, true> : draft_kernel<1, false>);
+    const int ki = (ms - 1) * 2 + (zp ? 1 : 0);
+    if (!configured[ki][dev]) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (err != cudaSuccess) return record_launch(err);
-        configured[ms - 1][dev] = 1;
+        configured[ki][dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
@@ -1336,7 +1383,7 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t err = ms == 2 ? cudaLaunchKernelEx(&cfg, draft_kernel<2>, p) : cudaLaunchKernelEx(&cfg, draft_kernel<1>, p);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, p);
     return record_launch(err);
 }
 

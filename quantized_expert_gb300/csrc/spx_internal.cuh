@@ -59,6 +59,14 @@ constexpr int kW4ColGroupBytes = 64 + 4 * 512;
 __host__ __device__ inline size_t w4_colblk_bytes(int E, int H, int I) {
     return (size_t)E * (H / 32) * (I / 128) * kW4ColGroupBytes;
 }
+// Zero points of asymmetric INT4 experts (a buffer of their own): gate/up
+// [E][I/S][H/128][2S] fp16, then down [E][H/32][I/128][32] fp16.
+__host__ __device__ inline size_t w4_zeros_gu_bytes(int E, int H, int I, int S) {
+    return (size_t)E * (I / S) * (H / 128) * 2 * S * 2;
+}
+__host__ __device__ inline size_t w4_zeros_dn_bytes(int E, int H, int I) {
+    return (size_t)E * (H / 32) * (I / 128) * 32 * 2;
+}
 __host__ __device__ inline size_t w4_colblk_offset(int E, int H, int I, int S) {
     return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
 }
@@ -282,6 +290,7 @@ struct EngineParams {
     // routed experts (packed units)
     const uint8_t *routed;
     const __half *w4_sdown;  // INT4: down scales [E][I/128][H]
+    const uint8_t *w4_zeros; // INT4, nullable: repacked per-group zero points (else 8)
     int routed_fmt;          // 0 INT4, 1 FP16
     int S;                   // routed slice width (INT4: 16/32; FP16: 16)
     int E, I, k;

@@ -204,6 +204,40 @@ static int grid_for(size_t total) {
     return (int)g;
 }
 
+// Zero points, gate/up: [E][I/S units][H/128 groups][2S] fp16 in the order
+// of the packed scales (gate columns, then up columns).
+__global__ void w4_pack_zeros_gu(const int32_t *zg, const int32_t *zu, int E, int H, int I, int S, uint16_t *dst) {
+    const int spe = I / S, G = H / 128;
+    const size_t total = (size_t)E * spe * G * 2 * S;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int c2 = idx % (2 * S);
+        const int grp = (idx / (2 * S)) % G;
+        const size_t unit = idx / ((size_t)2 * S * G);
+        const int e = unit / spe, j = unit % spe;
+        const int i = j * S + (c2 % S);
+        const int32_t *src = c2 < S ? zg : zu;
+        const uint32_t w = static_cast<uint32_t>(src[((size_t)e * G + grp) * (I / 8) + i / 8]);
+        dst[idx] = __half_as_ushort(__float2half((float)((w >> (4 * (i % 8))) & 15u)));
+    }
+}
+
+// Zero points, down: [E][H/32 pairs][I/128 groups][32] fp16 in the order of
+// the column-block scales.
+__global__ void w4_pack_zeros_dn(const int32_t *zd, int E, int H, int I, uint16_t *dst) {
+    const int NQ = H / 32, G = I / 128;
+    const size_t total = (size_t)E * NQ * G * 32;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int qm = idx % 32;
+        const size_t gi = idx / 32;
+        const int grp = gi % G;
+        const int Q = (gi / G) % NQ;
+        const int e = gi / ((size_t)G * NQ);
+        const int n = down_col(2 * Q + (qm >> 4), qm & 15);
+        const uint32_t w = static_cast<uint32_t>(zd[((size_t)e * G + grp) * (H / 8) + n / 8]);
+        dst[idx] = __half_as_ushort(__float2half((float)((w >> (4 * (n % 8))) & 15u)));
+    }
+}
+
 }  // namespace spx
 
 using namespace spx;
@@ -246,6 +280,27 @@ extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, con
     w4_pack_colblk_scales<<<grid_for(tot), 256, 0, s>>>(s_down, E, H, I, cb);
     tot = (size_t)E * (H / 32) * (I / 128) * 512;
     w4_pack_colblk_codes<<<grid_for(tot), 256, 0, s>>>(qw_down, E, H, I, cb);
+    return record_launch(cudaGetLastError());
+}
+
+extern "C" size_t spx_w4_zeros_bytes(int E, int H, int I, int S) {
+    if (!spx_w4_packed_bytes(E, H, I, S)) return 0;
+    return w4_zeros_gu_bytes(E, H, I, S) + w4_zeros_dn_bytes(E, H, I);
+}
+
+extern "C" int spx_w4_zeros_repack(const int32_t *qz_gate, const int32_t *qz_up, const int32_t *qz_down, int E,
+                                   int H, int I, int S, void *zeros, spx_stream_t stream) {
+    if (!qz_gate || !qz_up || !qz_down || !zeros) return SPX_ERR_INVALID_ARG;
+    if (E < 1 || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
+    if ((S != 16 && S != 32) || H % 128 || I % 128 || H > kMaxH || E > kMaxE) return SPX_ERR_UNSUPPORTED;
+    if (!aligned16(zeros)) return SPX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *out = static_cast<uint16_t *>(zeros);
+    size_t tot = (size_t)E * (I / S) * (H / 128) * 2 * S;
+    w4_pack_zeros_gu<<<grid_for(tot), 256, 0, s>>>(qz_gate, qz_up, E, H, I, S, out);
+    tot = (size_t)E * (H / 32) * (I / 128) * 32;
+    w4_pack_zeros_dn<<<grid_for(tot), 256, 0, s>>>(qz_down, E, H, I,
+                                                   out + w4_zeros_gu_bytes(E, H, I, S) / sizeof(uint16_t));
     return record_launch(cudaGetLastError());
 }
 

@@ -28,7 +28,8 @@ class SpxError(RuntimeError):
 
 
 class W4Experts(C.Structure):
-    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int), ("slice_cols", C.c_int)]
+    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int), ("slice_cols", C.c_int),
+                ("zeros", C.c_void_p)]
 
 
 class F16Experts(C.Structure):
@@ -65,6 +66,8 @@ _SIGS = {
     "spx_w4_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
     "spx_f16_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "spx_w4_repack": (C.c_int, [C.c_void_p] * 6 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "spx_w4_zeros_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "spx_w4_zeros_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_f16_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_workspace_size": (C.c_size_t, [C.c_int] * 6),
     "spx_shared_packed_bytes": (C.c_size_t, [C.c_int, C.c_int]),
@@ -199,9 +202,10 @@ class PackedW4:
     H: int
     I: int
     S: int
+    zeros: torch.Tensor | None = None  # repacked per-group zero points (None: zero point 8)
 
     def cstruct(self) -> W4Experts:
-        return W4Experts(self.buf.data_ptr(), self.E, self.H, self.I, self.S)
+        return W4Experts(self.buf.data_ptr(), self.E, self.H, self.I, self.S, _p(self.zeros))
 
 
 @dataclass
@@ -237,6 +241,18 @@ def spx_w4_repack(qw_gate, s_gate, qw_up, s_up, qw_down, s_down, slice_cols=32, 
     _chk(load().spx_w4_repack(_p(qw_gate), _p(s_gate), _p(qw_up), _p(s_up), _p(qw_down), _p(s_down), E, H, I,
                               slice_cols, _p(buf), _stream(stream)), "spx_w4_repack")
     return PackedW4(buf, E, H, I, slice_cols)
+
+
+def spx_w4_zeros_repack(w4: PackedW4, qz_gate, qz_up, qz_down, stream=None) -> PackedW4:
+    """Canonical qzeros ([E][K/128][N/8] int32 per matrix, low nibble first) -> the
+    same experts with zero points attached (a new PackedW4 sharing w4's weights)."""
+    n = load().spx_w4_zeros_bytes(w4.E, w4.H, w4.I, w4.S)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_w4_zeros_bytes")
+    buf = torch.empty(n, dtype=torch.uint8, device=w4.buf.device)
+    _chk(load().spx_w4_zeros_repack(_p(qz_gate), _p(qz_up), _p(qz_down), w4.E, w4.H, w4.I, w4.S, _p(buf),
+                                    _stream(stream)), "spx_w4_zeros_repack")
+    return PackedW4(w4.buf, w4.E, w4.H, w4.I, w4.S, buf)
 
 
 def spx_f16_repack(w_gate, w_up, w_down, stream=None) -> PackedF16:

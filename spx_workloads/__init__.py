@@ -44,7 +44,7 @@ __all__ = [
 ]
 
 # stream tags (part of the seeding key, never of the arithmetic)
-TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM = range(1, 9)
+TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM, TAG_ZEROS = range(1, 10)
 HOT_LOG_A = 1.1510  # ln a, a = 3.1614
 ZIPF_S = 1.1
 
@@ -188,6 +188,20 @@ def gen_w4_expert(shape: LayerShape, layer: int, e: int) -> dict:
     qu, su = _w4_matrix(rng, H, I)
     qd, sd = _w4_matrix(rng, I, H)
     return dict(qw_gate=qg, s_gate=sg, qw_up=qu, s_up=su, qw_down=qd, s_down=sd)
+
+
+def gen_w4_zeros(shape: LayerShape, layer: int, e: int) -> dict:
+    """Per-group zero points of INT4 expert e (the asymmetric, AWQ-style form),
+    packed like GPTQ qzeros: ``qz_gate``/``qz_up`` [H/128, I/8] int32,
+    ``qz_down`` [I/128, H/8], zero point of column n at bits 4*(n%8) of word
+    n/8, uniform over 0..15."""
+    H, I = shape.H, shape.I
+    rng = rng_for(shape, TAG_ZEROS, layer, e)
+
+    def words(K, N):
+        return rng.integers(0, 2 ** 32, size=(K // 128, N // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+
+    return dict(qz_gate=words(H, I), qz_up=words(H, I), qz_down=words(I, H))
 
 
 def gen_f16_expert(shape: LayerShape, layer: int, e: int) -> dict:

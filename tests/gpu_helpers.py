@@ -49,12 +49,18 @@ class Layer:
     weights (for the library).  Only experts in `needed` are generated; the
     others are zero on the device (the kernels never read them)."""
 
-    def __init__(self, shape: W.LayerShape, layer: int = 0, needed=None, draft=True, verify=True, slice_cols=32):
+    def __init__(self, shape: W.LayerShape, layer: int = 0, needed=None, draft=True, verify=True, slice_cols=32,
+                 zeros=False):
         self.shape = s = shape
         self.layer = layer
         needed = sorted(set(range(s.E) if needed is None else needed))
         self.needed = needed
         self.w4_host = {e: W.gen_w4_expert(s, layer, e) for e in needed} if (draft or s.verify_is_dequant) else {}
+        self.zeros = zeros
+        if zeros:  # asymmetric INT4: per-group zero points on every draft expert
+            assert draft and not (verify and s.verify_is_dequant)
+            for e in needed:
+                self.w4_host[e] = dict(self.w4_host[e], **W.gen_w4_zeros(s, layer, e))
         self.f16_host = {}
         if verify:
             for e in needed:
@@ -87,6 +93,13 @@ class Layer:
                                                         ex["qw_down"], ex["s_down"])
         p = spx.spx_w4_repack(dev(qg), dev(sg.view(np.int16)), dev(qu), dev(su.view(np.int16)), dev(qd),
                               dev(sd.view(np.int16)), slice_cols=S)
+        if self.zeros:
+            zg = np.zeros((E, H // 128, I // 8), np.int32)
+            zu = np.zeros_like(zg)
+            zd = np.zeros((E, I // 128, H // 8), np.int32)
+            for e, ex in self.w4_host.items():
+                zg[e], zu[e], zd[e] = ex["qz_gate"], ex["qz_up"], ex["qz_down"]
+            p = spx.spx_w4_zeros_repack(p, dev(zg), dev(zu), dev(zd))
         torch.cuda.synchronize()
         return p
 

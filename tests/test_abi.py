@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_sizes_and_strings(lib):
     from quantized_expert_gb300 import spx
-    assert spx.spx_version() == 101
+    assert spx.spx_version() == 102
     assert spx.status_string(0) == "ok"
     assert "timed out" in spx.status_string(-5)
     # INT4 unit = 49*H*S/32 bytes; down scales copied once per expert
@@ -85,22 +85,25 @@ def test_header_is_plain_c():
                                "-o", os.path.join(d, "t.o")])
 
 
-def test_layer_args_layout_matches_the_header(tmp_path):
-    """The binding's spx_layer_args mirrors the C struct: a program compiled
-    against include/spx.h reports its size and field offsets."""
+@pytest.mark.parametrize("cname,pyname", [("spx_layer_args", "LayerArgs"), ("spx_w4_experts", "W4Experts"),
+                                           ("spx_f16_experts", "F16Experts"), ("spx_shared", "Shared")])
+def test_struct_layouts_match_the_header(tmp_path, cname, pyname):
+    """The binding's argument structs mirror the C structs: a program compiled
+    against include/spx.h reports each one's size and field offsets."""
     import ctypes as C
     import os
     import subprocess
     from quantized_expert_gb300 import spx
+    cls = getattr(spx, pyname)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     src = tmp_path / "layout.c"
-    fields = [f for f, _ in spx.LayerArgs._fields_]
-    body = "\n".join(f'    printf("%zu\\n", offsetof(spx_layer_args, {f}));' for f in fields)
+    fields = [f for f, _ in cls._fields_]
+    body = "\n".join(f'    printf("%zu\\n", offsetof({cname}, {f}));' for f in fields)
     src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "spx.h"\nint main(void) {\n'
-                   '    printf("%zu\\n", sizeof(spx_layer_args));\n' + body + "\n    return 0;\n}\n")
+                   f'    printf("%zu\\n", sizeof({cname}));\n' + body + "\n    return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)], check=True)
     got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
-    assert got[0] == C.sizeof(spx.LayerArgs)
+    assert got[0] == C.sizeof(cls)
     for f, off in zip(fields, got[1:]):
-        assert getattr(spx.LayerArgs, f).offset == off, f
+        assert getattr(cls, f).offset == off, f

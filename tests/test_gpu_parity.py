@@ -538,3 +538,101 @@ def test_batched_draft_full_size(T):
     assert np.array_equal(routing.sorted_slots.cpu().numpy(), g["sorted_slots"])
     for rep, o in enumerate(outs):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"batched draft T={T} rep {rep}")
+
+
+# ------------------------------------------- asymmetric INT4 (zero points)
+@pytest.mark.parametrize("T,S", [(1, 32), (1, 16), (4, 32), (8, 16)])
+def test_draft_layer_zero_points_full_size(T, S):
+    """Per-group zero points (the AWQ form, W = (code - zero) * scale, zeros
+    uniform over 0..15) on every draft expert, DeepSeek-V2-Lite shape, through
+    spx_moe_layer: routing bit-exact, output within tolerance of the oracle."""
+    gh = _gh()
+    s = W.CONFIGS["deepseek_v2_lite"]
+    x = W.gen_x(s, T, step=60 + T)
+    logits = W.gen_logits(s, T, step=60 + T)
+    need = gh.needed_experts(s, [logits], [x])
+    lay = gh.Layer(s, needed=need, verify=False, slice_cols=S, zeros=True)
+    ref = lay.oracle_layer("draft", x, logits=logits)
+    outs, routing, _ = _run_layer(lay, "draft", x, logits)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"zero points T={T} S={S} rep {rep}")
+
+
+@pytest.mark.parametrize("case", [0, 1, 2, 4])
+def test_draft_unit_call_zero_points(case):
+    """spx_moe_draft_w4a16 with zero points on the small cases of at most 8
+    tokens (several tiles, ragged groups, both slice widths)."""
+    spx, gh = _spx(), _gh()
+    s, T, S = SMALL_CASES[case]
+    x = W.gen_x(s, T, step=70 + case)
+    lg = np.random.default_rng(70 + case).standard_normal((T, s.E))
+    ids, w = oracle.route_topk(lg, s.k, s.renorm)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), verify=False, slice_cols=S, zeros=True)
+    g, r = _routing_dev(ids, s.E)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    y_ref = np.stack([oracle.swiglu_w4(x[int(sl) // s.k], lay.w4_host[int(ids.reshape(-1)[sl])])
+                      for sl in g["sorted_slots"]])
+    y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
+    for rep in range(2):
+        spx.spx_moe_draft_w4a16(gh.dev_f16(x), lay.w4, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                                r["n_active"], y, ws)
+        torch.cuda.synchronize()
+        gh.check_close(y.cpu().numpy(), y_ref, f"zero points case {case} rep {rep}")
+    assert spx.spx_workspace_status(ws) == 0
+
+
+def test_zero_points_of_eight_match_the_symmetric_path():
+    """Zero points all 8 reduce the asymmetric form to the symmetric one: the
+    start values are the symmetric ones and the down correction adds exactly
+    zero, so every item's partial sums are bit-identical to the zero-point-free
+    launch's; the outputs then differ at most by the order of the fp32 atomic
+    additions across items."""
+    spx, gh = _spx(), _gh()
+    s, T, S = SMALL_CASES[2]
+    x = W.gen_x(s, T, step=80)
+    ids, _ = oracle.route_topk(np.random.default_rng(80).standard_normal((T, s.E)), s.k, s.renorm)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), verify=False, slice_cols=S)
+    eights = np.int32(np.uint32(0x88888888).view(np.int32))
+    E, H, I = s.E, s.H, s.I
+    w4z = spx.spx_w4_zeros_repack(lay.w4, gh.dev(np.full((E, H // 128, I // 8), eights, np.int32)),
+                                  gh.dev(np.full((E, H // 128, I // 8), eights, np.int32)),
+                                  gh.dev(np.full((E, I // 128, H // 8), eights, np.int32)))
+    g, r = _routing_dev(ids, s.E)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    ys = []
+    for w4 in (lay.w4, w4z):
+        y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
+        spx.spx_moe_draft_w4a16(gh.dev_f16(x), w4, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                                r["n_active"], y, ws)
+        torch.cuda.synchronize()
+        ys.append(y.cpu().numpy())
+    assert np.allclose(ys[0], ys[1], rtol=0, atol=1e-6 * np.abs(ys[0]).max())
+
+
+def test_zero_points_unsupported_outside_the_draft_launch():
+    """Zero points are served by the draft launch (T <= 8) only: a larger
+    batch, and the cache-aware path, return SPX_ERR_UNSUPPORTED."""
+    spx, gh = _spx(), _gh()
+    from quantized_expert_gb300.spx import SpxError
+    s = _small("deepseek_v2_lite", I=256, E=16)
+    T = 9
+    lay = gh.Layer(s, needed=list(range(s.E)), verify=False, slice_cols=16, zeros=True)
+    ids, _ = oracle.route_topk(np.random.default_rng(90).standard_normal((T, s.E)), s.k, s.renorm)
+    g, r = _routing_dev(ids, s.E)
+    y = torch.empty(T * s.k, s.H, device="cuda")
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_draft_w4a16(gh.dev_f16(W.gen_x(s, T)), lay.w4, s.k, r["offsets"], r["sorted_slots"],
+                                r["active"], r["n_active"], y, spx.new_workspace(T, s.H, s.I, s.E, s.k))
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
+    T = 1
+    routing = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    lg = gh.dev(np.random.default_rng(91).standard_normal((T, s.E)).astype(np.float32))
+    resident = torch.ones(s.E, dtype=torch.uint8, device="cuda")
+    args, keep = spx.layer_args(0, gh.dev_f16(W.gen_x(s, T)), s.E, s.k, s.renorm, lg, routing, out, ws, w4=lay.w4,
+                                shared=lay.shared, resident=resident)
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_layer(args, None)
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
