@@ -41,6 +41,7 @@ _fp = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _u16 = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 _i32 = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
 _u32 = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+_u8 = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
 
 
 def build(force: bool = False) -> str:
@@ -75,6 +76,8 @@ def lib():
                                          _i32, _u16, C.c_void_p, _dp, C.c_void_p]
             L.orc_swiglu_w4.argtypes = [_u16, C.c_int, C.c_int, _i32, _u16, _i32, _u16, _i32, _u16, _dp, C.c_void_p]
             L.orc_swiglu_f16.argtypes = [_u16, C.c_int, C.c_int, _u16, _u16, _u16, _dp, C.c_void_p]
+            L.orc_q8_dequant.argtypes = [_u8, C.c_int, C.c_int, _dp]
+            L.orc_swiglu_q8.argtypes = [_u16, C.c_int, C.c_int, _u8, _u8, _u8, _dp, C.c_void_p]
             L.orc_shared_gate.argtypes = [_u16, _u16, C.c_int]
             L.orc_shared_gate.restype = C.c_double
             L.orc_combine.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, C.c_void_p, C.c_void_p, _dp, _u16]
@@ -174,6 +177,33 @@ def swiglu_w4(x_row, ex: dict, want_h: bool = False):
     return (y, h) if want_h else y
 
 
+def q8_dequant(w) -> np.ndarray:
+    """GGUF Q8_0 matrix, uint8 [N][K/32][34] blocks ([out][in] order) -> W [N][K]."""
+    w = _c(w, np.uint8)
+    N, K = w.shape[0], w.shape[1] * 32
+    out = np.empty((N, K), np.float64)
+    lib().orc_q8_dequant(w, N, K, out)
+    return out
+
+
+def swiglu_q8(x_row, ex: dict, want_h: bool = False):
+    """Q8_0 expert MLP on one token: ex holds q8_gate, q8_up [I][H/32][34] and
+    q8_down [H][I/32][34] uint8 blocks."""
+    x_row = _c(x_row, np.uint16)
+    H = x_row.shape[0]
+    I = ex["q8_gate"].shape[0]
+    y = np.empty(H, np.float64)
+    h = np.empty(I, np.float64) if want_h else None
+    lib().orc_swiglu_q8(x_row, H, I, _c(ex["q8_gate"], np.uint8), _c(ex["q8_up"], np.uint8),
+                        _c(ex["q8_down"], np.uint8), y, h.ctypes.data if want_h else None)
+    return (y, h) if want_h else y
+
+
+def swiglu_draft(x_row, ex: dict, want_h: bool = False):
+    """The draft expert MLP in the expert's own format (Q8_0 or INT4)."""
+    return swiglu_q8(x_row, ex, want_h) if "q8_gate" in ex else swiglu_w4(x_row, ex, want_h)
+
+
 def swiglu_f16(x_row, ex: dict, want_h: bool = False):
     x_row = _c(x_row, np.uint16)
     H = x_row.shape[0]
@@ -222,7 +252,8 @@ def moe_layer(mode: str, x, k: int, renorm: bool, expert, E: int, logits=None, w
     """One MoE layer for T tokens.
 
     mode: "draft" (INT4 routed experts, ``expert(e)`` returns the GPTQ dict)
-    or "verify" (FP16 routed experts, ``expert(e)`` returns the [out,in] dict).
+    or "verify" (FP16 routed experts, ``expert(e)`` returns the [out,in] dict);
+    a draft expert dict with ``q8_gate`` is a GGUF Q8_0 expert.
     ``logits`` (fp32 [T,E]) are used as given when ``w_router`` is None,
     otherwise computed from x . w_router^T.  ``shared``: dict of FP16 shared
     expert weights (+ optional ``w_sgate``) or None.  ``elb``: uint32 [L,E]
@@ -238,7 +269,7 @@ def moe_layer(mode: str, x, k: int, renorm: bool, expert, E: int, logits=None, w
     if elb is not None:
         elb_accumulate(elb, layer, ids)
     g = gather_by_expert(ids, E)
-    mlp = swiglu_w4 if mode == "draft" else swiglu_f16
+    mlp = swiglu_draft if mode == "draft" else swiglu_f16
     y_slot = np.zeros((T * k, H), np.float64)
     # experts in ascending id order; each expert's tokens in slot order
     for a in range(g["n_active"]):

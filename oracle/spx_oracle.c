@@ -324,6 +324,58 @@ void orc_swiglu_w4(const uint16_t *x, int H, int I,
     orc_swiglu_w4z(x, H, I, qg, sg, NULL, qu, su, NULL, qd, sd, NULL, y, h_out);
 }
 
+/* ------------------------------------------------------------------ */
+/* GGUF Q8_0 experts [S1 Main Findings: GGUF drafts at Q2, Q4 and Q8].  */
+/* Reading (the GGUF format definition; the pages name the format       */
+/* only): a weight matrix in [out][in] order, each row of `in` values   */
+/* cut into blocks of 32 consecutive values; a block is 34 bytes, the   */
+/* binary16 scale d (little-endian) then 32 signed 8-bit codes, and     */
+/* value j of the block is d * code[j].                                 */
+/* ------------------------------------------------------------------ */
+
+static inline double q8_at(const uint8_t *w, const double *tab, int K, int n, int kk)
+{
+    const uint8_t *blk = w + ((int64_t)n * (K / 32) + kk / 32) * 34;
+    uint16_t d = (uint16_t)(blk[0] | (blk[1] << 8));
+    int code = (int)(int8_t)blk[2 + kk % 32];
+    return (double)code * tab[d];
+}
+
+/* out[n][kk] = W[n][kk] for an N x K matrix ([out][in]). */
+void orc_q8_dequant(const uint8_t *w, int N, int K, double *out)
+{
+    const double *tab = half_tab();
+    for (int n = 0; n < N; ++n)
+        for (int kk = 0; kk < K; ++kk)
+            out[(int64_t)n * K + kk] = q8_at(w, tab, K, n, kk);
+}
+
+/* Q8_0 expert on one token: wg, wu [I][H/32] blocks; wd [H][I/32] blocks. */
+void orc_swiglu_q8(const uint16_t *x, int H, int I, const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
+                   double *y, double *h_out)
+{
+    const double *tab = half_tab();
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int kk = 0; kk < H; ++kk) {
+            double xk = tab[x[kk]];
+            g += q8_at(wg, tab, H, i, kk) * xk;
+            u += q8_at(wu, tab, H, i, kk) * xk;
+        }
+        h[i] = silu(g) * u;
+    }
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i)
+            acc += q8_at(wd, tab, I, n, i) * h[i];
+        y[n] = acc;
+    }
+    if (h_out)
+        memcpy(h_out, h, sizeof(double) * (size_t)I);
+    free(h);
+}
+
 /* FP16 expert, PyTorch [out, in] layout: wg, wu [I][H]; wd [H][I]. */
 void orc_swiglu_f16(const uint16_t *x, int H, int I,
                     const uint16_t *wg, const uint16_t *wu, const uint16_t *wd,

@@ -44,7 +44,7 @@ __all__ = [
 ]
 
 # stream tags (part of the seeding key, never of the arithmetic)
-TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM, TAG_ZEROS = range(1, 10)
+TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM, TAG_ZEROS, TAG_Q8 = range(1, 11)
 HOT_LOG_A = 1.1510  # ln a, a = 3.1614
 ZIPF_S = 1.1
 
@@ -202,6 +202,27 @@ def gen_w4_zeros(shape: LayerShape, layer: int, e: int) -> dict:
         return rng.integers(0, 2 ** 32, size=(K // 128, N // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
 
     return dict(qz_gate=words(H, I), qz_up=words(H, I), qz_down=words(I, H))
+
+
+def _q8_matrix(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
+    """GGUF Q8_0 blocks of an [N][K] matrix: uint8 [N][K/32][34], each block a
+    little-endian fp16 scale U(0.0003, 0.00125) then 32 int8 codes uniform
+    over -128..127 (weights of the INT4 experts' magnitude)."""
+    d = rng.uniform(0.0003, 0.00125, size=(N, K // 32)).astype(np.float16).view(np.uint16)
+    codes = rng.integers(0, 256, size=(N, K // 32, 32), dtype=np.uint8)
+    out = np.empty((N, K // 32, 34), np.uint8)
+    out[:, :, 0] = d & 0xFF
+    out[:, :, 1] = d >> 8
+    out[:, :, 2:] = codes
+    return out
+
+
+def gen_q8_expert(shape: LayerShape, layer: int, e: int) -> dict:
+    """GGUF Q8_0 draft expert e in [out][in] order: ``q8_gate``/``q8_up``
+    [I][H/32][34] uint8, ``q8_down`` [H][I/32][34]."""
+    H, I = shape.H, shape.I
+    rng = rng_for(shape, TAG_Q8, layer, e)
+    return dict(q8_gate=_q8_matrix(rng, I, H), q8_up=_q8_matrix(rng, I, H), q8_down=_q8_matrix(rng, H, I))
 
 
 def gen_f16_expert(shape: LayerShape, layer: int, e: int) -> dict:

@@ -250,6 +250,85 @@ def test_identity_expert_with_zero_points():
     assert np.allclose(y, xd * expit(xd) * xd, rtol=1e-14, atol=1e-300)
 
 
+# ------------------------------------------------------- GGUF Q8_0 draft
+def _q8_blocks(codes, d):
+    """[N][K] int codes and [N][K/32] fp16 scales -> [N][K/32][34] uint8 Q8_0 blocks."""
+    N, K = codes.shape
+    out = np.zeros((N, K // 32, 34), np.uint8)
+    dv = np.asarray(d, np.float16).view(np.uint16)
+    out[:, :, 0] = dv & 0xFF
+    out[:, :, 1] = dv >> 8
+    out[:, :, 2:] = codes.astype(np.int8).view(np.uint8).reshape(N, K // 32, 32)
+    return out
+
+
+def test_q8_dequant_hand_derived_golden():
+    gold = json.load(open(os.path.join(GOLD, "gguf_q8_0.json")))
+    cases = gold["cases"]
+    w = np.zeros((1, len(cases), 34), np.uint8)
+    for b, case in enumerate(cases):
+        w[0, b, :2] = case["d_bytes"]
+        w[0, b, 2:2 + len(case["code_bytes"])] = case["code_bytes"]
+        assert float(np.array(case["d_bytes"], np.uint8).view(np.float16)[0]) == case["d"]
+    out = oracle.q8_dequant(w)
+    for b, case in enumerate(cases):
+        assert list(out[0, 32 * b:32 * b + 8]) == case["values"]
+        assert not np.any(out[0, 32 * b + 8:32 * b + 32])
+
+
+def test_q8_dequant_every_code_and_position():
+    """W[n][k] = d[n][k/32] * code[n][k] for every int8 code at every position."""
+    N, K = 8, 256
+    codes = ((np.arange(N)[:, None] * 37 + np.arange(K)[None, :] * 11) % 256) - 128
+    d = ((np.arange(N * K // 32).reshape(N, K // 32) % 13) - 6.5) / 16.0
+    out = oracle.q8_dequant(_q8_blocks(codes, d))
+    ref = codes * np.repeat(np.asarray(d, np.float16).astype(np.float64), 32, axis=1)
+    assert np.array_equal(out, ref)
+    assert set(np.unique(codes)) == set(range(-128, 128))
+
+
+def test_q8_expert_equals_the_same_weights_in_int4():
+    """A GPTQ INT4 expert re-expressed exactly in Q8_0 (code q - 8, the group
+    scale on each of the group's four blocks) gives the same MLP output, term
+    for term: the Q8_0 indexing is pinned to the INT4 one."""
+    shape = W.scaled(W.CONFIGS["tiny"], H=256, I=384)
+    ex = W.gen_w4_expert(shape, 0, 1)
+    q8 = {}
+    for name, K in (("gate", shape.H), ("up", shape.H), ("down", shape.I)):
+        Wk = oracle.w4_dequant(ex["qw_" + name], ex["s_" + name])          # [K][N]
+        s = ex["s_" + name].view(np.float16).astype(np.float64)            # [K/128][N]
+        d = np.repeat(s, 4, axis=0).T                                      # [N][K/32]
+        codes = np.rint(Wk.T / np.repeat(d, 32, axis=1)).astype(np.int64)  # q - 8, exact
+        assert np.array_equal(codes * np.repeat(d, 32, axis=1), Wk.T)
+        q8["q8_" + name] = _q8_blocks(codes, d.astype(np.float16))
+    for step in range(3):
+        x = W.gen_x(shape, 1, step=step)[0]
+        y4, h4 = oracle.swiglu_w4(x, ex, want_h=True)
+        y8, h8 = oracle.swiglu_q8(x, q8, want_h=True)
+        assert np.array_equal(h4, h8) and np.array_equal(y4, y8)
+
+
+def test_q8_identity_expert_closed_form():
+    n = 256
+    codes = np.eye(n, dtype=np.int64)
+    eye = _q8_blocks(codes, np.ones((n, n // 32)))
+    ex = dict(q8_gate=eye, q8_up=eye, q8_down=eye)
+    x = (np.random.default_rng(6).standard_normal(n) * 2).astype(np.float16)
+    xd = x.astype(np.float64)
+    assert np.allclose(oracle.swiglu_q8(x.view(np.uint16), ex), xd * expit(xd) * xd, rtol=1e-14, atol=1e-300)
+
+
+def test_q8_mlp_matches_dequantised_matmul():
+    shape = W.scaled(W.CONFIGS["tiny"], H=256, I=384)
+    ex = W.gen_q8_expert(shape, 0, 0)
+    x = W.gen_x(shape, 1)[0]
+    Wg, Wu, Wd = (oracle.q8_dequant(ex[k]) for k in ("q8_gate", "q8_up", "q8_down"))  # [out][in]
+    xd = x.view(np.float16).astype(np.float64)
+    g, u = Wg @ xd, Wu @ xd
+    ref = Wd @ (g * expit(g) * u)
+    assert np.allclose(oracle.swiglu_q8(x, ex), ref, rtol=1e-10, atol=1e-10)
+
+
 # ---------------------------------------------------------------- MLP
 def _identity_w4(n):
     q = np.full((n // 8, n), 0x88888888, np.uint32)
