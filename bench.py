@@ -72,8 +72,11 @@ def f16_expert_bytes(s, I=None):
     return 3 * s.H * I * 2
 
 
-def layer_bytes(s, mode, T, n_unique, zeros=False):
-    b = n_unique * (w4_expert_bytes(s) if mode == "draft" else f16_expert_bytes(s))
+def layer_bytes(s, mode, T, n_unique, zeros=False, q8=False):
+    if q8:  # GGUF Q8_0: 34 bytes per 32 weights
+        b = n_unique * 3 * s.H * s.I * 34 // 32
+    else:
+        b = n_unique * (w4_expert_bytes(s) if mode == "draft" else f16_expert_bytes(s))
     if zeros:  # fp16 zero points: one per group of 128 rows and column, of the three matrices
         b += n_unique * 2 * (3 * s.H * s.I // 128)
     if s.I_s:
@@ -695,6 +698,21 @@ def run_draft_batch(args):
             st["w4"] = spx.spx_w4_zeros_repack(st["w4"], words(E, H // 128, I // 8), words(E, H // 128, I // 8),
                                                words(E, I // 128, H // 8))
         torch.cuda.synchronize()
+    if args.q8:  # GGUF Q8_0 experts instead of INT4: random codes, scales U(0.0003, 0.00125)
+        E, H, I = s.E, s.H, s.I
+        for i, st in enumerate(sets):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(3_000_017 * (s.seed + 1) + i)
+
+            def blocks(N, K):
+                b = torch.randint(0, 256, (E, N, K // 32, 34), dtype=torch.uint8, device="cuda", generator=g)
+                d = (torch.rand((E, N, K // 32), device="cuda", generator=g) * 0.00095 + 0.0003).half()
+                b[..., :2] = d.view(torch.uint8).view(E, N, K // 32, 2)
+                return b
+
+            st["w4"] = None
+            st["q8"] = spx.spx_q8_repack(blocks(I, H), blocks(I, H), blocks(H, I))
+            torch.cuda.synchronize()
     peak, peak_src = measured_peaks()
     rows = []
     stream = torch.cuda.Stream()
@@ -708,12 +726,14 @@ def run_draft_batch(args):
         out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
         keep = [spx.layer_args(0, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, out, ws,
                                w4=sets[i % NSETS]["w4"], shared=sets[i % NSETS]["shared"],
-                               w_router=sets[i % NSETS]["w_router"]) for i in range(NSETS * NINPUTS)]
+                               w_router=sets[i % NSETS]["w_router"], q8=sets[i % NSETS].get("q8"))
+                for i in range(NSETS * NINPUTS)]
         nb = []
         for i in range(NINPUTS):
             spx.spx_moe_layer(keep[i][0])
             torch.cuda.synchronize()
-            nb.append((int(r.n_active.item()), layer_bytes(s, "draft", T, int(r.n_active.item()), args.zeros)))
+            nb.append((int(r.n_active.item()),
+                       layer_bytes(s, "draft", T, int(r.n_active.item()), args.zeros, args.q8)))
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 spx.spx_moe_layer(keep[i % len(keep)][0], stream)
@@ -731,7 +751,7 @@ def run_draft_batch(args):
                      "gbs": round(byt / (us * 1e-6) / 1e9, 1), "frac": round(byt / (us * 1e-6) / 1e9 / peak, 3),
                      "tokens_per_s": round(T / (us * 1e-6), 1)})
         assert spx.spx_workspace_status(ws) == 0
-    zp = ", per-group zero points" if args.zeros else ""
+    zp = ", per-group zero points" if args.zeros else ", GGUF Q8_0 experts" if args.q8 else ""
     line = {"metric": "draft layer with T requests' tokens per call, device us per layer",
             "config": {"workload": f"{s.name} draft{zp}, T = 1, 2, 4, 8 (one token per request)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
@@ -761,6 +781,7 @@ def main():
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
     ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
+    ap.add_argument("--q8", action="store_true", help="with --draft-batch: GGUF Q8_0 experts instead of INT4")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
     if args.loop:

@@ -83,7 +83,7 @@ extern "C" const char *spx_status_string(int st) {
     }
 }
 
-extern "C" int spx_version(void) { return 102; }
+extern "C" int spx_version(void) { return 103; }
 
 extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
@@ -172,6 +172,35 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     return launch_engine(p, s, false);
 }
 
+extern "C" int spx_moe_draft_q8a16(const uint16_t *x, int T, const spx_q8_experts *w, int k, const int32_t *offsets,
+                                   const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
+                                   float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
+    if (!w || !w->packed || !y_sorted) return SPX_ERR_INVALID_ARG;
+    int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes, 0,
+                                 16);
+    if (st) return st;
+    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_INVALID_ARG;
+    if (!draft_supported(T, w->H, w->I, 16, 0, w->E, k)) return SPX_ERR_UNSUPPORTED;  // the draft launch only
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    EngineParams p = base_params(x, T, w->H, ws);
+    p.routed = static_cast<const uint8_t *>(w->packed);
+    p.routed_fmt = kFmtQ8;
+    p.S = 16;
+    p.E = w->E;
+    p.I = w->I;
+    p.k = k;
+    p.routed_enabled = 1;
+    p.active = active;
+    p.n_active = n_active;
+    p.tables = ws_tables(ws, T, w->H);
+    p.mode = 0;  // sorted rows
+    p.yout = y_sorted;
+    if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
+    st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
+    if (st) return st;
+    return launch_draft(p, nullptr, ws_scratch_base(T, w->H), false, s);
+}
+
 extern "C" int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_experts *w, int k, const int32_t *offsets,
                                    const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
                                    float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
@@ -256,7 +285,14 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     int I = 0;
     const uint8_t *routed = nullptr;
     int S = kF16S;
-    if (a->mode == 0) {
+    const bool q8 = a->mode == 0 && a->q8;
+    if (q8) {
+        if (a->w4 || !a->q8->packed || a->q8->E != E || a->q8->H != H) return SPX_ERR_INVALID_ARG;
+        if (!al16(a->q8->packed)) return SPX_ERR_INVALID_ARG;
+        I = a->q8->I;
+        S = 16;
+        routed = static_cast<const uint8_t *>(a->q8->packed);
+    } else if (a->mode == 0) {
         if (!a->w4 || !a->w4->packed || a->w4->E != E || a->w4->H != H) return SPX_ERR_INVALID_ARG;
         if (!al16(a->w4->packed) || !al16(a->w4->zeros)) return SPX_ERR_INVALID_ARG;
         I = a->w4->I;
@@ -280,8 +316,8 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     const bool cache_aware = a->resident || a->ready;
     const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
 
-    const bool zeros = a->mode == 0 && a->w4->zeros;
-    if (zeros && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k))) return SPX_ERR_UNSUPPORTED;
+    const bool zeros = a->mode == 0 && !q8 && a->w4->zeros;
+    if ((zeros || q8) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k))) return SPX_ERR_UNSUPPORTED;
     if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k)) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch
@@ -305,7 +341,8 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         rt.n_active = a->n_active;
         EngineParams p = base_params(a->x, T, H, a->ws);
         p.routed = routed;
-        p.w4_zeros = static_cast<const uint8_t *>(a->w4->zeros);
+        p.routed_fmt = q8 ? kFmtQ8 : 0;
+        p.w4_zeros = q8 ? nullptr : static_cast<const uint8_t *>(a->w4->zeros);
         p.S = S;
         p.E = E;
         p.I = I;

@@ -43,6 +43,11 @@ constexpr int kDkRdGroups = 7;    // INT4 down groups (of 128 rows of I) per RD 
 // zero points of an RD item (32 per group) after its largest weight run
 constexpr int kDkRdZeroOff = kDkRdGroups * kW4ColGroupBytes;
 static_assert(kDkRdZeroOff % 16 == 0 && kDkRdZeroOff + kDkRdGroups * 64 <= kDkData, "RD zero points fit the stage");
+// GGUF Q8_0 experts: groups of 128 rows of 4352 bytes, three per routed item
+constexpr int kDkQ8Groups = 3;
+static_assert(kDkQ8Groups * kQ8GroupBytes <= kDkData, "Q8_0 items fit the stage");
+// draft expert formats (template argument of the launch)
+enum : int { DK_FMT_W4 = 0, DK_FMT_W4Z = 1, DK_FMT_Q8 = 2 };
 constexpr int kDkSdSteps = 16;    // k-steps of I_s per SD item
 constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
 constexpr int kDkDBatch = 2;      // down items per queue unit
@@ -84,19 +89,21 @@ struct DkGeom {
     int sg_cols, sg_nks, sg_nr;  // shared gate/up: blocks of 16 columns, k-steps per item, items per block
     int sd_nr;                   // shared down ranges of kDkSdSteps k-steps
     int rg_blocks, rg_gpi, rg_nr;
-    int rd_nr;
+    int rd_gpi, rd_nr;  // routed down: groups per item, ranges
 };
 
-__host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s) {
+// q8: GGUF Q8_0 experts (S = 16), whose groups are four times the INT4 size.
+__host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s, bool q8 = false) {
     DkGeom g;
     g.sg_cols = I_s / 16;
     g.sg_nks = ((H / 16) % 16 == 0) ? 16 : 8;
     g.sg_nr = (H / 16) / g.sg_nks;
     g.sd_nr = (I_s / 16 + kDkSdSteps - 1) / kDkSdSteps;
     g.rg_blocks = I / S;
-    g.rg_gpi = S == 32 ? 4 : 8;
+    g.rg_gpi = q8 ? kDkQ8Groups : (S == 32 ? 4 : 8);
     g.rg_nr = (H / 128 + g.rg_gpi - 1) / g.rg_gpi;
-    g.rd_nr = (I / 128 + kDkRdGroups - 1) / kDkRdGroups;
+    g.rd_gpi = q8 ? kDkQ8Groups : kDkRdGroups;
+    g.rd_nr = (I / 128 + g.rd_gpi - 1) / g.rd_gpi;
     return g;
 }
 
@@ -107,7 +114,8 @@ struct DkScratch {
 };
 __host__ __device__ inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I, int I_s, int nact_max) {
-    const DkGeom g = dk_geom(H, I, 16, I_s);
+    const DkGeom g = dk_geom(H, I, 16, I_s, true);  // the format with the most down ranges
+    static_assert(kDkQ8Groups <= kDkRdGroups, "ready counts sized for the smallest down items");
     DkScratch s;
     size_t o = al256(base);
     s.qctr = o;  // one 256-byte line per queue shard
@@ -188,7 +196,8 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int 
 }
 
 struct DkParams {
-    const uint8_t *w4;      // packed INT4 experts
+    const uint8_t *w4;      // packed INT4 (or Q8_0) experts
+    int q8;                 // the experts are GGUF Q8_0 (S = 16)
     const __half *zeros_gu, *zeros_dn;  // nullable: per-group zero points (else 8), repacked
     size_t w4_colblk;       // byte offset of the column-block-major down weights
     int S;                  // INT4 slice width
@@ -278,7 +287,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     uint8_t *ring = smem + L.ring;
     const uint64_t pol = policy_evict_first();
     const int H = p.H, I = p.I, T = p.T;
-    const DkGeom g = dk_geom(H, I, p.S, p.I_s);
+    const DkGeom g = dk_geom(H, I, p.S, p.I_s, p.q8 != 0);
     const int NQ = H / 32;
     const int nSGb = p.sh ? g.sg_cols : 0;
     const int nSD = p.sh ? NQ * g.sd_nr : 0;
@@ -391,10 +400,12 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                 h.r = r;
                 h.k0 = r * g.rg_gpi;
                 h.n = min(g.rg_gpi, H / 128 - h.k0);
-                const uint8_t *src = p.w4 + unit * w4_unit_bytes(H, p.S) + (size_t)h.k0 * w4_group_bytes(p.S);
+                const size_t gb = p.q8 ? (size_t)kQ8GroupBytes : w4_group_bytes(p.S);
+                const size_t ub = p.q8 ? q8_unit_bytes(H) : w4_unit_bytes(H, p.S);
+                const uint8_t *src = p.w4 + unit * ub + (size_t)h.k0 * gb;
                 // zero points (2S per group, as the scales) in the stage's h area, unused by these items
                 const __half *zs = p.zeros_gu ? p.zeros_gu + (unit * (H / 128) + h.k0) * 2 * p.S : nullptr;
-                if (!issue(h, src, h.n * (uint32_t)w4_group_bytes(p.S), nullptr, 0, nullptr, 0, zs,
+                if (!issue(h, src, h.n * (uint32_t)gb, nullptr, 0, nullptr, 0, zs,
                            zs ? h.n * 4u * p.S : 0u, (uint32_t)L.hs_off))
                     return false;
             }
@@ -426,13 +437,13 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                 h.blk = rem - h.r * NQ;
                 h.e = act[h.a];
                 if (h.e < 0 || h.e >= p.E) continue;  // unusable routing entry
-                h.k0 = h.r * kDkRdGroups;
-                h.n = min(kDkRdGroups, I / 128 - h.k0);
-                const uint8_t *src =
-                    p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * kW4ColGroupBytes;
+                h.k0 = h.r * g.rd_gpi;
+                h.n = min(g.rd_gpi, I / 128 - h.k0);
+                const uint32_t gb = p.q8 ? (uint32_t)kQ8GroupBytes : (uint32_t)kW4ColGroupBytes;
+                const uint8_t *src = p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * gb;
                 const __half *zs =
                     p.zeros_dn ? p.zeros_dn + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * 32 : nullptr;
-                if (!issue(h, src, h.n * kW4ColGroupBytes, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4,
+                if (!issue(h, src, h.n * gb, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4,
                            h.n * 8 * T * 32, p.rdy_r + h.a * g.rd_nr + h.r, h.n * 8, zs, zs ? h.n * 64u : 0u,
                            (uint32_t)kDkRdZeroOff))
                     return false;
@@ -722,8 +733,11 @@ __device__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *s
 }
 
 // INT4 draft kernel; MS = S/16 of the packed INT4 units.
-template <int MS, bool ZP>
+template <int MS, int FMT>
 __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
+    constexpr bool ZP = FMT == DK_FMT_W4Z;  // INT4 with per-group zero points
+    constexpr bool Q8 = FMT == DK_FMT_Q8;   // GGUF Q8_0 (S = 16)
+    static_assert(!Q8 || MS == 1, "Q8_0 experts use 16-column slices");
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
@@ -783,7 +797,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int H = p.H, I = p.I, T = p.T, xstr = L.xs_stride;
     const int ctid = threadIdx.x;
-    const DkGeom geo = dk_geom(H, I, p.S, p.I_s);
+    const DkGeom geo = dk_geom(H, I, p.S, p.I_s, Q8);
     griddep_wait();  // x, the logits and the workspace may come from the preceding launch
     // one token over at most 64 experts: every consumer warp ranks a share
     const bool sel_all = p.logits && T == 1 && p.E <= 8 * kDkCons && p.E <= 64 && p.k <= 32;
@@ -1036,69 +1050,105 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             continue;
         }
         if (h.kind == DK_RG) {
-            // routed INT4 gate/up: slice of S = 16*MS columns, groups [k0, k0+n) of H
+            // routed INT4 (or Q8_0) gate/up: slice of S = 16*MS columns, groups [k0, k0+n) of H
             const int n_e = min(max(stn[h.a], 0), T);
             const bool okx = g < n_e;
             int tok = okx ? ste[h.a * T + g].tok : 0;
             tok = (tok >= 0 && tok < T) ? tok : 0;
             const __half *xr = xs + tok * xstr + 2 * q4;
-            // Raw codes into the mma: rows m < 8 of a tile get 1024 + q, rows m >= 8
-            // get 1024 + 16 q (the magic-exponent fragments without their fix-up).
-            // Starting each group's accumulator at -1032 (resp. -1152) times the
-            // group's x sum leaves sum (q - 8) x (resp. 16 times it): the zero
-            // point and the x16 fold into the start value and the row scale.
-            const int ng = H / 128;
-            int tc0 = 2 * q4 < n_e ? ste[h.a * T + 2 * q4].tok : 0;
-            int tc1 = 2 * q4 + 1 < n_e ? ste[h.a * T + 2 * q4 + 1].tok : 0;
-            tc0 = (tc0 >= 0 && tc0 < T) ? tc0 : 0;
-            tc1 = (tc1 >= 0 && tc1 < T) ? tc1 : 0;
-            const float *sx0 = sxs + tc0 * ng, *sx1 = sxs + tc1 * ng;
             float run[NTW][4] = {};
-            for (int gr = 0; gr < h.n; ++gr) {
-                const uint8_t *gp = stage + (size_t)gr * gbytes;
-                const __half *scp = reinterpret_cast<const __half *>(gp);
-                const float s0 = sx0[h.k0 + gr], s1 = sx1[h.k0 + gr];
-                float acc[NTW][4];
+            if constexpr (Q8) {
+                // GGUF Q8_0: per group of 128 rows, four blocks of 32 rows (two
+                // k-steps) with their own scales; the codes become exact fp16
+                // values, one block's products are summed, then scaled
+                for (int gr = 0; gr < h.n; ++gr) {
+                    const uint8_t *gp = stage + (size_t)gr * kQ8GroupBytes;
+                    const __half *scp = reinterpret_cast<const __half *>(gp);
 #pragma unroll
-                for (int t = 0; t < NTW; ++t) {
-                    // with zero points z: start at -(1024 + z) and -(1024 + 16 z) times the sum
-                    float za = 8.f, zb = 8.f;
-                    if constexpr (ZP) {
-                        const __half *zp = reinterpret_cast<const __half *>(stage + L.hs_off) + gr * 32 * MS;
-                        za = __half2float(zp[t * 16 + g]);
-                        zb = __half2float(zp[t * 16 + g + 8]);
-                    }
-                    const float ca = -(1024.f + za), cb = -(1024.f + 16.f * zb);
-                    acc[t][0] = ca * s0;
-                    acc[t][1] = ca * s1;
-                    acc[t][2] = cb * s0;
-                    acc[t][3] = cb * s1;
-                }
+                    for (int sb = 0; sb < 4; ++sb) {
+                        float acc[NTW][4] = {};
 #pragma unroll
-                for (int ib = 0; ib < BPG; ++ib) {
-                    const uint4 v = lds128(gp + 64 * MS + ib * 512 + lane * 16);
-                    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int ki = 0; ki < KB; ++ki) {
-                        const int ks = (h.k0 + gr) * 8 + ib * KB + ki;
-                        const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
-                        const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int kl = 2 * sb + kk;
+                            const int ks = (h.k0 + gr) * 8 + kl;
+                            const uint4 v = lds128(gp + kQ8ScaleBytes + kl * 512 + lane * 16);
+                            const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
+                            const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
+                            uint32_t a[4];
+                            q8_frag(v.x, v.y, a);
+                            mma_16816(acc[0], a, b0, b1);
+                            q8_frag(v.z, v.w, a);
+                            mma_16816(acc[1], a, b0, b1);
+                        }
 #pragma unroll
                         for (int t = 0; t < NTW; ++t) {
-                            uint32_t a[4];
-                            codes_frag(words[ki * NTW + t], a);
-                            mma_16816(acc[t], a, b0, b1);
+                            const float sa = __half2float(scp[sb * 32 + t * 16 + g]);
+                            const float sc = __half2float(scp[sb * 32 + t * 16 + g + 8]);
+                            run[t][0] = fmaf(sa, acc[t][0], run[t][0]);
+                            run[t][1] = fmaf(sa, acc[t][1], run[t][1]);
+                            run[t][2] = fmaf(sc, acc[t][2], run[t][2]);
+                            run[t][3] = fmaf(sc, acc[t][3], run[t][3]);
                         }
                     }
                 }
+            } else {
+                // Raw codes into the mma: rows m < 8 of a tile get 1024 + q, rows m >= 8
+                // get 1024 + 16 q (the magic-exponent fragments without their fix-up).
+                // Starting each group's accumulator at -1032 (resp. -1152) times the
+                // group's x sum leaves sum (q - 8) x (resp. 16 times it): the zero
+                // point and the x16 fold into the start value and the row scale.
+                const int ng = H / 128;
+                int tc0 = 2 * q4 < n_e ? ste[h.a * T + 2 * q4].tok : 0;
+                int tc1 = 2 * q4 + 1 < n_e ? ste[h.a * T + 2 * q4 + 1].tok : 0;
+                tc0 = (tc0 >= 0 && tc0 < T) ? tc0 : 0;
+                tc1 = (tc1 >= 0 && tc1 < T) ? tc1 : 0;
+                const float *sx0 = sxs + tc0 * ng, *sx1 = sxs + tc1 * ng;
+                for (int gr = 0; gr < h.n; ++gr) {
+                    const uint8_t *gp = stage + (size_t)gr * gbytes;
+                    const __half *scp = reinterpret_cast<const __half *>(gp);
+                    const float s0 = sx0[h.k0 + gr], s1 = sx1[h.k0 + gr];
+                    float acc[NTW][4];
 #pragma unroll
-                for (int t = 0; t < NTW; ++t) {
-                    const float sa = __half2float(scp[t * 16 + g]);
-                    const float sb = __half2float(scp[t * 16 + g + 8]) * 0.0625f;
-                    run[t][0] = fmaf(sa, acc[t][0], run[t][0]);
-                    run[t][1] = fmaf(sa, acc[t][1], run[t][1]);
-                    run[t][2] = fmaf(sb, acc[t][2], run[t][2]);
-                    run[t][3] = fmaf(sb, acc[t][3], run[t][3]);
+                    for (int t = 0; t < NTW; ++t) {
+                        // with zero points z: start at -(1024 + z) and -(1024 + 16 z) times the sum
+                        float za = 8.f, zb = 8.f;
+                        if constexpr (ZP) {
+                            const __half *zp = reinterpret_cast<const __half *>(stage + L.hs_off) + gr * 32 * MS;
+                            za = __half2float(zp[t * 16 + g]);
+                            zb = __half2float(zp[t * 16 + g + 8]);
+                        }
+                        const float ca = -(1024.f + za), cb = -(1024.f + 16.f * zb);
+                        acc[t][0] = ca * s0;
+                        acc[t][1] = ca * s1;
+                        acc[t][2] = cb * s0;
+                        acc[t][3] = cb * s1;
+                    }
+#pragma unroll
+                    for (int ib = 0; ib < BPG; ++ib) {
+                        const uint4 v = lds128(gp + 64 * MS + ib * 512 + lane * 16);
+                        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int ki = 0; ki < KB; ++ki) {
+                            const int ks = (h.k0 + gr) * 8 + ib * KB + ki;
+                            const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
+                            const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
+#pragma unroll
+                            for (int t = 0; t < NTW; ++t) {
+                                uint32_t a[4];
+                                codes_frag(words[ki * NTW + t], a);
+                                mma_16816(acc[t], a, b0, b1);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const float sa = __half2float(scp[t * 16 + g]);
+                        const float sb = __half2float(scp[t * 16 + g + 8]) * 0.0625f;
+                        run[t][0] = fmaf(sa, acc[t][0], run[t][0]);
+                        run[t][1] = fmaf(sa, acc[t][1], run[t][1]);
+                        run[t][2] = fmaf(sb, acc[t][2], run[t][2]);
+                        run[t][3] = fmaf(sb, acc[t][3], run[t][3]);
+                    }
                 }
             }
             __syncwarp();
@@ -1117,7 +1167,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 }
             }
             gu_done(h, MS, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.blk * MS) * T * 4, (size_t)T * 4,
-                    p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / kDkRdGroups, MS);
+                    p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / geo.rd_gpi, MS);
             continue;
         }
         if (h.kind == DK_SD) {
@@ -1166,61 +1216,95 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             }
             continue;
         }
-        // DK_RD: routed INT4 down: output pair blk, groups [k0, k0+n) of I
+        // DK_RD: routed INT4 (or Q8_0) down: output pair blk, groups [k0, k0+n) of I
         {
             const int n_e = min(max(stn[h.a], 0), T);
             const bool okb = g < n_e;
             float run[2][4] = {};
-            for (int gr = 0; gr < h.n; ++gr) {
-                const uint8_t *gp = stage + (size_t)gr * kW4ColGroupBytes;
-                const __half *scp = reinterpret_cast<const __half *>(gp);
-                float acc[2][4] = {};
-                float hsum = 0.f;  // zero points: this lane's part of the group's h sum for token g
+            if constexpr (Q8) {
+                // GGUF Q8_0, as the gate/up items: four 32-row blocks per group
+                for (int gr = 0; gr < h.n; ++gr) {
+                    const uint8_t *gp = stage + (size_t)gr * kQ8GroupBytes;
+                    const __half *scp = reinterpret_cast<const __half *>(gp);
 #pragma unroll
-                for (int ib = 0; ib < 4; ++ib) {
-                    const uint4 v = lds128(gp + 64 + ib * 512 + lane * 16);
-                    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+                    for (int sb = 0; sb < 4; ++sb) {
+                        float acc[2][4] = {};
 #pragma unroll
-                    for (int ki = 0; ki < 2; ++ki) {
-                        const int ksr = gr * 8 + ib * 2 + ki;  // k-step within the slice
-                        uint2 bv = make_uint2(0u, 0u);
-                        if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ksr * T + g) * 4 + q4);
-                        if constexpr (ZP) {
-                            const float2 f0 = __half22float2(u32_as_h2(bv.x)), f1 = __half22float2(u32_as_h2(bv.y));
-                            hsum += (f0.x + f0.y) + (f1.x + f1.y);
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int kl = 2 * sb + kk;
+                            const int ksr = gr * 8 + kl;  // k-step within the slice
+                            const uint4 v = lds128(gp + kQ8ScaleBytes + kl * 512 + lane * 16);
+                            uint2 bv = make_uint2(0u, 0u);
+                            if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ksr * T + g) * 4 + q4);
+                            uint32_t a[4];
+                            q8_frag(v.x, v.y, a);
+                            mma_16816(acc[0], a, bv.x, bv.y);
+                            q8_frag(v.z, v.w, a);
+                            mma_16816(acc[1], a, bv.x, bv.y);
                         }
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
-                            uint32_t a[4];
-                            dequant_frag(words[ki * 2 + q], a);
-                            mma_16816(acc[q], a, bv.x, bv.y);
+                            const float sa = __half2float(scp[sb * 32 + q * 16 + g]);
+                            const float sc = __half2float(scp[sb * 32 + q * 16 + g + 8]);
+                            run[q][0] = fmaf(sa, acc[q][0], run[q][0]);
+                            run[q][1] = fmaf(sa, acc[q][1], run[q][1]);
+                            run[q][2] = fmaf(sc, acc[q][2], run[q][2]);
+                            run[q][3] = fmaf(sc, acc[q][3], run[q][3]);
                         }
                     }
                 }
-                if constexpr (ZP) {
-                    // (q - z) = (q - 8) + (8 - z): add (8 - z) times the group's h sum of each token
-                    hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
-                    hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
-                    const float hc0 = __shfl_sync(0xffffffffu, hsum, 8 * q4);
-                    const float hc1 = __shfl_sync(0xffffffffu, hsum, 8 * q4 + 4);
-                    const __half *zp = reinterpret_cast<const __half *>(stage + kDkRdZeroOff) + gr * 32;
+            } else {
+                for (int gr = 0; gr < h.n; ++gr) {
+                    const uint8_t *gp = stage + (size_t)gr * kW4ColGroupBytes;
+                    const __half *scp = reinterpret_cast<const __half *>(gp);
+                    float acc[2][4] = {};
+                    float hsum = 0.f;  // zero points: this lane's part of the group's h sum for token g
+#pragma unroll
+                    for (int ib = 0; ib < 4; ++ib) {
+                        const uint4 v = lds128(gp + 64 + ib * 512 + lane * 16);
+                        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int ki = 0; ki < 2; ++ki) {
+                            const int ksr = gr * 8 + ib * 2 + ki;  // k-step within the slice
+                            uint2 bv = make_uint2(0u, 0u);
+                            if (okb) bv = *reinterpret_cast<const uint2 *>(hsl + ((size_t)ksr * T + g) * 4 + q4);
+                            if constexpr (ZP) {
+                                const float2 f0 = __half22float2(u32_as_h2(bv.x)), f1 = __half22float2(u32_as_h2(bv.y));
+                                hsum += (f0.x + f0.y) + (f1.x + f1.y);
+                            }
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                uint32_t a[4];
+                                dequant_frag(words[ki * 2 + q], a);
+                                mma_16816(acc[q], a, bv.x, bv.y);
+                            }
+                        }
+                    }
+                    if constexpr (ZP) {
+                        // (q - z) = (q - 8) + (8 - z): add (8 - z) times the group's h sum of each token
+                        hsum += __shfl_xor_sync(0xffffffffu, hsum, 1);
+                        hsum += __shfl_xor_sync(0xffffffffu, hsum, 2);
+                        const float hc0 = __shfl_sync(0xffffffffu, hsum, 8 * q4);
+                        const float hc1 = __shfl_sync(0xffffffffu, hsum, 8 * q4 + 4);
+                        const __half *zp = reinterpret_cast<const __half *>(stage + kDkRdZeroOff) + gr * 32;
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const float da = 8.f - __half2float(zp[q * 16 + g]);
+                            const float db = 8.f - __half2float(zp[q * 16 + g + 8]);
+                            acc[q][0] = fmaf(da, hc0, acc[q][0]);
+                            acc[q][1] = fmaf(da, hc1, acc[q][1]);
+                            acc[q][2] = fmaf(db, hc0, acc[q][2]);
+                            acc[q][3] = fmaf(db, hc1, acc[q][3]);
+                        }
+                    }
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
-                        const float da = 8.f - __half2float(zp[q * 16 + g]);
-                        const float db = 8.f - __half2float(zp[q * 16 + g + 8]);
-                        acc[q][0] = fmaf(da, hc0, acc[q][0]);
-                        acc[q][1] = fmaf(da, hc1, acc[q][1]);
-                        acc[q][2] = fmaf(db, hc0, acc[q][2]);
-                        acc[q][3] = fmaf(db, hc1, acc[q][3]);
+                        const float sa = __half2float(scp[q * 16 + g]), sb = __half2float(scp[q * 16 + g + 8]);
+                        run[q][0] = fmaf(sa, acc[q][0], run[q][0]);
+                        run[q][1] = fmaf(sa, acc[q][1], run[q][1]);
+                        run[q][2] = fmaf(sb, acc[q][2], run[q][2]);
+                        run[q][3] = fmaf(sb, acc[q][3], run[q][3]);
                     }
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float sa = __half2float(scp[q * 16 + g]), sb = __half2float(scp[q * 16 + g + 8]);
-                    run[q][0] = fmaf(sa, acc[q][0], run[q][0]);
-                    run[q][1] = fmaf(sa, acc[q][1], run[q][1]);
-                    run[q][2] = fmaf(sb, acc[q][2], run[q][2]);
-                    run[q][3] = fmaf(sb, acc[q][3], run[q][3]);
                 }
             }
             int row[2] = {-1, -1};
@@ -1309,12 +1393,13 @@ bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k) {
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
     DkParams p{};
     p.w4 = e.routed;
+    p.q8 = e.routed_fmt == kFmtQ8 ? 1 : 0;
     if (e.w4_zeros) {
         p.zeros_gu = reinterpret_cast<const __half *>(e.w4_zeros);
         p.zeros_dn = reinterpret_cast<const __half *>(e.w4_zeros + w4_zeros_gu_bytes(e.E, e.H, e.I, e.S));
     }
     p.S = e.S;
-    p.w4_colblk = w4_colblk_offset(e.E, e.H, e.I, e.S);
+    p.w4_colblk = p.q8 ? q8_units_bytes(e.E, e.H, e.I) : w4_colblk_offset(e.E, e.H, e.I, e.S);
     p.sh = e.shared;
     p.w_sgate = e.w_sgate;
     p.I_s = e.shared ? e.I_s : 0;
@@ -1360,14 +1445,17 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.nstages = nst;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    static int configured[4][64] = {};
+    static int configured[5][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
     const int ms = e.S / 16;
     const bool zp = p.zeros_gu != nullptr;
-    void (*kern)(const DkParams) = ms == 2 ? (zp ? draft_kernel<2, true> : draft_kernel<2, false>)
-                                           : (zp ? draft_kernel<1, true> : draft_kernel<1, false>);
-    const int ki = (ms - 1) * 2 + (zp ? 1 : 0);
+    if (p.q8 && (ms != 1 || zp)) return SPX_ERR_UNSUPPORTED;
+    void (*kern)(const DkParams) =
+        p.q8 ? draft_kernel<1, DK_FMT_Q8>
+             : ms == 2 ? (zp ? draft_kernel<2, DK_FMT_W4Z> : draft_kernel<2, DK_FMT_W4>)
+                       : (zp ? draft_kernel<1, DK_FMT_W4Z> : draft_kernel<1, DK_FMT_W4>);
+    const int ki = p.q8 ? 4 : (ms - 1) * 2 + (zp ? 1 : 0);
     if (!configured[ki][dev]) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (err != cudaSuccess) return record_launch(err);

@@ -67,6 +67,20 @@ __host__ __device__ inline size_t w4_zeros_gu_bytes(int E, int H, int I, int S) 
 __host__ __device__ inline size_t w4_zeros_dn_bytes(int E, int H, int I) {
     return (size_t)E * (H / 32) * (I / 128) * 32 * 2;
 }
+// GGUF Q8_0 experts (draft launch only; S = 16).  A group of 128 rows is four
+// Q8_0 blocks of 32 rows: 4 x 32 fp16 scales ([block][tile-row order], as the
+// INT4 scales) followed by the group's 8 k-steps of codes, 512 B each (32
+// lanes x 16 B; a lane's 16 B = tile 0's 8 codes, then tile 1's; code byte j
+// of a tile is register j/2, half j%2 of its A fragment).
+//   gate/up units [E][I/16]: H/128 groups (tiles: gate, up);
+//   then down, column-block-major [E][H/32][I/128] groups (tiles: the pair's two).
+constexpr int kQ8ScaleBytes = 4 * 32 * 2;
+constexpr int kQ8GroupBytes = kQ8ScaleBytes + 8 * 512;
+__host__ __device__ inline size_t q8_unit_bytes(int H) { return (size_t)(H / 128) * kQ8GroupBytes; }
+__host__ __device__ inline size_t q8_units_bytes(int E, int H, int I) { return (size_t)E * (I / 16) * q8_unit_bytes(H); }
+__host__ __device__ inline size_t q8_packed_bytes(int E, int H, int I) {
+    return q8_units_bytes(E, H, I) + (size_t)E * (H / 32) * (I / 128) * kQ8GroupBytes;
+}
 __host__ __device__ inline size_t w4_colblk_offset(int E, int H, int I, int S) {
     return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
 }
@@ -254,6 +268,19 @@ __device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t (&a)[4]) {
     a[2] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w8, kLo, kMagic)), sub));
     a[3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w8, kHi, kMagic)), mul, add));
 }
+// Eight Q8_0 codes (w0: registers 0-1, w1: registers 2-3) -> one m16k16 A
+// fragment of exact fp16 codes.  Flipping the sign bit makes the byte
+// code + 128; placed under fp16 1024.0's exponent it gives 1152 + code, and
+// subtracting 1152 leaves the code (|code| <= 128, exact).
+__device__ __forceinline__ void q8_frag(uint32_t w0, uint32_t w1, uint32_t (&a)[4]) {
+    const uint32_t kExp = 0x64646464u;
+    const __half2 sub = u32_as_h2(0x64806480u);  // (1152, 1152)
+    const uint32_t f0 = w0 ^ 0x80808080u, f1 = w1 ^ 0x80808080u;
+    a[0] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(f0, kExp, 0x4140)), sub));
+    a[1] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(f0, kExp, 0x4342)), sub));
+    a[2] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(f1, kExp, 0x4140)), sub));
+    a[3] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(f1, kExp, 0x4342)), sub));
+}
 // One packed INT4 word -> the same fragment positions holding the raw
 // magic-exponent values: registers 0 and 2 (rows m < 8) get 1024 + q,
 // registers 1 and 3 (rows m >= 8) get 1024 + 16 q, all exact in fp16.  The
@@ -286,12 +313,13 @@ struct RouteParams {
     WsHeader *hdr;
 };
 
+constexpr int kFmtQ8 = 2;  // EngineParams::routed_fmt of GGUF Q8_0 experts
 struct EngineParams {
     // routed experts (packed units)
     const uint8_t *routed;
     const __half *w4_sdown;  // INT4: down scales [E][I/128][H]
     const uint8_t *w4_zeros; // INT4, nullable: repacked per-group zero points (else 8)
-    int routed_fmt;          // 0 INT4, 1 FP16
+    int routed_fmt;          // 0 INT4, 1 FP16, kFmtQ8 GGUF Q8_0 (draft launch only)
     int S;                   // routed slice width (INT4: 16/32; FP16: 16)
     int E, I, k;
     int routed_enabled;

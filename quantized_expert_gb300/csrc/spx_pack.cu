@@ -238,6 +238,95 @@ __global__ void w4_pack_zeros_dn(const int32_t *zd, int E, int H, int I, uint16_
     }
 }
 
+// ---------------------------------------------------------- GGUF Q8_0 --
+// Canonical Q8_0 matrix [out N][in K]: per row, K/32 blocks of 34 bytes (fp16
+// scale, little-endian, then 32 int8 codes).  Code and scale of (n, k):
+__device__ __forceinline__ uint8_t q8_code(const uint8_t *w, int K, size_t e, int N, int n, int k) {
+    return w[((e * N + n) * (K / 32) + k / 32) * 34 + 2 + k % 32];
+}
+__device__ __forceinline__ uint16_t q8_scale(const uint8_t *w, int K, size_t e, int N, int n, int blk) {
+    const uint8_t *b = w + ((e * N + n) * (K / 32) + blk) * 34;
+    return (uint16_t)(b[0] | (b[1] << 8));
+}
+
+// Gate/up units: one thread per (unit, group, k-step, lane, tile) writes the
+// lane's 8 codes of that tile; scales: one thread per (unit, group, block, column).
+__global__ void q8_pack_gu(const uint8_t *wg, const uint8_t *wu, int E, int H, int I, uint8_t *packed) {
+    const int spe = I / 16, G = H / 128;
+    const size_t total = (size_t)E * spe * G * 8 * 32 * 2;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(idx & 1);
+        const int lane = (int)((idx >> 1) & 31);
+        const int kl = (int)((idx >> 6) & 7);
+        const size_t ug = idx >> 9;  // unit * G + group
+        const int grp = (int)(ug % G);
+        const size_t unit = ug / G;
+        const size_t e = unit / spe;
+        const int j = (int)(unit % spe);
+        const uint8_t *src = t == 0 ? wg : wu;
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb) {
+            const int r = jb >> 1;
+            const int n = j * 16 + frag_row(lane, r);
+            const int k = grp * 128 + kl * 16 + frag_col(lane, r, jb & 1);
+            w[jb >> 2] |= (uint32_t)q8_code(src, H, e, I, n, k) << (8 * (jb & 3));
+        }
+        uint8_t *dst = packed + unit * q8_unit_bytes(H) + (size_t)grp * kQ8GroupBytes + kQ8ScaleBytes + kl * 512 +
+                       lane * 16 + t * 8;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    }
+    const size_t ns = (size_t)E * spe * G * 4 * 32;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < ns; idx += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(idx & 31);
+        const int sb = (int)((idx >> 5) & 3);
+        const size_t ug = idx >> 7;
+        const int grp = (int)(ug % G);
+        const size_t unit = ug / G;
+        const size_t e = unit / spe;
+        const int n = (int)(unit % spe) * 16 + (c & 15);
+        const uint16_t v = q8_scale(c < 16 ? wg : wu, H, e, I, n, grp * 4 + sb);
+        reinterpret_cast<uint16_t *>(packed + unit * q8_unit_bytes(H) + (size_t)grp * kQ8GroupBytes)[sb * 32 + c] = v;
+    }
+}
+
+// Down, column-block-major: one thread per (expert, pair, group, k-step, lane,
+// tile) for the codes, one per (expert, pair, group, block, tile row) for scales.
+__global__ void q8_pack_dn(const uint8_t *wd, int E, int H, int I, uint8_t *region) {
+    const int NQ = H / 32, G = I / 128;
+    const size_t total = (size_t)E * NQ * G * 8 * 32 * 2;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int q = (int)(idx & 1);
+        const int lane = (int)((idx >> 1) & 31);
+        const int kl = (int)((idx >> 6) & 7);
+        const size_t gi = idx >> 9;  // (e * NQ + Q) * G + group
+        const int grp = (int)(gi % G);
+        const int Q = (int)((gi / G) % NQ);
+        const size_t e = gi / ((size_t)G * NQ);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb) {
+            const int r = jb >> 1;
+            const int n = down_col(2 * Q + q, frag_row(lane, r));
+            const int i = grp * 128 + kl * 16 + frag_col(lane, r, jb & 1);
+            w[jb >> 2] |= (uint32_t)q8_code(wd, I, e, H, n, i) << (8 * (jb & 3));
+        }
+        uint8_t *dst = region + gi * kQ8GroupBytes + kQ8ScaleBytes + kl * 512 + lane * 16 + q * 8;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    }
+    const size_t ns = (size_t)E * NQ * G * 4 * 32;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < ns; idx += (size_t)gridDim.x * blockDim.x) {
+        const int qm = (int)(idx & 31);
+        const int sb = (int)((idx >> 5) & 3);
+        const size_t gi = idx >> 7;
+        const int grp = (int)(gi % G);
+        const int Q = (int)((gi / G) % NQ);
+        const size_t e = gi / ((size_t)G * NQ);
+        const int n = down_col(2 * Q + (qm >> 4), qm & 15);
+        reinterpret_cast<uint16_t *>(region + gi * kQ8GroupBytes)[sb * 32 + qm] = q8_scale(wd, I, e, H, n, grp * 4 + sb);
+    }
+}
+
 }  // namespace spx
 
 using namespace spx;
@@ -280,6 +369,25 @@ extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, con
     w4_pack_colblk_scales<<<grid_for(tot), 256, 0, s>>>(s_down, E, H, I, cb);
     tot = (size_t)E * (H / 32) * (I / 128) * 512;
     w4_pack_colblk_codes<<<grid_for(tot), 256, 0, s>>>(qw_down, E, H, I, cb);
+    return record_launch(cudaGetLastError());
+}
+
+extern "C" size_t spx_q8_packed_bytes(int E, int H, int I) {
+    if (E < 1 || H < 128 || I < 128 || H % 128 || I % 128) return 0;
+    return q8_packed_bytes(E, H, I);
+}
+
+extern "C" int spx_q8_repack(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int E, int H, int I,
+                             void *packed, spx_stream_t stream) {
+    if (!w_gate || !w_up || !w_down || !packed) return SPX_ERR_INVALID_ARG;
+    if (E < 1 || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
+    if (H % 128 || I % 128 || H > kMaxH || E > kMaxE) return SPX_ERR_UNSUPPORTED;
+    if (!aligned16(packed)) return SPX_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *out = static_cast<uint8_t *>(packed);
+    q8_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 128) * 512), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
+    q8_pack_dn<<<grid_for((size_t)E * (H / 32) * (I / 128) * 512), 256, 0, s>>>(w_down, E, H, I,
+                                                                                out + q8_units_bytes(E, H, I));
     return record_launch(cudaGetLastError());
 }
 

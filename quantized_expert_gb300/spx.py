@@ -36,6 +36,10 @@ class F16Experts(C.Structure):
     _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int)]
 
 
+class Q8Experts(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int)]
+
+
 class Shared(C.Structure):
     _fields_ = [("packed", C.c_void_p), ("w_sgate", C.c_void_p), ("H", C.c_int), ("I_s", C.c_int)]
 
@@ -49,7 +53,8 @@ class LayerArgs(C.Structure):
                 ("offsets", C.c_void_p), ("sorted_slots", C.c_void_p), ("active", C.c_void_p),
                 ("n_active", C.c_void_p), ("out", C.c_void_p), ("ws", C.c_void_p), ("ws_bytes", C.c_size_t),
                 ("ev_experts_begin", C.c_void_p), ("ev_experts_end", C.c_void_p),
-                ("resident", C.c_void_p), ("ready", C.c_void_p), ("wait_budget_ns", C.c_uint64)]
+                ("resident", C.c_void_p), ("ready", C.c_void_p), ("wait_budget_ns", C.c_uint64),
+                ("q8", C.POINTER(Q8Experts))]
 
 
 _SIGS = {
@@ -67,6 +72,8 @@ _SIGS = {
     "spx_f16_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "spx_w4_repack": (C.c_int, [C.c_void_p] * 6 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_w4_zeros_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "spx_q8_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "spx_q8_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_w4_zeros_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_f16_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_workspace_size": (C.c_size_t, [C.c_int] * 6),
@@ -75,6 +82,8 @@ _SIGS = {
     "spx_workspace_init": (C.c_int, [C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "spx_moe_draft_w4a16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(W4Experts), C.c_int] + [C.c_void_p] * 5 +
+                            [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "spx_moe_draft_q8a16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(Q8Experts), C.c_int] + [C.c_void_p] * 5 +
                             [C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_moe_verify_fp16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(F16Experts), C.c_int] + [C.c_void_p] * 5 +
                             [C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -209,6 +218,17 @@ class PackedW4:
 
 
 @dataclass
+class PackedQ8:
+    buf: torch.Tensor
+    E: int
+    H: int
+    I: int
+
+    def cstruct(self) -> Q8Experts:
+        return Q8Experts(self.buf.data_ptr(), self.E, self.H, self.I)
+
+
+@dataclass
 class PackedF16:
     buf: torch.Tensor
     E: int
@@ -255,6 +275,19 @@ def spx_w4_zeros_repack(w4: PackedW4, qz_gate, qz_up, qz_down, stream=None) -> P
     return PackedW4(w4.buf, w4.E, w4.H, w4.I, w4.S, buf)
 
 
+def spx_q8_repack(w_gate, w_up, w_down, stream=None) -> PackedQ8:
+    """Canonical GGUF Q8_0 experts (uint8 gate, up [E][I][H/32][34], down
+    [E][H][I/32][34]) -> packed for the draft launch."""
+    E, I, hb, _ = w_gate.shape
+    H = hb * 32
+    n = load().spx_q8_packed_bytes(E, H, I)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_q8_packed_bytes")
+    buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
+    _chk(load().spx_q8_repack(_p(w_gate), _p(w_up), _p(w_down), E, H, I, _p(buf), _stream(stream)), "spx_q8_repack")
+    return PackedQ8(buf, E, H, I)
+
+
 def spx_f16_repack(w_gate, w_up, w_down, stream=None) -> PackedF16:
     """Canonical [E][I][H], [E][I][H], [E][H][I] fp16 -> packed units."""
     E, I, H = w_gate.shape
@@ -284,6 +317,14 @@ def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_acti
     _chk(load().spx_moe_draft_w4a16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
                                     _p(n_active), _p(y_sorted), _p(ws), ws.numel(), _stream(stream)),
          "spx_moe_draft_w4a16")
+
+
+def spx_moe_draft_q8a16(x, w: PackedQ8, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+    T = x.shape[0]
+    cs = w.cstruct()
+    _chk(load().spx_moe_draft_q8a16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
+                                    _p(n_active), _p(y_sorted), _p(ws), ws.numel(), _stream(stream)),
+         "spx_moe_draft_q8a16")
 
 
 def spx_moe_verify_fp16(x, w: PackedF16, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
@@ -321,8 +362,9 @@ class Routing:
 
 def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: PackedW4 | None = None,
                f16: PackedF16 | None = None, shared: PackedShared | None = None, w_router=None, elb=None,
-               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0):
+               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0, q8: PackedQ8 | None = None):
     """Build (and keep alive) the argument block of one spx_moe_layer call.
+    Draft experts are INT4 (w4) or GGUF Q8_0 (q8), one of the two.
     resident (uint8 [E]) and ready (int32/uint32 [E]) are the optional
     cache-aware expert order and ready flags; wait_budget_ns bounds every
     device-side wait (0 = the library default)."""
@@ -335,6 +377,10 @@ def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: Pac
         s4 = w4.cstruct()
         keep.append(s4)
         a.w4 = C.pointer(s4)
+    if q8 is not None:
+        s8 = q8.cstruct()
+        keep.append(s8)
+        a.q8 = C.pointer(s8)
     if f16 is not None:
         s16 = f16.cstruct()
         keep.append(s16)

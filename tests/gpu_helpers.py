@@ -50,12 +50,16 @@ class Layer:
     others are zero on the device (the kernels never read them)."""
 
     def __init__(self, shape: W.LayerShape, layer: int = 0, needed=None, draft=True, verify=True, slice_cols=32,
-                 zeros=False):
+                 zeros=False, q8=False):
         self.shape = s = shape
         self.layer = layer
         needed = sorted(set(range(s.E) if needed is None else needed))
         self.needed = needed
         self.w4_host = {e: W.gen_w4_expert(s, layer, e) for e in needed} if (draft or s.verify_is_dequant) else {}
+        self.q8 = None
+        if q8:  # GGUF Q8_0 draft experts instead of INT4
+            assert draft and not zeros and not (verify and s.verify_is_dequant)
+            self.w4_host = {e: W.gen_q8_expert(s, layer, e) for e in needed}
         self.zeros = zeros
         if zeros:  # asymmetric INT4: per-group zero points on every draft expert
             assert draft and not (verify and s.verify_is_dequant)
@@ -69,7 +73,9 @@ class Layer:
         self.shared_host = W.gen_shared(s, layer)
         self.router_host = W.gen_router(s, layer) if s.logits == "router" else None
         self.w4 = self.f16 = self.shared = None
-        if draft:
+        if draft and q8:
+            self.q8 = self._pack_q8()
+        elif draft:
             self.w4 = self._pack_w4(slice_cols)
         if verify:
             self.f16 = self._pack_f16()
@@ -100,6 +106,18 @@ class Layer:
             for e, ex in self.w4_host.items():
                 zg[e], zu[e], zd[e] = ex["qz_gate"], ex["qz_up"], ex["qz_down"]
             p = spx.spx_w4_zeros_repack(p, dev(zg), dev(zu), dev(zd))
+        torch.cuda.synchronize()
+        return p
+
+    def _pack_q8(self):
+        s = self.shape
+        E, H, I = s.E, s.H, s.I
+        wg = np.zeros((E, I, H // 32, 34), np.uint8)
+        wu = np.zeros_like(wg)
+        wd = np.zeros((E, H, I // 32, 34), np.uint8)
+        for e, ex in self.w4_host.items():
+            wg[e], wu[e], wd[e] = ex["q8_gate"], ex["q8_up"], ex["q8_down"]
+        p = spx.spx_q8_repack(dev(wg), dev(wu), dev(wd))
         torch.cuda.synchronize()
         return p
 

@@ -260,7 +260,7 @@ def _run_layer(lay, mode, x, logits, elb=None):
         T, s.E, dtype=torch.float32, device="cuda")
     args, keep = spx.layer_args(0 if mode == "draft" else 1, gh.dev_f16(x), s.E, s.k, s.renorm, d_lg, routing, out,
                                 ws, w4=lay.w4, f16=lay.f16, shared=lay.shared, w_router=lay.w_router, elb=elb,
-                                layer=lay.layer)
+                                layer=lay.layer, q8=lay.q8)
     outs = []
     for rep in range(2):
         spx.spx_moe_layer(args, None)
@@ -636,3 +636,83 @@ def test_zero_points_unsupported_outside_the_draft_launch():
     with pytest.raises(SpxError) as ei:
         spx.spx_moe_layer(args, None)
     assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------- GGUF Q8_0 drafts
+@pytest.mark.parametrize("name,T", [("deepseek_v2_lite", 1), ("deepseek_v2_lite", 8), ("qwen15_moe", 1),
+                                    ("phi35_moe", 1)])
+def test_q8_draft_layer_full_size(name, T):
+    """GGUF Q8_0 draft experts (fp16 scale per 32 weights, int8 codes) at
+    full size through spx_moe_layer: routing bit-exact, output within
+    tolerance of the oracle."""
+    gh = _gh()
+    s = W.CONFIGS[name]
+    x = W.gen_x(s, T, step=100 + T)
+    logits = None if s.logits == "router" else W.gen_logits(s, T, step=100 + T)
+    need = gh.needed_experts(s, [logits], [x])
+    lay = gh.Layer(s, needed=need, verify=False, q8=True)
+    ref = lay.oracle_layer("draft", x, logits=logits)
+    outs, routing, _ = _run_layer(lay, "draft", x, logits)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    g = ref["gather"]
+    assert np.array_equal(routing.sorted_slots.cpu().numpy(), g["sorted_slots"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"q8 {name} T={T} rep {rep}")
+
+
+@pytest.mark.parametrize("case", [1, 2, 4])
+def test_q8_draft_unit_call(case):
+    """spx_moe_draft_q8a16 on the small cases of at most 8 tokens with
+    16-column slices: per-slot expert outputs against the oracle."""
+    spx, gh = _spx(), _gh()
+    s, T, S = SMALL_CASES[case]
+    x = W.gen_x(s, T, step=110 + case)
+    lg = np.random.default_rng(110 + case).standard_normal((T, s.E))
+    ids, w = oracle.route_topk(lg, s.k, s.renorm)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), verify=False, q8=True)
+    g, r = _routing_dev(ids, s.E)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    y_ref = np.stack([oracle.swiglu_q8(x[int(sl) // s.k], lay.w4_host[int(ids.reshape(-1)[sl])])
+                      for sl in g["sorted_slots"]])
+    y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
+    for rep in range(2):
+        spx.spx_moe_draft_q8a16(gh.dev_f16(x), lay.q8, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                                r["n_active"], y, ws)
+        torch.cuda.synchronize()
+        gh.check_close(y.cpu().numpy(), y_ref, f"q8 case {case} rep {rep}")
+    assert spx.spx_workspace_status(ws) == 0
+
+
+def test_q8_unsupported_and_invalid_calls():
+    """Q8_0 experts are served by the draft launch (T <= 8) only: a larger
+    batch and the cache-aware path return SPX_ERR_UNSUPPORTED; INT4 and Q8_0
+    experts in one call are an invalid argument."""
+    spx, gh = _spx(), _gh()
+    from quantized_expert_gb300.spx import SpxError
+    s = _small("deepseek_v2_lite", I=256, E=16)
+    lay = gh.Layer(s, needed=list(range(s.E)), verify=False, q8=True)
+    T = 9
+    ids, _ = oracle.route_topk(np.random.default_rng(120).standard_normal((T, s.E)), s.k, s.renorm)
+    g, r = _routing_dev(ids, s.E)
+    y = torch.empty(T * s.k, s.H, device="cuda")
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_draft_q8a16(gh.dev_f16(W.gen_x(s, T)), lay.q8, s.k, r["offsets"], r["sorted_slots"],
+                                r["active"], r["n_active"], y, spx.new_workspace(T, s.H, s.I, s.E, s.k))
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
+    T = 1
+    routing = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    lg = gh.dev(np.random.default_rng(121).standard_normal((T, s.E)).astype(np.float32))
+    x = gh.dev_f16(W.gen_x(s, T))
+    resident = torch.ones(s.E, dtype=torch.uint8, device="cuda")
+    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, q8=lay.q8, shared=lay.shared,
+                                resident=resident)
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_layer(args, None)
+    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
+    w4 = gh.Layer(s, needed=[0], verify=False, slice_cols=16).w4
+    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, w4=w4, q8=lay.q8)
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_layer(args, None)
+    assert ei.value.status == spx.SPX_ERR_INVALID_ARG
