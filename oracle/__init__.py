@@ -78,6 +78,9 @@ def lib():
             L.orc_swiglu_f16.argtypes = [_u16, C.c_int, C.c_int, _u16, _u16, _u16, _dp, C.c_void_p]
             L.orc_q8_dequant.argtypes = [_u8, C.c_int, C.c_int, _dp]
             L.orc_swiglu_q8.argtypes = [_u16, C.c_int, C.c_int, _u8, _u8, _u8, _dp, C.c_void_p]
+            L.orc_q2k_dequant.argtypes = [_u8, C.c_int, C.c_int, _dp]
+            L.orc_swiglu_gguf.argtypes = [_u16, C.c_int, C.c_int, C.c_int, _u8, C.c_int, _u8, C.c_int, _u8, _dp,
+                                          C.c_void_p]
             L.orc_shared_gate.argtypes = [_u16, _u16, C.c_int]
             L.orc_shared_gate.restype = C.c_double
             L.orc_combine.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, C.c_void_p, C.c_void_p, _dp, _u16]
@@ -199,8 +202,32 @@ def swiglu_q8(x_row, ex: dict, want_h: bool = False):
     return (y, h) if want_h else y
 
 
+def q2k_dequant(w) -> np.ndarray:
+    """GGUF Q2_K matrix, uint8 [N][K/256][84] super-blocks ([out][in] order) -> W [N][K]."""
+    w = _c(w, np.uint8)
+    N, K = w.shape[0], w.shape[1] * 256
+    out = np.empty((N, K), np.float64)
+    lib().orc_q2k_dequant(w, N, K, out)
+    return out
+
+
+def swiglu_q2k(x_row, ex: dict, want_h: bool = False):
+    """Expert with Q2_K gate/up (q2k_gate, q2k_up [I][H/256][84] uint8) and a
+    Q8_0 down projection (q8_down [H][I/32][34])."""
+    x_row = _c(x_row, np.uint16)
+    H = x_row.shape[0]
+    I = ex["q2k_gate"].shape[0]
+    y = np.empty(H, np.float64)
+    h = np.empty(I, np.float64) if want_h else None
+    lib().orc_swiglu_gguf(x_row, H, I, 1, _c(ex["q2k_gate"], np.uint8), 1, _c(ex["q2k_up"], np.uint8), 0,
+                          _c(ex["q8_down"], np.uint8), y, h.ctypes.data if want_h else None)
+    return (y, h) if want_h else y
+
+
 def swiglu_draft(x_row, ex: dict, want_h: bool = False):
-    """The draft expert MLP in the expert's own format (Q8_0 or INT4)."""
+    """The draft expert MLP in the expert's own format (Q2_K/Q8_0, Q8_0 or INT4)."""
+    if "q2k_gate" in ex:
+        return swiglu_q2k(x_row, ex, want_h)
     return swiglu_q8(x_row, ex, want_h) if "q8_gate" in ex else swiglu_w4(x_row, ex, want_h)
 
 

@@ -350,9 +350,46 @@ void orc_q8_dequant(const uint8_t *w, int N, int K, double *out)
             out[(int64_t)n * K + kk] = q8_at(w, tab, K, n, kk);
 }
 
-/* Q8_0 expert on one token: wg, wu [I][H/32] blocks; wd [H][I/32] blocks. */
-void orc_swiglu_q8(const uint16_t *x, int H, int I, const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
-                   double *y, double *h_out)
+/* GGUF Q2_K [S1 Main Findings: GGUF Q2 drafts].  Reading (the GGUF
+ * format): a row is cut into super-blocks of 256 consecutive values, each
+ * 84 bytes: 16 bytes of sub-block parameters, 64 bytes of 2-bit codes, then
+ * the binary16 scale d and the binary16 min scale dmin (little-endian).
+ * Sub-block b = 16 consecutive values; its byte holds the 4-bit scale sc
+ * (low nibble) and the 4-bit min m (high nibble).  Value w of the
+ * super-block has its code q (0..3) at bits 2*((w % 128) / 32) of code byte
+ * 32*(w / 128) + w % 32, and equals d*sc*q - dmin*m.  Rows need a multiple
+ * of 256 values. */
+static inline double q2k_at(const uint8_t *w, const double *tab, int K, int n, int kk)
+{
+    const uint8_t *blk = w + ((int64_t)n * (K / 256) + kk / 256) * 84;
+    int wi = kk % 256;
+    int par = blk[wi / 16];
+    int q = (blk[16 + 32 * (wi / 128) + wi % 32] >> (2 * ((wi % 128) / 32))) & 3;
+    double d = tab[(uint16_t)(blk[80] | (blk[81] << 8))];
+    double dmin = tab[(uint16_t)(blk[82] | (blk[83] << 8))];
+    return d * (double)(par & 15) * (double)q - dmin * (double)(par >> 4);
+}
+
+/* Matrix value by format: ORC_Q8_0 or ORC_Q2_K. */
+enum { ORC_Q8_0 = 0, ORC_Q2_K = 1 };
+static inline double gguf_at(int type, const uint8_t *w, const double *tab, int K, int n, int kk)
+{
+    return type == ORC_Q2_K ? q2k_at(w, tab, K, n, kk) : q8_at(w, tab, K, n, kk);
+}
+
+/* out[n][kk] = W[n][kk] of a Q2_K matrix, N x K ([out][in]). */
+void orc_q2k_dequant(const uint8_t *w, int N, int K, double *out)
+{
+    const double *tab = half_tab();
+    for (int n = 0; n < N; ++n)
+        for (int kk = 0; kk < K; ++kk)
+            out[(int64_t)n * K + kk] = q2k_at(w, tab, K, n, kk);
+}
+
+/* GGUF expert on one token, each matrix in its own format (tg, tu, td):
+ * wg, wu [I] rows of H values; wd [H] rows of I values. */
+void orc_swiglu_gguf(const uint16_t *x, int H, int I, int tg, const uint8_t *wg, int tu, const uint8_t *wu, int td,
+                     const uint8_t *wd, double *y, double *h_out)
 {
     const double *tab = half_tab();
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
@@ -360,20 +397,27 @@ void orc_swiglu_q8(const uint16_t *x, int H, int I, const uint8_t *wg, const uin
         double g = 0.0, u = 0.0;
         for (int kk = 0; kk < H; ++kk) {
             double xk = tab[x[kk]];
-            g += q8_at(wg, tab, H, i, kk) * xk;
-            u += q8_at(wu, tab, H, i, kk) * xk;
+            g += gguf_at(tg, wg, tab, H, i, kk) * xk;
+            u += gguf_at(tu, wu, tab, H, i, kk) * xk;
         }
         h[i] = silu(g) * u;
     }
     for (int n = 0; n < H; ++n) {
         double acc = 0.0;
         for (int i = 0; i < I; ++i)
-            acc += q8_at(wd, tab, I, n, i) * h[i];
+            acc += gguf_at(td, wd, tab, I, n, i) * h[i];
         y[n] = acc;
     }
     if (h_out)
         memcpy(h_out, h, sizeof(double) * (size_t)I);
     free(h);
+}
+
+/* Q8_0 expert on one token: wg, wu [I][H/32] blocks; wd [H][I/32] blocks. */
+void orc_swiglu_q8(const uint16_t *x, int H, int I, const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
+                   double *y, double *h_out)
+{
+    orc_swiglu_gguf(x, H, I, ORC_Q8_0, wg, ORC_Q8_0, wu, ORC_Q8_0, wd, y, h_out);
 }
 
 /* FP16 expert, PyTorch [out, in] layout: wg, wu [I][H]; wd [H][I]. */

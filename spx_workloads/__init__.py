@@ -44,7 +44,8 @@ __all__ = [
 ]
 
 # stream tags (part of the seeding key, never of the arithmetic)
-TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM, TAG_ZEROS, TAG_Q8 = range(1, 11)
+(TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM, TAG_ZEROS, TAG_Q8,
+ TAG_Q2K) = range(1, 12)
 HOT_LOG_A = 1.1510  # ln a, a = 3.1614
 ZIPF_S = 1.1
 
@@ -223,6 +224,28 @@ def gen_q8_expert(shape: LayerShape, layer: int, e: int) -> dict:
     H, I = shape.H, shape.I
     rng = rng_for(shape, TAG_Q8, layer, e)
     return dict(q8_gate=_q8_matrix(rng, I, H), q8_up=_q8_matrix(rng, I, H), q8_down=_q8_matrix(rng, H, I))
+
+
+def _q2k_matrix(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
+    """GGUF Q2_K super-blocks of an [N][K] matrix: uint8 [N][K/256][84]; the
+    sub-block bytes and codes uniform, d U(0.001, 0.003) and dmin
+    U(0.001, 0.004) fp16 little-endian (weights of the INT4 experts' scale)."""
+    out = rng.integers(0, 256, size=(N, K // 256, 84), dtype=np.uint8)
+    d = rng.uniform(0.001, 0.003, size=(N, K // 256)).astype(np.float16).view(np.uint16)
+    dmin = rng.uniform(0.001, 0.004, size=(N, K // 256)).astype(np.float16).view(np.uint16)
+    out[:, :, 80], out[:, :, 81] = d & 0xFF, d >> 8
+    out[:, :, 82], out[:, :, 83] = dmin & 0xFF, dmin >> 8
+    return out
+
+
+def gen_q2k_expert(shape: LayerShape, layer: int, e: int) -> dict:
+    """Draft expert e with GGUF Q2_K gate/up (``q2k_gate``/``q2k_up``
+    [I][H/256][84] uint8) and a GGUF Q8_0 down projection (``q8_down``
+    [H][I/32][34]): Q2_K rows need a multiple of 256 values, which the down
+    rows (I values) of the 1408-wide shapes are not."""
+    H, I = shape.H, shape.I
+    rng = rng_for(shape, TAG_Q2K, layer, e)
+    return dict(q2k_gate=_q2k_matrix(rng, I, H), q2k_up=_q2k_matrix(rng, I, H), q8_down=_q8_matrix(rng, H, I))
 
 
 def gen_f16_expert(shape: LayerShape, layer: int, e: int) -> dict:

@@ -329,6 +329,96 @@ def test_q8_mlp_matches_dequantised_matmul():
     assert np.allclose(oracle.swiglu_q8(x, ex), ref, rtol=1e-10, atol=1e-10)
 
 
+# ------------------------------------------------------- GGUF Q2_K draft
+def _q2k_blocks(q, sc, mn, d, dmin):
+    """Codes q [N][K] (0..3), sub-block scales and mins [N][K/16] (0..15), fp16
+    d and dmin [N][K/256] -> [N][K/256][84] uint8 Q2_K super-blocks (code of
+    value w at bits 2*((w%128)//32) of byte 16 + 32*(w//128) + w%32)."""
+    N, K = q.shape
+    out = np.zeros((N, K // 256, 84), np.uint8)
+    out[:, :, :16] = (np.asarray(sc) | (np.asarray(mn) << 4)).reshape(N, K // 256, 16)
+    qb = q.reshape(N, K // 256, 256)
+    for w in range(256):
+        out[:, :, 16 + 32 * (w // 128) + w % 32] |= (qb[:, :, w] << (2 * ((w % 128) // 32))).astype(np.uint8)
+    for off, v in ((80, d), (82, dmin)):
+        bits = np.asarray(v, np.float16).view(np.uint16)
+        out[:, :, off] = bits & 0xFF
+        out[:, :, off + 1] = bits >> 8
+    return out
+
+
+def test_q2k_dequant_hand_derived_golden():
+    gold = json.load(open(os.path.join(GOLD, "gguf_q2_k.json")))
+    blk = np.zeros((1, 1, 84), np.uint8)
+    blk[0, 0, :16] = gold["sub_block_bytes"]
+    for i, v in gold["code_bytes"].items():
+        blk[0, 0, 16 + int(i)] = v
+    blk[0, 0, 80:82] = gold["d_bytes"]
+    blk[0, 0, 82:84] = gold["dmin_bytes"]
+    assert float(np.array(gold["d_bytes"], np.uint8).view(np.float16)[0]) == gold["d"]
+    assert float(np.array(gold["dmin_bytes"], np.uint8).view(np.float16)[0]) == gold["dmin"]
+    out = oracle.q2k_dequant(blk)[0]
+    for w, v in gold["checks"]:
+        assert out[w] == v, w
+
+
+def test_q2k_dequant_every_position_closed_form():
+    """d*sc*q - dmin*m at every value position of two super-blocks per row,
+    every code, every scale and min nibble."""
+    rng = np.random.default_rng(11)
+    N, K = 6, 512
+    q = rng.integers(0, 4, size=(N, K))
+    sc = rng.integers(0, 16, size=(N, K // 16))
+    mn = rng.integers(0, 16, size=(N, K // 16))
+    d = rng.uniform(0.01, 0.1, size=(N, K // 256)).astype(np.float16)
+    dmin = rng.uniform(0.01, 0.1, size=(N, K // 256)).astype(np.float16)
+    out = oracle.q2k_dequant(_q2k_blocks(q, sc, mn, d, dmin))
+    rep16 = lambda a: np.repeat(a, 16, axis=1)  # noqa: E731
+    rep256 = lambda a: np.repeat(np.asarray(a, np.float64), 256, axis=1)  # noqa: E731
+    ref = rep256(d) * rep16(sc) * q - rep256(dmin) * rep16(mn)
+    assert np.array_equal(out, ref)
+    assert set(np.unique(q)) == set(range(4)) and set(np.unique(sc)) == set(range(16))
+
+
+def test_q2k_expert_equals_its_fp16_copy():
+    """Q2_K gate/up and Q8_0 down with power-of-two scales, so every weight is
+    exact in fp16: the expert equals the FP16 oracle on those weights term
+    for term (both sum in the same order)."""
+    rng = np.random.default_rng(12)
+    H, I = 512, 256
+    ex = {}
+    for name in ("gate", "up"):
+        q = rng.integers(0, 4, size=(I, H))
+        sc = rng.integers(0, 16, size=(I, H // 16))
+        mn = rng.integers(0, 16, size=(I, H // 16))
+        d = np.full((I, H // 256), 2.0 ** -9)
+        dmin = np.full((I, H // 256), 2.0 ** -8)
+        ex["q2k_" + name] = _q2k_blocks(q, sc, mn, d, dmin)
+    codes = rng.integers(-128, 128, size=(H, I))
+    ex["q8_down"] = _q8_blocks(codes, np.full((H, I // 32), 2.0 ** -12))
+    f16 = dict(w_gate=oracle.q2k_dequant(ex["q2k_gate"]).astype(np.float16).view(np.uint16),
+               w_up=oracle.q2k_dequant(ex["q2k_up"]).astype(np.float16).view(np.uint16),
+               w_down=oracle.q8_dequant(ex["q8_down"]).astype(np.float16).view(np.uint16))
+    assert np.array_equal(f16["w_gate"].view(np.float16).astype(np.float64), oracle.q2k_dequant(ex["q2k_gate"]))
+    shape = W.scaled(W.CONFIGS["tiny"], H=H, I=I)
+    for step in range(2):
+        x = W.gen_x(shape, 1, step=step)[0]
+        y2, h2 = oracle.swiglu_q2k(x, ex, want_h=True)
+        y16, h16 = oracle.swiglu_f16(x, f16, want_h=True)
+        assert np.array_equal(h2, h16) and np.array_equal(y2, y16)
+
+
+def test_q2k_identity_expert_closed_form():
+    n = 256
+    q = np.eye(n, dtype=np.int64)
+    one = np.ones((n, n // 16), np.int64)
+    gu = _q2k_blocks(q, one, 0 * one, np.ones((n, 1)), np.ones((n, 1)))
+    ex = dict(q2k_gate=gu, q2k_up=gu, q8_down=_q8_blocks(np.eye(n, dtype=np.int64), np.ones((n, n // 32))))
+    x = (np.random.default_rng(13).standard_normal(n) * 2).astype(np.float16)
+    xd = x.astype(np.float64)
+    assert np.allclose(oracle.swiglu_q2k(x.view(np.uint16), ex), xd * expit(xd) * xd, rtol=1e-14, atol=1e-300)
+
+
 # ---------------------------------------------------------------- MLP
 def _identity_w4(n):
     q = np.full((n // 8, n), 0x88888888, np.uint32)
