@@ -72,9 +72,11 @@ def f16_expert_bytes(s, I=None):
     return 3 * s.H * I * 2
 
 
-def layer_bytes(s, mode, T, n_unique, zeros=False, q8=False):
-    if q8:  # GGUF Q8_0: 34 bytes per 32 weights
+def layer_bytes(s, mode, T, n_unique, zeros=False, gguf=None):
+    if gguf == "q8_0":  # GGUF Q8_0: 34 bytes per 32 weights
         b = n_unique * 3 * s.H * s.I * 34 // 32
+    elif gguf == "q2_k":  # Q2_K gate/up (84 bytes per 256 weights), Q8_0 down
+        b = n_unique * (2 * s.H * s.I * 84 // 256 + s.H * s.I * 34 // 32)
     else:
         b = n_unique * (w4_expert_bytes(s) if mode == "draft" else f16_expert_bytes(s))
     if zeros:  # fp16 zero points: one per group of 128 rows and column, of the three matrices
@@ -698,20 +700,30 @@ def run_draft_batch(args):
             st["w4"] = spx.spx_w4_zeros_repack(st["w4"], words(E, H // 128, I // 8), words(E, H // 128, I // 8),
                                                words(E, I // 128, H // 8))
         torch.cuda.synchronize()
-    if args.q8:  # GGUF Q8_0 experts instead of INT4: random codes, scales U(0.0003, 0.00125)
+    if args.gguf:  # GGUF experts instead of INT4: random codes, scales of the INT4 weights' magnitude
         E, H, I = s.E, s.H, s.I
         for i, st in enumerate(sets):
             g = torch.Generator(device="cuda")
             g.manual_seed(3_000_017 * (s.seed + 1) + i)
 
-            def blocks(N, K):
+            def scales(shape, lo, hi):
+                return (torch.rand(shape, device="cuda", generator=g) * (hi - lo) + lo).half().view(torch.uint8)
+
+            def q8(N, K):  # Q8_0 blocks, d U(0.0003, 0.00125)
                 b = torch.randint(0, 256, (E, N, K // 32, 34), dtype=torch.uint8, device="cuda", generator=g)
-                d = (torch.rand((E, N, K // 32), device="cuda", generator=g) * 0.00095 + 0.0003).half()
-                b[..., :2] = d.view(torch.uint8).view(E, N, K // 32, 2)
+                b[..., :2] = scales((E, N, K // 32), 0.0003, 0.00125).view(E, N, K // 32, 2)
                 return b
 
+            def q2k(N, K):  # Q2_K super-blocks, d U(0.001, 0.003), dmin U(0.001, 0.004)
+                b = torch.randint(0, 256, (E, N, K // 256, 84), dtype=torch.uint8, device="cuda", generator=g)
+                b[..., 80:82] = scales((E, N, K // 256), 0.001, 0.003).view(E, N, K // 256, 2)
+                b[..., 82:84] = scales((E, N, K // 256), 0.001, 0.004).view(E, N, K // 256, 2)
+                return b
+
+            gu = q8 if args.gguf == "q8_0" else q2k
             st["w4"] = None
-            st["q8"] = spx.spx_q8_repack(blocks(I, H), blocks(I, H), blocks(H, I))
+            st["gguf"] = spx.spx_gguf_repack(gu(I, H), gu(I, H), q8(H, I),
+                                             spx.SPX_GGUF_Q8_0 if args.gguf == "q8_0" else spx.SPX_GGUF_Q2_K)
             torch.cuda.synchronize()
     peak, peak_src = measured_peaks()
     rows = []
@@ -726,14 +738,14 @@ def run_draft_batch(args):
         out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
         keep = [spx.layer_args(0, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, out, ws,
                                w4=sets[i % NSETS]["w4"], shared=sets[i % NSETS]["shared"],
-                               w_router=sets[i % NSETS]["w_router"], q8=sets[i % NSETS].get("q8"))
+                               w_router=sets[i % NSETS]["w_router"], gguf=sets[i % NSETS].get("gguf"))
                 for i in range(NSETS * NINPUTS)]
         nb = []
         for i in range(NINPUTS):
             spx.spx_moe_layer(keep[i][0])
             torch.cuda.synchronize()
             nb.append((int(r.n_active.item()),
-                       layer_bytes(s, "draft", T, int(r.n_active.item()), args.zeros, args.q8)))
+                       layer_bytes(s, "draft", T, int(r.n_active.item()), args.zeros, args.gguf)))
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 spx.spx_moe_layer(keep[i % len(keep)][0], stream)
@@ -751,7 +763,8 @@ def run_draft_batch(args):
                      "gbs": round(byt / (us * 1e-6) / 1e9, 1), "frac": round(byt / (us * 1e-6) / 1e9 / peak, 3),
                      "tokens_per_s": round(T / (us * 1e-6), 1)})
         assert spx.spx_workspace_status(ws) == 0
-    zp = ", per-group zero points" if args.zeros else ", GGUF Q8_0 experts" if args.q8 else ""
+    zp = (", per-group zero points" if args.zeros else ", GGUF Q8_0 experts" if args.gguf == "q8_0"
+          else ", GGUF Q2_K gate/up + Q8_0 down experts" if args.gguf == "q2_k" else "")
     line = {"metric": "draft layer with T requests' tokens per call, device us per layer",
             "config": {"workload": f"{s.name} draft{zp}, T = 1, 2, 4, 8 (one token per request)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
@@ -781,7 +794,7 @@ def main():
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
     ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
-    ap.add_argument("--q8", action="store_true", help="with --draft-batch: GGUF Q8_0 experts instead of INT4")
+    ap.add_argument("--gguf", choices=["q8_0", "q2_k"], help="with --draft-batch: GGUF experts instead of INT4")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
     if args.loop:

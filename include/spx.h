@@ -157,18 +157,27 @@ typedef struct {
     int E, H, I;
 } spx_f16_experts;
 
-/* GGUF Q8_0 draft experts [P1 Main Findings: GGUF drafts at Q2, Q4 and Q8].
- * Canonical input per matrix, PyTorch [out][in] order: each row of `in`
- * weights is in/32 blocks of 34 bytes, a binary16 scale d (little-endian)
- * then 32 signed 8-bit codes, weight j of the block = d * code[j]:
- *   gate, up [E][I][H/32][34]; down [E][H][I/32][34]  (uint8, device).
- * Repacked (spx_q8_repack) into the draft launch's streaming order, 16
- * columns per slice.  Served by draft calls of T <= 8 (the one-launch draft
- * path); other calls with Q8_0 experts return SPX_ERR_UNSUPPORTED. */
+/* GGUF draft experts [P1 Main Findings: GGUF drafts at Q2, Q4 and Q8].
+ * Canonical input per matrix, uint8 on the device, PyTorch [out][in] order
+ * (each row holds the `in` weights of one output):
+ *   Q8_0: a row is in/32 blocks of 34 bytes, a binary16 scale d
+ *     (little-endian) then 32 signed 8-bit codes; weight j = d * code[j].
+ *   Q2_K: a row is in/256 super-blocks of 84 bytes: 16 bytes, one per
+ *     sub-block of 16 weights (low nibble scale sc, high nibble min m); 64
+ *     bytes of 2-bit codes, weight w's code at bits 2*((w % 128) / 32) of byte
+ *     32*(w / 128) + w % 32; binary16 d; binary16 dmin (little-endian);
+ *     weight = d * sc * q - dmin * m.  Needs in % 256 == 0.
+ * gate and up are in gate_up_type ([E][I][H/32][34] or [E][I][H/256][84]);
+ * down is Q8_0 ([E][H][I/32][34]): the down rows of the 1408-wide shapes are
+ * not a multiple of 256.  Repacked (spx_gguf_repack) into the draft launch's
+ * streaming order, 16 columns per slice.  Served by draft calls of T <= 8
+ * (the one-launch draft path); other calls return SPX_ERR_UNSUPPORTED. */
+enum { SPX_GGUF_Q8_0 = 0, SPX_GGUF_Q2_K = 1 };
 typedef struct {
-    const void *packed; /* spx_q8_packed_bytes() bytes, from spx_q8_repack() */
+    const void *packed; /* spx_gguf_packed_bytes() bytes, from spx_gguf_repack() */
     int E, H, I;
-} spx_q8_experts;
+    int gate_up_type;   /* SPX_GGUF_Q8_0 or SPX_GGUF_Q2_K */
+} spx_gguf_experts;
 
 /* Shared expert(s): one FP16 MLP of intermediate size I_s (several shared
  * experts concatenated along I are one MLP, as the intermediate sum splits).
@@ -182,7 +191,8 @@ typedef struct {
 
 SPX_API size_t spx_w4_packed_bytes(int E, int H, int I, int slice_cols);
 SPX_API size_t spx_f16_packed_bytes(int E, int H, int I);
-SPX_API size_t spx_q8_packed_bytes(int E, int H, int I); /* H, I multiples of 128; else 0 */
+/* H, I multiples of 128 (Q2_K: H of 256); else 0 */
+SPX_API size_t spx_gguf_packed_bytes(int E, int H, int I, int gate_up_type);
 /* Shared expert pack: the FP16 units of one expert followed by its down
  * weights once more in output-block order (read by the draft launch). */
 SPX_API size_t spx_shared_packed_bytes(int H, int I_s);
@@ -203,11 +213,11 @@ SPX_API size_t spx_w4_zeros_bytes(int E, int H, int I, int slice_cols);
 SPX_API int spx_w4_zeros_repack(const int32_t *qz_gate, const int32_t *qz_up, const int32_t *qz_down,
                                 int E, int H, int I, int slice_cols, void *zeros, spx_stream_t stream);
 
-/* Repack canonical GGUF Q8_0 experts (layout above spx_q8_experts) into
- * `packed` (device, 16-byte aligned, spx_q8_packed_bytes() bytes);
+/* Repack canonical GGUF experts (layouts above spx_gguf_experts) into
+ * `packed` (device, 16-byte aligned, spx_gguf_packed_bytes() bytes);
  * deterministic. */
-SPX_API int spx_q8_repack(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int E, int H, int I,
-                          void *packed, spx_stream_t stream);
+SPX_API int spx_gguf_repack(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int E, int H, int I,
+                            int gate_up_type, void *packed, spx_stream_t stream);
 
 /* Repack one canonical FP16 shared expert ([I_s][H], [I_s][H], [H][I_s]) into
  * `packed` (device, spx_shared_packed_bytes() bytes, 16-byte aligned). */
@@ -252,9 +262,9 @@ SPX_API int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_experts *
                         const int32_t *active, const int32_t *n_active,
                         float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream);
 
-/* The draft unit call with GGUF Q8_0 experts (T <= 8; else
- * SPX_ERR_UNSUPPORTED); arguments and output as spx_moe_draft_w4a16. */
-SPX_API int spx_moe_draft_q8a16(const uint16_t *x, int T, const spx_q8_experts *w, int k,
+/* The draft unit call with GGUF experts (T <= 8; else SPX_ERR_UNSUPPORTED);
+ * arguments and output as spx_moe_draft_w4a16. */
+SPX_API int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_experts *w, int k,
                         const int32_t *offsets, const int32_t *sorted_slots,
                         const int32_t *active, const int32_t *n_active,
                         float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream);
@@ -318,10 +328,10 @@ typedef struct {
     const uint32_t *ready;
     /* Bound of every device-side wait of the call in ns; 0 = 2 s. */
     uint64_t wait_budget_ns;
-    /* mode 0 with GGUF Q8_0 draft experts instead of INT4 (w4 must then be
-     * NULL): draft calls of T <= 8 without cache-aware options only, else
+    /* mode 0 with GGUF draft experts instead of INT4 (w4 must then be NULL):
+     * draft calls of T <= 8 without cache-aware options only, else
      * SPX_ERR_UNSUPPORTED. */
-    const spx_q8_experts *q8;
+    const spx_gguf_experts *gguf;
 } spx_layer_args;
 
 /* One layer.  Draft calls with T <= 8 (and no cache-aware options) are one

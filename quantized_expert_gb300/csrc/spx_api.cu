@@ -83,7 +83,7 @@ extern "C" const char *spx_status_string(int st) {
     }
 }
 
-extern "C" int spx_version(void) { return 103; }
+extern "C" int spx_version(void) { return 104; }
 
 extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
@@ -172,19 +172,24 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     return launch_engine(p, s, false);
 }
 
-extern "C" int spx_moe_draft_q8a16(const uint16_t *x, int T, const spx_q8_experts *w, int k, const int32_t *offsets,
+static int gguf_fmt(const spx_gguf_experts *w) {
+    return w->gate_up_type == SPX_GGUF_Q8_0 ? kFmtQ8 : w->gate_up_type == SPX_GGUF_Q2_K ? kFmtQ2K : -1;
+}
+
+extern "C" int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_experts *w, int k, const int32_t *offsets,
                                    const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
                                    float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream) {
     if (!w || !w->packed || !y_sorted) return SPX_ERR_INVALID_ARG;
     int st = check_expert_common(x, T, w->H, w->E, w->I, k, offsets, sorted_slots, active, n_active, ws, ws_bytes, 0,
                                  16);
     if (st) return st;
-    if (!al16(w->packed) || !al16(y_sorted)) return SPX_ERR_INVALID_ARG;
-    if (!draft_supported(T, w->H, w->I, 16, 0, w->E, k)) return SPX_ERR_UNSUPPORTED;  // the draft launch only
+    if (!al16(w->packed) || !al16(y_sorted) || gguf_fmt(w) < 0) return SPX_ERR_INVALID_ARG;
+    if (!draft_supported(T, w->H, w->I, 16, 0, w->E, k, gguf_fmt(w) == kFmtQ2K))
+        return SPX_ERR_UNSUPPORTED;  // the draft launch only
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
     p.routed = static_cast<const uint8_t *>(w->packed);
-    p.routed_fmt = kFmtQ8;
+    p.routed_fmt = gguf_fmt(w);
     p.S = 16;
     p.E = w->E;
     p.I = w->I;
@@ -285,13 +290,13 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     int I = 0;
     const uint8_t *routed = nullptr;
     int S = kF16S;
-    const bool q8 = a->mode == 0 && a->q8;
-    if (q8) {
-        if (a->w4 || !a->q8->packed || a->q8->E != E || a->q8->H != H) return SPX_ERR_INVALID_ARG;
-        if (!al16(a->q8->packed)) return SPX_ERR_INVALID_ARG;
-        I = a->q8->I;
+    const bool gguf = a->mode == 0 && a->gguf;
+    if (gguf) {
+        if (a->w4 || !a->gguf->packed || a->gguf->E != E || a->gguf->H != H) return SPX_ERR_INVALID_ARG;
+        if (!al16(a->gguf->packed) || gguf_fmt(a->gguf) < 0) return SPX_ERR_INVALID_ARG;
+        I = a->gguf->I;
         S = 16;
-        routed = static_cast<const uint8_t *>(a->q8->packed);
+        routed = static_cast<const uint8_t *>(a->gguf->packed);
     } else if (a->mode == 0) {
         if (!a->w4 || !a->w4->packed || a->w4->E != E || a->w4->H != H) return SPX_ERR_INVALID_ARG;
         if (!al16(a->w4->packed) || !al16(a->w4->zeros)) return SPX_ERR_INVALID_ARG;
@@ -316,9 +321,10 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     const bool cache_aware = a->resident || a->ready;
     const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
 
-    const bool zeros = a->mode == 0 && !q8 && a->w4->zeros;
-    if ((zeros || q8) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k))) return SPX_ERR_UNSUPPORTED;
-    if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k)) {
+    const bool zeros = a->mode == 0 && !gguf && a->w4->zeros;
+    const bool q2k = gguf && gguf_fmt(a->gguf) == kFmtQ2K;
+    if ((zeros || gguf) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k, q2k))) return SPX_ERR_UNSUPPORTED;
+    if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k, q2k)) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch
         // computes the logits first and the draft launch overlaps it.
@@ -341,8 +347,8 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
         rt.n_active = a->n_active;
         EngineParams p = base_params(a->x, T, H, a->ws);
         p.routed = routed;
-        p.routed_fmt = q8 ? kFmtQ8 : 0;
-        p.w4_zeros = q8 ? nullptr : static_cast<const uint8_t *>(a->w4->zeros);
+        p.routed_fmt = gguf ? gguf_fmt(a->gguf) : 0;
+        p.w4_zeros = gguf ? nullptr : static_cast<const uint8_t *>(a->w4->zeros);
         p.S = S;
         p.E = E;
         p.I = I;

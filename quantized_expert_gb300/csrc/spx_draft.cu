@@ -46,8 +46,12 @@ static_assert(kDkRdZeroOff % 16 == 0 && kDkRdZeroOff + kDkRdGroups * 64 <= kDkDa
 // GGUF Q8_0 experts: groups of 128 rows of 4352 bytes, three per routed item
 constexpr int kDkQ8Groups = 3;
 static_assert(kDkQ8Groups * kQ8GroupBytes <= kDkData, "Q8_0 items fit the stage");
-// draft expert formats (template argument of the launch)
-enum : int { DK_FMT_W4 = 0, DK_FMT_W4Z = 1, DK_FMT_Q8 = 2 };
+// GGUF Q2_K gate/up: super-blocks of 256 rows of 2688 bytes, four per routed item
+constexpr int kDkQ2kSbs = 4;
+static_assert(kDkQ2kSbs * kQ2kSbBytes <= kDkData, "Q2_K items fit the stage");
+// draft expert formats (template argument of the launch): INT4, INT4 with zero
+// points, GGUF Q8_0, and GGUF Q2_K gate/up with a Q8_0 down projection
+enum : int { DK_FMT_W4 = 0, DK_FMT_W4Z = 1, DK_FMT_Q8 = 2, DK_FMT_Q2K = 3 };
 constexpr int kDkSdSteps = 16;    // k-steps of I_s per SD item
 constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
 constexpr int kDkDBatch = 2;      // down items per queue unit
@@ -92,17 +96,19 @@ struct DkGeom {
     int rd_gpi, rd_nr;  // routed down: groups per item, ranges
 };
 
-// q8: GGUF Q8_0 experts (S = 16), whose groups are four times the INT4 size.
-__host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s, bool q8 = false) {
+// fmt: DK_FMT_*; the GGUF formats use S = 16, Q2_K gate/up items count
+// super-blocks of 256 rows instead of groups of 128.
+__host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s, int fmt = DK_FMT_W4) {
+    const bool q8dn = fmt == DK_FMT_Q8 || fmt == DK_FMT_Q2K;
     DkGeom g;
     g.sg_cols = I_s / 16;
     g.sg_nks = ((H / 16) % 16 == 0) ? 16 : 8;
     g.sg_nr = (H / 16) / g.sg_nks;
     g.sd_nr = (I_s / 16 + kDkSdSteps - 1) / kDkSdSteps;
     g.rg_blocks = I / S;
-    g.rg_gpi = q8 ? kDkQ8Groups : (S == 32 ? 4 : 8);
-    g.rg_nr = (H / 128 + g.rg_gpi - 1) / g.rg_gpi;
-    g.rd_gpi = q8 ? kDkQ8Groups : kDkRdGroups;
+    g.rg_gpi = fmt == DK_FMT_Q8 ? kDkQ8Groups : fmt == DK_FMT_Q2K ? kDkQ2kSbs : (S == 32 ? 4 : 8);
+    g.rg_nr = (H / (fmt == DK_FMT_Q2K ? 256 : 128) + g.rg_gpi - 1) / g.rg_gpi;
+    g.rd_gpi = q8dn ? kDkQ8Groups : kDkRdGroups;
     g.rd_nr = (I / 128 + g.rd_gpi - 1) / g.rd_gpi;
     return g;
 }
@@ -114,7 +120,7 @@ struct DkScratch {
 };
 __host__ __device__ inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I, int I_s, int nact_max) {
-    const DkGeom g = dk_geom(H, I, 16, I_s, true);  // the format with the most down ranges
+    const DkGeom g = dk_geom(H, I, 16, I_s, DK_FMT_Q8);  // the format with the most down ranges
     static_assert(kDkQ8Groups <= kDkRdGroups, "ready counts sized for the smallest down items");
     DkScratch s;
     size_t o = al256(base);
@@ -135,10 +141,11 @@ __host__ __device__ inline DkScratch dk_scratch(size_t base, int T, int H, int I
 // Shared memory.  One gate/up slot per ring stage: a column block holds at
 // least one stage until it completes, so slots never run out before stages.
 struct DkLayout {
-    int bars, hdrs, misc, gamma, act, sfree, scnt, pstate, pend, sacc, rids, rpw, rrank, rsv, stn, ste, sx, xs, ring,
-        stage, hs_off, total, xs_stride, slot_floats;
+    int bars, hdrs, misc, gamma, act, sfree, scnt, pstate, pend, sacc, rids, rpw, rrank, rsv, stn, ste, sx, sx16, xs,
+        ring, stage, hs_off, total, xs_stride, slot_floats;
 };
-__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E) {
+// q2k: room for the 16-row x sums of GGUF Q2_K gate/up items (hi, lo fp16).
+__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E, bool q2k = false) {
     DkLayout L;
     int o = 0;
     L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier
@@ -182,6 +189,9 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int 
     L.sx = o;  // [T][H/128] group sums of x (fp32)
     o += T * (H / 128) * 4;
     o = (o + 15) & ~15;
+    L.sx16 = o;  // Q2_K: [T][H/16] sums of x over 16 rows, fp16 hi, then fp16 lo
+    o += q2k ? T * (H / 16) * 4 : 0;
+    o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
     o += T * (H + 8) * 2;
@@ -197,7 +207,7 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int 
 
 struct DkParams {
     const uint8_t *w4;      // packed INT4 (or Q8_0) experts
-    int q8;                 // the experts are GGUF Q8_0 (S = 16)
+    int fmt;                // DK_FMT_* of the routed experts
     const __half *zeros_gu, *zeros_dn;  // nullable: per-group zero points (else 8), repacked
     size_t w4_colblk;       // byte offset of the column-block-major down weights
     int S;                  // INT4 slice width
@@ -287,7 +297,8 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     uint8_t *ring = smem + L.ring;
     const uint64_t pol = policy_evict_first();
     const int H = p.H, I = p.I, T = p.T;
-    const DkGeom g = dk_geom(H, I, p.S, p.I_s, p.q8 != 0);
+    const DkGeom g = dk_geom(H, I, p.S, p.I_s, p.fmt);
+    const bool q8dn = p.fmt == DK_FMT_Q8 || p.fmt == DK_FMT_Q2K;
     const int NQ = H / 32;
     const int nSGb = p.sh ? g.sg_cols : 0;
     const int nSD = p.sh ? NQ * g.sd_nr : 0;
@@ -399,9 +410,13 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             for (int r = 0; r < g.rg_nr; ++r) {
                 h.r = r;
                 h.k0 = r * g.rg_gpi;
-                h.n = min(g.rg_gpi, H / 128 - h.k0);
-                const size_t gb = p.q8 ? (size_t)kQ8GroupBytes : w4_group_bytes(p.S);
-                const size_t ub = p.q8 ? q8_unit_bytes(H) : w4_unit_bytes(H, p.S);
+                h.n = min(g.rg_gpi, H / (p.fmt == DK_FMT_Q2K ? 256 : 128) - h.k0);
+                const size_t gb = p.fmt == DK_FMT_Q8    ? (size_t)kQ8GroupBytes
+                                  : p.fmt == DK_FMT_Q2K ? (size_t)kQ2kSbBytes
+                                                        : w4_group_bytes(p.S);
+                const size_t ub = p.fmt == DK_FMT_Q8    ? q8_unit_bytes(H)
+                                  : p.fmt == DK_FMT_Q2K ? q2k_unit_bytes(H)
+                                                        : w4_unit_bytes(H, p.S);
                 const uint8_t *src = p.w4 + unit * ub + (size_t)h.k0 * gb;
                 // zero points (2S per group, as the scales) in the stage's h area, unused by these items
                 const __half *zs = p.zeros_gu ? p.zeros_gu + (unit * (H / 128) + h.k0) * 2 * p.S : nullptr;
@@ -439,7 +454,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                 if (h.e < 0 || h.e >= p.E) continue;  // unusable routing entry
                 h.k0 = h.r * g.rd_gpi;
                 h.n = min(g.rd_gpi, I / 128 - h.k0);
-                const uint32_t gb = p.q8 ? (uint32_t)kQ8GroupBytes : (uint32_t)kW4ColGroupBytes;
+                const uint32_t gb = q8dn ? (uint32_t)kQ8GroupBytes : (uint32_t)kW4ColGroupBytes;
                 const uint8_t *src = p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * gb;
                 const __half *zs =
                     p.zeros_dn ? p.zeros_dn + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * 32 : nullptr;
@@ -737,13 +752,15 @@ template <int MS, int FMT>
 __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     constexpr bool ZP = FMT == DK_FMT_W4Z;  // INT4 with per-group zero points
     constexpr bool Q8 = FMT == DK_FMT_Q8;   // GGUF Q8_0 (S = 16)
-    static_assert(!Q8 || MS == 1, "Q8_0 experts use 16-column slices");
+    constexpr bool Q2K = FMT == DK_FMT_Q2K; // GGUF Q2_K gate/up, Q8_0 down (S = 16)
+    constexpr bool Q8DN = Q8 || Q2K;        // Q8_0 down items
+    static_assert(!(Q8 || Q2K) || MS == 1, "GGUF experts use 16-column slices");
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
     griddep_launch_dependents();
     const int nst = p.nstages;
-    const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E);
+    const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E, Q2K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -797,7 +814,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int H = p.H, I = p.I, T = p.T, xstr = L.xs_stride;
     const int ctid = threadIdx.x;
-    const DkGeom geo = dk_geom(H, I, p.S, p.I_s, Q8);
+    const DkGeom geo = dk_geom(H, I, p.S, p.I_s, FMT);
     griddep_wait();  // x, the logits and the workspace may come from the preceding launch
     // one token over at most 64 experts: every consumer warp ranks a share
     const bool sel_all = p.logits && T == 1 && p.E <= 8 * kDkCons && p.E <= 64 && p.k <= 32;
@@ -819,6 +836,15 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             for (int q = 0; q < 4; ++q) {
                 const float2 f = __half22float2(vh[q]);
                 sum += f.x + f.y;
+            }
+        }
+        if constexpr (Q2K) {  // sums over 16 rows (this lane's chunk and its pair's), as an fp16 pair hi + lo
+            const float s16 = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
+            if ((lane & 1) == 0 && idx < T * (H / 8)) {
+                __half *sxh = reinterpret_cast<__half *>(smem + L.sx16);
+                const __half hi = __float2half_rn(s16);
+                sxh[idx / 2] = hi;  // [t][16-row block]: idx/2 = t*(H/16) + block
+                sxh[T * (H / 16) + idx / 2] = __float2half_rn(s16 - __half2float(hi));
             }
         }
 #pragma unroll
@@ -1091,6 +1117,78 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                         }
                     }
                 }
+            } else if constexpr (Q2K) {
+                // GGUF Q2_K: super-blocks of 256 rows = 16 k-steps; k-step b is
+                // sub-block b of every row, with its own 4-bit scale sc and min m.
+                // The fragment holds sc*q (exact in fp16: one fused multiply-add
+                // of the magic value 1024 + q), so one accumulator spans the
+                // super-block; the mins enter through one more product, of the
+                // rows' 16 mins with the token's 16 sub-block sums of x (those
+                // split into an fp16 pair hi + lo).  Then d and dmin per row.
+                const __half *sxh = reinterpret_cast<const __half *>(smem + L.sx16) + tok * (H / 16);
+                const __half *sxl = sxh + T * (H / 16);
+                const __half2 k1024 = u32_as_h2(0x64006400u), km1024 = u32_as_h2(0xE400E400u);
+                for (int gr = 0; gr < h.n; ++gr) {
+                    const uint8_t *sp = stage + (size_t)gr * kQ2kSbBytes;
+                    const __half *dd = reinterpret_cast<const __half *>(sp);  // d [32], then dmin [32]
+                    const int sbg = h.k0 + gr;                                // super-block of H
+                    const uint4 c0 = lds128(sp + kQ2kScaleOff + g * 32);
+                    const uint4 c1 = lds128(sp + kQ2kScaleOff + g * 32 + 16);
+                    const uint32_t scw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    float am[NTW][4] = {}, an[NTW][4] = {};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = lds128(sp + kQ2kCodeOff + c * 512 + lane * 16);
+                        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int kl = 4 * c + kk;
+                            const int ks = sbg * 16 + kl;
+                            const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
+                            const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
+                            const uint32_t su = scw[kl >> 1] >> (16 * (kl & 1));  // nibbles: (t, row g / g+8)
+#pragma unroll
+                            for (int t = 0; t < NTW; ++t) {
+                                const uint32_t na = (su >> (8 * t)) & 15u, nb = (su >> (8 * t + 4)) & 15u;
+                                const __half2 sa2 = __hsub2(u32_as_h2((na * 0x10001u) | 0x64006400u), k1024);
+                                const __half2 sb2 = __hsub2(u32_as_h2((nb * 0x10001u) | 0x64006400u), k1024);
+                                const __half2 oa2 = __hmul2(sa2, km1024), ob2 = __hmul2(sb2, km1024);
+                                uint32_t a[4];
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) {
+                                    const uint32_t raw =
+                                        lop3_and_or(words[kk] >> (2 * (4 * t + r)), 0x00030003u, 0x64006400u);
+                                    a[r] = h2_as_u32(__hfma2(u32_as_h2(raw), (r & 1) ? sb2 : sa2, (r & 1) ? ob2 : oa2));
+                                }
+                                mma_16816(am[t], a, b0, b1);
+                            }
+                        }
+                    }
+                    const uint32_t bh0 = okx ? lds32(sxh + sbg * 16 + 2 * q4) : 0u;
+                    const uint32_t bh1 = okx ? lds32(sxh + sbg * 16 + 2 * q4 + 8) : 0u;
+                    const uint32_t bl0 = okx ? lds32(sxl + sbg * 16 + 2 * q4) : 0u;
+                    const uint32_t bl1 = okx ? lds32(sxl + sbg * 16 + 2 * q4 + 8) : 0u;
+                    const uint2 mw = lds64(sp + kQ2kMinOff + lane * 8);
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const uint32_t w = t == 0 ? mw.x : mw.y;
+                        uint32_t a[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            a[r] = h2_as_u32(__hsub2(u32_as_h2(lop3_and_or(w >> (4 * r), 0x000F000Fu, 0x64006400u)), k1024));
+                        mma_16816(an[t], a, bh0, bh1);
+                        mma_16816(an[t], a, bl0, bl1);
+                    }
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const float da = __half2float(dd[t * 16 + g]), db = __half2float(dd[t * 16 + g + 8]);
+                        const float ma = __half2float(dd[32 + t * 16 + g]), mb = __half2float(dd[32 + t * 16 + g + 8]);
+                        run[t][0] += da * am[t][0] - ma * an[t][0];
+                        run[t][1] += da * am[t][1] - ma * an[t][1];
+                        run[t][2] += db * am[t][2] - mb * an[t][2];
+                        run[t][3] += db * am[t][3] - mb * an[t][3];
+                    }
+                }
             } else {
                 // Raw codes into the mma: rows m < 8 of a tile get 1024 + q, rows m >= 8
                 // get 1024 + 16 q (the magic-exponent fragments without their fix-up).
@@ -1221,7 +1319,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             const int n_e = min(max(stn[h.a], 0), T);
             const bool okb = g < n_e;
             float run[2][4] = {};
-            if constexpr (Q8) {
+            if constexpr (Q8DN) {
                 // GGUF Q8_0, as the gate/up items: four 32-row blocks per group
                 for (int gr = 0; gr < h.n; ++gr) {
                     const uint8_t *gp = stage + (size_t)gr * kQ8GroupBytes;
@@ -1384,22 +1482,30 @@ size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max
     return dk_scratch(base, T, H, I, I_s, nact_max).end;
 }
 
-bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k) {
+bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k, bool q2k) {
+    if (q2k && (H % 256 || S != 16)) return false;
     if (T < 1 || T > 8 || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
     if (I_s % 16 || E < 1 || k < 1 || E > kMaxE || T * k > kMaxSlots) return false;
-    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E).total <= kSmemLimit;
+    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E, q2k).total <= kSmemLimit;
 }
 
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
     DkParams p{};
     p.w4 = e.routed;
-    p.q8 = e.routed_fmt == kFmtQ8 ? 1 : 0;
+    const bool zp = e.w4_zeros != nullptr;
+    p.fmt = e.routed_fmt == kFmtQ8    ? DK_FMT_Q8
+            : e.routed_fmt == kFmtQ2K ? DK_FMT_Q2K
+            : zp                      ? DK_FMT_W4Z
+                                      : DK_FMT_W4;
+    const bool q2k = p.fmt == DK_FMT_Q2K;
     if (e.w4_zeros) {
         p.zeros_gu = reinterpret_cast<const __half *>(e.w4_zeros);
         p.zeros_dn = reinterpret_cast<const __half *>(e.w4_zeros + w4_zeros_gu_bytes(e.E, e.H, e.I, e.S));
     }
     p.S = e.S;
-    p.w4_colblk = p.q8 ? q8_units_bytes(e.E, e.H, e.I) : w4_colblk_offset(e.E, e.H, e.I, e.S);
+    p.w4_colblk = p.fmt == DK_FMT_Q8    ? q8_units_bytes(e.E, e.H, e.I)
+                  : p.fmt == DK_FMT_Q2K ? q2k_units_bytes(e.E, e.H, e.I)
+                                        : w4_colblk_offset(e.E, e.H, e.I, e.S);
     p.sh = e.shared;
     p.w_sgate = e.w_sgate;
     p.I_s = e.shared ? e.I_s : 0;
@@ -1439,23 +1545,25 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.rdy_s = reinterpret_cast<int *>(ws + sc.rdy_s);
     p.rdy_r = reinterpret_cast<int *>(ws + sc.rdy_r);
     int nst = 12;  // <= kDkMaxStages
-    DkLayout L = dk_layout(e.T, e.H, nst, e.k, p.nact_max, e.E);
-    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E);
+    DkLayout L = dk_layout(e.T, e.H, nst, e.k, p.nact_max, e.E, q2k);
+    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E, q2k);
     if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
     p.nstages = nst;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    static int configured[5][64] = {};
+    static int configured[6][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
     const int ms = e.S / 16;
-    const bool zp = p.zeros_gu != nullptr;
-    if (p.q8 && (ms != 1 || zp)) return SPX_ERR_UNSUPPORTED;
+    const bool gguf = p.fmt == DK_FMT_Q8 || p.fmt == DK_FMT_Q2K;
+    if (gguf && (ms != 1 || zp)) return SPX_ERR_UNSUPPORTED;
+    if (q2k && e.H % 256) return SPX_ERR_UNSUPPORTED;
     void (*kern)(const DkParams) =
-        p.q8 ? draft_kernel<1, DK_FMT_Q8>
-             : ms == 2 ? (zp ? draft_kernel<2, DK_FMT_W4Z> : draft_kernel<2, DK_FMT_W4>)
-                       : (zp ? draft_kernel<1, DK_FMT_W4Z> : draft_kernel<1, DK_FMT_W4>);
-    const int ki = p.q8 ? 4 : (ms - 1) * 2 + (zp ? 1 : 0);
+        p.fmt == DK_FMT_Q8    ? draft_kernel<1, DK_FMT_Q8>
+        : p.fmt == DK_FMT_Q2K ? draft_kernel<1, DK_FMT_Q2K>
+        : ms == 2             ? (zp ? draft_kernel<2, DK_FMT_W4Z> : draft_kernel<2, DK_FMT_W4>)
+                              : (zp ? draft_kernel<1, DK_FMT_W4Z> : draft_kernel<1, DK_FMT_W4>);
+    const int ki = p.fmt == DK_FMT_Q8 ? 4 : p.fmt == DK_FMT_Q2K ? 5 : (ms - 1) * 2 + (zp ? 1 : 0);
     if (!configured[ki][dev]) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (err != cudaSuccess) return record_launch(err);

@@ -81,6 +81,26 @@ __host__ __device__ inline size_t q8_units_bytes(int E, int H, int I) { return (
 __host__ __device__ inline size_t q8_packed_bytes(int E, int H, int I) {
     return q8_units_bytes(E, H, I) + (size_t)E * (H / 32) * (I / 128) * kQ8GroupBytes;
 }
+// GGUF Q2_K gate/up (draft launch only; S = 16; H a multiple of 256), one
+// super-block of 256 rows of a slice's two tiles (gate, up) in 2688 bytes:
+//   d [32] fp16, dmin [32] fp16 (tile-row order t*16 + m);
+//   sub-block scales [g 0..7][k-step 0..15] u16, nibble j = (tile j/2, row
+//     g + 8*(j%2)) at bits 4j;
+//   mins [lane][tile] u32 in A-fragment order (k = sub-block): nibble of
+//     register r, half h at bits 16h + 4r;
+//   codes: 4 blocks of 512 B, each 4 k-steps (32 lanes x 16 B; lane word =
+//     one k-step, code of tile t, register r, half h at bits 16h + 2(4t + r)).
+// Gate/up units [E][I/16] of H/256 super-blocks, then the down projection in
+// the Q8_0 column-block-major layout.
+constexpr int kQ2kScaleOff = 128;
+constexpr int kQ2kMinOff = kQ2kScaleOff + 8 * 16 * 2;
+constexpr int kQ2kCodeOff = kQ2kMinOff + 32 * 2 * 4;
+constexpr int kQ2kSbBytes = kQ2kCodeOff + 4 * 512;
+static_assert(kQ2kSbBytes == 2688, "Q2_K super-block of a slice: 2.625 bits per weight");
+__host__ __device__ inline size_t q2k_unit_bytes(int H) { return (size_t)(H / 256) * kQ2kSbBytes; }
+__host__ __device__ inline size_t q2k_units_bytes(int E, int H, int I) {
+    return (size_t)E * (I / 16) * q2k_unit_bytes(H);
+}
 __host__ __device__ inline size_t w4_colblk_offset(int E, int H, int I, int S) {
     return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
 }
@@ -231,6 +251,11 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
                  : "r"(smem_u32(p)));
     return v;
 }
+__device__ __forceinline__ uint2 lds64(const void *p) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+    return v;
+}
 __device__ __forceinline__ uint32_t lds32(const void *p) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
@@ -313,13 +338,14 @@ struct RouteParams {
     WsHeader *hdr;
 };
 
-constexpr int kFmtQ8 = 2;  // EngineParams::routed_fmt of GGUF Q8_0 experts
+constexpr int kFmtQ8 = 2;   // EngineParams::routed_fmt of GGUF Q8_0 experts
+constexpr int kFmtQ2K = 3;  // ... of GGUF Q2_K gate/up with Q8_0 down
 struct EngineParams {
     // routed experts (packed units)
     const uint8_t *routed;
     const __half *w4_sdown;  // INT4: down scales [E][I/128][H]
     const uint8_t *w4_zeros; // INT4, nullable: repacked per-group zero points (else 8)
-    int routed_fmt;          // 0 INT4, 1 FP16, kFmtQ8 GGUF Q8_0 (draft launch only)
+    int routed_fmt;          // 0 INT4, 1 FP16, kFmtQ8 / kFmtQ2K GGUF (draft launch only)
     int S;                   // routed slice width (INT4: 16/32; FP16: 16)
     int E, I, k;
     int routed_enabled;
@@ -364,7 +390,7 @@ struct DraftRouting {
     int layer;
     int32_t *counts, *offsets, *sorted_slots, *active, *n_active;
 };
-bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1);
+bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1, bool q2k = false);
 size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max);
 // rt == nullptr: routing from e.active / e.n_active and the token tables e.tables.
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s);

@@ -50,7 +50,7 @@ using namespace spx;
 extern "C" int spx_moe_layer_noalloc(const spx_layer_args *args, spx_stream_t stream) {
     if (!args) return SPX_ERR_INVALID_ARG;
     const int I = args->mode != 0 ? (args->f16 ? args->f16->I : 0)
-                                  : args->q8 ? args->q8->I : (args->w4 ? args->w4->I : 0);
+                                  : args->gguf ? args->gguf->I : (args->w4 ? args->w4->I : 0);
     const int I_s = args->shared ? args->shared->I_s : 0;
     const size_t need = spx_workspace_size(args->T, args->H, I, args->E, args->k, I_s);
     if (need == 0) return SPX_ERR_UNSUPPORTED;

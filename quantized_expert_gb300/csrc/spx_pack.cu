@@ -327,6 +327,83 @@ __global__ void q8_pack_dn(const uint8_t *wd, int E, int H, int I, uint8_t *regi
     }
 }
 
+// ---------------------------------------------------------- GGUF Q2_K --
+// Canonical Q2_K matrix [out N][in K]: per row, K/256 super-blocks of 84
+// bytes (16 sub-block bytes: scale low nibble, min high nibble; 64 code bytes;
+// fp16 d; fp16 dmin).  Code of value wi (0..255) of a super-block:
+__device__ __forceinline__ const uint8_t *q2k_block(const uint8_t *w, int K, size_t e, int N, int n, int sb) {
+    return w + ((e * N + n) * (K / 256) + sb) * 84;
+}
+__device__ __forceinline__ uint32_t q2k_code(const uint8_t *blk, int wi) {
+    return (blk[16 + 32 * (wi / 128) + wi % 32] >> (2 * ((wi % 128) / 32))) & 3u;
+}
+
+// Gate/up units: codes, one thread per (unit, super-block, code block, lane,
+// k-step word); then d/dmin, sub-block scale words and min words.
+__global__ void q2k_pack_gu(const uint8_t *wg, const uint8_t *wu, int E, int H, int I, uint8_t *packed) {
+    const int spe = I / 16, NS = H / 256;
+    const size_t npair = (size_t)E * spe * NS;
+    const size_t ub = q2k_unit_bytes(H);
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < npair * 512;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int kk = (int)(idx & 3);
+        const int lane = (int)((idx >> 2) & 31);
+        const int c = (int)((idx >> 7) & 3);
+        const size_t us = idx >> 9;  // unit * NS + super-block
+        const int sb = (int)(us % NS);
+        const size_t unit = us / NS;
+        const size_t e = unit / spe;
+        const int jj = (int)(unit % spe);
+        uint32_t word = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint8_t *blk = q2k_block(t ? wu : wg, H, e, I, jj * 16 + frag_row(lane, r), sb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    word |= q2k_code(blk, 16 * (4 * c + kk) + frag_col(lane, r, h)) << (16 * h + 2 * (4 * t + r));
+            }
+        }
+        *reinterpret_cast<uint32_t *>(packed + unit * ub + (size_t)sb * kQ2kSbBytes + kQ2kCodeOff + c * 512 +
+                                      lane * 16 + kk * 4) = word;
+    }
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < npair * 224;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int item = (int)(idx % 224);
+        const size_t us = idx / 224;
+        const int sb = (int)(us % NS);
+        const size_t unit = us / NS;
+        const size_t e = unit / spe;
+        const int jj = (int)(unit % spe);
+        uint8_t *base = packed + unit * ub + (size_t)sb * kQ2kSbBytes;
+        if (item < 32) {  // d and dmin of tile item/16, row item%16
+            const uint8_t *blk = q2k_block(item < 16 ? wg : wu, H, e, I, jj * 16 + item % 16, sb);
+            reinterpret_cast<uint16_t *>(base)[item] = (uint16_t)(blk[80] | (blk[81] << 8));
+            reinterpret_cast<uint16_t *>(base)[32 + item] = (uint16_t)(blk[82] | (blk[83] << 8));
+        } else if (item < 160) {  // scale nibbles of (g, k-step)
+            const int g = (item - 32) / 16, ks = (item - 32) % 16;
+            uint32_t u = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t *blk = q2k_block(j >> 1 ? wu : wg, H, e, I, jj * 16 + g + 8 * (j & 1), sb);
+                u |= (uint32_t)(blk[ks] & 15) << (4 * j);
+            }
+            reinterpret_cast<uint16_t *>(base + kQ2kScaleOff)[g * 16 + ks] = (uint16_t)u;
+        } else {  // min nibbles of (lane, tile) in A-fragment order
+            const int lane = (item - 160) / 2, t = (item - 160) % 2;
+            uint32_t w = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint8_t *blk = q2k_block(t ? wu : wg, H, e, I, jj * 16 + frag_row(lane, r), sb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) w |= (uint32_t)(blk[frag_col(lane, r, h)] >> 4) << (16 * h + 4 * r);
+            }
+            reinterpret_cast<uint32_t *>(base + kQ2kMinOff)[lane * 2 + t] = w;
+        }
+    }
+}
+
 }  // namespace spx
 
 using namespace spx;
@@ -372,22 +449,33 @@ extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, con
     return record_launch(cudaGetLastError());
 }
 
-extern "C" size_t spx_q8_packed_bytes(int E, int H, int I) {
+extern "C" size_t spx_gguf_packed_bytes(int E, int H, int I, int gate_up_type) {
     if (E < 1 || H < 128 || I < 128 || H % 128 || I % 128) return 0;
-    return q8_packed_bytes(E, H, I);
+    if (gate_up_type == SPX_GGUF_Q8_0) return q8_packed_bytes(E, H, I);
+    if (gate_up_type == SPX_GGUF_Q2_K && H % 256 == 0)
+        return q2k_units_bytes(E, H, I) + (q8_packed_bytes(E, H, I) - q8_units_bytes(E, H, I));
+    return 0;
 }
 
-extern "C" int spx_q8_repack(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int E, int H, int I,
-                             void *packed, spx_stream_t stream) {
+extern "C" int spx_gguf_repack(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, int E, int H, int I,
+                               int gate_up_type, void *packed, spx_stream_t stream) {
     if (!w_gate || !w_up || !w_down || !packed) return SPX_ERR_INVALID_ARG;
     if (E < 1 || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
+    if (gate_up_type != SPX_GGUF_Q8_0 && gate_up_type != SPX_GGUF_Q2_K) return SPX_ERR_INVALID_ARG;
     if (H % 128 || I % 128 || H > kMaxH || E > kMaxE) return SPX_ERR_UNSUPPORTED;
+    if (gate_up_type == SPX_GGUF_Q2_K && H % 256) return SPX_ERR_UNSUPPORTED;
     if (!aligned16(packed)) return SPX_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *out = static_cast<uint8_t *>(packed);
-    q8_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 128) * 512), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
-    q8_pack_dn<<<grid_for((size_t)E * (H / 32) * (I / 128) * 512), 256, 0, s>>>(w_down, E, H, I,
-                                                                                out + q8_units_bytes(E, H, I));
+    size_t units;
+    if (gate_up_type == SPX_GGUF_Q8_0) {
+        q8_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 128) * 512), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
+        units = q8_units_bytes(E, H, I);
+    } else {
+        q2k_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 256) * 512), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
+        units = q2k_units_bytes(E, H, I);
+    }
+    q8_pack_dn<<<grid_for((size_t)E * (H / 32) * (I / 128) * 512), 256, 0, s>>>(w_down, E, H, I, out + units);
     return record_launch(cudaGetLastError());
 }
 

@@ -36,8 +36,8 @@ class F16Experts(C.Structure):
     _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int)]
 
 
-class Q8Experts(C.Structure):
-    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int)]
+class GgufExperts(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int), ("gate_up_type", C.c_int)]
 
 
 class Shared(C.Structure):
@@ -54,7 +54,7 @@ class LayerArgs(C.Structure):
                 ("n_active", C.c_void_p), ("out", C.c_void_p), ("ws", C.c_void_p), ("ws_bytes", C.c_size_t),
                 ("ev_experts_begin", C.c_void_p), ("ev_experts_end", C.c_void_p),
                 ("resident", C.c_void_p), ("ready", C.c_void_p), ("wait_budget_ns", C.c_uint64),
-                ("q8", C.POINTER(Q8Experts))]
+                ("gguf", C.POINTER(GgufExperts))]
 
 
 _SIGS = {
@@ -72,8 +72,8 @@ _SIGS = {
     "spx_f16_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "spx_w4_repack": (C.c_int, [C.c_void_p] * 6 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_w4_zeros_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
-    "spx_q8_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
-    "spx_q8_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
+    "spx_gguf_packed_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+    "spx_gguf_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_w4_zeros_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_f16_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_workspace_size": (C.c_size_t, [C.c_int] * 6),
@@ -83,7 +83,7 @@ _SIGS = {
     "spx_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p]),
     "spx_moe_draft_w4a16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(W4Experts), C.c_int] + [C.c_void_p] * 5 +
                             [C.c_void_p, C.c_size_t, C.c_void_p]),
-    "spx_moe_draft_q8a16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(Q8Experts), C.c_int] + [C.c_void_p] * 5 +
+    "spx_moe_draft_gguf": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(GgufExperts), C.c_int] + [C.c_void_p] * 5 +
                             [C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_moe_verify_fp16": (C.c_int, [C.c_void_p, C.c_int, C.POINTER(F16Experts), C.c_int] + [C.c_void_p] * 5 +
                             [C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -217,15 +217,19 @@ class PackedW4:
         return W4Experts(self.buf.data_ptr(), self.E, self.H, self.I, self.S, _p(self.zeros))
 
 
+SPX_GGUF_Q8_0, SPX_GGUF_Q2_K = 0, 1
+
+
 @dataclass
-class PackedQ8:
+class PackedGguf:
     buf: torch.Tensor
     E: int
     H: int
     I: int
+    gate_up_type: int  # SPX_GGUF_Q8_0 or SPX_GGUF_Q2_K; down is Q8_0
 
-    def cstruct(self) -> Q8Experts:
-        return Q8Experts(self.buf.data_ptr(), self.E, self.H, self.I)
+    def cstruct(self) -> GgufExperts:
+        return GgufExperts(self.buf.data_ptr(), self.E, self.H, self.I, self.gate_up_type)
 
 
 @dataclass
@@ -275,17 +279,19 @@ def spx_w4_zeros_repack(w4: PackedW4, qz_gate, qz_up, qz_down, stream=None) -> P
     return PackedW4(w4.buf, w4.E, w4.H, w4.I, w4.S, buf)
 
 
-def spx_q8_repack(w_gate, w_up, w_down, stream=None) -> PackedQ8:
-    """Canonical GGUF Q8_0 experts (uint8 gate, up [E][I][H/32][34], down
-    [E][H][I/32][34]) -> packed for the draft launch."""
-    E, I, hb, _ = w_gate.shape
-    H = hb * 32
-    n = load().spx_q8_packed_bytes(E, H, I)
+def spx_gguf_repack(w_gate, w_up, w_down, gate_up_type=SPX_GGUF_Q8_0, stream=None) -> PackedGguf:
+    """Canonical GGUF experts -> packed for the draft launch: gate, up uint8
+    [E][I][H/32][34] (Q8_0) or [E][I][H/256][84] (Q2_K); down [E][H][I/32][34]
+    (Q8_0)."""
+    E, I, nb, bb = w_gate.shape
+    H = nb * (32 if gate_up_type == SPX_GGUF_Q8_0 else 256)
+    n = load().spx_gguf_packed_bytes(E, H, I, gate_up_type)
     if n == 0:
-        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_q8_packed_bytes")
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_gguf_packed_bytes")
     buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
-    _chk(load().spx_q8_repack(_p(w_gate), _p(w_up), _p(w_down), E, H, I, _p(buf), _stream(stream)), "spx_q8_repack")
-    return PackedQ8(buf, E, H, I)
+    _chk(load().spx_gguf_repack(_p(w_gate), _p(w_up), _p(w_down), E, H, I, gate_up_type, _p(buf), _stream(stream)),
+         "spx_gguf_repack")
+    return PackedGguf(buf, E, H, I, gate_up_type)
 
 
 def spx_f16_repack(w_gate, w_up, w_down, stream=None) -> PackedF16:
@@ -319,12 +325,12 @@ def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_acti
          "spx_moe_draft_w4a16")
 
 
-def spx_moe_draft_q8a16(x, w: PackedQ8, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+def spx_moe_draft_gguf(x, w: PackedGguf, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
     T = x.shape[0]
     cs = w.cstruct()
-    _chk(load().spx_moe_draft_q8a16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
-                                    _p(n_active), _p(y_sorted), _p(ws), ws.numel(), _stream(stream)),
-         "spx_moe_draft_q8a16")
+    _chk(load().spx_moe_draft_gguf(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
+                                   _p(n_active), _p(y_sorted), _p(ws), ws.numel(), _stream(stream)),
+         "spx_moe_draft_gguf")
 
 
 def spx_moe_verify_fp16(x, w: PackedF16, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
@@ -362,9 +368,9 @@ class Routing:
 
 def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: PackedW4 | None = None,
                f16: PackedF16 | None = None, shared: PackedShared | None = None, w_router=None, elb=None,
-               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0, q8: PackedQ8 | None = None):
+               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0, gguf: PackedGguf | None = None):
     """Build (and keep alive) the argument block of one spx_moe_layer call.
-    Draft experts are INT4 (w4) or GGUF Q8_0 (q8), one of the two.
+    Draft experts are INT4 (w4) or GGUF (gguf), one of the two.
     resident (uint8 [E]) and ready (int32/uint32 [E]) are the optional
     cache-aware expert order and ready flags; wait_budget_ns bounds every
     device-side wait (0 = the library default)."""
@@ -377,10 +383,10 @@ def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: Pac
         s4 = w4.cstruct()
         keep.append(s4)
         a.w4 = C.pointer(s4)
-    if q8 is not None:
-        s8 = q8.cstruct()
-        keep.append(s8)
-        a.q8 = C.pointer(s8)
+    if gguf is not None:
+        sg = gguf.cstruct()
+        keep.append(sg)
+        a.gguf = C.pointer(sg)
     if f16 is not None:
         s16 = f16.cstruct()
         keep.append(s16)

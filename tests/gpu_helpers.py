@@ -50,16 +50,17 @@ class Layer:
     others are zero on the device (the kernels never read them)."""
 
     def __init__(self, shape: W.LayerShape, layer: int = 0, needed=None, draft=True, verify=True, slice_cols=32,
-                 zeros=False, q8=False):
+                 zeros=False, gguf=None):
         self.shape = s = shape
         self.layer = layer
         needed = sorted(set(range(s.E) if needed is None else needed))
         self.needed = needed
         self.w4_host = {e: W.gen_w4_expert(s, layer, e) for e in needed} if (draft or s.verify_is_dequant) else {}
-        self.q8 = None
-        if q8:  # GGUF Q8_0 draft experts instead of INT4
+        self.gguf = None
+        if gguf:  # GGUF draft experts instead of INT4: "q8_0", or "q2_k" gate/up with a Q8_0 down
             assert draft and not zeros and not (verify and s.verify_is_dequant)
-            self.w4_host = {e: W.gen_q8_expert(s, layer, e) for e in needed}
+            gen = W.gen_q8_expert if gguf == "q8_0" else W.gen_q2k_expert
+            self.w4_host = {e: gen(s, layer, e) for e in needed}
         self.zeros = zeros
         if zeros:  # asymmetric INT4: per-group zero points on every draft expert
             assert draft and not (verify and s.verify_is_dequant)
@@ -73,8 +74,8 @@ class Layer:
         self.shared_host = W.gen_shared(s, layer)
         self.router_host = W.gen_router(s, layer) if s.logits == "router" else None
         self.w4 = self.f16 = self.shared = None
-        if draft and q8:
-            self.q8 = self._pack_q8()
+        if draft and gguf:
+            self.gguf = self._pack_gguf(gguf)
         elif draft:
             self.w4 = self._pack_w4(slice_cols)
         if verify:
@@ -109,15 +110,17 @@ class Layer:
         torch.cuda.synchronize()
         return p
 
-    def _pack_q8(self):
+    def _pack_gguf(self, kind):
         s = self.shape
         E, H, I = s.E, s.H, s.I
-        wg = np.zeros((E, I, H // 32, 34), np.uint8)
+        q2 = kind == "q2_k"
+        wg = np.zeros((E, I, H // 256, 84) if q2 else (E, I, H // 32, 34), np.uint8)
         wu = np.zeros_like(wg)
         wd = np.zeros((E, H, I // 32, 34), np.uint8)
+        pre = "q2k_" if q2 else "q8_"
         for e, ex in self.w4_host.items():
-            wg[e], wu[e], wd[e] = ex["q8_gate"], ex["q8_up"], ex["q8_down"]
-        p = spx.spx_q8_repack(dev(wg), dev(wu), dev(wd))
+            wg[e], wu[e], wd[e] = ex[pre + "gate"], ex[pre + "up"], ex["q8_down"]
+        p = spx.spx_gguf_repack(dev(wg), dev(wu), dev(wd), spx.SPX_GGUF_Q2_K if q2 else spx.SPX_GGUF_Q8_0)
         torch.cuda.synchronize()
         return p
 

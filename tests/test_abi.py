@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_sizes_and_strings(lib):
     from quantized_expert_gb300 import spx
-    assert spx.spx_version() == 103
+    assert spx.spx_version() == 104
     assert spx.status_string(0) == "ok"
     assert "timed out" in spx.status_string(-5)
     # INT4 unit = 49*H*S/32 bytes; down scales copied once per expert
@@ -87,7 +87,7 @@ def test_header_is_plain_c():
 
 @pytest.mark.parametrize("cname,pyname", [("spx_layer_args", "LayerArgs"), ("spx_w4_experts", "W4Experts"),
                                            ("spx_f16_experts", "F16Experts"), ("spx_shared", "Shared"),
-                                           ("spx_q8_experts", "Q8Experts")])
+                                           ("spx_gguf_experts", "GgufExperts")])
 def test_struct_layouts_match_the_header(tmp_path, cname, pyname):
     """The binding's argument structs mirror the C structs: a program compiled
     against include/spx.h reports each one's size and field offsets."""

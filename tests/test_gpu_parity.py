@@ -260,7 +260,7 @@ def _run_layer(lay, mode, x, logits, elb=None):
         T, s.E, dtype=torch.float32, device="cuda")
     args, keep = spx.layer_args(0 if mode == "draft" else 1, gh.dev_f16(x), s.E, s.k, s.renorm, d_lg, routing, out,
                                 ws, w4=lay.w4, f16=lay.f16, shared=lay.shared, w_router=lay.w_router, elb=elb,
-                                layer=lay.layer, q8=lay.q8)
+                                layer=lay.layer, gguf=lay.gguf)
     outs = []
     for rep in range(2):
         spx.spx_moe_layer(args, None)
@@ -638,66 +638,70 @@ def test_zero_points_unsupported_outside_the_draft_launch():
     assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
 
 
-# ----------------------------------------------------- GGUF Q8_0 drafts
+# ------------------------------------------------------------- GGUF drafts
+@pytest.mark.parametrize("kind", ["q8_0", "q2_k"])
 @pytest.mark.parametrize("name,T", [("deepseek_v2_lite", 1), ("deepseek_v2_lite", 8), ("qwen15_moe", 1),
                                     ("phi35_moe", 1)])
-def test_q8_draft_layer_full_size(name, T):
-    """GGUF Q8_0 draft experts (fp16 scale per 32 weights, int8 codes) at
-    full size through spx_moe_layer: routing bit-exact, output within
-    tolerance of the oracle."""
+def test_gguf_draft_layer_full_size(name, T, kind):
+    """GGUF draft experts at full size through spx_moe_layer: Q8_0 (fp16
+    scale per 32 weights, int8 codes), or Q2_K gate/up (super-blocks of 256
+    with 4-bit sub-block scales and mins, 2-bit codes) with a Q8_0 down
+    projection: routing bit-exact, output within tolerance of the oracle."""
     gh = _gh()
     s = W.CONFIGS[name]
     x = W.gen_x(s, T, step=100 + T)
     logits = None if s.logits == "router" else W.gen_logits(s, T, step=100 + T)
     need = gh.needed_experts(s, [logits], [x])
-    lay = gh.Layer(s, needed=need, verify=False, q8=True)
+    lay = gh.Layer(s, needed=need, verify=False, gguf=kind)
     ref = lay.oracle_layer("draft", x, logits=logits)
     outs, routing, _ = _run_layer(lay, "draft", x, logits)
     assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
     g = ref["gather"]
     assert np.array_equal(routing.sorted_slots.cpu().numpy(), g["sorted_slots"])
     for rep, o in enumerate(outs):
-        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"q8 {name} T={T} rep {rep}")
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{kind} {name} T={T} rep {rep}")
 
 
+@pytest.mark.parametrize("kind", ["q8_0", "q2_k"])
 @pytest.mark.parametrize("case", [1, 2, 4])
-def test_q8_draft_unit_call(case):
-    """spx_moe_draft_q8a16 on the small cases of at most 8 tokens with
+def test_gguf_draft_unit_call(case, kind):
+    """spx_moe_draft_gguf on the small cases of at most 8 tokens with
     16-column slices: per-slot expert outputs against the oracle."""
     spx, gh = _spx(), _gh()
     s, T, S = SMALL_CASES[case]
     x = W.gen_x(s, T, step=110 + case)
     lg = np.random.default_rng(110 + case).standard_normal((T, s.E))
     ids, w = oracle.route_topk(lg, s.k, s.renorm)
-    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), verify=False, q8=True)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), verify=False, gguf=kind)
     g, r = _routing_dev(ids, s.E)
     ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
-    y_ref = np.stack([oracle.swiglu_q8(x[int(sl) // s.k], lay.w4_host[int(ids.reshape(-1)[sl])])
+    y_ref = np.stack([oracle.swiglu_draft(x[int(sl) // s.k], lay.w4_host[int(ids.reshape(-1)[sl])])
                       for sl in g["sorted_slots"]])
     y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
     for rep in range(2):
-        spx.spx_moe_draft_q8a16(gh.dev_f16(x), lay.q8, s.k, r["offsets"], r["sorted_slots"], r["active"],
-                                r["n_active"], y, ws)
+        spx.spx_moe_draft_gguf(gh.dev_f16(x), lay.gguf, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                               r["n_active"], y, ws)
         torch.cuda.synchronize()
-        gh.check_close(y.cpu().numpy(), y_ref, f"q8 case {case} rep {rep}")
+        gh.check_close(y.cpu().numpy(), y_ref, f"{kind} case {case} rep {rep}")
     assert spx.spx_workspace_status(ws) == 0
 
 
-def test_q8_unsupported_and_invalid_calls():
-    """Q8_0 experts are served by the draft launch (T <= 8) only: a larger
-    batch and the cache-aware path return SPX_ERR_UNSUPPORTED; INT4 and Q8_0
-    experts in one call are an invalid argument."""
+def test_gguf_unsupported_and_invalid_calls():
+    """GGUF experts are served by the draft launch (T <= 8) only: a larger
+    batch and the cache-aware path return SPX_ERR_UNSUPPORTED; Q2_K needs H a
+    multiple of 256; INT4 and GGUF experts in one call, or an unknown format,
+    are invalid arguments."""
     spx, gh = _spx(), _gh()
     from quantized_expert_gb300.spx import SpxError
     s = _small("deepseek_v2_lite", I=256, E=16)
-    lay = gh.Layer(s, needed=list(range(s.E)), verify=False, q8=True)
+    lay = gh.Layer(s, needed=list(range(s.E)), verify=False, gguf="q8_0")
     T = 9
     ids, _ = oracle.route_topk(np.random.default_rng(120).standard_normal((T, s.E)), s.k, s.renorm)
     g, r = _routing_dev(ids, s.E)
     y = torch.empty(T * s.k, s.H, device="cuda")
     with pytest.raises(SpxError) as ei:
-        spx.spx_moe_draft_q8a16(gh.dev_f16(W.gen_x(s, T)), lay.q8, s.k, r["offsets"], r["sorted_slots"],
-                                r["active"], r["n_active"], y, spx.new_workspace(T, s.H, s.I, s.E, s.k))
+        spx.spx_moe_draft_gguf(gh.dev_f16(W.gen_x(s, T)), lay.gguf, s.k, r["offsets"], r["sorted_slots"],
+                               r["active"], r["n_active"], y, spx.new_workspace(T, s.H, s.I, s.E, s.k))
     assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
     T = 1
     routing = spx.Routing.empty(T, s.E, s.k)
@@ -706,13 +710,20 @@ def test_q8_unsupported_and_invalid_calls():
     lg = gh.dev(np.random.default_rng(121).standard_normal((T, s.E)).astype(np.float32))
     x = gh.dev_f16(W.gen_x(s, T))
     resident = torch.ones(s.E, dtype=torch.uint8, device="cuda")
-    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, q8=lay.q8, shared=lay.shared,
+    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, gguf=lay.gguf, shared=lay.shared,
                                 resident=resident)
     with pytest.raises(SpxError) as ei:
         spx.spx_moe_layer(args, None)
     assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
     w4 = gh.Layer(s, needed=[0], verify=False, slice_cols=16).w4
-    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, w4=w4, q8=lay.q8)
+    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, w4=w4, gguf=lay.gguf)
     with pytest.raises(SpxError) as ei:
         spx.spx_moe_layer(args, None)
     assert ei.value.status == spx.SPX_ERR_INVALID_ARG
+    bad = spx.PackedGguf(lay.gguf.buf, lay.gguf.E, lay.gguf.H, lay.gguf.I, 7)
+    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, gguf=bad)
+    with pytest.raises(SpxError) as ei:
+        spx.spx_moe_layer(args, None)
+    assert ei.value.status == spx.SPX_ERR_INVALID_ARG
+    assert spx.load().spx_gguf_packed_bytes(4, 384, 256, spx.SPX_GGUF_Q2_K) == 0   # H not a multiple of 256
+    assert spx.load().spx_gguf_packed_bytes(4, 384, 256, spx.SPX_GGUF_Q8_0) > 0
