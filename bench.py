@@ -436,7 +436,7 @@ def run_mine(args):
                      "frac": round(kv_bytes / (kv_us * 1e-6) / 1e9 / peak, 3),
                      "traffic": traffic_of("verify"), "traffic_capture": PROFILED_TRAFFIC["verify"],
                      "launch_us": round(kv_us, 2), "bytes_per_launch": int(kv_bytes)},
-        "draft_roofline": {"bound": "hbm", "kernel": "draft_kernel<2> (draft launch: routing + INT4 experts)",
+        "draft_roofline": {"bound": "hbm", "kernel": "draft_kernel<2, 0> (draft launch: routing + INT4 experts)",
                            "achieved": round(kd_bytes / (kd_us * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
                            "frac": round(kd_bytes / (kd_us * 1e-6) / 1e9 / peak, 3), "launch_us": round(kd_us, 2),
                            "bytes_per_launch": int(kd_bytes), "traffic": traffic_of("draft"),
