@@ -41,7 +41,7 @@ METRIC = "MoE layer µs & achieved HBM GB/s vs GB300 peak, draft T=1 / verify T=
 PROFILED_TRAFFIC = {
     "verify": {"dram_bytes": 675_098_624 + 3_160_320, "algorithmic_bytes": 674_897_920,
                "summary": "profiles/engine_kernel_deepseek_v2_lite_verify.md"},
-    "draft": {"dram_bytes": 61_510_144 + 183_296, "algorithmic_bytes": 61_374_720,
+    "draft": {"dram_bytes": 61_515_008 + 109_568, "algorithmic_bytes": 61_374_720,
               "summary": "profiles/draft_kernel_deepseek_v2_lite_draft.md"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
