@@ -53,6 +53,22 @@ def traffic_of(which):
     return None if t is None else t["dram_bytes"]
 
 
+def job_throughput(tot_bytes, ms_total, device=None):
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's
+    device time (max over ranks), and that time in ms.  One process when
+    torch.distributed is not initialised; otherwise all ranks must call it
+    (tensors on `device`: the GPU under NCCL, the CPU under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t_max = torch.tensor([float(ms_total)], dtype=torch.float64, device=device)
+        b_sum = torch.tensor([float(tot_bytes)], dtype=torch.float64, device=device)
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b_sum, op=dist.ReduceOp.SUM)
+        ms_total, tot_bytes = float(t_max.item()), float(b_sum.item())
+    return tot_bytes / (ms_total * 1e-3) / 1e9, ms_total
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -320,12 +336,7 @@ def run_mine(args):
     step_bytes = [nbytes[i % NINPUTS] for i in range(args.steps)]
     tot_bytes = sum(d + v for d, v in step_bytes)
     ms_step = ms_total / args.steps
-    t_max = ms_total
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    value = world * tot_bytes / (t_max * 1e-3) / 1e9
+    value, t_max = job_throughput(tot_bytes, ms_total, device="cuda")
 
     d_bytes = statistics.mean(b[0] for b in step_bytes)
     v_bytes = statistics.mean(b[1] for b in step_bytes)
