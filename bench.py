@@ -422,7 +422,7 @@ def run_mine(args):
     cstream.synchronize()
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e_gbs = world * tot_bytes / e2e_s / 1e9
+    e2e_gbs, _ = job_throughput(tot_bytes, e2e_s * 1e3, device="cuda")  # slowest rank's wall time
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
