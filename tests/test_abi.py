@@ -108,3 +108,31 @@ def test_struct_layouts_match_the_header(tmp_path, cname, pyname):
     assert got[0] == C.sizeof(cls)
     for f, off in zip(fields, got[1:]):
         assert getattr(cls, f).offset == off, f
+
+
+def test_draft_format_sizes_and_validation(lib):
+    """Host-side sizes and argument checks of the zero-point and GGUF entry
+    points (no CUDA call is made on these paths)."""
+    from quantized_expert_gb300 import spx
+    E, H, I = 64, 2048, 1408
+    # zero points: fp16 per (group of 128 rows, column) of gate, up and down
+    assert lib.spx_w4_zeros_bytes(E, H, I, 32) == 2 * (2 * E * (H // 128) * I + E * (I // 128) * H)
+    assert lib.spx_w4_zeros_bytes(E, H, I, 24) == 0
+    # GGUF: Q8_0 gate/up/down 34 B per 32 weights; Q2_K gate/up 84 B per 256 weights + Q8_0 down
+    q8 = E * H * I * 34 // 32
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q8_0) == 3 * q8  # scales inside the 34-byte blocks
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q2_K) == 2 * E * H * I * 84 // 256 + q8
+    assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q2_K) == 0   # Q2_K rows: multiples of 256
+    assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q8_0) == E * 384 * I * 34 // 32 * 3
+    assert lib.spx_gguf_packed_bytes(E, H, I, 7) == 0
+    fake = C.c_void_p(256)
+    assert lib.spx_gguf_repack(None, fake, fake, E, H, I, 0, fake, None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_gguf_repack(fake, fake, fake, E, H, I, 7, fake, None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_gguf_repack(fake, fake, fake, E, 384, I, spx.SPX_GGUF_Q2_K, fake, None) == \
+        spx.SPX_ERR_UNSUPPORTED
+    assert lib.spx_gguf_repack(fake, fake, fake, E, H, I, 0, C.c_void_p(264), None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_w4_zeros_repack(None, fake, fake, E, H, I, 32, fake, None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_w4_zeros_repack(fake, fake, fake, E, H, I, 24, fake, None) == spx.SPX_ERR_UNSUPPORTED
+    g = spx.GgufExperts(256, 8, 256, 512, 9)
+    assert lib.spx_moe_draft_gguf(fake, 4, C.byref(g), 2, fake, fake, fake, fake, fake, None, 0, None) == \
+        spx.SPX_ERR_WORKSPACE
