@@ -1146,12 +1146,14 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                             const int ks = sbg * 16 + kl;
                             const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
                             const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
-                            const uint32_t su = scw[kl >> 1] >> (16 * (kl & 1));  // nibbles: (t, row g / g+8)
+                            // the k-step's four scale nibbles (t, row g / g+8), in both halves
+                            const uint32_t su = ((scw[kl >> 1] >> (16 * (kl & 1))) & 0xFFFFu) * 0x10001u;
 #pragma unroll
                             for (int t = 0; t < NTW; ++t) {
-                                const uint32_t na = (su >> (8 * t)) & 15u, nb = (su >> (8 * t + 4)) & 15u;
-                                const __half2 sa2 = __hsub2(u32_as_h2((na * 0x10001u) | 0x64006400u), k1024);
-                                const __half2 sb2 = __hsub2(u32_as_h2((nb * 0x10001u) | 0x64006400u), k1024);
+                                const __half2 sa2 =
+                                    __hsub2(u32_as_h2(lop3_and_or(su >> (8 * t), 0x000F000Fu, 0x64006400u)), k1024);
+                                const __half2 sb2 =
+                                    __hsub2(u32_as_h2(lop3_and_or(su >> (8 * t + 4), 0x000F000Fu, 0x64006400u)), k1024);
                                 const __half2 oa2 = __hmul2(sa2, km1024), ob2 = __hmul2(sb2, km1024);
                                 uint32_t a[4];
 #pragma unroll

@@ -686,6 +686,30 @@ def test_gguf_draft_unit_call(case, kind):
     assert spx.spx_workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("kind", ["q8_0", "q2_k"])
+def test_gguf_draft_ragged_ranges(kind):
+    """Ragged item ranges: H = 1536 is 6 Q2_K super-blocks (items of 4 + 2) or
+    12 Q8_0 groups (3 + 3 + 3 + 3); I = 384 is one Q8_0 down range of 3 groups
+    and 24 slices; T = 3 tokens over 8 experts, k = 2."""
+    spx, gh = _spx(), _gh()
+    s = _small("phi35_moe", H=1536, I=384, E=8, k=2)
+    T = 3
+    x = W.gen_x(s, T, step=130)
+    lg = np.random.default_rng(130).standard_normal((T, s.E))
+    ids, w = oracle.route_topk(lg, s.k, s.renorm)
+    lay = gh.Layer(s, needed=sorted(set(ids.reshape(-1).tolist())), verify=False, gguf=kind)
+    g, r = _routing_dev(ids, s.E)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    y_ref = np.stack([oracle.swiglu_draft(x[int(sl) // s.k], lay.w4_host[int(ids.reshape(-1)[sl])])
+                      for sl in g["sorted_slots"]])
+    y = torch.empty(T * s.k, s.H, dtype=torch.float32, device="cuda")
+    spx.spx_moe_draft_gguf(gh.dev_f16(x), lay.gguf, s.k, r["offsets"], r["sorted_slots"], r["active"],
+                           r["n_active"], y, ws)
+    torch.cuda.synchronize()
+    gh.check_close(y.cpu().numpy(), y_ref, f"{kind} ragged")
+    assert spx.spx_workspace_status(ws) == 0
+
+
 def test_gguf_unsupported_and_invalid_calls():
     """GGUF experts are served by the draft launch (T <= 8) only: a larger
     batch and the cache-aware path return SPX_ERR_UNSUPPORTED; Q2_K needs H a
