@@ -8,7 +8,9 @@
  *       shared experts, INT4 routed experts), 3 (Expert Lookahead Buffer: GPU-
  *       resident, layer-indexed expert-activation counters), 4 (fused multi-
  *       expert INT4 draft kernel that gathers tokens by expert in one launch;
- *       expert-wise verification reordering); "Methodology in Plain English".
+ *       expert-wise verification reordering); "Methodology in Plain English";
+ *       Main Findings (routing fidelity of drafts quantised by GPTQ, AWQ and
+ *       GGUF at Q2, Q4 and Q8: the other draft formats below).
  *  [P2] richland.au, "Specter previews expert routing with an INT4 copy of the
  *       model itself", section "What shipped": GPTQ INT4 with group size 128,
  *       routers and shared experts reuse the target's FP16 tensors, W4A16
