@@ -79,6 +79,7 @@ def lib():
             L.orc_q8_dequant.argtypes = [_u8, C.c_int, C.c_int, _dp]
             L.orc_swiglu_q8.argtypes = [_u16, C.c_int, C.c_int, _u8, _u8, _u8, _dp, C.c_void_p]
             L.orc_q2k_dequant.argtypes = [_u8, C.c_int, C.c_int, _dp]
+            L.orc_q4k_dequant.argtypes = [_u8, C.c_int, C.c_int, _dp]
             L.orc_swiglu_gguf.argtypes = [_u16, C.c_int, C.c_int, C.c_int, _u8, C.c_int, _u8, C.c_int, _u8, _dp,
                                           C.c_void_p]
             L.orc_shared_gate.argtypes = [_u16, _u16, C.c_int]
@@ -211,23 +212,43 @@ def q2k_dequant(w) -> np.ndarray:
     return out
 
 
-def swiglu_q2k(x_row, ex: dict, want_h: bool = False):
-    """Expert with Q2_K gate/up (q2k_gate, q2k_up [I][H/256][84] uint8) and a
-    Q8_0 down projection (q8_down [H][I/32][34])."""
+def q4k_dequant(w) -> np.ndarray:
+    """GGUF Q4_K matrix, uint8 [N][K/256][144] super-blocks ([out][in] order) -> W [N][K]."""
+    w = _c(w, np.uint8)
+    N, K = w.shape[0], w.shape[1] * 256
+    out = np.empty((N, K), np.float64)
+    lib().orc_q4k_dequant(w, N, K, out)
+    return out
+
+
+_GGUF_TYPE = {"q2k": 1, "q4k": 2}
+
+
+def swiglu_kquant(x_row, ex: dict, want_h: bool = False):
+    """Expert with K-quant gate/up (q2k_gate, q2k_up [I][H/256][84] or q4k_gate,
+    q4k_up [I][H/256][144] uint8) and a Q8_0 down projection (q8_down
+    [H][I/32][34])."""
+    pre = "q2k" if "q2k_gate" in ex else "q4k"
+    ty = _GGUF_TYPE[pre]
     x_row = _c(x_row, np.uint16)
     H = x_row.shape[0]
-    I = ex["q2k_gate"].shape[0]
+    I = ex[pre + "_gate"].shape[0]
     y = np.empty(H, np.float64)
     h = np.empty(I, np.float64) if want_h else None
-    lib().orc_swiglu_gguf(x_row, H, I, 1, _c(ex["q2k_gate"], np.uint8), 1, _c(ex["q2k_up"], np.uint8), 0,
+    lib().orc_swiglu_gguf(x_row, H, I, ty, _c(ex[pre + "_gate"], np.uint8), ty, _c(ex[pre + "_up"], np.uint8), 0,
                           _c(ex["q8_down"], np.uint8), y, h.ctypes.data if want_h else None)
     return (y, h) if want_h else y
 
 
+swiglu_q2k = swiglu_kquant
+swiglu_q4k = swiglu_kquant
+
+
 def swiglu_draft(x_row, ex: dict, want_h: bool = False):
-    """The draft expert MLP in the expert's own format (Q2_K/Q8_0, Q8_0 or INT4)."""
-    if "q2k_gate" in ex:
-        return swiglu_q2k(x_row, ex, want_h)
+    """The draft expert MLP in the expert's own format (Q2_K or Q4_K gate/up
+    with Q8_0 down, Q8_0, or INT4)."""
+    if "q2k_gate" in ex or "q4k_gate" in ex:
+        return swiglu_kquant(x_row, ex, want_h)
     return swiglu_q8(x_row, ex, want_h) if "q8_gate" in ex else swiglu_w4(x_row, ex, want_h)
 
 

@@ -370,11 +370,58 @@ static inline double q2k_at(const uint8_t *w, const double *tab, int K, int n, i
     return d * (double)(par & 15) * (double)q - dmin * (double)(par >> 4);
 }
 
-/* Matrix value by format: ORC_Q8_0 or ORC_Q2_K. */
-enum { ORC_Q8_0 = 0, ORC_Q2_K = 1 };
+/* GGUF Q4_K [S1 Main Findings: GGUF Q4 drafts].  Reading (the GGUF format):
+ * super-blocks of 256 consecutive values in 144 bytes: binary16 d, binary16
+ * dmin (little-endian), 12 bytes of 6-bit sub-block scales and mins, then
+ * 128 bytes of 4-bit codes.  Sub-block s = 32 consecutive values (8 per
+ * super-block).  For s < 4: scale = byte[s] & 63, min = byte[s+4] & 63; for
+ * s >= 4: scale = (byte[s+4] & 15) | (byte[s-4] >> 6) << 4 and
+ * min = (byte[s+4] >> 4) | (byte[s] >> 6) << 4 (bytes of the 12).  Value w:
+ * chunk c = w / 64 uses code byte 32*c + w % 32, its low nibble for
+ * w % 64 < 32 (sub-block 2c), its high nibble otherwise (sub-block 2c+1);
+ * value = d*scale*q - dmin*min. */
+static inline void q4k_scale_min(const uint8_t *sc12, int s, int *scale, int *mn)
+{
+    if (s < 4) {
+        *scale = sc12[s] & 63;
+        *mn = sc12[s + 4] & 63;
+    } else {
+        *scale = (sc12[s + 4] & 15) | ((sc12[s - 4] >> 6) << 4);
+        *mn = (sc12[s + 4] >> 4) | ((sc12[s] >> 6) << 4);
+    }
+}
+
+static inline double q4k_at(const uint8_t *w, const double *tab, int K, int n, int kk)
+{
+    const uint8_t *blk = w + ((int64_t)n * (K / 256) + kk / 256) * 144;
+    int wi = kk % 256;
+    int scale, mn;
+    q4k_scale_min(blk + 4, wi / 32, &scale, &mn);
+    int byte = blk[16 + 32 * (wi / 64) + wi % 32];
+    int q = (wi % 64) < 32 ? (byte & 15) : (byte >> 4);
+    double d = tab[(uint16_t)(blk[0] | (blk[1] << 8))];
+    double dmin = tab[(uint16_t)(blk[2] | (blk[3] << 8))];
+    return d * (double)scale * (double)q - dmin * (double)mn;
+}
+
+/* out[n][kk] = W[n][kk] of a Q4_K matrix, N x K ([out][in]). */
+void orc_q4k_dequant(const uint8_t *w, int N, int K, double *out)
+{
+    const double *tab = half_tab();
+    for (int n = 0; n < N; ++n)
+        for (int kk = 0; kk < K; ++kk)
+            out[(int64_t)n * K + kk] = q4k_at(w, tab, K, n, kk);
+}
+
+/* Matrix value by format: ORC_Q8_0, ORC_Q2_K or ORC_Q4_K. */
+enum { ORC_Q8_0 = 0, ORC_Q2_K = 1, ORC_Q4_K = 2 };
 static inline double gguf_at(int type, const uint8_t *w, const double *tab, int K, int n, int kk)
 {
-    return type == ORC_Q2_K ? q2k_at(w, tab, K, n, kk) : q8_at(w, tab, K, n, kk);
+    if (type == ORC_Q2_K)
+        return q2k_at(w, tab, K, n, kk);
+    if (type == ORC_Q4_K)
+        return q4k_at(w, tab, K, n, kk);
+    return q8_at(w, tab, K, n, kk);
 }
 
 /* out[n][kk] = W[n][kk] of a Q2_K matrix, N x K ([out][in]). */

@@ -45,7 +45,7 @@ __all__ = [
 
 # stream tags (part of the seeding key, never of the arithmetic)
 (TAG_X, TAG_ROUTER, TAG_LOGITS, TAG_W4, TAG_F16, TAG_SHARED, TAG_SGATE, TAG_PERM, TAG_ZEROS, TAG_Q8,
- TAG_Q2K) = range(1, 12)
+ TAG_Q2K, TAG_Q4K) = range(1, 13)
 HOT_LOG_A = 1.1510  # ln a, a = 3.1614
 ZIPF_S = 1.1
 
@@ -246,6 +246,27 @@ def gen_q2k_expert(shape: LayerShape, layer: int, e: int) -> dict:
     H, I = shape.H, shape.I
     rng = rng_for(shape, TAG_Q2K, layer, e)
     return dict(q2k_gate=_q2k_matrix(rng, I, H), q2k_up=_q2k_matrix(rng, I, H), q8_down=_q8_matrix(rng, H, I))
+
+
+def _q4k_matrix(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
+    """GGUF Q4_K super-blocks of an [N][K] matrix: uint8 [N][K/256][144]; the
+    scale/min bytes and codes uniform, d U(0.00015, 0.0004) and dmin
+    U(0.0003, 0.001) fp16 little-endian (weights of the INT4 experts' scale)."""
+    out = rng.integers(0, 256, size=(N, K // 256, 144), dtype=np.uint8)
+    d = rng.uniform(0.00015, 0.0004, size=(N, K // 256)).astype(np.float16).view(np.uint16)
+    dmin = rng.uniform(0.0003, 0.001, size=(N, K // 256)).astype(np.float16).view(np.uint16)
+    out[:, :, 0], out[:, :, 1] = d & 0xFF, d >> 8
+    out[:, :, 2], out[:, :, 3] = dmin & 0xFF, dmin >> 8
+    return out
+
+
+def gen_q4k_expert(shape: LayerShape, layer: int, e: int) -> dict:
+    """Draft expert e with GGUF Q4_K gate/up (``q4k_gate``/``q4k_up``
+    [I][H/256][144] uint8) and a GGUF Q8_0 down projection (``q8_down``
+    [H][I/32][34]), for the reason given at gen_q2k_expert."""
+    H, I = shape.H, shape.I
+    rng = rng_for(shape, TAG_Q4K, layer, e)
+    return dict(q4k_gate=_q4k_matrix(rng, I, H), q4k_up=_q4k_matrix(rng, I, H), q8_down=_q8_matrix(rng, H, I))
 
 
 def gen_f16_expert(shape: LayerShape, layer: int, e: int) -> dict:

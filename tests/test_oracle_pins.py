@@ -419,6 +419,92 @@ def test_q2k_identity_expert_closed_form():
     assert np.allclose(oracle.swiglu_q2k(x.view(np.uint16), ex), xd * expit(xd) * xd, rtol=1e-14, atol=1e-300)
 
 
+# ------------------------------------------------------- GGUF Q4_K draft
+def _q4k_scale_bytes(sc, mn):
+    """8 six-bit scales and mins -> the 12 bytes of a Q4_K super-block."""
+    b = np.zeros(12, np.int64)
+    for s in range(4):
+        b[s] = (sc[s] & 63) | ((sc[s + 4] >> 4) << 6)
+        b[s + 4] = (mn[s] & 63) | ((mn[s + 4] >> 4) << 6)
+        b[s + 8] = (sc[s + 4] & 15) | ((mn[s + 4] & 15) << 4)
+    return b.astype(np.uint8)
+
+
+def _q4k_blocks(q, sc, mn, d, dmin):
+    """Codes q [N][K] (0..15), sub-block scales and mins [N][K/32] (0..63), fp16
+    d and dmin [N][K/256] -> [N][K/256][144] uint8 Q4_K super-blocks."""
+    N, K = q.shape
+    out = np.zeros((N, K // 256, 144), np.uint8)
+    for n in range(N):
+        for b in range(K // 256):
+            out[n, b, 4:16] = _q4k_scale_bytes(sc[n, 8 * b:8 * b + 8], mn[n, 8 * b:8 * b + 8])
+    qb = q.reshape(N, K // 256, 256)
+    for w in range(256):
+        sh = 0 if w % 64 < 32 else 4
+        out[:, :, 16 + 32 * (w // 64) + w % 32] |= (qb[:, :, w] << sh).astype(np.uint8)
+    for off, v in ((0, d), (2, dmin)):
+        bits = np.asarray(v, np.float16).view(np.uint16)
+        out[:, :, off] = bits & 0xFF
+        out[:, :, off + 1] = bits >> 8
+    return out
+
+
+def test_q4k_dequant_hand_derived_golden():
+    gold = json.load(open(os.path.join(GOLD, "gguf_q4_k.json")))
+    blk = np.zeros((1, 1, 144), np.uint8)
+    blk[0, 0, 0:2] = gold["d_bytes"]
+    blk[0, 0, 2:4] = gold["dmin_bytes"]
+    blk[0, 0, 4:16] = gold["scale_bytes"]
+    for i, v in gold["code_bytes"].items():
+        blk[0, 0, 16 + int(i)] = v
+    assert list(_q4k_scale_bytes(np.array(gold["scales"]), np.array(gold["mins"]))) == gold["scale_bytes"]
+    out = oracle.q4k_dequant(blk)[0]
+    for w, v in gold["checks"]:
+        assert out[w] == v, w
+
+
+def test_q4k_dequant_every_position_closed_form():
+    """d*scale*q - dmin*min at every value position, every code, scales and
+    mins over the full 6-bit range in every sub-block slot."""
+    rng = np.random.default_rng(21)
+    N, K = 6, 512
+    q = rng.integers(0, 16, size=(N, K))
+    sc = rng.integers(0, 64, size=(N, K // 32))
+    mn = rng.integers(0, 64, size=(N, K // 32))
+    d = rng.uniform(0.01, 0.1, size=(N, K // 256)).astype(np.float16)
+    dmin = rng.uniform(0.01, 0.1, size=(N, K // 256)).astype(np.float16)
+    out = oracle.q4k_dequant(_q4k_blocks(q, sc, mn, d, dmin))
+    rep32 = lambda a: np.repeat(a, 32, axis=1)  # noqa: E731
+    rep256 = lambda a: np.repeat(np.asarray(a, np.float64), 256, axis=1)  # noqa: E731
+    ref = rep256(d) * rep32(sc) * q - rep256(dmin) * rep32(mn)
+    assert np.array_equal(out, ref)
+    assert set(np.unique(q)) == set(range(16)) and sc.max() == 63 and mn.min() == 0
+
+
+def test_q4k_expert_equals_its_fp16_copy():
+    """Q4_K gate/up and Q8_0 down with power-of-two scales (every weight exact
+    in fp16) equal the FP16 oracle on those weights term for term."""
+    rng = np.random.default_rng(22)
+    H, I = 512, 256
+    ex = {}
+    for name in ("gate", "up"):
+        q = rng.integers(0, 16, size=(I, H))
+        sc = rng.integers(0, 64, size=(I, H // 32))
+        mn = rng.integers(0, 64, size=(I, H // 32))
+        ex["q4k_" + name] = _q4k_blocks(q, sc, mn, np.full((I, H // 256), 2.0 ** -12), np.full((I, H // 256), 2.0 ** -8))
+    ex["q8_down"] = _q8_blocks(rng.integers(-128, 128, size=(H, I)), np.full((H, I // 32), 2.0 ** -12))
+    f16 = dict(w_gate=oracle.q4k_dequant(ex["q4k_gate"]).astype(np.float16).view(np.uint16),
+               w_up=oracle.q4k_dequant(ex["q4k_up"]).astype(np.float16).view(np.uint16),
+               w_down=oracle.q8_dequant(ex["q8_down"]).astype(np.float16).view(np.uint16))
+    assert np.array_equal(f16["w_up"].view(np.float16).astype(np.float64), oracle.q4k_dequant(ex["q4k_up"]))
+    shape = W.scaled(W.CONFIGS["tiny"], H=H, I=I)
+    for step in range(2):
+        x = W.gen_x(shape, 1, step=step)[0]
+        y4, h4 = oracle.swiglu_q4k(x, ex, want_h=True)
+        y16, h16 = oracle.swiglu_f16(x, f16, want_h=True)
+        assert np.array_equal(h4, h16) and np.array_equal(y4, y16)
+
+
 # ---------------------------------------------------------------- MLP
 def _identity_w4(n):
     q = np.full((n // 8, n), 0x88888888, np.uint32)
