@@ -91,8 +91,8 @@ def f16_expert_bytes(s, I=None):
 def layer_bytes(s, mode, T, n_unique, zeros=False, gguf=None):
     if gguf == "q8_0":  # GGUF Q8_0: 34 bytes per 32 weights
         b = n_unique * 3 * s.H * s.I * 34 // 32
-    elif gguf == "q2_k":  # Q2_K gate/up (84 bytes per 256 weights), Q8_0 down
-        b = n_unique * (2 * s.H * s.I * 84 // 256 + s.H * s.I * 34 // 32)
+    elif gguf in ("q2_k", "q4_k"):  # K-quant gate/up as packed (84 or 148 bytes per 256 weights), Q8_0 down
+        b = n_unique * (2 * s.H * s.I * (84 if gguf == "q2_k" else 148) // 256 + s.H * s.I * 34 // 32)
     else:
         b = n_unique * (w4_expert_bytes(s) if mode == "draft" else f16_expert_bytes(s))
     if zeros:  # fp16 zero points: one per group of 128 rows and column, of the three matrices
@@ -731,10 +731,16 @@ def run_draft_batch(args):
                 b[..., 82:84] = scales((E, N, K // 256), 0.001, 0.004).view(E, N, K // 256, 2)
                 return b
 
-            gu = q8 if args.gguf == "q8_0" else q2k
+            def q4k(N, K):  # Q4_K super-blocks, d U(0.00015, 0.0004), dmin U(0.0003, 0.001)
+                b = torch.randint(0, 256, (E, N, K // 256, 144), dtype=torch.uint8, device="cuda", generator=g)
+                b[..., 0:2] = scales((E, N, K // 256), 0.00015, 0.0004).view(E, N, K // 256, 2)
+                b[..., 2:4] = scales((E, N, K // 256), 0.0003, 0.001).view(E, N, K // 256, 2)
+                return b
+
+            gu, ty = {"q8_0": (q8, spx.SPX_GGUF_Q8_0), "q2_k": (q2k, spx.SPX_GGUF_Q2_K),
+                      "q4_k": (q4k, spx.SPX_GGUF_Q4_K)}[args.gguf]
             st["w4"] = None
-            st["gguf"] = spx.spx_gguf_repack(gu(I, H), gu(I, H), q8(H, I),
-                                             spx.SPX_GGUF_Q8_0 if args.gguf == "q8_0" else spx.SPX_GGUF_Q2_K)
+            st["gguf"] = spx.spx_gguf_repack(gu(I, H), gu(I, H), q8(H, I), ty)
             torch.cuda.synchronize()
     peak, peak_src = measured_peaks()
     rows = []
@@ -775,7 +781,7 @@ def run_draft_batch(args):
                      "tokens_per_s": round(T / (us * 1e-6), 1)})
         assert spx.spx_workspace_status(ws) == 0
     zp = (", per-group zero points" if args.zeros else ", GGUF Q8_0 experts" if args.gguf == "q8_0"
-          else ", GGUF Q2_K gate/up + Q8_0 down experts" if args.gguf == "q2_k" else "")
+          else f", GGUF {args.gguf.upper()} gate/up + Q8_0 down experts" if args.gguf else "")
     line = {"metric": "draft layer with T requests' tokens per call, device us per layer",
             "config": {"workload": f"{s.name} draft{zp}, T = 1, 2, 4, 8 (one token per request)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
@@ -805,7 +811,7 @@ def main():
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
     ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
-    ap.add_argument("--gguf", choices=["q8_0", "q2_k"], help="with --draft-batch: GGUF experts instead of INT4")
+    ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"], help="with --draft-batch: GGUF experts instead of INT4")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
     if args.loop:

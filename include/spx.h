@@ -169,16 +169,24 @@ typedef struct {
  *     bytes of 2-bit codes, weight w's code at bits 2*((w % 128) / 32) of byte
  *     32*(w / 128) + w % 32; binary16 d; binary16 dmin (little-endian);
  *     weight = d * sc * q - dmin * m.  Needs in % 256 == 0.
- * gate and up are in gate_up_type ([E][I][H/32][34] or [E][I][H/256][84]);
+ *   Q4_K: a row is in/256 super-blocks of 144 bytes: binary16 d, binary16
+ *     dmin, 12 bytes of 6-bit scales and mins of the 8 sub-blocks of 32
+ *     weights (s < 4: scale = b[s] & 63, min = b[s+4] & 63; s >= 4: scale =
+ *     (b[s+4] & 15) | (b[s-4] >> 6) << 4, min = (b[s+4] >> 4) | (b[s] >> 6)
+ *     << 4), then 128 bytes of 4-bit codes, weight w in byte 32*(w / 64) +
+ *     w % 32, low nibble when w % 64 < 32, else high nibble; weight =
+ *     d * scale * q - dmin * min.  Needs in % 256 == 0.
+ * gate and up are in gate_up_type ([E][I][H/32][34], [E][I][H/256][84] or
+ * [E][I][H/256][144]);
  * down is Q8_0 ([E][H][I/32][34]): the down rows of the 1408-wide shapes are
  * not a multiple of 256.  Repacked (spx_gguf_repack) into the draft launch's
  * streaming order, 16 columns per slice.  Served by draft calls of T <= 8
  * (the one-launch draft path); other calls return SPX_ERR_UNSUPPORTED. */
-enum { SPX_GGUF_Q8_0 = 0, SPX_GGUF_Q2_K = 1 };
+enum { SPX_GGUF_Q8_0 = 0, SPX_GGUF_Q2_K = 1, SPX_GGUF_Q4_K = 2 };
 typedef struct {
     const void *packed; /* spx_gguf_packed_bytes() bytes, from spx_gguf_repack() */
     int E, H, I;
-    int gate_up_type;   /* SPX_GGUF_Q8_0 or SPX_GGUF_Q2_K */
+    int gate_up_type;   /* SPX_GGUF_Q8_0, SPX_GGUF_Q2_K or SPX_GGUF_Q4_K */
 } spx_gguf_experts;
 
 /* Shared expert(s): one FP16 MLP of intermediate size I_s (several shared
@@ -193,7 +201,7 @@ typedef struct {
 
 SPX_API size_t spx_w4_packed_bytes(int E, int H, int I, int slice_cols);
 SPX_API size_t spx_f16_packed_bytes(int E, int H, int I);
-/* H, I multiples of 128 (Q2_K: H of 256); else 0 */
+/* H, I multiples of 128 (Q2_K, Q4_K: H of 256); else 0 */
 SPX_API size_t spx_gguf_packed_bytes(int E, int H, int I, int gate_up_type);
 /* Shared expert pack: the FP16 units of one expert followed by its down
  * weights once more in output-block order (read by the draft launch). */

@@ -83,7 +83,7 @@ extern "C" const char *spx_status_string(int st) {
     }
 }
 
-extern "C" int spx_version(void) { return 104; }
+extern "C" int spx_version(void) { return 105; }
 
 extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
@@ -173,7 +173,12 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
 }
 
 static int gguf_fmt(const spx_gguf_experts *w) {
-    return w->gate_up_type == SPX_GGUF_Q8_0 ? kFmtQ8 : w->gate_up_type == SPX_GGUF_Q2_K ? kFmtQ2K : -1;
+    switch (w->gate_up_type) {
+    case SPX_GGUF_Q8_0: return kFmtQ8;
+    case SPX_GGUF_Q2_K: return kFmtQ2K;
+    case SPX_GGUF_Q4_K: return kFmtQ4K;
+    default: return -1;
+    }
 }
 
 extern "C" int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_experts *w, int k, const int32_t *offsets,
@@ -184,7 +189,7 @@ extern "C" int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_exper
                                  16);
     if (st) return st;
     if (!al16(w->packed) || !al16(y_sorted) || gguf_fmt(w) < 0) return SPX_ERR_INVALID_ARG;
-    if (!draft_supported(T, w->H, w->I, 16, 0, w->E, k, gguf_fmt(w) == kFmtQ2K))
+    if (!draft_supported(T, w->H, w->I, 16, 0, w->E, k, gguf_fmt(w) == kFmtQ2K || gguf_fmt(w) == kFmtQ4K))
         return SPX_ERR_UNSUPPORTED;  // the draft launch only
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
@@ -322,9 +327,9 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
 
     const bool zeros = a->mode == 0 && !gguf && a->w4->zeros;
-    const bool q2k = gguf && gguf_fmt(a->gguf) == kFmtQ2K;
-    if ((zeros || gguf) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k, q2k))) return SPX_ERR_UNSUPPORTED;
-    if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k, q2k)) {
+    const bool kq = gguf && (gguf_fmt(a->gguf) == kFmtQ2K || gguf_fmt(a->gguf) == kFmtQ4K);
+    if ((zeros || gguf) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k, kq))) return SPX_ERR_UNSUPPORTED;
+    if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k, kq)) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch
         // computes the logits first and the draft launch overlaps it.

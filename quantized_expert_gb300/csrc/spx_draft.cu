@@ -49,9 +49,13 @@ static_assert(kDkQ8Groups * kQ8GroupBytes <= kDkData, "Q8_0 items fit the stage"
 // GGUF Q2_K gate/up: super-blocks of 256 rows of 2688 bytes, four per routed item
 constexpr int kDkQ2kSbs = 4;
 static_assert(kDkQ2kSbs * kQ2kSbBytes <= kDkData, "Q2_K items fit the stage");
+// GGUF Q4_K gate/up: super-blocks of 4736 bytes, three per routed item
+constexpr int kDkQ4kSbs = 3;
+static_assert(kDkQ4kSbs * kQ4kSbBytes <= kDkData, "Q4_K items fit the stage");
 // draft expert formats (template argument of the launch): INT4, INT4 with zero
-// points, GGUF Q8_0, and GGUF Q2_K gate/up with a Q8_0 down projection
-enum : int { DK_FMT_W4 = 0, DK_FMT_W4Z = 1, DK_FMT_Q8 = 2, DK_FMT_Q2K = 3 };
+// points, GGUF Q8_0, and GGUF Q2_K or Q4_K gate/up with a Q8_0 down projection
+enum : int { DK_FMT_W4 = 0, DK_FMT_W4Z = 1, DK_FMT_Q8 = 2, DK_FMT_Q2K = 3, DK_FMT_Q4K = 4 };
+__host__ __device__ inline bool dk_kquant(int fmt) { return fmt == DK_FMT_Q2K || fmt == DK_FMT_Q4K; }
 constexpr int kDkSdSteps = 16;    // k-steps of I_s per SD item
 constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
 constexpr int kDkDBatch = 2;      // down items per queue unit
@@ -96,18 +100,21 @@ struct DkGeom {
     int rd_gpi, rd_nr;  // routed down: groups per item, ranges
 };
 
-// fmt: DK_FMT_*; the GGUF formats use S = 16, Q2_K gate/up items count
+// fmt: DK_FMT_*; the GGUF formats use S = 16, K-quant gate/up items count
 // super-blocks of 256 rows instead of groups of 128.
 __host__ __device__ inline DkGeom dk_geom(int H, int I, int S, int I_s, int fmt = DK_FMT_W4) {
-    const bool q8dn = fmt == DK_FMT_Q8 || fmt == DK_FMT_Q2K;
+    const bool q8dn = fmt == DK_FMT_Q8 || dk_kquant(fmt);
     DkGeom g;
     g.sg_cols = I_s / 16;
     g.sg_nks = ((H / 16) % 16 == 0) ? 16 : 8;
     g.sg_nr = (H / 16) / g.sg_nks;
     g.sd_nr = (I_s / 16 + kDkSdSteps - 1) / kDkSdSteps;
     g.rg_blocks = I / S;
-    g.rg_gpi = fmt == DK_FMT_Q8 ? kDkQ8Groups : fmt == DK_FMT_Q2K ? kDkQ2kSbs : (S == 32 ? 4 : 8);
-    g.rg_nr = (H / (fmt == DK_FMT_Q2K ? 256 : 128) + g.rg_gpi - 1) / g.rg_gpi;
+    g.rg_gpi = fmt == DK_FMT_Q8    ? kDkQ8Groups
+               : fmt == DK_FMT_Q2K ? kDkQ2kSbs
+               : fmt == DK_FMT_Q4K ? kDkQ4kSbs
+                                   : (S == 32 ? 4 : 8);
+    g.rg_nr = (H / (dk_kquant(fmt) ? 256 : 128) + g.rg_gpi - 1) / g.rg_gpi;
     g.rd_gpi = q8dn ? kDkQ8Groups : kDkRdGroups;
     g.rd_nr = (I / 128 + g.rd_gpi - 1) / g.rd_gpi;
     return g;
@@ -144,8 +151,9 @@ struct DkLayout {
     int bars, hdrs, misc, gamma, act, sfree, scnt, pstate, pend, sacc, rids, rpw, rrank, rsv, stn, ste, sx, sx16, xs,
         ring, stage, hs_off, total, xs_stride, slot_floats;
 };
-// q2k: room for the 16-row x sums of GGUF Q2_K gate/up items (hi, lo fp16).
-__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E, bool q2k = false) {
+// kq: room for the x sums of GGUF K-quant gate/up items (hi, lo fp16; over 16
+// rows for Q2_K, 32 rows for Q4_K).
+__host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E, bool kq = false) {
     DkLayout L;
     int o = 0;
     L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier
@@ -189,8 +197,8 @@ __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int 
     L.sx = o;  // [T][H/128] group sums of x (fp32)
     o += T * (H / 128) * 4;
     o = (o + 15) & ~15;
-    L.sx16 = o;  // Q2_K: [T][H/16] sums of x over 16 rows, fp16 hi, then fp16 lo
-    o += q2k ? T * (H / 16) * 4 : 0;
+    L.sx16 = o;  // Q2_K: [T][H/16] sums of x over 16 rows, fp16 hi, then lo (Q4_K: [T][H/32] each)
+    o += kq ? T * (H / 16) * 4 : 0;
     o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
@@ -298,7 +306,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     const uint64_t pol = policy_evict_first();
     const int H = p.H, I = p.I, T = p.T;
     const DkGeom g = dk_geom(H, I, p.S, p.I_s, p.fmt);
-    const bool q8dn = p.fmt == DK_FMT_Q8 || p.fmt == DK_FMT_Q2K;
+    const bool q8dn = p.fmt == DK_FMT_Q8 || dk_kquant(p.fmt);
     const int NQ = H / 32;
     const int nSGb = p.sh ? g.sg_cols : 0;
     const int nSD = p.sh ? NQ * g.sd_nr : 0;
@@ -410,12 +418,14 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             for (int r = 0; r < g.rg_nr; ++r) {
                 h.r = r;
                 h.k0 = r * g.rg_gpi;
-                h.n = min(g.rg_gpi, H / (p.fmt == DK_FMT_Q2K ? 256 : 128) - h.k0);
+                h.n = min(g.rg_gpi, H / (dk_kquant(p.fmt) ? 256 : 128) - h.k0);
                 const size_t gb = p.fmt == DK_FMT_Q8    ? (size_t)kQ8GroupBytes
                                   : p.fmt == DK_FMT_Q2K ? (size_t)kQ2kSbBytes
+                                  : p.fmt == DK_FMT_Q4K ? (size_t)kQ4kSbBytes
                                                         : w4_group_bytes(p.S);
                 const size_t ub = p.fmt == DK_FMT_Q8    ? q8_unit_bytes(H)
                                   : p.fmt == DK_FMT_Q2K ? q2k_unit_bytes(H)
+                                  : p.fmt == DK_FMT_Q4K ? q4k_unit_bytes(H)
                                                         : w4_unit_bytes(H, p.S);
                 const uint8_t *src = p.w4 + unit * ub + (size_t)h.k0 * gb;
                 // zero points (2S per group, as the scales) in the stage's h area, unused by these items
@@ -753,14 +763,15 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     constexpr bool ZP = FMT == DK_FMT_W4Z;  // INT4 with per-group zero points
     constexpr bool Q8 = FMT == DK_FMT_Q8;   // GGUF Q8_0 (S = 16)
     constexpr bool Q2K = FMT == DK_FMT_Q2K; // GGUF Q2_K gate/up, Q8_0 down (S = 16)
-    constexpr bool Q8DN = Q8 || Q2K;        // Q8_0 down items
-    static_assert(!(Q8 || Q2K) || MS == 1, "GGUF experts use 16-column slices");
+    constexpr bool Q4K = FMT == DK_FMT_Q4K; // GGUF Q4_K gate/up, Q8_0 down (S = 16)
+    constexpr bool Q8DN = Q8 || Q2K || Q4K; // Q8_0 down items
+    static_assert(!Q8DN || MS == 1, "GGUF experts use 16-column slices");
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
     griddep_launch_dependents();
     const int nst = p.nstages;
-    const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E, Q2K);
+    const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E, Q2K || Q4K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -845,6 +856,16 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 const __half hi = __float2half_rn(s16);
                 sxh[idx / 2] = hi;  // [t][16-row block]: idx/2 = t*(H/16) + block
                 sxh[T * (H / 16) + idx / 2] = __float2half_rn(s16 - __half2float(hi));
+            }
+        }
+        if constexpr (Q4K) {  // sums over 32 rows (four chunks), as an fp16 pair hi + lo
+            float s32 = sum + __shfl_xor_sync(0xffffffffu, sum, 1);
+            s32 += __shfl_xor_sync(0xffffffffu, s32, 2);
+            if ((lane & 3) == 0 && idx < T * (H / 8)) {
+                __half *sxh = reinterpret_cast<__half *>(smem + L.sx16);
+                const __half hi = __float2half_rn(s32);
+                sxh[idx / 4] = hi;  // [t][32-row block]: idx/4 = t*(H/32) + block
+                sxh[T * (H / 32) + idx / 4] = __float2half_rn(s32 - __half2float(hi));
             }
         }
 #pragma unroll
@@ -1191,6 +1212,80 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                         run[t][3] += db * am[t][3] - mb * an[t][3];
                     }
                 }
+            } else if constexpr (Q4K) {
+                // GGUF Q4_K: super-blocks of 256 rows; sub-block c = 32 rows = k-steps
+                // 2c and 2c+1, with a 6-bit scale and min per row.  As for Q2_K the
+                // fragment holds scale*q (<= 945, exact in fp16 through one fused
+                // multiply-add), and the mins enter through one more product with the
+                // token's eight 32-row sums of x (k = sub-block, k >= 8 zero).
+                const __half *sxh = reinterpret_cast<const __half *>(smem + L.sx16) + tok * (H / 32);
+                const __half *sxl = sxh + T * (H / 32);
+                const __half2 k1024 = u32_as_h2(0x64006400u), km1024 = u32_as_h2(0xE400E400u);
+                const uint32_t kExp = 0x64646464u;
+                for (int gr = 0; gr < h.n; ++gr) {
+                    const uint8_t *sp = stage + (size_t)gr * kQ4kSbBytes;
+                    const __half *dd = reinterpret_cast<const __half *>(sp);  // d [32], then dmin [32]
+                    const int sbg = h.k0 + gr;                                // super-block of H
+                    const uint4 c0 = lds128(sp + kQ4kScaleOff + g * 32);
+                    const uint4 c1 = lds128(sp + kQ4kScaleOff + g * 32 + 16);
+                    const uint32_t scw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    float am[NTW][4] = {}, an[NTW][4] = {};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = lds128(sp + kQ4kCodeOff + c * 512 + lane * 16);
+                        const uint32_t words[4] = {v.x, v.y, v.z, v.w};  // [k-step][tile]
+                        __half2 sc2[NTW][2], of2[NTW][2];                 // (scale, -1024 scale) of rows g, g+8
+#pragma unroll
+                        for (int t = 0; t < NTW; ++t) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint32_t sel = (2 * t + j) * 0x0101u + 0x4040u;  // byte 2t+j under 0x64
+                                sc2[t][j] = __hsub2(u32_as_h2(__byte_perm(scw[c], kExp, sel)), k1024);
+                                of2[t][j] = __hmul2(sc2[t][j], km1024);
+                            }
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int ks = sbg * 16 + 2 * c + kk;
+                            const uint32_t b0 = okx ? lds32(xr + 16 * ks) : 0u;
+                            const uint32_t b1 = okx ? lds32(xr + 16 * ks + 8) : 0u;
+#pragma unroll
+                            for (int t = 0; t < NTW; ++t) {
+                                const uint32_t w = words[2 * kk + t];
+                                uint32_t a[4];
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) {
+                                    const uint32_t raw = lop3_and_or(w >> (4 * r), 0x000F000Fu, 0x64006400u);
+                                    a[r] = h2_as_u32(__hfma2(u32_as_h2(raw), sc2[t][r & 1], of2[t][r & 1]));
+                                }
+                                mma_16816(am[t], a, b0, b1);
+                            }
+                        }
+                    }
+                    const uint32_t bh0 = okx ? lds32(sxh + sbg * 8 + 2 * q4) : 0u;
+                    const uint32_t bl0 = okx ? lds32(sxl + sbg * 8 + 2 * q4) : 0u;
+                    const uint2 mw = lds64(sp + kQ4kMinOff + lane * 8);
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const uint32_t w = t == 0 ? mw.x : mw.y;
+                        uint32_t a[4];
+                        a[0] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, kExp, 0x4140u)), k1024));
+                        a[1] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, kExp, 0x4342u)), k1024));
+                        a[2] = 0u;
+                        a[3] = 0u;
+                        mma_16816(an[t], a, bh0, 0u);
+                        mma_16816(an[t], a, bl0, 0u);
+                    }
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t) {
+                        const float da = __half2float(dd[t * 16 + g]), db = __half2float(dd[t * 16 + g + 8]);
+                        const float ma = __half2float(dd[32 + t * 16 + g]), mb = __half2float(dd[32 + t * 16 + g + 8]);
+                        run[t][0] += da * am[t][0] - ma * an[t][0];
+                        run[t][1] += da * am[t][1] - ma * an[t][1];
+                        run[t][2] += db * am[t][2] - mb * an[t][2];
+                        run[t][3] += db * am[t][3] - mb * an[t][3];
+                    }
+                }
             } else {
                 // Raw codes into the mma: rows m < 8 of a tile get 1024 + q, rows m >= 8
                 // get 1024 + 16 q (the magic-exponent fragments without their fix-up).
@@ -1484,11 +1579,11 @@ size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max
     return dk_scratch(base, T, H, I, I_s, nact_max).end;
 }
 
-bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k, bool q2k) {
-    if (q2k && (H % 256 || S != 16)) return false;
+bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k, bool kq) {
+    if (kq && (H % 256 || S != 16)) return false;
     if (T < 1 || T > 8 || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
     if (I_s % 16 || E < 1 || k < 1 || E > kMaxE || T * k > kMaxSlots) return false;
-    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E, q2k).total <= kSmemLimit;
+    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E, kq).total <= kSmemLimit;
 }
 
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
@@ -1497,9 +1592,10 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     const bool zp = e.w4_zeros != nullptr;
     p.fmt = e.routed_fmt == kFmtQ8    ? DK_FMT_Q8
             : e.routed_fmt == kFmtQ2K ? DK_FMT_Q2K
+            : e.routed_fmt == kFmtQ4K ? DK_FMT_Q4K
             : zp                      ? DK_FMT_W4Z
                                       : DK_FMT_W4;
-    const bool q2k = p.fmt == DK_FMT_Q2K;
+    const bool kq = dk_kquant(p.fmt);
     if (e.w4_zeros) {
         p.zeros_gu = reinterpret_cast<const __half *>(e.w4_zeros);
         p.zeros_dn = reinterpret_cast<const __half *>(e.w4_zeros + w4_zeros_gu_bytes(e.E, e.H, e.I, e.S));
@@ -1507,6 +1603,7 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.S = e.S;
     p.w4_colblk = p.fmt == DK_FMT_Q8    ? q8_units_bytes(e.E, e.H, e.I)
                   : p.fmt == DK_FMT_Q2K ? q2k_units_bytes(e.E, e.H, e.I)
+                  : p.fmt == DK_FMT_Q4K ? q4k_units_bytes(e.E, e.H, e.I)
                                         : w4_colblk_offset(e.E, e.H, e.I, e.S);
     p.sh = e.shared;
     p.w_sgate = e.w_sgate;
@@ -1547,25 +1644,29 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.rdy_s = reinterpret_cast<int *>(ws + sc.rdy_s);
     p.rdy_r = reinterpret_cast<int *>(ws + sc.rdy_r);
     int nst = 12;  // <= kDkMaxStages
-    DkLayout L = dk_layout(e.T, e.H, nst, e.k, p.nact_max, e.E, q2k);
-    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E, q2k);
+    DkLayout L = dk_layout(e.T, e.H, nst, e.k, p.nact_max, e.E, kq);
+    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E, kq);
     if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
     p.nstages = nst;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    static int configured[6][64] = {};
+    static int configured[7][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
     const int ms = e.S / 16;
-    const bool gguf = p.fmt == DK_FMT_Q8 || p.fmt == DK_FMT_Q2K;
+    const bool gguf = p.fmt == DK_FMT_Q8 || kq;
     if (gguf && (ms != 1 || zp)) return SPX_ERR_UNSUPPORTED;
-    if (q2k && e.H % 256) return SPX_ERR_UNSUPPORTED;
+    if (kq && e.H % 256) return SPX_ERR_UNSUPPORTED;
     void (*kern)(const DkParams) =
         p.fmt == DK_FMT_Q8    ? draft_kernel<1, DK_FMT_Q8>
         : p.fmt == DK_FMT_Q2K ? draft_kernel<1, DK_FMT_Q2K>
+        : p.fmt == DK_FMT_Q4K ? draft_kernel<1, DK_FMT_Q4K>
         : ms == 2             ? (zp ? draft_kernel<2, DK_FMT_W4Z> : draft_kernel<2, DK_FMT_W4>)
                               : (zp ? draft_kernel<1, DK_FMT_W4Z> : draft_kernel<1, DK_FMT_W4>);
-    const int ki = p.fmt == DK_FMT_Q8 ? 4 : p.fmt == DK_FMT_Q2K ? 5 : (ms - 1) * 2 + (zp ? 1 : 0);
+    const int ki = p.fmt == DK_FMT_Q8    ? 4
+                   : p.fmt == DK_FMT_Q2K ? 5
+                   : p.fmt == DK_FMT_Q4K ? 6
+                                         : (ms - 1) * 2 + (zp ? 1 : 0);
     if (!configured[ki][dev]) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (err != cudaSuccess) return record_launch(err);

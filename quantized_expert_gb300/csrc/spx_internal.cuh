@@ -101,6 +101,24 @@ __host__ __device__ inline size_t q2k_unit_bytes(int H) { return (size_t)(H / 25
 __host__ __device__ inline size_t q2k_units_bytes(int E, int H, int I) {
     return (size_t)E * (I / 16) * q2k_unit_bytes(H);
 }
+// GGUF Q4_K gate/up (draft launch only; S = 16; H a multiple of 256), one
+// super-block of 256 rows of a slice's two tiles in 4736 bytes:
+//   d [32] fp16, dmin [32] fp16 (tile-row order t*16 + m);
+//   sub-block scales [g 0..7][sub-block 0..7] u32, byte j = (tile j/2, row
+//     g + 8*(j%2)), 6-bit values;
+//   mins [lane][tile] u32: bytes (row g, sub-block 2c), (g, 2c+1), (g+8, 2c),
+//     (g+8, 2c+1) with c = lane%4 (the A fragment's registers 0-1, k = sub-block);
+//   codes: 8 blocks of 512 B, each 2 k-steps (32 lanes x 16 B; lane words
+//     [k-step][tile], code of register r, half h at bits 16h + 4r).
+constexpr int kQ4kScaleOff = 128;
+constexpr int kQ4kMinOff = kQ4kScaleOff + 8 * 8 * 4;
+constexpr int kQ4kCodeOff = kQ4kMinOff + 32 * 2 * 4;
+constexpr int kQ4kSbBytes = kQ4kCodeOff + 8 * 512;
+static_assert(kQ4kSbBytes == 4736, "Q4_K super-block of a slice: 4.625 bits per weight");
+__host__ __device__ inline size_t q4k_unit_bytes(int H) { return (size_t)(H / 256) * kQ4kSbBytes; }
+__host__ __device__ inline size_t q4k_units_bytes(int E, int H, int I) {
+    return (size_t)E * (I / 16) * q4k_unit_bytes(H);
+}
 __host__ __device__ inline size_t w4_colblk_offset(int E, int H, int I, int S) {
     return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
 }
@@ -340,12 +358,13 @@ struct RouteParams {
 
 constexpr int kFmtQ8 = 2;   // EngineParams::routed_fmt of GGUF Q8_0 experts
 constexpr int kFmtQ2K = 3;  // ... of GGUF Q2_K gate/up with Q8_0 down
+constexpr int kFmtQ4K = 4;  // ... of GGUF Q4_K gate/up with Q8_0 down
 struct EngineParams {
     // routed experts (packed units)
     const uint8_t *routed;
     const __half *w4_sdown;  // INT4: down scales [E][I/128][H]
     const uint8_t *w4_zeros; // INT4, nullable: repacked per-group zero points (else 8)
-    int routed_fmt;          // 0 INT4, 1 FP16, kFmtQ8 / kFmtQ2K GGUF (draft launch only)
+    int routed_fmt;          // 0 INT4, 1 FP16, kFmtQ8 / kFmtQ2K / kFmtQ4K GGUF (draft launch only)
     int S;                   // routed slice width (INT4: 16/32; FP16: 16)
     int E, I, k;
     int routed_enabled;
@@ -390,7 +409,8 @@ struct DraftRouting {
     int layer;
     int32_t *counts, *offsets, *sorted_slots, *active, *n_active;
 };
-bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1, bool q2k = false);
+// kq: GGUF K-quant gate/up (Q2_K, Q4_K): H a multiple of 256, S = 16, room for x sums
+bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1, bool kq = false);
 size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max);
 // rt == nullptr: routing from e.active / e.n_active and the token tables e.tables.
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s);

@@ -404,6 +404,91 @@ __global__ void q2k_pack_gu(const uint8_t *wg, const uint8_t *wu, int E, int H, 
     }
 }
 
+// ---------------------------------------------------------- GGUF Q4_K --
+// Canonical Q4_K matrix [out N][in K]: per row, K/256 super-blocks of 144
+// bytes (fp16 d, fp16 dmin, 12 bytes of 6-bit sub-block scales and mins, 128
+// bytes of 4-bit codes).
+__device__ __forceinline__ const uint8_t *q4k_block(const uint8_t *w, int K, size_t e, int N, int n, int sb) {
+    return w + ((e * N + n) * (K / 256) + sb) * 144;
+}
+// 6-bit scale (want_min = 0) or min (1) of sub-block s (0..7): the first four
+// sub-blocks keep theirs in the low 6 bits of bytes s / s+4; the last four
+// take 4 bits from byte s+4 (scale low nibble, min high nibble) and their top
+// 2 bits from the high bits of bytes s-4 (scale) / s (min).
+__device__ __forceinline__ uint32_t q4k_param(const uint8_t *blk, int s, int want_min) {
+    const uint8_t *b = blk + 4;
+    if (s < 4) return (uint32_t)(b[s + 4 * want_min] & 63);
+    if (!want_min) return (uint32_t)((b[s + 4] & 15) | ((b[s - 4] >> 6) << 4));
+    return (uint32_t)((b[s + 4] >> 4) | ((b[s] >> 6) << 4));
+}
+__device__ __forceinline__ uint32_t q4k_code(const uint8_t *blk, int wi) {
+    const uint8_t byte = blk[16 + 32 * (wi / 64) + wi % 32];
+    return (wi % 64) < 32 ? (byte & 15u) : (uint32_t)(byte >> 4);
+}
+
+// Gate/up units: codes, one thread per (unit, super-block, block of 2
+// k-steps, lane, word); then d/dmin, scale words and min words.
+__global__ void q4k_pack_gu(const uint8_t *wg, const uint8_t *wu, int E, int H, int I, uint8_t *packed) {
+    const int spe = I / 16, NS = H / 256;
+    const size_t npair = (size_t)E * spe * NS;
+    const size_t ub = q4k_unit_bytes(H);
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < npair * 1024;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int wd = (int)(idx & 3);  // lane word: k-step wd/2 of the block, tile wd%2
+        const int lane = (int)((idx >> 2) & 31);
+        const int c = (int)((idx >> 7) & 7);
+        const size_t us = idx >> 10;  // unit * NS + super-block
+        const int sb = (int)(us % NS);
+        const size_t unit = us / NS;
+        const size_t e = unit / spe;
+        const int jj = (int)(unit % spe);
+        const int t = wd & 1, ks = 2 * c + (wd >> 1);
+        uint32_t word = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint8_t *blk = q4k_block(t ? wu : wg, H, e, I, jj * 16 + frag_row(lane, r), sb);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) word |= q4k_code(blk, 16 * ks + frag_col(lane, r, h)) << (16 * h + 4 * r);
+        }
+        *reinterpret_cast<uint32_t *>(packed + unit * ub + (size_t)sb * kQ4kSbBytes + kQ4kCodeOff + c * 512 +
+                                      lane * 16 + wd * 4) = word;
+    }
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < npair * 160;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int item = (int)(idx % 160);
+        const size_t us = idx / 160;
+        const int sb = (int)(us % NS);
+        const size_t unit = us / NS;
+        const size_t e = unit / spe;
+        const int jj = (int)(unit % spe);
+        uint8_t *base = packed + unit * ub + (size_t)sb * kQ4kSbBytes;
+        if (item < 32) {  // d and dmin of tile item/16, row item%16
+            const uint8_t *blk = q4k_block(item < 16 ? wg : wu, H, e, I, jj * 16 + item % 16, sb);
+            reinterpret_cast<uint16_t *>(base)[item] = (uint16_t)(blk[0] | (blk[1] << 8));
+            reinterpret_cast<uint16_t *>(base)[32 + item] = (uint16_t)(blk[2] | (blk[3] << 8));
+        } else if (item < 96) {  // scales of (g, sub-block): bytes (tile j/2, row g + 8*(j%2))
+            const int g = (item - 32) / 8, s = (item - 32) % 8;
+            uint32_t w = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t *blk = q4k_block(j >> 1 ? wu : wg, H, e, I, jj * 16 + g + 8 * (j & 1), sb);
+                w |= q4k_param(blk, s, 0) << (8 * j);
+            }
+            reinterpret_cast<uint32_t *>(base + kQ4kScaleOff)[g * 8 + s] = w;
+        } else {  // mins of (lane, tile): A-fragment registers 0-1, k = sub-block
+            const int lane = (item - 96) / 2, t = (item - 96) % 2;
+            uint32_t w = 0;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint8_t *blk = q4k_block(t ? wu : wg, H, e, I, jj * 16 + frag_row(lane, r), sb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) w |= q4k_param(blk, frag_col(lane, r, h), 1) << (8 * (2 * r + h));
+            }
+            reinterpret_cast<uint32_t *>(base + kQ4kMinOff)[lane * 2 + t] = w;
+        }
+    }
+}
+
 }  // namespace spx
 
 using namespace spx;
@@ -452,8 +537,9 @@ extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, con
 extern "C" size_t spx_gguf_packed_bytes(int E, int H, int I, int gate_up_type) {
     if (E < 1 || H < 128 || I < 128 || H % 128 || I % 128) return 0;
     if (gate_up_type == SPX_GGUF_Q8_0) return q8_packed_bytes(E, H, I);
-    if (gate_up_type == SPX_GGUF_Q2_K && H % 256 == 0)
-        return q2k_units_bytes(E, H, I) + (q8_packed_bytes(E, H, I) - q8_units_bytes(E, H, I));
+    const size_t down = q8_packed_bytes(E, H, I) - q8_units_bytes(E, H, I);
+    if (gate_up_type == SPX_GGUF_Q2_K && H % 256 == 0) return q2k_units_bytes(E, H, I) + down;
+    if (gate_up_type == SPX_GGUF_Q4_K && H % 256 == 0) return q4k_units_bytes(E, H, I) + down;
     return 0;
 }
 
@@ -461,9 +547,10 @@ extern "C" int spx_gguf_repack(const uint8_t *w_gate, const uint8_t *w_up, const
                                int gate_up_type, void *packed, spx_stream_t stream) {
     if (!w_gate || !w_up || !w_down || !packed) return SPX_ERR_INVALID_ARG;
     if (E < 1 || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
-    if (gate_up_type != SPX_GGUF_Q8_0 && gate_up_type != SPX_GGUF_Q2_K) return SPX_ERR_INVALID_ARG;
+    if (gate_up_type != SPX_GGUF_Q8_0 && gate_up_type != SPX_GGUF_Q2_K && gate_up_type != SPX_GGUF_Q4_K)
+        return SPX_ERR_INVALID_ARG;
     if (H % 128 || I % 128 || H > kMaxH || E > kMaxE) return SPX_ERR_UNSUPPORTED;
-    if (gate_up_type == SPX_GGUF_Q2_K && H % 256) return SPX_ERR_UNSUPPORTED;
+    if (gate_up_type != SPX_GGUF_Q8_0 && H % 256) return SPX_ERR_UNSUPPORTED;
     if (!aligned16(packed)) return SPX_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *out = static_cast<uint8_t *>(packed);
@@ -471,9 +558,12 @@ extern "C" int spx_gguf_repack(const uint8_t *w_gate, const uint8_t *w_up, const
     if (gate_up_type == SPX_GGUF_Q8_0) {
         q8_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 128) * 512), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
         units = q8_units_bytes(E, H, I);
-    } else {
+    } else if (gate_up_type == SPX_GGUF_Q2_K) {
         q2k_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 256) * 512), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
         units = q2k_units_bytes(E, H, I);
+    } else {
+        q4k_pack_gu<<<grid_for((size_t)E * (I / 16) * (H / 256) * 1024), 256, 0, s>>>(w_gate, w_up, E, H, I, out);
+        units = q4k_units_bytes(E, H, I);
     }
     q8_pack_dn<<<grid_for((size_t)E * (H / 32) * (I / 128) * 512), 256, 0, s>>>(w_down, E, H, I, out + units);
     return record_launch(cudaGetLastError());

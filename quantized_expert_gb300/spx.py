@@ -217,7 +217,7 @@ class PackedW4:
         return W4Experts(self.buf.data_ptr(), self.E, self.H, self.I, self.S, _p(self.zeros))
 
 
-SPX_GGUF_Q8_0, SPX_GGUF_Q2_K = 0, 1
+SPX_GGUF_Q8_0, SPX_GGUF_Q2_K, SPX_GGUF_Q4_K = 0, 1, 2
 
 
 @dataclass
@@ -226,7 +226,7 @@ class PackedGguf:
     E: int
     H: int
     I: int
-    gate_up_type: int  # SPX_GGUF_Q8_0 or SPX_GGUF_Q2_K; down is Q8_0
+    gate_up_type: int  # SPX_GGUF_Q8_0, SPX_GGUF_Q2_K or SPX_GGUF_Q4_K; down is Q8_0
 
     def cstruct(self) -> GgufExperts:
         return GgufExperts(self.buf.data_ptr(), self.E, self.H, self.I, self.gate_up_type)
@@ -281,8 +281,8 @@ def spx_w4_zeros_repack(w4: PackedW4, qz_gate, qz_up, qz_down, stream=None) -> P
 
 def spx_gguf_repack(w_gate, w_up, w_down, gate_up_type=SPX_GGUF_Q8_0, stream=None) -> PackedGguf:
     """Canonical GGUF experts -> packed for the draft launch: gate, up uint8
-    [E][I][H/32][34] (Q8_0) or [E][I][H/256][84] (Q2_K); down [E][H][I/32][34]
-    (Q8_0)."""
+    [E][I][H/32][34] (Q8_0), [E][I][H/256][84] (Q2_K) or [E][I][H/256][144]
+    (Q4_K); down [E][H][I/32][34] (Q8_0)."""
     E, I, nb, bb = w_gate.shape
     H = nb * (32 if gate_up_type == SPX_GGUF_Q8_0 else 256)
     n = load().spx_gguf_packed_bytes(E, H, I, gate_up_type)

@@ -57,9 +57,9 @@ class Layer:
         self.needed = needed
         self.w4_host = {e: W.gen_w4_expert(s, layer, e) for e in needed} if (draft or s.verify_is_dequant) else {}
         self.gguf = None
-        if gguf:  # GGUF draft experts instead of INT4: "q8_0", or "q2_k" gate/up with a Q8_0 down
+        if gguf:  # GGUF draft experts instead of INT4: "q8_0", or "q2_k" / "q4_k" gate/up with a Q8_0 down
             assert draft and not zeros and not (verify and s.verify_is_dequant)
-            gen = W.gen_q8_expert if gguf == "q8_0" else W.gen_q2k_expert
+            gen = {"q8_0": W.gen_q8_expert, "q2_k": W.gen_q2k_expert, "q4_k": W.gen_q4k_expert}[gguf]
             self.w4_host = {e: gen(s, layer, e) for e in needed}
         self.zeros = zeros
         if zeros:  # asymmetric INT4: per-group zero points on every draft expert
@@ -113,14 +113,15 @@ class Layer:
     def _pack_gguf(self, kind):
         s = self.shape
         E, H, I = s.E, s.H, s.I
-        q2 = kind == "q2_k"
-        wg = np.zeros((E, I, H // 256, 84) if q2 else (E, I, H // 32, 34), np.uint8)
+        blk, pre, ty = {"q8_0": ((H // 32, 34), "q8_", spx.SPX_GGUF_Q8_0),
+                        "q2_k": ((H // 256, 84), "q2k_", spx.SPX_GGUF_Q2_K),
+                        "q4_k": ((H // 256, 144), "q4k_", spx.SPX_GGUF_Q4_K)}[kind]
+        wg = np.zeros((E, I) + blk, np.uint8)
         wu = np.zeros_like(wg)
         wd = np.zeros((E, H, I // 32, 34), np.uint8)
-        pre = "q2k_" if q2 else "q8_"
         for e, ex in self.w4_host.items():
             wg[e], wu[e], wd[e] = ex[pre + "gate"], ex[pre + "up"], ex["q8_down"]
-        p = spx.spx_gguf_repack(dev(wg), dev(wu), dev(wd), spx.SPX_GGUF_Q2_K if q2 else spx.SPX_GGUF_Q8_0)
+        p = spx.spx_gguf_repack(dev(wg), dev(wu), dev(wd), ty)
         torch.cuda.synchronize()
         return p
 

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_sizes_and_strings(lib):
     from quantized_expert_gb300 import spx
-    assert spx.spx_version() == 104
+    assert spx.spx_version() == 105
     assert spx.status_string(0) == "ok"
     assert "timed out" in spx.status_string(-5)
     # INT4 unit = 49*H*S/32 bytes; down scales copied once per expert
@@ -122,7 +122,12 @@ def test_draft_format_sizes_and_validation(lib):
     q8 = E * H * I * 34 // 32
     assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q8_0) == 3 * q8  # scales inside the 34-byte blocks
     assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q2_K) == 2 * E * H * I * 84 // 256 + q8
+    # Q4_K as packed: 4736 bytes per super-block of a 16-column slice (the 6-bit
+    # scales and mins unpacked to bytes: 148 bytes per 256 weights, 144 in the file)
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q4_K) == E * (I // 16) * (H // 256) * 4736 + q8
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q4_K) == 2 * E * H * I * 148 // 256 + q8
     assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q2_K) == 0   # Q2_K rows: multiples of 256
+    assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q4_K) == 0
     assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q8_0) == E * 384 * I * 34 // 32 * 3
     assert lib.spx_gguf_packed_bytes(E, H, I, 7) == 0
     fake = C.c_void_p(256)

@@ -639,14 +639,15 @@ def test_zero_points_unsupported_outside_the_draft_launch():
 
 
 # ------------------------------------------------------------- GGUF drafts
-@pytest.mark.parametrize("kind", ["q8_0", "q2_k"])
+@pytest.mark.parametrize("kind", ["q8_0", "q2_k", "q4_k"])
 @pytest.mark.parametrize("name,T", [("deepseek_v2_lite", 1), ("deepseek_v2_lite", 8), ("qwen15_moe", 1),
                                     ("phi35_moe", 1)])
 def test_gguf_draft_layer_full_size(name, T, kind):
     """GGUF draft experts at full size through spx_moe_layer: Q8_0 (fp16
-    scale per 32 weights, int8 codes), or Q2_K gate/up (super-blocks of 256
-    with 4-bit sub-block scales and mins, 2-bit codes) with a Q8_0 down
-    projection: routing bit-exact, output within tolerance of the oracle."""
+    scale per 32 weights, int8 codes), or Q2_K / Q4_K gate/up (super-blocks
+    of 256 with 4- / 6-bit sub-block scales and mins, 2- / 4-bit codes) with a
+    Q8_0 down projection: routing bit-exact, output within tolerance of the
+    oracle."""
     gh = _gh()
     s = W.CONFIGS[name]
     x = W.gen_x(s, T, step=100 + T)
@@ -662,7 +663,7 @@ def test_gguf_draft_layer_full_size(name, T, kind):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{kind} {name} T={T} rep {rep}")
 
 
-@pytest.mark.parametrize("kind", ["q8_0", "q2_k"])
+@pytest.mark.parametrize("kind", ["q8_0", "q2_k", "q4_k"])
 @pytest.mark.parametrize("case", [1, 2, 4])
 def test_gguf_draft_unit_call(case, kind):
     """spx_moe_draft_gguf on the small cases of at most 8 tokens with
@@ -686,11 +687,11 @@ def test_gguf_draft_unit_call(case, kind):
     assert spx.spx_workspace_status(ws) == 0
 
 
-@pytest.mark.parametrize("kind", ["q8_0", "q2_k"])
+@pytest.mark.parametrize("kind", ["q8_0", "q2_k", "q4_k"])
 def test_gguf_draft_ragged_ranges(kind):
-    """Ragged item ranges: H = 1536 is 6 Q2_K super-blocks (items of 4 + 2) or
-    12 Q8_0 groups (3 + 3 + 3 + 3); I = 384 is one Q8_0 down range of 3 groups
-    and 24 slices; T = 3 tokens over 8 experts, k = 2."""
+    """Ragged item ranges: H = 1536 is 6 super-blocks (Q2_K items of 4 + 2,
+    Q4_K items of 3 + 3) or 12 Q8_0 groups (3 + 3 + 3 + 3); I = 384 is one
+    Q8_0 down range of 3 groups and 24 slices; T = 3 tokens over 8 experts."""
     spx, gh = _spx(), _gh()
     s = _small("phi35_moe", H=1536, I=384, E=8, k=2)
     T = 3
@@ -750,4 +751,5 @@ def test_gguf_unsupported_and_invalid_calls():
         spx.spx_moe_layer(args, None)
     assert ei.value.status == spx.SPX_ERR_INVALID_ARG
     assert spx.load().spx_gguf_packed_bytes(4, 384, 256, spx.SPX_GGUF_Q2_K) == 0   # H not a multiple of 256
+    assert spx.load().spx_gguf_packed_bytes(4, 384, 256, spx.SPX_GGUF_Q4_K) == 0
     assert spx.load().spx_gguf_packed_bytes(4, 384, 256, spx.SPX_GGUF_Q8_0) > 0
