@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libspx.so")
 SOURCES = ["spx_route.cu", "spx_engine.cu", "spx_draft.cu", "spx_pack.cu", "spx_api.cu", "spx_noalloc.cu"]
-HEADERS = ["spx_internal.cuh", os.path.join("..", "..", "include", "spx.h")]
+# every header of csrc/ and the public one: a change to any rebuilds every source
+HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith(".cuh")) + [os.path.join("..", "..", "include", "spx.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
