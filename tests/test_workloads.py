@@ -63,3 +63,31 @@ def test_verify_logits_reuse_draft_steps():
     assert v.shape == (s.K + 1, s.E)
     for i in range(1, s.K + 1):
         assert np.array_equal(v[i - 1], W.draft_logits(s, 5, i)[0])
+
+
+def test_other_draft_format_generators():
+    """Zero points and GGUF experts: shapes, determinism, independent streams
+    and the scale ranges the recipe states (read back through the format's
+    byte layout, not through the oracle)."""
+    s = W.scaled(W.CONFIGS["tiny"], H=512, I=256)
+    z = W.gen_w4_zeros(s, 0, 1)
+    assert z["qz_gate"].shape == (s.H // 128, s.I // 8) and z["qz_down"].shape == (s.I // 128, s.H // 8)
+    nib = (z["qz_gate"].view(np.uint32)[..., None] >> (4 * np.arange(8, dtype=np.uint32))) & 15
+    assert set(np.unique(nib)) == set(range(16))
+    q8 = W.gen_q8_expert(s, 0, 1)
+    assert q8["q8_gate"].shape == (s.I, s.H // 32, 34) and q8["q8_down"].shape == (s.H, s.I // 32, 34)
+    d = q8["q8_gate"][..., :2].copy().view(np.float16).astype(np.float64)
+    assert d.min() >= 0.0003 - 1e-6 and d.max() <= 0.00125 + 1e-6
+    q2 = W.gen_q2k_expert(s, 0, 1)
+    assert q2["q2k_gate"].shape == (s.I, s.H // 256, 84) and q2["q8_down"].shape == (s.H, s.I // 32, 34)
+    d2 = q2["q2k_up"][..., 80:82].copy().view(np.float16).astype(np.float64)
+    m2 = q2["q2k_up"][..., 82:84].copy().view(np.float16).astype(np.float64)
+    assert d2.min() >= 0.001 - 1e-6 and d2.max() <= 0.003 + 1e-6 and m2.max() <= 0.004 + 1e-6
+    q4 = W.gen_q4k_expert(s, 0, 1)
+    assert q4["q4k_gate"].shape == (s.I, s.H // 256, 144)
+    d4 = q4["q4k_gate"][..., 0:2].copy().view(np.float16).astype(np.float64)
+    assert d4.min() >= 0.00015 - 1e-7 and d4.max() <= 0.0004 + 1e-6
+    for gen in (W.gen_w4_zeros, W.gen_q8_expert, W.gen_q2k_expert, W.gen_q4k_expert):
+        a, b, c = gen(s, 0, 2), gen(s, 0, 2), gen(s, 0, 3)
+        assert all(np.array_equal(a[k], b[k]) for k in a)
+        assert not all(np.array_equal(a[k], c[k]) for k in a)
