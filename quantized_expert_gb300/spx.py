@@ -318,6 +318,8 @@ def pack_shared(w_gate, w_up, w_down, w_sgate=None, stream=None) -> PackedShared
 
 
 def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+    """INT4 draft experts on gathered tokens: y_sorted [T*k][H] fp32, one row per
+    sorted slot (the gather arrays come from spx_gather_by_expert)."""
     T = x.shape[0]
     cs = w.cstruct()
     _chk(load().spx_moe_draft_w4a16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
@@ -326,6 +328,7 @@ def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_acti
 
 
 def spx_moe_draft_gguf(x, w: PackedGguf, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+    """spx_moe_draft_w4a16 with GGUF draft experts (T <= 8)."""
     T = x.shape[0]
     cs = w.cstruct()
     _chk(load().spx_moe_draft_gguf(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
@@ -334,6 +337,8 @@ def spx_moe_draft_gguf(x, w: PackedGguf, k, offsets, sorted_slots, active, n_act
 
 
 def spx_moe_verify_fp16(x, w: PackedF16, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
+    """FP16 verify experts on gathered tokens (each expert's weights read once
+    for all of its tokens); output as spx_moe_draft_w4a16."""
     T = x.shape[0]
     cs = w.cstruct()
     _chk(load().spx_moe_verify_fp16(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),
