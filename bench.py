@@ -53,6 +53,18 @@ def traffic_of(which):
     return None if t is None else t["dram_bytes"]
 
 
+def spread_us(ms_list):
+    """p10 / median / p90 of per-call times given in ms, in us (nearest rank)."""
+    v = sorted(ms_list)
+    if not v:
+        return {"p10": None, "median": None, "p90": None}
+
+    def rank(q):
+        return v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))] * 1e3
+
+    return {"p10": round(rank(0.1), 2), "median": round(statistics.median(v) * 1e3, 2), "p90": round(rank(0.9), 2)}
+
+
 def job_throughput(tot_bytes, ms_total, device=None):
     """Whole-job GB/s: the bytes every rank processed over the slowest rank's
     device time (max over ranks), and that time in ms.  One process when
@@ -440,7 +452,8 @@ def run_mine(args):
                    "verify_us": round(v_us, 2), "verify_gbs": round(v_bytes / (v_us * 1e-6) / 1e9, 1),
                    "verify_frac": round(v_bytes / (v_us * 1e-6) / 1e9 / peak, 3),
                    "verify_tokens_per_s": round(Tv / (v_us * 1e-6), 1),
-                   "draft_bytes": int(d_bytes), "verify_bytes": int(v_bytes)},
+                   "draft_bytes": int(d_bytes), "verify_bytes": int(v_bytes),
+                   "draft_us_spread": spread_us(d_ms), "verify_us_spread": spread_us(v_ms)},
         "roofline": {"bound": "hbm", "kernel": "engine_kernel<1,1,3> (verify expert launch, FP16 experts)",
                      "achieved": round(kv_bytes / (kv_us * 1e-6) / 1e9, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",

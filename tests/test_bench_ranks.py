@@ -48,3 +48,12 @@ def test_single_process_is_its_own_job():
     import bench
     value, t = bench.job_throughput(6.0e9, 100.0)
     assert t == 100.0 and value == pytest.approx(60.0)
+
+
+def test_spread_of_per_call_times():
+    import bench
+    ms = [0.010 * (i + 1) for i in range(11)]  # 10 .. 110 us
+    st = bench.spread_us(ms)
+    assert st == {"p10": 20.0, "median": 60.0, "p90": 100.0}
+    assert bench.spread_us([0.025]) == {"p10": 25.0, "median": 25.0, "p90": 25.0}
+    assert bench.spread_us([])["median"] is None
