@@ -12,13 +12,14 @@ the steps in the order the pages give them:
 
 Sources (page title + section): ai.info summary "Specter: Fast MoE Inference
 via Quantization-Enabled Multi-Step Speculative Offloading", Key
-Contributions 1-4 and "Methodology in Plain English"; richland.au "Specter
-previews expert routing with an INT4 copy of the model itself", "What
-shipped".
+Contributions 1-4, "Methodology in Plain English" and Main Findings (drafts
+quantised by GPTQ, AWQ and GGUF at Q2, Q4 and Q8: the zero-point and GGUF
+expert formats); richland.au "Specter previews expert routing with an INT4
+copy of the model itself", "What shipped".
 
-Parity status: every step has a pin in ``tests/test_oracle_*.py`` (closed
-forms, brute force, invariants, library routines); see the design notes for
-the list.
+Parity status: every step has a pin in ``tests/test_oracle_pins.py`` (closed
+forms, brute force, invariants, library routines, hand-derived format
+fixtures under ``tests/golden/``); the design notes list them.
 """
 from __future__ import annotations
 
