@@ -801,6 +801,107 @@ def run_draft_batch(args):
     print(json.dumps(line), flush=True)
 
 
+TL_EVENTS = ["entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "gu_last", "dn_w_first",
+             "dn_h_first", "dn_last", "prod_last", "cons_done", "out_done", "sg_last", "rg_first", "rg_last",
+             "w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "exit", "rd_h_last", "sd_last",
+             "w_poll", "bytes"]
+TL_FIRST_EV = {"entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "dn_w_first",
+               "dn_h_first", "cons_done", "rg_first"}
+TL_SUM_EV = {"w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "w_poll", "bytes"}
+
+
+def timeline_phases(buf, slots, nblocks):
+    """Per-phase table of draft launches from the profiling build's marks
+    (buf [slots][blocks][events] uint64): for each mark the earliest, median
+    and latest block in us after the launch's first block entered; sums per
+    block.  Averaged over the given slots."""
+    acc = {}
+    for sl in slots:
+        b = buf[sl, :nblocks, :].astype(np.uint64)
+        t = {}
+        for j, nm in enumerate(TL_EVENTS):
+            col = b[:, j]
+            if nm in TL_SUM_EV:
+                t[nm] = col.astype(np.float64)
+            elif nm in TL_FIRST_EV:
+                t[nm] = np.where(col != 0, (~col).astype(np.float64), np.nan)
+            else:
+                t[nm] = np.where(col != 0, col.astype(np.float64), np.nan)
+        t0 = np.nanmin(t["entry"])
+        for nm in TL_EVENTS:
+            v = t[nm]
+            if nm in TL_SUM_EV:
+                row = {"per_block_mean": float(np.mean(v)), "total": float(np.sum(v))}
+            else:
+                r = (v - t0) / 1e3
+                r = r[~np.isnan(r)]
+                if r.size == 0:
+                    continue
+                row = {"min": float(r.min()), "median": float(np.median(r)), "max": float(r.max()), "blocks": int(r.size)}
+            for k2, v2 in row.items():
+                acc.setdefault(nm, {}).setdefault(k2, []).append(v2)
+        acc.setdefault("_t0", []).append(t0)
+    out = {nm: {k2: round(float(np.mean(v2)), 3) for k2, v2 in d.items()} for nm, d in acc.items() if nm != "_t0"}
+    t0s = acc["_t0"]
+    if len(t0s) > 1:
+        out["launch_period_us"] = round(float(np.mean(np.diff(t0s))) / 1e3, 3)
+    return out
+
+
+def run_timeline(args):
+    """Phase marks of the draft launch at T = 1 (profiling build with
+    %globaltimer marks; timings of that build are not bench values): 8 launches
+    each alone (synchronised between them), then 8 back to back.  Prints one
+    JSON line with the per-phase table of both."""
+    import ctypes as C
+    import torch
+    from quantized_expert_gb300 import build as B, spx
+    lib = spx.load(B.build(variant="timeline"))
+    lib.spx_timeline_reset.restype = C.c_int
+    lib.spx_timeline_read.restype = C.c_int
+    lib.spx_timeline_read.argtypes = [C.c_void_p, C.c_size_t]
+    s = W.CONFIGS[args.config]
+    T = s.T_draft
+    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
+    xs = [torch.from_numpy(np.ascontiguousarray(W.gen_x(s, T, step=i)).view(np.float16)).cuda() for i in range(NINPUTS)]
+    lgs = [torch.from_numpy(W.gen_logits(s, T, step=i)).cuda() if s.logits != "router"
+           else torch.empty(T, s.E, device="cuda") for i in range(NINPUTS)]
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    r = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    keep = [spx.layer_args(0, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, out, ws,
+                           w4=sets[i % NSETS]["w4"], shared=sets[i % NSETS]["shared"],
+                           w_router=sets[i % NSETS]["w_router"]) for i in range(NSETS * NINPUTS)]
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    stream = torch.cuda.Stream()
+    buf = np.zeros((8, 256, 32), np.uint64)
+
+    def read():
+        torch.cuda.synchronize()
+        assert lib.spx_timeline_read(buf.ctypes.data, buf.size) == 0
+        return buf.copy()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            spx.spx_moe_layer(keep[i % len(keep)][0], stream)
+        torch.cuda.synchronize()
+        assert lib.spx_timeline_reset() == 0
+        for i in range(8):
+            spx.spx_moe_layer(keep[i][0], stream)
+            torch.cuda.synchronize()
+        iso = read()
+        assert lib.spx_timeline_reset() == 0
+        for i in range(8):
+            spx.spx_moe_layer(keep[8 + i][0], stream)
+        chained = read()
+    assert spx.spx_workspace_status(ws) == 0
+    line = {"timeline": "draft launch phase marks (profiling build; us after the launch's first block entered)",
+            "config": {"workload": f"{s.name} draft T={T}", "blocks": nsm},
+            "isolated": timeline_phases(iso, range(8), nsm),
+            "chained": timeline_phases(chained, range(1, 8), nsm)}
+    print(json.dumps(line), flush=True)
+
+
 def oracle_free_topk(lg, k):
     """Top-k expert ids of fp32 logits (value descending, index ascending), for
     choosing the resident set; no method arithmetic beyond the ordering."""
@@ -825,9 +926,13 @@ def main():
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
     ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
     ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"], help="with --draft-batch: GGUF experts instead of INT4")
+    ap.add_argument("--timeline", action="store_true",
+                    help="draft launch phase marks from the profiling build (prints its own line)")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
-    if args.loop:
+    if args.timeline:
+        run_timeline(args)
+    elif args.loop:
         run_loop(args)
     elif args.cached:
         run_cached(args)

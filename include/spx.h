@@ -363,14 +363,30 @@ SPX_API int spx_moe_layer(const spx_layer_args *args, spx_stream_t stream);
  * inside the library image, present on every GPU that loads the library until
  * the process exits.  Shapes whose spx_workspace_size(T, H, I, E, k, I_s)
  * exceeds 1 MiB are rejected with SPX_ERR_WORKSPACE (the DeepSeek-V2-Lite-
- * shaped layer fits at T = 1 and T = 17).  The call itself allocates nothing.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array: the call clears the part that must
- * start at zero, and calls that can overlap on the GPU (two streams, two host
- * threads) race on it.  The device-side status word is cleared by each call and
- * is not reported. */
+ * shaped layer fits at T = 1 and T = 17).  The call allocates nothing, provided
+ * spx_noalloc_init() has run on the current device first; on a device where it
+ * has not, the call returns SPX_ERR_WORKSPACE and enqueues nothing.  Arguments
+ * are checked before anything is enqueued; then the call clears the part of
+ * the array that must start at zero.  Every call shares the one array, which
+ * keeps the last call's contents, so calls that can overlap on the GPU (two
+ * streams, two host threads) race on it.  A bounded device-side wait that
+ * gives up is reported in the array's status word: read it with
+ * spx_noalloc_status() after the call, before the next one. */
 SPX_API int spx_moe_layer_noalloc(const spx_layer_args *args, spx_stream_t stream);
+/* Set-up of spx_moe_layer_noalloc for the current device, once per device at
+ * start-up, before any stream capture: loads every kernel the layer call can
+ * launch and the fixed scratch array onto the device (this allocates device
+ * memory for the library's code and the array, which is why it is a call of
+ * its own) and looks up the array's address.  Later calls on the device
+ * return SPX_OK at once.  After cudaDeviceReset, call it again.  No
+ * counterpart in the paper. */
+SPX_API int spx_noalloc_init(void);
+/* Asynchronously copy the fixed scratch array's status word (SPX_OK or
+ * SPX_ERR_TIMEOUT) of the current device into *status (page-locked host
+ * memory or device memory), ordered on `stream` after the layer calls before
+ * it; SPX_ERR_WORKSPACE if spx_noalloc_init has not run on the device.  No
+ * counterpart in the paper. */
+SPX_API int spx_noalloc_status(int32_t *status, spx_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -3,6 +3,11 @@
 Each .cu file is compiled to an object in parallel, then linked into a shared
 library against the shared CUDA runtime (so the process keeps a single
 runtime instance alongside PyTorch).  Output: ``_build/libspx.so``.
+
+``build(variant="timeline")`` builds the profiling library
+``_build/timeline/libspx_timeline.so`` instead: the same sources with
+``-DSPX_TIMELINE``, whose draft launch records %globaltimer phase marks
+(``spx_timeline_reset`` / ``spx_timeline_read``).  The product never loads it.
 """
 from __future__ import annotations
 
@@ -16,6 +21,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libspx.so")
+VARIANTS = {None: (BUILD, LIB, []),
+            "timeline": (os.path.join(BUILD, "timeline"), os.path.join(BUILD, "timeline", "libspx_timeline.so"),
+                         ["-DSPX_TIMELINE"])}
 SOURCES = ["spx_route.cu", "spx_engine.cu", "spx_draft.cu", "spx_pack.cu", "spx_api.cu", "spx_noalloc.cu"]
 # every header of csrc/ and the public one: a change to any rebuilds every source
 HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith(".cuh")) + [os.path.join("..", "..", "include", "spx.h")]
@@ -38,20 +46,21 @@ def _stale(out: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, variant: str | None = None) -> str:
+    bdir, lib, extra = VARIANTS[variant]
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS]
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         if force or _stale(o, [s] + hdrs):
-            cmd = [cc, *ARCH, *FLAGS, "-c", s, "-o", o]
+            cmd = [cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o]
             if ptxas_info:
                 cmd += ["-Xptxas", "-v"]
             jobs.append((src, cmd))
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
 
     def run(job):
         name, cmd = job
@@ -65,16 +74,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     sys.stderr.write(out)
                 if rc != 0:
                     raise RuntimeError(f"nvcc failed on {name}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart=shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link of libspx.so failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                variant="timeline" if "--timeline" in sys.argv else None))

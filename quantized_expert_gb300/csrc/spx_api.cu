@@ -284,6 +284,10 @@ extern "C" int spx_combine(const float *y_sorted, const int32_t *sorted_slots, c
 }
 
 extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
+    return moe_layer(a, reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
+}
+
+int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t clear_bytes) {
     if (!a) return SPX_ERR_INVALID_ARG;
     const int T = a->T, H = a->H, E = a->E, k = a->k;
     int st = route_validate(a->x, a->w_router, a->logits, T, H, E, k, a->topk_ids, a->topk_w);
@@ -321,7 +325,6 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     st = check_shared(a->shared, H);
     if (st) return st;
     if (reinterpret_cast<uintptr_t>(a->out) & 7) return SPX_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool timed = a->ev_experts_begin || a->ev_experts_end;
     const bool cache_aware = a->resident || a->ready;
     const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
@@ -329,6 +332,11 @@ extern "C" int spx_moe_layer(const spx_layer_args *a, spx_stream_t stream) {
     const bool zeros = a->mode == 0 && !gguf && a->w4->zeros;
     const bool kq = gguf && (gguf_fmt(a->gguf) == kFmtQ2K || gguf_fmt(a->gguf) == kFmtQ4K);
     if ((zeros || gguf) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k, kq))) return SPX_ERR_UNSUPPORTED;
+    // every check has passed: only now may the caller's scratch be cleared
+    if (clear) {
+        const cudaError_t ce = cudaMemsetAsync(clear, 0, clear_bytes, s);
+        if (ce != cudaSuccess) return record_launch(ce);
+    }
     if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k, kq)) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch

@@ -33,8 +33,11 @@
 #include "spx_internal.cuh"
 #include "spx_routing.cuh"
 #include "spx_draft_gguf.cuh"
+#include "spx_timeline.cuh"
 
 #include <math.h>
+
+#include <atomic>
 
 namespace spx {
 
@@ -91,7 +94,7 @@ struct DPend {
     const int *rdy;
     int target;
     uint32_t bytes;
-    uint32_t pad[2];
+    unsigned long long t_reg;  // profiling build: when the producer registered it
 };
 
 struct DkGeom {
@@ -244,6 +247,7 @@ struct DkParams {
     int *rdy_s, *rdy_r;
     int nact_max, nstages;
     uint64_t wait_budget_ns;
+    int tl_slot;  // profiling build: slot of this launch's phase marks
 };
 
 // Like mbar_try_wait, but the thread may sleep up to `ns` in the wait (it
@@ -339,10 +343,13 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                      const int *rdy, int target, const void *zsrc = nullptr, uint32_t zbytes = 0,
                      uint32_t zoff = 0) -> bool {
         const int st = (int)(it % nst);
+        const unsigned long long tw = TL_NOW();
         if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
             ok = false;
             return false;
         }
+        TL_ADD(p.tl_slot, TL_W_EMPTY, TL_NOW() - tw);
+        TL_ADD(p.tl_slot, TL_BYTES, bytes + zbytes);
         h.seq = (int)it;
         h.hpar = (int)((hpar_bits >> st) & 1u);
         hdrs[st] = h;
@@ -357,6 +364,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             pend[st].rdy = rdy;
             pend[st].target = target;
             pend[st].bytes = hs_bytes;
+            pend[st].t_reg = TL_NOW();
             __threadfence_block();
             pstate[st] = 1;
         }
@@ -490,7 +498,9 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     // this thread waits for it; the counters come after.
     uint32_t tkA = blockIdx.x / kDkShards;
     const bool more = run_unit((int)tkA * kDkShards + shard);
+    TL_FIRST(p.tl_slot, TL_PROD_STATIC);
     griddep_wait();
+    TL_FIRST(p.tl_slot, TL_PROD_GRIDDEP);
     if (more) {
         uint32_t tkB = nsm + atomicAdd(ctr, 1u);
         while (true) {
@@ -501,6 +511,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         }
     }
     if (ok) {
+        TL_LAST(p.tl_slot, TL_PROD_LAST);
         __threadfence_block();
         misc[3] = 1;  // no more h copies to register
         for (int w = 0; w < kDkCons; ++w) {  // one end marker per consumer warp
@@ -586,6 +597,7 @@ __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
                     any = true;
                 }
                 bulk_g2s_plain(ring + (size_t)j * L.stage + L.hs_off, pend[j].src, pend[j].bytes, &hfull[j]);
+                TL_ADD(p.tl_slot, TL_W_POLL, TL_NOW() - pend[j].t_reg);
                 issued |= 1u << j;
                 ipar = (ipar & ~(1u << j)) | ((uint32_t)hdrs[j].hpar << j);
                 pstate[j] = 0;
@@ -771,6 +783,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
     griddep_launch_dependents();
+    if (threadIdx.x == 0) TL_FIRST(p.tl_slot, TL_ENTRY);
     const int nst = p.nstages;
     const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E, Q2K || Q4K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -856,6 +869,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         if ((lane & 15) == 0 && idx < T * (H / 8)) sxs[idx / 16] = sum;  // [t][group]: idx/16 = t*(H/128) + group
     }
     all_sync();  // x is in shared memory
+    if (ctid == 0) TL_FIRST(p.tl_slot, TL_X_STAGED);
     // Routing: warps t < T select token t (every block the same way; block 0
     // also writes the routing outputs); the last of them builds the token
     // tables and raises misc[4].  The other warps go straight to the shared
@@ -866,6 +880,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             misc[5] = na;
             __threadfence_block();
             *reinterpret_cast<volatile int *>(misc + 4) = 1;
+            TL_FIRST(p.tl_slot, TL_ROUTED);
         }
     };
     if (sel_all) {
@@ -1007,6 +1022,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         // landed yet; a parity wait cannot tell those two phases apart, so the
         // fill is accepted only when its header carries this ticket.
         bool got = false;
+        const unsigned long long twf = TL_NOW();
         {
             const uint32_t par = (uint32_t)(idx / nst) & 1;
             const volatile int *seqp = &hdrs[st].seq;
@@ -1026,6 +1042,12 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         }
         if (!got) break;
         const DHeader h = hdrs[st];
+        if (TL_ON && lane == 0) {
+            TL_ADD(p.tl_slot, TL_W_FULL, TL_NOW() - twf);
+            TL_FIRST(p.tl_slot, TL_FIRST_FILL);
+            if (h.kind == DK_SD || h.kind == DK_RD) TL_FIRST(p.tl_slot, TL_DN_W_FIRST);
+            if (h.kind == DK_RG) TL_FIRST(p.tl_slot, TL_RG_FIRST);
+        }
         const uint8_t *stage = ring + (size_t)st * L.stage;
         if (h.kind == DK_DONE) {
             // release it too: with fewer stages than warps the end markers reuse stages
@@ -1038,8 +1060,14 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         const uint2 *hsl = reinterpret_cast<const uint2 *>(stage + L.hs_off);
         if (h.kind == DK_SD || h.kind == DK_RD) {
             // the intermediate slice lands after the weights (poller's copy)
+            const unsigned long long twh = TL_NOW();
             if (!mbar_wait_sleep_bounded(&hfull[st], (uint32_t)h.hpar, abort_flag, &p.hdr->status, p.wait_budget_ns))
                 break;
+            if (TL_ON && lane == 0) {
+                TL_ADD(p.tl_slot, TL_W_HFULL, TL_NOW() - twh);
+                TL_FIRST(p.tl_slot, TL_DN_H_FIRST);
+                if (h.kind == DK_RD) TL_LAST(p.tl_slot, TL_RD_H_LAST);
+            }
         }
         if (h.kind == DK_SG) {
             // shared gate/up: 16 columns (tiles: gate, up), k-steps [k0, k0+n) of H
@@ -1077,6 +1105,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 }
             }
             gu_done(h, 1, p.hf_s + (size_t)h.blk * T * 4, 0, p.rdy_s + h.blk / kDkSdSteps, 1);
+            if (TL_ON && lane == 0) {
+                TL_LAST(p.tl_slot, TL_SG_LAST);
+                TL_LAST(p.tl_slot, TL_GU_LAST);
+                TL_ADD(p.tl_slot, TL_N_SG, 1);
+            }
             continue;
         }
         if (h.kind == DK_RG) {
@@ -1172,6 +1205,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             }
             gu_done(h, MS, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.blk * MS) * T * 4, (size_t)T * 4,
                     p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / geo.rd_gpi, MS);
+            if (TL_ON && lane == 0) {
+                TL_LAST(p.tl_slot, TL_RG_LAST);
+                TL_LAST(p.tl_slot, TL_GU_LAST);
+                TL_ADD(p.tl_slot, TL_N_RG, 1);
+            }
             continue;
         }
         if (h.kind == DK_SD) {
@@ -1217,6 +1255,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                     o.w = (acc[0][1][2 + hf] + acc[1][1][2 + hf]) * w;
                     atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)col * H + n0), o);
                 }
+            }
+            if (TL_ON && lane == 0) {
+                TL_LAST(p.tl_slot, TL_SD_LAST);
+                TL_LAST(p.tl_slot, TL_DN_LAST);
+                TL_ADD(p.tl_slot, TL_N_SD, 1);
             }
             continue;
         }
@@ -1306,12 +1349,17 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                     atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)row[hf] * H + n0), o);
                 }
             }
+            if (TL_ON && lane == 0) {
+                TL_LAST(p.tl_slot, TL_DN_LAST);
+                TL_ADD(p.tl_slot, TL_N_RD, 1);
+            }
         }
     }
 
     // completion ticket; the last block writes the fp16 output and resets
     __threadfence();  // this thread's output additions, before the block counts as done
     all_sync();
+    if (ctid == 0) TL_FIRST(p.tl_slot, TL_CONS_DONE);
     if (ctid == 0) {
         __threadfence();
         const uint32_t t = atomicAdd(&p.hdr->done_ticket, 1u);
@@ -1350,10 +1398,56 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         if (ctid < kDkShards) p.qctr[64 * ctid] = 0;
         if (ctid == 0) p.hdr->done_ticket = 0;
         __threadfence();
+        if (ctid == 0) TL_LAST(p.tl_slot, TL_OUT_DONE);
     }
+    if (ctid == 0) TL_LAST(p.tl_slot, TL_EXIT);
 }
 
 // ------------------------------------------------------------ launching --
+#if TL_ON
+static std::atomic<int> g_tl_next{0};
+#endif
+
+// The launch's template instances, indexed as launch_draft picks them.
+using DraftKernel = void (*)(const DkParams);
+static DraftKernel draft_instance(int ki) {
+    switch (ki) {
+    case 0: return draft_kernel<1, DK_FMT_W4>;
+    case 1: return draft_kernel<1, DK_FMT_W4Z>;
+    case 2: return draft_kernel<2, DK_FMT_W4>;
+    case 3: return draft_kernel<2, DK_FMT_W4Z>;
+    case 4: return draft_kernel<1, DK_FMT_Q8>;
+    case 5: return draft_kernel<1, DK_FMT_Q2K>;
+    case 6: return draft_kernel<1, DK_FMT_Q4K>;
+    default: return nullptr;
+    }
+}
+constexpr int kDraftInstances = 7;
+
+// Loads instance ki on the current device and raises its dynamic shared-memory
+// limit, once per device.
+static int configure_draft(int ki) {
+    static int configured[kDraftInstances][64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
+    if (ki < 0 || ki >= kDraftInstances) return SPX_ERR_UNSUPPORTED;
+    if (!configured[ki][dev]) {
+        cudaError_t err =
+            cudaFuncSetAttribute(draft_instance(ki), cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (err != cudaSuccess) return record_launch(err);
+        configured[ki][dev] = 1;
+    }
+    return SPX_OK;
+}
+
+int draft_preload() {
+    for (int ki = 0; ki < kDraftInstances; ++ki) {
+        const int st = configure_draft(ki);
+        if (st) return st;
+    }
+    return SPX_OK;
+}
+
 size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max) {
     return dk_scratch(base, T, H, I, I_s, nact_max).end;
 }
@@ -1401,6 +1495,9 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.out = e.out;
     p.hdr = e.hdr;
     p.wait_budget_ns = e.wait_budget_ns;
+#if TL_ON
+    p.tl_slot = g_tl_next.fetch_add(1) % kTlSlots;
+#endif
     p.nact_max = e.E < e.T * e.k ? e.E : e.T * e.k;
     if (rt) {
         p.logits = rt->logits;
@@ -1429,28 +1526,17 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.nstages = nst;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    static int configured[7][64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
     const int ms = e.S / 16;
     const bool gguf = p.fmt == DK_FMT_Q8 || kq;
     if (gguf && (ms != 1 || zp)) return SPX_ERR_UNSUPPORTED;
     if (kq && e.H % 256) return SPX_ERR_UNSUPPORTED;
-    void (*kern)(const DkParams) =
-        p.fmt == DK_FMT_Q8    ? draft_kernel<1, DK_FMT_Q8>
-        : p.fmt == DK_FMT_Q2K ? draft_kernel<1, DK_FMT_Q2K>
-        : p.fmt == DK_FMT_Q4K ? draft_kernel<1, DK_FMT_Q4K>
-        : ms == 2             ? (zp ? draft_kernel<2, DK_FMT_W4Z> : draft_kernel<2, DK_FMT_W4>)
-                              : (zp ? draft_kernel<1, DK_FMT_W4Z> : draft_kernel<1, DK_FMT_W4>);
     const int ki = p.fmt == DK_FMT_Q8    ? 4
                    : p.fmt == DK_FMT_Q2K ? 5
                    : p.fmt == DK_FMT_Q4K ? 6
                                          : (ms - 1) * 2 + (zp ? 1 : 0);
-    if (!configured[ki][dev]) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-        if (err != cudaSuccess) return record_launch(err);
-        configured[ki][dev] = 1;
-    }
+    const int cst = configure_draft(ki);
+    if (cst) return cst;
+    const DraftKernel kern = draft_instance(ki);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
     cfg.blockDim = dim3(kDkThreads);
@@ -1466,3 +1552,19 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
 }
 
 }  // namespace spx
+
+#if TL_ON
+// Profiling build only: clear every slot of phase marks (the next draft launch
+// writes slot 0), and copy them out ([kTlSlots][kTlBlocks][kTlEvents] words).
+extern "C" __attribute__((visibility("default"))) int spx_timeline_reset(void) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, spx::g_tl) != cudaSuccess) return SPX_ERR_CUDA;
+    if (cudaMemset(p, 0, sizeof(spx::g_tl)) != cudaSuccess) return SPX_ERR_CUDA;
+    spx::g_tl_next.store(0);
+    return SPX_OK;
+}
+extern "C" __attribute__((visibility("default"))) int spx_timeline_read(unsigned long long *host, size_t words) {
+    if (!host || words < sizeof(spx::g_tl) / 8) return SPX_ERR_INVALID_ARG;
+    return cudaMemcpyFromSymbol(host, spx::g_tl, sizeof(spx::g_tl)) == cudaSuccess ? SPX_OK : SPX_ERR_CUDA;
+}
+#endif

@@ -974,6 +974,22 @@ static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, i
     return false;
 }
 
+// Loads the kernel instance on the current device and raises its dynamic
+// shared-memory limit, once per device.
+template <int RFMT, int MS4, int NT>
+static int configure_engine() {
+    static int configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(engine_kernel<RFMT, MS4, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return record_launch(e);
+        configured[dev] = 1;
+    }
+    return SPX_OK;
+}
+
 template <int RFMT, int MS4, int NT>
 static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     EngineParams p = p0;
@@ -986,15 +1002,8 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     p.groups = G;
     p.nstages = nsg;
     p.chunk = chunk;
-    static int configured[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPX_ERR_CUDA;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(engine_kernel<RFMT, MS4, NT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-        if (e != cudaSuccess) return record_launch(e);
-        configured[dev] = 1;
-    }
+    const int st = configure_engine<RFMT, MS4, NT>();
+    if (st) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms);
     cfg.blockDim = dim3(kThreads);
@@ -1023,6 +1032,21 @@ int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
     if (nt == 1) return launch_engine_t<FMT_F16, 1, 1>(p, s, pdl);
     if (nt == 3) return launch_engine_t<FMT_F16, 1, 3>(p, s, pdl);
     return launch_engine_t<FMT_F16, 1, 8>(p, s, pdl);
+}
+
+int engine_preload() {
+    int st = SPX_OK;
+    if (!st) st = configure_engine<FMT_W4, 2, 1>();
+    if (!st) st = configure_engine<FMT_W4, 2, 3>();
+    if (!st) st = configure_engine<FMT_W4, 1, 1>();
+    if (!st) st = configure_engine<FMT_W4, 1, 3>();
+    if (!st) st = configure_engine<FMT_W4, 1, 8>();
+    if (!st) st = configure_engine<FMT_F16, 1, 1>();
+    if (!st) st = configure_engine<FMT_F16, 1, 3>();
+    if (!st) st = configure_engine<FMT_F16, 1, 8>();
+    cudaFuncAttributes fa;
+    if (!st) st = record_launch(cudaFuncGetAttributes(&fa, tables_kernel));
+    return st;
 }
 
 int engine_fits(int T, int H, int fmt, int S) {

@@ -422,5 +422,13 @@ int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int
 // -------------------------------------------------------- host helpers --
 int device_sm_count();
 int record_launch(cudaError_t e);
+// Load every kernel the layer call can launch on the current device (and set
+// its shared-memory limit), so that later launches load no code.
+int route_preload();
+int engine_preload();
+int draft_preload();
+// The layer call: validates every argument, then (clear != nullptr) zeroes
+// clear_bytes of `clear` on the stream, then enqueues the launches.
+int moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t clear_bytes);
 
 }  // namespace spx

@@ -288,6 +288,13 @@ int launch_route(const RouteParams &p, cudaStream_t s, bool pdl) {
     return record_launch(cudaLaunchKernelEx(&cfg, route_kernel, p));
 }
 
+int route_preload() {
+    cudaFuncAttributes fa;
+    int st = record_launch(cudaFuncGetAttributes(&fa, route_kernel));
+    if (!st) st = record_launch(cudaFuncGetAttributes(&fa, router_logits_kernel));
+    return st;
+}
+
 int route_validate(const uint16_t *x, const uint16_t *w_router, const float *logits, int T, int H, int E, int k,
                    const int32_t *ids, const float *w) {
     int st = check_route_shape(T, H, E, k);

@@ -91,6 +91,8 @@ _SIGS = {
                               C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "spx_moe_layer": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
     "spx_moe_layer_noalloc": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
+    "spx_noalloc_init": (C.c_int, []),
+    "spx_noalloc_status": (C.c_int, [C.c_void_p, C.c_void_p]),
 }
 
 
@@ -417,7 +419,21 @@ def spx_moe_layer(args: LayerArgs, stream=None):
     _chk(load().spx_moe_layer(C.byref(args), _stream(stream)), "spx_moe_layer")
 
 
+def spx_noalloc_init():
+    """Set-up of the no-allocation layer call on the current device (once, at
+    start-up, before any stream capture): loads the library's kernels and its
+    fixed scratch array onto the device."""
+    _chk(load().spx_noalloc_init(), "spx_noalloc_init")
+
+
 def spx_moe_layer_noalloc(args: LayerArgs, stream=None):
     """The same layer with the library's fixed scratch instead of args.ws (for
-    callers that cannot allocate device memory); see include/spx.h."""
+    callers that cannot allocate device memory); spx_noalloc_init() must have
+    run on the device.  See include/spx.h."""
     _chk(load().spx_moe_layer_noalloc(C.byref(args), _stream(stream)), "spx_moe_layer_noalloc")
+
+
+def spx_noalloc_status(out: torch.Tensor, stream=None):
+    """Enqueue a copy of the fixed scratch's status word into `out` (one int32
+    on the device, or pinned host memory); read it after the stream syncs."""
+    _chk(load().spx_noalloc_status(C.c_void_p(out.data_ptr()), _stream(stream)), "spx_noalloc_status")

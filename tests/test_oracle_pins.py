@@ -44,6 +44,57 @@ def test_half_encode_rne_vs_numpy():
     assert np.array_equal(ours, ref)
 
 
+# -------------------------------------------------------- router product
+def _f16(a):
+    return np.asarray(a, np.float64).astype(np.float16).view(np.uint16)
+
+
+def test_router_logits_one_hot_router_rows_select_x():
+    """A router row that is 1.0 at position h and 0 elsewhere gives the
+    logit x[t][h] exactly; positions cover both ends of H, so a loop over a
+    wrong range of h, or over the wrong operand, fails."""
+    rng = np.random.default_rng(11)
+    T, H, E = 5, 640, 9
+    x = _f16(rng.standard_normal((T, H)))
+    pos = np.array([0, H - 1, 1, H - 2, 127, 128, 300, 511, 513])
+    wr = np.zeros((E, H), np.uint16)
+    wr[np.arange(E), pos] = _f16(1.0)
+    got = oracle.router_logits(x, wr)
+    want = x.view(np.float16).astype(np.float64)[:, pos]
+    assert np.array_equal(got, want)
+
+
+def test_router_logits_one_hot_tokens_select_router_columns():
+    """The transposed case: token t that is 1.0 at position h_t picks
+    column h_t of every router row, logits[t][e] = wr[e][h_t]."""
+    rng = np.random.default_rng(12)
+    T, H, E = 6, 384, 64
+    wr = _f16(rng.standard_normal((E, H)) * 0.02)
+    pos = np.array([0, H - 1, 5, 200, 257, 128])
+    x = np.zeros((T, H), np.uint16)
+    x[np.arange(T), pos] = _f16(1.0)
+    got = oracle.router_logits(x, wr)
+    assert np.array_equal(got, wr.view(np.float16).astype(np.float64)[:, pos].T)
+
+
+def test_router_logits_vs_numpy_matmul_and_closed_form():
+    """Random fp16 operands: fp64 products of fp16 values are exact, so the
+    oracle's ascending-h sum agrees with numpy's fp64 product to a few ulp of
+    the sum of |terms|; a router of constant rows c gives c * sum_h x[t][h]."""
+    rng = np.random.default_rng(13)
+    for T, H, E in [(1, 2048, 64), (9, 2048, 60), (4, 256, 8), (17, 4096, 16)]:
+        x = _f16(rng.standard_normal((T, H)))
+        wr = _f16(rng.standard_normal((E, H)) * 0.02)
+        xd, wd = x.view(np.float16).astype(np.float64), wr.view(np.float16).astype(np.float64)
+        got = oracle.router_logits(x, wr)
+        ref = xd @ wd.T
+        bound = 4 * H * np.finfo(np.float64).eps * (np.abs(xd) @ np.abs(wd).T)
+        assert np.all(np.abs(got - ref) <= bound)
+        c = 0.25
+        const = oracle.router_logits(x, np.full((3, H), _f16(c), np.uint16))
+        assert np.allclose(const, c * xd.sum(1, keepdims=True), rtol=0, atol=4 * H * 2.2e-16 * np.abs(xd).sum())
+
+
 # ------------------------------------------------------------- routing
 def _brute_topk(v, k):
     order = sorted(range(len(v)), key=lambda e: (-float(np.float32(v[e])), e))
