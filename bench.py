@@ -1,16 +1,20 @@
 """Benchmark of the per-layer MoE expert hot path (libspx) on one GB300.
 
-One step = one draft layer (T = 1, fused INT4 experts) + one verify layer
-(T = K+1 = 17, expert-reordered FP16 experts), each the full chain route ->
-top-k -> counters -> gather -> experts -> shared expert -> combine, on the
-DeepSeek-V2-Lite-shaped layer (H 2048, I 1408, 64 experts top-6, 2 shared
-experts).  Weights are random (seeded, generated on the device); 8 weight sets
-(11.4 GB) are rotated so that no step finds its weights in the 126 MB L2.
+One step = one 26-layer DeepSeek-V2-Lite-shaped draft-then-verify cycle (the
+largest single-GPU workload): K = 16 draft steps at T = 1 through all 26 layers
+(fused INT4 experts, the lookahead counters on), then one verify pass at
+T = K+1 = 17 through all 26 layers (expert-reordered FP16 experts); every
+layer is the full chain route -> top-k -> counters -> gather -> experts ->
+shared expert -> combine through spx_moe_layer.  Independent seeded weights per
+layer (37 GB) are generated on the device, so no layer finds its weights in the
+126 MB L2.
 
-value = algorithmic HBM bytes of the step / device time of the step (GB/s):
-  routed INT4 bytes of the unique experts the draft token selects, routed FP16
-  bytes of the unique experts the 17 verify tokens select, the FP16 shared
-  expert twice, activations, logits and outputs.
+value = algorithmic HBM bytes of a cycle / device time of a cycle (GB/s): the
+unique routed experts of every call (INT4 for the draft, FP16 for the verify,
+from the library's own routing), the FP16 shared expert of every call,
+activations, logits and outputs.  The same line carries per-layer figures of
+the three single-layer shapes (DeepSeek-V2-Lite, Qwen1.5-MoE, Phi-3.5-MoE;
+draft T = 1 and verify T = K+1), each timed as a chain of back-to-back calls.
 
 ``--impl reference`` times the CPU oracle (test infrastructure, single core)
 on a bounded sample of the same workload.
@@ -34,23 +38,51 @@ import numpy as np  # noqa: E402
 import spx_workloads as W  # noqa: E402
 
 METRIC = "MoE layer µs & achieved HBM GB/s vs GB300 peak, draft T=1 / verify T=K+1"
-# DRAM bytes (read + write) of one launch in the ncu captures summarised in
-# profiles/ (bench.py --loop, input set 0), with that launch's algorithmic
-# bytes.  They describe the kernels as captured: set them to None when a
-# kernel changes until it is captured again.
+CYCLE = "deepseek_v2_lite_x26"
+GATE_CONFIGS = ("deepseek_v2_lite", "qwen15_moe", "phi35_moe")
+# DRAM bytes (read + write) of one launch from an ncu capture of
+# `bench.py --loop draft|verify --sets 2` (DeepSeek-V2-Lite-shaped, input set
+# 0), with that launch's algorithmic bytes and the hash of the kernel sources
+# the capture ran.  traffic_of() returns the bytes only while the sources still
+# hash the same; a changed kernel reports null until it is captured again.
+KERNEL_SOURCES = {
+    "draft": ["spx_draft.cu", "spx_draft_gguf.cuh", "spx_routing.cuh", "spx_internal.cuh"],
+    "verify": ["spx_engine.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
+}
 PROFILED_TRAFFIC = {
-    "verify": {"dram_bytes": 675_098_624 + 3_160_320, "algorithmic_bytes": 674_897_920,
-               "summary": "profiles/engine_kernel_deepseek_v2_lite_verify.md"},
-    "draft": {"dram_bytes": 61_515_008 + 109_568, "algorithmic_bytes": 61_374_720,
-              "summary": "profiles/draft_kernel_deepseek_v2_lite_draft.md"},
+    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_098_624 + 3_160_320,
+               "algorithmic_bytes": 674_897_920, "source_sha": None},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_515_008 + 109_568, "algorithmic_bytes": 61_374_720,
+              "source_sha": None},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
 
 
+def source_sha(which):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[which]:
+        with open(os.path.join(ROOT, "quantized_expert_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_of(which):
+    """DRAM bytes per launch from the last capture, or None when the kernel's
+    sources changed since (or no capture was recorded for them)."""
     t = PROFILED_TRAFFIC.get(which)
-    return None if t is None else t["dram_bytes"]
+    if t is None or t["source_sha"] != source_sha(which):
+        return None
+    return t["dram_bytes"]
+
+
+def traffic_note(which):
+    t = PROFILED_TRAFFIC[which]
+    if traffic_of(which) is None:
+        return f"no ncu capture of the current {t['kernel']} sources"
+    return (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one {t['kernel']} launch "
+            f"(algorithmic {t['algorithmic_bytes']} B), sources {t['source_sha']}")
 
 
 def spread_us(ms_list):
@@ -130,7 +162,7 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -210,6 +242,10 @@ def make_inputs(s, i):
 
 
 def run_mine(args):
+    """The headline step: one 26-layer draft-then-verify cycle (K = 16 draft
+    steps at T = 1 through every layer with the lookahead counters on, then one
+    verify pass at T = 17), plus per-layer figures of the three single-layer
+    shapes, all through spx_moe_layer."""
     import torch
     from quantized_expert_gb300 import build as spx_build
     from quantized_expert_gb300 import spx
@@ -218,6 +254,7 @@ def run_mine(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
@@ -226,70 +263,11 @@ def run_mine(args):
     if world > 1:
         dist.barrier()
     spx.load()
-    s = W.CONFIGS[args.config]
-    Td, Tv = s.T_draft, s.T_verify
-
-    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
-    inputs = [make_inputs(s, i) for i in range(NINPUTS)]
-
-    def f16dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
-
-    dev_in = []
-    for d in inputs:
-        e = dict(x_d=f16dev(d["x_d"]), x_v=f16dev(d["x_v"]))
-        e["lg_d"] = torch.from_numpy(d["lg_d"]).cuda() if "lg_d" in d else torch.empty(Td, s.E, device="cuda")
-        e["lg_v"] = torch.from_numpy(d["lg_v"]).cuda() if "lg_v" in d else torch.empty(Tv, s.E, device="cuda")
-        dev_in.append(e)
-    L = s.layers
-    elb = torch.zeros(max(L, NSETS), s.E, dtype=torch.int32, device="cuda")
-    ws_d = spx.new_workspace(Td, s.H, s.I, s.E, s.k, s.I_s)
-    ws_v = spx.new_workspace(Tv, s.H, s.I, s.E, s.k, s.I_s)
-    r_d = spx.Routing.empty(Td, s.E, s.k)
-    r_v = spx.Routing.empty(Tv, s.E, s.k)
-    out_d = torch.empty(Td, s.H, dtype=torch.float16, device="cuda")
-    out_v = torch.empty(Tv, s.H, dtype=torch.float16, device="cuda")
-
-    def step_args(i):
-        st_d = sets[i % NSETS]
-        st_v = sets[(i + NSETS // 2) % NSETS]
-        inp = dev_in[i % NINPUTS]
-        ad, kd = spx.layer_args(0, inp["x_d"], s.E, s.k, s.renorm, inp["lg_d"], r_d, out_d, ws_d, w4=st_d["w4"],
-                                shared=st_d["shared"], w_router=st_d["w_router"], elb=elb, layer=i % NSETS)
-        av, kv = spx.layer_args(1, inp["x_v"], s.E, s.k, s.renorm, inp["lg_v"], r_v, out_v, ws_v, f16=st_v["f16"],
-                                shared=st_v["shared"], w_router=st_v["w_router"])
-        return ad, av, (kd, kv)
-
-    timed_keep = []
-
-    def step_args_timed(i, evd, evv):
-        st_d = sets[i % NSETS]
-        st_v = sets[(i + NSETS // 2) % NSETS]
-        inp = dev_in[i % NINPUTS]
-        ad, kd = spx.layer_args(0, inp["x_d"], s.E, s.k, s.renorm, inp["lg_d"], r_d, out_d, ws_d, w4=st_d["w4"],
-                                shared=st_d["shared"], w_router=st_d["w_router"], elb=elb, layer=i % NSETS,
-                                events=evd)
-        av, kv = spx.layer_args(1, inp["x_v"], s.E, s.k, s.renorm, inp["lg_v"], r_v, out_v, ws_v, f16=st_v["f16"],
-                                shared=st_v["shared"], w_router=st_v["w_router"], events=evv)
-        timed_keep.append((ad, av, kd, kv))
-        return ad, av
-
-    # unique experts per input (from the library's own routing) -> algorithmic bytes
-    nbytes = []
-    nd_list, nv_list = [], []
-    for i in range(NINPUTS):
-        ad, av, keep = step_args(i)
-        spx.spx_moe_layer(ad)
-        spx.spx_moe_layer(av)
-        torch.cuda.synchronize()
-        nd, nv = int(r_d.n_active.item()), int(r_v.n_active.item())
-        nd_list.append(nd)
-        nv_list.append(nv)
-        nbytes.append((layer_bytes(s, "draft", Td, nd), layer_bytes(s, "verify", Tv, nv)))
-
+    peak, peak_src = measured_peaks()
+    s = W.CONFIGS[CYCLE]
+    L, K, E, k, H, Tv = s.layers, s.K, s.E, s.k, s.H, s.T_verify
+    lays = [make_weight_set(s, l, torch, spx) for l in range(L)]
     stream = torch.cuda.Stream()
-    nrot = NSETS * NINPUTS // int(np.gcd(NSETS, NINPUTS))
-    keeps = [step_args(i) for i in range(nrot)]
 
     def sync_all():
         torch.cuda.synchronize()
@@ -300,98 +278,93 @@ def run_mine(args):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    # pass 1: the timed region proper (eager launches; the host enqueues well
-    # ahead of the device, so launch overhead is off the clock)
+    # one cycle's inputs: host (pinned) and two device copies (e2e double buffer)
+    host = {"xd": np.stack([[W.gen_x(s, 1, layer=l, step=st) for l in range(L)] for st in range(1, K + 1)]),
+            "lgd": np.stack([[W.draft_logits(s, l, st) for l in range(L)] for st in range(1, K + 1)]),
+            "xv": np.stack([W.gen_x(s, Tv, layer=l, step=K + 1, which=1) for l in range(L)]),
+            "lgv": np.stack([W.verify_logits(s, l) for l in range(L)])}
+    host_t = {n: torch.from_numpy(np.ascontiguousarray(a.view(np.float16) if a.dtype == np.uint16 else a)).pin_memory()
+              for n, a in host.items()}
+    dev_in = [{n: t.cuda() for n, t in host_t.items()} for _ in range(2)]
+    dev_out = [{"od": torch.zeros(L, 1, H, dtype=torch.float16, device="cuda"),
+                "ov": torch.zeros(L, Tv, H, dtype=torch.float16, device="cuda"),
+                "elb": torch.zeros(L, E, dtype=torch.int32, device="cuda")} for _ in range(2)]
+    ws_d, ws_v = spx.new_workspace(1, H, s.I, E, k, s.I_s), spx.new_workspace(Tv, H, s.I, E, k, s.I_s)
+    r_d, r_v = spx.Routing.empty(1, E, k), spx.Routing.empty(Tv, E, k)
+
+    def cycle_args(b):
+        di, do = dev_in[b], dev_out[b]
+        d = [[spx.layer_args(0, di["xd"][st, l], E, k, s.renorm, di["lgd"][st, l], r_d, do["od"][l], ws_d,
+                             w4=lays[l]["w4"], shared=lays[l]["shared"], elb=do["elb"], layer=l)
+              for l in range(L)] for st in range(K)]
+        v = [spx.layer_args(1, di["xv"][l], E, k, s.renorm, di["lgv"][l], r_v, do["ov"][l], ws_v,
+                            f16=lays[l]["f16"], shared=lays[l]["shared"]) for l in range(L)]
+        return d, v
+
+    cargs = [cycle_args(0), cycle_args(1)]
+
+    def cycle(b, evs=None):
+        d, v = cargs[b]
+        if evs:
+            evs[0].record(stream)
+        spx.spx_elb_reset(dev_out[b]["elb"], stream)
+        for st in range(K):
+            for l in range(L):
+                spx.spx_moe_layer(d[st][l][0], stream)
+        if evs:
+            evs[1].record(stream)
+        for l in range(L):
+            spx.spx_moe_layer(v[l][0], stream)
+        if evs:
+            evs[2].record(stream)
+
+    # algorithmic bytes of a cycle, from the library's own routing (untimed pass)
+    draft_bytes = verify_bytes = 0
+    nv_list = []
+    d0, v0 = cargs[0]
+    spx.spx_elb_reset(dev_out[0]["elb"])
+    for st in range(K):
+        for l in range(L):
+            spx.spx_moe_layer(d0[st][l][0])
+            draft_bytes += layer_bytes(s, "draft", 1, int(r_d.n_active.item()))
+    for l in range(L):
+        spx.spx_moe_layer(v0[l][0])
+        nv_list.append(int(r_v.n_active.item()))
+        verify_bytes += layer_bytes(s, "verify", Tv, nv_list[-1])
+    elb = dev_out[0]["elb"].cpu().numpy()
+    distinct = (elb > 0).sum(1)
+    cycle_bytes = draft_bytes + verify_bytes
+    n_draft = K * L
+
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            ad, av, _ = keeps[i % nrot]
-            spx.spx_moe_layer(ad, stream)
-            spx.spx_moe_layer(av, stream)
+            cycle(i % 2)
     sync_all()
+    evs = [(ev(), ev(), ev()) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        e0, e1 = ev(), ev()
         with torch.cuda.stream(stream):
-            e0, e1 = ev(), ev()
             e0.record(stream)
             for i in range(args.steps):
-                ad, av, _ = keeps[i % nrot]
-                spx.spx_moe_layer(ad, stream)
-                spx.spx_moe_layer(av, stream)
+                cycle(i % 2, evs[i])
             e1.record(stream)
         sync_all()
         ms_total = e0.elapsed_time(e1)
-        time.sleep(0.2)
+        time.sleep(0.05)
     clocks = clk.summary()
-
-    # pass 2: same steps with events between the layers and around each
-    # expert launch (per-layer and per-kernel durations for the roofline)
-    lay_ev, ker_ev = [], []
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            a, b, c = ev(), ev(), ev()
-            kd, kv = (ev(), ev()), (ev(), ev())
-            for e_ in kd + kv:  # create the event; libspx re-records it around the expert launch
-                e_.record(stream)
-            ad, ae = step_args_timed(i, kd, kv)
-            a.record(stream)
-            spx.spx_moe_layer(ad, stream)
-            b.record(stream)
-            spx.spx_moe_layer(ae, stream)
-            c.record(stream)
-            lay_ev.append((a, b, c))
-            ker_ev.append((kd, kv))
-    sync_all()
-    d_ms = [a.elapsed_time(b) for a, b, c in lay_ev]
-    v_ms = [b.elapsed_time(c) for a, b, c in lay_ev]
-    kd_ms = [k[0][0].elapsed_time(k[0][1]) for k in ker_ev]
-    kv_ms = [k[1][0].elapsed_time(k[1][1]) for k in ker_ev]
-
-    step_bytes = [nbytes[i % NINPUTS] for i in range(args.steps)]
-    tot_bytes = sum(d + v for d, v in step_bytes)
+    dph = [a.elapsed_time(b) for a, b, c in evs]
+    vph = [b.elapsed_time(c) for a, b, c in evs]
+    value, _ = job_throughput(cycle_bytes * args.steps, ms_total, device="cuda")
     ms_step = ms_total / args.steps
-    value, t_max = job_throughput(tot_bytes, ms_total, device="cuda")
+    d_us = statistics.median(dph) * 1e3 / n_draft  # per chained draft launch
+    v_us = statistics.median(vph) * 1e3 / L         # per verify layer (routing + expert launch)
 
-    d_bytes = statistics.mean(b[0] for b in step_bytes)
-    v_bytes = statistics.mean(b[1] for b in step_bytes)
-    d_us = statistics.median(d_ms) * 1e3
-    v_us = statistics.median(v_ms) * 1e3
-    kd_us = statistics.mean(kd_ms) * 1e3
-    kv_us = statistics.mean(kv_ms) * 1e3
-    # expert-launch bytes.  Verify: the layer's bytes minus what the routing
-    # launch reads.  Draft: the draft launch routes its token itself, so it
-    # reads everything the layer reads (a router product, where there is one,
-    # runs in a launch of its own before it).
-    kv_bytes = v_bytes - Tv * s.E * 4 - (s.E * s.H * 2 if s.logits == "router" else 0)
-    kd_bytes = d_bytes - (s.E * s.H * 2 if s.logits == "router" else 0)
-    peak, peak_src = measured_peaks()
-
-    # e2e: host buffers through the public API, copies inside the timed region.
-    # A serving loop's pipelining: a copy stream moves step i+1's inputs in and
-    # step i's outputs out while the compute stream runs step i (two output
-    # buffers, events between the streams).
-    host_in = []
-    for d in inputs:
-        h = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.float16) if v.dtype == np.uint16 else v)).pin_memory()
-             for k, v in d.items()}
-        host_in.append(h)
-    host_out_d = torch.empty(Td, s.H, dtype=torch.float16).pin_memory()
-    host_out_v = torch.empty(Tv, s.H, dtype=torch.float16).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values())
-    d2h = host_out_d.numel() * 2 + host_out_v.numel() * 2
-    outs2 = [(out_d, out_v), (torch.empty_like(out_d), torch.empty_like(out_v))]
-
-    def e2e_args(i):
-        st_d = sets[i % NSETS]
-        st_v = sets[(i + NSETS // 2) % NSETS]
-        inp = dev_in[i % NINPUTS]
-        od, ov = outs2[i % 2]
-        ad, kd = spx.layer_args(0, inp["x_d"], s.E, s.k, s.renorm, inp["lg_d"], r_d, od, ws_d, w4=st_d["w4"],
-                                shared=st_d["shared"], w_router=st_d["w_router"], elb=elb, layer=i % NSETS)
-        av, kv = spx.layer_args(1, inp["x_v"], s.E, s.k, s.renorm, inp["lg_v"], r_v, ov, ws_v, f16=st_v["f16"],
-                                shared=st_v["shared"], w_router=st_v["w_router"])
-        return ad, av, (kd, kv)
-
-    nrot2 = nrot if nrot % 2 == 0 else 2 * nrot
-    keeps2 = [e2e_args(i) for i in range(nrot2)]
+    # e2e: each step's inputs copied in from pinned host memory and its outputs
+    # (verify outputs, last draft outputs, lookahead counters) copied back, on a
+    # copy stream that overlaps the neighbouring steps (double buffers).
+    host_out = [{n: torch.empty_like(t, device="cpu").pin_memory() for n, t in dev_out[0].items()} for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_t.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     cstream = torch.cuda.Stream()
     n_all = args.warmup + args.steps
     ev_in = [torch.cuda.Event() for _ in range(n_all)]
@@ -400,10 +373,10 @@ def run_mine(args):
 
     def h2d_step(i):
         with torch.cuda.stream(cstream):
-            h = host_in[i % NINPUTS]
-            inp = dev_in[i % NINPUTS]
-            for k, v in h.items():
-                inp[k].copy_(v, non_blocking=True)
+            if i >= 2:
+                cstream.wait_event(ev_done[i - 2])  # the buffer's previous step has finished
+            for n, t in host_t.items():
+                dev_in[i % 2][n].copy_(t, non_blocking=True)
             ev_in[i].record(cstream)
 
     sync_all()
@@ -416,61 +389,73 @@ def run_mine(args):
         if i == 0 or i == args.warmup:
             h2d_step(i)
         if i + 1 < n_all and i + 1 != args.warmup:
-            h2d_step(i + 1)  # the next step's inputs, during this step's layers
+            h2d_step(i + 1)
         with torch.cuda.stream(stream):
             stream.wait_event(ev_in[i])
             if i >= 2:
                 stream.wait_event(ev_out[i - 2])  # this output buffer has been read back
-            ad, av, _ = keeps2[i % nrot2]
-            spx.spx_moe_layer(ad, stream)
-            spx.spx_moe_layer(av, stream)
+            cycle(i % 2)
             ev_done[i].record(stream)
         with torch.cuda.stream(cstream):
             cstream.wait_event(ev_done[i])
-            od, ov = outs2[i % 2]
-            host_out_d.copy_(od, non_blocking=True)
-            host_out_v.copy_(ov, non_blocking=True)
+            for n, t in host_out[i % 2].items():
+                t.copy_(dev_out[i % 2][n], non_blocking=True)
             ev_out[i].record(cstream)
     cstream.synchronize()
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e_gbs, _ = job_throughput(tot_bytes, e2e_s * 1e3, device="cuda")  # slowest rank's wall time
+    e2e_gbs, _ = job_throughput(cycle_bytes * args.steps, e2e_s * 1e3, device="cuda")
+    assert spx.spx_workspace_status(ws_d) == 0 and spx.spx_workspace_status(ws_v) == 0
 
+    # per-layer figures of the three single-layer shapes
+    per_cfg = {}
+    for name in GATE_CONFIGS:
+        c = W.CONFIGS[name]
+        sets = lays if name == "deepseek_v2_lite" else [make_weight_set(c, i, torch, spx) for i in range(NSETS)]
+        per_cfg[name] = layer_figures(c, sets, torch, spx, stream, peak)
+        if sets is not lays:
+            del sets
+            torch.cuda.empty_cache()
+
+    pt_d, pt_v = traffic_of("draft"), traffic_of("verify")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 (int4 draft weights, fp32 accumulate)",
-        "data": "synthetic (seeded random weights and activations; drawn Zipf(1.1) router logits)",
-        "config": {"workload": f"{s.name} layer: draft T={Td} + verify T={Tv}", "H": s.H, "I": s.I, "E": s.E,
-                   "k": s.k, "I_shared": s.I_s, "draft_T": Td, "verify_T": Tv,
-                   "l2": f"{NSETS} rotated weight sets ({NSETS * 1.43:.1f} GB) > L2; no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "unique_experts_draft": statistics.mean(nd_list), "unique_experts_verify": statistics.mean(nv_list)},
-        "layers": {"draft_us": round(d_us, 2), "draft_gbs": round(d_bytes / (d_us * 1e-6) / 1e9, 1),
-                   "draft_frac": round(d_bytes / (d_us * 1e-6) / 1e9 / peak, 3),
-                   "draft_tokens_per_s": round(Td / (d_us * 1e-6), 1),
-                   "verify_us": round(v_us, 2), "verify_gbs": round(v_bytes / (v_us * 1e-6) / 1e9, 1),
-                   "verify_frac": round(v_bytes / (v_us * 1e-6) / 1e9 / peak, 3),
-                   "verify_tokens_per_s": round(Tv / (v_us * 1e-6), 1),
-                   "draft_bytes": int(d_bytes), "verify_bytes": int(v_bytes),
-                   "draft_us_spread": spread_us(d_ms), "verify_us_spread": spread_us(v_ms)},
-        "roofline": {"bound": "hbm", "kernel": "engine_kernel<1,1,3> (verify expert launch, FP16 experts)",
-                     "achieved": round(kv_bytes / (kv_us * 1e-6) / 1e9, 1), "peak": peak,
+        "data": "synthetic (seeded random weights and activations per layer; drawn Zipf(1.1) router logits)",
+        "config": {"workload": f"{s.name}: 26-layer DeepSeek-V2-Lite-shaped draft-then-verify cycle, {K} draft steps "
+                               f"(T=1) x {L} layers + one verify pass (T={Tv}) x {L} layers",
+                   "layers": L, "K": K, "H": H, "I": s.I, "E": E, "k": k, "I_shared": s.I_s,
+                   "l2": f"{L} layer weight sets ({L * 1.43:.0f} GB) > L2; no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "cycle": {"us_per_cycle": round(ms_step * 1e3, 1), "draft_phase_us": round(statistics.median(dph) * 1e3, 1),
+                  "verify_phase_us": round(statistics.median(vph) * 1e3, 1),
+                  "draft_layer_us": round(d_us, 2), "verify_layer_us": round(v_us, 2),
+                  "bytes_per_cycle": int(cycle_bytes), "draft_bytes": int(draft_bytes),
+                  "verify_bytes": int(verify_bytes), "frac_of_peak": round(value / peak, 3),
+                  "verify_unique_experts_mean": round(statistics.mean(nv_list), 2),
+                  "elb_distinct_experts_per_layer": {"mean": round(float(distinct.mean()), 2),
+                                                     "min": int(distinct.min()), "max": int(distinct.max())}},
+        "roofline": {"bound": "hbm", "kernel": "draft_kernel<2, 0> (draft launch: routing + INT4 experts + shared "
+                                               "expert + combine), the cycle's dominant kernel",
+                     "achieved": round(draft_bytes / n_draft / (d_us * 1e-6) / 1e9, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(kv_bytes / (kv_us * 1e-6) / 1e9 / peak, 3),
-                     "traffic": traffic_of("verify"), "traffic_capture": PROFILED_TRAFFIC["verify"],
-                     "launch_us": round(kv_us, 2), "bytes_per_launch": int(kv_bytes)},
-        "draft_roofline": {"bound": "hbm", "kernel": "draft_kernel<2, 0> (draft launch: routing + INT4 experts)",
-                           "achieved": round(kd_bytes / (kd_us * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
-                           "frac": round(kd_bytes / (kd_us * 1e-6) / 1e9 / peak, 3), "launch_us": round(kd_us, 2),
-                           "bytes_per_launch": int(kd_bytes), "traffic": traffic_of("draft"),
-                           "traffic_capture": PROFILED_TRAFFIC["draft"]},
+                     "frac": round(draft_bytes / n_draft / (d_us * 1e-6) / 1e9 / peak, 3),
+                     "traffic": pt_d, "traffic_source": traffic_note("draft"),
+                     "launch_us": round(d_us, 2), "bytes_per_launch": int(draft_bytes / n_draft),
+                     "timing": f"CUDA events around the draft phase of every timed cycle ({n_draft} launches back "
+                               f"to back on the launching stream), median over cycles / {n_draft}"},
+        "verify_roofline": {"bound": "hbm", "kernel": "route_kernel + engine_kernel<1,1,3> (verify layer)",
+                            "achieved": round(verify_bytes / L / (v_us * 1e-6) / 1e9, 1), "peak": peak,
+                            "unit": "GB/s", "frac": round(verify_bytes / L / (v_us * 1e-6) / 1e9 / peak, 3),
+                            "layer_us": round(v_us, 2), "bytes_per_layer": int(verify_bytes / L),
+                            "traffic": pt_v, "traffic_source": traffic_note("verify")},
+        "configs": per_cfg,
         "clocks": clocks,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        # per step: the draft launch (+ the router product when the layer has a
-        # router weight), the verify routing launch, the verify expert launch
-        "gpu_launches": (3 + (1 if s.logits == "router" else 0)) * args.steps,
+        # per cycle: K*L draft launches, L routing launches, L verify expert launches
+        "gpu_launches": (n_draft + 2 * L) * args.steps,
     }
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s)
@@ -478,6 +463,75 @@ def run_mine(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def layer_figures(s, sets, torch, spx, stream, peak, n_batches=10):
+    """Per-layer figures of one shape: draft (T = 1) and verify (T = K+1) layers
+    timed back to back (batches of chained calls over rotated weight sets and
+    inputs; events around each batch only, so the launch chain is kept), and the
+    expert launch alone (events around it)."""
+    out = {}
+    for mode, T, chain in (("draft", s.T_draft, 64), ("verify", s.T_verify, 16)):
+        which = 0 if mode == "draft" else 1
+        xs = [torch.from_numpy(np.ascontiguousarray(W.gen_x(s, T, step=i, which=which)).view(np.float16)).cuda()
+              for i in range(NINPUTS)]
+        lgs = [torch.from_numpy(W.gen_logits(s, T, step=i, which=which)).cuda() if s.logits != "router"
+               else torch.empty(T, s.E, device="cuda") for i in range(NINPUTS)]
+        ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+        r = spx.Routing.empty(T, s.E, s.k)
+        o = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+        n = len(sets) * NINPUTS // int(np.gcd(len(sets), NINPUTS))
+
+        def call_args(i, events=None):
+            st = sets[i % len(sets)]
+            return spx.layer_args(which, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, o, ws,
+                                  w4=st["w4"] if mode == "draft" else None,
+                                  f16=st["f16"] if mode == "verify" else None, shared=st["shared"],
+                                  w_router=st["w_router"], events=events)
+
+        keep = [call_args(i) for i in range(n)]
+        nb = []
+        for i in range(NINPUTS):  # unique experts per input, from the library's routing
+            spx.spx_moe_layer(keep[i][0])
+            nb.append(layer_bytes(s, mode, T, int(r.n_active.item())))
+        byt = float(np.mean(nb))
+        with torch.cuda.stream(stream):
+            for i in range(2 * chain):
+                spx.spx_moe_layer(keep[i % n][0], stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_batches)]
+            j = 0
+            for a, b in evs:
+                a.record(stream)
+                for _ in range(chain):
+                    spx.spx_moe_layer(keep[j % n][0], stream)
+                    j += 1
+                b.record(stream)
+        torch.cuda.synchronize()
+        per = [a.elapsed_time(b) / chain for a, b in evs]  # ms per layer, per batch
+        # the expert launch alone (events recorded around it; no overlap with neighbours)
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(16)]
+        kkeep = []
+        with torch.cuda.stream(stream):
+            for i, e_ in enumerate(kev):
+                for x in e_:
+                    x.record(stream)
+                ka = call_args(i, events=e_)
+                kkeep.append(ka)
+                spx.spx_moe_layer(ka[0], stream)
+        torch.cuda.synchronize()
+        k_us = statistics.mean(a.elapsed_time(b) for a, b in kev) * 1e3
+        k_bytes = byt - (T * s.E * 4 if mode == "verify" else 0) - (s.E * s.H * 2 if s.logits == "router" else 0)
+        assert spx.spx_workspace_status(ws) == 0
+        us = statistics.median(per) * 1e3
+        out[mode] = {"T": T, "layer_us": spread_us(per), "gbs": round(byt / (us * 1e-6) / 1e9, 1),
+                     "frac": round(byt / (us * 1e-6) / 1e9 / peak, 3), "tokens_per_s": round(T / (us * 1e-6), 1),
+                     "bytes": int(byt),
+                     "expert_launch_alone": {"us": round(k_us, 2), "bytes": int(k_bytes),
+                                             "gbs": round(k_bytes / (k_us * 1e-6) / 1e9, 1),
+                                             "frac": round(k_bytes / (k_us * 1e-6) / 1e9 / peak, 3)},
+                     "timing": f"{n_batches} batches of {chain} layer calls back to back; spread over batches"}
+    return out
 
 
 # ---------------------------------------------------------------- oracle --
@@ -500,15 +554,16 @@ def cpu_baseline(s, reps=1):
     dt = (time.perf_counter() - t0) / reps
     b = layer_bytes(s, "draft", s.T_draft, len(need_d)) + layer_bytes(s, "verify", s.T_verify, len(need_v))
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"1 draft (T={s.T_draft}) + 1 verify (T={s.T_verify}) layer of {s.name}, input set 0, "
-                      f"{reps} rep(s), {dt:.2f} s per step"}
+            "sample": f"1 draft (T={s.T_draft}) + 1 verify (T={s.T_verify}) layer of {s.name} (one of the cycle's "
+                      f"{s.layers * (s.K + 1)} layer calls), input set 0, {reps} rep(s), {dt:.2f} s per sample; "
+                      f"GB/s = the sample's algorithmic bytes / its time"}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    s = W.CONFIGS[args.config]
+    s = W.CONFIGS[CYCLE]
     times = []
     cb = None
     for i in range(args.warmup + args.steps):
@@ -520,87 +575,12 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{s.name} layer: draft T={s.T_draft} + verify T={s.T_verify}"},
+            "config": {"workload": f"{s.name}: 26-layer DeepSeek-V2-Lite-shaped draft-then-verify cycle, {s.K} draft "
+                                   f"steps (T=1) x {s.layers} layers + one verify pass (T={s.T_verify}) x {s.layers} "
+                                   f"layers"},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": cb["sample"]},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-
-
-def run_cycle(args):
-    """The 26-layer draft-then-verify cycle: K draft steps at T = 1 through every
-    layer (Expert Lookahead Buffer counters on), then one verify pass at T = K+1;
-    independent weights per layer.  Prints one JSON line: device us per cycle,
-    achieved GB/s of the cycle's algorithmic bytes, ELB distinct experts per layer."""
-    import torch
-    from quantized_expert_gb300 import build as B, spx
-    import oracle
-    B.build()
-    spx.load()
-    s = W.CONFIGS["deepseek_v2_lite_x26"]
-    L, K, E, k, Tv = s.layers, s.K, s.E, s.k, s.T_verify
-    lays = [make_weight_set(s, l, torch, spx) for l in range(L)]
-
-    def f16dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
-    xd = {(st, l): f16dev(W.gen_x(s, 1, layer=l, step=st)) for st in range(1, K + 1) for l in range(L)}
-    lgd = {(st, l): torch.from_numpy(W.draft_logits(s, l, st)).cuda() for st in range(1, K + 1) for l in range(L)}
-    xv = [f16dev(W.gen_x(s, Tv, layer=l, step=K + 1, which=1)) for l in range(L)]
-    lgv = [torch.from_numpy(W.verify_logits(s, l)).cuda() for l in range(L)]
-    # algorithmic bytes of one cycle (unique experts of every call, from the drawn logits)
-    cyc_bytes = 0
-    for l in range(L):
-        for st in range(1, K + 1):
-            ids, _ = oracle.route_topk(W.draft_logits(s, l, st).astype(np.float64), k, s.renorm)
-            cyc_bytes += layer_bytes(s, "draft", 1, len(set(ids.reshape(-1).tolist())))
-        ids, _ = oracle.route_topk(W.verify_logits(s, l).astype(np.float64), k, s.renorm)
-        cyc_bytes += layer_bytes(s, "verify", Tv, len(set(ids.reshape(-1).tolist())))
-    elb = torch.zeros(L, E, dtype=torch.int32, device="cuda")
-    ws_d, ws_v = spx.new_workspace(1, s.H, s.I, E, k, s.I_s), spx.new_workspace(Tv, s.H, s.I, E, k, s.I_s)
-    r_d, r_v = spx.Routing.empty(1, E, k), spx.Routing.empty(Tv, E, k)
-    out_d = torch.empty(1, s.H, dtype=torch.float16, device="cuda")
-    out_v = torch.empty(Tv, s.H, dtype=torch.float16, device="cuda")
-    draft_args = [[spx.layer_args(0, xd[(st, l)], E, k, s.renorm, lgd[(st, l)], r_d, out_d, ws_d,
-                                  w4=lays[l]["w4"], shared=lays[l]["shared"], elb=elb, layer=l)
-                   for l in range(L)] for st in range(1, K + 1)]
-    verify_args = [spx.layer_args(1, xv[l], E, k, s.renorm, lgv[l], r_v, out_v, ws_v, f16=lays[l]["f16"],
-                                  shared=lays[l]["shared"]) for l in range(L)]
-    stream = torch.cuda.Stream()
-
-    def cycle():
-        spx.spx_elb_reset(elb, stream)
-        for st in range(K):
-            for l in range(L):
-                spx.spx_moe_layer(draft_args[st][l][0], stream)
-        for l in range(L):
-            spx.spx_moe_layer(verify_args[l][0], stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup)):
-            cycle()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n = max(1, args.steps)
-        e0.record(stream)
-        for _ in range(n):
-            cycle()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / n
-    got = elb.cpu().numpy()
-    distinct = (got > 0).sum(1)
-    peak, peak_src = measured_peaks()
-    gbs = cyc_bytes / (us * 1e-6) / 1e9
-    line = {"metric": "26-layer draft-then-verify cycle, device us per cycle", "value": round(us, 1), "unit": "us",
-            "higher_is_better": False, "n_gpus": 1, "steps": n, "warmup": max(1, args.warmup),
-            "data": "synthetic (independent seeded weights per layer; drawn Zipf(1.1) router logits)",
-            "config": {"workload": f"{s.name}: {K} draft steps (T=1) x {L} layers + verify (T={Tv}) x {L} layers",
-                       "layer_calls_per_cycle": (K + 1) * L},
-            "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3), "peak": peak,
-            "peak_source": peak_src, "bytes_per_cycle": int(cyc_bytes),
-            "elb_distinct_experts_per_layer": {"mean": round(float(distinct.mean()), 2), "min": int(distinct.min()),
-                                               "max": int(distinct.max())},
-            "elb_calls_per_layer": int(got.sum(1)[0]) // k}
     print(json.dumps(line), flush=True)
 
 
@@ -804,10 +784,11 @@ def run_draft_batch(args):
 TL_EVENTS = ["entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "gu_last", "dn_w_first",
              "dn_h_first", "dn_last", "prod_last", "cons_done", "out_done", "sg_last", "rg_first", "rg_last",
              "w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "exit", "rd_h_last", "sd_last",
-             "w_poll", "bytes"]
+             "w_poll", "bytes", "w_ticket", "n_ticket", "w_route", "issue"]
 TL_FIRST_EV = {"entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "dn_w_first",
                "dn_h_first", "cons_done", "rg_first"}
-TL_SUM_EV = {"w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "w_poll", "bytes"}
+TL_SUM_EV = {"w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "w_poll", "bytes", "w_ticket",
+             "n_ticket", "w_route", "issue"}
 
 
 def timeline_phases(buf, slots, nblocks):
@@ -920,7 +901,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--sets", type=int, default=NSETS, help="rotated weight sets (8 defeat L2)")
     ap.add_argument("--loop", choices=["draft", "verify"], help="profiling driver: layer calls only, no timing")
-    ap.add_argument("--cycle", action="store_true", help="the 26-layer draft-then-verify cycle (prints its own line)")
     ap.add_argument("--loop-n", type=int, default=12)
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
@@ -938,8 +918,6 @@ def main():
         run_cached(args)
     elif args.draft_batch:
         run_draft_batch(args)
-    elif args.cycle:
-        run_cycle(args)
     elif args.impl == "reference":
         if args.steps > 3:
             args.steps = 3

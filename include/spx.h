@@ -104,6 +104,58 @@ SPX_API int spx_elb_read(const uint32_t *elb, int L, int E, uint32_t *dst, spx_s
 SPX_API int spx_elb_reset(uint32_t *elb, int L, int E, spx_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Layer-Aware Prefetch Planner  [P1 Key Contributions 3 (counter snapshots  */
+/* feed a planner with Cold Start, Prefetch Overlap and Final Cleanup phases  */
+/* and adaptively sized draft chunks); Methodology (chunks sized so compute  */
+/* roughly matches transfer time on a parallel stream); P2 What shipped (a   */
+/* compact prefetch plan at chunk boundaries)]                                */
+/* ------------------------------------------------------------------------ */
+/* The pages name the phases and the sizing goal only; the rule below is this
+ * library's reading.  One call per draft-chunk boundary of a speculation cycle
+ * of K draft steps (host code; all pointers host memory):
+ *  phase: SPX_PLAN_COLD_START when steps_done == 0, SPX_PLAN_PREFETCH_OVERLAP
+ *    when 0 < steps_done < K, SPX_PLAN_FINAL_CLEANUP when steps_done == K.
+ *  demand of layer l: experts e with elb[l][e] > 0 (a snapshot of the counters
+ *    after steps_done draft steps, e.g. from spx_elb_read) and cached[l][e] == 0,
+ *    most counted first, ties to the lower expert index.
+ *  actions, layers ascending (the order the verify pass needs them in): each
+ *    demanded expert is loaded; when the layer already caches cfg->capacity
+ *    experts, the lowest-index cached expert with a zero count is evicted
+ *    first; when every cached expert has a nonzero count, the layer's remaining
+ *    demand is left to the verify pass.  cached[][] (in/out) is updated.
+ *    actions[3*i .. 3*i+2] = {layer, expert, SPX_PLAN_LOAD or SPX_PLAN_EVICT}.
+ *  next_chunk: draft steps to run before the next call = ceil(loads *
+ *    copy_us / step_us) clamped to [min_chunk, K - steps_done] (cold start with
+ *    no load: min_chunk; final cleanup: 0).
+ * max_actions must be at least twice the number of demanded experts (2*L*E is
+ * always enough); otherwise SPX_ERR_INVALID_ARG and nothing is changed. */
+enum { SPX_PLAN_COLD_START = 0, SPX_PLAN_PREFETCH_OVERLAP = 1, SPX_PLAN_FINAL_CLEANUP = 2 };
+enum { SPX_PLAN_EVICT = 0, SPX_PLAN_LOAD = 1 };
+typedef struct {
+    int L, E, K;       /* layers, experts per layer, draft steps per cycle */
+    int capacity;      /* experts of one layer the device holds at once (1..E) */
+    int min_chunk;     /* least draft steps per chunk (>= 1) */
+    double step_us;    /* device time of one draft step through all L layers (> 0) */
+    double copy_us;    /* host-to-device time of one expert's weights (>= 0) */
+} spx_plan_cfg;
+SPX_API int spx_plan_prefetch(const spx_plan_cfg *cfg, const uint32_t *elb, int steps_done, uint8_t *cached,
+                              int32_t *actions, int max_actions, int *n_actions, int *next_chunk, int *phase);
+/* Executor of a plan on `stream` (a stream parallel to the compute stream):
+ * per SPX_PLAN_LOAD, one cudaMemcpyAsync of expert e's expert_bytes from
+ * host_experts[l] + e*expert_bytes (page-locked host memory) to
+ * dev_experts[l] + e*expert_bytes (device), then resident[l*E+e] = 1 (when
+ * resident != NULL) and ready[l*E+e] = nonzero; per SPX_PLAN_EVICT,
+ * ready[l*E+e] = 0 and resident[l*E+e] = 0.  ready/resident are device
+ * arrays [L][E]; pass ready + l*E (and resident + l*E) to layer l's verify
+ * call (spx_layer_args), whose expert launch waits for each routed expert's
+ * flag.  For the FP16 packed experts of spx_f16_repack, expert_bytes =
+ * spx_f16_packed_bytes(1, H, I) (expert e's units are contiguous).  Every
+ * action is checked before anything is enqueued. */
+SPX_API int spx_prefetch_issue(const int32_t *actions, int n_actions, const void *const *host_experts,
+                               void *const *dev_experts, size_t expert_bytes, uint32_t *ready, uint8_t *resident,
+                               int L, int E, spx_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Gather tokens by expert (counting sort)  [P1 Key Contributions 4]         */
 /* ------------------------------------------------------------------------ */
 /* Flat slots s = t*k + j.  counts [E]: assignments per expert; offsets [E+1]:

@@ -322,6 +322,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     auto n_act = [&]() -> int {
         if (na < 0) {
             const uint64_t t0 = global_timer_ns();
+            const unsigned long long twr = TL_NOW();
             while (!misc[4]) {
                 if (misc[0] || global_timer_ns() - t0 > p.wait_budget_ns) {
                     atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
@@ -332,6 +333,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             }
             __threadfence_block();
             na = misc[5];
+            TL_ADD(p.tl_slot, TL_W_ROUTE, TL_NOW() - twr);
         }
         return na;
     };
@@ -348,7 +350,8 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             ok = false;
             return false;
         }
-        TL_ADD(p.tl_slot, TL_W_EMPTY, TL_NOW() - tw);
+        const unsigned long long tis = TL_NOW();
+        TL_ADD(p.tl_slot, TL_W_EMPTY, tis - tw);
         TL_ADD(p.tl_slot, TL_BYTES, bytes + zbytes);
         h.seq = (int)it;
         h.hpar = (int)((hpar_bits >> st) & 1u);
@@ -368,6 +371,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             __threadfence_block();
             pstate[st] = 1;
         }
+        TL_ADD(p.tl_slot, TL_ISSUE, TL_NOW() - tis);
         ++it;
         return true;
     };
@@ -505,8 +509,10 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         uint32_t tkB = nsm + atomicAdd(ctr, 1u);
         while (true) {
             tkA = nsm + atomicAdd(ctr, 1u);
+            TL_TICKET(p.tl_slot, tkB, misc + 15);
             if (!run_unit((int)tkB * kDkShards + shard)) break;
             tkB = nsm + atomicAdd(ctr, 1u);
+            TL_TICKET(p.tl_slot, tkA, misc + 15);
             if (!run_unit((int)tkA * kDkShards + shard)) break;
         }
     }

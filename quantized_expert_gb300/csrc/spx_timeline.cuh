@@ -46,6 +46,10 @@ enum TlEvent : int {
     TL_SD_LAST = 25,       // last: shared down item finished
     TL_W_POLL = 26,        // sum: ns from a down item's registration to its intermediate copy
     TL_BYTES = 27,         // sum: weight bytes the producer issued
+    TL_W_TICKET = 28,      // sum: producer ns waiting for a queue ticket's value
+    TL_N_TICKET = 29,      // sum: queue tickets used
+    TL_W_ROUTE = 30,       // sum: producer ns waiting for the routing
+    TL_ISSUE = 31,         // sum: producer ns inside a fill's issue (after the free stage)
 };
 
 }  // namespace spx
@@ -63,10 +67,20 @@ __device__ __forceinline__ unsigned long long *tl_word(int slot, int ev) {
 #define TL_ADD(slot, ev, v) atomicAdd(::spx::tl_word((slot), (ev)), (unsigned long long)(v))
 #define TL_NOW() ::spx::global_timer_ns()
 #define TL_ON 1
+// waits for v (a queue ticket in flight) by storing it to a shared word, and
+// counts the wait
+#define TL_TICKET(slot, v, sinkp)                                     \
+    do {                                                              \
+        const unsigned long long t_ = TL_NOW();                       \
+        *(volatile uint32_t *)(sinkp) = (v);                          \
+        TL_ADD((slot), ::spx::TL_W_TICKET, TL_NOW() - t_);            \
+        TL_ADD((slot), ::spx::TL_N_TICKET, 1);                        \
+    } while (0)
 #else
 #define TL_FIRST(slot, ev) ((void)0)
 #define TL_LAST(slot, ev) ((void)0)
 #define TL_ADD(slot, ev, v) ((void)0)
 #define TL_NOW() 0ull
 #define TL_ON 0
+#define TL_TICKET(slot, v, sinkp) ((void)0)
 #endif

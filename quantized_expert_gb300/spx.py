@@ -19,6 +19,8 @@ from . import build as _build
 _lib = None
 
 SPX_OK, SPX_ERR_INVALID_ARG, SPX_ERR_UNSUPPORTED, SPX_ERR_WORKSPACE, SPX_ERR_CUDA, SPX_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+SPX_PLAN_COLD_START, SPX_PLAN_PREFETCH_OVERLAP, SPX_PLAN_FINAL_CLEANUP = 0, 1, 2
+SPX_PLAN_EVICT, SPX_PLAN_LOAD = 0, 1
 
 
 class SpxError(RuntimeError):
@@ -42,6 +44,11 @@ class GgufExperts(C.Structure):
 
 class Shared(C.Structure):
     _fields_ = [("packed", C.c_void_p), ("w_sgate", C.c_void_p), ("H", C.c_int), ("I_s", C.c_int)]
+
+
+class PlanCfg(C.Structure):
+    _fields_ = [("L", C.c_int), ("E", C.c_int), ("K", C.c_int), ("capacity", C.c_int), ("min_chunk", C.c_int),
+                ("step_us", C.c_double), ("copy_us", C.c_double)]
 
 
 class LayerArgs(C.Structure):
@@ -92,6 +99,10 @@ _SIGS = {
     "spx_moe_layer": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
     "spx_moe_layer_noalloc": (C.c_int, [C.POINTER(LayerArgs), C.c_void_p]),
     "spx_noalloc_init": (C.c_int, []),
+    "spx_plan_prefetch": (C.c_int, [C.POINTER(PlanCfg), C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_int,
+                                    C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_int)]),
+    "spx_prefetch_issue": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
+                                     C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "spx_noalloc_status": (C.c_int, [C.c_void_p, C.c_void_p]),
 }
 
@@ -437,3 +448,35 @@ def spx_noalloc_status(out: torch.Tensor, stream=None):
     """Enqueue a copy of the fixed scratch's status word into `out` (one int32
     on the device, or pinned host memory); read it after the stream syncs."""
     _chk(load().spx_noalloc_status(C.c_void_p(out.data_ptr()), _stream(stream)), "spx_noalloc_status")
+
+
+# ----------------------------------------------------------- prefetch plan --
+def spx_plan_prefetch(cfg: PlanCfg, elb, steps_done: int, cached):
+    """One planning call at a draft-chunk boundary (host numpy arrays: elb
+    uint32 [L][E], cached uint8 [L][E], updated in place).  Returns (phase,
+    actions int32 [n][3] = layer, expert, SPX_PLAN_LOAD/EVICT, next_chunk)."""
+    import numpy as np
+    elb = np.ascontiguousarray(elb, dtype=np.uint32)
+    if cached.dtype != np.uint8 or not cached.flags.c_contiguous:
+        raise ValueError("cached must be a contiguous uint8 array")
+    cap = 2 * cfg.L * cfg.E
+    acts = np.zeros((cap, 3), np.int32)
+    n, chunk, phase = C.c_int(), C.c_int(), C.c_int()
+    _chk(load().spx_plan_prefetch(C.byref(cfg), elb.ctypes.data, int(steps_done), cached.ctypes.data,
+                                  acts.ctypes.data, cap, C.byref(n), C.byref(chunk), C.byref(phase)),
+         "spx_plan_prefetch")
+    return phase.value, acts[:n.value].copy(), chunk.value
+
+
+def spx_prefetch_issue(actions, host_experts, dev_experts, expert_bytes: int, ready, resident=None, stream=None):
+    """Enqueue a plan's copies and flag updates on `stream` (host_experts: list
+    of page-locked host tensors per layer; dev_experts: device tensors per
+    layer; ready/resident: device [L][E])."""
+    import numpy as np
+    acts = np.ascontiguousarray(actions, dtype=np.int32)
+    L = len(dev_experts)
+    hp = (C.c_void_p * L)(*[t.data_ptr() for t in host_experts])
+    dp = (C.c_void_p * L)(*[t.data_ptr() for t in dev_experts])
+    E = ready.shape[-1]
+    _chk(load().spx_prefetch_issue(acts.ctypes.data, int(acts.shape[0]), hp, dp, int(expert_bytes), _p(ready),
+                                   _p(resident), L, E, _stream(stream)), "spx_prefetch_issue")

@@ -57,3 +57,4 @@ def test_spread_of_per_call_times():
     assert st == {"p10": 20.0, "median": 60.0, "p90": 100.0}
     assert bench.spread_us([0.025]) == {"p10": 25.0, "median": 25.0, "p90": 25.0}
     assert bench.spread_us([])["median"] is None
+
