@@ -143,9 +143,12 @@ SPX_API int spx_plan_prefetch(const spx_plan_cfg *cfg, const uint32_t *elb, int 
 /* Executor of a plan on `stream` (a stream parallel to the compute stream):
  * per SPX_PLAN_LOAD, one cudaMemcpyAsync of expert e's expert_bytes from
  * host_experts[l] + e*expert_bytes (page-locked host memory) to
- * dev_experts[l] + e*expert_bytes (device), then resident[l*E+e] = 1 (when
- * resident != NULL) and ready[l*E+e] = nonzero; per SPX_PLAN_EVICT,
- * ready[l*E+e] = 0 and resident[l*E+e] = 0.  ready/resident are device
+ * dev_experts[l] + e*expert_bytes (device), then resident[l*E+e] = nonzero
+ * (when resident != NULL) and ready[l*E+e] = nonzero; per SPX_PLAN_EVICT,
+ * ready[l*E+e] = 0 and resident[l*E+e] = 0.  The flags are host-to-device
+ * copies from host_flags: 8 bytes of page-locked host memory holding
+ * {1,0,0,0, 0,0,0,0} (the copy engines write them, so no SM is needed while
+ * an expert launch that waits for them holds every SM).  ready/resident are device
  * arrays [L][E]; pass ready + l*E (and resident + l*E) to layer l's verify
  * call (spx_layer_args), whose expert launch waits for each routed expert's
  * flag.  For the FP16 packed experts of spx_f16_repack, expert_bytes =
@@ -153,7 +156,7 @@ SPX_API int spx_plan_prefetch(const spx_plan_cfg *cfg, const uint32_t *elb, int 
  * action is checked before anything is enqueued. */
 SPX_API int spx_prefetch_issue(const int32_t *actions, int n_actions, const void *const *host_experts,
                                void *const *dev_experts, size_t expert_bytes, uint32_t *ready, uint8_t *resident,
-                               int L, int E, spx_stream_t stream);
+                               const uint8_t *host_flags, int L, int E, spx_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Gather tokens by expert (counting sort)  [P1 Key Contributions 4]         */

@@ -90,8 +90,8 @@ extern "C" int spx_plan_prefetch(const spx_plan_cfg *cfg, const uint32_t *elb, i
 
 extern "C" int spx_prefetch_issue(const int32_t *actions, int n_actions, const void *const *host_experts,
                                   void *const *dev_experts, size_t expert_bytes, uint32_t *ready, uint8_t *resident,
-                                  int L, int E, spx_stream_t stream) {
-    if (n_actions < 0 || (n_actions > 0 && (!actions || !host_experts || !dev_experts || !ready)))
+                                  const uint8_t *host_flags, int L, int E, spx_stream_t stream) {
+    if (n_actions < 0 || (n_actions > 0 && (!actions || !host_experts || !dev_experts || !ready || !host_flags)))
         return SPX_ERR_INVALID_ARG;
     if (L < 1 || E < 1 || expert_bytes == 0) return SPX_ERR_INVALID_ARG;
     for (int i = 0; i < n_actions; ++i) {  // every action checked before anything is enqueued
@@ -105,17 +105,21 @@ extern "C" int spx_prefetch_issue(const int32_t *actions, int n_actions, const v
         const int l = actions[3 * i], e = actions[3 * i + 1];
         const size_t f = (size_t)l * E + e;
         cudaError_t err;
+        // Flags are host-to-device copies of the caller's page-locked constants
+        // (bytes 0-3 nonzero, 4-7 zero): the copy engines write them, so no SM
+        // is needed while an expert launch that waits for them holds every SM.
+        const uint8_t *val = host_flags + (actions[3 * i + 2] == SPX_PLAN_LOAD ? 0 : 4);
         if (actions[3 * i + 2] == SPX_PLAN_LOAD) {
             // one copy per expert (its packed bytes are contiguous), then its
             // flags, in stream order behind the copy
             err = cudaMemcpyAsync(static_cast<uint8_t *>(dev_experts[l]) + (size_t)e * expert_bytes,
                                   static_cast<const uint8_t *>(host_experts[l]) + (size_t)e * expert_bytes,
                                   expert_bytes, cudaMemcpyHostToDevice, s);
-            if (err == cudaSuccess && resident) err = cudaMemsetAsync(resident + f, 1, 1, s);
-            if (err == cudaSuccess) err = cudaMemsetAsync(ready + f, 1, sizeof(uint32_t), s);  // nonzero = ready
+            if (err == cudaSuccess && resident) err = cudaMemcpyAsync(resident + f, val, 1, cudaMemcpyHostToDevice, s);
+            if (err == cudaSuccess) err = cudaMemcpyAsync(ready + f, val, sizeof(uint32_t), cudaMemcpyHostToDevice, s);
         } else {
-            err = cudaMemsetAsync(ready + f, 0, sizeof(uint32_t), s);
-            if (err == cudaSuccess && resident) err = cudaMemsetAsync(resident + f, 0, 1, s);
+            err = cudaMemcpyAsync(ready + f, val, sizeof(uint32_t), cudaMemcpyHostToDevice, s);
+            if (err == cudaSuccess && resident) err = cudaMemcpyAsync(resident + f, val, 1, cudaMemcpyHostToDevice, s);
         }
         if (err != cudaSuccess) return record_launch(err);
     }

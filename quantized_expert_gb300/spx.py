@@ -102,7 +102,7 @@ _SIGS = {
     "spx_plan_prefetch": (C.c_int, [C.POINTER(PlanCfg), C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_int,
                                     C.POINTER(C.c_int), C.POINTER(C.c_int), C.POINTER(C.c_int)]),
     "spx_prefetch_issue": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
-                                     C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
+                                     C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "spx_noalloc_status": (C.c_int, [C.c_void_p, C.c_void_p]),
 }
 
@@ -468,6 +468,17 @@ def spx_plan_prefetch(cfg: PlanCfg, elb, steps_done: int, cached):
     return phase.value, acts[:n.value].copy(), chunk.value
 
 
+_HOST_FLAGS = None
+
+
+def prefetch_host_flags():
+    """The executor's page-locked flag constants {1,0,0,0, 0,0,0,0}."""
+    global _HOST_FLAGS
+    if _HOST_FLAGS is None:
+        _HOST_FLAGS = torch.tensor([1, 0, 0, 0, 0, 0, 0, 0], dtype=torch.uint8).pin_memory()
+    return _HOST_FLAGS
+
+
 def spx_prefetch_issue(actions, host_experts, dev_experts, expert_bytes: int, ready, resident=None, stream=None):
     """Enqueue a plan's copies and flag updates on `stream` (host_experts: list
     of page-locked host tensors per layer; dev_experts: device tensors per
@@ -479,4 +490,5 @@ def spx_prefetch_issue(actions, host_experts, dev_experts, expert_bytes: int, re
     dp = (C.c_void_p * L)(*[t.data_ptr() for t in dev_experts])
     E = ready.shape[-1]
     _chk(load().spx_prefetch_issue(acts.ctypes.data, int(acts.shape[0]), hp, dp, int(expert_bytes), _p(ready),
-                                   _p(resident), L, E, _stream(stream)), "spx_prefetch_issue")
+                                   _p(resident), C.c_void_p(prefetch_host_flags().data_ptr()), L, E,
+                                   _stream(stream)), "spx_prefetch_issue")

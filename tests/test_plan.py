@@ -156,5 +156,8 @@ def test_library_planner_rejects_bad_arguments_without_side_effects():
     # the executor checks every action before enqueueing anything (no CUDA call here)
     bad_acts = np.array([[0, 1, spx.SPX_PLAN_LOAD], [5, 0, spx.SPX_PLAN_LOAD]], np.int32)
     ptrs = (C.c_void_p * 2)(256, 256)
-    assert lib.spx_prefetch_issue(bad_acts.ctypes.data, 2, ptrs, ptrs, 1024, C.c_void_p(256), None, 2, 4,
+    flags = np.array([1, 0, 0, 0, 0, 0, 0, 0], np.uint8)
+    assert lib.spx_prefetch_issue(bad_acts.ctypes.data, 2, ptrs, ptrs, 1024, C.c_void_p(256), None,
+                                  flags.ctypes.data, 2, 4, None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_prefetch_issue(bad_acts.ctypes.data, 1, ptrs, ptrs, 1024, C.c_void_p(256), None, None, 2, 4,
                                   None) == spx.SPX_ERR_INVALID_ARG
