@@ -784,11 +784,13 @@ def run_draft_batch(args):
 TL_EVENTS = ["entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "gu_last", "dn_w_first",
              "dn_h_first", "dn_last", "prod_last", "cons_done", "out_done", "sg_last", "rg_first", "rg_last",
              "w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "exit", "rd_h_last", "sd_last",
-             "w_poll", "bytes", "w_ticket", "n_ticket", "w_route", "issue"]
+             "w_poll", "bytes", "w_ticket", "n_ticket", "w_route", "issue", "p_sg", "p_rg", "p_dn", "p_fence",
+             "p_slot", "c_sg", "c_rg", "c_sd", "c_rd", "c_gu_done", "c_out"]
 TL_FIRST_EV = {"entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "dn_w_first",
                "dn_h_first", "cons_done", "rg_first"}
 TL_SUM_EV = {"w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "w_poll", "bytes", "w_ticket",
-             "n_ticket", "w_route", "issue"}
+             "n_ticket", "w_route", "issue", "p_sg", "p_rg", "p_dn", "p_fence", "p_slot", "c_sg", "c_rg", "c_sd",
+             "c_rd", "c_gu_done", "c_out"}
 
 
 def timeline_phases(buf, slots, nblocks):
@@ -855,11 +857,20 @@ def run_timeline(args):
                            w_router=sets[i % NSETS]["w_router"]) for i in range(NSETS * NINPUTS)]
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     stream = torch.cuda.Stream()
-    buf = np.zeros((8, 256, 32), np.uint64)
+    buf = np.zeros((8, 256, 48), np.uint64)
+
+    lib.spx_timeline_trace.restype = C.c_int
+    lib.spx_timeline_trace.argtypes = [C.c_void_p, C.c_size_t]
+    # per launch slot, 2 traced blocks: fill[48][4], item[64][4], unit[16][2] u32, t0 u64, nitem, pad
+    tr_words = 48 * 4 + 64 * 4 + 16 * 2 + 2 + 2
+    trbuf = np.zeros((8, 2, tr_words), np.uint32)
+    traces = {}
 
     def read():
         torch.cuda.synchronize()
         assert lib.spx_timeline_read(buf.ctypes.data, buf.size) == 0
+        assert lib.spx_timeline_trace(trbuf.ctypes.data, trbuf.nbytes) == 0
+        traces[len(traces)] = trbuf.copy()
         return buf.copy()
 
     with torch.cuda.stream(stream):
@@ -879,7 +890,11 @@ def run_timeline(args):
     line = {"timeline": "draft launch phase marks (profiling build; us after the launch's first block entered)",
             "config": {"workload": f"{s.name} draft T={T}", "blocks": nsm},
             "isolated": timeline_phases(iso, range(8), nsm),
-            "chained": timeline_phases(chained, range(1, 8), nsm)}
+            "chained": timeline_phases(chained, range(1, 8), nsm),
+            "trace": {"words": "per launch slot, blocks 0 and grid/2: fill[48][4] (wait start, stage free, issued, "
+                               "kind<<24|bytes), item[64][4] (warp<<8|kind, landed, intermediate landed, done), "
+                               "unit[16][2] (start, unit), t0 (2 words), nitem, pad; ns after block entry",
+                      "isolated_slot4": traces[0][4].tolist(), "chained_slot4": traces[1][4].tolist()}}
     print(json.dumps(line), flush=True)
 
 

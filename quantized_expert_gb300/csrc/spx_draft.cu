@@ -42,6 +42,9 @@
 namespace spx {
 
 enum : int { DK_SG = 0, DK_RG = 1, DK_SD = 2, DK_RD = 3, DK_DONE = 4 };
+// dynamic shared memory of the launch at most (the profiling build keeps its
+// marks in static shared memory next to it)
+constexpr int kDkSmemLimit = kSmemLimit - (TL_ON ? kTlEvents * 8 + (int)sizeof(TrBlock) + 64 : 0);
 constexpr int kDkData = 16896;    // largest item: 4 INT4 groups of 32 columns (or 8 of 16)
 constexpr int kDkRdGroups = 7;    // INT4 down groups (of 128 rows of I) per RD item
 // zero points of an RD item (32 per group) after its largest weight run
@@ -346,11 +349,13 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                      uint32_t zoff = 0) -> bool {
         const int st = (int)(it % nst);
         const unsigned long long tw = TL_NOW();
+        const uint32_t tr_w = TR_NOW();
         if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
             ok = false;
             return false;
         }
         const unsigned long long tis = TL_NOW();
+        const uint32_t tr_r = TR_NOW();
         TL_ADD(p.tl_slot, TL_W_EMPTY, tis - tw);
         TL_ADD(p.tl_slot, TL_BYTES, bytes + zbytes);
         h.seq = (int)it;
@@ -368,10 +373,20 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             pend[st].target = target;
             pend[st].bytes = hs_bytes;
             pend[st].t_reg = TL_NOW();
+            const unsigned long long tf = TL_NOW();
             __threadfence_block();
+            TL_ADD(p.tl_slot, TL_P_FENCE, TL_NOW() - tf);
             pstate[st] = 1;
         }
         TL_ADD(p.tl_slot, TL_ISSUE, TL_NOW() - tis);
+#if TL_ON
+        if (TR_ON() && it < (uint32_t)kTrFills) {
+            s_tr.fill[it][0] = tr_w;
+            s_tr.fill[it][1] = tr_r;
+            s_tr.fill[it][2] = TR_NOW();
+            s_tr.fill[it][3] = ((uint32_t)h.kind << 24) | ((bytes + zbytes) & 0xffffffu);
+        }
+#endif
         ++it;
         return true;
     };
@@ -380,6 +395,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         const int slot = bseq % nst;
         if (sfree[slot] != bseq) {  // the slot's previous block is still being completed
             const uint64_t t0 = global_timer_ns();
+            TL_ADD(p.tl_slot, TL_P_SLOT, 0);
             while (sfree[slot] != bseq) {
                 if (misc[0]) {
                     ok = false;
@@ -392,6 +408,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
                     return false;
                 }
             }
+            TL_ADD(p.tl_slot, TL_P_SLOT, global_timer_ns() - t0);
         }
         h.slot = slot;
         h.nitems = nitems;
@@ -500,8 +517,24 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     // routing and the ready counts are the consumers' and the poller's, who
     // wait for the preceding launch themselves), so they are issued before
     // this thread waits for it; the counters come after.
+    // profiling build: producer time per unit kind
+    int tr_nunit = 0;
+    auto timed_unit = [&](int u) -> bool {
+        const unsigned long long t = TL_NOW();
+#if TL_ON
+        if (TR_ON() && tr_nunit < kTrUnits) {
+            s_tr.unit[tr_nunit][0] = TR_NOW();
+            s_tr.unit[tr_nunit][1] = (uint32_t)u;
+        }
+        ++tr_nunit;
+#endif
+        const bool r = run_unit(u);
+        TL_ADD(p.tl_slot, u < nSGb ? TL_P_SG : (na >= 0 && u - nSGb < na * g.rg_blocks) ? TL_P_RG : TL_P_DN,
+               TL_NOW() - t);
+        return r;
+    };
     uint32_t tkA = blockIdx.x / kDkShards;
-    const bool more = run_unit((int)tkA * kDkShards + shard);
+    const bool more = timed_unit((int)tkA * kDkShards + shard);
     TL_FIRST(p.tl_slot, TL_PROD_STATIC);
     griddep_wait();
     TL_FIRST(p.tl_slot, TL_PROD_GRIDDEP);
@@ -510,10 +543,10 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
         while (true) {
             tkA = nsm + atomicAdd(ctr, 1u);
             TL_TICKET(p.tl_slot, tkB, misc + 15);
-            if (!run_unit((int)tkB * kDkShards + shard)) break;
+            if (!timed_unit((int)tkB * kDkShards + shard)) break;
             tkB = nsm + atomicAdd(ctr, 1u);
             TL_TICKET(p.tl_slot, tkA, misc + 15);
-            if (!run_unit((int)tkA * kDkShards + shard)) break;
+            if (!timed_unit((int)tkA * kDkShards + shard)) break;
         }
     }
     if (ok) {
@@ -789,7 +822,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
     griddep_launch_dependents();
-    if (threadIdx.x == 0) TL_FIRST(p.tl_slot, TL_ENTRY);
+    TL_INIT();
     const int nst = p.nstages;
     const DkLayout L = dk_layout(p.T, p.H, nst, p.k, p.nact_max, p.E, Q2K || Q4K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -822,6 +855,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         fence_mbar_init();
     }
     __syncthreads();
+    if (threadIdx.x == 0) TL_FIRST(p.tl_slot, TL_ENTRY);
     if (warp == kDkCons) {
         if (lane == 0) dk_producer(p, smem, L);
         return;
@@ -1048,6 +1082,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         }
         if (!got) break;
         const DHeader h = hdrs[st];
+        const uint32_t tr_got = TR_NOW();
         if (TL_ON && lane == 0) {
             TL_ADD(p.tl_slot, TL_W_FULL, TL_NOW() - twf);
             TL_FIRST(p.tl_slot, TL_FIRST_FILL);
@@ -1075,6 +1110,21 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 if (h.kind == DK_RD) TL_LAST(p.tl_slot, TL_RD_H_LAST);
             }
         }
+        const unsigned long long tc = TL_NOW();  // profiling build: item compute start
+        const uint32_t tr_h = TR_NOW();
+#if TL_ON
+        auto tr_item = [&](int kind) {
+            if (TR_ON()) {
+                const uint32_t i = atomicAdd(&s_tr.nitem, 1u);
+                if (i < (uint32_t)kTrItems) {
+                    s_tr.item[i][0] = ((uint32_t)warp << 8) | (uint32_t)kind;
+                    s_tr.item[i][1] = tr_got;
+                    s_tr.item[i][2] = tr_h;
+                    s_tr.item[i][3] = TR_NOW();
+                }
+            }
+        };
+#endif
         if (h.kind == DK_SG) {
             // shared gate/up: 16 columns (tiles: gate, up), k-steps [k0, k0+n) of H
             // two accumulator sets (even / odd k-steps) in registers: the k loop
@@ -1110,8 +1160,14 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                     }
                 }
             }
+            const unsigned long long tg = TL_NOW();
             gu_done(h, 1, p.hf_s + (size_t)h.blk * T * 4, 0, p.rdy_s + h.blk / kDkSdSteps, 1);
             if (TL_ON && lane == 0) {
+                TL_ADD(p.tl_slot, TL_C_GU_DONE, TL_NOW() - tg);
+                TL_ADD(p.tl_slot, TL_C_SG, TL_NOW() - tc);
+#if TL_ON
+                tr_item(DK_SG);
+#endif
                 TL_LAST(p.tl_slot, TL_SG_LAST);
                 TL_LAST(p.tl_slot, TL_GU_LAST);
                 TL_ADD(p.tl_slot, TL_N_SG, 1);
@@ -1209,9 +1265,15 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                     }
                 }
             }
+            const unsigned long long tg = TL_NOW();
             gu_done(h, MS, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.blk * MS) * T * 4, (size_t)T * 4,
                     p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / geo.rd_gpi, MS);
             if (TL_ON && lane == 0) {
+                TL_ADD(p.tl_slot, TL_C_GU_DONE, TL_NOW() - tg);
+                TL_ADD(p.tl_slot, TL_C_RG, TL_NOW() - tc);
+#if TL_ON
+                tr_item(DK_RG);
+#endif
                 TL_LAST(p.tl_slot, TL_RG_LAST);
                 TL_LAST(p.tl_slot, TL_GU_LAST);
                 TL_ADD(p.tl_slot, TL_N_RG, 1);
@@ -1249,6 +1311,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 __threadfence_block();
             }
             const int n0 = 32 * h.blk + 4 * g;
+            const unsigned long long to = TL_NOW();
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int col = 2 * q4 + hf;
@@ -1263,6 +1326,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 }
             }
             if (TL_ON && lane == 0) {
+                TL_ADD(p.tl_slot, TL_C_OUT, TL_NOW() - to);
+                TL_ADD(p.tl_slot, TL_C_SD, TL_NOW() - tc);
+#if TL_ON
+                tr_item(DK_SD);
+#endif
                 TL_LAST(p.tl_slot, TL_SD_LAST);
                 TL_LAST(p.tl_slot, TL_DN_LAST);
                 TL_ADD(p.tl_slot, TL_N_SD, 1);
@@ -1344,6 +1412,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
             const int n0 = 32 * h.blk + 4 * g;
             const int rmax = p.mode == 0 ? T * p.k : T;
+            const unsigned long long to = TL_NOW();
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 if (row[hf] >= 0 && row[hf] < rmax) {
@@ -1356,6 +1425,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 }
             }
             if (TL_ON && lane == 0) {
+                TL_ADD(p.tl_slot, TL_C_OUT, TL_NOW() - to);
+                TL_ADD(p.tl_slot, TL_C_RD, TL_NOW() - tc);
+#if TL_ON
+                tr_item(DK_RD);
+#endif
                 TL_LAST(p.tl_slot, TL_DN_LAST);
                 TL_ADD(p.tl_slot, TL_N_RD, 1);
             }
@@ -1407,6 +1481,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         if (ctid == 0) TL_LAST(p.tl_slot, TL_OUT_DONE);
     }
     if (ctid == 0) TL_LAST(p.tl_slot, TL_EXIT);
+    if (TL_ON) {
+        __syncwarp();
+        all_sync();
+        TL_FLUSH(p.tl_slot, ctid);
+    }
 }
 
 // ------------------------------------------------------------ launching --
@@ -1439,7 +1518,7 @@ static int configure_draft(int ki) {
     if (ki < 0 || ki >= kDraftInstances) return SPX_ERR_UNSUPPORTED;
     if (!configured[ki][dev]) {
         cudaError_t err =
-            cudaFuncSetAttribute(draft_instance(ki), cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+            cudaFuncSetAttribute(draft_instance(ki), cudaFuncAttributeMaxDynamicSharedMemorySize, kDkSmemLimit);
         if (err != cudaSuccess) return record_launch(err);
         configured[ki][dev] = 1;
     }
@@ -1462,7 +1541,7 @@ bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k, bool kq)
     if (kq && (H % 256 || S != 16)) return false;
     if (T < 1 || T > 8 || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
     if (I_s % 16 || E < 1 || k < 1 || E > kMaxE || T * k > kMaxSlots) return false;
-    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E, kq).total <= kSmemLimit;
+    return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E, kq).total <= kDkSmemLimit;
 }
 
 int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratch_base, bool pdl, cudaStream_t s) {
@@ -1527,8 +1606,8 @@ int launch_draft(const EngineParams &e, const DraftRouting *rt, size_t ws_scratc
     p.rdy_r = reinterpret_cast<int *>(ws + sc.rdy_r);
     int nst = 12;  // <= kDkMaxStages
     DkLayout L = dk_layout(e.T, e.H, nst, e.k, p.nact_max, e.E, kq);
-    while (nst > 4 && L.total > kSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E, kq);
-    if (L.total > kSmemLimit) return SPX_ERR_UNSUPPORTED;
+    while (nst > 4 && L.total > kDkSmemLimit) L = dk_layout(e.T, e.H, --nst, e.k, p.nact_max, e.E, kq);
+    if (L.total > kDkSmemLimit) return SPX_ERR_UNSUPPORTED;
     p.nstages = nst;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
@@ -1566,8 +1645,14 @@ extern "C" __attribute__((visibility("default"))) int spx_timeline_reset(void) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, spx::g_tl) != cudaSuccess) return SPX_ERR_CUDA;
     if (cudaMemset(p, 0, sizeof(spx::g_tl)) != cudaSuccess) return SPX_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, spx::g_tr) != cudaSuccess) return SPX_ERR_CUDA;
+    if (cudaMemset(p, 0, sizeof(spx::g_tr)) != cudaSuccess) return SPX_ERR_CUDA;
     spx::g_tl_next.store(0);
     return SPX_OK;
+}
+extern "C" __attribute__((visibility("default"))) int spx_timeline_trace(void *host, size_t bytes) {
+    if (!host || bytes < sizeof(spx::g_tr)) return SPX_ERR_INVALID_ARG;
+    return cudaMemcpyFromSymbol(host, spx::g_tr, sizeof(spx::g_tr)) == cudaSuccess ? SPX_OK : SPX_ERR_CUDA;
 }
 extern "C" __attribute__((visibility("default"))) int spx_timeline_read(unsigned long long *host, size_t words) {
     if (!host || words < sizeof(spx::g_tl) / 8) return SPX_ERR_INVALID_ARG;

@@ -20,7 +20,7 @@ def test_timeline_phases_on_synthetic_marks():
     complemented, last marks plain, sums per block; times relative to the
     launch's first block."""
     import numpy as np
-    buf = np.zeros((8, 256, 32), np.uint64)
+    buf = np.zeros((8, 256, 48), np.uint64)
     ev = bench.TL_EVENTS
     for sl in range(8):
         base = 10 ** 9 + sl * 30000
