@@ -781,6 +781,157 @@ def run_draft_batch(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefetch(args):
+    """The Layer-Aware Prefetch Planner on GB300: L DeepSeek-V2-Lite-shaped
+    layers whose routed FP16 verify experts live in page-locked host (Grace)
+    memory and reach HBM over NVLink-C2C, one speculation cycle of K draft
+    steps then the verify pass.  Three arms on the same inputs: every expert
+    resident (no copy); on demand (each layer's verify experts copied when the
+    verify pass starts, the verify launches waiting on their ready flags); and
+    planned (the planner's copies issued at the draft-chunk boundaries from the
+    lookahead counters, the rest loaded behind the verify launches).  Prints
+    one JSON line: cycle and verify-pass us of each arm, and the share of the
+    on-demand copy wait that the plan hides."""
+    import ctypes as C  # noqa: F401
+    import torch
+    from quantized_expert_gb300 import build as B, spx
+    B.build()
+    lib = spx.load()
+    s = W.CONFIGS[CYCLE]
+    L, K, E, k, H, Tv = min(args.prefetch_layers, s.layers), s.K, s.E, s.k, s.H, s.T_verify
+    lays = [make_weight_set(s, l, torch, spx) for l in range(L)]
+    eb = lib.spx_f16_packed_bytes(1, H, s.I)
+    host = [ly["f16"].buf.cpu().pin_memory() for ly in lays]
+    dev = [ly["f16"].buf for ly in lays]
+    f16 = [spx.PackedF16(d, E, H, s.I) for d in dev]
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    f16dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()  # noqa: E731
+    xd = [[f16dev(W.gen_x(s, 1, layer=l, step=st)) for l in range(L)] for st in range(1, K + 1)]
+    lgd = [[torch.from_numpy(W.draft_logits(s, l, st)).cuda() for l in range(L)] for st in range(1, K + 1)]
+    xv = [f16dev(W.gen_x(s, Tv, layer=l, step=K + 1, which=1)) for l in range(L)]
+    lgv_host = [W.verify_logits(s, l) for l in range(L)]
+    lgv = [torch.from_numpy(a).cuda() for a in lgv_host]
+    verify_need = [sorted(set(oracle_free_topk(a, k).reshape(-1).tolist())) for a in lgv_host]
+    elb = torch.zeros(L, E, dtype=torch.int32, device="cuda")
+    elb_host = torch.zeros(L, E, dtype=torch.int32).pin_memory()
+    ready = torch.zeros(L, E, dtype=torch.int32, device="cuda")
+    resident = torch.zeros(L, E, dtype=torch.uint8, device="cuda")
+    ws_d, ws_v = spx.new_workspace(1, H, s.I, E, k, s.I_s), spx.new_workspace(Tv, H, s.I, E, k, s.I_s)
+    r_d, r_v = spx.Routing.empty(1, E, k), spx.Routing.empty(Tv, E, k)
+    od = torch.empty(1, H, dtype=torch.float16, device="cuda")
+    ov = torch.empty(Tv, H, dtype=torch.float16, device="cuda")
+    dargs = [[spx.layer_args(0, xd[st][l], E, k, s.renorm, lgd[st][l], r_d, od, ws_d, w4=lays[l]["w4"],
+                             shared=lays[l]["shared"], elb=elb, layer=l) for l in range(L)] for st in range(K)]
+    vres = [spx.layer_args(1, xv[l], E, k, s.renorm, lgv[l], r_v, ov, ws_v, f16=f16[l], shared=lays[l]["shared"])
+            for l in range(L)]
+    vflag = [spx.layer_args(1, xv[l], E, k, s.renorm, lgv[l], r_v, ov, ws_v, f16=f16[l], shared=lays[l]["shared"],
+                            resident=resident[l], ready=ready[l]) for l in range(L)]
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def draft_steps(a, b):
+        with torch.cuda.stream(stream):
+            for st in range(a, b):
+                for l in range(L):
+                    spx.spx_moe_layer(dargs[st][l][0], stream)
+
+    # measured inputs of the plan: one draft step through the L layers, one expert's copy
+    draft_steps(0, K)
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    draft_steps(0, K)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step_us = e0.elapsed_time(e1) * 1e3 / K
+    with torch.cuda.stream(side):
+        e0.record(side)
+        for i in range(8):
+            dev[0][(i % E) * eb:(i % E + 1) * eb].copy_(host[0][(i % E) * eb:(i % E + 1) * eb], non_blocking=True)
+        e1.record(side)
+    torch.cuda.synchronize()
+    copy_us = e0.elapsed_time(e1) * 1e3 / 8
+    cfg = spx.PlanCfg(L, E, K, E, 1, step_us, copy_us)
+
+    def offload():
+        torch.cuda.synchronize()
+        for d in dev:
+            d.zero_()
+        ready.zero_()
+        resident.zero_()
+        torch.cuda.synchronize()
+
+    def verify_pass(flags):
+        with torch.cuda.stream(stream):
+            for l in range(L):
+                spx.spx_moe_layer((vflag if flags else vres)[l][0], stream)
+
+    def load_all(need_by_layer, cached):
+        acts = [[l, e, spx.SPX_PLAN_LOAD] for l in range(L) for e in need_by_layer[l] if not cached[l, e]]
+        for l in range(L):
+            cached[l, need_by_layer[l]] = 1
+        spx.spx_prefetch_issue(np.array(acts, np.int32).reshape(-1, 3), host, dev, eb, ready, resident, stream=side)
+        return len(acts)
+
+    res = {}
+    for arm in ("resident", "on_demand", "planned"):
+        reps = []
+        for rep in range(max(1, min(args.steps, 5))):
+            if arm == "resident":
+                for l in range(L):  # restore the weights once; they stay
+                    if rep == 0:
+                        dev[l].copy_(host[l], non_blocking=True)
+                torch.cuda.synchronize()
+            else:
+                offload()
+            spx.spx_elb_reset(elb, stream)
+            cached = np.zeros((L, E), np.uint8)
+            c0, c1, c2 = ev(), ev(), ev()
+            c0.record(stream)
+            nload = 0
+            if arm == "planned":
+                done, phase = 0, spx.SPX_PLAN_COLD_START
+                while True:
+                    if done:
+                        spx.spx_elb_read(elb, elb_host, stream)
+                        stream.synchronize()  # the snapshot at the chunk boundary
+                    snap = elb_host.numpy().astype(np.uint32) if done else np.zeros((L, E), np.uint32)
+                    phase, acts, chunk = spx.spx_plan_prefetch(cfg, snap, done, cached)
+                    side.wait_stream(stream)
+                    spx.spx_prefetch_issue(acts, host, dev, eb, ready, resident, stream=side)
+                    nload += int((acts[:, 2] == spx.SPX_PLAN_LOAD).sum()) if len(acts) else 0
+                    if phase == spx.SPX_PLAN_FINAL_CLEANUP:
+                        break
+                    draft_steps(done, done + chunk)
+                    done += chunk
+            else:
+                draft_steps(0, K)
+            c1.record(stream)
+            if arm != "resident":
+                side.wait_stream(stream)
+                nload += load_all(verify_need, cached)  # the verify's experts not cached yet
+            verify_pass(arm != "resident")
+            c2.record(stream)
+            torch.cuda.synchronize()
+            reps.append((c0.elapsed_time(c2) * 1e3, c1.elapsed_time(c2) * 1e3, nload))
+            assert spx.spx_workspace_status(ws_v) == 0 and spx.spx_workspace_status(ws_d) == 0
+        res[arm] = {"cycle_us": round(statistics.median(r[0] for r in reps), 1),
+                    "verify_pass_us": round(statistics.median(r[1] for r in reps), 1),
+                    "expert_loads": reps[-1][2]}
+    wait_od = res["on_demand"]["verify_pass_us"] - res["resident"]["verify_pass_us"]
+    wait_pl = res["planned"]["verify_pass_us"] - res["resident"]["verify_pass_us"]
+    line = {"metric": "verify-pass copy wait hidden by the Layer-Aware Prefetch Planner",
+            "config": {"workload": f"{s.name} shape, {L} layers, K={K} draft steps (T=1) then verify (T={Tv}); routed "
+                                   f"FP16 experts in page-locked host memory, copied over NVLink-C2C",
+                       "expert_bytes": int(eb), "step_us": round(step_us, 1), "copy_us_per_expert": round(copy_us, 1),
+                       "link_gbs": round(eb / (copy_us * 1e-6) / 1e9, 1)},
+            "arms": res,
+            "hidden_share": round(1.0 - wait_pl / wait_od, 3) if wait_od > 0 else None,
+            "reps": max(1, min(args.steps, 5))}
+    print(json.dumps(line), flush=True)
+
+
 TL_EVENTS = ["entry", "prod_static", "prod_griddep", "x_staged", "routed", "first_fill", "gu_last", "dn_w_first",
              "dn_h_first", "dn_last", "prod_last", "cons_done", "out_done", "sg_last", "rg_first", "rg_last",
              "w_full", "w_hfull", "w_empty", "n_sg", "n_rg", "n_sd", "n_rd", "exit", "rd_h_last", "sd_last",
@@ -862,7 +1013,7 @@ def run_timeline(args):
     lib.spx_timeline_trace.restype = C.c_int
     lib.spx_timeline_trace.argtypes = [C.c_void_p, C.c_size_t]
     # per launch slot, 2 traced blocks: fill[48][4], item[64][4], unit[16][2] u32, t0 u64, nitem, pad
-    tr_words = 48 * 4 + 64 * 4 + 16 * 2 + 2 + 2
+    tr_words = 48 * 4 + 64 * 4 + 16 * 2 + 2 + 2 + 8
     trbuf = np.zeros((8, 2, tr_words), np.uint32)
     traces = {}
 
@@ -893,7 +1044,8 @@ def run_timeline(args):
             "chained": timeline_phases(chained, range(1, 8), nsm),
             "trace": {"words": "per launch slot, blocks 0 and grid/2: fill[48][4] (wait start, stage free, issued, "
                                "kind<<24|bytes), item[64][4] (warp<<8|kind, landed, intermediate landed, done), "
-                               "unit[16][2] (start, unit), t0 (2 words), nitem, pad; ns after block entry",
+                               "unit[16][2] (start, unit), t0 (2 words), nitem, pad, route[8] (routing warp: "
+                               "start, selected, outputs, tables, published); ns after block entry",
                       "isolated_slot4": traces[0][4].tolist(), "chained_slot4": traces[1][4].tolist()}}
     print(json.dumps(line), flush=True)
 
@@ -921,11 +1073,16 @@ def main():
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
     ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
     ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"], help="with --draft-batch: GGUF experts instead of INT4")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="verify copy wait hidden by the prefetch plan (prints its own line)")
+    ap.add_argument("--prefetch-layers", type=int, default=4)
     ap.add_argument("--timeline", action="store_true",
                     help="draft launch phase marks from the profiling build (prints its own line)")
     args = ap.parse_args()
     globals()["NSETS"] = max(1, args.sets)
-    if args.timeline:
+    if args.prefetch:
+        run_prefetch(args)
+    elif args.timeline:
         run_timeline(args)
     elif args.loop:
         run_loop(args)

@@ -41,10 +41,10 @@
 
 namespace spx {
 
-enum : int { DK_SG = 0, DK_RG = 1, DK_SD = 2, DK_RD = 3, DK_DONE = 4 };
+enum : int { DK_SG = 0, DK_RG = 1, DK_SD = 2, DK_RD = 3, DK_DONE = 4, DK_NOP = 5 };
 // dynamic shared memory of the launch at most (the profiling build keeps its
 // marks in static shared memory next to it)
-constexpr int kDkSmemLimit = kSmemLimit - (TL_ON ? kTlEvents * 8 + (int)sizeof(TrBlock) + 64 : 0);
+constexpr int kDkSmemLimit = kSmemLimit - (TL_ON ? 4096 : 0);
 constexpr int kDkData = 16896;    // largest item: 4 INT4 groups of 32 columns (or 8 of 16)
 constexpr int kDkRdGroups = 7;    // INT4 down groups (of 128 rows of I) per RD item
 // zero points of an RD item (32 per group) after its largest weight run
@@ -68,12 +68,23 @@ constexpr int kDkMaxStages = 16;  // ring stages (and gate/up slots) at most
 constexpr int kDkDBatch = 2;      // down items per queue unit
 constexpr int kDkShards = 8;      // independent queue counters (SM b uses shard b % kDkShards)
 constexpr uint32_t kDkSleepNs = 1000;  // longest sleep of a waiting warp inside one try_wait
-// Eleven consumer warps, then the producer and the poller (13 warps).  Warps
-// share an SM sub-partition by warp index mod 4, so four warps share one
-// sub-partition's 16K registers: a thread may use at most 128 (kDkMaxRegs).
+// Warp roles.  An SM's four sub-partitions (each with its own scheduler,
+// instruction cache and tensor pipe) take warps by index mod 4.  The producer
+// (warp 3) and the poller (warp 7) share sub-partition 3 with one consumer
+// warp (11); the other ten consumer warps fill sub-partitions 0-2, so the
+// producer competes with little consumer work while the consumers' tensor-
+// core products use all four pipes.  Four warps share one sub-partition's
+// 16K registers: a thread may use at most 128 (kDkMaxRegs).
 constexpr int kDkCons = 11;
-constexpr int kDkThreads = (kDkCons + 2) * 32;
-constexpr int kDkMaxRegs = 65536 / (((kDkCons + 2 + 3) / 4) * 4 * 32) / 8 * 8;
+constexpr int kDkWarps = 13;
+constexpr int kDkProducerWarp = 3, kDkPollerWarp = 7;
+constexpr int kDkThreads = kDkWarps * 32;
+constexpr int kDkMaxRegs = 65536 / (((kDkWarps + 3) / 4) * 4 * 32) / 8 * 8;
+// consumer index 0..10 of a consumer warp
+__host__ __device__ constexpr int dk_consumer_index(int warp) {
+    return warp - (warp > kDkProducerWarp) - (warp > kDkPollerWarp);
+}
+static_assert(dk_consumer_index(kDkWarps - 1) == kDkCons - 1, "eleven consumer warps");
 static_assert(kDkMaxRegs >= 64, "registers per thread of the draft launch");
 
 struct __align__(16) DHeader {
@@ -268,14 +279,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                                        int32_t *status, uint64_t budget_ns) {
+                                                        int32_t *status, uint64_t budget_ns,
+                                                        int32_t site = SITE_HSLICE) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (*abort) return false;
         if (mbar_try_wait_sleep(bar, parity, kDkSleepNs)) return true;
         if (global_timer_ns() - t0 > budget_ns) {
-            atomicCAS(status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            record_timeout(status, site);
             *abort = 1;
             return false;
         }
@@ -295,18 +307,36 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 // memory, [5] number of active experts.
 
 // ------------------------------------------------------------- producer --
+// One ring fill as a producer lane describes it: the stage header, the
+// weights (and zero points) to copy, and for a down item the h slice the
+// poller copies once it is complete.
+struct DFill {
+    DHeader h;
+    const uint8_t *src;
+    const void *zsrc, *hsrc;
+    const int *rdy;
+    uint32_t bytes, zbytes, zoff, hs_bytes;
+    int target;
+};
+
 // Queue tickets: [shared gate/up blocks][routed gate/up blocks][down items in
 // pairs].  Every gate/up block is dequeued before any down item, and a block's
 // items enter this SM's ring before anything it dequeues later, so h always
 // completes: the down items that wait for it never hold up a gate/up item.
-__device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L) {
+//
+// The whole producer warp runs this: lane j describes fill j of the current
+// queue unit, and up to min(stages, 16) lanes issue their fills at once, so
+// the serial work per fill is the copy issue itself (a lone thread spent ~0.4
+// us of address arithmetic per fill).  Lane 0 takes the queue tickets.
+__device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L, int lane) {
+    constexpr unsigned kAll = 0xffffffffu;
     const int nst = p.nstages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + nst;
     uint64_t *hfull = empty + nst;
     DHeader *hdrs = reinterpret_cast<DHeader *>(smem + L.hdrs);
     volatile int *misc = reinterpret_cast<volatile int *>(smem + L.misc);
-    int *act = reinterpret_cast<int *>(smem + L.act);
+    const int *act = reinterpret_cast<const int *>(smem + L.act);
     volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
     volatile int *pstate = reinterpret_cast<volatile int *>(smem + L.pstate);
     DPend *pend = reinterpret_cast<DPend *>(smem + L.pend);
@@ -318,123 +348,173 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     const int NQ = H / 32;
     const int nSGb = p.sh ? g.sg_cols : 0;
     const int nSD = p.sh ? NQ * g.sd_nr : 0;
-    bool ok = true;
+    const int ngroups = H / (dk_kquant(p.fmt) ? 256 : 128);  // gate/up groups (K-quant: super-blocks) of H
+    const size_t rg_gb = p.fmt == DK_FMT_Q8    ? (size_t)kQ8GroupBytes
+                         : p.fmt == DK_FMT_Q2K ? (size_t)kQ2kSbBytes
+                         : p.fmt == DK_FMT_Q4K ? (size_t)kQ4kSbBytes
+                                               : w4_group_bytes(p.S);
+    const size_t rg_ub = p.fmt == DK_FMT_Q8    ? q8_unit_bytes(H)
+                         : p.fmt == DK_FMT_Q2K ? q2k_unit_bytes(H)
+                         : p.fmt == DK_FMT_Q4K ? q4k_unit_bytes(H)
+                                               : w4_unit_bytes(H, p.S);
+    const uint32_t rd_gb = q8dn ? (uint32_t)kQ8GroupBytes : (uint32_t)kW4ColGroupBytes;
+    const int wmax = nst < 16 ? nst : 16;  // fills issued per round: distinct stages
+    bool ok = true;                        // warp-uniform
     int na = -1;
+    uint32_t it = 0;         // fills issued so far
+    uint32_t hpar_bits = 0;  // bit st: phase parity of hfull[st] for the stage's next down fill
+    int bseq = 0;            // gate/up column blocks taken so far
+    // A bounded wait gave up: record it once and raise the block's abort flag.
+    auto timed_out = [&](int32_t site) {
+        if (lane == 0) {
+            record_timeout(&p.hdr->status, site);
+            misc[0] = 1;
+        }
+        ok = false;
+    };
+    auto expired = [&](uint64_t t0) { return __any_sync(kAll, global_timer_ns() - t0 > p.wait_budget_ns); };
+    // Shared words other warps write are read by lane 0 and broadcast: every
+    // lane then takes the same branch, so the lanes of this warp always meet
+    // at the same collective (lanes that read such a word each for itself can
+    // see different values and drift apart).
+    auto rd0 = [&](const volatile int *w) {
+        int v = 0;
+        if (lane == 0) v = *w;
+        return __shfl_sync(kAll, v, 0);
+    };
     // Active experts: the consumer warps route the launch's tokens into shared
     // memory at start; routed work waits for that (shared gate/up does not).
     auto n_act = [&]() -> int {
         if (na < 0) {
             const uint64_t t0 = global_timer_ns();
-            const unsigned long long twr = TL_NOW();
-            while (!misc[4]) {
-                if (misc[0] || global_timer_ns() - t0 > p.wait_budget_ns) {
-                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
-                    misc[0] = 1;
+            while (!rd0(misc + 4)) {  // a sleeping poll: the consumer warps route meanwhile
+                if (rd0(misc)) {
                     ok = false;
                     return na = 0;
                 }
+                if (expired(t0)) {
+                    timed_out(SITE_ROUTING);
+                    return na = 0;
+                }
+                __nanosleep(64);
             }
             __threadfence_block();
-            na = misc[5];
-            TL_ADD(p.tl_slot, TL_W_ROUTE, TL_NOW() - twr);
+            na = rd0(misc + 5);
         }
         return na;
     };
-    uint32_t it = 0;
-    uint32_t hpar_bits = 0;  // bit st: phase parity of hfull[st] for the stage's next down fill
-    // One ring fill: weights; a down item's h slice is left to the poller,
-    // which counts it on the same barrier.
-    auto issue = [&](DHeader &h, const uint8_t *src, uint32_t bytes, const void *hsrc, uint32_t hs_bytes,
-                     const int *rdy, int target, const void *zsrc = nullptr, uint32_t zbytes = 0,
-                     uint32_t zoff = 0) -> bool {
-        const int st = (int)(it % nst);
-        const unsigned long long tw = TL_NOW();
-        const uint32_t tr_w = TR_NOW();
-        if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status, p.wait_budget_ns)) {
-            ok = false;
-            return false;
-        }
-        const unsigned long long tis = TL_NOW();
-        const uint32_t tr_r = TR_NOW();
-        TL_ADD(p.tl_slot, TL_W_EMPTY, tis - tw);
-        TL_ADD(p.tl_slot, TL_BYTES, bytes + zbytes);
-        h.seq = (int)it;
-        h.hpar = (int)((hpar_bits >> st) & 1u);
-        hdrs[st] = h;
-        uint8_t *dst = ring + (size_t)st * L.stage;
-        mbar_arrive_expect_tx(&full[st], bytes + zbytes);
-        bulk_g2s(dst, src, bytes, &full[st], pol);
-        if (zbytes) bulk_g2s(dst + zoff, zsrc, zbytes, &full[st], pol);
-        if (hs_bytes) {
-            mbar_arrive_expect_tx(&hfull[st], hs_bytes);  // completed by the poller's copy
-            hpar_bits ^= 1u << st;
-            pend[st].src = hsrc;
-            pend[st].rdy = rdy;
-            pend[st].target = target;
-            pend[st].bytes = hs_bytes;
-            pend[st].t_reg = TL_NOW();
-            const unsigned long long tf = TL_NOW();
-            __threadfence_block();
-            TL_ADD(p.tl_slot, TL_P_FENCE, TL_NOW() - tf);
-            pstate[st] = 1;
-        }
-        TL_ADD(p.tl_slot, TL_ISSUE, TL_NOW() - tis);
-#if TL_ON
-        if (TR_ON() && it < (uint32_t)kTrFills) {
-            s_tr.fill[it][0] = tr_w;
-            s_tr.fill[it][1] = tr_r;
-            s_tr.fill[it][2] = TR_NOW();
-            s_tr.fill[it][3] = ((uint32_t)h.kind << 24) | ((bytes + zbytes) & 0xffffffu);
-        }
-#endif
-        ++it;
-        return true;
-    };
-    int bseq = 0;
+    // Slot of the next gate/up column block (its partial sums meet there).
     auto take_slot = [&](DHeader &h, int nitems) -> bool {
         const int slot = bseq % nst;
-        if (sfree[slot] != bseq) {  // the slot's previous block is still being completed
+        if (rd0(sfree + slot) != bseq) {  // the slot's previous block is still being completed
             const uint64_t t0 = global_timer_ns();
-            TL_ADD(p.tl_slot, TL_P_SLOT, 0);
-            while (sfree[slot] != bseq) {
-                if (misc[0]) {
+            while (rd0(sfree + slot) != bseq) {
+                if (rd0(misc)) {
                     ok = false;
                     return false;
                 }
-                if (global_timer_ns() - t0 > p.wait_budget_ns) {
-                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
-                    misc[0] = 1;
-                    ok = false;
+                if (expired(t0)) {
+                    timed_out(SITE_SLOT);
                     return false;
                 }
+                __nanosleep(64);
             }
-            TL_ADD(p.tl_slot, TL_P_SLOT, global_timer_ns() - t0);
         }
         h.slot = slot;
         h.nitems = nitems;
         h.bseq = bseq++;
         return true;
     };
-    // Issues every item of queue unit u; false once the queue is exhausted (or on failure).
-    auto run_unit = [&](int u) -> bool {
-        if (u < 0) return false;  // a corrupted queue counter (workspace not zeroed): stop
+    // Issues fills 0..n-1 of the unit (lane j holds fill j), in rounds of at
+    // most wmax lanes whose stages are all free.
+    auto issue_fills = [&](const DFill &f, int n) -> bool {
+        __syncwarp();  // lanes that finished describing their fill early wait here
+        for (int base = 0; base < n; base += wmax) {
+            const int cnt = min(wmax, n - base);
+            const bool mine = lane >= base && lane < base + cnt;
+            const uint32_t fi = it + (uint32_t)(lane - base);
+            const int st = mine ? (int)(fi % (uint32_t)nst) : 0;
+            const uint32_t par = ((fi / (uint32_t)nst) & 1u) ^ 1u;
+            const uint32_t tr_w = TR_NOW();
+            bool free_ = !mine || mbar_try_wait(&empty[st], par);
+            if (!__all_sync(kAll, free_)) {
+                const uint64_t t0 = global_timer_ns();
+                while (true) {
+                    if (!free_) free_ = mbar_try_wait_sleep(&empty[st], par, kDkSleepNs);
+                    if (__all_sync(kAll, free_)) break;
+                    if (rd0(misc)) {
+                        ok = false;
+                        return false;
+                    }
+                    if (expired(t0)) {
+                        timed_out(SITE_STAGE);
+                        return false;
+                    }
+                }
+            }
+            const uint32_t tr_r = TR_NOW();
+            const bool hs = mine && f.hs_bytes;
+            if (mine) {
+                DHeader h = f.h;
+                h.seq = (int)fi;
+                h.hpar = (int)((hpar_bits >> st) & 1u);
+                hdrs[st] = h;
+                uint8_t *dst = ring + (size_t)st * L.stage;
+                mbar_arrive_expect_tx(&full[st], f.bytes + f.zbytes);
+                if (f.bytes) bulk_g2s(dst, f.src, f.bytes, &full[st], pol);
+                if (f.zbytes) bulk_g2s(dst + f.zoff, f.zsrc, f.zbytes, &full[st], pol);
+                if (hs) {
+                    mbar_arrive_expect_tx(&hfull[st], f.hs_bytes);  // completed by the poller's copy
+                    pend[st].src = f.hsrc;
+                    pend[st].rdy = f.rdy;
+                    pend[st].target = f.target;
+                    pend[st].bytes = f.hs_bytes;
+                    pend[st].t_reg = TL_NOW();
+                }
+            }
+            const uint32_t hmask = __reduce_or_sync(kAll, hs ? (1u << st) : 0u);
+            if (hmask) {
+                __threadfence_block();  // the pending entries before their flags
+                if (hs) pstate[st] = 1;
+                hpar_bits ^= hmask;
+            }
+#if TL_ON
+            if (mine && TR_ON() && fi < (uint32_t)kTrFills) {
+                s_tr.fill[fi][0] = tr_w;
+                s_tr.fill[fi][1] = tr_r;
+                s_tr.fill[fi][2] = TR_NOW();
+                s_tr.fill[fi][3] = ((uint32_t)f.h.kind << 24) | ((f.bytes + f.zbytes) & 0xffffffu);
+            }
+#else
+            (void)tr_w;
+            (void)tr_r;
+#endif
+            it += (uint32_t)cnt;
+            if (lane == 0) misc[14] = (int)it;  // fills issued (read when a wait gives up)
+        }
+        return true;
+    };
+    // Fills of queue unit u, lane j describing fill j: the fill count, 0 to
+    // skip the unit, -1 once the queue is exhausted (or on failure).
+    auto expand = [&](int u, DFill &f) -> int {
+        if (u < 0) return -1;  // a corrupted queue counter (workspace not zeroed): stop
+        f = DFill{};
         if (u < nSGb) {
             DHeader h{};
             h.kind = DK_SG;
             h.blk = u;
-            if (!take_slot(h, g.sg_nr)) return false;
-            for (int r = 0; r < g.sg_nr; ++r) {
-                h.r = r;
-                h.k0 = r * g.sg_nks;
-                h.n = g.sg_nks;
-                const uint8_t *src = p.sh + (size_t)h.blk * f16_unit_bytes(H) + (size_t)h.k0 * 1024;
-                if (!issue(h, src, h.n * 1024, nullptr, 0, nullptr, 0)) return false;
-            }
-            return true;
+            if (!take_slot(h, g.sg_nr)) return -1;
+            h.r = lane;
+            h.k0 = lane * g.sg_nks;
+            h.n = g.sg_nks;
+            f.h = h;
+            f.src = p.sh + (size_t)h.blk * f16_unit_bytes(H) + (size_t)h.k0 * 1024;
+            f.bytes = (uint32_t)h.n * 1024;
+            return g.sg_nr;
         }
         int v = u - nSGb;
         const int nA = n_act();
-        if (!ok) return false;
+        if (!ok) return -1;
         const int nRGb = nA * g.rg_blocks;
         if (v < nRGb) {
             DHeader h{};
@@ -442,69 +522,88 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
             h.a = v / g.rg_blocks;
             h.blk = v - h.a * g.rg_blocks;
             h.e = act[h.a];
-            if (h.e < 0 || h.e >= p.E) return true;  // unusable routing entry
-            if (!take_slot(h, g.rg_nr)) return false;
+            if (h.e < 0 || h.e >= p.E) return 0;  // unusable routing entry
+            if (!take_slot(h, g.rg_nr)) return -1;
             const size_t unit = (size_t)h.e * g.rg_blocks + h.blk;
-            for (int r = 0; r < g.rg_nr; ++r) {
-                h.r = r;
-                h.k0 = r * g.rg_gpi;
-                h.n = min(g.rg_gpi, H / (dk_kquant(p.fmt) ? 256 : 128) - h.k0);
-                const size_t gb = p.fmt == DK_FMT_Q8    ? (size_t)kQ8GroupBytes
-                                  : p.fmt == DK_FMT_Q2K ? (size_t)kQ2kSbBytes
-                                  : p.fmt == DK_FMT_Q4K ? (size_t)kQ4kSbBytes
-                                                        : w4_group_bytes(p.S);
-                const size_t ub = p.fmt == DK_FMT_Q8    ? q8_unit_bytes(H)
-                                  : p.fmt == DK_FMT_Q2K ? q2k_unit_bytes(H)
-                                  : p.fmt == DK_FMT_Q4K ? q4k_unit_bytes(H)
-                                                        : w4_unit_bytes(H, p.S);
-                const uint8_t *src = p.w4 + unit * ub + (size_t)h.k0 * gb;
-                // zero points (2S per group, as the scales) in the stage's h area, unused by these items
-                const __half *zs = p.zeros_gu ? p.zeros_gu + (unit * (H / 128) + h.k0) * 2 * p.S : nullptr;
-                if (!issue(h, src, h.n * (uint32_t)gb, nullptr, 0, nullptr, 0, zs,
-                           zs ? h.n * 4u * p.S : 0u, (uint32_t)L.hs_off))
-                    return false;
+            h.r = lane;
+            h.k0 = lane * g.rg_gpi;
+            h.n = min(g.rg_gpi, ngroups - h.k0);
+            f.h = h;
+            f.src = p.w4 + unit * rg_ub + (size_t)h.k0 * rg_gb;
+            f.bytes = (uint32_t)(h.n * rg_gb);
+            if (p.zeros_gu) {  // zero points (2S per group, as the scales) in the stage's h area, unused by these items
+                f.zsrc = p.zeros_gu + (unit * (H / 128) + h.k0) * 2 * p.S;
+                f.zbytes = (uint32_t)h.n * 4u * (uint32_t)p.S;
+                f.zoff = (uint32_t)L.hs_off;
             }
-            return true;
+            return g.rg_nr;
         }
         v -= nRGb;
         const int nRD = nA * NQ * g.rd_nr;
-        if (v * kDkDBatch >= nSD + nRD) return false;
-        for (int j = 0; j < kDkDBatch; ++j) {
-            int d = v * kDkDBatch + j;
-            if (d >= nSD + nRD) break;
-            DHeader h{};
-            if (d < nSD) {
-                h.kind = DK_SD;
-                h.r = d / NQ;
-                h.blk = d - h.r * NQ;
-                h.k0 = h.r * kDkSdSteps;
-                h.n = min(kDkSdSteps, p.I_s / 16 - h.k0);
-                const uint8_t *src =
-                    p.sh + shared_pairdown_offset(H, p.I_s) + ((size_t)h.blk * (p.I_s / 16) + h.k0) * 1024;
-                if (!issue(h, src, h.n * 1024, p.hf_s + (size_t)h.k0 * T * 4, h.n * T * 32, p.rdy_s + h.r, h.n))
-                    return false;
-            } else {
-                d -= nSD;
-                h.kind = DK_RD;
-                h.a = d / (NQ * g.rd_nr);
-                const int rem = d - h.a * (NQ * g.rd_nr);
-                h.r = rem / NQ;
-                h.blk = rem - h.r * NQ;
-                h.e = act[h.a];
-                if (h.e < 0 || h.e >= p.E) continue;  // unusable routing entry
-                h.k0 = h.r * g.rd_gpi;
-                h.n = min(g.rd_gpi, I / 128 - h.k0);
-                const uint32_t gb = q8dn ? (uint32_t)kQ8GroupBytes : (uint32_t)kW4ColGroupBytes;
-                const uint8_t *src = p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * gb;
-                const __half *zs =
-                    p.zeros_dn ? p.zeros_dn + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * 32 : nullptr;
-                if (!issue(h, src, h.n * gb, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4,
-                           h.n * 8 * T * 32, p.rdy_r + h.a * g.rd_nr + h.r, h.n * 8, zs, zs ? h.n * 64u : 0u,
-                           (uint32_t)kDkRdZeroOff))
-                    return false;
-            }
+        const int d0 = v * kDkDBatch;
+        if (d0 >= nSD + nRD) return -1;
+        const int n = min(kDkDBatch, nSD + nRD - d0);
+        int d = d0 + lane;
+        if (lane >= n) return n;
+        DHeader h{};
+        if (d < nSD) {
+            h.kind = DK_SD;
+            h.r = d / NQ;
+            h.blk = d - h.r * NQ;
+            h.k0 = h.r * kDkSdSteps;
+            h.n = min(kDkSdSteps, p.I_s / 16 - h.k0);
+            f.h = h;
+            f.src = p.sh + shared_pairdown_offset(H, p.I_s) + ((size_t)h.blk * (p.I_s / 16) + h.k0) * 1024;
+            f.bytes = (uint32_t)h.n * 1024;
+            f.hsrc = p.hf_s + (size_t)h.k0 * T * 4;
+            f.hs_bytes = (uint32_t)(h.n * T * 32);
+            f.rdy = p.rdy_s + h.r;
+            f.target = h.n;
+            return n;
         }
-        return true;
+        d -= nSD;
+        h.kind = DK_RD;
+        h.a = d / (NQ * g.rd_nr);
+        const int rem = d - h.a * (NQ * g.rd_nr);
+        h.r = rem / NQ;
+        h.blk = rem - h.r * NQ;
+        h.e = act[h.a];
+        if (h.e < 0 || h.e >= p.E) {  // unusable routing entry: an empty fill the consumer skips
+            h.kind = DK_NOP;
+            f.h = h;
+            return n;
+        }
+        h.k0 = h.r * g.rd_gpi;
+        h.n = min(g.rd_gpi, I / 128 - h.k0);
+        f.h = h;
+        f.src = p.w4 + p.w4_colblk + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * rd_gb;
+        f.bytes = (uint32_t)h.n * rd_gb;
+        f.hsrc = p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.k0 * 8) * T * 4;
+        f.hs_bytes = (uint32_t)(h.n * 8 * T * 32);
+        f.rdy = p.rdy_r + h.a * g.rd_nr + h.r;
+        f.target = h.n * 8;
+        if (p.zeros_dn) {
+            f.zsrc = p.zeros_dn + (((size_t)h.e * NQ + h.blk) * (I / 128) + h.k0) * 32;
+            f.zbytes = (uint32_t)h.n * 64u;
+            f.zoff = (uint32_t)kDkRdZeroOff;
+        }
+        return n;
+    };
+    int tr_nunit = 0;
+    DFill f;
+    auto run_unit = [&](int u) -> bool {
+#if TL_ON
+        if (lane == 0 && TR_ON() && tr_nunit < kTrUnits) {
+            s_tr.unit[tr_nunit][0] = TR_NOW();
+            s_tr.unit[tr_nunit][1] = (uint32_t)u;
+        }
+        ++tr_nunit;
+#else
+        (void)tr_nunit;
+#endif
+        const int n = expand(u, f);
+        if (n < 0) return false;
+        return n == 0 || issue_fills(f, n);
     };
     // The queue is split into kDkShards interleaved shards (unit u belongs to
     // shard u % kDkShards) so that each counter serves a few SMs only.  Each
@@ -513,62 +612,44 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L)
     const int shard = (int)(blockIdx.x % kDkShards);
     const uint32_t nsm = (gridDim.x - shard + kDkShards - 1) / kDkShards;  // blocks on this shard
     uint32_t *ctr = p.qctr + 64 * shard;
-    // The static unit's items need no global memory but its weights (the
+    // The static unit's fills need no global memory but its weights (the
     // routing and the ready counts are the consumers' and the poller's, who
     // wait for the preceding launch themselves), so they are issued before
-    // this thread waits for it; the counters come after.
-    // profiling build: producer time per unit kind
-    int tr_nunit = 0;
-    auto timed_unit = [&](int u) -> bool {
-        const unsigned long long t = TL_NOW();
-#if TL_ON
-        if (TR_ON() && tr_nunit < kTrUnits) {
-            s_tr.unit[tr_nunit][0] = TR_NOW();
-            s_tr.unit[tr_nunit][1] = (uint32_t)u;
-        }
-        ++tr_nunit;
-#endif
-        const bool r = run_unit(u);
-        TL_ADD(p.tl_slot, u < nSGb ? TL_P_SG : (na >= 0 && u - nSGb < na * g.rg_blocks) ? TL_P_RG : TL_P_DN,
-               TL_NOW() - t);
-        return r;
-    };
-    uint32_t tkA = blockIdx.x / kDkShards;
-    const bool more = timed_unit((int)tkA * kDkShards + shard);
-    TL_FIRST(p.tl_slot, TL_PROD_STATIC);
+    // this warp waits for it; the counters come after.
+    const bool more = run_unit((int)(blockIdx.x / kDkShards) * kDkShards + shard);
+    if (lane == 0) TLB_FIRST(p.tl_slot, TL_PROD_STATIC);
     griddep_wait();
-    TL_FIRST(p.tl_slot, TL_PROD_GRIDDEP);
+    if (lane == 0) TLB_FIRST(p.tl_slot, TL_PROD_GRIDDEP);
     if (more) {
-        uint32_t tkB = nsm + atomicAdd(ctr, 1u);
+        uint32_t tA = 0, tB = 0;
+        if (lane == 0) tB = nsm + atomicAdd(ctr, 1u);
         while (true) {
-            tkA = nsm + atomicAdd(ctr, 1u);
-            TL_TICKET(p.tl_slot, tkB, misc + 15);
-            if (!timed_unit((int)tkB * kDkShards + shard)) break;
-            tkB = nsm + atomicAdd(ctr, 1u);
-            TL_TICKET(p.tl_slot, tkA, misc + 15);
-            if (!timed_unit((int)tkA * kDkShards + shard)) break;
+            if (lane == 0) tA = nsm + atomicAdd(ctr, 1u);
+            __syncwarp();
+            if (!run_unit((int)__shfl_sync(kAll, tB, 0) * kDkShards + shard)) break;
+            if (lane == 0) tB = nsm + atomicAdd(ctr, 1u);
+            __syncwarp();
+            if (!run_unit((int)__shfl_sync(kAll, tA, 0) * kDkShards + shard)) break;
+        }
+        // The ticket taken ahead is still in flight: wait for both values (a
+        // returned value means the add is done at L2) and fence, so that no
+        // add of this block can land after the last block has reset the queue
+        // counters for the next call (the end markers only release at block
+        // scope).
+        if (lane == 0) {
+            misc[15] = (int)(tA ^ tB);
+            __threadfence();
         }
     }
     if (ok) {
-        TL_LAST(p.tl_slot, TL_PROD_LAST);
+        if (lane == 0) TLB_LAST(p.tl_slot, TL_PROD_LAST);
         __threadfence_block();
-        misc[3] = 1;  // no more h copies to register
-        for (int w = 0; w < kDkCons; ++w) {  // one end marker per consumer warp
-            const int st = (int)(it % nst);
-            if (!mbar_wait_sleep_bounded(&empty[st], ((it / nst) & 1) ^ 1, misc, &p.hdr->status,
-                                         p.wait_budget_ns)) {
-                ok = false;
-                break;
-            }
-            DHeader h{};
-            h.kind = DK_DONE;
-            h.seq = (int)it;
-            hdrs[st] = h;
-            mbar_arrive(&full[st]);
-            ++it;
-        }
+        if (lane == 0) misc[3] = 1;  // no more h copies to register
+        f = DFill{};                 // one end marker per consumer warp
+        f.h.kind = DK_DONE;
+        issue_fills(f, kDkCons);
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
         // bounded wait for the copies in flight before the block may exit
         const uint32_t first = it > (uint32_t)nst ? it - nst : 0;
         for (uint32_t j = first; j < it; ++j) {
@@ -645,7 +726,7 @@ __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
         if (any) {
             t_last = global_timer_ns();
         } else if (global_timer_ns() - t_last > p.wait_budget_ns) {
-            atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            record_timeout(&p.hdr->status, SITE_POLLER);
             misc[0] = 1;
             drain();
             return;
@@ -855,21 +936,24 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) TL_FIRST(p.tl_slot, TL_ENTRY);
-    if (warp == kDkCons) {
-        if (lane == 0) dk_producer(p, smem, L);
+    if (threadIdx.x == 0) TLB_FIRST(p.tl_slot, TL_ENTRY);
+    if (warp == kDkProducerWarp) {
+        dk_producer(p, smem, L, lane);
         return;
     }
-    if (warp == kDkCons + 1) {
+    if (warp == kDkPollerWarp) {
         if (lane == 0) dk_poller(p, smem, L);
         return;
     }
+    const int cw = dk_consumer_index(warp);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
     uint32_t allphase = 0;
+    // Consumer barrier; a waiting warp sleeps in the wait (it leaves the
+    // issue slots and shared memory to the warps the others wait for).
     auto all_sync = [&]() {
         __syncwarp();
         if (lane == 0) mbar_arrive(allbar);
-        mbar_wait_bounded(allbar, allphase & 1, abort_flag, &p.hdr->status, p.wait_budget_ns);
+        mbar_wait_sleep_bounded(allbar, allphase & 1, abort_flag, &p.hdr->status, p.wait_budget_ns, SITE_ALL_SYNC);
         allphase ^= 1;
         __syncwarp();
     };
@@ -878,18 +962,64 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     float *gamma = reinterpret_cast<float *>(smem + L.gamma);
     __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int H = p.H, I = p.I, T = p.T, xstr = L.xs_stride;
-    const int ctid = threadIdx.x;
+    const int ctid = cw * 32 + lane;
     const DkGeom geo = dk_geom(H, I, p.S, p.I_s, FMT);
     griddep_wait();  // x, the logits and the workspace may come from the preceding launch
-    // one token over at most 64 experts: every consumer warp ranks a share
-    const bool sel_all = p.logits && T == 1 && p.E <= 8 * kDkCons && p.E <= 64 && p.k <= 32;
-    float *sv0 = reinterpret_cast<float *>(smem + L.rsv);
-    if (sel_all && ctid < p.E) sv0[ctid] = __ldcg(p.logits + ctid);
+    // Routing outputs in shared memory are complete: publish them to the
+    // producer (misc[4]) and to the routed items.
+    auto publish_routing = [&](int na) {
+        __syncwarp();
+        if (lane == 0) {
+            misc[5] = na;
+            __threadfence_block();
+            *reinterpret_cast<volatile int *>(misc + 4) = 1;
+            TLB_FIRST(p.tl_slot, TL_ROUTED);
+        }
+    };
+    // One token with given logits: warp 0 selects its experts at once,
+    // straight from the logits in global memory, while the other warps stage
+    // x; it arrives on the x barrier first (it stages none) and waits on it
+    // after the routing is published.
+    const bool route1 = p.logits && T == 1;
+    if (route1 && cw == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(allbar);
+#if TL_ON
+        if (lane == 0 && TR_ON()) s_tr.route[0] = TR_NOW();
+#endif
+        int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
+        float *rpw = reinterpret_cast<float *>(smem + L.rpw);
+        const int E = p.E, k = p.k;
+        select_token([&](int e) { return __ldcg(p.logits + e); }, E, k, p.renorm, lane, rids, rpw,
+                     reinterpret_cast<float *>(smem + L.rsv));
+#if TL_ON
+        if (lane == 0 && TR_ON()) s_tr.route[1] = TR_NOW();
+#endif
+        if (blockIdx.x == 0)
+            for (int r = lane; r < k; r += 32) {
+                const int e = rids[r];
+                p.topk_ids[r] = e;
+                p.topk_w[r] = rpw[r];
+                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
+            }
+#if TL_ON
+        if (lane == 0 && TR_ON()) s_tr.route[2] = TR_NOW();
+#endif
+        const int na_r = route_tables_warp(p, L, smem, lane, blockIdx.x == 0);
+#if TL_ON
+        if (lane == 0 && TR_ON()) s_tr.route[3] = TR_NOW();
+#endif
+        publish_routing(na_r);
+#if TL_ON
+        if (lane == 0 && TR_ON()) s_tr.route[4] = TR_NOW();
+#endif
+    }
 
     // x into shared memory, and its sums over each group of 128 (16 chunks of
     // 8 = one half-warp, as the stride is a multiple of 16 chunks)
     float *sxs = reinterpret_cast<float *>(smem + L.sx);
-    for (int base = warp * 32; base < T * (H / 8); base += kDkCons * 32) {
+    const int xw = route1 ? cw - 1 : cw, nxw = route1 ? kDkCons - 1 : kDkCons;  // staging warps
+    for (int base = xw * 32; xw >= 0 && base < T * (H / 8); base += nxw * 32) {
         const int idx = base + lane;
         float sum = 0.f;
         if (idx < T * (H / 8)) {
@@ -908,49 +1038,26 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         if ((lane & 15) == 0 && idx < T * (H / 8)) sxs[idx / 16] = sum;  // [t][group]: idx/16 = t*(H/128) + group
     }
-    all_sync();  // x is in shared memory
-    if (ctid == 0) TL_FIRST(p.tl_slot, TL_X_STAGED);
-    // Routing: warps t < T select token t (every block the same way; block 0
-    // also writes the routing outputs); the last of them builds the token
-    // tables and raises misc[4].  The other warps go straight to the shared
-    // expert's items, which need no routing.
-    auto publish_routing = [&](int na) {
+    if (route1 && cw == 0) {  // its arrival came first
+        mbar_wait_sleep_bounded(allbar, allphase & 1, abort_flag, &p.hdr->status, p.wait_budget_ns, SITE_ALL_SYNC);
+        allphase ^= 1;
         __syncwarp();
-        if (lane == 0) {
-            misc[5] = na;
-            __threadfence_block();
-            *reinterpret_cast<volatile int *>(misc + 4) = 1;
-            TL_FIRST(p.tl_slot, TL_ROUTED);
-        }
-    };
-    if (sel_all) {
-        int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
-        float *rpw = reinterpret_cast<float *>(smem + L.rpw);
-        const int E = p.E, k = p.k;
-        if (warp < (E + 7) / 8) select_rank_warp(sv0, E, k, warp, lane, rids, rpw);
-        all_sync();  // every expert ranked
-        if (warp == 0) {
-            if (lane == 0 && p.renorm) {
-                float psel = 0.f;
-                for (int r = 0; r < k; ++r) psel += rpw[r];
-                for (int r = 0; r < k; ++r) rpw[r] = rpw[r] / psel;
-            }
-            __syncwarp();
-            if (blockIdx.x == 0 && lane < k) {
-                const int e = rids[lane];
-                p.topk_ids[lane] = e;
-                p.topk_w[lane] = rpw[lane];
-                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
-            }
-            publish_routing(route_tables_warp(p, L, smem, lane, blockIdx.x == 0));
-        }
+    } else {
+        all_sync();  // x is in shared memory
+    }
+    if (ctid == 0) TLB_FIRST(p.tl_slot, TL_X_STAGED);
+    // Routing of several tokens: warps t < T select token t (every block the
+    // same way; block 0 also writes the routing outputs); the last of them
+    // builds the token tables and raises misc[4].  The other warps go straight
+    // to the shared expert's items, which need no routing.
+    if (route1) {
     } else if (p.logits) {
-        if (warp < T) {
+        if (cw < T) {
             int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
             float *rpw = reinterpret_cast<float *>(smem + L.rpw);
             const int E = p.E, k = p.k;
             int mine = 0;
-            for (int t = warp; t < T; t += kDkCons, ++mine) {
+            for (int t = cw; t < T; t += kDkCons, ++mine) {
                 const float *lg = p.logits + (size_t)t * E;
                 select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k, rpw + t * k,
                              reinterpret_cast<float *>(smem + L.rsv) + t * E);
@@ -973,11 +1080,11 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 publish_routing(route_tables_warp(p, L, smem, lane, blockIdx.x == 0));
             }
         }
-    } else if (warp == 0) {
+    } else if (cw == 0) {
         publish_routing(load_tables_warp(p, L, smem, lane));
     }
     // shared-expert gate per token (only the shared down items use it; misc[7])
-    if (warp == kDkCons - 1) {
+    if (cw == kDkCons - 1) {
         if (p.sh && p.w_sgate) {
             // the gate row in chunks of 2048 halves: a lane's 8 loads of a chunk issued at once
             float z[kMaxT < 8 ? kMaxT : 8] = {};
@@ -1062,19 +1169,38 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         // landed yet; a parity wait cannot tell those two phases apart, so the
         // fill is accepted only when its header carries this ticket.
         bool got = false;
-        const unsigned long long twf = TL_NOW();
+        [[maybe_unused]] const unsigned long long twf = TL_NOW();
         {
             const uint32_t par = (uint32_t)(idx / nst) & 1;
             const volatile int *seqp = &hdrs[st].seq;
             const uint64_t t0 = global_timer_ns();
             while (true) {
-                if (mbar_try_wait_sleep(&full[st], par, kDkSleepNs) && *seqp == idx) {
+                // every lane waits on the barrier itself (each needs the
+                // completion's ordering); the fill is taken once all have seen
+                // it, so the warp leaves the loop together
+                const bool seen = mbar_try_wait_sleep(&full[st], par, kDkSleepNs) && *seqp == idx;
+                if (__all_sync(0xffffffffu, seen)) {
                     got = true;
                     break;
                 }
-                if (*abort_flag) break;
-                if (global_timer_ns() - t0 > p.wait_budget_ns) {
-                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+                if (__any_sync(0xffffffffu, global_timer_ns() - t0 > p.wait_budget_ns)) {
+                    // the state of the ring at the wait that gave up, for diagnosis
+                    if (lane == 0 && atomicCAS(&p.hdr->pad[0], 0u, 1u) == 0u) {
+                        p.hdr->pad[1] = (uint32_t)idx;
+                        p.hdr->pad[2] = (uint32_t)st;
+                        p.hdr->pad[3] = (uint32_t)*seqp;
+                        p.hdr->pad[4] = (uint32_t)misc[2];
+                        p.hdr->pad[5] = (uint32_t)misc[14];
+                        p.hdr->pad[6] = (uint32_t)misc[3];
+                        p.hdr->pad[7] = blockIdx.x;
+                        p.hdr->pad[8] = (uint32_t)nst;
+                        p.hdr->pad[9] = mbar_try_wait(&full[st], par) ? 1u : 0u;
+                        p.hdr->pad[10] = (uint32_t)hdrs[st].kind;
+                        p.hdr->pad[11] = (uint32_t)cw;
+                        for (int j = 0; j < nst && j < 16; ++j) p.hdr->pad[12 + j] = (uint32_t)hdrs[j].seq;
+                    }
+                    record_timeout(&p.hdr->status, SITE_FILL);
                     *abort_flag = 1;
                     break;
                 }
@@ -1082,7 +1208,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         }
         if (!got) break;
         const DHeader h = hdrs[st];
-        const uint32_t tr_got = TR_NOW();
+        [[maybe_unused]] const uint32_t tr_got = TR_NOW();
         if (TL_ON && lane == 0) {
             TL_ADD(p.tl_slot, TL_W_FULL, TL_NOW() - twf);
             TL_FIRST(p.tl_slot, TL_FIRST_FILL);
@@ -1090,34 +1216,40 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             if (h.kind == DK_RG) TL_FIRST(p.tl_slot, TL_RG_FIRST);
         }
         const uint8_t *stage = ring + (size_t)st * L.stage;
-        if (h.kind == DK_DONE) {
+        if (h.kind == DK_DONE || h.kind == DK_NOP) {
             // release it too: with fewer stages than warps the end markers reuse stages
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
-            break;
+            if (h.kind == DK_DONE) break;
+            continue;
         }
         const int *stn = reinterpret_cast<const int *>(smem + L.stn);
         const TokEntry *ste = reinterpret_cast<const TokEntry *>(smem + L.ste);
         const uint2 *hsl = reinterpret_cast<const uint2 *>(stage + L.hs_off);
         if (h.kind == DK_SD || h.kind == DK_RD) {
-            // the intermediate slice lands after the weights (poller's copy)
-            const unsigned long long twh = TL_NOW();
-            if (!mbar_wait_sleep_bounded(&hfull[st], (uint32_t)h.hpar, abort_flag, &p.hdr->status, p.wait_budget_ns))
+            // the intermediate slice lands after the weights (poller's copy); the
+            // warp goes on only if every lane saw it
+            [[maybe_unused]] const unsigned long long twh = TL_NOW();
+            const bool hs_ok =
+                mbar_wait_sleep_bounded(&hfull[st], (uint32_t)h.hpar, abort_flag, &p.hdr->status, p.wait_budget_ns);
+            if (!__all_sync(0xffffffffu, hs_ok)) {
+                *abort_flag = 1;
                 break;
+            }
             if (TL_ON && lane == 0) {
                 TL_ADD(p.tl_slot, TL_W_HFULL, TL_NOW() - twh);
                 TL_FIRST(p.tl_slot, TL_DN_H_FIRST);
                 if (h.kind == DK_RD) TL_LAST(p.tl_slot, TL_RD_H_LAST);
             }
         }
-        const unsigned long long tc = TL_NOW();  // profiling build: item compute start
-        const uint32_t tr_h = TR_NOW();
+        [[maybe_unused]] const unsigned long long tc = TL_NOW();  // profiling build: item compute start
+        [[maybe_unused]] const uint32_t tr_h = TR_NOW();
 #if TL_ON
         auto tr_item = [&](int kind) {
             if (TR_ON()) {
                 const uint32_t i = atomicAdd(&s_tr.nitem, 1u);
                 if (i < (uint32_t)kTrItems) {
-                    s_tr.item[i][0] = ((uint32_t)warp << 8) | (uint32_t)kind;
+                    s_tr.item[i][0] = ((uint32_t)cw << 8) | (uint32_t)kind;
                     s_tr.item[i][1] = tr_got;
                     s_tr.item[i][2] = tr_h;
                     s_tr.item[i][3] = TR_NOW();
@@ -1160,7 +1292,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                     }
                 }
             }
-            const unsigned long long tg = TL_NOW();
+            [[maybe_unused]] const unsigned long long tg = TL_NOW();
             gu_done(h, 1, p.hf_s + (size_t)h.blk * T * 4, 0, p.rdy_s + h.blk / kDkSdSteps, 1);
             if (TL_ON && lane == 0) {
                 TL_ADD(p.tl_slot, TL_C_GU_DONE, TL_NOW() - tg);
@@ -1265,7 +1397,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                     }
                 }
             }
-            const unsigned long long tg = TL_NOW();
+            [[maybe_unused]] const unsigned long long tg = TL_NOW();
             gu_done(h, MS, p.hf_r + ((size_t)h.a * (I / 16) + (size_t)h.blk * MS) * T * 4, (size_t)T * 4,
                     p.rdy_r + h.a * geo.rd_nr + (h.blk * 16 * MS / 128) / geo.rd_gpi, MS);
             if (TL_ON && lane == 0) {
@@ -1304,14 +1436,14 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
                 const uint64_t t0 = global_timer_ns();
                 while (!*reinterpret_cast<volatile int *>(misc + 7) && !*abort_flag) {
                     if (global_timer_ns() - t0 > p.wait_budget_ns) {
-                        atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                        record_timeout(&p.hdr->status, SITE_GATE);
                         *abort_flag = 1;
                     }
                 }
                 __threadfence_block();
             }
             const int n0 = 32 * h.blk + 4 * g;
-            const unsigned long long to = TL_NOW();
+            [[maybe_unused]] const unsigned long long to = TL_NOW();
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int col = 2 * q4 + hf;
@@ -1412,7 +1544,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             if (lane == 0) mbar_arrive(&empty[st]);  // the stage is read
             const int n0 = 32 * h.blk + 4 * g;
             const int rmax = p.mode == 0 ? T * p.k : T;
-            const unsigned long long to = TL_NOW();
+            [[maybe_unused]] const unsigned long long to = TL_NOW();
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 if (row[hf] >= 0 && row[hf] < rmax) {
@@ -1439,7 +1571,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     // completion ticket; the last block writes the fp16 output and resets
     __threadfence();  // this thread's output additions, before the block counts as done
     all_sync();
-    if (ctid == 0) TL_FIRST(p.tl_slot, TL_CONS_DONE);
+    if (ctid == 0) TLB_FIRST(p.tl_slot, TL_CONS_DONE);
     if (ctid == 0) {
         __threadfence();
         const uint32_t t = atomicAdd(&p.hdr->done_ticket, 1u);
@@ -1478,9 +1610,9 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         if (ctid < kDkShards) p.qctr[64 * ctid] = 0;
         if (ctid == 0) p.hdr->done_ticket = 0;
         __threadfence();
-        if (ctid == 0) TL_LAST(p.tl_slot, TL_OUT_DONE);
+        if (ctid == 0) TLB_LAST(p.tl_slot, TL_OUT_DONE);
     }
-    if (ctid == 0) TL_LAST(p.tl_slot, TL_EXIT);
+    if (ctid == 0) TLB_LAST(p.tl_slot, TL_EXIT);
     if (TL_ON) {
         __syncwarp();
         all_sync();

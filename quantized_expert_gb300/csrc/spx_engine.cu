@@ -32,6 +32,7 @@
 // shared-memory atomics.
 #include "spx_internal.cuh"
 
+#include <limits.h>
 #include <math.h>
 
 namespace spx {
@@ -214,7 +215,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             const uint64_t t0 = global_timer_ns();
             while (ld_acquire_u32(p.ready + e) == 0u) {
                 if (*abort_flag || global_timer_ns() - t0 > p.wait_budget_ns) {
-                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    record_timeout(&p.hdr->status, SITE_ENGINE);
                     *abort_flag = 1;
                     return false;
                 }
@@ -372,11 +373,22 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         if (progressed) {
             t_prog = clock64();
         } else if (*abort_flag || clock64() - t_prog > budget) {
-            atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            record_timeout(&p.hdr->status, SITE_ENGINE);
             *abort_flag = 1;
             aborted = true;
             break;
         }
+    }
+    // Each stream's counter value fetched ahead may still be in flight: wait
+    // for every value (a returned value means the add is done at L2) and
+    // fence, so that no add of this block can land after the last block has
+    // reset the counter for the next call.
+    {
+        int seen = 0;
+#pragma unroll
+        for (int g = 0; g < G; ++g) seen ^= s[g].pend_u;
+        if (seen == INT_MIN) atomicCAS(&p.hdr->status, 0, 0);  // reads the values; never true
+        __threadfence();
     }
     // Drain: every issued copy has been waited on by the consumers unless the
     // block aborted; in that case wait (bounded) for the copies in flight.
@@ -846,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             bool ok = true;
             while (*dt < gridDim.x) {
                 if (*abort_flag || global_timer_ns() - t0 > p.wait_budget_ns) {
-                    atomicCAS(&p.hdr->status, 0, (int32_t)SPX_ERR_TIMEOUT);
+                    record_timeout(&p.hdr->status, SITE_ENGINE);
                     ok = false;
                     break;
                 }

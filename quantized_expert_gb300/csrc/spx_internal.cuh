@@ -5,6 +5,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/spx.h"
@@ -30,9 +31,21 @@ struct WsHeader {
     int32_t status;          // SPX_OK or SPX_ERR_TIMEOUT (sticky)
     uint32_t route_ticket;   // completed blocks of the router product
     uint32_t exit_ticket;    // blocks of the expert launch done with its output pass
-    uint32_t pad[59];
+    int32_t timeout_site;    // which bounded wait gave up first (with status; 0 = none)
+    uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+static_assert(offsetof(WsHeader, timeout_site) - offsetof(WsHeader, status) == 3 * sizeof(int32_t),
+              "a wait that holds &status records its site three words on");
+// Bounded waits that give up record their site next to the status word.
+enum : int32_t { SITE_ALL_SYNC = 1, SITE_FILL = 2, SITE_HSLICE = 3, SITE_GATE = 4, SITE_ROUTING = 5, SITE_SLOT = 6,
+                 SITE_STAGE = 7, SITE_POLLER = 8, SITE_ENGINE = 9 };
+#if defined(__CUDACC__)
+__device__ __forceinline__ void record_timeout(int32_t *status, int32_t site) {
+    atomicCAS(status, 0, (int32_t)SPX_ERR_TIMEOUT);
+    atomicCAS(status + 3, 0, site);
+}
+#endif
 constexpr size_t kWsAccOffset = 256;
 
 
@@ -215,7 +228,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (*abort) return false;
         if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > budget_ns) {
-            atomicCAS(status, 0, (int32_t)SPX_ERR_TIMEOUT);
+            record_timeout(status, SITE_ALL_SYNC);
             *abort = 1;
             return false;
         }

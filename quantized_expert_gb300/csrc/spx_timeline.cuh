@@ -76,6 +76,7 @@ struct TrBlock {
     uint32_t unit[kTrUnits][2];  // start, queue unit
     unsigned long long t0;
     uint32_t nitem, pad;
+    uint32_t route[8];           // routing warp: start, selected, outputs, tables, published
 };
 
 }  // namespace spx
@@ -92,9 +93,14 @@ __device__ __forceinline__ int tr_block() {
 }
 __device__ __forceinline__ uint32_t tr_now() { return (uint32_t)(global_timer_ns() - s_tr.t0); }
 }  // namespace spx
-#define TL_FIRST(slot, ev) atomicMax(&::spx::s_tl[(ev)], ~(unsigned long long)::spx::global_timer_ns())
-#define TL_LAST(slot, ev) atomicMax(&::spx::s_tl[(ev)], (unsigned long long)::spx::global_timer_ns())
-#define TL_ADD(slot, ev, v) atomicAdd(&::spx::s_tl[(ev)], (unsigned long long)(v))
+// Per-block marks (a few per block): shared-memory atomics.  The per-fill and
+// per-item marks are compiled out: their 64-bit shared atomics (compare-and-
+// swap loops) slowed the very paths they measured; the trace covers them.
+#define TLB_FIRST(slot, ev) atomicMax(&::spx::s_tl[(ev)], ~(unsigned long long)::spx::global_timer_ns())
+#define TLB_LAST(slot, ev) atomicMax(&::spx::s_tl[(ev)], (unsigned long long)::spx::global_timer_ns())
+#define TL_FIRST(slot, ev) ((void)0)
+#define TL_LAST(slot, ev) ((void)0)
+#define TL_ADD(slot, ev, v) ((void)0)
 #define TL_NOW() ::spx::global_timer_ns()
 #define TL_ON 1
 // clear the block's shared words (before the block's first barrier)
@@ -121,14 +127,10 @@ __device__ __forceinline__ uint32_t tr_now() { return (uint32_t)(global_timer_ns
 #define TR_NOW() ::spx::tr_now()
 // waits for v (a queue ticket in flight) by storing it to a shared word, and
 // counts the wait
-#define TL_TICKET(slot, v, sinkp)                                     \
-    do {                                                              \
-        const unsigned long long t_ = TL_NOW();                       \
-        *(volatile uint32_t *)(sinkp) = (v);                          \
-        TL_ADD((slot), ::spx::TL_W_TICKET, TL_NOW() - t_);            \
-        TL_ADD((slot), ::spx::TL_N_TICKET, 1);                        \
-    } while (0)
+#define TL_TICKET(slot, v, sinkp) ((void)0)
 #else
+#define TLB_FIRST(slot, ev) ((void)0)
+#define TLB_LAST(slot, ev) ((void)0)
 #define TL_FIRST(slot, ev) ((void)0)
 #define TL_LAST(slot, ev) ((void)0)
 #define TL_ADD(slot, ev, v) ((void)0)

@@ -92,6 +92,9 @@ def test_cycle_26_layers_elb_and_routing():
             args, keep = spx.layer_args(0, gh.dev_f16(x), E, k, s.renorm, gh.dev(lg), r_d, out_d, ws_d, w4=w4,
                                         shared=sh, elb=elb, layer=l)
             spx.spx_moe_layer(args)
+            hdr = ws_d[:256].view(torch.int32).cpu().numpy()  # status word and the site of a wait that gave up
+            assert hdr[2] == 0, (f"draft step {st} layer {l}: status {hdr[2]}, wait site {hdr[5]}, ring state "
+                                 f"{hdr[6:18]}, stage seqs {hdr[18:34]}")
             ids = draft_ids[(st, l)]
             oracle.elb_accumulate(elb_ref, l, ids)
             if lay is not None:
