@@ -616,30 +616,38 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L,
     // routing and the ready counts are the consumers' and the poller's, who
     // wait for the preceding launch themselves), so they are issued before
     // this warp waits for it; the counters come after.
-    const bool more = run_unit((int)(blockIdx.x / kDkShards) * kDkShards + shard);
-    if (lane == 0) TLB_FIRST(p.tl_slot, TL_PROD_STATIC);
-    griddep_wait();
-    if (lane == 0) TLB_FIRST(p.tl_slot, TL_PROD_GRIDDEP);
-    if (more) {
-        uint32_t tA = 0, tB = 0;
-        if (lane == 0) tB = nsm + atomicAdd(ctr, 1u);
-        while (true) {
-            if (lane == 0) tA = nsm + atomicAdd(ctr, 1u);
-            __syncwarp();
-            if (!run_unit((int)__shfl_sync(kAll, tB, 0) * kDkShards + shard)) break;
-            if (lane == 0) tB = nsm + atomicAdd(ctr, 1u);
-            __syncwarp();
-            if (!run_unit((int)__shfl_sync(kAll, tA, 0) * kDkShards + shard)) break;
+    // One call site of the unit logic (it is large): the first pass runs the
+    // static unit, then waits for the preceding launch; later passes take a
+    // ticket that was fetched one unit ahead.
+    uint32_t tk = blockIdx.x / kDkShards;  // lane 0: the unit's ticket
+    uint32_t tnext = 0;                    // lane 0: the next ticket, in flight
+    bool first = true, took = false;
+    while (true) {
+        const bool more = run_unit((int)__shfl_sync(kAll, tk, 0) * kDkShards + shard);
+        if (first) {
+            first = false;
+            if (lane == 0) TLB_FIRST(p.tl_slot, TL_PROD_STATIC);
+            griddep_wait();
+            if (lane == 0) TLB_FIRST(p.tl_slot, TL_PROD_GRIDDEP);
+            if (!more) break;
+            if (lane == 0) tnext = nsm + atomicAdd(ctr, 1u);
+            took = true;
+        } else if (!more) {
+            break;
         }
-        // The ticket taken ahead is still in flight: wait for both values (a
-        // returned value means the add is done at L2) and fence, so that no
-        // add of this block can land after the last block has reset the queue
-        // counters for the next call (the end markers only release at block
-        // scope).
         if (lane == 0) {
-            misc[15] = (int)(tA ^ tB);
-            __threadfence();
+            tk = tnext;  // fetched a whole unit ago
+            tnext = nsm + atomicAdd(ctr, 1u);
         }
+        __syncwarp();
+    }
+    // The ticket taken ahead is still in flight: wait for its value (a
+    // returned value means the add is done at L2) and fence, so that no add of
+    // this block can land after the last block has reset the queue counters
+    // for the next call (the end markers only release at block scope).
+    if (took && lane == 0) {
+        misc[15] = (int)tnext;
+        __threadfence();
     }
     if (ok) {
         if (lane == 0) TLB_LAST(p.tl_slot, TL_PROD_LAST);
@@ -704,24 +712,26 @@ __device__ void dk_poller(const DkParams &p, uint8_t *smem, const DkLayout &L) {
             continue;
         }
         __threadfence_block();
+        // all pending counts are loaded at once, then the complete slices copied
         int v[kDkMaxStages];
 #pragma unroll
         for (int j = 0; j < kDkMaxStages; ++j) v[j] = ((m >> j) & 1u) ? ld_relaxed_gpu(pend[j].rdy) : 0;
-        bool any = false;
+        uint32_t go = 0;
 #pragma unroll
-        for (int j = 0; j < kDkMaxStages; ++j) {
-            if (((m >> j) & 1u) && v[j] >= pend[j].target) {
-                if (!any) {
-                    fence_acq_rel_gpu();         // the h stores counted by the ready count
-                    fence_proxy_async_global();  // ... are read through the bulk-copy proxy
-                    any = true;
-                }
-                bulk_g2s_plain(ring + (size_t)j * L.stage + L.hs_off, pend[j].src, pend[j].bytes, &hfull[j]);
-                TL_ADD(p.tl_slot, TL_W_POLL, TL_NOW() - pend[j].t_reg);
-                issued |= 1u << j;
-                ipar = (ipar & ~(1u << j)) | ((uint32_t)hdrs[j].hpar << j);
-                pstate[j] = 0;
-            }
+        for (int j = 0; j < kDkMaxStages; ++j) go |= (((m >> j) & 1u) && v[j] >= pend[j].target ? 1u : 0u) << j;
+        const bool any = go != 0;
+        if (any) {
+            fence_acq_rel_gpu();         // the h stores counted by the ready count
+            fence_proxy_async_global();  // ... are read through the bulk-copy proxy
+        }
+        while (go) {
+            const int j = __ffs(go) - 1;
+            go &= go - 1;
+            bulk_g2s_plain(ring + (size_t)j * L.stage + L.hs_off, pend[j].src, pend[j].bytes, &hfull[j]);
+            TL_ADD(p.tl_slot, TL_W_POLL, TL_NOW() - pend[j].t_reg);
+            issued |= 1u << j;
+            ipar = (ipar & ~(1u << j)) | ((uint32_t)hdrs[j].hpar << j);
+            pstate[j] = 0;
         }
         if (any) {
             t_last = global_timer_ns();
@@ -767,7 +777,8 @@ __device__ __forceinline__ void finalize_block(float *sa, int T, int nk, int lan
 // table (ste[a*T + rank]: token s/k, output row s/k, gate weight, in slot
 // order; stn[a] entries).  With out (block 0) the gather arrays of the routing
 // outputs are written as well.  Returns the number of active experts.
-__device__ int route_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane, bool out) {
+__device__ __noinline__ int route_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane,
+                                              bool out) {
     const int E = p.E, k = p.k, T = p.T, n = T * k;
     const int32_t *ids = reinterpret_cast<const int32_t *>(smem + L.rids);
     const float *pw = reinterpret_cast<const float *>(smem + L.rpw);
@@ -865,7 +876,7 @@ __device__ int route_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *
 
 // The unit call's routing: active experts and their token tables from global
 // memory (written by the preceding launches), into shared memory.
-__device__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane) {
+__device__ __noinline__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane) {
     const int T = p.T;
     int *act = reinterpret_cast<int *>(smem + L.act);
     int *stn = reinterpret_cast<int *>(smem + L.stn);
@@ -990,8 +1001,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
         float *rpw = reinterpret_cast<float *>(smem + L.rpw);
         const int E = p.E, k = p.k;
-        select_token([&](int e) { return __ldcg(p.logits + e); }, E, k, p.renorm, lane, rids, rpw,
-                     reinterpret_cast<float *>(smem + L.rsv));
+        select_token_global(p.logits, E, k, p.renorm, lane, rids, rpw);
 #if TL_ON
         if (lane == 0 && TR_ON()) s_tr.route[1] = TR_NOW();
 #endif
@@ -1059,8 +1069,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             int mine = 0;
             for (int t = cw; t < T; t += kDkCons, ++mine) {
                 const float *lg = p.logits + (size_t)t * E;
-                select_token([&](int e) { return __ldcg(lg + e); }, E, k, p.renorm, lane, rids + t * k, rpw + t * k,
-                             reinterpret_cast<float *>(smem + L.rsv) + t * E);
+                select_token_global(lg, E, k, p.renorm, lane, rids + t * k, rpw + t * k);
                 if (blockIdx.x == 0 && lane == 0)
                     for (int r = 0; r < k; ++r) {
                         const int e = rids[t * k + r];
@@ -1086,40 +1095,29 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     // shared-expert gate per token (only the shared down items use it; misc[7])
     if (cw == kDkCons - 1) {
         if (p.sh && p.w_sgate) {
-            // the gate row in chunks of 2048 halves: a lane's 8 loads of a chunk issued at once
-            float z[kMaxT < 8 ? kMaxT : 8] = {};
-            for (int c0 = 0; c0 < H; c0 += 2048) {
-                uint4 wv[8];
+            // lane l sums the gate row's 8-value chunks l, l + 32, ... (a few
+            // loads in flight; later tokens find the row in L1), then the warp
+            // adds the lanes' sums
+            const uint4 *wrow = reinterpret_cast<const uint4 *>(p.w_sgate);
+#pragma unroll 1
+            for (int t = 0; t < T; ++t) {
+                float z = 0.f;
+#pragma unroll 4
+                for (int c = lane; c < H / 8; c += 32) {
+                    const uint4 wv = __ldg(wrow + c);
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * xstr + c * 8);
+                    const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+                    const __half2 *wh = reinterpret_cast<const __half2 *>(&wv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (c0 + i * 256 + lane * 8 < H)
-                        wv[i] = __ldg(reinterpret_cast<const uint4 *>(p.w_sgate + c0) + i * 32 + lane);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (t >= T) break;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (c0 + i * 256 + lane * 8 >= H) break;
-                        const uint4 xv =
-                            *reinterpret_cast<const uint4 *>(xs + (size_t)t * xstr + c0 + i * 256 + lane * 8);
-                        const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-                        const __half2 *wh = reinterpret_cast<const __half2 *>(&wv[i]);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 a = __half22float2(xh[q]), b = __half22float2(wh[q]);
-                            z[t] = fmaf(a.x, b.x, z[t]);
-                            z[t] = fmaf(a.y, b.y, z[t]);
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 a = __half22float2(xh[q]), b = __half22float2(wh[q]);
+                        z = fmaf(a.x, b.x, z);
+                        z = fmaf(a.y, b.y, z);
                     }
                 }
-            }
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (t >= T) break;
-                float zt = z[t];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) zt += __shfl_xor_sync(0xffffffffu, zt, o);
-                if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-zt));
+                for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-z));
             }
         } else if (lane < T) {
             gamma[lane] = 1.0f;

@@ -137,6 +137,15 @@ __device__ __forceinline__ void select_token(Logit lg, int E, int k, int renorm,
         default: select_token_n<8>(lg, E, k, renorm, lane, ids, w, sv); break;
     }
 }
+
+// The same selection for logits in global memory (one token's row), kept out
+// of line with one instance (up to 8 experts per lane): a kernel that selects
+// once per launch keeps its hot loops close together in the instruction
+// cache instead of carrying an unrolled copy per expert count.
+static __device__ __noinline__ void select_token_global(const float *logits, int E, int k, int renorm, int lane,
+                                                 int32_t *ids, float *w) {
+    select_token_n<8>([&](int e) { return __ldcg(logits + e); }, E, k, renorm, lane, ids, w, nullptr);
+}
 #endif  // __CUDACC__
 
 }  // namespace spx
