@@ -1012,8 +1012,8 @@ def run_timeline(args):
 
     lib.spx_timeline_trace.restype = C.c_int
     lib.spx_timeline_trace.argtypes = [C.c_void_p, C.c_size_t]
-    # per launch slot, 2 traced blocks: fill[48][4], item[64][4], unit[16][2] u32, t0 u64, nitem, pad
-    tr_words = 48 * 4 + 64 * 4 + 16 * 2 + 2 + 2 + 8
+    # per launch slot, 2 traced blocks: fill[48][4], item[64][4], unit[16][4] u32, t0 u64, nitem, pad
+    tr_words = 48 * 4 + 64 * 4 + 16 * 4 + 2 + 2 + 8
     trbuf = np.zeros((8, 2, tr_words), np.uint32)
     traces = {}
 
@@ -1044,7 +1044,7 @@ def run_timeline(args):
             "chained": timeline_phases(chained, range(1, 8), nsm),
             "trace": {"words": "per launch slot, blocks 0 and grid/2: fill[48][4] (wait start, stage free, issued, "
                                "kind<<24|bytes), item[64][4] (warp<<8|kind, landed, intermediate landed, done), "
-                               "unit[16][2] (start, unit), t0 (2 words), nitem, pad, route[8] (routing warp: "
+                               "unit[16][4] (start, unit, described, issued), t0 (2 words), nitem, pad, route[8] (routing warp: "
                                "start, selected, outputs, tables, published); ns after block entry",
                       "isolated_slot4": traces[0][4].tolist(), "chained_slot4": traces[1][4].tolist()}}
     print(json.dumps(line), flush=True)

@@ -602,8 +602,15 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L,
         (void)tr_nunit;
 #endif
         const int n = expand(u, f);
+#if TL_ON
+        if (lane == 0 && TR_ON() && tr_nunit <= kTrUnits) s_tr.unit[tr_nunit - 1][2] = TR_NOW();
+#endif
         if (n < 0) return false;
-        return n == 0 || issue_fills(f, n);
+        const bool r = n == 0 || issue_fills(f, n);
+#if TL_ON
+        if (lane == 0 && TR_ON() && tr_nunit <= kTrUnits) s_tr.unit[tr_nunit - 1][3] = TR_NOW();
+#endif
+        return r;
     };
     // The queue is split into kDkShards interleaved shards (unit u belongs to
     // shard u % kDkShards) so that each counter serves a few SMs only.  Each

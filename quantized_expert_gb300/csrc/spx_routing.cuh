@@ -21,107 +21,95 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Inverse of logit_key for a nonzero key (gives +0 for a -0 logit, which
+// has the same softmax term).
+__device__ __forceinline__ float key_logit(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // Warp-collective selection for one token.  lg(e) returns logit e (fp32, the
-// precision every decision is taken in); E <= 256, k <= E.  The experts are
-// taken in the order (value descending, index ascending): k rounds, each a
-// warp-wide maximum of the order keys, ties to the lowest expert index.
+// precision every decision is taken in); E <= 32 NPER, k <= E.  The experts
+// are taken in the order (value descending, index ascending): k rounds, each
+// a warp-wide maximum of the order keys; the lane holding it (expert
+// e = lane + 32 j, its lowest such j) takes the round, and when several lanes
+// hold it, the one with the lowest expert index does.  The round's winner
+// stores ids[r] and drops the key; the key itself is known to every lane,
+// and lane r keeps it (ranks from 32 on go through w[r]).  Afterwards each
+// rank's lane computes its weight:
 // p = expf(v - max) / sum over all E of expf(v - max) (each lane sums its
-// experts e = lane + 32 j in j order, then a fixed xor-shuffle tree);
+// experts in j order, then a fixed xor-shuffle tree);
 // weight = p, or p / (sum of the k selected p, in rank order) when renorm.
-// The lane owning the rank-r expert writes ids[r] and w[r]; sv (E floats of
-// shared scratch) is not used.
+// ids and w must be visible to the whole warp (shared or global memory).
 template <int NPER, class Logit>
 __device__ __forceinline__ void select_token_n(Logit lg, int E, int k, int renorm, int lane, int32_t *ids, float *w,
-                                               float *sv) {
+                                              float *sv) {
     (void)sv;
-    float v[NPER];
+    constexpr uint32_t kAll = 0xffffffffu;
     uint32_t key[NPER];
-    float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
         const int e = lane + 32 * j;
-        v[j] = e < E ? lg(e) : -INFINITY;
-        key[j] = e < E ? logit_key(v[j]) : 0u;
-        if (e < E) m = fmaxf(m, v[j]);
+        key[j] = e < E ? logit_key(lg(e)) : 0u;
     }
+    // this lane's best key, the lowest j among equal keys
+    uint32_t bk = 0u;
+    int bj = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int j = 0; j < NPER; ++j)
+        if (key[j] > bk) {
+            bk = key[j];
+            bj = j;
+        }
+    uint32_t mk = __reduce_max_sync(kAll, bk);
+    const float m = key_logit(mk);
     float z = 0.f;
 #pragma unroll
     for (int j = 0; j < NPER; ++j)
-        if (lane + 32 * j < E) z += expf(v[j] - m);
+        if (lane + 32 * j < E) z += expf(key_logit(key[j]) - m);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kAll, z, o);
+    uint32_t rk = 0u;  // the key of rank `lane`
     for (int r = 0; r < k; ++r) {
-        uint32_t bk = 0u;
-        int bj = 0;
-#pragma unroll
-        for (int j = 0; j < NPER; ++j)
-            if (key[j] > bk) {  // strict: the lowest j among equal keys
-                bk = key[j];
-                bj = j;
-            }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, (bk == mk && mk != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
-        if ((int)(win & 31u) == lane && win != 0xffffffffu) {
+        if (r > 0) mk = __reduce_max_sync(kAll, bk);
+        const uint32_t held = __ballot_sync(kAll, bk == mk);
+        int wl = __ffs(held) - 1;
+        if (held & (held - 1u))  // a tie across lanes: the lowest expert index
+            wl = (int)(__reduce_min_sync(kAll, bk == mk ? (uint32_t)(lane + 32 * bj) : 0xffffffffu) & 31u);
+        if (lane == (r & 31)) {
+            if (r < 32) rk = mk;
+            else w[r] = __uint_as_float(mk);
+        }
+        if (lane == wl) {  // the winner records its expert, drops it and finds its next best
+            ids[r] = lane + 32 * bj;
 #pragma unroll
             for (int j = 0; j < NPER; ++j)
-                if (j == (int)(win >> 5)) {
-                    ids[r] = (int32_t)win;
-                    w[r] = expf(v[j] - m) / z;
-                    key[j] = 0u;
+                if (j == bj) key[j] = 0u;
+            bk = 0u;
+            bj = 0;
+#pragma unroll
+            for (int j = 0; j < NPER; ++j)
+                if (key[j] > bk) {
+                    bk = key[j];
+                    bj = j;
                 }
         }
     }
     __syncwarp();
-    if (lane == 0 && renorm) {
+    float p = 0.f;  // rank `lane`'s weight
+    if (lane < k) p = expf(key_logit(rk) - m) / z;
+    for (int r = lane + 32; r < k; r += 32) w[r] = expf(key_logit(__float_as_uint(w[r])) - m) / z;
+    if (renorm) {
         float psel = 0.f;
-        for (int r = 0; r < k; ++r) psel += w[r];
-        for (int r = 0; r < k; ++r) w[r] = w[r] / psel;
+        const int k1 = k < 32 ? k : 32;
+        for (int r = 0; r < k1; ++r) psel += __shfl_sync(kAll, p, r);
+        __syncwarp();
+        for (int r = 32; r < k; ++r) psel += w[r];
+        __syncwarp();
+        p = p / psel;
+        for (int r = lane + 32; r < k; r += 32) w[r] = w[r] / psel;
     }
+    if (lane < k) w[lane] = p;
     __syncwarp();
-}
-
-// Selection for one token by several warps of a block (E <= 64): sv holds
-// the token's E logits in shared memory.  Each calling warp computes the
-// maximum and the softmax sum exactly as select_token_n does, and ranks eight
-// experts e = 8 w + lane/4 (four lanes per expert, each counting a quarter
-// of the others; rank = experts before e in the order value descending,
-// index ascending); the lane holding a rank-r expert (r < k) writes ids[r]
-// and its softmax weight w[r] (renormalisation is left to the caller, once
-// every warp is done).  Warps w >= E/8 have nothing to rank and may skip it.
-__device__ __forceinline__ void select_rank_warp(const float *sv, int E, int k, int w, int lane, int32_t *ids,
-                                                 float *wout) {
-    float v[2];
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int e = lane + 32 * j;
-        v[j] = e < E ? sv[e] : -INFINITY;
-        if (e < E) m = fmaxf(m, v[j]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-        if (lane + 32 * j < E) z += expf(v[j] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    const int e = 8 * w + (lane >> 2), q = lane & 3;
-    const float ve = e < E ? sv[e] : 0.f;
-    int rank = 0;
-    if (e < E)
-        for (int e2 = q; e2 < E; e2 += 4) {
-            const float u = sv[e2];
-            rank += (u > ve || (u == ve && e2 < e)) ? 1 : 0;
-        }
-    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
-    if (e < E && q == 0 && rank < k) {
-        ids[rank] = e;
-        wout[rank] = expf(ve - m) / z;
-    }
 }
 
 template <class Logit>
@@ -139,12 +127,15 @@ __device__ __forceinline__ void select_token(Logit lg, int E, int k, int renorm,
 }
 
 // The same selection for logits in global memory (one token's row), kept out
-// of line with one instance (up to 8 experts per lane): a kernel that selects
+// of line with two instances (up to 2 and up to 8 experts per lane): a kernel that selects
 // once per launch keeps its hot loops close together in the instruction
 // cache instead of carrying an unrolled copy per expert count.
 static __device__ __noinline__ void select_token_global(const float *logits, int E, int k, int renorm, int lane,
                                                  int32_t *ids, float *w) {
-    select_token_n<8>([&](int e) { return __ldcg(logits + e); }, E, k, renorm, lane, ids, w, nullptr);
+    if (E <= 64)
+        select_token_n<2>([&](int e) { return __ldcg(logits + e); }, E, k, renorm, lane, ids, w, nullptr);
+    else
+        select_token_n<8>([&](int e) { return __ldcg(logits + e); }, E, k, renorm, lane, ids, w, nullptr);
 }
 #endif  // __CUDACC__
 

@@ -73,7 +73,7 @@ constexpr int kTrFills = 48, kTrItems = 64, kTrUnits = 16, kTrBlocks = 2;
 struct TrBlock {
     uint32_t fill[kTrFills][4];  // wait start, stage free, issued, kind << 24 | bytes
     uint32_t item[kTrItems][4];  // warp << 8 | kind, fill landed, intermediate landed, done
-    uint32_t unit[kTrUnits][2];  // start, queue unit
+    uint32_t unit[kTrUnits][4];  // start, queue unit, described, fills issued
     unsigned long long t0;
     uint32_t nitem, pad;
     uint32_t route[8];           // routing warp: start, selected, outputs, tables, published
