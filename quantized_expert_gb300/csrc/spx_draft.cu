@@ -793,43 +793,6 @@ __device__ __noinline__ int route_tables_warp(const DkParams &p, const DkLayout 
     int *act = reinterpret_cast<int *>(smem + L.act);
     int *stn = reinterpret_cast<int *>(smem + L.stn);
     TokEntry *ste = reinterpret_cast<TokEntry *>(smem + L.ste);
-    if (T == 1 && k <= 32) {
-        // one token: its k experts are distinct, one slot each; an expert's
-        // place in the active list = the selected experts below it
-        const int e = lane < k ? ids[lane] : 0x7fffffff;
-        int a = 0;
-        for (int s2 = 0; s2 < k; ++s2) a += __shfl_sync(0xffffffffu, e, s2) < e;
-        if (lane < k) {
-            TokEntry te;
-            te.tok = 0;
-            te.row = 0;
-            te.scale = pw[lane];
-            te.pad = 0;
-            ste[a] = te;
-            act[a] = e;
-            stn[a] = 1;
-            if (out) p.sorted_slots[a] = lane;
-        }
-        if (out) {
-            __syncwarp();
-            for (int e2 = lane; e2 < E; e2 += 32) {
-                int c = 0, below = 0;
-                for (int s2 = 0; s2 < k; ++s2) {
-                    const int es = ids[s2];
-                    c += es == e2;
-                    below += es < e2;
-                }
-                p.counts[e2] = c;
-                p.offsets[e2] = below;
-                p.active_out[e2] = e2 < k ? act[e2] : -1;
-            }
-            if (lane == 0) {
-                p.offsets[E] = k;
-                *p.n_active_out = k;
-            }
-        }
-        return k;
-    }
     int nfirst = 0;
     for (int s = lane; s < n; s += 32) {  // rank of slot s among the earlier slots of its expert
         const int e = ids[s];
@@ -879,6 +842,72 @@ __device__ __noinline__ int route_tables_warp(const DkParams &p, const DkLayout 
         }
     }
     return na;
+}
+
+// One token, at most 32 selections (every block the same way): its k
+// experts straight from the logits in global memory, then the active-expert
+// table (an expert's place = the selected experts below it; each holds one
+// slot, the token's).  Returns k.  The routing outputs are written apart, by
+// route_one_outputs, once the tables are published.
+__device__ __noinline__ int route_one_token(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane) {
+    const int E = p.E, k = p.k;
+    int32_t *ids = reinterpret_cast<int32_t *>(smem + L.rids);
+    float *pw = reinterpret_cast<float *>(smem + L.rpw);
+    select_token_global(p.logits, E, k, p.renorm, lane, ids, pw);
+#if TL_ON
+    if (lane == 0 && TR_ON()) s_tr.route[1] = TR_NOW();
+#endif
+    int *act = reinterpret_cast<int *>(smem + L.act);
+    int *stn = reinterpret_cast<int *>(smem + L.stn);
+    TokEntry *ste = reinterpret_cast<TokEntry *>(smem + L.ste);
+    const int e = lane < k ? ids[lane] : 0x7fffffff;
+    int a = 0;
+    for (int s2 = 0; s2 < k; ++s2) a += __shfl_sync(0xffffffffu, e, s2) < e;
+    if (lane < k) {
+        TokEntry te;
+        te.tok = 0;
+        te.row = 0;
+        te.scale = pw[lane];
+        te.pad = 0;
+        ste[a] = te;
+        act[a] = e;
+        stn[a] = 1;
+    }
+    return k;
+}
+
+// Block 0's routing outputs for one token (k <= 32): the selections and
+// their weights, the lookahead counters, and the gather arrays (per-expert
+// counts and offsets, slots in expert order, the active list).
+__device__ __noinline__ void route_one_outputs(const DkParams &p, const DkLayout &L, const uint8_t *smem, int lane) {
+    const int E = p.E, k = p.k;
+    const int32_t *ids = reinterpret_cast<const int32_t *>(smem + L.rids);
+    const float *pw = reinterpret_cast<const float *>(smem + L.rpw);
+    const int *act = reinterpret_cast<const int *>(smem + L.act);
+    const int e = lane < k ? ids[lane] : 0x7fffffff;
+    if (lane < k) {
+        int a = 0;
+        for (int s2 = 0; s2 < k; ++s2) a += ids[s2] < e;
+        p.topk_ids[lane] = e;
+        p.topk_w[lane] = pw[lane];
+        p.sorted_slots[a] = lane;
+        if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
+    }
+    for (int e2 = lane; e2 < E; e2 += 32) {
+        int c = 0, below = 0;
+        for (int s2 = 0; s2 < k; ++s2) {
+            const int es = ids[s2];
+            c += es == e2;
+            below += es < e2;
+        }
+        p.counts[e2] = c;
+        p.offsets[e2] = below;
+        p.active_out[e2] = e2 < k ? act[e2] : -1;
+    }
+    if (lane == 0) {
+        p.offsets[E] = k;
+        *p.n_active_out = k;
+    }
 }
 
 // The unit call's routing: active experts and their token tables from global
@@ -1005,28 +1034,26 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
 #if TL_ON
         if (lane == 0 && TR_ON()) s_tr.route[0] = TR_NOW();
 #endif
-        int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
-        float *rpw = reinterpret_cast<float *>(smem + L.rpw);
-        const int E = p.E, k = p.k;
-        select_token_global(p.logits, E, k, p.renorm, lane, rids, rpw);
+        if (p.k <= 32) {
+            publish_routing(route_one_token(p, L, smem, lane));
 #if TL_ON
-        if (lane == 0 && TR_ON()) s_tr.route[1] = TR_NOW();
+            if (lane == 0 && TR_ON()) s_tr.route[3] = TR_NOW();
 #endif
-        if (blockIdx.x == 0)
-            for (int r = lane; r < k; r += 32) {
-                const int e = rids[r];
-                p.topk_ids[r] = e;
-                p.topk_w[r] = rpw[r];
-                if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
-            }
-#if TL_ON
-        if (lane == 0 && TR_ON()) s_tr.route[2] = TR_NOW();
-#endif
-        const int na_r = route_tables_warp(p, L, smem, lane, blockIdx.x == 0);
-#if TL_ON
-        if (lane == 0 && TR_ON()) s_tr.route[3] = TR_NOW();
-#endif
-        publish_routing(na_r);
+            if (blockIdx.x == 0) route_one_outputs(p, L, smem, lane);  // off the routed items' path
+        } else {
+            int32_t *rids = reinterpret_cast<int32_t *>(smem + L.rids);
+            float *rpw = reinterpret_cast<float *>(smem + L.rpw);
+            const int E = p.E, k = p.k;
+            select_token_global(p.logits, E, k, p.renorm, lane, rids, rpw);
+            if (blockIdx.x == 0)
+                for (int r = lane; r < k; r += 32) {
+                    const int e = rids[r];
+                    p.topk_ids[r] = e;
+                    p.topk_w[r] = rpw[r];
+                    if (p.elb) atomicAdd(p.elb + (size_t)p.layer * E + e, 1u);
+                }
+            publish_routing(route_tables_warp(p, L, smem, lane, blockIdx.x == 0));
+        }
 #if TL_ON
         if (lane == 0 && TR_ON()) s_tr.route[4] = TR_NOW();
 #endif
@@ -1585,31 +1612,6 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     all_sync();
     if (misc[1]) {
         __threadfence();
-        if (p.mode == 2) {
-            // batches of 8 float4 per thread, all loads of a batch in flight
-            const int n4 = T * H / 4;
-            constexpr int kNth = kDkCons * 32, kBatch = 8;
-            float4 *acc4 = reinterpret_cast<float4 *>(p.yout);
-            for (int i0 = ctid; i0 < n4; i0 += kNth * kBatch) {
-                float4 v[kBatch];
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int idx = i0 + j * kNth;
-                    v[j] = idx < n4 ? __ldcg(acc4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int idx = i0 + j * kNth;
-                    if (idx < n4) {
-                        uint2 o;
-                        o.x = h2_as_u32(__floats2half2_rn(v[j].x, v[j].y));
-                        o.y = h2_as_u32(__floats2half2_rn(v[j].z, v[j].w));
-                        reinterpret_cast<uint2 *>(p.out)[idx] = o;
-                        __stcg(acc4 + idx, make_float4(0.f, 0.f, 0.f, 0.f));
-                    }
-                }
-            }
-        }
         for (int i = ctid; i < geo.sd_nr; i += kDkCons * 32) p.rdy_s[i] = 0;
         for (int i = ctid; i < p.nact_max * geo.rd_nr; i += kDkCons * 32) p.rdy_r[i] = 0;
         if (ctid < kDkShards) p.qctr[64 * ctid] = 0;
