@@ -804,7 +804,8 @@ def run_prefetch(args):
     host = [ly["f16"].buf.cpu().pin_memory() for ly in lays]
     dev = [ly["f16"].buf for ly in lays]
     f16 = [spx.PackedF16(d, E, H, s.I) for d in dev]
-    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    stream = torch.cuda.Stream()
+    sides = [torch.cuda.Stream() for _ in range(max(1, args.prefetch_streams))]  # copy streams
     f16dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()  # noqa: E731
     xd = [[f16dev(W.gen_x(s, 1, layer=l, step=st)) for l in range(L)] for st in range(1, K + 1)]
     lgd = [[torch.from_numpy(W.draft_logits(s, l, st)).cuda() for l in range(L)] for st in range(1, K + 1)]
@@ -845,13 +846,20 @@ def run_prefetch(args):
     e1.record(stream)
     torch.cuda.synchronize()
     step_us = e0.elapsed_time(e1) * 1e3 / K
-    with torch.cuda.stream(side):
-        e0.record(side)
-        for i in range(8):
-            dev[0][(i % E) * eb:(i % E + 1) * eb].copy_(host[0][(i % E) * eb:(i % E + 1) * eb], non_blocking=True)
-        e1.record(side)
+    # one expert's copy time with the copies spread over the copy streams
+    ncp = 8 * len(sides)
     torch.cuda.synchronize()
-    copy_us = e0.elapsed_time(e1) * 1e3 / 8
+    e0.record(stream)
+    for sd in sides:
+        sd.wait_stream(stream)
+    for i in range(ncp):
+        with torch.cuda.stream(sides[i % len(sides)]):
+            dev[0][(i % E) * eb:(i % E + 1) * eb].copy_(host[0][(i % E) * eb:(i % E + 1) * eb], non_blocking=True)
+    for sd in sides:
+        stream.wait_stream(sd)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    copy_us = e0.elapsed_time(e1) * 1e3 / ncp
     cfg = spx.PlanCfg(L, E, K, E, 1, step_us, copy_us)
 
     def offload():
@@ -867,11 +875,22 @@ def run_prefetch(args):
             for l in range(L):
                 spx.spx_moe_layer((vflag if flags else vres)[l][0], stream)
 
+    def issue(acts):
+        # actions dealt round-robin to the copy streams: each expert's copy and
+        # its flags stay in one stream's order
+        acts = np.asarray(acts, np.int32).reshape(-1, 3)
+        for sd in sides:
+            sd.wait_stream(stream)
+        for j, sd in enumerate(sides):
+            part = acts[j::len(sides)]
+            if len(part):
+                spx.spx_prefetch_issue(part, host, dev, eb, ready, resident, stream=sd)
+
     def load_all(need_by_layer, cached):
         acts = [[l, e, spx.SPX_PLAN_LOAD] for l in range(L) for e in need_by_layer[l] if not cached[l, e]]
         for l in range(L):
             cached[l, need_by_layer[l]] = 1
-        spx.spx_prefetch_issue(np.array(acts, np.int32).reshape(-1, 3), host, dev, eb, ready, resident, stream=side)
+        issue(acts)
         return len(acts)
 
     res = {}
@@ -898,8 +917,7 @@ def run_prefetch(args):
                         stream.synchronize()  # the snapshot at the chunk boundary
                     snap = elb_host.numpy().astype(np.uint32) if done else np.zeros((L, E), np.uint32)
                     phase, acts, chunk = spx.spx_plan_prefetch(cfg, snap, done, cached)
-                    side.wait_stream(stream)
-                    spx.spx_prefetch_issue(acts, host, dev, eb, ready, resident, stream=side)
+                    issue(acts)
                     nload += int((acts[:, 2] == spx.SPX_PLAN_LOAD).sum()) if len(acts) else 0
                     if phase == spx.SPX_PLAN_FINAL_CLEANUP:
                         break
@@ -909,10 +927,11 @@ def run_prefetch(args):
                 draft_steps(0, K)
             c1.record(stream)
             if arm != "resident":
-                side.wait_stream(stream)
                 nload += load_all(verify_need, cached)  # the verify's experts not cached yet
             verify_pass(arm != "resident")
             c2.record(stream)
+            for sd in sides:
+                stream.wait_stream(sd)
             torch.cuda.synchronize()
             reps.append((c0.elapsed_time(c2) * 1e3, c1.elapsed_time(c2) * 1e3, nload))
             assert spx.spx_workspace_status(ws_v) == 0 and spx.spx_workspace_status(ws_d) == 0
@@ -924,7 +943,8 @@ def run_prefetch(args):
     line = {"metric": "verify-pass copy wait hidden by the Layer-Aware Prefetch Planner",
             "config": {"workload": f"{s.name} shape, {L} layers, K={K} draft steps (T=1) then verify (T={Tv}); routed "
                                    f"FP16 experts in page-locked host memory, copied over NVLink-C2C",
-                       "expert_bytes": int(eb), "step_us": round(step_us, 1), "copy_us_per_expert": round(copy_us, 1),
+                       "expert_bytes": int(eb), "step_us": round(step_us, 1), "copy_streams": len(sides),
+                       "copy_us_per_expert": round(copy_us, 1),
                        "link_gbs": round(eb / (copy_us * 1e-6) / 1e9, 1)},
             "arms": res,
             "hidden_share": round(1.0 - wait_pl / wait_od, 3) if wait_od > 0 else None,
@@ -1076,6 +1096,7 @@ def main():
     ap.add_argument("--prefetch", action="store_true",
                     help="verify copy wait hidden by the prefetch plan (prints its own line)")
     ap.add_argument("--prefetch-layers", type=int, default=4)
+    ap.add_argument("--prefetch-streams", type=int, default=4, help="with --prefetch: copy streams of the executor")
     ap.add_argument("--timeline", action="store_true",
                     help="draft launch phase marks from the profiling build (prints its own line)")
     args = ap.parse_args()
