@@ -50,10 +50,10 @@ KERNEL_SOURCES = {
     "verify": ["spx_engine.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_098_624 + 3_160_320,
-               "algorithmic_bytes": 674_897_920, "source_sha": None},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_515_008 + 109_568, "algorithmic_bytes": 61_374_720,
-              "source_sha": None},
+    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_096_064 + 3_027_712,
+               "algorithmic_bytes": 674_897_920, "source_sha": "318d6c7accafd9eb"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_648 + 797_696, "algorithmic_bytes": 61_374_720,
+              "source_sha": "d331d7992ba30449"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
@@ -584,6 +584,55 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def apply_formats(s, sets, args, torch, spx):
+    """Replace each weight set's INT4 draft experts by the format the flags ask
+    for: --zeros (INT4 with seeded per-group zero points) or --gguf (GGUF
+    super-blocks with random codes and scales of the INT4 weights' magnitude)."""
+    if args.zeros:  # asymmetric INT4: seeded per-group zero points on every set
+        E, H, I = s.E, s.H, s.I
+        for i, st in enumerate(sets):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(2_000_003 * (s.seed + 1) + i)
+
+            def words(*shape):
+                return torch.randint(-2 ** 31, 2 ** 31, shape, dtype=torch.int32, device="cuda", generator=g)
+
+            st["w4"] = spx.spx_w4_zeros_repack(st["w4"], words(E, H // 128, I // 8), words(E, H // 128, I // 8),
+                                               words(E, I // 128, H // 8))
+        torch.cuda.synchronize()
+    if args.gguf:  # GGUF experts instead of INT4: random codes, scales of the INT4 weights' magnitude
+        E, H, I = s.E, s.H, s.I
+        for i, st in enumerate(sets):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(3_000_017 * (s.seed + 1) + i)
+
+            def scales(shape, lo, hi):
+                return (torch.rand(shape, device="cuda", generator=g) * (hi - lo) + lo).half().view(torch.uint8)
+
+            def q8(N, K):  # Q8_0 blocks, d U(0.0003, 0.00125)
+                b = torch.randint(0, 256, (E, N, K // 32, 34), dtype=torch.uint8, device="cuda", generator=g)
+                b[..., :2] = scales((E, N, K // 32), 0.0003, 0.00125).view(E, N, K // 32, 2)
+                return b
+
+            def q2k(N, K):  # Q2_K super-blocks, d U(0.001, 0.003), dmin U(0.001, 0.004)
+                b = torch.randint(0, 256, (E, N, K // 256, 84), dtype=torch.uint8, device="cuda", generator=g)
+                b[..., 80:82] = scales((E, N, K // 256), 0.001, 0.003).view(E, N, K // 256, 2)
+                b[..., 82:84] = scales((E, N, K // 256), 0.001, 0.004).view(E, N, K // 256, 2)
+                return b
+
+            def q4k(N, K):  # Q4_K super-blocks, d U(0.00015, 0.0004), dmin U(0.0003, 0.001)
+                b = torch.randint(0, 256, (E, N, K // 256, 144), dtype=torch.uint8, device="cuda", generator=g)
+                b[..., 0:2] = scales((E, N, K // 256), 0.00015, 0.0004).view(E, N, K // 256, 2)
+                b[..., 2:4] = scales((E, N, K // 256), 0.0003, 0.001).view(E, N, K // 256, 2)
+                return b
+
+            gu, ty = {"q8_0": (q8, spx.SPX_GGUF_Q8_0), "q2_k": (q2k, spx.SPX_GGUF_Q2_K),
+                      "q4_k": (q4k, spx.SPX_GGUF_Q4_K)}[args.gguf]
+            st["w4"] = None
+            st["gguf"] = spx.spx_gguf_repack(gu(I, H), gu(I, H), q8(H, I), ty)
+            torch.cuda.synchronize()
+
+
 def run_loop(args):
     """Profiling driver: --loop-n layer calls of one mode on --sets weight sets,
     no timing (the command that ncu captures wrap)."""
@@ -593,18 +642,26 @@ def run_loop(args):
     spx.load()
     s = W.CONFIGS[args.config]
     sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
-    inp = make_inputs(s, 0)
     draft = args.loop == "draft"
-    T = s.T_draft if draft else s.T_verify
-    xk, lk = ("x_d", "lg_d") if draft else ("x_v", "lg_v")
-    x = torch.from_numpy(np.ascontiguousarray(inp[xk]).view(np.float16)).cuda()
-    lg = torch.from_numpy(inp[lk]).cuda() if lk in inp else torch.empty(T, s.E, device="cuda")
+    if draft:
+        apply_formats(s, sets, args, torch, spx)
+    if args.tokens:  # another token count than the shape's draft / verify one
+        T = args.tokens
+        x = torch.from_numpy(np.ascontiguousarray(W.gen_x(s, T, step=1)).view(np.float16)).cuda()
+        lg = (torch.from_numpy(W.gen_logits(s, T, step=1)).cuda() if s.logits != "router"
+              else torch.empty(T, s.E, device="cuda"))
+    else:
+        inp = make_inputs(s, 0)
+        T = s.T_draft if draft else s.T_verify
+        xk, lk = ("x_d", "lg_d") if draft else ("x_v", "lg_v")
+        x = torch.from_numpy(np.ascontiguousarray(inp[xk]).view(np.float16)).cuda()
+        lg = torch.from_numpy(inp[lk]).cuda() if lk in inp else torch.empty(T, s.E, device="cuda")
     ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
     r = spx.Routing.empty(T, s.E, s.k)
     out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
     keep = [spx.layer_args(0 if draft else 1, x, s.E, s.k, s.renorm, lg, r, out, ws,
                            w4=st["w4"] if draft else None, f16=None if draft else st["f16"], shared=st["shared"],
-                           w_router=st["w_router"]) for st in sets]
+                           w_router=st["w_router"], gguf=st.get("gguf") if draft else None) for st in sets]
     for i in range(args.loop_n):
         spx.spx_moe_layer(keep[i % len(keep)][0])
     torch.cuda.synchronize()
@@ -692,49 +749,7 @@ def run_draft_batch(args):
     spx.load()
     s = W.CONFIGS[args.config]
     sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
-    if args.zeros:  # asymmetric INT4: seeded per-group zero points on every set
-        E, H, I = s.E, s.H, s.I
-        for i, st in enumerate(sets):
-            g = torch.Generator(device="cuda")
-            g.manual_seed(2_000_003 * (s.seed + 1) + i)
-
-            def words(*shape):
-                return torch.randint(-2 ** 31, 2 ** 31, shape, dtype=torch.int32, device="cuda", generator=g)
-
-            st["w4"] = spx.spx_w4_zeros_repack(st["w4"], words(E, H // 128, I // 8), words(E, H // 128, I // 8),
-                                               words(E, I // 128, H // 8))
-        torch.cuda.synchronize()
-    if args.gguf:  # GGUF experts instead of INT4: random codes, scales of the INT4 weights' magnitude
-        E, H, I = s.E, s.H, s.I
-        for i, st in enumerate(sets):
-            g = torch.Generator(device="cuda")
-            g.manual_seed(3_000_017 * (s.seed + 1) + i)
-
-            def scales(shape, lo, hi):
-                return (torch.rand(shape, device="cuda", generator=g) * (hi - lo) + lo).half().view(torch.uint8)
-
-            def q8(N, K):  # Q8_0 blocks, d U(0.0003, 0.00125)
-                b = torch.randint(0, 256, (E, N, K // 32, 34), dtype=torch.uint8, device="cuda", generator=g)
-                b[..., :2] = scales((E, N, K // 32), 0.0003, 0.00125).view(E, N, K // 32, 2)
-                return b
-
-            def q2k(N, K):  # Q2_K super-blocks, d U(0.001, 0.003), dmin U(0.001, 0.004)
-                b = torch.randint(0, 256, (E, N, K // 256, 84), dtype=torch.uint8, device="cuda", generator=g)
-                b[..., 80:82] = scales((E, N, K // 256), 0.001, 0.003).view(E, N, K // 256, 2)
-                b[..., 82:84] = scales((E, N, K // 256), 0.001, 0.004).view(E, N, K // 256, 2)
-                return b
-
-            def q4k(N, K):  # Q4_K super-blocks, d U(0.00015, 0.0004), dmin U(0.0003, 0.001)
-                b = torch.randint(0, 256, (E, N, K // 256, 144), dtype=torch.uint8, device="cuda", generator=g)
-                b[..., 0:2] = scales((E, N, K // 256), 0.00015, 0.0004).view(E, N, K // 256, 2)
-                b[..., 2:4] = scales((E, N, K // 256), 0.0003, 0.001).view(E, N, K // 256, 2)
-                return b
-
-            gu, ty = {"q8_0": (q8, spx.SPX_GGUF_Q8_0), "q2_k": (q2k, spx.SPX_GGUF_Q2_K),
-                      "q4_k": (q4k, spx.SPX_GGUF_Q4_K)}[args.gguf]
-            st["w4"] = None
-            st["gguf"] = spx.spx_gguf_repack(gu(I, H), gu(I, H), q8(H, I), ty)
-            torch.cuda.synchronize()
+    apply_formats(s, sets, args, torch, spx)
     peak, peak_src = measured_peaks()
     rows = []
     stream = torch.cuda.Stream()
@@ -1089,10 +1104,13 @@ def main():
     ap.add_argument("--sets", type=int, default=NSETS, help="rotated weight sets (8 defeat L2)")
     ap.add_argument("--loop", choices=["draft", "verify"], help="profiling driver: layer calls only, no timing")
     ap.add_argument("--loop-n", type=int, default=12)
+    ap.add_argument("--tokens", type=int, default=0, help="with --loop: tokens per call (default: the shape's)")
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
-    ap.add_argument("--zeros", action="store_true", help="with --draft-batch: INT4 experts with per-group zero points")
-    ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"], help="with --draft-batch: GGUF experts instead of INT4")
+    ap.add_argument("--zeros", action="store_true",
+                    help="with --draft-batch or --loop draft: INT4 experts with per-group zero points")
+    ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"],
+                    help="with --draft-batch or --loop draft: GGUF experts instead of INT4")
     ap.add_argument("--prefetch", action="store_true",
                     help="verify copy wait hidden by the prefetch plan (prints its own line)")
     ap.add_argument("--prefetch-layers", type=int, default=4)
