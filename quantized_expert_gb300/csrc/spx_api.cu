@@ -148,7 +148,7 @@ extern "C" int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_expert
     if (st) return st;
     if (!al16(w->packed) || !al16(y_sorted) || !al16(w->zeros)) return SPX_ERR_INVALID_ARG;
     const bool draft = draft_supported(T, w->H, w->I, w->slice_cols, 0, w->E, k);
-    if (w->zeros && !draft) return SPX_ERR_UNSUPPORTED;  // zero points: the draft launch only
+    if (w->zeros && !draft && !engine_fits(T, w->H, kFmtW4Z, w->slice_cols)) return SPX_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
     p.routed = static_cast<const uint8_t *>(w->packed);
@@ -331,7 +331,9 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
 
     const bool zeros = a->mode == 0 && !gguf && a->w4->zeros;
     const bool kq = gguf && (gguf_fmt(a->gguf) == kFmtQ2K || gguf_fmt(a->gguf) == kFmtQ4K);
-    if ((zeros || gguf) && (cache_aware || !draft_supported(T, H, I, S, I_s, E, k, kq))) return SPX_ERR_UNSUPPORTED;
+    const bool via_draft = !cache_aware && draft_supported(T, H, I, S, I_s, E, k, kq);
+    if (gguf && !via_draft) return SPX_ERR_UNSUPPORTED;  // GGUF experts: the draft launch only
+    if (zeros && !via_draft && !engine_fits(T, H, kFmtW4Z, S)) return SPX_ERR_UNSUPPORTED;
     // every check has passed: only now may the caller's scratch be cleared
     if (clear) {
         const cudaError_t ce = cudaMemsetAsync(clear, 0, clear_bytes, s);
@@ -414,6 +416,7 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
     EngineParams p = base_params(a->x, T, H, a->ws);
     p.routed = routed;
     p.routed_fmt = a->mode == 0 ? 0 : 1;
+    p.w4_zeros = zeros ? static_cast<const uint8_t *>(a->w4->zeros) : nullptr;
     p.S = S;
     if (a->mode == 0) p.w4_sdown = reinterpret_cast<const __half *>(routed + w4_units_bytes(E, H, I, S));
     p.E = E;

@@ -1612,6 +1612,31 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     all_sync();
     if (misc[1]) {
         __threadfence();
+        if (p.mode == 2) {
+            // batches of 8 float4 per thread, all loads of a batch in flight
+            const int n4 = T * H / 4;
+            constexpr int kNth = kDkCons * 32, kBatch = 8;
+            float4 *acc4 = reinterpret_cast<float4 *>(p.yout);
+            for (int i0 = ctid; i0 < n4; i0 += kNth * kBatch) {
+                float4 v[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = i0 + j * kNth;
+                    v[j] = idx < n4 ? __ldcg(acc4 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = i0 + j * kNth;
+                    if (idx < n4) {
+                        uint2 o;
+                        o.x = h2_as_u32(__floats2half2_rn(v[j].x, v[j].y));
+                        o.y = h2_as_u32(__floats2half2_rn(v[j].z, v[j].w));
+                        reinterpret_cast<uint2 *>(p.out)[idx] = o;
+                        __stcg(acc4 + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+                    }
+                }
+            }
+        }
         for (int i = ctid; i < geo.sd_nr; i += kDkCons * 32) p.rdy_s[i] = 0;
         for (int i = ctid; i < p.nact_max * geo.rd_nr; i += kDkCons * 32) p.rdy_r[i] = 0;
         if (ctid < kDkShards) p.qctr[64 * ctid] = 0;

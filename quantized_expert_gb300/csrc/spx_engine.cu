@@ -44,7 +44,7 @@ enum : int { HK_GU = 1, HK_DOWN = 2, HK_DONE = 3 };
 // HF_PAIR: the unit is an FP16 pair (a down chunk holds both slices' blocks).
 enum : int { HF_UNIT_START = 1, HF_GU_LAST = 2, HF_GU_FINAL = 4, HF_SUB1 = 8, HF_PAIR = 16 };
 enum : int { MODE_SORTED = 0, MODE_ACC = 1, MODE_LAYER = 2 };
-enum : int { FMT_W4 = 0, FMT_F16 = 1 };
+enum : int { FMT_W4 = 0, FMT_F16 = 1, FMT_W4Z = kFmtW4Z };  // FMT_W4Z: INT4 with per-group zero points
 
 struct __align__(16) ChunkHeader {
     int unit;
@@ -67,7 +67,7 @@ constexpr int kHsStride = 40;                     // halves per intermediate row
 constexpr int kEpiBlocks = 16;                    // blocks sharing the fp16 output pass
 
 struct SmemLayout {
-    int bars, hdrs, gamma, misc, red, hs, sd, xs, ring, total;
+    int bars, hdrs, gamma, misc, red, hs, sd, zd, xsum, xs, ring, total;
     int xs_stride;  // halves per activation row
     int red_rs;     // floats per red row
 };
@@ -78,9 +78,11 @@ __host__ __device__ inline int engine_smax(bool w4, int S) { return w4 && S > 2 
 // G groups of 8/G consumer warps; nsg stages per group.
 // red: per group, [2*smax][T] fp32 gate/up sums (the group's warps add into it);
 // hs : per group, [npad][kHsStride] fp16 intermediate; sd: per group, 2 x [H]
-// fp16 down-scale rows (INT4 only, double-buffered by unit parity).
+// fp16 down-scale rows (INT4 only, double-buffered by unit parity); with zero
+// points (zp) zd: the same for the down zero-point rows, and xsum: [T][H/128]
+// fp32 sums of each activation row over each group of 128.
 __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg,
-                                                  int chunk) {
+                                                  int chunk, bool zp = false) {
     SmemLayout L;
     const int nst = G * nsg;
     int o = 0;
@@ -101,6 +103,11 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     o = (o + 15) & ~15;
     L.sd = o;
     if (w4) o += G * 2 * H * 2;
+    o = (o + 15) & ~15;
+    L.zd = o;
+    if (zp) o += G * 2 * H * 2;
+    L.xsum = o;
+    if (zp) o += T * (H / 128) * 4;
     o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
@@ -238,7 +245,10 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
         s[g].pend_u = fetch();
     }
     const int chunk = p.chunk;
-    const int W4GPC = chunk / (int)w4_group_bytes(p.S);  // whole INT4 groups per chunk
+    // zero points: a gate/up chunk carries its groups' zero points (2S fp16
+    // per group, as the scales) after their codes
+    const bool zp = p.w4_zeros != nullptr && !rf16;
+    const int W4GPC = chunk / ((int)w4_group_bytes(p.S) + (zp ? 4 * p.S : 0));  // whole INT4 groups per chunk
     long long t_prog = clock64();
     const long long budget = (long long)p.wait_budget_ns * 2;  // cycles at ~2 GHz
     bool aborted = false;
@@ -297,7 +307,7 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             h.e = S_.e;
             h.i0 = shared ? S_.u * 2 * kF16S : S_.i0;
             h.flags = 0;
-            const uint8_t *src2 = nullptr;  // second slice of an FP16 pair's down chunk
+            const uint8_t *src2 = nullptr;  // second slice of an FP16 pair's down chunk, or INT4 zero points
             uint32_t bytes2 = 0;
             if (S_.fmt == FMT_W4) {
                 const int S = p.S;
@@ -310,6 +320,11 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                     h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == ngr ? HF_GU_LAST | HF_GU_FINAL : 0);
                     src = S_.base + (size_t)S_.b * w4_group_bytes(S);
                     bytes = h.nb * (uint32_t)w4_group_bytes(S);
+                    if (zp) {
+                        const size_t uix = (size_t)S_.e * nu_r + S_.i0 / S;
+                        src2 = p.w4_zeros + (uix * (H / 128) + S_.b) * 4 * S;
+                        bytes2 = h.nb * 4u * (uint32_t)S;
+                    }
                     S_.b += h.nb;
                     if (S_.b >= ngr) S_.phase = 1, S_.b = 0;
                 } else {
@@ -421,20 +436,29 @@ __device__ __forceinline__ void group_sync(const EngineParams &p, Sync &sy, vola
     __syncwarp();
 }
 
-// RFMT: format of the routed experts (INT4 draft or FP16 verify); the FP16
-// kernel carries no INT4 code.  Nine warps per block put three warps on one SM
-// sub-partition, whose 16K registers cap a thread at 168 registers.
+// RFMT: format of the routed experts (INT4 draft, INT4 with zero points, or
+// FP16 verify); the FP16 kernel carries no INT4 code.  Nine warps per block
+// put three warps on one SM sub-partition, whose 16K registers cap a thread
+// at 168 registers.
+//
+// Zero points (FMT_W4Z; the AWQ form W = s (q - z), z per group of 128 input
+// rows and output column): the mma sums x (q - 8) as for symmetric INT4, and
+// the group's term s (8 - z) * (sum of x over the group) is added per token
+// column (gate/up); the down projection adds s (8 - z) * (sum of h over the
+// unit's S intermediate rows, which lie in one group of 128).
 template <int RFMT, int MS4, int NT>
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams p) {
+    constexpr bool ZP = RFMT == FMT_W4Z;
+    constexpr bool W4R = RFMT == FMT_W4 || ZP;  // INT4 routed experts
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
     griddep_launch_dependents();
-    const bool has_w4 = RFMT == FMT_W4 && p.routed_enabled;
+    const bool has_w4 = W4R && p.routed_enabled;
     const int smax = engine_smax(has_w4, p.S);
     const int G = p.groups, nsg = p.nstages;
     const int gwarps = kConsumerWarps / G;
-    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg, p.chunk);
+    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg, p.chunk, ZP);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -477,6 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     float *red = reinterpret_cast<float *>(smem + L.red) + (size_t)grp_id * 2 * smax * rs;
     __half *hs = reinterpret_cast<__half *>(smem + L.hs) + (size_t)grp_id * npad * kHsStride;
     __half *sdg = reinterpret_cast<__half *>(smem + L.sd) + (size_t)grp_id * 2 * p.H;
+    __half *zdg = reinterpret_cast<__half *>(smem + L.zd) + (size_t)grp_id * 2 * p.H;  // ZP only
+    const float *xsum = reinterpret_cast<const float *>(smem + L.xsum);                 // ZP only
+    const int ngr = p.H / 128;
     __half *xs = reinterpret_cast<__half *>(smem + L.xs);
     const int ctid = threadIdx.x;  // 0..255
     const int H = p.H;
@@ -486,6 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     for (int idx = ctid; idx < G * 2 * smax * rs; idx += kConsumerWarps * 32)
         reinterpret_cast<float *>(smem + L.red)[idx] = 0.f;
     mbar_wait_bounded(xbar, 0, abort_flag, &p.hdr->status, p.wait_budget_ns);
+    if (ZP) {  // each activation row's sums over the groups of 128
+        float *xsw = reinterpret_cast<float *>(smem + L.xsum);
+        for (int idx = ctid; idx < p.T * ngr; idx += kConsumerWarps * 32) {
+            const int t = idx / ngr, gi = idx - t * ngr;
+            const __half2 *xr2 = reinterpret_cast<const __half2 *>(xs + (size_t)t * L.xs_stride + gi * 128);
+            float sum = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < 64; ++j) {
+                const float2 f = __half22float2(xr2[j]);
+                sum += f.x + f.y;
+            }
+            xsw[idx] = sum;
+        }
+    }
     group_sync(p, as, abort_flag);
     // shared-expert gate per token: gamma = 1 / (1 + exp(-x . w_sgate)), else 1
     if (p.shared && p.w_sgate) {
@@ -512,7 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     int u_fmt = FMT_F16, u_S = kF16S, u_e = 0, u_i0 = 0, n_e = 0, nact = 0;
     uint32_t ucount = 0;     // units started by this group (selects the down-scale buffer)
     const __half *sdcur = sdg;
+    const __half *zdcur = zdg;
     int xoff[NT];
+    int ctok[NT][2];     // ZP: tokens of this lane's output columns 2*q4, 2*q4+1 of each n-tile
+    float hsum[NT][2];   // ZP: their sums of h over the unit's intermediate rows
     int orow[NT][2];
     float oscl[NT][2];
     float run[NTW][NT][4];                // gate/up partial sums of this warp for the whole unit
@@ -555,15 +599,19 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                     const int col = nt * 8 + 2 * q4 + hf;
                     int r = 0;
                     float sc = 0.f;
+                    int ct = 0;
                     if (col < n) {
                         if (h.shared) {
                             r = col;
                             sc = p.mode == MODE_SORTED ? 1.f : gamma[col];
+                            ct = col;
                         } else {
                             r = tb->e[col].row;
                             sc = tb->e[col].scale;
+                            ct = tb->e[col].tok;
                         }
                     }
+                    ctok[nt][hf] = (ct >= 0 && ct < p.T) ? ct : 0;
                     const bool okr = r >= 0 && r < rmax;
                     orow[nt][hf] = okr ? r : 0;
                     oscl[nt][hf] = okr ? sc : 0.f;
@@ -575,19 +623,31 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int r = 0; r < 4; ++r) run[t][nt][r] = 0.f;
-            if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
+            if (W4R && u_fmt == FMT_W4) {
                 // fetch this unit's down-scale row into the group's buffer for
                 // this unit's parity; waited for at the gate/up -> down boundary
                 __half *dst = sdg + (size_t)(ucount & 1) * H;
                 const __half *srow = p.w4_sdown + ((size_t)u_e * (p.I / 128) + u_i0 / 128) * H;
                 for (int idx = gtid; idx < H / 8; idx += gwarps * 32) cp_async16(dst + idx * 8, srow + idx * 8);
+                if (ZP) {
+                    // and its down zero-point row: [E][H/32][I/128][32], 32 outputs a piece
+                    __half *zdst = zdg + (size_t)(ucount & 1) * H;
+                    const __half *zdn = reinterpret_cast<const __half *>(
+                        p.w4_zeros + w4_zeros_gu_bytes(p.E, H, p.I, p.S));
+                    const int nig = p.I / 128, gi = u_i0 / 128;
+                    for (int idx = gtid; idx < H / 8; idx += gwarps * 32) {
+                        const int blk = idx >> 2;
+                        cp_async16(zdst + idx * 8, zdn + (((size_t)u_e * (H / 32) + blk) * nig + gi) * 32 + (idx & 3) * 8);
+                    }
+                    zdcur = zdst;
+                }
                 cp_async_commit();
                 sdcur = dst;
             }
             ++ucount;
         }
         if (n_e > 0 && h.kind == HK_GU) {
-            if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
+            if (W4R && u_fmt == FMT_W4) {
                 // blocks of KB k-steps; 8/KB blocks per group after 4S bytes of scales
                 constexpr int KB = 2 / MS4;
                 constexpr int BPG = 8 / KB;
@@ -595,32 +655,55 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                 const int nblk = h.nb * BPG;
                 const int per = (nblk + gwarps - 1) / gwarps;
                 const int bb = gw * per, be = min(bb + per, nblk);
+                const __half *zsp = reinterpret_cast<const __half *>(stage + (size_t)h.nb * gb);  // ZP: after the codes
                 float acc[NTW][NT][4];
-                float sA[NTW], sB[NTW];
+                float sA[NTW], sB[NTW], dA[NTW], dB[NTW];  // scales; ZP: 8 - zero point
                 int grp = -1;
+                bool zfirst = false;  // ZP: this warp holds the group's first block (the group's
+                                      // zero-point term is added once, by that warp)
 #pragma unroll
-                for (int t = 0; t < NTW; ++t) sA[t] = sB[t] = 0.f;
+                for (int t = 0; t < NTW; ++t) sA[t] = sB[t] = dA[t] = dB[t] = 0.f;
+                // adds the finished group's sums, scaled (ZP: with the group's
+                // zero-point term per token column when this warp holds the
+                // group's first block; a group's blocks may be split between
+                // two warps)
+                auto flush = [&]() {
+                    float xa[NT][2];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+                            xa[nt][hf] = ZP && zfirst ? xsum[ctok[nt][hf] * ngr + h.b0 + grp] : 0.f;
+#pragma unroll
+                    for (int t = 0; t < NTW; ++t)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            run[t][nt][0] = fmaf(sA[t], ZP ? fmaf(dA[t], xa[nt][0], acc[t][nt][0]) : acc[t][nt][0],
+                                                 run[t][nt][0]);
+                            run[t][nt][1] = fmaf(sA[t], ZP ? fmaf(dA[t], xa[nt][1], acc[t][nt][1]) : acc[t][nt][1],
+                                                 run[t][nt][1]);
+                            run[t][nt][2] = fmaf(sB[t], ZP ? fmaf(dB[t], xa[nt][0], acc[t][nt][2]) : acc[t][nt][2],
+                                                 run[t][nt][2]);
+                            run[t][nt][3] = fmaf(sB[t], ZP ? fmaf(dB[t], xa[nt][1], acc[t][nt][3]) : acc[t][nt][3],
+                                                 run[t][nt][3]);
+                        }
+                };
                 for (int bl = bb; bl < be; ++bl) {
                     const int gr = bl / BPG, ib = bl - gr * BPG;
                     const uint8_t *gp = stage + (size_t)gr * gb;
                     if (gr != grp) {
-                        if (grp >= 0) {
-#pragma unroll
-                            for (int t = 0; t < NTW; ++t)
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
-                                    run[t][nt][0] = fmaf(sA[t], acc[t][nt][0], run[t][nt][0]);
-                                    run[t][nt][1] = fmaf(sA[t], acc[t][nt][1], run[t][nt][1]);
-                                    run[t][nt][2] = fmaf(sB[t], acc[t][nt][2], run[t][nt][2]);
-                                    run[t][nt][3] = fmaf(sB[t], acc[t][nt][3], run[t][nt][3]);
-                                }
-                        }
+                        if (grp >= 0) flush();
                         grp = gr;
+                        zfirst = ib == 0;
                         const __half *scp = reinterpret_cast<const __half *>(gp);
 #pragma unroll
                         for (int t = 0; t < NTW; ++t) {
                             sA[t] = __half2float(scp[t * 16 + g]);
                             sB[t] = __half2float(scp[t * 16 + g + 8]);
+                            if (ZP) {
+                                dA[t] = 8.f - __half2float(zsp[gr * 2 * u_S + t * 16 + g]);
+                                dB[t] = 8.f - __half2float(zsp[gr * 2 * u_S + t * 16 + g + 8]);
+                            }
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -650,17 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                         }
                     }
                 }
-                if (grp >= 0) {
-#pragma unroll
-                    for (int t = 0; t < NTW; ++t)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            run[t][nt][0] = fmaf(sA[t], acc[t][nt][0], run[t][nt][0]);
-                            run[t][nt][1] = fmaf(sA[t], acc[t][nt][1], run[t][nt][1]);
-                            run[t][nt][2] = fmaf(sB[t], acc[t][nt][2], run[t][nt][2]);
-                            run[t][nt][3] = fmaf(sB[t], acc[t][nt][3], run[t][nt][3]);
-                        }
-                }
+                if (grp >= 0) flush();
             } else {
                 const int nb = h.nb;
                 const int per = (nb + gwarps - 1) / gwarps;
@@ -690,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             const int per = (nb + gwarps - 1) / gwarps;
             const int bb = gw * per, be = min(bb + per, nb);
             for (int b = bb; b < be; ++b) {
-                if (RFMT == FMT_W4 && u_fmt == FMT_W4) {
+                if (W4R && u_fmt == FMT_W4) {
                     // block = 4/MS4 m-tiles (2/MS4 pairs), lane words [tile][ks]
                     constexpr int NPAIR = 2 / MS4;
                     const uint4 v = lds128(stage + (size_t)b * 512 + lane * 16);
@@ -707,6 +780,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                         const uint2 sv = *reinterpret_cast<const uint2 *>(sdcur + n0);
                         const float2 s01 = __half22float2(u32_as_h2(sv.x));
                         const float2 s23 = __half22float2(u32_as_h2(sv.y));
+                        float2 d01 = make_float2(0.f, 0.f), d23 = d01;  // ZP: 8 - zero point of outputs n0..n0+3
+                        if (ZP) {
+                            // the zero-point row keeps the column-block order of
+                            // the pair's 32 outputs: output 32 Q + 4 m' + 2 q + h
+                            // (m' < 8, tile q, row half h) sits at 16 q + 8 h + m'
+                            const __half *zq = zdcur + (n0 - 4 * g);
+                            d01 = make_float2(8.f - __half2float(zq[g]), 8.f - __half2float(zq[g + 8]));
+                            d23 = make_float2(8.f - __half2float(zq[16 + g]), 8.f - __half2float(zq[24 + g]));
+                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             if (nt < nact) {
@@ -721,6 +803,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                                     const int col = nt * 8 + 2 * q4 + hf;
                                     if (col < n_e) {
                                         const float w = oscl[nt][hf];
+                                        if (ZP) {
+                                            const float hsm = hsum[nt][hf];
+                                            acc[0][hf] = fmaf(d01.x, hsm, acc[0][hf]);
+                                            acc[0][2 + hf] = fmaf(d01.y, hsm, acc[0][2 + hf]);
+                                            acc[1][hf] = fmaf(d23.x, hsm, acc[1][hf]);
+                                            acc[1][2 + hf] = fmaf(d23.y, hsm, acc[1][2 + hf]);
+                                        }
                                         float4 o;
                                         o.x = acc[0][hf] * s01.x * w;
                                         o.y = acc[0][2 + hf] * s01.y * w;
@@ -810,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             // SiLU, h -> fp16 fragments; the buffer is left zeroed for the
             // group's next unit
             const int S = u_S;
-            if (RFMT == FMT_W4) cp_async_wait_all();  // this thread's share of the down-scale row
+            if (W4R) cp_async_wait_all();  // this thread's share of the down-scale (and zero-point) row
             group_sync(p, gs, abort_flag);
             // only the unit's n_e token columns hold sums (the others stay
             // zero); h columns past n_e feed output columns that are never
@@ -834,6 +923,23 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                     hb0[ks][nt] = okh ? lds32(hr) : 0u;
                     hb1[ks][nt] = okh ? lds32(hr + 8) : 0u;
                 }
+            if (ZP) {  // this lane's output columns' sums of h over the unit's rows
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int col = nt * 8 + 2 * q4 + hf;
+                        float sum = 0.f;
+                        if (col < n_e) {
+                            const __half2 *hr2 = reinterpret_cast<const __half2 *>(hs + col * kHsStride);
+                            for (int i = 0; i < S / 2; ++i) {
+                                const float2 f = __half22float2(hr2[i]);
+                                sum += f.x + f.y;
+                            }
+                        }
+                        hsum[nt][hf] = sum;
+                    }
+            }
         }
         ++it;
     }
@@ -954,30 +1060,31 @@ int engine_nt(int T) { return T <= 8 ? 1 : (T <= 24 ? 3 : 8); }
 // 434 us on GB300; DeepSeek-V2-Lite-shaped, 36 KB chunks: two groups).  Below
 // kChunk per chunk even then, one group with as many kChunk stages as fit.
 constexpr int kGroupSplitMin = 28 * 1024;
-static int fit_chunk(int T, int H, int npad, int smax, bool w4, int G, int nsg) {
-    const int base = smem_layout(T, H, npad, smax, w4, G, nsg, 0).total;
+static int fit_chunk(int T, int H, int npad, int smax, bool w4, int G, int nsg, bool zp) {
+    const int base = smem_layout(T, H, npad, smax, w4, G, nsg, 0, zp).total;
     int chunk = ((kSmemLimit - base) / (G * nsg) - meta_bytes_for(T)) / 1024 * 1024;
     return chunk > 4 * kChunk ? 4 * kChunk : chunk;
 }
-static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes, int &chunk) {
+static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes, int &chunk,
+                            bool zp = false) {
     G = 2;
     nsg = 2;
-    chunk = fit_chunk(T, H, npad, smax, w4, G, nsg);
+    chunk = fit_chunk(T, H, npad, smax, w4, G, nsg, zp);
     if (chunk < kGroupSplitMin) {
-        const int c1 = fit_chunk(T, H, npad, smax, w4, 1, 2);
+        const int c1 = fit_chunk(T, H, npad, smax, w4, 1, 2, zp);
         if (c1 >= kChunk && c1 > chunk) {
             G = 1;
             chunk = c1;
         }
     }
     if (chunk >= kChunk) {
-        bytes = smem_layout(T, H, npad, smax, w4, G, nsg, chunk).total;
+        bytes = smem_layout(T, H, npad, smax, w4, G, nsg, chunk, zp).total;
         return bytes <= kSmemLimit;
     }
     G = 1;
     chunk = kChunk;
     for (nsg = 12; nsg >= 2; --nsg) {
-        const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk);
+        const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk, zp);
         if (L.total <= kSmemLimit) {
             bytes = L.total;
             return true;
@@ -1007,10 +1114,11 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     EngineParams p = p0;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    const bool w4 = RFMT == FMT_W4 && p.routed_enabled;
+    const bool w4 = (RFMT == FMT_W4 || RFMT == FMT_W4Z) && p.routed_enabled;
     const int smax = engine_smax(w4, p.S);
     int G, nsg, bytes, chunk;
-    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk)) return SPX_ERR_UNSUPPORTED;
+    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk, RFMT == FMT_W4Z))
+        return SPX_ERR_UNSUPPORTED;
     p.groups = G;
     p.nstages = nsg;
     p.chunk = chunk;
@@ -1031,6 +1139,16 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
 
 int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
     const int nt = engine_nt(p.T);
+    if (p.routed_enabled && p.routed_fmt == FMT_W4 && p.w4_zeros) {
+        if (p.S == 32) {
+            if (nt == 1) return launch_engine_t<FMT_W4Z, 2, 1>(p, s, pdl);
+            if (nt == 3) return launch_engine_t<FMT_W4Z, 2, 3>(p, s, pdl);
+            return SPX_ERR_UNSUPPORTED;
+        }
+        if (nt == 1) return launch_engine_t<FMT_W4Z, 1, 1>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<FMT_W4Z, 1, 3>(p, s, pdl);
+        return launch_engine_t<FMT_W4Z, 1, 8>(p, s, pdl);
+    }
     if (p.routed_enabled && p.routed_fmt == FMT_W4) {
         if (p.S == 32) {
             if (nt == 1) return launch_engine_t<FMT_W4, 2, 1>(p, s, pdl);
@@ -1053,6 +1171,11 @@ int engine_preload() {
     if (!st) st = configure_engine<FMT_W4, 1, 1>();
     if (!st) st = configure_engine<FMT_W4, 1, 3>();
     if (!st) st = configure_engine<FMT_W4, 1, 8>();
+    if (!st) st = configure_engine<FMT_W4Z, 2, 1>();
+    if (!st) st = configure_engine<FMT_W4Z, 2, 3>();
+    if (!st) st = configure_engine<FMT_W4Z, 1, 1>();
+    if (!st) st = configure_engine<FMT_W4Z, 1, 3>();
+    if (!st) st = configure_engine<FMT_W4Z, 1, 8>();
     if (!st) st = configure_engine<FMT_F16, 1, 1>();
     if (!st) st = configure_engine<FMT_F16, 1, 3>();
     if (!st) st = configure_engine<FMT_F16, 1, 8>();
@@ -1063,10 +1186,11 @@ int engine_preload() {
 
 int engine_fits(int T, int H, int fmt, int S) {
     const int npad = 8 * ((T + 7) / 8);
-    const bool w4 = fmt == FMT_W4;
+    const bool zp = fmt == FMT_W4Z;
+    const bool w4 = fmt == FMT_W4 || zp;
     if (w4 && S == 32 && engine_nt(T) == 8) return 0;
     int G, nsg, bytes, chunk;
-    return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk) ? 1 : 0;
+    return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk, zp) ? 1 : 0;
 }
 
 }  // namespace spx

@@ -372,6 +372,7 @@ struct RouteParams {
 constexpr int kFmtQ8 = 2;   // EngineParams::routed_fmt of GGUF Q8_0 experts
 constexpr int kFmtQ2K = 3;  // ... of GGUF Q2_K gate/up with Q8_0 down
 constexpr int kFmtQ4K = 4;  // ... of GGUF Q4_K gate/up with Q8_0 down
+constexpr int kFmtW4Z = 5;  // expert-launch instance of INT4 with zero points (routed_fmt stays 0)
 struct EngineParams {
     // routed experts (packed units)
     const uint8_t *routed;
