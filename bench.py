@@ -50,10 +50,10 @@ KERNEL_SOURCES = {
     "verify": ["spx_engine.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_096_064 + 3_027_712,
-               "algorithmic_bytes": 674_897_920, "source_sha": "318d6c7accafd9eb"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_648 + 797_696, "algorithmic_bytes": 61_374_720,
-              "source_sha": "d331d7992ba30449"},
+    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_101_952 + 3_017_728,
+               "algorithmic_bytes": 674_897_920, "source_sha": "6a7fe007f80e4ae0"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_508_608 + 731_392, "algorithmic_bytes": 61_374_720,
+              "source_sha": "918b14f8bfe660e9"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
