@@ -189,8 +189,8 @@ extern "C" int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_exper
                                  16);
     if (st) return st;
     if (!al16(w->packed) || !al16(y_sorted) || gguf_fmt(w) < 0) return SPX_ERR_INVALID_ARG;
-    if (!draft_supported(T, w->H, w->I, 16, 0, w->E, k, gguf_fmt(w) == kFmtQ2K || gguf_fmt(w) == kFmtQ4K))
-        return SPX_ERR_UNSUPPORTED;  // the draft launch only
+    const bool draft = draft_supported(T, w->H, w->I, 16, 0, w->E, k, gguf_fmt(w) == kFmtQ2K || gguf_fmt(w) == kFmtQ4K);
+    if (!draft && !engine_fits(T, w->H, gguf_fmt(w), 16)) return SPX_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EngineParams p = base_params(x, T, w->H, ws);
     p.routed = static_cast<const uint8_t *>(w->packed);
@@ -208,7 +208,8 @@ extern "C" int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_exper
     if (cudaMemsetAsync(y_sorted, 0, sizeof(float) * (size_t)T * k * w->H, s) != cudaSuccess) return SPX_ERR_CUDA;
     st = launch_tables(offsets, sorted_slots, active, n_active, T, k, w->E, ws_tables(ws, T, w->H), s);
     if (st) return st;
-    return launch_draft(p, nullptr, ws_scratch_base(T, w->H), false, s);
+    if (draft) return launch_draft(p, nullptr, ws_scratch_base(T, w->H), false, s);
+    return launch_engine(p, s, false);
 }
 
 extern "C" int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_experts *w, int k, const int32_t *offsets,
@@ -332,7 +333,7 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
     const bool zeros = a->mode == 0 && !gguf && a->w4->zeros;
     const bool kq = gguf && (gguf_fmt(a->gguf) == kFmtQ2K || gguf_fmt(a->gguf) == kFmtQ4K);
     const bool via_draft = !cache_aware && draft_supported(T, H, I, S, I_s, E, k, kq);
-    if (gguf && !via_draft) return SPX_ERR_UNSUPPORTED;  // GGUF experts: the draft launch only
+    if (gguf && !via_draft && !engine_fits(T, H, gguf_fmt(a->gguf), 16)) return SPX_ERR_UNSUPPORTED;
     if (zeros && !via_draft && !engine_fits(T, H, kFmtW4Z, S)) return SPX_ERR_UNSUPPORTED;
     // every check has passed: only now may the caller's scratch be cleared
     if (clear) {
@@ -415,10 +416,10 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
 
     EngineParams p = base_params(a->x, T, H, a->ws);
     p.routed = routed;
-    p.routed_fmt = a->mode == 0 ? 0 : 1;
+    p.routed_fmt = gguf ? gguf_fmt(a->gguf) : a->mode == 0 ? 0 : 1;
     p.w4_zeros = zeros ? static_cast<const uint8_t *>(a->w4->zeros) : nullptr;
     p.S = S;
-    if (a->mode == 0) p.w4_sdown = reinterpret_cast<const __half *>(routed + w4_units_bytes(E, H, I, S));
+    if (a->mode == 0 && !gguf) p.w4_sdown = reinterpret_cast<const __half *>(routed + w4_units_bytes(E, H, I, S));
     p.E = E;
     p.I = I;
     p.k = k;

@@ -136,6 +136,7 @@ struct Stream {
     uint32_t it;
     bool done;
     const uint8_t *base;
+    const uint8_t *dbase;  // GGUF: the unit's down codes (unit order)
 };
 
 // G (groups) is a template parameter so that the per-group stream state
@@ -249,6 +250,13 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
     // per group, as the scales) after their codes
     const bool zp = p.w4_zeros != nullptr && !rf16;
     const int W4GPC = chunk / ((int)w4_group_bytes(p.S) + (zp ? 4 * p.S : 0));  // whole INT4 groups per chunk
+    // GGUF routed experts (S = 16): gate/up in groups of 128 rows (Q8_0) or
+    // super-blocks of 256 (Q2_K, Q4_K), down as 512 B pair blocks in unit order
+    const bool gg = p.routed_fmt == kFmtQ8 || p.routed_fmt == kFmtQ2K || p.routed_fmt == kFmtQ4K;
+    const int gg_gb = p.routed_fmt == kFmtQ8 ? kQ8GroupBytes : p.routed_fmt == kFmtQ2K ? kQ2kSbBytes : kQ4kSbBytes;
+    const int gg_ngr = p.routed_fmt == kFmtQ8 ? H / 128 : H / 256;
+    const size_t gg_ub = (size_t)gg_ngr * gg_gb;
+    const int GGPC = chunk / gg_gb;  // whole GGUF groups per chunk
     long long t_prog = clock64();
     const long long budget = (long long)p.wait_budget_ns * 2;  // cycles at ~2 GHz
     bool aborted = false;
@@ -297,8 +305,13 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
                     int a, i;
                     routed_slot(u - n_sh, a, i, S_.nsub);
                     S_.i0 = i * p.S;
-                    const size_t ub = S_.fmt == FMT_W4 ? w4_unit_bytes(H, p.S) : f16_unit_bytes(H);
-                    S_.base = p.routed + ((size_t)e * nu_r + i) * ub;
+                    const size_t uix = (size_t)e * nu_r + i;
+                    if (gg) {
+                        S_.base = p.routed + uix * gg_ub;
+                        S_.dbase = p.routed + gguf_udn_offset(p.E, H, p.I, p.routed_fmt) + uix * ((size_t)H * 16);
+                    } else {
+                        S_.base = p.routed + uix * (S_.fmt == FMT_W4 ? w4_unit_bytes(H, p.S) : f16_unit_bytes(H));
+                    }
                 }
             }
             const bool shared = S_.u < n_sh;
@@ -309,7 +322,27 @@ __device__ void producer_loop(const EngineParams &p, uint8_t *smem, const SmemLa
             h.flags = 0;
             const uint8_t *src2 = nullptr;  // second slice of an FP16 pair's down chunk, or INT4 zero points
             uint32_t bytes2 = 0;
-            if (S_.fmt == FMT_W4) {
+            if (gg && !shared) {
+                if (S_.phase == 0) {
+                    h.kind = HK_GU;
+                    h.b0 = S_.b;
+                    h.nb = min(GGPC, gg_ngr - S_.b);
+                    h.flags = (S_.b == 0 ? HF_UNIT_START : 0) | (S_.b + h.nb == gg_ngr ? HF_GU_LAST | HF_GU_FINAL : 0);
+                    src = S_.base + (size_t)S_.b * gg_gb;
+                    bytes = h.nb * (uint32_t)gg_gb;
+                    S_.b += h.nb;
+                    if (S_.b >= gg_ngr) S_.phase = 1, S_.b = 0;
+                } else {
+                    const int nbd = H / 32;
+                    h.kind = HK_DOWN;
+                    h.b0 = S_.b;
+                    h.nb = min(chunk / 512, nbd - S_.b);
+                    src = S_.dbase + (size_t)S_.b * 512;
+                    bytes = h.nb * 512;
+                    S_.b += h.nb;
+                    if (S_.b >= nbd) S_.u = -1;
+                }
+            } else if (S_.fmt == FMT_W4) {
                 const int S = p.S;
                 const int ngr = H / 128;
                 const int nbd = (int)(w4_dn_bytes(H, S) / 512);
@@ -450,11 +483,12 @@ template <int RFMT, int MS4, int NT>
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams p) {
     constexpr bool ZP = RFMT == FMT_W4Z;
     constexpr bool W4R = RFMT == FMT_W4 || ZP;  // INT4 routed experts
+    constexpr bool GG = RFMT == kFmtQ8;         // GGUF Q8_0 routed experts (S = 16)
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
     griddep_launch_dependents();
-    const bool has_w4 = W4R && p.routed_enabled;
+    const bool has_w4 = (W4R || GG) && p.routed_enabled;  // per-unit down-scale rows
     const int smax = engine_smax(has_w4, p.S);
     const int G = p.groups, nsg = p.nstages;
     const int gwarps = kConsumerWarps / G;
@@ -575,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         const uint8_t *stage = ring + (size_t)st * (p.chunk + meta_bytes_for(p.T));
         if (h.flags & HF_UNIT_START) {
             // unit setup from the header and the token table in the meta area
-            u_fmt = (h.shared || RFMT == FMT_F16) ? FMT_F16 : FMT_W4;
+            u_fmt = (h.shared || RFMT == FMT_F16) ? FMT_F16 : GG ? RFMT : FMT_W4;
             u_S = u_fmt == FMT_F16 ? kF16S * ((h.flags & HF_PAIR) ? 2 : 1) : p.S;
             u_e = h.e;
             u_i0 = h.i0;
@@ -623,11 +657,16 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int r = 0; r < 4; ++r) run[t][nt][r] = 0.f;
-            if (W4R && u_fmt == FMT_W4) {
+            if ((W4R && u_fmt == FMT_W4) || (GG && u_fmt == RFMT)) {
                 // fetch this unit's down-scale row into the group's buffer for
                 // this unit's parity; waited for at the gate/up -> down boundary
+                // (INT4: per group of 128 intermediate rows; GGUF Q8_0: per
+                // block of 32)
                 __half *dst = sdg + (size_t)(ucount & 1) * H;
-                const __half *srow = p.w4_sdown + ((size_t)u_e * (p.I / 128) + u_i0 / 128) * H;
+                const __half *srow =
+                    GG ? reinterpret_cast<const __half *>(p.routed + gguf_uds_offset(p.E, H, p.I, RFMT)) +
+                             ((size_t)u_e * (p.I / 32) + u_i0 / 32) * H
+                       : p.w4_sdown + ((size_t)u_e * (p.I / 128) + u_i0 / 128) * H;
                 for (int idx = gtid; idx < H / 8; idx += gwarps * 32) cp_async16(dst + idx * 8, srow + idx * 8);
                 if (ZP) {
                     // and its down zero-point row: [E][H/32][I/128][32], 32 outputs a piece
@@ -734,6 +773,65 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                     }
                 }
                 if (grp >= 0) flush();
+            } else if (GG && u_fmt == RFMT) {
+                // GGUF Q8_0: a group = 4 blocks of 32 rows (2 k-steps each, one
+                // scale per column); codes become exact fp16 values, a block's
+                // two k-steps are summed in fp32, then scaled
+                const int nks = h.nb * 8;
+                const int per = (nks + gwarps - 1) / gwarps;
+                const int kb = gw * per, ke = min(kb + per, nks);
+                float acc[2][NT][4];
+                float sA[2] = {0.f, 0.f}, sB[2] = {0.f, 0.f};
+                int blk = -1;  // current 32-row block (group * 4 + block)
+                auto flush = [&]() {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            run[t][nt][0] = fmaf(sA[t], acc[t][nt][0], run[t][nt][0]);
+                            run[t][nt][1] = fmaf(sA[t], acc[t][nt][1], run[t][nt][1]);
+                            run[t][nt][2] = fmaf(sB[t], acc[t][nt][2], run[t][nt][2]);
+                            run[t][nt][3] = fmaf(sB[t], acc[t][nt][3], run[t][nt][3]);
+                        }
+                };
+                for (int kk = kb; kk < ke; ++kk) {
+                    const int gr = kk >> 3, kl = kk & 7;
+                    const uint8_t *gp = stage + (size_t)gr * kQ8GroupBytes;
+                    if (gr * 4 + (kl >> 1) != blk) {
+                        if (blk >= 0) flush();
+                        blk = gr * 4 + (kl >> 1);
+                        const __half *scp = reinterpret_cast<const __half *>(gp) + (kl >> 1) * 32;
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            sA[t] = __half2float(scp[t * 16 + g]);
+                            sB[t] = __half2float(scp[t * 16 + g + 8]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) acc[t][nt][r] = 0.f;
+                        }
+                    }
+                    const uint4 v = lds128(gp + kQ8ScaleBytes + kl * 512 + lane * 16);
+                    const int ks = (h.b0 + gr) * 8 + kl;  // k-step within H
+                    uint32_t bf0[NT], bf1[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const bool okx = xoff[nt] >= 0;
+                        const __half *xr = xs + (okx ? xoff[nt] : 0) + 16 * ks;
+                        bf0[nt] = okx ? lds32(xr) : 0u;
+                        bf1[nt] = okx ? lds32(xr + 8) : 0u;
+                    }
+                    uint32_t a0[4], a1[4];
+                    q8_frag(v.x, v.y, a0);
+                    q8_frag(v.z, v.w, a1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        if (nt < nact) {
+                            mma_16816(acc[0][nt], a0, bf0[nt], bf1[nt]);
+                            mma_16816(acc[1][nt], a1, bf0[nt], bf1[nt]);
+                        }
+                }
+                if (blk >= 0) flush();
             } else {
                 const int nb = h.nb;
                 const int per = (nb + gwarps - 1) / gwarps;
@@ -763,7 +861,40 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             const int per = (nb + gwarps - 1) / gwarps;
             const int bb = gw * per, be = min(bb + per, nb);
             for (int b = bb; b < be; ++b) {
-                if (W4R && u_fmt == FMT_W4) {
+                if (GG && u_fmt == RFMT) {
+                    // GGUF Q8_0 down: block = one m-tile pair (one k-step of the
+                    // unit's 16 rows), the lane's 8 codes of each tile; one scale
+                    // per output for the unit's 32-row block
+                    const uint4 v = lds128(stage + (size_t)b * 512 + lane * 16);
+                    uint32_t a0[4], a1[4];
+                    q8_frag(v.x, v.y, a0);
+                    q8_frag(v.z, v.w, a1);
+                    const int n0 = 32 * (h.b0 + b) + 4 * g;
+                    const uint2 sv = *reinterpret_cast<const uint2 *>(sdcur + n0);
+                    const float2 s01 = __half22float2(u32_as_h2(sv.x));
+                    const float2 s23 = __half22float2(u32_as_h2(sv.y));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (nt < nact) {
+                            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                            mma_16816(acc[0], a0, hb0[0][nt], hb1[0][nt]);
+                            mma_16816(acc[1], a1, hb0[0][nt], hb1[0][nt]);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const int col = nt * 8 + 2 * q4 + hf;
+                                if (col < n_e) {
+                                    const float w = oscl[nt][hf];
+                                    float4 o;
+                                    o.x = acc[0][hf] * s01.x * w;
+                                    o.y = acc[0][2 + hf] * s01.y * w;
+                                    o.z = acc[1][hf] * s23.x * w;
+                                    o.w = acc[1][2 + hf] * s23.y * w;
+                                    atomicAdd(reinterpret_cast<float4 *>(p.yout + (size_t)orow[nt][hf] * H + n0), o);
+                                }
+                            }
+                        }
+                    }
+                } else if (W4R && u_fmt == FMT_W4) {
                     // block = 4/MS4 m-tiles (2/MS4 pairs), lane words [tile][ks]
                     constexpr int NPAIR = 2 / MS4;
                     const uint4 v = lds128(stage + (size_t)b * 512 + lane * 16);
@@ -899,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
             // SiLU, h -> fp16 fragments; the buffer is left zeroed for the
             // group's next unit
             const int S = u_S;
-            if (W4R) cp_async_wait_all();  // this thread's share of the down-scale (and zero-point) row
+            if (W4R || GG) cp_async_wait_all();  // this thread's share of the down-scale (and zero-point) row
             group_sync(p, gs, abort_flag);
             // only the unit's n_e token columns hold sums (the others stay
             // zero); h columns past n_e feed output columns that are never
@@ -1114,7 +1245,7 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     EngineParams p = p0;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    const bool w4 = (RFMT == FMT_W4 || RFMT == FMT_W4Z) && p.routed_enabled;
+    const bool w4 = (RFMT == FMT_W4 || RFMT == FMT_W4Z || RFMT == kFmtQ8) && p.routed_enabled;
     const int smax = engine_smax(w4, p.S);
     int G, nsg, bytes, chunk;
     if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk, RFMT == FMT_W4Z))
@@ -1139,6 +1270,12 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
 
 int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
     const int nt = engine_nt(p.T);
+    if (p.routed_enabled && p.routed_fmt == kFmtQ8) {
+        if (nt == 1) return launch_engine_t<kFmtQ8, 1, 1>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<kFmtQ8, 1, 3>(p, s, pdl);
+        return launch_engine_t<kFmtQ8, 1, 8>(p, s, pdl);
+    }
+    if (p.routed_enabled && (p.routed_fmt == kFmtQ2K || p.routed_fmt == kFmtQ4K)) return SPX_ERR_UNSUPPORTED;
     if (p.routed_enabled && p.routed_fmt == FMT_W4 && p.w4_zeros) {
         if (p.S == 32) {
             if (nt == 1) return launch_engine_t<FMT_W4Z, 2, 1>(p, s, pdl);
@@ -1176,6 +1313,9 @@ int engine_preload() {
     if (!st) st = configure_engine<FMT_W4Z, 1, 1>();
     if (!st) st = configure_engine<FMT_W4Z, 1, 3>();
     if (!st) st = configure_engine<FMT_W4Z, 1, 8>();
+    if (!st) st = configure_engine<kFmtQ8, 1, 1>();
+    if (!st) st = configure_engine<kFmtQ8, 1, 3>();
+    if (!st) st = configure_engine<kFmtQ8, 1, 8>();
     if (!st) st = configure_engine<FMT_F16, 1, 1>();
     if (!st) st = configure_engine<FMT_F16, 1, 3>();
     if (!st) st = configure_engine<FMT_F16, 1, 8>();
@@ -1187,7 +1327,8 @@ int engine_preload() {
 int engine_fits(int T, int H, int fmt, int S) {
     const int npad = 8 * ((T + 7) / 8);
     const bool zp = fmt == FMT_W4Z;
-    const bool w4 = fmt == FMT_W4 || zp;
+    const bool w4 = fmt == FMT_W4 || zp || fmt == kFmtQ8;  // per-unit down-scale rows
+    if (fmt == kFmtQ2K || fmt == kFmtQ4K) return 0;
     if (w4 && S == 32 && engine_nt(T) == 8) return 0;
     int G, nsg, bytes, chunk;
     return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk, zp) ? 1 : 0;

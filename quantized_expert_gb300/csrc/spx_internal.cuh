@@ -80,6 +80,10 @@ __host__ __device__ inline size_t w4_zeros_gu_bytes(int E, int H, int I, int S) 
 __host__ __device__ inline size_t w4_zeros_dn_bytes(int E, int H, int I) {
     return (size_t)E * (H / 32) * (I / 128) * 32 * 2;
 }
+constexpr int kFmtQ8 = 2;   // EngineParams::routed_fmt of GGUF Q8_0 experts
+constexpr int kFmtQ2K = 3;  // ... of GGUF Q2_K gate/up with Q8_0 down
+constexpr int kFmtQ4K = 4;  // ... of GGUF Q4_K gate/up with Q8_0 down
+constexpr int kFmtW4Z = 5;  // expert-launch instance of INT4 with zero points (routed_fmt stays 0)
 // GGUF Q8_0 experts (draft launch only; S = 16).  A group of 128 rows is four
 // Q8_0 blocks of 32 rows: 4 x 32 fp16 scales ([block][tile-row order], as the
 // INT4 scales) followed by the group's 8 k-steps of codes, 512 B each (32
@@ -131,6 +135,23 @@ static_assert(kQ4kSbBytes == 4736, "Q4_K super-block of a slice: 4.625 bits per 
 __host__ __device__ inline size_t q4k_unit_bytes(int H) { return (size_t)(H / 256) * kQ4kSbBytes; }
 __host__ __device__ inline size_t q4k_units_bytes(int E, int H, int I) {
     return (size_t)E * (I / 16) * q4k_unit_bytes(H);
+}
+// GGUF experts for the expert launch (draft calls above 8 tokens and
+// cache-aware ones): after the draft launch's layout, the Q8_0 down codes
+// again in unit order [E][I/16], a unit = H/32 blocks of 512 B, one per m-tile
+// pair P (32 lanes x 16 B: tile 0's 8 codes, then tile 1's, A[m][kc] = code of
+// W_down[down_col(2P+q, m)][16 j + kc]), then the down scales [E][I/32][H] fp16.
+__host__ __device__ inline size_t gguf_gu_units_bytes(int E, int H, int I, int fmt) {
+    return fmt == kFmtQ8 ? q8_units_bytes(E, H, I) : fmt == kFmtQ2K ? q2k_units_bytes(E, H, I) : q4k_units_bytes(E, H, I);
+}
+__host__ __device__ inline size_t gguf_udn_offset(int E, int H, int I, int fmt) {
+    return gguf_gu_units_bytes(E, H, I, fmt) + (q8_packed_bytes(E, H, I) - q8_units_bytes(E, H, I));
+}
+__host__ __device__ inline size_t gguf_uds_offset(int E, int H, int I, int fmt) {
+    return gguf_udn_offset(E, H, I, fmt) + (size_t)E * (I / 16) * H * 16;
+}
+__host__ __device__ inline size_t gguf_packed_total(int E, int H, int I, int fmt) {
+    return gguf_uds_offset(E, H, I, fmt) + (size_t)E * (I / 32) * H * 2;
 }
 __host__ __device__ inline size_t w4_colblk_offset(int E, int H, int I, int S) {
     return w4_units_bytes(E, H, I, S) + (size_t)E * (I / 128) * H * 2;
@@ -369,10 +390,6 @@ struct RouteParams {
     WsHeader *hdr;
 };
 
-constexpr int kFmtQ8 = 2;   // EngineParams::routed_fmt of GGUF Q8_0 experts
-constexpr int kFmtQ2K = 3;  // ... of GGUF Q2_K gate/up with Q8_0 down
-constexpr int kFmtQ4K = 4;  // ... of GGUF Q4_K gate/up with Q8_0 down
-constexpr int kFmtW4Z = 5;  // expert-launch instance of INT4 with zero points (routed_fmt stays 0)
 struct EngineParams {
     // routed experts (packed units)
     const uint8_t *routed;

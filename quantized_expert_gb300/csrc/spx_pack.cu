@@ -534,12 +534,45 @@ extern "C" int spx_w4_repack(const int32_t *qw_gate, const uint16_t *s_gate, con
     return record_launch(cudaGetLastError());
 }
 
+// Q8_0 down once more in unit order for the expert launch: one thread per
+// (unit, pair, lane, tile) writes the lane's 8 codes of that tile; then one
+// thread per (expert, block of 32 intermediate rows, output) writes a scale.
+__global__ void q8_pack_udn(const uint8_t *wd, int E, int H, int I, uint8_t *codes, uint16_t *scales) {
+    const int spe = I / 16, NP = H / 32;
+    const size_t total = (size_t)E * spe * NP * 32 * 2;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+        const int q = (int)(idx & 1);
+        const int lane = (int)((idx >> 1) & 31);
+        const size_t up = idx >> 6;  // unit * NP + pair
+        const int P = (int)(up % NP);
+        const size_t unit = up / NP;
+        const size_t e = unit / spe;
+        const int j = (int)(unit % spe);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb) {
+            const int r = jb >> 1;
+            const int n = down_col(2 * P + q, frag_row(lane, r));
+            const int k = j * 16 + frag_col(lane, r, jb & 1);
+            w[jb >> 2] |= (uint32_t)q8_code(wd, I, e, H, n, k) << (8 * (jb & 3));
+        }
+        *reinterpret_cast<uint2 *>(codes + unit * ((size_t)H * 16) + (size_t)P * 512 + lane * 16 + q * 8) =
+            make_uint2(w[0], w[1]);
+    }
+    const size_t ns = (size_t)E * (I / 32) * H;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < ns; idx += (size_t)gridDim.x * blockDim.x) {
+        const int n = (int)(idx % H);
+        const int b = (int)((idx / H) % (I / 32));
+        const size_t e = idx / ((size_t)H * (I / 32));
+        scales[idx] = q8_scale(wd, I, e, H, n, b);
+    }
+}
+
 extern "C" size_t spx_gguf_packed_bytes(int E, int H, int I, int gate_up_type) {
     if (E < 1 || H < 128 || I < 128 || H % 128 || I % 128) return 0;
-    if (gate_up_type == SPX_GGUF_Q8_0) return q8_packed_bytes(E, H, I);
-    const size_t down = q8_packed_bytes(E, H, I) - q8_units_bytes(E, H, I);
-    if (gate_up_type == SPX_GGUF_Q2_K && H % 256 == 0) return q2k_units_bytes(E, H, I) + down;
-    if (gate_up_type == SPX_GGUF_Q4_K && H % 256 == 0) return q4k_units_bytes(E, H, I) + down;
+    if (gate_up_type == SPX_GGUF_Q8_0) return gguf_packed_total(E, H, I, kFmtQ8);
+    if (gate_up_type == SPX_GGUF_Q2_K && H % 256 == 0) return gguf_packed_total(E, H, I, kFmtQ2K);
+    if (gate_up_type == SPX_GGUF_Q4_K && H % 256 == 0) return gguf_packed_total(E, H, I, kFmtQ4K);
     return 0;
 }
 
@@ -566,6 +599,10 @@ extern "C" int spx_gguf_repack(const uint8_t *w_gate, const uint8_t *w_up, const
         units = q4k_units_bytes(E, H, I);
     }
     q8_pack_dn<<<grid_for((size_t)E * (H / 32) * (I / 128) * 512), 256, 0, s>>>(w_down, E, H, I, out + units);
+    const int fmt = gate_up_type == SPX_GGUF_Q8_0 ? kFmtQ8 : gate_up_type == SPX_GGUF_Q2_K ? kFmtQ2K : kFmtQ4K;
+    q8_pack_udn<<<grid_for((size_t)E * (I / 16) * (H / 32) * 64), 256, 0, s>>>(
+        w_down, E, H, I, out + gguf_udn_offset(E, H, I, fmt),
+        reinterpret_cast<uint16_t *>(out + gguf_uds_offset(E, H, I, fmt)));
     return record_launch(cudaGetLastError());
 }
 

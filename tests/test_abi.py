@@ -118,17 +118,22 @@ def test_draft_format_sizes_and_validation(lib):
     # zero points: fp16 per (group of 128 rows, column) of gate, up and down
     assert lib.spx_w4_zeros_bytes(E, H, I, 32) == 2 * (2 * E * (H // 128) * I + E * (I // 128) * H)
     assert lib.spx_w4_zeros_bytes(E, H, I, 24) == 0
-    # GGUF: Q8_0 gate/up/down 34 B per 32 weights; Q2_K gate/up 84 B per 256 weights + Q8_0 down
+    # GGUF: Q8_0 gate/up/down 34 B per 32 weights; Q2_K gate/up 84 B per 256 weights + Q8_0 down;
+    # then, for the expert launch, the down codes once more in unit order (1 B per weight) and
+    # the down scales [E][I/32][H] fp16
     q8 = E * H * I * 34 // 32
-    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q8_0) == 3 * q8  # scales inside the 34-byte blocks
-    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q2_K) == 2 * E * H * I * 84 // 256 + q8
+
+    def udn(h):
+        return E * I * h + E * (I // 32) * h * 2
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q8_0) == 3 * q8 + udn(H)  # scales inside the blocks
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q2_K) == 2 * E * H * I * 84 // 256 + q8 + udn(H)
     # Q4_K as packed: 4736 bytes per super-block of a 16-column slice (the 6-bit
     # scales and mins unpacked to bytes: 148 bytes per 256 weights, 144 in the file)
-    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q4_K) == E * (I // 16) * (H // 256) * 4736 + q8
-    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q4_K) == 2 * E * H * I * 148 // 256 + q8
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q4_K) == E * (I // 16) * (H // 256) * 4736 + q8 + udn(H)
+    assert lib.spx_gguf_packed_bytes(E, H, I, spx.SPX_GGUF_Q4_K) == 2 * E * H * I * 148 // 256 + q8 + udn(H)
     assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q2_K) == 0   # Q2_K rows: multiples of 256
     assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q4_K) == 0
-    assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q8_0) == E * 384 * I * 34 // 32 * 3
+    assert lib.spx_gguf_packed_bytes(E, 384, I, spx.SPX_GGUF_Q8_0) == E * 384 * I * 34 // 32 * 3 + udn(384)
     assert lib.spx_gguf_packed_bytes(E, H, I, 7) == 0
     fake = C.c_void_p(256)
     assert lib.spx_gguf_repack(None, fake, fake, E, H, I, 0, fake, None) == spx.SPX_ERR_INVALID_ARG

@@ -687,11 +687,15 @@ def test_gguf_draft_layer_full_size(name, T, kind):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{kind} {name} T={T} rep {rep}")
 
 
-@pytest.mark.parametrize("kind", ["q8_0", "q2_k", "q4_k"])
-@pytest.mark.parametrize("case", [1, 2, 4])
+GGUF_ENGINE_KINDS = ["q8_0"]  # GGUF formats the expert launch serves (draft calls above 8 tokens, cache-aware)
+
+
+@pytest.mark.parametrize("kind,case", [(kd, c) for kd in ["q8_0", "q2_k", "q4_k"] for c in [1, 2, 4]] +
+                         [(kd, c) for kd in GGUF_ENGINE_KINDS for c in [3, 5, 6, 7, 8]])
 def test_gguf_draft_unit_call(case, kind):
-    """spx_moe_draft_gguf on the small cases of at most 8 tokens with
-    16-column slices: per-slot expert outputs against the oracle."""
+    """spx_moe_draft_gguf on the small cases with 16-column slices: per-slot
+    expert outputs against the oracle (up to 8 tokens on the draft launch,
+    then the expert launch with 1, 3 or 8 token tiles)."""
     spx, gh = _spx(), _gh()
     s, T, S = SMALL_CASES[case]
     x = W.gen_x(s, T, step=110 + case)
@@ -735,15 +739,59 @@ def test_gguf_draft_ragged_ranges(kind):
     assert spx.spx_workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("kind", GGUF_ENGINE_KINDS)
+@pytest.mark.parametrize("T", [9, 17])
+def test_gguf_layer_on_the_expert_launch_full_size(kind, T):
+    """GGUF draft layers above 8 tokens (DeepSeek-V2-Lite shape) take the
+    routing launch and the expert launch: routing bit-exact, output within
+    tolerance of the oracle."""
+    gh = _gh()
+    s = W.CONFIGS["deepseek_v2_lite"]
+    x = W.gen_x(s, T, step=140 + T)
+    logits = W.gen_logits(s, T, step=140 + T)
+    lay = gh.Layer(s, needed=gh.needed_experts(s, [logits], [x]), verify=False, gguf=kind)
+    ref = lay.oracle_layer("draft", x, logits=logits)
+    outs, routing, _ = _run_layer(lay, "draft", x, logits)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{kind} T={T} rep {rep}")
+
+
+@pytest.mark.parametrize("kind", GGUF_ENGINE_KINDS)
+@pytest.mark.parametrize("T", [1, 9])
+def test_cache_aware_draft_with_gguf(kind, T):
+    """A cache-aware draft layer call with GGUF experts (resident experts
+    first, ready flags all set) matches the oracle."""
+    spx, gh = _spx(), _gh()
+    s = _small("deepseek_v2_lite", I=256, E=16, I_s=512)
+    x = W.gen_x(s, T, step=150 + T)
+    logits = W.gen_logits(s, T, step=150 + T)
+    lay = gh.Layer(s, needed=gh.needed_experts(s, [logits], [x]), verify=False, gguf=kind)
+    ref = lay.oracle_layer("draft", x, logits=logits)
+    resident = torch.from_numpy((np.random.default_rng(T).random(s.E) < 0.5).astype(np.uint8)).cuda()
+    ready = torch.ones(s.E, dtype=torch.int32, device="cuda")
+    r = spx.Routing.empty(T, s.E, s.k)
+    out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    args, keep = spx.layer_args(0, gh.dev_f16(x), s.E, s.k, s.renorm, gh.dev(logits), r, out, ws, gguf=lay.gguf,
+                                shared=lay.shared, resident=resident, ready=ready)
+    for rep in range(2):
+        spx.spx_moe_layer(args)
+        torch.cuda.synchronize()
+        assert np.array_equal(r.topk_ids.cpu().numpy(), ref["ids"])
+        gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), f"cache {kind} {T} {rep}")
+    assert spx.spx_workspace_status(ws) == 0
+
+
 def test_gguf_unsupported_and_invalid_calls():
-    """GGUF experts are served by the draft launch (T <= 8) only: a larger
-    batch and the cache-aware path return SPX_ERR_UNSUPPORTED; Q2_K needs H a
-    multiple of 256; INT4 and GGUF experts in one call, or an unknown format,
-    are invalid arguments."""
+    """GGUF formats the expert launch does not serve (the K-quants) take draft
+    calls of T <= 8 only: a larger batch and the cache-aware path return
+    SPX_ERR_UNSUPPORTED; Q2_K needs H a multiple of 256; INT4 and GGUF experts
+    in one call, or an unknown format, are invalid arguments."""
     spx, gh = _spx(), _gh()
     from quantized_expert_gb300.spx import SpxError
     s = _small("deepseek_v2_lite", I=256, E=16)
-    lay = gh.Layer(s, needed=list(range(s.E)), verify=False, gguf="q8_0")
+    lay = gh.Layer(s, needed=list(range(s.E)), verify=False, gguf="q2_k")
     T = 9
     ids, _ = oracle.route_topk(np.random.default_rng(120).standard_normal((T, s.E)), s.k, s.renorm)
     g, r = _routing_dev(ids, s.E)
