@@ -204,8 +204,9 @@ typedef struct {
     /* Per-group zero points (asymmetric INT4, the AWQ form: W = (code - zero)
      * * scale) [P1 Main Findings: drafts quantised by GPTQ, AWQ and GGUF]:
      * spx_w4_zeros_bytes() bytes from spx_w4_zeros_repack(), or NULL for zero
-     * point 8.  Served by draft calls of T <= 8 (the one-launch draft path);
-     * other calls with zero points return SPX_ERR_UNSUPPORTED. */
+     * point 8.  Served by the one-launch draft path (T <= 8) and by the
+     * expert launch (more tokens, cache-aware calls; 32-column slices take at
+     * most 24 tokens there, else SPX_ERR_UNSUPPORTED). */
     const void *zeros;
 } spx_w4_experts;
 
@@ -235,8 +236,9 @@ typedef struct {
  * [E][I][H/256][144]);
  * down is Q8_0 ([E][H][I/32][34]): the down rows of the 1408-wide shapes are
  * not a multiple of 256.  Repacked (spx_gguf_repack) into the draft launch's
- * streaming order, 16 columns per slice.  Served by draft calls of T <= 8
- * (the one-launch draft path); other calls return SPX_ERR_UNSUPPORTED. */
+ * streaming order, 16 columns per slice, followed by the Q8_0 down weights in
+ * the expert launch's unit order.  Served by the one-launch draft path (T <=
+ * 8) and by the expert launch (more tokens, cache-aware calls). */
 enum { SPX_GGUF_Q8_0 = 0, SPX_GGUF_Q2_K = 1, SPX_GGUF_Q4_K = 2 };
 typedef struct {
     const void *packed; /* spx_gguf_packed_bytes() bytes, from spx_gguf_repack() */
@@ -327,8 +329,8 @@ SPX_API int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_experts *
                         const int32_t *active, const int32_t *n_active,
                         float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream);
 
-/* The draft unit call with GGUF experts (T <= 8; else SPX_ERR_UNSUPPORTED);
- * arguments and output as spx_moe_draft_w4a16. */
+/* The draft unit call with GGUF experts (the draft launch up to 8 tokens,
+ * the expert launch above); arguments and output as spx_moe_draft_w4a16. */
 SPX_API int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_experts *w, int k,
                         const int32_t *offsets, const int32_t *sorted_slots,
                         const int32_t *active, const int32_t *n_active,
@@ -393,9 +395,7 @@ typedef struct {
     const uint32_t *ready;
     /* Bound of every device-side wait of the call in ns; 0 = 2 s. */
     uint64_t wait_budget_ns;
-    /* mode 0 with GGUF draft experts instead of INT4 (w4 must then be NULL):
-     * draft calls of T <= 8 without cache-aware options only, else
-     * SPX_ERR_UNSUPPORTED. */
+    /* mode 0 with GGUF draft experts instead of INT4 (w4 must then be NULL). */
     const spx_gguf_experts *gguf;
 } spx_layer_args;
 

@@ -80,9 +80,11 @@ __host__ __device__ inline int engine_smax(bool w4, int S) { return w4 && S > 2 
 // hs : per group, [npad][kHsStride] fp16 intermediate; sd: per group, 2 x [H]
 // fp16 down-scale rows (INT4 only, double-buffered by unit parity); with zero
 // points (zp) zd: the same for the down zero-point rows, and xsum: [T][H/128]
-// fp32 sums of each activation row over each group of 128.
+// fp32 sums of each activation row over each group of 128; with GGUF K-quant
+// gate/up (kqs = 16 for Q2_K, 32 for Q4_K) xsum holds each row's sums over
+// kqs rows as fp16 pairs: [T][H/kqs] hi, then [T][H/kqs] lo.
 __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int smax, bool w4, int G, int nsg,
-                                                  int chunk, bool zp = false) {
+                                                  int chunk, bool zp = false, int kqs = 0) {
     SmemLayout L;
     const int nst = G * nsg;
     int o = 0;
@@ -108,6 +110,7 @@ __host__ __device__ inline SmemLayout smem_layout(int T, int H, int npad, int sm
     if (zp) o += G * 2 * H * 2;
     L.xsum = o;
     if (zp) o += T * (H / 128) * 4;
+    if (kqs) o += T * (H / kqs) * 4;
     o = (o + 15) & ~15;
     L.xs = o;
     L.xs_stride = H + 8;
@@ -483,7 +486,9 @@ template <int RFMT, int MS4, int NT>
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams p) {
     constexpr bool ZP = RFMT == FMT_W4Z;
     constexpr bool W4R = RFMT == FMT_W4 || ZP;  // INT4 routed experts
-    constexpr bool GG = RFMT == kFmtQ8;         // GGUF Q8_0 routed experts (S = 16)
+    constexpr bool Q2K = RFMT == kFmtQ2K, Q4K = RFMT == kFmtQ4K;
+    constexpr bool GG = RFMT == kFmtQ8 || Q2K || Q4K;  // GGUF routed experts (S = 16, Q8_0 down)
+    constexpr int KQS = Q2K ? 16 : Q4K ? 32 : 0;       // K-quant gate/up: rows per x sum
     extern __shared__ __align__(128) uint8_t smem[];
     // A launch that follows on the stream may be scheduled as SMs free up; it
     // reads nothing of this one before its own griddepcontrol.wait.
@@ -492,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     const int smax = engine_smax(has_w4, p.S);
     const int G = p.groups, nsg = p.nstages;
     const int gwarps = kConsumerWarps / G;
-    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg, p.chunk, ZP);
+    const SmemLayout L = smem_layout(p.T, p.H, p.npad, smax, has_w4, G, nsg, p.chunk, ZP, KQS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q4 = lane & 3;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -547,6 +552,23 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
     for (int idx = ctid; idx < G * 2 * smax * rs; idx += kConsumerWarps * 32)
         reinterpret_cast<float *>(smem + L.red)[idx] = 0.f;
     mbar_wait_bounded(xbar, 0, abort_flag, &p.hdr->status, p.wait_budget_ns);
+    if (KQS) {  // each activation row's sums over KQS rows, as fp16 pairs hi + lo
+        __half *xsh = reinterpret_cast<__half *>(smem + L.xsum);
+        const int nsb = p.H / KQS;
+        for (int idx = ctid; idx < p.T * nsb; idx += kConsumerWarps * 32) {
+            const int t = idx / nsb, b = idx - t * nsb;
+            const __half2 *xr2 = reinterpret_cast<const __half2 *>(xs + (size_t)t * L.xs_stride + b * KQS);
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < KQS / 2; ++j) {
+                const float2 f = __half22float2(xr2[j]);
+                sum += f.x + f.y;
+            }
+            const __half hi = __float2half_rn(sum);
+            xsh[idx] = hi;
+            xsh[p.T * nsb + idx] = __float2half_rn(sum - __half2float(hi));
+        }
+    }
     if (ZP) {  // each activation row's sums over the groups of 128
         float *xsw = reinterpret_cast<float *>(smem + L.xsum);
         for (int idx = ctid; idx < p.T * ngr; idx += kConsumerWarps * 32) {
@@ -773,7 +795,185 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
                     }
                 }
                 if (grp >= 0) flush();
-            } else if (GG && u_fmt == RFMT) {
+            } else if ((Q2K || Q4K) && u_fmt == RFMT) {
+                // GGUF Q2_K / Q4_K: whole super-blocks of 256 rows per warp (the
+                // min term is per super-block).  The fragment holds sc*q, exact in
+                // fp16 through one fused multiply-add of the magic value 1024 + q,
+                // so one accumulator spans the super-block; the mins enter through
+                // one more product, of the rows' sub-block mins with the token's
+                // sub-block sums of x (fp16 pairs hi + lo); then d and dmin per row.
+                constexpr int SBB = Q2K ? kQ2kSbBytes : kQ4kSbBytes;
+                const int nsb = h.nb;
+                const int per = (nsb + gwarps - 1) / gwarps;
+                const int s0 = gw * per, s1 = min(s0 + per, nsb);
+                const __half *xsh = reinterpret_cast<const __half *>(smem + L.xsum);
+                const int nxs = H / KQS;  // x sums per activation row
+                int xtk[NT];              // token of this lane's B column in each n-tile, -1 if none
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) xtk[nt] = xoff[nt] >= 0 ? (xoff[nt] - 2 * q4) / xs_stride : -1;
+                const __half2 k1024 = u32_as_h2(0x64006400u), km1024 = u32_as_h2(0xE400E400u);
+                for (int gr = s0; gr < s1; ++gr) {
+                    const uint8_t *sp = stage + (size_t)gr * SBB;
+                    const __half *dd = reinterpret_cast<const __half *>(sp);  // d [32], then dmin [32]
+                    const int sbg = h.b0 + gr;                              // super-block of H
+                    const uint4 c0 = lds128(sp + (Q2K ? kQ2kScaleOff : kQ4kScaleOff) + g * 32);
+                    const uint4 c1 = lds128(sp + (Q2K ? kQ2kScaleOff : kQ4kScaleOff) + g * 32 + 16);
+                    const uint32_t scw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    float am[2][NT][4];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) am[t][nt][r] = 0.f;
+                    if constexpr (Q2K) {
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = lds128(sp + kQ2kCodeOff + c * 512 + lane * 16);
+                            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const int kl = 4 * c + kk;
+                                const int ks = sbg * 16 + kl;
+                                uint32_t bf0[NT], bf1[NT];
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    const bool okx = xoff[nt] >= 0;
+                                    const __half *xr = xs + (okx ? xoff[nt] : 0) + 16 * ks;
+                                    bf0[nt] = okx ? lds32(xr) : 0u;
+                                    bf1[nt] = okx ? lds32(xr + 8) : 0u;
+                                }
+                                // the k-step's four scale nibbles (tile t, row g / g+8), in both halves
+                                const uint32_t su = ((scw[kl >> 1] >> (16 * (kl & 1))) & 0xFFFFu) * 0x10001u;
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    const __half2 sa2 =
+                                        __hsub2(u32_as_h2(lop3_and_or(su >> (8 * t), 0x000F000Fu, 0x64006400u)), k1024);
+                                    const __half2 sb2 = __hsub2(
+                                        u32_as_h2(lop3_and_or(su >> (8 * t + 4), 0x000F000Fu, 0x64006400u)), k1024);
+                                    const __half2 oa2 = __hmul2(sa2, km1024), ob2 = __hmul2(sb2, km1024);
+                                    uint32_t a[4];
+#pragma unroll
+                                    for (int r = 0; r < 4; ++r) {
+                                        const uint32_t raw =
+                                            lop3_and_or(words[kk] >> (2 * (4 * t + r)), 0x00030003u, 0x64006400u);
+                                        a[r] = h2_as_u32(__hfma2(u32_as_h2(raw), (r & 1) ? sb2 : sa2, (r & 1) ? ob2 : oa2));
+                                    }
+#pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt)
+                                        if (nt < nact) mma_16816(am[t][nt], a, bf0[nt], bf1[nt]);
+                                }
+                            }
+                        }
+                    } else {
+                        const uint32_t kExp = 0x64646464u;
+#pragma unroll 1
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 v = lds128(sp + kQ4kCodeOff + c * 512 + lane * 16);
+                            const uint32_t words[4] = {v.x, v.y, v.z, v.w};  // [k-step][tile]
+                            __half2 sc2[2][2], of2[2][2];                     // (scale, -1024 scale) of rows g, g+8
+#pragma unroll
+                            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                                for (int j = 0; j < 2; ++j) {
+                                    const uint32_t sel = (2 * t + j) * 0x0101u + 0x4040u;  // byte 2t+j under 0x64
+                                    sc2[t][j] = __hsub2(u32_as_h2(__byte_perm(scw[c], kExp, sel)), k1024);
+                                    of2[t][j] = __hmul2(sc2[t][j], km1024);
+                                }
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const int ks = sbg * 16 + 2 * c + kk;
+                                uint32_t bf0[NT], bf1[NT];
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    const bool okx = xoff[nt] >= 0;
+                                    const __half *xr = xs + (okx ? xoff[nt] : 0) + 16 * ks;
+                                    bf0[nt] = okx ? lds32(xr) : 0u;
+                                    bf1[nt] = okx ? lds32(xr + 8) : 0u;
+                                }
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    const uint32_t w = words[2 * kk + t];
+                                    uint32_t a[4];
+#pragma unroll
+                                    for (int r = 0; r < 4; ++r) {
+                                        const uint32_t raw = lop3_and_or(w >> (4 * r), 0x000F000Fu, 0x64006400u);
+                                        a[r] = h2_as_u32(__hfma2(u32_as_h2(raw), sc2[t][r & 1], of2[t][r & 1]));
+                                    }
+#pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt)
+                                        if (nt < nact) mma_16816(am[t][nt], a, bf0[nt], bf1[nt]);
+                                }
+                            }
+                        }
+                    }
+                    // d times the code products, then the same accumulators take
+                    // the min products (scaled by dmin and subtracted)
+                    float da[2], db[2], ma[2], mb[2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        da[t] = __half2float(dd[t * 16 + g]);
+                        db[t] = __half2float(dd[t * 16 + g + 8]);
+                        ma[t] = __half2float(dd[32 + t * 16 + g]);
+                        mb[t] = __half2float(dd[32 + t * 16 + g + 8]);
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            run[t][nt][0] = fmaf(da[t], am[t][nt][0], run[t][nt][0]);
+                            run[t][nt][1] = fmaf(da[t], am[t][nt][1], run[t][nt][1]);
+                            run[t][nt][2] = fmaf(db[t], am[t][nt][2], run[t][nt][2]);
+                            run[t][nt][3] = fmaf(db[t], am[t][nt][3], run[t][nt][3]);
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) am[t][nt][r] = 0.f;
+                        }
+                    uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const bool okx = xtk[nt] >= 0;
+                        const __half *xh = xsh + (okx ? xtk[nt] : 0) * nxs + sbg * (256 / KQS) + 2 * q4;
+                        const __half *xl = xh + p.T * nxs;
+                        bh0[nt] = okx ? lds32(xh) : 0u;
+                        bl0[nt] = okx ? lds32(xl) : 0u;
+                        bh1[nt] = okx && Q2K ? lds32(xh + 8) : 0u;  // Q4_K: 8 sub-blocks, k >= 8 zero
+                        bl1[nt] = okx && Q2K ? lds32(xl + 8) : 0u;
+                    }
+                    const uint2 mw = lds64(sp + (Q2K ? kQ2kMinOff : kQ4kMinOff) + lane * 8);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t w = t == 0 ? mw.x : mw.y;
+                        uint32_t a[4];
+                        if constexpr (Q2K) {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+                                a[r] = h2_as_u32(
+                                    __hsub2(u32_as_h2(lop3_and_or(w >> (4 * r), 0x000F000Fu, 0x64006400u)), k1024));
+                        } else {
+                            const uint32_t kExp = 0x64646464u;
+                            a[0] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, kExp, 0x4140u)), k1024));
+                            a[1] = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, kExp, 0x4342u)), k1024));
+                            a[2] = 0u;
+                            a[3] = 0u;
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            if (nt < nact) {
+                                mma_16816(am[t][nt], a, bh0[nt], bh1[nt]);
+                                mma_16816(am[t][nt], a, bl0[nt], bl1[nt]);
+                            }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            run[t][nt][0] = fmaf(-ma[t], am[t][nt][0], run[t][nt][0]);
+                            run[t][nt][1] = fmaf(-ma[t], am[t][nt][1], run[t][nt][1]);
+                            run[t][nt][2] = fmaf(-mb[t], am[t][nt][2], run[t][nt][2]);
+                            run[t][nt][3] = fmaf(-mb[t], am[t][nt][3], run[t][nt][3]);
+                        }
+                }
+            } else if (RFMT == kFmtQ8 && u_fmt == RFMT) {
                 // GGUF Q8_0: a group = 4 blocks of 32 rows (2 k-steps each, one
                 // scale per column); codes become exact fp16 values, a block's
                 // two k-steps are summed in fp32, then scaled
@@ -1191,31 +1391,31 @@ int engine_nt(int T) { return T <= 8 ? 1 : (T <= 24 ? 3 : 8); }
 // 434 us on GB300; DeepSeek-V2-Lite-shaped, 36 KB chunks: two groups).  Below
 // kChunk per chunk even then, one group with as many kChunk stages as fit.
 constexpr int kGroupSplitMin = 28 * 1024;
-static int fit_chunk(int T, int H, int npad, int smax, bool w4, int G, int nsg, bool zp) {
-    const int base = smem_layout(T, H, npad, smax, w4, G, nsg, 0, zp).total;
+static int fit_chunk(int T, int H, int npad, int smax, bool w4, int G, int nsg, bool zp, int kqs) {
+    const int base = smem_layout(T, H, npad, smax, w4, G, nsg, 0, zp, kqs).total;
     int chunk = ((kSmemLimit - base) / (G * nsg) - meta_bytes_for(T)) / 1024 * 1024;
     return chunk > 4 * kChunk ? 4 * kChunk : chunk;
 }
 static bool choose_geometry(int T, int H, int npad, int smax, bool w4, int &G, int &nsg, int &bytes, int &chunk,
-                            bool zp = false) {
+                            bool zp = false, int kqs = 0) {
     G = 2;
     nsg = 2;
-    chunk = fit_chunk(T, H, npad, smax, w4, G, nsg, zp);
+    chunk = fit_chunk(T, H, npad, smax, w4, G, nsg, zp, kqs);
     if (chunk < kGroupSplitMin) {
-        const int c1 = fit_chunk(T, H, npad, smax, w4, 1, 2, zp);
+        const int c1 = fit_chunk(T, H, npad, smax, w4, 1, 2, zp, kqs);
         if (c1 >= kChunk && c1 > chunk) {
             G = 1;
             chunk = c1;
         }
     }
     if (chunk >= kChunk) {
-        bytes = smem_layout(T, H, npad, smax, w4, G, nsg, chunk, zp).total;
+        bytes = smem_layout(T, H, npad, smax, w4, G, nsg, chunk, zp, kqs).total;
         return bytes <= kSmemLimit;
     }
     G = 1;
     chunk = kChunk;
     for (nsg = 12; nsg >= 2; --nsg) {
-        const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk, zp);
+        const SmemLayout L = smem_layout(T, H, npad, smax, w4, G, nsg, chunk, zp, kqs);
         if (L.total <= kSmemLimit) {
             bytes = L.total;
             return true;
@@ -1245,10 +1445,12 @@ static int launch_engine_t(const EngineParams &p0, cudaStream_t s, bool pdl) {
     EngineParams p = p0;
     const int sms = device_sm_count();
     if (sms <= 0) return SPX_ERR_CUDA;
-    const bool w4 = (RFMT == FMT_W4 || RFMT == FMT_W4Z || RFMT == kFmtQ8) && p.routed_enabled;
+    const bool w4 = (RFMT == FMT_W4 || RFMT == FMT_W4Z || RFMT == kFmtQ8 || RFMT == kFmtQ2K || RFMT == kFmtQ4K) &&
+                    p.routed_enabled;
     const int smax = engine_smax(w4, p.S);
+    const int kqs = RFMT == kFmtQ2K ? 16 : RFMT == kFmtQ4K ? 32 : 0;
     int G, nsg, bytes, chunk;
-    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk, RFMT == FMT_W4Z))
+    if (!choose_geometry(p.T, p.H, p.npad, smax, w4, G, nsg, bytes, chunk, RFMT == FMT_W4Z, kqs))
         return SPX_ERR_UNSUPPORTED;
     p.groups = G;
     p.nstages = nsg;
@@ -1275,7 +1477,16 @@ int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
         if (nt == 3) return launch_engine_t<kFmtQ8, 1, 3>(p, s, pdl);
         return launch_engine_t<kFmtQ8, 1, 8>(p, s, pdl);
     }
-    if (p.routed_enabled && (p.routed_fmt == kFmtQ2K || p.routed_fmt == kFmtQ4K)) return SPX_ERR_UNSUPPORTED;
+    if (p.routed_enabled && p.routed_fmt == kFmtQ2K) {
+        if (nt == 1) return launch_engine_t<kFmtQ2K, 1, 1>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<kFmtQ2K, 1, 3>(p, s, pdl);
+        return launch_engine_t<kFmtQ2K, 1, 8>(p, s, pdl);
+    }
+    if (p.routed_enabled && p.routed_fmt == kFmtQ4K) {
+        if (nt == 1) return launch_engine_t<kFmtQ4K, 1, 1>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<kFmtQ4K, 1, 3>(p, s, pdl);
+        return launch_engine_t<kFmtQ4K, 1, 8>(p, s, pdl);
+    }
     if (p.routed_enabled && p.routed_fmt == FMT_W4 && p.w4_zeros) {
         if (p.S == 32) {
             if (nt == 1) return launch_engine_t<FMT_W4Z, 2, 1>(p, s, pdl);
@@ -1316,6 +1527,12 @@ int engine_preload() {
     if (!st) st = configure_engine<kFmtQ8, 1, 1>();
     if (!st) st = configure_engine<kFmtQ8, 1, 3>();
     if (!st) st = configure_engine<kFmtQ8, 1, 8>();
+    if (!st) st = configure_engine<kFmtQ2K, 1, 1>();
+    if (!st) st = configure_engine<kFmtQ2K, 1, 3>();
+    if (!st) st = configure_engine<kFmtQ2K, 1, 8>();
+    if (!st) st = configure_engine<kFmtQ4K, 1, 1>();
+    if (!st) st = configure_engine<kFmtQ4K, 1, 3>();
+    if (!st) st = configure_engine<kFmtQ4K, 1, 8>();
     if (!st) st = configure_engine<FMT_F16, 1, 1>();
     if (!st) st = configure_engine<FMT_F16, 1, 3>();
     if (!st) st = configure_engine<FMT_F16, 1, 8>();
@@ -1327,11 +1544,12 @@ int engine_preload() {
 int engine_fits(int T, int H, int fmt, int S) {
     const int npad = 8 * ((T + 7) / 8);
     const bool zp = fmt == FMT_W4Z;
-    const bool w4 = fmt == FMT_W4 || zp || fmt == kFmtQ8;  // per-unit down-scale rows
-    if (fmt == kFmtQ2K || fmt == kFmtQ4K) return 0;
+    const bool w4 = fmt == FMT_W4 || zp || fmt == kFmtQ8 || fmt == kFmtQ2K || fmt == kFmtQ4K;  // down-scale rows
+    const int kqs = fmt == kFmtQ2K ? 16 : fmt == kFmtQ4K ? 32 : 0;
+    if (kqs && H % 256) return 0;
     if (w4 && S == 32 && engine_nt(T) == 8) return 0;
     int G, nsg, bytes, chunk;
-    return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk, zp) ? 1 : 0;
+    return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk, zp, kqs) ? 1 : 0;
 }
 
 }  // namespace spx

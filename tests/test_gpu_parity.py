@@ -687,7 +687,7 @@ def test_gguf_draft_layer_full_size(name, T, kind):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{kind} {name} T={T} rep {rep}")
 
 
-GGUF_ENGINE_KINDS = ["q8_0"]  # GGUF formats the expert launch serves (draft calls above 8 tokens, cache-aware)
+GGUF_ENGINE_KINDS = ["q8_0", "q2_k", "q4_k"]  # served by the expert launch too (above 8 tokens, cache-aware)
 
 
 @pytest.mark.parametrize("kind,case", [(kd, c) for kd in ["q8_0", "q2_k", "q4_k"] for c in [1, 2, 4]] +
@@ -783,35 +783,19 @@ def test_cache_aware_draft_with_gguf(kind, T):
     assert spx.spx_workspace_status(ws) == 0
 
 
-def test_gguf_unsupported_and_invalid_calls():
-    """GGUF formats the expert launch does not serve (the K-quants) take draft
-    calls of T <= 8 only: a larger batch and the cache-aware path return
-    SPX_ERR_UNSUPPORTED; Q2_K needs H a multiple of 256; INT4 and GGUF experts
-    in one call, or an unknown format, are invalid arguments."""
+def test_gguf_invalid_calls():
+    """INT4 and GGUF experts in one call, or an unknown GGUF format, are
+    invalid arguments; Q2_K and Q4_K need H a multiple of 256."""
     spx, gh = _spx(), _gh()
     from quantized_expert_gb300.spx import SpxError
     s = _small("deepseek_v2_lite", I=256, E=16)
     lay = gh.Layer(s, needed=list(range(s.E)), verify=False, gguf="q2_k")
-    T = 9
-    ids, _ = oracle.route_topk(np.random.default_rng(120).standard_normal((T, s.E)), s.k, s.renorm)
-    g, r = _routing_dev(ids, s.E)
-    y = torch.empty(T * s.k, s.H, device="cuda")
-    with pytest.raises(SpxError) as ei:
-        spx.spx_moe_draft_gguf(gh.dev_f16(W.gen_x(s, T)), lay.gguf, s.k, r["offsets"], r["sorted_slots"],
-                               r["active"], r["n_active"], y, spx.new_workspace(T, s.H, s.I, s.E, s.k))
-    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
     T = 1
     routing = spx.Routing.empty(T, s.E, s.k)
     out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
     ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
     lg = gh.dev(np.random.default_rng(121).standard_normal((T, s.E)).astype(np.float32))
     x = gh.dev_f16(W.gen_x(s, T))
-    resident = torch.ones(s.E, dtype=torch.uint8, device="cuda")
-    args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, gguf=lay.gguf, shared=lay.shared,
-                                resident=resident)
-    with pytest.raises(SpxError) as ei:
-        spx.spx_moe_layer(args, None)
-    assert ei.value.status == spx.SPX_ERR_UNSUPPORTED
     w4 = gh.Layer(s, needed=[0], verify=False, slice_cols=16).w4
     args, keep = spx.layer_args(0, x, s.E, s.k, s.renorm, lg, routing, out, ws, w4=w4, gguf=lay.gguf)
     with pytest.raises(SpxError) as ei:
