@@ -740,20 +740,24 @@ def run_cached(args):
 
 
 def run_draft_batch(args):
-    """Draft layers carrying T = 1, 2, 4, 8 tokens (one per request) in one
-    call: device us per layer, unique experts, algorithmic GB/s and draft
-    tokens/s.  Prints one JSON line."""
+    """Draft layers carrying T = 1, 2, 4, 8, 16 tokens (one per request) in one
+    call, or with --verify-batch verify layers of T = 9, 17, 33 tokens (more
+    tokens per expert): device us per layer, unique experts, algorithmic GB/s
+    and tokens/s.  Prints one JSON line."""
     import torch
     from quantized_expert_gb300 import build as B, spx
     B.build()
     spx.load()
     s = W.CONFIGS[args.config]
     sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
-    apply_formats(s, sets, args, torch, spx)
+    verify = args.verify_batch
+    if not verify:
+        apply_formats(s, sets, args, torch, spx)
     peak, peak_src = measured_peaks()
     rows = []
     stream = torch.cuda.Stream()
-    for T in (1, 2, 4, 8):
+    mode = 1 if verify else 0
+    for T in ((9, 17, 33) if verify else (1, 2, 4, 8, 16)):
         xs = [torch.from_numpy(np.ascontiguousarray(W.gen_x(s, T, step=i)).view(np.float16)).cuda()
               for i in range(NINPUTS)]
         lgs = [torch.from_numpy(W.gen_logits(s, T, step=i)).cuda() if s.logits != "router"
@@ -761,16 +765,22 @@ def run_draft_batch(args):
         ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
         r = spx.Routing.empty(T, s.E, s.k)
         out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
-        keep = [spx.layer_args(0, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, out, ws,
-                               w4=sets[i % NSETS]["w4"], shared=sets[i % NSETS]["shared"],
-                               w_router=sets[i % NSETS]["w_router"], gguf=sets[i % NSETS].get("gguf"))
-                for i in range(NSETS * NINPUTS)]
-        nb = []
-        for i in range(NINPUTS):
-            spx.spx_moe_layer(keep[i][0])
-            torch.cuda.synchronize()
-            nb.append((int(r.n_active.item()),
-                       layer_bytes(s, "draft", T, int(r.n_active.item()), args.zeros, args.gguf)))
+        try:
+            keep = [spx.layer_args(mode, xs[i % NINPUTS], s.E, s.k, s.renorm, lgs[i % NINPUTS], r, out, ws,
+                                   w4=None if verify else sets[i % NSETS]["w4"],
+                                   f16=sets[i % NSETS]["f16"] if verify else None, shared=sets[i % NSETS]["shared"],
+                                   w_router=sets[i % NSETS]["w_router"],
+                                   gguf=None if verify else sets[i % NSETS].get("gguf"))
+                    for i in range(NSETS * NINPUTS)]
+            nb = []
+            for i in range(NINPUTS):
+                spx.spx_moe_layer(keep[i][0])
+                torch.cuda.synchronize()
+                nb.append((int(r.n_active.item()), layer_bytes(s, "verify" if verify else "draft", T,
+                                                               int(r.n_active.item()), args.zeros, args.gguf)))
+        except spx.SpxError as err:  # a shape the launch does not take (activation rows beyond shared memory)
+            rows.append({"T": T, "unsupported": str(err)})
+            continue
         with torch.cuda.stream(stream):
             for i in range(args.warmup):
                 spx.spx_moe_layer(keep[i % len(keep)][0], stream)
@@ -790,8 +800,11 @@ def run_draft_batch(args):
         assert spx.spx_workspace_status(ws) == 0
     zp = (", per-group zero points" if args.zeros else ", GGUF Q8_0 experts" if args.gguf == "q8_0"
           else f", GGUF {args.gguf.upper()} gate/up + Q8_0 down experts" if args.gguf else "")
-    line = {"metric": "draft layer with T requests' tokens per call, device us per layer",
-            "config": {"workload": f"{s.name} draft{zp}, T = 1, 2, 4, 8 (one token per request)"},
+    line = {"metric": ("verify layer with T tokens per call" if verify else
+                       "draft layer with T requests' tokens per call") + ", device us per layer",
+            "config": {"workload": f"{s.name} verify, T = 9, 17, 33" if verify else
+                       f"{s.name} draft{zp}, T = 1, 2, 4, 8, 16 (one token per request; 16 on the routing "
+                       f"launch + expert launch)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
     print(json.dumps(line), flush=True)
 
@@ -1106,7 +1119,8 @@ def main():
     ap.add_argument("--loop-n", type=int, default=12)
     ap.add_argument("--tokens", type=int, default=0, help="with --loop: tokens per call (default: the shape's)")
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
-    ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8 (prints its own line)")
+    ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8, 16 (prints its own line)")
+    ap.add_argument("--verify-batch", action="store_true", help="verify layers at T = 9, 17, 33 (prints its own line)")
     ap.add_argument("--zeros", action="store_true",
                     help="with --draft-batch or --loop draft: INT4 experts with per-group zero points")
     ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"],
@@ -1127,7 +1141,7 @@ def main():
         run_loop(args)
     elif args.cached:
         run_cached(args)
-    elif args.draft_batch:
+    elif args.draft_batch or args.verify_batch:
         run_draft_batch(args)
     elif args.impl == "reference":
         if args.steps > 3:
