@@ -174,8 +174,8 @@ struct DkLayout {
 __host__ __device__ inline DkLayout dk_layout(int T, int H, int nst, int k, int nact_max, int E, bool kq = false) {
     DkLayout L;
     int o = 0;
-    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier
-    o += (3 * nst + 1) * 8;
+    L.bars = o;  // full[nst] (weights), empty[nst], hfull[nst] (h slices), all-consumer barrier, routing barrier
+    o += (3 * nst + 2) * 8;
     o = (o + 15) & ~15;
     L.hdrs = o;
     o += nst * (int)sizeof(DHeader);
@@ -384,10 +384,15 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L,
     };
     // Active experts: the consumer warps route the launch's tokens into shared
     // memory at start; routed work waits for that (shared gate/up does not).
+    // The routing barrier completes once per launch; every lane waits on it
+    // (a suspended wait that resumes as soon as the routing warp arrives).
+    uint64_t *rbar = hfull + nst + 1;
     auto n_act = [&]() -> int {
         if (na < 0) {
             const uint64_t t0 = global_timer_ns();
-            while (!rd0(misc + 4)) {  // a sleeping poll: the consumer warps route meanwhile
+            while (true) {
+                const bool seen = mbar_try_wait_sleep(rbar, 0, kDkSleepNs);
+                if (__all_sync(kAll, seen)) break;
                 if (rd0(misc)) {
                     ok = false;
                     return na = 0;
@@ -396,9 +401,7 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L,
                     timed_out(SITE_ROUTING);
                     return na = 0;
                 }
-                __nanosleep(64);
             }
-            __threadfence_block();
             na = rd0(misc + 5);
         }
         return na;
@@ -959,6 +962,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
     uint64_t *empty = full + nst;
     uint64_t *hfull = empty + nst;
     uint64_t *allbar = hfull + nst;
+    uint64_t *rbar = allbar + 1;  // routing published (one arrival, by the routing warp)
     int *misc = reinterpret_cast<int *>(smem + L.misc);
     int *scnt = reinterpret_cast<int *>(smem + L.scnt);
     volatile int *sfree = reinterpret_cast<volatile int *>(smem + L.sfree);
@@ -971,6 +975,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             mbar_init(&hfull[s], 1);
         }
         mbar_init(allbar, kDkCons);
+        mbar_init(rbar, 1);
         for (int i = 0; i < 16; ++i) misc[i] = 0;
         int *pstate = reinterpret_cast<int *>(smem + L.pstate);
         for (int s = 0; s < kDkMaxStages; ++s) {
@@ -1020,6 +1025,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
             misc[5] = na;
             __threadfence_block();
             *reinterpret_cast<volatile int *>(misc + 4) = 1;
+            mbar_arrive(rbar);  // wakes the producer's routing wait at once
             TLB_FIRST(p.tl_slot, TL_ROUTED);
         }
     };
