@@ -787,7 +787,7 @@ __device__ __forceinline__ void finalize_block(float *sa, int T, int nk, int lan
 // table (ste[a*T + rank]: token s/k, output row s/k, gate weight, in slot
 // order; stn[a] entries).  With out (block 0) the gather arrays of the routing
 // outputs are written as well.  Returns the number of active experts.
-__device__ __noinline__ int route_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane,
+__device__ __noinline__ int route_tables_warp(const DkParams &p, const DkLayout L, uint8_t *smem, int lane,
                                               bool out) {
     const int E = p.E, k = p.k, T = p.T, n = T * k;
     const int32_t *ids = reinterpret_cast<const int32_t *>(smem + L.rids);
@@ -852,7 +852,7 @@ __device__ __noinline__ int route_tables_warp(const DkParams &p, const DkLayout 
 // table (an expert's place = the selected experts below it; each holds one
 // slot, the token's).  Returns k.  The routing outputs are written apart, by
 // route_one_outputs, once the tables are published.
-__device__ __noinline__ int route_one_token(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane) {
+__device__ __noinline__ int route_one_token(const DkParams &p, const DkLayout L, uint8_t *smem, int lane) {
     const int E = p.E, k = p.k;
     int32_t *ids = reinterpret_cast<int32_t *>(smem + L.rids);
     float *pw = reinterpret_cast<float *>(smem + L.rpw);
@@ -882,7 +882,7 @@ __device__ __noinline__ int route_one_token(const DkParams &p, const DkLayout &L
 // Block 0's routing outputs for one token (k <= 32): the selections and
 // their weights, the lookahead counters, and the gather arrays (per-expert
 // counts and offsets, slots in expert order, the active list).
-__device__ __noinline__ void route_one_outputs(const DkParams &p, const DkLayout &L, const uint8_t *smem, int lane) {
+__device__ __noinline__ void route_one_outputs(const DkParams &p, const DkLayout L, const uint8_t *smem, int lane) {
     const int E = p.E, k = p.k;
     const int32_t *ids = reinterpret_cast<const int32_t *>(smem + L.rids);
     const float *pw = reinterpret_cast<const float *>(smem + L.rpw);
@@ -915,7 +915,7 @@ __device__ __noinline__ void route_one_outputs(const DkParams &p, const DkLayout
 
 // The unit call's routing: active experts and their token tables from global
 // memory (written by the preceding launches), into shared memory.
-__device__ __noinline__ int load_tables_warp(const DkParams &p, const DkLayout &L, uint8_t *smem, int lane) {
+__device__ __noinline__ int load_tables_warp(const DkParams &p, const DkLayout L, uint8_t *smem, int lane) {
     const int T = p.T;
     int *act = reinterpret_cast<int *>(smem + L.act);
     int *stn = reinterpret_cast<int *>(smem + L.stn);
