@@ -1647,7 +1647,8 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         for (int i = ctid; i < p.nact_max * geo.rd_nr; i += kDkCons * 32) p.rdy_r[i] = 0;
         if (ctid < kDkShards) p.qctr[64 * ctid] = 0;
         if (ctid == 0) p.hdr->done_ticket = 0;
-        __threadfence();
+        // no fence here: nothing in this launch reads these words again, and
+        // the launch that follows reads them only after this one has completed
         if (ctid == 0) TLB_LAST(p.tl_slot, TL_OUT_DONE);
     }
     if (ctid == 0) TLB_LAST(p.tl_slot, TL_EXIT);

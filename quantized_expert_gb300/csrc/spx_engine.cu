@@ -1337,10 +1337,11 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const EngineParams 
         if (ctid == 0) {
             __threadfence();
             if (atomicAdd(&p.hdr->exit_ticket, 1u) == (uint32_t)nhelp - 1) {
+                // no fence after these: the launch that follows reads them only
+                // after this one has completed
                 p.hdr->work_counter = 0;
                 p.hdr->done_ticket = 0;
                 p.hdr->exit_ticket = 0;
-                __threadfence();
             }
         }
     }
