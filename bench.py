@@ -50,10 +50,10 @@ KERNEL_SOURCES = {
     "verify": ["spx_engine.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_108_608 + 3_193_088,
-               "algorithmic_bytes": 674_897_920, "source_sha": "5ddc46a3dc846712"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_509_632 + 691_200, "algorithmic_bytes": 61_374_720,
-              "source_sha": "48aa0f593edc2421"},
+    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_109_120 + 2_899_200,
+               "algorithmic_bytes": 674_897_920, "source_sha": "8695ed057ff41471"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_672 + 192_512, "algorithmic_bytes": 61_374_720,
+              "source_sha": "e27d744ac0bc70de"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
