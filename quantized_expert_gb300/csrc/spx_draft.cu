@@ -70,21 +70,24 @@ constexpr int kDkShards = 8;      // independent queue counters (SM b uses shard
 constexpr uint32_t kDkSleepNs = 1000;  // longest sleep of a waiting warp inside one try_wait
 // Warp roles.  An SM's four sub-partitions (each with its own scheduler,
 // instruction cache and tensor pipe) take warps by index mod 4.  The producer
-// (warp 3) and the poller (warp 7) share sub-partition 3 with one consumer
-// warp (11); the other ten consumer warps fill sub-partitions 0-2, so the
-// producer competes with little consumer work while the consumers' tensor-
-// core products use all four pipes.  Four warps share one sub-partition's
-// 16K registers: a thread may use at most 128 (kDkMaxRegs).
-constexpr int kDkCons = 11;
-constexpr int kDkWarps = 13;
+// (warp 3) and the poller (warp 7) have sub-partition 3 to themselves (warp
+// 11, when the block has one, does nothing): a consumer warp there took the
+// issue slots from the producer, whose per-unit work then ran several times
+// slower.  The consumer warps fill sub-partitions 0-2.  The warps of a
+// sub-partition share its 16K registers (kDkMaxRegs per thread).
+constexpr int kDkCons = 9;
+constexpr int kDkWarps = 11;
 constexpr int kDkProducerWarp = 3, kDkPollerWarp = 7;
+constexpr int kDkIdleWarp = kDkWarps > 12 ? 11 : -1;  // keeps sub-partition 3 to the producer and the poller
 constexpr int kDkThreads = kDkWarps * 32;
-constexpr int kDkMaxRegs = 65536 / (((kDkWarps + 3) / 4) * 4 * 32) / 8 * 8;
-// consumer index 0..10 of a consumer warp
+constexpr int kDkMaxRegs = (65536 / (((kDkWarps + 3) / 4) * 4 * 32) / 8 * 8) < 168
+                               ? 65536 / (((kDkWarps + 3) / 4) * 4 * 32) / 8 * 8
+                               : 168;
+// consumer index 0..kDkCons-1 of a consumer warp
 __host__ __device__ constexpr int dk_consumer_index(int warp) {
-    return warp - (warp > kDkProducerWarp) - (warp > kDkPollerWarp);
+    return warp - (warp > kDkProducerWarp) - (warp > kDkPollerWarp) - (kDkIdleWarp >= 0 && warp > kDkIdleWarp);
 }
-static_assert(dk_consumer_index(kDkWarps - 1) == kDkCons - 1, "eleven consumer warps");
+static_assert(kDkWarps > kDkPollerWarp && kDkCons == kDkWarps - 2 - (kDkIdleWarp >= 0 ? 1 : 0), "consumer warps");
 static_assert(kDkMaxRegs >= 64, "registers per thread of the draft launch");
 
 struct __align__(16) DHeader {
@@ -997,6 +1000,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         if (lane == 0) dk_poller(p, smem, L);
         return;
     }
+    if (warp == kDkIdleWarp) return;
     const int cw = dk_consumer_index(warp);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
     uint32_t allphase = 0;
