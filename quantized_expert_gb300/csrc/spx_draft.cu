@@ -79,15 +79,23 @@ constexpr int kDkCons = 9;
 constexpr int kDkWarps = 11;
 constexpr int kDkProducerWarp = 3, kDkPollerWarp = 7;
 constexpr int kDkIdleWarp = kDkWarps > 12 ? 11 : -1;  // keeps sub-partition 3 to the producer and the poller
+constexpr int kDkIdleWarp2 = -1;
 constexpr int kDkThreads = kDkWarps * 32;
 constexpr int kDkMaxRegs = (65536 / (((kDkWarps + 3) / 4) * 4 * 32) / 8 * 8) < 168
                                ? 65536 / (((kDkWarps + 3) / 4) * 4 * 32) / 8 * 8
                                : 168;
-// consumer index 0..kDkCons-1 of a consumer warp
-__host__ __device__ constexpr int dk_consumer_index(int warp) {
-    return warp - (warp > kDkProducerWarp) - (warp > kDkPollerWarp) - (kDkIdleWarp >= 0 && warp > kDkIdleWarp);
+__host__ __device__ constexpr bool dk_not_consumer(int w) {
+    return w == kDkProducerWarp || w == kDkPollerWarp || w == kDkIdleWarp || w == kDkIdleWarp2;
 }
-static_assert(kDkWarps > kDkPollerWarp && kDkCons == kDkWarps - 2 - (kDkIdleWarp >= 0 ? 1 : 0), "consumer warps");
+// consumer index 0..kDkCons-1 of a consumer warp: the consumer warps below it
+__host__ __device__ constexpr int dk_consumer_index(int warp) {
+    int c = 0;
+    for (int w = 0; w < warp; ++w) c += dk_not_consumer(w) ? 0 : 1;
+    return c;
+}
+static_assert(kDkWarps > kDkPollerWarp && kDkWarps > kDkProducerWarp &&
+                  kDkCons == kDkWarps - 2 - (kDkIdleWarp >= 0 ? 1 : 0) - (kDkIdleWarp2 >= 0 ? 1 : 0),
+              "consumer warps");
 static_assert(kDkMaxRegs >= 64, "registers per thread of the draft launch");
 
 struct __align__(16) DHeader {
@@ -1000,7 +1008,7 @@ __global__ void __maxnreg__(kDkMaxRegs) draft_kernel(const DkParams p) {
         if (lane == 0) dk_poller(p, smem, L);
         return;
     }
-    if (warp == kDkIdleWarp) return;
+    if (warp == kDkIdleWarp || warp == kDkIdleWarp2) return;
     const int cw = dk_consumer_index(warp);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
     uint32_t allphase = 0;
