@@ -52,8 +52,8 @@ KERNEL_SOURCES = {
 PROFILED_TRAFFIC = {
     "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_109_120 + 2_899_200,
                "algorithmic_bytes": 674_897_920, "source_sha": "8695ed057ff41471"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_498_880 + 248_576, "algorithmic_bytes": 61_374_720,
-              "source_sha": "abe921986c617ff5"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 246_528, "algorithmic_bytes": 61_374_720,
+              "source_sha": "e4b5480fdc35b752"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
