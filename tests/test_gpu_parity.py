@@ -293,6 +293,28 @@ def test_layer_full_size(name, mode):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{name} {mode} rep {rep}")
 
 
+@pytest.mark.parametrize("E,k", [(256, 8), (64, 40), (33, 33), (16, 1)])
+def test_draft_layer_routing_extremes(E, k):
+    """One-token draft layers at the routing's edges: 256 experts (the wide
+    selection instance), more than 32 selections (the general table builder),
+    every expert selected, a single selection; routing outputs bit-exact
+    (ids, offsets, sorted slots), output within tolerance of the oracle."""
+    gh = _gh()
+    s = _small("deepseek_v2_lite", H=256, I=128, E=E, k=k, I_s=256)
+    T = 1
+    x = W.gen_x(s, T, step=170 + E + k)
+    logits = W.gen_logits(s, T, step=170 + E + k)
+    lay = gh.Layer(s, needed=gh.needed_experts(s, [logits], [x]), verify=False, slice_cols=16)
+    ref = lay.oracle_layer("draft", x, logits=logits)
+    outs, routing, _ = _run_layer(lay, "draft", x, logits)
+    assert np.array_equal(routing.topk_ids.cpu().numpy(), ref["ids"])
+    g = ref["gather"]
+    assert np.array_equal(routing.offsets.cpu().numpy(), g["offsets"])
+    assert np.array_equal(routing.sorted_slots.cpu().numpy(), g["sorted_slots"])
+    for rep, o in enumerate(outs):
+        gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"E={E} k={k} rep {rep}")
+
+
 @pytest.mark.parametrize("T", [1, 9, 17])
 def test_verify_layer_odd_slice_count(T):
     """Verify layer whose shared expert is an odd number of 16-column slices
