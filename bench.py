@@ -50,8 +50,8 @@ KERNEL_SOURCES = {
     "verify": ["spx_engine.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_109_120 + 2_899_200,
-               "algorithmic_bytes": 674_897_920, "source_sha": "8695ed057ff41471"},
+    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_120_896 + 2_966_016,
+               "algorithmic_bytes": 674_897_920, "source_sha": "3be060e464fb3afd"},
     "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 246_528, "algorithmic_bytes": 61_374_720,
               "source_sha": "e4b5480fdc35b752"},
 }
