@@ -1381,9 +1381,10 @@ int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int
 }
 
 // ------------------------------------------------------------ launching --
-// Token tiles of 8 an expert launch instance carries (FP16 verify: 1, 2, 3 or
-// 8; the INT4 and GGUF instances take 2 as 3).  The 2-tile FP16 instance for
-// 9-16 tokens needs 108 registers instead of 132 (verify at 9 tokens: 3% faster).
+// Token tiles of 8 an expert launch instance carries: 1, 2, 3 or 8.  The
+// 2-tile instances (9-16 tokens) need far fewer registers than the 3-tile
+// ones (FP16: 108 instead of 132; INT4 and zero points no longer spill):
+// verify at 9 tokens 3% faster, INT4 draft batches of 16 tokens 27%.
 int engine_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : (T <= 24 ? 3 : 8)); }
 
 // Geometry: two consumer groups of two stages each (two units in parallel,
@@ -1478,37 +1479,44 @@ int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
     const int nt = engine_nt(p.T);
     if (p.routed_enabled && p.routed_fmt == kFmtQ8) {
         if (nt == 1) return launch_engine_t<kFmtQ8, 1, 1>(p, s, pdl);
-        if (nt == 3 || nt == 2) return launch_engine_t<kFmtQ8, 1, 3>(p, s, pdl);
+        if (nt == 2) return launch_engine_t<kFmtQ8, 1, 2>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<kFmtQ8, 1, 3>(p, s, pdl);
         return launch_engine_t<kFmtQ8, 1, 8>(p, s, pdl);
     }
     if (p.routed_enabled && p.routed_fmt == kFmtQ2K) {
         if (nt == 1) return launch_engine_t<kFmtQ2K, 1, 1>(p, s, pdl);
-        if (nt == 3 || nt == 2) return launch_engine_t<kFmtQ2K, 1, 3>(p, s, pdl);
+        if (nt == 2) return launch_engine_t<kFmtQ2K, 1, 2>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<kFmtQ2K, 1, 3>(p, s, pdl);
         return launch_engine_t<kFmtQ2K, 1, 8>(p, s, pdl);
     }
     if (p.routed_enabled && p.routed_fmt == kFmtQ4K) {
         if (nt == 1) return launch_engine_t<kFmtQ4K, 1, 1>(p, s, pdl);
-        if (nt == 3 || nt == 2) return launch_engine_t<kFmtQ4K, 1, 3>(p, s, pdl);
+        if (nt == 2) return launch_engine_t<kFmtQ4K, 1, 2>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<kFmtQ4K, 1, 3>(p, s, pdl);
         return launch_engine_t<kFmtQ4K, 1, 8>(p, s, pdl);
     }
     if (p.routed_enabled && p.routed_fmt == FMT_W4 && p.w4_zeros) {
         if (p.S == 32) {
             if (nt == 1) return launch_engine_t<FMT_W4Z, 2, 1>(p, s, pdl);
-            if (nt == 3 || nt == 2) return launch_engine_t<FMT_W4Z, 2, 3>(p, s, pdl);
+            if (nt == 2) return launch_engine_t<FMT_W4Z, 2, 2>(p, s, pdl);
+            if (nt == 3) return launch_engine_t<FMT_W4Z, 2, 3>(p, s, pdl);
             return SPX_ERR_UNSUPPORTED;
         }
         if (nt == 1) return launch_engine_t<FMT_W4Z, 1, 1>(p, s, pdl);
-        if (nt == 3 || nt == 2) return launch_engine_t<FMT_W4Z, 1, 3>(p, s, pdl);
+        if (nt == 2) return launch_engine_t<FMT_W4Z, 1, 2>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<FMT_W4Z, 1, 3>(p, s, pdl);
         return launch_engine_t<FMT_W4Z, 1, 8>(p, s, pdl);
     }
     if (p.routed_enabled && p.routed_fmt == FMT_W4) {
         if (p.S == 32) {
             if (nt == 1) return launch_engine_t<FMT_W4, 2, 1>(p, s, pdl);
-            if (nt == 3 || nt == 2) return launch_engine_t<FMT_W4, 2, 3>(p, s, pdl);
+            if (nt == 2) return launch_engine_t<FMT_W4, 2, 2>(p, s, pdl);
+            if (nt == 3) return launch_engine_t<FMT_W4, 2, 3>(p, s, pdl);
             return SPX_ERR_UNSUPPORTED;  // INT4 slices of 32 columns take at most 24 tokens per expert
         }
         if (nt == 1) return launch_engine_t<FMT_W4, 1, 1>(p, s, pdl);
-        if (nt == 3 || nt == 2) return launch_engine_t<FMT_W4, 1, 3>(p, s, pdl);
+        if (nt == 2) return launch_engine_t<FMT_W4, 1, 2>(p, s, pdl);
+        if (nt == 3) return launch_engine_t<FMT_W4, 1, 3>(p, s, pdl);
         return launch_engine_t<FMT_W4, 1, 8>(p, s, pdl);
     }
     if (nt == 1) return launch_engine_t<FMT_F16, 1, 1>(p, s, pdl);
@@ -1520,6 +1528,13 @@ int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
 int engine_preload() {
     int st = SPX_OK;
     if (!st) st = configure_engine<FMT_W4, 2, 1>();
+    if (!st) st = configure_engine<FMT_W4, 2, 2>();
+    if (!st) st = configure_engine<FMT_W4, 1, 2>();
+    if (!st) st = configure_engine<FMT_W4Z, 2, 2>();
+    if (!st) st = configure_engine<FMT_W4Z, 1, 2>();
+    if (!st) st = configure_engine<kFmtQ8, 1, 2>();
+    if (!st) st = configure_engine<kFmtQ2K, 1, 2>();
+    if (!st) st = configure_engine<kFmtQ4K, 1, 2>();
     if (!st) st = configure_engine<FMT_W4, 2, 3>();
     if (!st) st = configure_engine<FMT_W4, 1, 1>();
     if (!st) st = configure_engine<FMT_W4, 1, 3>();
