@@ -1381,11 +1381,13 @@ int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int
 }
 
 // ------------------------------------------------------------ launching --
-// Token tiles of 8 an expert launch instance carries: 1, 2, 3 or 8.  The
-// 2-tile instances (9-16 tokens) need far fewer registers than the 3-tile
-// ones (FP16: 108 instead of 132; INT4 and zero points no longer spill):
-// verify at 9 tokens 3% faster, INT4 draft batches of 16 tokens 27%.
-int engine_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : (T <= 24 ? 3 : 8)); }
+// Token tiles of 8 an expert launch instance carries: 1, 2, 3, 5 (FP16 only;
+// the other formats take 5 as 8) or 8.  Narrower instances need fewer
+// registers: the 2-tile ones (9-16 tokens) do not spill (FP16: 108 registers
+// instead of 132): verify at 9 tokens 3% faster, INT4 draft batches of 16
+// tokens 27%; the 5-tile FP16 one (25-40 tokens, 162 registers, no spill)
+// took verify at 33 tokens from 372 to 257 us against the spilling 8-tile one.
+int engine_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : (T <= 24 ? 3 : (T <= 40 ? 5 : 8))); }
 
 // Geometry: two consumer groups of two stages each (two units in parallel,
 // each double-buffered), with the largest chunk (a multiple of 1 KB, at most
@@ -1522,6 +1524,7 @@ int launch_engine(const EngineParams &p, cudaStream_t s, bool pdl) {
     if (nt == 1) return launch_engine_t<FMT_F16, 1, 1>(p, s, pdl);
     if (nt == 2) return launch_engine_t<FMT_F16, 1, 2>(p, s, pdl);
     if (nt == 3) return launch_engine_t<FMT_F16, 1, 3>(p, s, pdl);
+    if (nt == 5) return launch_engine_t<FMT_F16, 1, 5>(p, s, pdl);
     return launch_engine_t<FMT_F16, 1, 8>(p, s, pdl);
 }
 
@@ -1555,6 +1558,7 @@ int engine_preload() {
     if (!st) st = configure_engine<kFmtQ4K, 1, 8>();
     if (!st) st = configure_engine<FMT_F16, 1, 1>();
     if (!st) st = configure_engine<FMT_F16, 1, 2>();
+    if (!st) st = configure_engine<FMT_F16, 1, 5>();
     if (!st) st = configure_engine<FMT_F16, 1, 3>();
     if (!st) st = configure_engine<FMT_F16, 1, 8>();
     cudaFuncAttributes fa;
@@ -1568,7 +1572,7 @@ int engine_fits(int T, int H, int fmt, int S) {
     const bool w4 = fmt == FMT_W4 || zp || fmt == kFmtQ8 || fmt == kFmtQ2K || fmt == kFmtQ4K;  // down-scale rows
     const int kqs = fmt == kFmtQ2K ? 16 : fmt == kFmtQ4K ? 32 : 0;
     if (kqs && H % 256) return 0;
-    if (w4 && S == 32 && engine_nt(T) == 8) return 0;
+    if (w4 && S == 32 && engine_nt(T) > 3) return 0;  // 32-column slices: at most 3 token tiles
     int G, nsg, bytes, chunk;
     return choose_geometry(T, H, npad, engine_smax(w4, S), w4, G, nsg, bytes, chunk, zp, kqs) ? 1 : 0;
 }
