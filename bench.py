@@ -50,8 +50,8 @@ KERNEL_SOURCES = {
     "verify": ["spx_engine.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_120_896 + 2_966_016,
-               "algorithmic_bytes": 674_897_920, "source_sha": "3be060e464fb3afd"},
+    "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_107_840 + 2_989_568,
+               "algorithmic_bytes": 674_897_920, "source_sha": "487d19f64ab1d38e"},
     "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 246_528, "algorithmic_bytes": 61_374_720,
               "source_sha": "e4b5480fdc35b752"},
 }
@@ -803,8 +803,8 @@ def run_draft_batch(args):
     line = {"metric": ("verify layer with T tokens per call" if verify else
                        "draft layer with T requests' tokens per call") + ", device us per layer",
             "config": {"workload": f"{s.name} verify, T = 9, 17, 33" if verify else
-                       f"{s.name} draft{zp}, T = 1, 2, 4, 8, 16 (one token per request; 16 on the routing "
-                       f"launch + expert launch)"},
+                       f"{s.name} draft{zp}, T = 1, 2, 4, 8, 16 (one token per request; 8 and 16 on the "
+                       f"routing launch + expert launch)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
     print(json.dumps(line), flush=True)
 

@@ -204,7 +204,7 @@ typedef struct {
     /* Per-group zero points (asymmetric INT4, the AWQ form: W = (code - zero)
      * * scale) [P1 Main Findings: drafts quantised by GPTQ, AWQ and GGUF]:
      * spx_w4_zeros_bytes() bytes from spx_w4_zeros_repack(), or NULL for zero
-     * point 8.  Served by the one-launch draft path (T <= 8) and by the
+     * point 8.  Served by the one-launch draft path (T <= 5) and by the
      * expert launch (more tokens, cache-aware calls; 32-column slices take at
      * most 24 tokens there, else SPX_ERR_UNSUPPORTED). */
     const void *zeros;
@@ -329,7 +329,7 @@ SPX_API int spx_moe_draft_w4a16(const uint16_t *x, int T, const spx_w4_experts *
                         const int32_t *active, const int32_t *n_active,
                         float *y_sorted, void *ws, size_t ws_bytes, spx_stream_t stream);
 
-/* The draft unit call with GGUF experts (the draft launch up to 8 tokens,
+/* The draft unit call with GGUF experts (the draft launch up to 5 tokens,
  * the expert launch above); arguments and output as spx_moe_draft_w4a16. */
 SPX_API int spx_moe_draft_gguf(const uint16_t *x, int T, const spx_gguf_experts *w, int k,
                         const int32_t *offsets, const int32_t *sorted_slots,
@@ -382,7 +382,7 @@ typedef struct {
     /* Cache-aware expert execution [P1 Key Contributions 3-4: experts the
      * lookahead saw are cache hits and run first; misses wait for their
      * weights].  Both nullable; when either is set the layer runs as a routing
-     * launch plus the expert launch (also for draft calls of T <= 8).
+     * launch plus the expert launch (also for draft calls of T <= 5).
      *   resident [E] uint8: nonzero = expert e's weights are resident; the
      *     routed experts are queued resident first, then the others, each in
      *     ascending expert order.  Only the order changes, not the result.
@@ -399,7 +399,7 @@ typedef struct {
     const spx_gguf_experts *gguf;
 } spx_layer_args;
 
-/* One layer.  Draft calls with T <= 8 (and no cache-aware options) are one
+/* One layer.  Draft calls with T <= 5 (and no cache-aware options) are one
  * launch that routes its tokens in every block (after a router-product launch
  * when w_router is given); other calls are a routing launch (router product,
  * softmax, top-k, counters, counting sort, token tables) and one persistent

@@ -94,7 +94,7 @@ static size_t ws_scratch_base(int T, int H) { return ws_order_offset(T, H) + (si
 extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
     if (T < 1 || H < 1 || T > kMaxT || H > kMaxH || I < 0 || E < 1 || k < 1 || I_s < 0) return 0;
     const size_t base = ws_scratch_base(T, H);
-    if (T > 8 || I % 128 || I_s % 16) return base;  // the split-K draft launch serves T <= 8 only
+    if (T > kDraftLaunchMaxT || I % 128 || I_s % 16) return base;  // only the draft launch has split-K scratch
     const int nact = E < T * k ? E : T * k;
     return draft_scratch_end(base, T, H, I, I_s, nact);
 }
@@ -340,7 +340,7 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
         const cudaError_t ce = cudaMemsetAsync(clear, 0, clear_bytes, s);
         if (ce != cudaSuccess) return record_launch(ce);
     }
-    if (a->mode == 0 && !cache_aware && draft_supported(T, H, I, S, I_s, E, k, kq)) {
+    if (a->mode == 0 && !cache_aware && via_draft) {
         // Draft layer: the draft launch routes its few tokens itself (no
         // routing launch before it); with a router weight a small launch
         // computes the logits first and the draft launch overlaps it.

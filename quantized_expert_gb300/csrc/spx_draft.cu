@@ -1,4 +1,4 @@
-// spx_draft.cu -- the fused multi-expert INT4 draft launch (T <= 8 tokens).
+// spx_draft.cu -- the fused multi-expert INT4 draft launch (T <= 5 tokens).
 //
 // Method (ai.info summary of the Specter paper, Key Contributions 2 and 4;
 // richland.au post, "What shipped"): a draft step runs every selected INT4
@@ -1722,7 +1722,7 @@ size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max
 
 bool draft_supported(int T, int H, int I, int S, int I_s, int E, int k, bool kq) {
     if (kq && (H % 256 || S != 16)) return false;
-    if (T < 1 || T > 8 || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
+    if (T < 1 || T > kDraftLaunchMaxT || H % 128 || I % 128 || (S != 16 && S != 32)) return false;
     if (I_s % 16 || E < 1 || k < 1 || E > kMaxE || T * k > kMaxSlots) return false;
     return dk_layout(T, H, 4, k, E < T * k ? E : T * k, E, kq).total <= kDkSmemLimit;
 }

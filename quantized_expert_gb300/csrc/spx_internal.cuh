@@ -136,7 +136,7 @@ __host__ __device__ inline size_t q4k_unit_bytes(int H) { return (size_t)(H / 25
 __host__ __device__ inline size_t q4k_units_bytes(int E, int H, int I) {
     return (size_t)E * (I / 16) * q4k_unit_bytes(H);
 }
-// GGUF experts for the expert launch (draft calls above 8 tokens and
+// GGUF experts for the expert launch (draft calls above 5 tokens and
 // cache-aware ones): after the draft launch's layout, the Q8_0 down codes
 // again in unit order [E][I/16], a unit = H/32 blocks of 512 B, one per m-tile
 // pair P (32 lanes x 16 B: tile 0's 8 codes, then tile 1's, A[m][kc] = code of
@@ -441,6 +441,11 @@ struct DraftRouting {
     int32_t *counts, *offsets, *sorted_slots, *active, *n_active;
 };
 // kq: GGUF K-quant gate/up (Q2_K, Q4_K): H a multiple of 256, S = 16, room for x sums
+// Calls of at most this many tokens take the draft launch.  Its token loop would
+// take up to 8 (one n-tile), but from 6 tokens on the routing launch + expert
+// launch is as fast or faster (measured on GB300 at 5-8 tokens on the DeepSeek-,
+// Qwen- and Phi-shaped layers), so larger calls go there.
+constexpr int kDraftLaunchMaxT = 5;
 bool draft_supported(int T, int H, int I, int S, int I_s, int E = 1, int k = 1, bool kq = false);
 size_t draft_scratch_end(size_t base, int T, int H, int I, int I_s, int nact_max);
 // rt == nullptr: routing from e.active / e.n_active and the token tables e.tables.

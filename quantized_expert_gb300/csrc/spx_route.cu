@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteParams p) {
     select_block(p);
 }
 
-// Router product for the draft layer call (T <= 8): one block per expert row.
+// Router product for the draft layer call (T <= 5): one block per expert row.
 // A dependent launch may start at once and waits for the logits with
 // griddepcontrol.wait.
 __global__ void __launch_bounds__(256) router_logits_kernel(const __half *x, const __half *wr, int T, int H, int E,

@@ -341,7 +341,7 @@ def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_acti
 
 
 def spx_moe_draft_gguf(x, w: PackedGguf, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
-    """spx_moe_draft_w4a16 with GGUF draft experts (T <= 8)."""
+    """spx_moe_draft_w4a16 with GGUF draft experts."""
     T = x.shape[0]
     cs = w.cstruct()
     _chk(load().spx_moe_draft_gguf(_p(x), T, C.byref(cs), k, _p(offsets), _p(sorted_slots), _p(active),

@@ -48,7 +48,7 @@ def test_sizes_and_strings(lib):
     assert lib.spx_w4_packed_bytes(64, 2048, 1408, 24) == 0
     assert lib.spx_f16_packed_bytes(64, 2048, 1408) == 64 * 1408 * 2048 * 2 * 3
     assert lib.spx_workspace_size(17, 2048, 1408, 64, 6, 2816) >= 256 + 17 * 2048 * 4
-    # the T <= 8 draft launch adds its split-K scratch
+    # the draft launch (up to 5 tokens) adds its split-K scratch
     assert lib.spx_workspace_size(1, 2048, 1408, 64, 6, 2816) > lib.spx_workspace_size(1, 2048, 0, 64, 6, 0)
     assert lib.spx_workspace_size(65, 2048, 1408, 64, 6, 0) == 0
 

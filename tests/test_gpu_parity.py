@@ -139,11 +139,12 @@ SMALL_CASES = [
     (_small("tiny"), 4, 16),
     (_small("deepseek_v2_lite", I=256, E=16), 1, 32),
     (_small("deepseek_v2_lite", I=256, E=16), 17, 32),
-    (_small("deepseek_v2_lite", I=256, E=16), 8, 16),    # draft launch with 8 tokens, 16-column slices
+    (_small("deepseek_v2_lite", I=256, E=16), 8, 16),    # 8 tokens, 16-column slices: the expert launch's 1-tile instance
     (_small("qwen15_moe", I=384, E=12, I_s=512), 9, 16),
     (_small("phi35_moe", H=1024, I=512), 17, 16),
     (_small("phi35_moe", H=1024, I=512, k=2), 33, 16),   # > 24 tokens: 64-token kernel
     (_small("deepseek_v2_lite", H=256, I=128, E=8, k=8), 64, 16),  # k = E, maximum T
+    (_small("deepseek_v2_lite", I=256, E=16), 5, 16),    # the draft launch's largest call
 ]
 
 
@@ -541,10 +542,11 @@ def test_cache_aware_ready_flag_never_set_times_out():
     gh.check_close(gh.f16_out(out), ref["out_half"].view(np.float16).astype(np.float64), "after a timeout")
 
 
-@pytest.mark.parametrize("T", [4, 8])
+@pytest.mark.parametrize("T", [4, 5, 8])
 def test_batched_draft_full_size(T):
     """Several requests' draft tokens in one draft call (DeepSeek-V2-Lite
-    shape, T = 4 and 8 tokens): one launch, each expert the tokens share read
+    shape, T = 4, 5 and 8 tokens; up to 5 one draft launch, 8 through the
+    routing launch and the expert launch), each expert the tokens share read
     once; routing outputs bit-exact and the layer output within tolerance."""
     gh = _gh()
     s = W.CONFIGS["deepseek_v2_lite"]
@@ -563,12 +565,12 @@ def test_batched_draft_full_size(T):
 
 
 # ------------------------------------------- asymmetric INT4 (zero points)
-@pytest.mark.parametrize("T,S", [(1, 32), (1, 16), (4, 32), (8, 16), (9, 16), (17, 16), (17, 32)])
+@pytest.mark.parametrize("T,S", [(1, 32), (1, 16), (4, 32), (5, 16), (8, 16), (9, 16), (17, 16), (17, 32)])
 def test_draft_layer_zero_points_full_size(T, S):
     """Per-group zero points (the AWQ form, W = (code - zero) * scale, zeros
     uniform over 0..15) on every draft expert, DeepSeek-V2-Lite shape, through
     spx_moe_layer: routing bit-exact, output within tolerance of the oracle.
-    Up to 8 tokens the draft launch serves the call, from 9 on the routing
+    Up to 5 tokens the draft launch serves the call, from 6 on the routing
     launch and the expert launch."""
     gh = _gh()
     s = W.CONFIGS["deepseek_v2_lite"]
@@ -583,11 +585,11 @@ def test_draft_layer_zero_points_full_size(T, S):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"zero points T={T} S={S} rep {rep}")
 
 
-@pytest.mark.parametrize("case", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("case", [0, 1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_draft_unit_call_zero_points(case):
     """spx_moe_draft_w4a16 with zero points on the small cases (several tiles,
-    ragged token tiles and groups, both slice widths; up to 8 tokens on the
-    draft launch, then the expert launch with 1, 3 or 8 token tiles)."""
+    ragged token tiles and groups, both slice widths; up to 5 tokens on the
+    draft launch, then the expert launch with 1, 2, 3, 5 or 8 token tiles)."""
     spx, gh = _spx(), _gh()
     s, T, S = SMALL_CASES[case]
     x = W.gen_x(s, T, step=70 + case)
@@ -638,7 +640,7 @@ def test_zero_points_of_eight_match_the_symmetric_path(case):
     # expert launch: a reassociation of fp32 sums over H = 2048 products
     # (measured 8.5e-6 of the largest output at 32-column slices)
     d = float(np.abs(ys[0] - ys[1]).max()) / float(np.abs(ys[0]).max())
-    assert d <= (1e-6 if T <= 8 else 3e-5), d
+    assert d <= (1e-6 if T <= 5 else 3e-5), d
 
 
 @pytest.mark.parametrize("T", [1, 9])
@@ -686,7 +688,7 @@ def test_zero_points_wide_slices_reject_many_tokens():
 
 # ------------------------------------------------------------- GGUF drafts
 @pytest.mark.parametrize("kind", ["q8_0", "q2_k", "q4_k"])
-@pytest.mark.parametrize("name,T", [("deepseek_v2_lite", 1), ("deepseek_v2_lite", 8), ("qwen15_moe", 1),
+@pytest.mark.parametrize("name,T", [("deepseek_v2_lite", 1), ("deepseek_v2_lite", 5), ("qwen15_moe", 1),
                                     ("phi35_moe", 1)])
 def test_gguf_draft_layer_full_size(name, T, kind):
     """GGUF draft experts at full size through spx_moe_layer: Q8_0 (fp16
@@ -709,15 +711,15 @@ def test_gguf_draft_layer_full_size(name, T, kind):
         gh.check_close(o, ref["out_half"].view(np.float16).astype(np.float64), f"{kind} {name} T={T} rep {rep}")
 
 
-GGUF_ENGINE_KINDS = ["q8_0", "q2_k", "q4_k"]  # served by the expert launch too (above 8 tokens, cache-aware)
+GGUF_ENGINE_KINDS = ["q8_0", "q2_k", "q4_k"]  # served by the expert launch too (above 5 tokens, cache-aware)
 
 
-@pytest.mark.parametrize("kind,case", [(kd, c) for kd in ["q8_0", "q2_k", "q4_k"] for c in [1, 2, 4]] +
-                         [(kd, c) for kd in GGUF_ENGINE_KINDS for c in [3, 5, 6, 7, 8]])
+@pytest.mark.parametrize("kind,case", [(kd, c) for kd in ["q8_0", "q2_k", "q4_k"] for c in [1, 2, 9]] +
+                         [(kd, c) for kd in GGUF_ENGINE_KINDS for c in [3, 4, 5, 6, 7, 8]])
 def test_gguf_draft_unit_call(case, kind):
     """spx_moe_draft_gguf on the small cases with 16-column slices: per-slot
-    expert outputs against the oracle (up to 8 tokens on the draft launch,
-    then the expert launch with 1, 3 or 8 token tiles)."""
+    expert outputs against the oracle (up to 5 tokens on the draft launch,
+    then the expert launch with 1, 2, 3, 5 or 8 token tiles)."""
     spx, gh = _spx(), _gh()
     s, T, S = SMALL_CASES[case]
     x = W.gen_x(s, T, step=110 + case)
@@ -764,7 +766,7 @@ def test_gguf_draft_ragged_ranges(kind):
 @pytest.mark.parametrize("kind", GGUF_ENGINE_KINDS)
 @pytest.mark.parametrize("T", [9, 17])
 def test_gguf_layer_on_the_expert_launch_full_size(kind, T):
-    """GGUF draft layers above 8 tokens (DeepSeek-V2-Lite shape) take the
+    """GGUF draft layers above 5 tokens (DeepSeek-V2-Lite shape) take the
     routing launch and the expert launch: routing bit-exact, output within
     tolerance of the oracle."""
     gh = _gh()
