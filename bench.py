@@ -52,8 +52,8 @@ KERNEL_SOURCES = {
 PROFILED_TRAFFIC = {
     "verify": {"kernel": "engine_kernel<1,1,3>", "dram_bytes": 675_107_840 + 2_989_568,
                "algorithmic_bytes": 674_897_920, "source_sha": "487d19f64ab1d38e"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 246_528, "algorithmic_bytes": 61_374_720,
-              "source_sha": "e4b5480fdc35b752"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_648 + 225_280, "algorithmic_bytes": 61_374_720,
+              "source_sha": "e510f961ab199be3"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
