@@ -204,8 +204,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- workload ----
-def make_weight_set(s, idx, torch, spx):
-    """Random canonical weights on the device (seeded), repacked for the kernels."""
+def make_weight_set(s, idx, torch, spx, tc_pack=False):
+    """Random canonical weights on the device (seeded), repacked for the kernels
+    (tc_pack: the FP16 verify weights also in the tile pack of the
+    tensor-memory verify launches)."""
     g = torch.Generator(device="cuda")
     g.manual_seed(1_000_003 * (s.seed + 1) + idx)
     E, H, I = s.E, s.H, s.I
@@ -222,11 +224,11 @@ def make_weight_set(s, idx, torch, spx):
 
     w4 = spx.spx_w4_repack(codes(E, H // 8, I), scales(E, H // 128, I), codes(E, H // 8, I),
                            scales(E, H // 128, I), codes(E, I // 8, H), scales(E, I // 128, H), slice_cols=32)
-    f16 = spx.spx_f16_repack(normal(E, I, H), normal(E, I, H), normal(E, H, I))
+    f16 = spx.spx_f16_repack(normal(E, I, H), normal(E, I, H), normal(E, H, I), tc=tc_pack)
     sh = None
     if s.I_s:
         sh = spx.pack_shared(normal(s.I_s, H), normal(s.I_s, H), normal(H, s.I_s),
-                             normal(H) if s.shared_gate else None)
+                             normal(H) if s.shared_gate else None, tc=tc_pack)
     wr = normal(E, H) if s.logits == "router" else None
     torch.cuda.synchronize()
     return dict(w4=w4, f16=f16, shared=sh, w_router=wr)
@@ -411,7 +413,8 @@ def run_mine(args):
     per_cfg = {}
     for name in GATE_CONFIGS:
         c = W.CONFIGS[name]
-        sets = lays if name == "deepseek_v2_lite" else [make_weight_set(c, i, torch, spx) for i in range(NSETS)]
+        sets = lays if name == "deepseek_v2_lite" else [make_weight_set(c, i, torch, spx, tc_pack=True)
+                                                        for i in range(NSETS)]
         per_cfg[name] = layer_figures(c, sets, torch, spx, stream, peak)
         if sets is not lays:
             del sets
@@ -531,6 +534,11 @@ def layer_figures(s, sets, torch, spx, stream, peak, n_batches=10):
                                              "gbs": round(k_bytes / (k_us * 1e-6) / 1e9, 1),
                                              "frac": round(k_bytes / (k_us * 1e-6) / 1e9 / peak, 3)},
                      "timing": f"{n_batches} batches of {chain} layer calls back to back; spread over batches"}
+        if mode == "verify":
+            # the library's automatic choice (tile packs given only for the Qwen and Phi shapes here)
+            tc = sets[0]["f16"].tc is not None and (T >= 25 or T * s.H >= 65536)
+            out[mode]["launches"] = ("routing + tensor-memory launches (gather, tcgen05 gate/up, tcgen05 down, "
+                                     "output)" if tc else "routing + expert launch")
     return out
 
 
@@ -641,8 +649,9 @@ def run_loop(args):
     B.build()
     spx.load()
     s = W.CONFIGS[args.config]
-    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
     draft = args.loop == "draft"
+    launch = 0 if draft else args.verify_launch
+    sets = [make_weight_set(s, i, torch, spx, tc_pack=launch != 1) for i in range(NSETS)]
     if draft:
         apply_formats(s, sets, args, torch, spx)
     if args.tokens:  # another token count than the shape's draft / verify one
@@ -656,12 +665,13 @@ def run_loop(args):
         xk, lk = ("x_d", "lg_d") if draft else ("x_v", "lg_v")
         x = torch.from_numpy(np.ascontiguousarray(inp[xk]).view(np.float16)).cuda()
         lg = torch.from_numpy(inp[lk]).cuda() if lk in inp else torch.empty(T, s.E, device="cuda")
-    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+    ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s, tc=launch == 2)
     r = spx.Routing.empty(T, s.E, s.k)
     out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
     keep = [spx.layer_args(0 if draft else 1, x, s.E, s.k, s.renorm, lg, r, out, ws,
                            w4=st["w4"] if draft else None, f16=None if draft else st["f16"], shared=st["shared"],
-                           w_router=st["w_router"], gguf=st.get("gguf") if draft else None) for st in sets]
+                           w_router=st["w_router"], gguf=st.get("gguf") if draft else None, verify_launch=launch)
+            for st in sets]
     for i in range(args.loop_n):
         spx.spx_moe_layer(keep[i % len(keep)][0])
     torch.cuda.synchronize()
@@ -749,20 +759,21 @@ def run_draft_batch(args):
     B.build()
     spx.load()
     s = W.CONFIGS[args.config]
-    sets = [make_weight_set(s, i, torch, spx) for i in range(NSETS)]
     verify = args.verify_batch
+    launch = args.verify_launch if verify else 0
+    sets = [make_weight_set(s, i, torch, spx, tc_pack=verify and launch != 1) for i in range(NSETS)]
     if not verify:
         apply_formats(s, sets, args, torch, spx)
     peak, peak_src = measured_peaks()
     rows = []
     stream = torch.cuda.Stream()
     mode = 1 if verify else 0
-    for T in ((9, 17, 33) if verify else (1, 2, 4, 8, 16)):
+    for T in ((9, 17, 33, 64) if verify else (1, 2, 4, 8, 16)):
         xs = [torch.from_numpy(np.ascontiguousarray(W.gen_x(s, T, step=i)).view(np.float16)).cuda()
               for i in range(NINPUTS)]
         lgs = [torch.from_numpy(W.gen_logits(s, T, step=i)).cuda() if s.logits != "router"
                else torch.empty(T, s.E, device="cuda") for i in range(NINPUTS)]
-        ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s)
+        ws = spx.new_workspace(T, s.H, s.I, s.E, s.k, s.I_s, tc=launch == 2)
         r = spx.Routing.empty(T, s.E, s.k)
         out = torch.empty(T, s.H, dtype=torch.float16, device="cuda")
         try:
@@ -770,7 +781,7 @@ def run_draft_batch(args):
                                    w4=None if verify else sets[i % NSETS]["w4"],
                                    f16=sets[i % NSETS]["f16"] if verify else None, shared=sets[i % NSETS]["shared"],
                                    w_router=sets[i % NSETS]["w_router"],
-                                   gguf=None if verify else sets[i % NSETS].get("gguf"))
+                                   gguf=None if verify else sets[i % NSETS].get("gguf"), verify_launch=launch)
                     for i in range(NSETS * NINPUTS)]
             nb = []
             for i in range(NINPUTS):
@@ -802,7 +813,9 @@ def run_draft_batch(args):
           else f", GGUF {args.gguf.upper()} gate/up + Q8_0 down experts" if args.gguf else "")
     line = {"metric": ("verify layer with T tokens per call" if verify else
                        "draft layer with T requests' tokens per call") + ", device us per layer",
-            "config": {"workload": f"{s.name} verify, T = 9, 17, 33" if verify else
+            "config": {"workload": f"{s.name} verify, T = 9, 17, 33, 64, " + {
+                0: "automatic launch choice (tensor-memory launches from 25 tokens)", 1: "expert launch",
+                2: "tensor-memory launches"}[launch] if verify else
                        f"{s.name} draft{zp}, T = 1, 2, 4, 8, 16 (one token per request; 8 and 16 on the "
                        f"routing launch + expert launch)"},
             "peak": peak, "peak_source": peak_src, "rows": rows, "steps": args.steps, "warmup": args.warmup}
@@ -1120,7 +1133,10 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="with --loop: tokens per call (default: the shape's)")
     ap.add_argument("--cached", action="store_true", help="cache-aware verify vs plain (prints its own line)")
     ap.add_argument("--draft-batch", action="store_true", help="draft layers at T = 1, 2, 4, 8, 16 (prints its own line)")
-    ap.add_argument("--verify-batch", action="store_true", help="verify layers at T = 9, 17, 33 (prints its own line)")
+    ap.add_argument("--verify-batch", action="store_true",
+                    help="verify layers at T = 9, 17, 33, 64 (prints its own line)")
+    ap.add_argument("--verify-launch", type=int, default=0, choices=(0, 1, 2),
+                    help="--verify-batch: 0 automatic, 1 the expert launch, 2 the tensor-memory launches")
     ap.add_argument("--zeros", action="store_true",
                     help="with --draft-batch or --loop draft: INT4 experts with per-group zero points")
     ap.add_argument("--gguf", choices=["q8_0", "q2_k", "q4_k"],

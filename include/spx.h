@@ -213,6 +213,13 @@ typedef struct {
 typedef struct {
     const void *packed; /* spx_f16_packed_bytes() bytes, from spx_f16_repack() */
     int E, H, I;
+    /* Optional (NULL = none): the same experts in the tile pack of the
+     * tensor-memory launches (spx_f16_tc_repack; I % 64 == 0).  With it (and
+     * the shared expert's, when there is one) a verify layer call can run on
+     * those launches (tcgen05 products, operands by TMA tensor copies): calls
+     * of 25 to 64 tokens or of T * H >= 65536 by default, any call with
+     * spx_layer_args.verify_launch = 2. */
+    const void *tc_packed;
 } spx_f16_experts;
 
 /* GGUF draft experts [P1 Main Findings: GGUF drafts at Q2, Q4 and Q8].
@@ -238,7 +245,7 @@ typedef struct {
  * not a multiple of 256.  Repacked (spx_gguf_repack) into the draft launch's
  * streaming order, 16 columns per slice, followed by the Q8_0 down weights in
  * the expert launch's unit order.  Served by the one-launch draft path (T <=
- * 8) and by the expert launch (more tokens, cache-aware calls). */
+ * 5) and by the expert launch (more tokens, cache-aware calls). */
 enum { SPX_GGUF_Q8_0 = 0, SPX_GGUF_Q2_K = 1, SPX_GGUF_Q4_K = 2 };
 typedef struct {
     const void *packed; /* spx_gguf_packed_bytes() bytes, from spx_gguf_repack() */
@@ -254,6 +261,10 @@ typedef struct {
     const void *packed;      /* spx_shared_packed_bytes(H, I_s) bytes, from spx_shared_repack() */
     const uint16_t *w_sgate; /* nullable; 16-byte aligned */
     int H, I_s;
+    /* Optional (NULL = none): the shared expert in the tile pack of the
+     * tensor-memory launches (spx_shared_tc_repack; I_s % 64 == 0); needed,
+     * with the routed experts' one, by those launches. */
+    const void *tc_packed;
 } spx_shared;
 
 SPX_API size_t spx_w4_packed_bytes(int E, int H, int I, int slice_cols);
@@ -295,6 +306,24 @@ SPX_API int spx_shared_repack(const uint16_t *w_gate, const uint16_t *w_up, cons
 SPX_API int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
                    int E, int H, int I, void *packed, spx_stream_t stream);
 
+/* Tile pack of the tensor-memory verify launches [P1 Key Contributions 4:
+ * expert-wise verification as one dense product per expert].  Per expert:
+ * the gate/up tiles (unit u = 64 columns of I, k-chunk kc = 64 rows of H, in
+ * that order), then the down tiles (128-row block hb of H, k-chunk kc = 64
+ * columns of I); a tile is 128 rows x 64 fp16 (16 KB), row-major.  Gate/up
+ * tile row 32q + i (q < 4) holds gate column 64u + 16q + i for i < 16 and up
+ * column 64u + 16q + i - 16 for i >= 16.  Bytes = E * 3 * I * H * 2 (the
+ * canonical matrices' size); 0 if H % 128 or I % 64. */
+SPX_API size_t spx_f16_tc_packed_bytes(int E, int H, int I);
+/* Canonical [E][I][H], [E][I][H], [E][H][I] fp16 (16-byte aligned) into
+ * `tc_packed` (device, spx_f16_tc_packed_bytes() bytes, 16-byte aligned). */
+SPX_API int spx_f16_tc_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
+                              int E, int H, int I, void *tc_packed, spx_stream_t stream);
+/* The shared expert ([I_s][H], [I_s][H], [H][I_s]): the pack of one expert,
+ * spx_f16_tc_packed_bytes(1, H, I_s) bytes. */
+SPX_API int spx_shared_tc_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down,
+                                 int H, int I_s, void *tc_packed, spx_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Workspace                                                                  */
 /* ------------------------------------------------------------------------ */
@@ -302,6 +331,11 @@ SPX_API int spx_f16_repack(const uint16_t *w_gate, const uint16_t *w_up, const u
  * experts of intermediate size I (E of them, top-k) and a shared expert of
  * intermediate size I_s (0 = none); 0 if the shape is outside the limits. */
 SPX_API size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s);
+/* Bytes of workspace for a verify layer call forced onto the tensor-memory
+ * launches (spx_layer_args.verify_launch = 2) with T tokens; equal to
+ * spx_workspace_size() from T = 25 on and where T * H >= 65536.  0 if the shape cannot take them
+ * (I or I_s not a multiple of 64, or outside the limits). */
+SPX_API size_t spx_workspace_size_tc(int T, int H, int I, int E, int k, int I_s);
 /* Zero a workspace; required once before first use (kernels leave it zeroed
  * again on exit) and after any call whose status word reported an error. */
 SPX_API int spx_workspace_init(void *ws, size_t ws_bytes, spx_stream_t stream);
@@ -397,6 +431,14 @@ typedef struct {
     uint64_t wait_budget_ns;
     /* mode 0 with GGUF draft experts instead of INT4 (w4 must then be NULL). */
     const spx_gguf_experts *gguf;
+    /* mode 1: which launches run the experts.  0 = automatic (the
+     * tensor-memory launches for 25 to 64 tokens, or T * H >= 65536, when the
+     * tile packs are given
+     * and no cache-aware option is set, else the expert launch); 1 = the
+     * expert launch; 2 = the tensor-memory launches (tile packs required, no
+     * cache-aware options, ws_bytes at least spx_workspace_size_tc(); else
+     * SPX_ERR_UNSUPPORTED / SPX_ERR_WORKSPACE). */
+    int verify_launch;
 } spx_layer_args;
 
 /* One layer.  Draft calls with T <= 5 (and no cache-aware options) are one

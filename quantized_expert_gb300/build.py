@@ -25,7 +25,7 @@ VARIANTS = {None: (BUILD, LIB, []),
             "timeline": (os.path.join(BUILD, "timeline"), os.path.join(BUILD, "timeline", "libspx_timeline.so"),
                          ["-DSPX_TIMELINE"])}
 SOURCES = ["spx_route.cu", "spx_engine.cu", "spx_draft.cu", "spx_pack.cu", "spx_api.cu", "spx_noalloc.cu",
-           "spx_plan.cu"]
+           "spx_plan.cu", "spx_tc.cu"]
 # every header of csrc/ and the public one: a change to any rebuilds every source
 HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith(".cuh")) + [os.path.join("..", "..", "include", "spx.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

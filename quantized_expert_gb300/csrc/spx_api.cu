@@ -83,7 +83,7 @@ extern "C" const char *spx_status_string(int st) {
     }
 }
 
-extern "C" int spx_version(void) { return 105; }
+extern "C" int spx_version(void) { return 106; }
 
 extern "C" const char *spx_last_cuda_error(void) {
     return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
@@ -91,12 +91,29 @@ extern "C" const char *spx_last_cuda_error(void) {
 
 static size_t ws_scratch_base(int T, int H) { return ws_order_offset(T, H) + (size_t)kMaxE * 4; }
 
-extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
+static size_t ws_size_core(int T, int H, int I, int E, int k, int I_s) {
     if (T < 1 || H < 1 || T > kMaxT || H > kMaxH || I < 0 || E < 1 || k < 1 || I_s < 0) return 0;
     const size_t base = ws_scratch_base(T, H);
     if (T > kDraftLaunchMaxT || I % 128 || I_s % 16) return base;  // only the draft launch has split-K scratch
     const int nact = E < T * k ? E : T * k;
     return draft_scratch_end(base, T, H, I, I_s, nact);
+}
+// The tensor-memory launches' scratch starts on the first 1024-byte boundary
+// after the routing tables (it is never used together with the draft scratch).
+static size_t ws_tc_offset(int T, int H) { return (ws_scratch_base(T, H) + 1023) / 1024 * 1024; }
+
+extern "C" size_t spx_workspace_size_tc(int T, int H, int I, int E, int k, int I_s) {
+    const size_t core = ws_size_core(T, H, I, E, k, I_s);
+    if (!core || I < 64 || I % 64 || I_s % 64 || H % 128) return 0;
+    const size_t tc = ws_tc_offset(T, H) + tc_scratch_bytes(T, H, I, E, k, I_s);
+    return tc > core ? tc : core;
+}
+
+extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
+    const size_t core = ws_size_core(T, H, I, E, k, I_s);
+    if (!core || !tc_preferred(T, H)) return core;
+    const size_t tc = spx_workspace_size_tc(T, H, I, E, k, I_s);
+    return tc > core ? tc : core;
 }
 
 static TokTable *ws_tables(void *ws, int T, int H) {
@@ -117,14 +134,15 @@ extern "C" int spx_workspace_status(const void *ws, int32_t *host_status, spx_st
 
 static int check_expert_common(const uint16_t *x, int T, int H, int E, int I, int k, const int32_t *offsets,
                                const int32_t *sorted_slots, const int32_t *active, const int32_t *n_active,
-                               void *ws, size_t ws_bytes, int fmt, int S, int I_s = 0) {
+                               void *ws, size_t ws_bytes, int fmt, int S, int I_s = 0, bool tc = false) {
     if (!x || !offsets || !sorted_slots || !active || !n_active) return SPX_ERR_INVALID_ARG;
     if (T < 1 || k < 1 || E < 1 || k > E || H < 1 || I < 1) return SPX_ERR_INVALID_ARG;
     if (T > kMaxT || E > kMaxE || T * k > kMaxSlots || H % 128 || I % 128 || H > kMaxH) return SPX_ERR_UNSUPPORTED;
     if (fmt == 0 && S != 16 && S != 32) return SPX_ERR_UNSUPPORTED;
-    if (!engine_fits(T, H, fmt, S)) return SPX_ERR_UNSUPPORTED;
+    if (!tc && !engine_fits(T, H, fmt, S)) return SPX_ERR_UNSUPPORTED;
     if (!al16(x)) return SPX_ERR_INVALID_ARG;
-    if (!ws || ws_bytes < spx_workspace_size(T, H, I, E, k, I_s) || !al16(ws)) return SPX_ERR_WORKSPACE;
+    const size_t need = tc ? spx_workspace_size_tc(T, H, I, E, k, I_s) : spx_workspace_size(T, H, I, E, k, I_s);
+    if (!ws || ws_bytes < need || !al16(ws)) return SPX_ERR_WORKSPACE;
     return SPX_OK;
 }
 
@@ -240,6 +258,24 @@ extern "C" int spx_moe_verify_fp16(const uint16_t *x, int T, const spx_f16_exper
     return launch_engine(p, s, false);
 }
 
+extern "C" size_t spx_f16_tc_packed_bytes(int E, int H, int I) {
+    if (E < 1 || H < 128 || I < 64 || H % 128 || I % 64 || H > kMaxH || E > kMaxE) return 0;
+    return (size_t)E * tc_tiles(H, I) * 16384;
+}
+
+extern "C" int spx_f16_tc_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down, int E, int H,
+                                 int I, void *tc_packed, spx_stream_t stream) {
+    if (!w_gate || !w_up || !w_down || !tc_packed) return SPX_ERR_INVALID_ARG;
+    if (!al16(w_gate) || !al16(w_up) || !al16(w_down) || !al16(tc_packed)) return SPX_ERR_INVALID_ARG;
+    if (!spx_f16_tc_packed_bytes(E, H, I)) return SPX_ERR_UNSUPPORTED;
+    return launch_tc_repack(w_gate, w_up, w_down, E, H, I, tc_packed, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int spx_shared_tc_repack(const uint16_t *w_gate, const uint16_t *w_up, const uint16_t *w_down, int H,
+                                    int I_s, void *tc_packed, spx_stream_t stream) {
+    return spx_f16_tc_repack(w_gate, w_up, w_down, 1, H, I_s, tc_packed, stream);
+}
+
 static int check_shared(const spx_shared *sh, int H) {
     if (!sh) return SPX_OK;
     if (!sh->packed || sh->H != H || sh->I_s < kF16S || sh->I_s % kF16S) return SPX_ERR_INVALID_ARG;
@@ -320,14 +356,28 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
         routed = static_cast<const uint8_t *>(a->f16->packed);
     }
     const int I_s = a->shared ? a->shared->I_s : 0;
+    const bool cache_aware = a->resident || a->ready;
+    // verify: the tensor-memory launches (canonical FP16 matrices) or the expert launch
+    bool use_tc = false;
+    if (a->mode == 1) {
+        if (a->verify_launch < 0 || a->verify_launch > 2) return SPX_ERR_INVALID_ARG;
+        const spx_shared *sh = a->shared;
+        if (!al16(a->f16->tc_packed) || (sh && !al16(sh->tc_packed))) return SPX_ERR_INVALID_ARG;
+        const bool canon = a->f16->tc_packed && (!sh || sh->tc_packed) && I % 64 == 0 && I_s % 64 == 0;
+        if (a->verify_launch == 2) {
+            if (!canon || cache_aware) return SPX_ERR_UNSUPPORTED;
+            use_tc = true;
+        } else if (a->verify_launch == 0) {
+            use_tc = canon && !cache_aware && tc_preferred(T, H);
+        }
+    }
     st = check_expert_common(a->x, T, H, E, I, k, a->offsets, a->sorted_slots, a->active, a->n_active, a->ws,
-                             a->ws_bytes, a->mode == 0 ? 0 : 1, S, I_s);
+                             a->ws_bytes, a->mode == 0 ? 0 : 1, S, I_s, use_tc);
     if (st) return st;
     st = check_shared(a->shared, H);
     if (st) return st;
     if (reinterpret_cast<uintptr_t>(a->out) & 7) return SPX_ERR_INVALID_ARG;
     const bool timed = a->ev_experts_begin || a->ev_experts_end;
-    const bool cache_aware = a->resident || a->ready;
     const uint64_t budget = a->wait_budget_ns ? a->wait_budget_ns : kWaitBudgetNs;
 
     const bool zeros = a->mode == 0 && !gguf && a->w4->zeros;
@@ -413,6 +463,37 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
     rp.hdr = static_cast<WsHeader *>(a->ws);
     st = launch_route(rp, s, !timed);
     if (st) return st;
+
+    if (use_tc) {
+        TcArgs t{};
+        t.x = reinterpret_cast<const __half *>(a->x);
+        t.T = T;
+        t.H = H;
+        t.E = E;
+        t.I = I;
+        t.k = k;
+        t.I_s = I_s;
+        t.routed_tc = a->f16->tc_packed;
+        if (a->shared) {
+            t.shared_tc = a->shared->tc_packed;
+            t.w_sgate = reinterpret_cast<const __half *>(a->shared->w_sgate);
+        }
+        t.active = a->active;
+        t.n_active = a->n_active;
+        t.tables = ws_tables(a->ws, T, H);
+        t.scratch = static_cast<uint8_t *>(a->ws) + ws_tc_offset(T, H);
+        t.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
+        t.out = reinterpret_cast<__half *>(a->out);
+        t.hdr = static_cast<WsHeader *>(a->ws);
+        t.wait_budget_ns = budget;
+        if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
+            return SPX_ERR_CUDA;
+        st = launch_tc_verify(t, s, !timed);
+        if (st) return st;
+        if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
+            return SPX_ERR_CUDA;
+        return SPX_OK;
+    }
 
     EngineParams p = base_params(a->x, T, H, a->ws);
     p.routed = routed;

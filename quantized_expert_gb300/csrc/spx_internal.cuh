@@ -39,7 +39,7 @@ static_assert(offsetof(WsHeader, timeout_site) - offsetof(WsHeader, status) == 3
               "a wait that holds &status records its site three words on");
 // Bounded waits that give up record their site next to the status word.
 enum : int32_t { SITE_ALL_SYNC = 1, SITE_FILL = 2, SITE_HSLICE = 3, SITE_GATE = 4, SITE_ROUTING = 5, SITE_SLOT = 6,
-                 SITE_STAGE = 7, SITE_POLLER = 8, SITE_ENGINE = 9 };
+                 SITE_STAGE = 7, SITE_POLLER = 8, SITE_ENGINE = 9, SITE_TC = 10 };
 #if defined(__CUDACC__)
 __device__ __forceinline__ void record_timeout(int32_t *status, int32_t site) {
     atomicCAS(status, 0, (int32_t)SPX_ERR_TIMEOUT);
@@ -454,6 +454,40 @@ int launch_router_logits(const __half *x, const __half *wr, int T, int H, int E,
                          bool pdl);
 int launch_tables(const int32_t *offsets, const int32_t *sorted_slots, const int32_t *active,
                   const int32_t *n_active, int T, int k, int E, TokTable *tables, cudaStream_t s);
+
+// Verify experts on the tensor-memory launches (spx_tc.cu): FP16 experts in
+// that path's tile pack, a routing launch's token tables, the layer's fp32
+// accumulator.
+struct TcArgs {
+    const __half *x;
+    int T, H, E, I, k, I_s;
+    const void *routed_tc;                                        // spx_f16_tc_repack pack of the routed experts
+    const void *shared_tc;                                        // the shared expert's, or null
+    const __half *w_sgate;                                        // nullable
+    const int32_t *active, *n_active;
+    const TokTable *tables;
+    void *scratch;  // tc_scratch_bytes(), 1024-byte aligned
+    float *acc;     // [T][H], zero on entry and on exit
+    __half *out;
+    WsHeader *hdr;
+    uint64_t wait_budget_ns;
+};
+// Verify calls take the tensor-memory launches (when the experts' tile packs
+// are given) from kTcMinT tokens, or from kTcMinTH activation elements (T x H):
+// the expert launch keeps every activation row in shared memory, so its
+// weight ring shrinks as T x H grows, while the tensor-memory launches stream
+// activation tiles.  Measured on GB300: at 9 and 17 tokens the expert launch
+// is as fast or faster on the 2048-wide shapes (T x H <= 34816), at 17 tokens
+// of the 4096-wide one (69632) it is 30% slower, at 33 tokens slower on all.
+constexpr int kTcMinT = 25;
+constexpr long long kTcMinTH = 65536;
+inline bool tc_preferred(int T, int H) { return T >= kTcMinT || (long long)T * H >= kTcMinTH; }
+size_t tc_scratch_bytes(int T, int H, int I, int E, int k, int I_s);
+size_t tc_tiles(int H, int I);  // 16 KB tiles of one expert's pack
+int launch_tc_repack(const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int E, int H, int I, void *dst,
+                     cudaStream_t s);
+int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl);
+int tc_preload();
 
 // -------------------------------------------------------- host helpers --
 int device_sm_count();

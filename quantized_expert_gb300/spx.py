@@ -35,7 +35,8 @@ class W4Experts(C.Structure):
 
 
 class F16Experts(C.Structure):
-    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int)]
+    _fields_ = [("packed", C.c_void_p), ("E", C.c_int), ("H", C.c_int), ("I", C.c_int),
+                ("tc_packed", C.c_void_p)]
 
 
 class GgufExperts(C.Structure):
@@ -43,7 +44,8 @@ class GgufExperts(C.Structure):
 
 
 class Shared(C.Structure):
-    _fields_ = [("packed", C.c_void_p), ("w_sgate", C.c_void_p), ("H", C.c_int), ("I_s", C.c_int)]
+    _fields_ = [("packed", C.c_void_p), ("w_sgate", C.c_void_p), ("H", C.c_int), ("I_s", C.c_int),
+                ("tc_packed", C.c_void_p)]
 
 
 class PlanCfg(C.Structure):
@@ -61,7 +63,7 @@ class LayerArgs(C.Structure):
                 ("n_active", C.c_void_p), ("out", C.c_void_p), ("ws", C.c_void_p), ("ws_bytes", C.c_size_t),
                 ("ev_experts_begin", C.c_void_p), ("ev_experts_end", C.c_void_p),
                 ("resident", C.c_void_p), ("ready", C.c_void_p), ("wait_budget_ns", C.c_uint64),
-                ("gguf", C.POINTER(GgufExperts))]
+                ("gguf", C.POINTER(GgufExperts)), ("verify_launch", C.c_int)]
 
 
 _SIGS = {
@@ -84,6 +86,10 @@ _SIGS = {
     "spx_w4_zeros_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_f16_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_workspace_size": (C.c_size_t, [C.c_int] * 6),
+    "spx_workspace_size_tc": (C.c_size_t, [C.c_int] * 6),
+    "spx_f16_tc_packed_bytes": (C.c_size_t, [C.c_int] * 3),
+    "spx_f16_tc_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p, C.c_void_p]),
+    "spx_shared_tc_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 2 + [C.c_void_p, C.c_void_p]),
     "spx_shared_packed_bytes": (C.c_size_t, [C.c_int, C.c_int]),
     "spx_shared_repack": (C.c_int, [C.c_void_p] * 3 + [C.c_int, C.c_int, C.c_void_p, C.c_void_p]),
     "spx_workspace_init": (C.c_int, [C.c_void_p, C.c_size_t, C.c_void_p]),
@@ -168,9 +174,10 @@ def spx_workspace_size(T: int, H: int, I: int = 0, E: int = 1, k: int = 1, I_s: 
 
 
 def new_workspace(T: int, H: int, I: int = 0, E: int = 1, k: int = 1, I_s: int = 0, device="cuda",
-                  stream=None) -> torch.Tensor:
-    """Allocate (through torch) and zero a workspace for up to T tokens."""
-    n = spx_workspace_size(T, H, I, E, k, I_s)
+                  stream=None, tc: bool = False) -> torch.Tensor:
+    """Allocate (through torch) and zero a workspace for up to T tokens
+    (tc: for verify calls forced onto the tensor-memory launches)."""
+    n = (load().spx_workspace_size_tc if tc else spx_workspace_size)(T, H, I, E, k, I_s)
     if n == 0:
         raise SpxError(SPX_ERR_UNSUPPORTED, "spx_workspace_size")
     ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -251,9 +258,10 @@ class PackedF16:
     E: int
     H: int
     I: int
+    tc: torch.Tensor | None = None  # tile pack of the tensor-memory verify launches
 
     def cstruct(self) -> F16Experts:
-        return F16Experts(self.buf.data_ptr(), self.E, self.H, self.I)
+        return F16Experts(self.buf.data_ptr(), self.E, self.H, self.I, _p(self.tc))
 
 
 @dataclass
@@ -262,9 +270,10 @@ class PackedShared:
     w_sgate: torch.Tensor | None
     H: int
     I_s: int
+    tc: torch.Tensor | None = None  # tile pack of the tensor-memory verify launches
 
     def cstruct(self) -> Shared:
-        return Shared(self.buf.data_ptr(), _p(self.w_sgate), self.H, self.I_s)
+        return Shared(self.buf.data_ptr(), _p(self.w_sgate), self.H, self.I_s, _p(self.tc))
 
 
 def spx_w4_repack(qw_gate, s_gate, qw_up, s_up, qw_down, s_down, slice_cols=32, stream=None) -> PackedW4:
@@ -307,19 +316,34 @@ def spx_gguf_repack(w_gate, w_up, w_down, gate_up_type=SPX_GGUF_Q8_0, stream=Non
     return PackedGguf(buf, E, H, I, gate_up_type)
 
 
-def spx_f16_repack(w_gate, w_up, w_down, stream=None) -> PackedF16:
-    """Canonical [E][I][H], [E][I][H], [E][H][I] fp16 -> packed units."""
+def spx_f16_tc_repack(w_gate, w_up, w_down, stream=None) -> torch.Tensor:
+    """Canonical [E][I][H], [E][I][H], [E][H][I] fp16 -> the tile pack of the
+    tensor-memory verify launches (uint8 tensor)."""
+    E, I, H = w_gate.shape
+    n = load().spx_f16_tc_packed_bytes(E, H, I)
+    if n == 0:
+        raise SpxError(SPX_ERR_UNSUPPORTED, "spx_f16_tc_packed_bytes")
+    buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
+    _chk(load().spx_f16_tc_repack(_p(w_gate), _p(w_up), _p(w_down), E, H, I, _p(buf), _stream(stream)),
+         "spx_f16_tc_repack")
+    return buf
+
+
+def spx_f16_repack(w_gate, w_up, w_down, stream=None, tc=False) -> PackedF16:
+    """Canonical [E][I][H], [E][I][H], [E][H][I] fp16 -> packed units (tc: also
+    the tile pack of the tensor-memory verify launches)."""
     E, I, H = w_gate.shape
     n = load().spx_f16_packed_bytes(E, H, I)
     if n == 0:
         raise SpxError(SPX_ERR_UNSUPPORTED, "spx_f16_packed_bytes")
     buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
     _chk(load().spx_f16_repack(_p(w_gate), _p(w_up), _p(w_down), E, H, I, _p(buf), _stream(stream)), "spx_f16_repack")
-    return PackedF16(buf, E, H, I)
+    return PackedF16(buf, E, H, I, spx_f16_tc_repack(w_gate, w_up, w_down, stream) if tc else None)
 
 
-def pack_shared(w_gate, w_up, w_down, w_sgate=None, stream=None) -> PackedShared:
-    """Shared expert [I_s][H], [I_s][H], [H][I_s] fp16 -> packed (spx_shared_repack)."""
+def pack_shared(w_gate, w_up, w_down, w_sgate=None, stream=None, tc=False) -> PackedShared:
+    """Shared expert [I_s][H], [I_s][H], [H][I_s] fp16 -> packed (spx_shared_repack);
+    tc as spx_f16_repack."""
     I_s, H = w_gate.shape
     n = load().spx_shared_packed_bytes(H, I_s)
     if n == 0:
@@ -327,7 +351,8 @@ def pack_shared(w_gate, w_up, w_down, w_sgate=None, stream=None) -> PackedShared
     buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
     _chk(load().spx_shared_repack(_p(w_gate), _p(w_up), _p(w_down), H, I_s, _p(buf), _stream(stream)),
          "spx_shared_repack")
-    return PackedShared(buf, w_sgate, H, I_s)
+    return PackedShared(buf, w_sgate, H, I_s, spx_f16_tc_repack(w_gate[None], w_up[None], w_down[None], stream)
+                        if tc else None)
 
 
 def spx_moe_draft_w4a16(x, w: PackedW4, k, offsets, sorted_slots, active, n_active, y_sorted, ws, stream=None):
@@ -386,12 +411,15 @@ class Routing:
 
 def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: PackedW4 | None = None,
                f16: PackedF16 | None = None, shared: PackedShared | None = None, w_router=None, elb=None,
-               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0, gguf: PackedGguf | None = None):
+               layer=0, events=None, resident=None, ready=None, wait_budget_ns=0, gguf: PackedGguf | None = None,
+               verify_launch=0):
     """Build (and keep alive) the argument block of one spx_moe_layer call.
     Draft experts are INT4 (w4) or GGUF (gguf), one of the two.
     resident (uint8 [E]) and ready (int32/uint32 [E]) are the optional
     cache-aware expert order and ready flags; wait_budget_ns bounds every
-    device-side wait (0 = the library default)."""
+    device-side wait (0 = the library default).  verify_launch: 0 automatic,
+    1 the expert launch, 2 the tensor-memory launches (needs the tile packs
+    on f16 and shared)."""
     T, H = x.shape
     keep = []
     a = LayerArgs()
@@ -423,6 +451,7 @@ def layer_args(mode, x, E, k, renorm, logits, routing: Routing, out, ws, w4: Pac
         a.ev_experts_begin, a.ev_experts_end = events[0].cuda_event, events[1].cuda_event
         keep.append(events)
     a.resident, a.ready, a.wait_budget_ns = _p(resident), _p(ready), int(wait_budget_ns)
+    a.verify_launch = int(verify_launch)
     return a, keep
 
 

@@ -83,7 +83,8 @@ class Layer:
         if self.shared_host is not None:
             sh = self.shared_host
             self.shared = spx.pack_shared(dev_f16(sh["w_gate"]), dev_f16(sh["w_up"]), dev_f16(sh["w_down"]),
-                                          dev_f16(sh["w_sgate"]) if "w_sgate" in sh else None)
+                                          dev_f16(sh["w_sgate"]) if "w_sgate" in sh else None,
+                                          tc=s.I_s % 64 == 0 and s.H % 128 == 0)
         self.w_router = dev_f16(self.router_host) if self.router_host is not None else None
 
     def _pack_w4(self, S):
@@ -133,7 +134,8 @@ class Layer:
         wd = np.zeros((E, H, I), np.uint16)
         for e, ex in self.f16_host.items():
             wg[e], wu[e], wd[e] = ex["w_gate"], ex["w_up"], ex["w_down"]
-        p = spx.spx_f16_repack(dev_f16(wg), dev_f16(wu), dev_f16(wd))
+        # the tile pack of the tensor-memory verify launches where the shape allows one
+        p = spx.spx_f16_repack(dev_f16(wg), dev_f16(wu), dev_f16(wd), tc=I % 64 == 0 and H % 128 == 0)
         torch.cuda.synchronize()
         return p
 

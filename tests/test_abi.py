@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_sizes_and_strings(lib):
     from quantized_expert_gb300 import spx
-    assert spx.spx_version() == 105
+    assert spx.spx_version() == 106
     assert spx.status_string(0) == "ok"
     assert "timed out" in spx.status_string(-5)
     # INT4 unit = 49*H*S/32 bytes; down scales copied once per expert
@@ -51,6 +51,19 @@ def test_sizes_and_strings(lib):
     # the draft launch (up to 5 tokens) adds its split-K scratch
     assert lib.spx_workspace_size(1, 2048, 1408, 64, 6, 2816) > lib.spx_workspace_size(1, 2048, 0, 64, 6, 0)
     assert lib.spx_workspace_size(65, 2048, 1408, 64, 6, 0) == 0
+    # tile pack of the tensor-memory verify launches: the canonical matrices' size, 16 KB tiles
+    assert lib.spx_f16_tc_packed_bytes(64, 2048, 1408) == 64 * 3 * 1408 * 2048 * 2
+    assert lib.spx_f16_tc_packed_bytes(16, 4096, 6400) == 16 * 3 * 6400 * 4096 * 2
+    assert lib.spx_f16_tc_packed_bytes(1, 2048, 1400) == 0 and lib.spx_f16_tc_packed_bytes(1, 2112, 1408) == 0
+    # their scratch: T=33 (and T*H >= 65536) calls get it by default, a forced T=17 call asks for it
+    ws17 = lib.spx_workspace_size(17, 2048, 1408, 64, 6, 2816)
+    ws17tc = lib.spx_workspace_size_tc(17, 2048, 1408, 64, 6, 2816)
+    nslot, npm = 64 + 1, 32
+    assert ws17tc >= ws17 + nslot * npm * (2048 + 2816) * 2
+    assert lib.spx_workspace_size(17, 4096, 6400, 16, 2, 0) == lib.spx_workspace_size_tc(17, 4096, 6400, 16, 2, 0)
+    assert lib.spx_workspace_size(33, 2048, 1408, 64, 6, 2816) == lib.spx_workspace_size_tc(33, 2048, 1408, 64, 6,
+                                                                                           2816)
+    assert lib.spx_workspace_size_tc(17, 2048, 1400, 64, 6, 0) == 0
 
 
 def test_validation_before_any_launch(lib):
