@@ -109,6 +109,12 @@ extern "C" size_t spx_workspace_size_tc(int T, int H, int I, int E, int k, int I
     return tc > core ? tc : core;
 }
 
+size_t spx::workspace_bytes(int T, int H, int I, int E, int k, int I_s, int launch) {
+    if (launch == 1) return ws_size_core(T, H, I, E, k, I_s);
+    if (launch == 2) return spx_workspace_size_tc(T, H, I, E, k, I_s);
+    return spx_workspace_size(T, H, I, E, k, I_s);
+}
+
 extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
     const size_t core = ws_size_core(T, H, I, E, k, I_s);
     if (!core || !tc_preferred(T, H)) return core;
@@ -141,7 +147,7 @@ static int check_expert_common(const uint16_t *x, int T, int H, int E, int I, in
     if (fmt == 0 && S != 16 && S != 32) return SPX_ERR_UNSUPPORTED;
     if (!tc && !engine_fits(T, H, fmt, S)) return SPX_ERR_UNSUPPORTED;
     if (!al16(x)) return SPX_ERR_INVALID_ARG;
-    const size_t need = tc ? spx_workspace_size_tc(T, H, I, E, k, I_s) : spx_workspace_size(T, H, I, E, k, I_s);
+    const size_t need = workspace_bytes(T, H, I, E, k, I_s, tc ? 2 : 1);
     if (!ws || ws_bytes < need || !al16(ws)) return SPX_ERR_WORKSPACE;
     return SPX_OK;
 }

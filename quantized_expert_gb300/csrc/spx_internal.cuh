@@ -476,12 +476,18 @@ struct TcArgs {
 // are given) from kTcMinT tokens, or from kTcMinTH activation elements (T x H):
 // the expert launch keeps every activation row in shared memory, so its
 // weight ring shrinks as T x H grows, while the tensor-memory launches stream
-// activation tiles.  Measured on GB300: at 9 and 17 tokens the expert launch
-// is as fast or faster on the 2048-wide shapes (T x H <= 34816), at 17 tokens
-// of the 4096-wide one (69632) it is 30% slower, at 33 tokens slower on all.
-constexpr int kTcMinT = 25;
+// activation tiles.  Measured on GB300 (DeepSeek-, Qwen- and Phi-shaped
+// layers): at 9 tokens the expert launch is 8-10% faster on the 2048-wide
+// shapes and equal on the 4096-wide one; at 17 tokens the tensor-memory
+// launches are equal or faster on all three (Phi-shaped 24% faster); from 33
+// tokens faster on all.
+constexpr int kTcMinT = 17;
 constexpr long long kTcMinTH = 65536;
 inline bool tc_preferred(int T, int H) { return T >= kTcMinT || (long long)T * H >= kTcMinTH; }
+// Workspace bytes of a call: launch 0 = spx_workspace_size (room for whichever
+// launches the automatic choice may take), 1 = without the tensor-memory
+// launches' scratch, 2 = spx_workspace_size_tc.
+size_t workspace_bytes(int T, int H, int I, int E, int k, int I_s, int launch);
 size_t tc_scratch_bytes(int T, int H, int I, int E, int k, int I_s);
 size_t tc_tiles(int H, int I);  // 16 KB tiles of one expert's pack
 int launch_tc_repack(const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int E, int H, int I, void *dst,

@@ -21,9 +21,11 @@
 namespace spx {
 
 // Scratch of spx_moe_layer_noalloc: 1 MiB, held by every GPU that loads the
-// library until the process exits.  Enough for any layer whose
-// spx_workspace_size(T, H, I, E, k, I_s) is at most 1 MiB (for example the
-// DeepSeek-V2-Lite-shaped layer at T = 1 and at T = 17).
+// library until the process exits.  Enough for any layer whose workspace
+// without the tensor-memory verify launches' scratch is at most 1 MiB (for
+// example the DeepSeek-V2-Lite-shaped layer at T = 1 and at T = 17); a verify
+// call whose automatic choice would take those launches takes the expert
+// launch here when their scratch does not fit.
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -83,13 +85,19 @@ extern "C" int spx_moe_layer_noalloc(const spx_layer_args *args, spx_stream_t st
     const int I = args->mode != 0 ? (args->f16 ? args->f16->I : 0)
                                   : args->gguf ? args->gguf->I : (args->w4 ? args->w4->I : 0);
     const int I_s = args->shared ? args->shared->I_s : 0;
-    const size_t need = spx_workspace_size(args->T, args->H, I, args->E, args->k, I_s);
+    spx_layer_args a = *args;
+    const int launch = args->mode == 1 ? args->verify_launch : 1;
+    size_t need = workspace_bytes(args->T, args->H, I, args->E, args->k, I_s, launch);
+    if (launch == 0 && need > kNoAllocScratchBytes) {
+        // the tensor-memory verify launches' scratch does not fit: the expert launch serves the call
+        a.verify_launch = 1;
+        need = workspace_bytes(args->T, args->H, I, args->E, args->k, I_s, 1);
+    }
     if (need == 0) return SPX_ERR_UNSUPPORTED;
     if (need > kNoAllocScratchBytes) return SPX_ERR_WORKSPACE;  // T*H beyond the fixed scratch
     void *scratch = nullptr;
     int st = noalloc_scratch(&scratch);
     if (st) return st;
-    spx_layer_args a = *args;
     a.ws = scratch;
     a.ws_bytes = kNoAllocScratchBytes;
     // The array keeps the previous call's contents: the layer call clears the

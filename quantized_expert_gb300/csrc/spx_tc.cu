@@ -11,8 +11,8 @@
 // grow with the token count:
 //
 //   gather launch   x rows of each active expert (and every token for the
-//                   shared expert) copied into one zero-padded block per
-//                   expert slot; the shared-expert gate per token.
+//                   shared expert) copied into one block of rows per expert
+//                   slot; the shared-expert gate per token.
 //   gate/up launch  unit = (slot, 64 columns of I): D[128 x Np] = A . B^T
 //                   with A = 64 gate rows and 64 up rows of the expert
 //                   ([I][H], k = H), B = the slot's Np token rows; epilogue
@@ -189,7 +189,7 @@ struct TcUnit {
     int e;     // expert id (routed) or -1
     int n;     // tokens of the slot
     int pos;   // gate/up: first column of I; down: first row of H
-    int kc0;   // first k stage (a shared-expert down unit covers one piece of I_s)
+    int kc0;   // first k stage (a down unit covers one piece of its k range)
     int nk;    // k stages
 };
 
@@ -197,101 +197,113 @@ struct TcUnit {
 __device__ __forceinline__ int tc_gu_count(const TcParams &p, int nact) {
     return (p.has_shared ? p.I_s / kTcKc : 0) + nact * (p.I / kTcKc);
 }
-// Pieces of I_s per shared-expert down unit: its k range is cut to the routed
-// units' (I) so that no block draws a unit several times longer than the rest;
-// the pieces' partial sums meet in the accumulator.
-__device__ __forceinline__ int tc_shared_pieces(const TcParams &p) { return (p.I_s + p.I - 1) / p.I; }
-// down units: the shared expert's (H/128 blocks x pieces) first, then every active expert's H/128
+// Down units cut their k range (I or I_s) into pieces of at most min(I, H)/64
+// stages, as equal as possible: no unit is longer than a gate/up unit, so the
+// last round of units on the SMs stays short; the pieces' partial sums meet in
+// the accumulator.
+struct TcSplit {
+    int pieces, len;  // pieces per 128-row block, k stages per piece (the last may be shorter)
+};
+__device__ __forceinline__ TcSplit tc_split(const TcParams &p, int ks) {
+    const int lim = min(p.I, p.H) / kTcKc;  // >= 1: I and H are multiples of 64
+    TcSplit d;
+    d.pieces = ks > 0 ? (ks + lim - 1) / lim : 0;
+    d.len = ks > 0 ? (ks + d.pieces - 1) / d.pieces : 0;
+    return d;
+}
+// down units: the shared expert's (H/128 blocks x pieces) first, then every active expert's
 __device__ __forceinline__ int tc_dn_count(const TcParams &p, int nact) {
-    return (p.has_shared ? (p.H / 128) * tc_shared_pieces(p) : 0) + nact * (p.H / 128);
+    const int sh = p.has_shared ? (p.H / 128) * tc_split(p, p.I_s / kTcKc).pieces : 0;
+    return sh + nact * (p.H / 128) * tc_split(p, p.I / kTcKc).pieces;
 }
 // slot_e / slot_n: expert and token count of every slot, staged in shared
-// memory once per block (slot 0, the shared expert: -1 and T).
+// memory once per block (slot 0, the shared expert: -1 and T).  A unit with
+// t.n == 0 or t.nk == 0 is skipped by every role alike.
 template <bool DOWN>
 __device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *slot_e, const int *slot_n) {
     TcUnit t;
-    const int pieces = DOWN ? tc_shared_pieces(p) : 1;
-    const int per_s = DOWN ? (p.H / 128) * pieces : p.I_s / kTcKc;
-    const int ns = p.has_shared ? per_s : 0;
-    if (u < ns) {
-        t.slot = 0;
-        t.e = -1;
-        t.n = p.T;
-        if (DOWN) {
-            const int hb = u / pieces, pc = u - hb * pieces;
-            const int kpp = p.I / kTcKc, ks = p.I_s / kTcKc;  // k stages per piece, in all
-            t.pos = 128 * hb;
-            t.kc0 = pc * kpp;
-            t.nk = min(kpp, ks - t.kc0);
-        } else {
-            t.pos = kTcKc * u;
-            t.kc0 = 0;
-            t.nk = p.H / kTcKc;
+    if (!DOWN) {
+        const int ns = p.has_shared ? p.I_s / kTcKc : 0;
+        const int per = p.I / kTcKc;
+        int a = -1, v = u;
+        if (u >= ns) {
+            a = (u - ns) / per;
+            v = u - ns - a * per;
         }
+        t.slot = 1 + a;
+        t.e = a < 0 ? -1 : slot_e[1 + a];
+        t.n = a < 0 ? p.T : slot_n[1 + a];
+        t.pos = kTcKc * v;
+        t.kc0 = 0;
+        t.nk = p.H / kTcKc;
         return t;
     }
-    u -= ns;
-    const int per = DOWN ? p.H / 128 : p.I / kTcKc;
-    const int a = u / per;
+    const TcSplit ds = tc_split(p, p.I_s / kTcKc), dr = tc_split(p, p.I / kTcKc);
+    const int ns = p.has_shared ? (p.H / 128) * ds.pieces : 0;
+    int a = -1, v = u;
+    if (u >= ns) {
+        const int per = (p.H / 128) * dr.pieces;
+        a = (u - ns) / per;
+        v = u - ns - a * per;
+    }
+    const TcSplit d = a < 0 ? ds : dr;
+    const int ks = (a < 0 ? p.I_s : p.I) / kTcKc;
+    const int hb = v / d.pieces, pc = v - hb * d.pieces;
     t.slot = 1 + a;
-    t.e = slot_e[1 + a];
-    t.n = slot_n[1 + a];
-    t.pos = (u - a * per) * (DOWN ? 128 : kTcKc);
-    t.kc0 = 0;
-    t.nk = DOWN ? p.I / kTcKc : p.H / kTcKc;
+    t.e = a < 0 ? -1 : slot_e[1 + a];
+    t.n = a < 0 ? p.T : slot_n[1 + a];
+    t.pos = 128 * hb;
+    t.kc0 = pc * d.len;
+    t.nk = max(0, min(d.len, ks - t.kc0));
     return t;
 }
 
 // ------------------------------------------------------ gather launch --
-__global__ void __launch_bounds__(256) tc_gather_kernel(const __grid_constant__ TcParams p) {
+// One warp per (slot, row) with slot < 1 + min(E, T*k) and row < T, then one
+// warp per token for the shared-expert gate.  Only a slot's n real rows are
+// written: the rows up to its 16-row tile hold whatever the workspace held, as
+// a token row of the product only ever reaches that token's own output column,
+// which the epilogues leave out.
+__global__ void __launch_bounds__(256) tc_gather_kernel(const __grid_constant__ TcParams p, int nslot) {
     griddep_launch_dependents();
     griddep_wait();
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
     const int nact = tc_nact(p);
-    const int hv = p.H / 8;  // 16-byte pieces per row
-    for (int slot = blockIdx.x; slot <= nact; slot += gridDim.x) {
-        if (slot == 0 && !p.has_shared) continue;
-        int n = p.T;
-        const TokEntry *ent = nullptr;
+    if (warp < nslot * p.T) {
+        const int slot = warp / p.T, r = warp - slot * p.T;
+        if (slot > nact || (slot == 0 && !p.has_shared)) return;
+        int tok = r;
         if (slot > 0) {
             int e = p.active[slot - 1];
             e = (e < 0 || e >= p.E) ? 0 : e;
-            n = p.tables[e].n;
+            int n = p.tables[e].n;
             n = (n < 0 || n > p.T) ? 0 : n;
-            ent = p.tables[e].e;
+            if (r >= n) return;
+            tok = p.tables[e].e[r].tok;
+            tok = (tok < 0 || tok >= p.T) ? 0 : tok;
         }
-        const int np = (n + 15) & ~15;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.xs + (size_t)slot * p.npm * p.H);
-        for (int idx = threadIdx.x; idx < np * hv; idx += blockDim.x) {
-            const int r = idx / hv, c = idx - r * hv;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < n) {
-                int tok = ent ? ent[r].tok : r;
-                tok = (tok < 0 || tok >= p.T) ? 0 : tok;
-                v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.H) + c);
-            }
-            dst[idx] = v;
-        }
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.H);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.xs + ((size_t)slot * p.npm + r) * p.H);
+        for (int c = lane; c < p.H / 8; c += 32) dst[c] = __ldg(src + c);
+        return;
     }
     // shared-expert gate per token: gamma = 1 / (1 + exp(-x . w_sgate)), else 1
-    if (blockIdx.x == gridDim.x - 1) {
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int t = warp; t < p.T; t += blockDim.x / 32) {
-            float g = 1.0f;
-            if (p.w_sgate) {
-                float z = 0.f;
-                for (int hh = lane * 2; hh < p.H; hh += 64) {
-                    const float2 xv = __half22float2(*reinterpret_cast<const __half2 *>(p.x + (size_t)t * p.H + hh));
-                    const float2 wv = __half22float2(*reinterpret_cast<const __half2 *>(p.w_sgate + hh));
-                    z = fmaf(xv.x, wv.x, z);
-                    z = fmaf(xv.y, wv.y, z);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-                g = 1.0f / (1.0f + expf(-z));
-            }
-            if (lane == 0) p.gam[t] = g;
+    const int t = warp - nslot * p.T;
+    if (t >= p.T) return;
+    float g = 1.0f;
+    if (p.w_sgate) {
+        float z = 0.f;
+        for (int hh = lane * 2; hh < p.H; hh += 64) {
+            const float2 xv = __half22float2(*reinterpret_cast<const __half2 *>(p.x + (size_t)t * p.H + hh));
+            const float2 wv = __half22float2(*reinterpret_cast<const __half2 *>(p.w_sgate + hh));
+            z = fmaf(xv.x, wv.x, z);
+            z = fmaf(xv.y, wv.y, z);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        g = 1.0f / (1.0f + expf(-z));
     }
+    if (lane == 0) p.gam[t] = g;
 }
 
 // ------------------------------------------------- product launches ----
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         bool ok = true;
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
             const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n);
-            if (t.n == 0) continue;
+            if (t.n == 0 || t.nk == 0) continue;
             const int nb = (t.n + 15) >> 4;
             const uint32_t bytes = (uint32_t)kTcABytes + (uint32_t)nb * 16 * kTcKc * 2;
             const int brow = t.slot * p.npm;
@@ -396,7 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         bool ok = true;
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
             const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n);
-            if (t.n == 0) continue;
+            if (t.n == 0 || t.nk == 0) continue;
             const int b = (int)(uc & 1);
             if (!tc_wait(&acce[b], ((uc >> 1) & 1) ^ 1, abort_flag, p)) break;
             tc_fence_after();
@@ -429,7 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         uint32_t uc = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
             const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n);
-            if (t.n == 0) continue;
+            if (t.n == 0 || t.nk == 0) continue;
             const int b = (int)(uc & 1);
             if (!tc_wait(&accf[b], (uc >> 1) & 1, abort_flag, p)) break;
             tc_fence_after();
@@ -674,8 +686,9 @@ int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl) {
 
     const int nsm = device_sm_count();
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = tc_config(dim3(nslot < 2 * nsm ? nslot : 2 * nsm), 256, 0, s, pdl, attr);
-    int st = record_launch(cudaLaunchKernelEx(&cfg, tc_gather_kernel, p));
+    const int gwarps = (nslot + 1) * T;  // slot rows, then the gate's tokens
+    cudaLaunchConfig_t cfg = tc_config(dim3((gwarps + 7) / 8), 256, 0, s, pdl, attr);
+    int st = record_launch(cudaLaunchKernelEx(&cfg, tc_gather_kernel, p, nslot));
     if (st) return st;
     cfg = tc_config(dim3(nsm), kTcThreads, kTcSmem, s, true, attr);
     st = record_launch(cudaLaunchKernelEx(&cfg, tc_kernel<false>, p));

@@ -90,7 +90,7 @@ def test_tc_verify_invalid_calls():
     misaligned pack is an invalid argument."""
     spx, gh = _spx(), _gh()
     s = W.scaled(W.CONFIGS["deepseek_v2_lite"], I=256, E=16, I_s=512)
-    T = 17
+    T = 9  # below the automatic choice: spx_workspace_size leaves the tensor-memory scratch out
     x = W.gen_x(s, T, step=270)
     lay = gh.Layer(s, needed=list(range(s.E)), draft=False, verify=True)
     routing = spx.Routing.empty(T, s.E, s.k)
