@@ -197,30 +197,50 @@ struct TcUnit {
 __device__ __forceinline__ int tc_gu_count(const TcParams &p, int nact) {
     return (p.has_shared ? p.I_s / kTcKc : 0) + nact * (p.I / kTcKc);
 }
-// Down units cut their k range (I or I_s) into pieces of at most min(I, H)/64
-// stages, as equal as possible: no unit is longer than a gate/up unit, so the
-// last round of units on the SMs stays short; the pieces' partial sums meet in
-// the accumulator.
+// Down units cut their k range (I or I_s) into pieces of at most
+// min(I, H)/64/m stages, as equal as possible: no unit is longer than a
+// gate/up unit; the pieces' partial sums meet in the accumulator.  m (1..3) is
+// chosen per launch from the unit count: the one that minimises rounds over
+// the grid x (stages per piece + kTcUnitCost), so that the last round of units
+// stays short.  kTcUnitCost, a unit's fixed cost in stages, was bracketed on
+// GB300: the DeepSeek-shaped layer at 17 tokens (624 units of 22 stages, 4.1
+// rounds, or 1248 of 11) ran faster with m = 1, so it exceeds 2.75; the
+// Phi-shaped one (832 units of 50 stages or 1664 of 25) faster with m = 2, so
+// it is below 5.  Every block computes the same m from n_active.
+constexpr int kTcUnitCost = 4;
 struct TcSplit {
     int pieces, len;  // pieces per 128-row block, k stages per piece (the last may be shorter)
 };
-__device__ __forceinline__ TcSplit tc_split(const TcParams &p, int ks) {
-    const int lim = min(p.I, p.H) / kTcKc;  // >= 1: I and H are multiples of 64
+__device__ __forceinline__ TcSplit tc_split(const TcParams &p, int ks, int m) {
+    const int lim = max(1, min(p.I, p.H) / kTcKc / m);  // I and H are multiples of 64
     TcSplit d;
     d.pieces = ks > 0 ? (ks + lim - 1) / lim : 0;
     d.len = ks > 0 ? (ks + d.pieces - 1) / d.pieces : 0;
     return d;
 }
 // down units: the shared expert's (H/128 blocks x pieces) first, then every active expert's
-__device__ __forceinline__ int tc_dn_count(const TcParams &p, int nact) {
-    const int sh = p.has_shared ? (p.H / 128) * tc_split(p, p.I_s / kTcKc).pieces : 0;
-    return sh + nact * (p.H / 128) * tc_split(p, p.I / kTcKc).pieces;
+__device__ __forceinline__ int tc_dn_count_m(const TcParams &p, int nact, int m) {
+    const int sh = p.has_shared ? (p.H / 128) * tc_split(p, p.I_s / kTcKc, m).pieces : 0;
+    return sh + nact * (p.H / 128) * tc_split(p, p.I / kTcKc, m).pieces;
+}
+__device__ __forceinline__ int tc_down_m(const TcParams &p, int nact, int grid) {
+    int best = 1;
+    long long best_cost = -1;
+    for (int m = 1; m <= 3; ++m) {
+        const int len = tc_split(p, p.I / kTcKc, m).len;
+        const long long cost = (long long)((tc_dn_count_m(p, nact, m) + grid - 1) / grid) * (len + kTcUnitCost);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = m;
+        }
+    }
+    return best;
 }
 // slot_e / slot_n: expert and token count of every slot, staged in shared
 // memory once per block (slot 0, the shared expert: -1 and T).  A unit with
 // t.n == 0 or t.nk == 0 is skipped by every role alike.
 template <bool DOWN>
-__device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *slot_e, const int *slot_n) {
+__device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *slot_e, const int *slot_n, int m) {
     TcUnit t;
     if (!DOWN) {
         const int ns = p.has_shared ? p.I_s / kTcKc : 0;
@@ -238,7 +258,7 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *s
         t.nk = p.H / kTcKc;
         return t;
     }
-    const TcSplit ds = tc_split(p, p.I_s / kTcKc), dr = tc_split(p, p.I / kTcKc);
+    const TcSplit ds = tc_split(p, p.I_s / kTcKc, m), dr = tc_split(p, p.I / kTcKc, m);
     const int ns = p.has_shared ? (p.H / 128) * ds.pieces : 0;
     int a = -1, v = u;
     if (u >= ns) {
@@ -352,7 +372,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
 
     griddep_wait();  // routing, token tables, gathered rows / h are complete
     const int nact = tc_nact(p);
-    const int nunits = DOWN ? tc_dn_count(p, nact) : tc_gu_count(p, nact);
+    const int dm = DOWN ? tc_down_m(p, nact, (int)gridDim.x) : 1;  // down k-piece multiplier
+    const int nunits = DOWN ? tc_dn_count_m(p, nact, dm) : tc_gu_count(p, nact);
     for (int a = threadIdx.x; a <= nact; a += blockDim.x) {
         int e = -1, n = p.T;
         if (a > 0) {
@@ -372,7 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         uint32_t it = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n);
+            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n, dm);
             if (t.n == 0 || t.nk == 0) continue;
             const int nb = (t.n + 15) >> 4;
             const uint32_t bytes = (uint32_t)kTcABytes + (uint32_t)nb * 16 * kTcKc * 2;
@@ -407,7 +428,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         uint32_t it = 0, uc = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n);
+            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n, dm);
             if (t.n == 0 || t.nk == 0) continue;
             const int b = (int)(uc & 1);
             if (!tc_wait(&acce[b], ((uc >> 1) & 1) ^ 1, abort_flag, p)) break;
@@ -440,7 +461,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         uint32_t uc = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n);
+            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n, dm);
             if (t.n == 0 || t.nk == 0) continue;
             const int b = (int)(uc & 1);
             if (!tc_wait(&accf[b], (uc >> 1) & 1, abort_flag, p)) break;
