@@ -478,11 +478,11 @@ struct TcArgs {
 // weight ring shrinks as T x H grows, while the tensor-memory launches stream
 // activation tiles.  Measured on GB300 (DeepSeek-, Qwen- and Phi-shaped
 // layers): at 9 tokens the expert launch is 8-10% faster on the 2048-wide
-// shapes and equal on the 4096-wide one; at 17 tokens the tensor-memory
-// launches are equal or faster on all three (Phi-shaped 24% faster); from 33
-// tokens faster on all.
+// shapes (T x H = 18432) and 3% slower on the 4096-wide one (36864); at 17
+// tokens the tensor-memory launches are equal or faster on all three (Phi-shaped
+// 25% faster); from 33 tokens 35-40% faster, or the only ones with a geometry.
 constexpr int kTcMinT = 17;
-constexpr long long kTcMinTH = 65536;
+constexpr long long kTcMinTH = 36864;
 inline bool tc_preferred(int T, int H) { return T >= kTcMinT || (long long)T * H >= kTcMinTH; }
 // Workspace bytes of a call: launch 0 = spx_workspace_size (room for whichever
 // launches the automatic choice may take), 1 = without the tensor-memory

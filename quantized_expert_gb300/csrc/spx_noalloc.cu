@@ -72,6 +72,7 @@ extern "C" int spx_noalloc_init(void) {
     st = route_preload();
     if (!st) st = engine_preload();
     if (!st) st = draft_preload();
+    if (!st) st = tc_preload();
     if (st) return st;
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
