@@ -540,7 +540,7 @@ def layer_figures(s, sets, torch, spx, stream, peak, n_batches=10):
                      "timing": f"{n_batches} batches of {chain} layer calls back to back; spread over batches"}
         if mode == "verify":
             # the library's automatic choice (every shape here has its tile packs)
-            tc = sets[0]["f16"].tc is not None and (T >= 17 or T * s.H >= 36864)
+            tc = sets[0]["f16"].tc is not None and T >= 9
             out[mode]["launches"] = ("routing + tensor-memory launches (gather, tcgen05 gate/up, tcgen05 down, "
                                      "output)" if tc else "routing + expert launch")
     return out

@@ -217,7 +217,7 @@ typedef struct {
      * tensor-memory launches (spx_f16_tc_repack; I % 64 == 0).  With it (and
      * the shared expert's, when there is one) a verify layer call can run on
      * those launches (tcgen05 products, operands by TMA tensor copies): calls
-     * of 17 to 64 tokens or of T * H >= 36864 by default, any call with
+     * of 9 to 64 tokens by default, any call with
      * spx_layer_args.verify_launch = 2. */
     const void *tc_packed;
 } spx_f16_experts;
@@ -333,7 +333,7 @@ SPX_API int spx_shared_tc_repack(const uint16_t *w_gate, const uint16_t *w_up, c
 SPX_API size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s);
 /* Bytes of workspace for a verify layer call forced onto the tensor-memory
  * launches (spx_layer_args.verify_launch = 2) with T tokens; equal to
- * spx_workspace_size() from T = 17 on and where T * H >= 36864.  0 if the shape cannot take them
+ * spx_workspace_size() from T = 9 on.  0 if the shape cannot take them
  * (I or I_s not a multiple of 64, or outside the limits). */
 SPX_API size_t spx_workspace_size_tc(int T, int H, int I, int E, int k, int I_s);
 /* Zero a workspace; required once before first use (kernels leave it zeroed
@@ -432,8 +432,7 @@ typedef struct {
     /* mode 0 with GGUF draft experts instead of INT4 (w4 must then be NULL). */
     const spx_gguf_experts *gguf;
     /* mode 1: which launches run the experts.  0 = automatic (the
-     * tensor-memory launches for 17 to 64 tokens, or T * H >= 36864, when the
-     * tile packs are given
+     * tensor-memory launches for 9 to 64 tokens when the tile packs are given
      * and no cache-aware option is set, else the expert launch); 1 = the
      * expert launch; 2 = the tensor-memory launches (tile packs required, no
      * cache-aware options, ws_bytes at least spx_workspace_size_tc(); else

@@ -117,7 +117,7 @@ size_t spx::workspace_bytes(int T, int H, int I, int E, int k, int I_s, int laun
 
 extern "C" size_t spx_workspace_size(int T, int H, int I, int E, int k, int I_s) {
     const size_t core = ws_size_core(T, H, I, E, k, I_s);
-    if (!core || !tc_preferred(T, H)) return core;
+    if (!core || !tc_preferred(T)) return core;
     const size_t tc = spx_workspace_size_tc(T, H, I, E, k, I_s);
     return tc > core ? tc : core;
 }
@@ -374,7 +374,7 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
             if (!canon || cache_aware) return SPX_ERR_UNSUPPORTED;
             use_tc = true;
         } else if (a->verify_launch == 0) {
-            use_tc = canon && !cache_aware && tc_preferred(T, H);
+            use_tc = canon && !cache_aware && tc_preferred(T);
         }
     }
     st = check_expert_common(a->x, T, H, E, I, k, a->offsets, a->sorted_slots, a->active, a->n_active, a->ws,

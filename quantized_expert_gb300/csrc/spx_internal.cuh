@@ -472,18 +472,15 @@ struct TcArgs {
     WsHeader *hdr;
     uint64_t wait_budget_ns;
 };
-// Verify calls take the tensor-memory launches (when the experts' tile packs
-// are given) from kTcMinT tokens, or from kTcMinTH activation elements (T x H):
-// the expert launch keeps every activation row in shared memory, so its
-// weight ring shrinks as T x H grows, while the tensor-memory launches stream
-// activation tiles.  Measured on GB300 (DeepSeek-, Qwen- and Phi-shaped
-// layers): at 9 tokens the expert launch is 8-10% faster on the 2048-wide
-// shapes (T x H = 18432) and 3% slower on the 4096-wide one (36864); at 17
-// tokens the tensor-memory launches are equal or faster on all three (Phi-shaped
-// 25% faster); from 33 tokens 35-40% faster, or the only ones with a geometry.
-constexpr int kTcMinT = 17;
-constexpr long long kTcMinTH = 36864;
-inline bool tc_preferred(int T, int H) { return T >= kTcMinT || (long long)T * H >= kTcMinTH; }
+// Verify calls of at least kTcMinT tokens take the tensor-memory launches
+// when the experts' tile packs are given.  Measured on GB300 (DeepSeek-, Qwen-
+// and Phi-shaped layers, µs per layer, expert launch -> tensor-memory
+// launches): 9 tokens 88.9 -> 86.8, 104.7 -> 103.8, 263.2 -> 244.1; 17 tokens
+// 127.0 -> 114.4, 152.8 -> 140.9, 424.8 -> 313.0; from 33 tokens the expert
+// launch is 40% slower or has no geometry (its activation rows stay in shared
+// memory; the tensor-memory launches stream them).
+constexpr int kTcMinT = 9;
+inline bool tc_preferred(int T) { return T >= kTcMinT; }
 // Workspace bytes of a call: launch 0 = spx_workspace_size (room for whichever
 // launches the automatic choice may take), 1 = without the tensor-memory
 // launches' scratch, 2 = spx_workspace_size_tc.

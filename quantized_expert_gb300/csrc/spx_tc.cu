@@ -12,15 +12,19 @@
 //
 //   gather launch   x rows of each active expert (and every token for the
 //                   shared expert) copied into one block of rows per expert
-//                   slot; the shared-expert gate per token.
-//   gate/up launch  unit = (slot, 64 columns of I): D[128 x Np] = A . B^T
-//                   with A = 64 gate rows and 64 up rows of the expert
+//                   slot; the shared-expert gate per token; the slots' ready
+//                   counts zeroed.
+//   product launch  gate/up units, then down units:
+//                   gate/up unit = (slot, 64 columns of I): D[128 x Np] =
+//                   A . B^T with A = 64 gate rows and 64 up rows of the expert
 //                   ([I][H], k = H), B = the slot's Np token rows; epilogue
-//                   h = silu(gate) * up (fp16) into the slot's h rows.
-//   down launch     unit = (slot, 128 rows of H): D[128 x Np] = Wd . h^T
-//                   (k = I); epilogue: each token's share, scaled by its
-//                   routing weight (or the shared gate), added to the fp32
-//                   accumulator of its output row.
+//                   h = silu(gate) * up (fp16) into the slot's h rows, then
+//                   the slot's ready count;
+//                   down unit = (slot, 128 rows of H, a piece of I): D[128 x
+//                   Np] = Wd . h^T, read once the slot's ready count is full;
+//                   epilogue: each token's share, scaled by its routing weight
+//                   (or the shared gate), added to the fp32 accumulator of its
+//                   output row.
 //   output launch   out = fp16(accumulator); the accumulator is cleared.
 //
 // Every launch is a programmatic dependent of the one before it.
@@ -60,6 +64,7 @@ constexpr int kTcThreads = 192;                     // producer, issuer, 4 epilo
 constexpr uint32_t kTcAccCols = 64;                 // columns of one accumulator (Np <= 64)
 constexpr uint32_t kTcTmemCols = 2 * kTcAccCols;    // two accumulators, a power of two >= 32
 constexpr int kTcSlotBytes = 2 * (kMaxE + 1) * 4;    // expert and token count per slot
+static_assert((kMaxE + 1) * 4 <= 3072, "the ready counts fit between the gate and the rows of the scratch");
 constexpr size_t kTcSmem = 1024 + (size_t)kTcStages * kTcStageBytes + 256 + kTcSlotBytes;
 static_assert(kMaxT <= 64, "one accumulator holds every token of a slot");
 
@@ -72,6 +77,7 @@ struct TcParams {
     const TokTable *tables;
     __half *xs, *hs;
     float *gam, *acc;
+    uint32_t *ready;  // per slot: epilogue warps done with a gate/up unit of the slot (4 per unit)
     __half *out;
     WsHeader *hdr;
     uint64_t budget;
@@ -185,6 +191,7 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
 
 // One unit of work, decoded the same way by every role of a block.
 struct TcUnit {
+    bool down; // a down unit (else gate/up)
     int slot;  // 0 = shared expert, 1 + a = active expert a
     int e;     // expert id (routed) or -1
     int n;     // tokens of the slot
@@ -239,10 +246,12 @@ __device__ __forceinline__ int tc_down_m(const TcParams &p, int nact, int grid) 
 // slot_e / slot_n: expert and token count of every slot, staged in shared
 // memory once per block (slot 0, the shared expert: -1 and T).  A unit with
 // t.n == 0 or t.nk == 0 is skipped by every role alike.
-template <bool DOWN>
-__device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *slot_e, const int *slot_n, int m) {
+// Units of the product launch: the ngu gate/up units, then the down units.
+__device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *slot_e, const int *slot_n, int m,
+                                          int ngu) {
     TcUnit t;
-    if (!DOWN) {
+    t.down = u >= ngu;
+    if (!t.down) {
         const int ns = p.has_shared ? p.I_s / kTcKc : 0;
         const int per = p.I / kTcKc;
         int a = -1, v = u;
@@ -258,6 +267,7 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *s
         t.nk = p.H / kTcKc;
         return t;
     }
+    u -= ngu;
     const TcSplit ds = tc_split(p, p.I_s / kTcKc, m), dr = tc_split(p, p.I / kTcKc, m);
     const int ns = p.has_shared ? (p.H / 128) * ds.pieces : 0;
     int a = -1, v = u;
@@ -287,8 +297,10 @@ __device__ __forceinline__ TcUnit tc_unit(const TcParams &p, int u, const int *s
 __global__ void __launch_bounds__(256) tc_gather_kernel(const __grid_constant__ TcParams p, int nslot) {
     griddep_launch_dependents();
     griddep_wait();
-    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    const int gtid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+    const int warp = gtid >> 5, lane = threadIdx.x & 31;
     const int nact = tc_nact(p);
+    if (gtid < nslot) p.ready[gtid] = 0u;  // the product launch reads them after this launch completes
     if (warp < nslot * p.T) {
         const int slot = warp / p.T, r = warp - slot * p.T;
         if (slot > nact || (slot == 0 && !p.has_shared)) return;
@@ -326,9 +338,38 @@ __global__ void __launch_bounds__(256) tc_gather_kernel(const __grid_constant__ 
     if (lane == 0) p.gam[t] = g;
 }
 
-// ------------------------------------------------- product launches ----
-template <bool DOWN>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant__ TcParams p) {
+// ------------------------------------------------- product launch ------
+__device__ __forceinline__ uint32_t tc_ld_acquire(const uint32_t *c) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    return v;
+}
+// Bounded wait until *c >= target (another block's gate/up epilogues), then
+// the h rows they stored may be read by TMA copies (async proxy).
+__device__ __forceinline__ bool tc_wait_count(const uint32_t *c, uint32_t target, volatile int *abort,
+                                              const TcParams &p) {
+    if (tc_ld_acquire(c) < target) {
+        const uint64_t t0 = global_timer_ns();
+        while (tc_ld_acquire(c) < target) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > p.budget) {
+                record_timeout(&p.hdr->status, SITE_TC);
+                *abort = 1;
+                return false;
+            }
+            __nanosleep(128);
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// Gate/up units of every slot, then the down units, in one persistent launch:
+// a down unit's h rows are read once the slot's gate/up units have all been
+// drained (its ready count).  Every block takes its gate/up units before any
+// down unit, and a block's own epilogue never waits for its producer, so each
+// wait ends once the gate/up units ahead of it are done.
+__global__ void __launch_bounds__(kTcThreads, 1) tc_mlp_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t tc_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)kTcStages * kTcStageBytes);
@@ -358,7 +399,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&p.tm_w);
-        prefetch_tmap(DOWN ? &p.tm_hs : &p.tm_xs);
+        prefetch_tmap(&p.tm_xs);
+        prefetch_tmap(&p.tm_hs);
         if (p.has_shared) prefetch_tmap(&p.tm_sw);
     }
     if (warp == 1) {
@@ -370,10 +412,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    griddep_wait();  // routing, token tables, gathered rows / h are complete
+    griddep_wait();  // routing, token tables, gathered rows and zeroed ready counts are complete
     const int nact = tc_nact(p);
-    const int dm = DOWN ? tc_down_m(p, nact, (int)gridDim.x) : 1;  // down k-piece multiplier
-    const int nunits = DOWN ? tc_dn_count_m(p, nact, dm) : tc_gu_count(p, nact);
+    const int dm = tc_down_m(p, nact, (int)gridDim.x);  // down k-piece multiplier
+    const int ngu = tc_gu_count(p, nact);
+    const int nunits = ngu + tc_dn_count_m(p, nact, dm);
     for (int a = threadIdx.x; a <= nact; a += blockDim.x) {
         int e = -1, n = p.T;
         if (a > 0) {
@@ -393,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         uint32_t it = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n, dm);
+            const TcUnit t = tc_unit(p, u, slot_e, slot_n, dm, ngu);
             if (t.n == 0 || t.nk == 0) continue;
             const int nb = (t.n + 15) >> 4;
             const uint32_t bytes = (uint32_t)kTcABytes + (uint32_t)nb * 16 * kTcKc * 2;
@@ -404,17 +447,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                     ok = false;
                     break;
                 }
+                const int Iw = t.slot == 0 ? p.I_s : p.I;
+                // a down unit's h rows: once every gate/up unit of the slot has been drained
+                if (t.down && kc == 0 &&
+                    !tc_wait_count(p.ready + t.slot, 4u * (uint32_t)(Iw / kTcKc), abort_flag, p)) {
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(&full[s], bytes);
                 uint8_t *sa = ring + (size_t)s * kTcStageBytes, *sb = sa + kTcABytes;
                 const int k0 = (t.kc0 + kc) * kTcKc;
                 // the unit's tile for this k-chunk (pack order: expert, gate/up tiles, down tiles)
-                const int Iw = t.slot == 0 ? p.I_s : p.I;
                 const int gu_tiles = (Iw / kTcKc) * (p.H / kTcKc);
                 const int tile = (t.slot == 0 ? 0 : t.e * (3 * gu_tiles / 2)) +
-                                 (DOWN ? gu_tiles + (t.pos / 128) * (Iw / kTcKc) : (t.pos / kTcKc) * (p.H / kTcKc)) +
+                                 (t.down ? gu_tiles + (t.pos / 128) * (Iw / kTcKc) : (t.pos / kTcKc) * (p.H / kTcKc)) +
                                  t.kc0 + kc;
                 tma_load_3d(sa, t.slot == 0 ? &p.tm_sw : &p.tm_w, 0, 0, tile, &full[s], pol_w);
-                const CUtensorMap *tb = DOWN ? &p.tm_hs : &p.tm_xs;
+                const CUtensorMap *tb = t.down ? &p.tm_hs : &p.tm_xs;
                 for (int j = 0; j < nb; ++j) tma_load_2d(sb + j * 2048, tb, k0, brow + 16 * j, &full[s], pol_act);
             }
         }
@@ -428,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         uint32_t it = 0, uc = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n, dm);
+            const TcUnit t = tc_unit(p, u, slot_e, slot_n, dm, ngu);
             if (t.n == 0 || t.nk == 0) continue;
             const int b = (int)(uc & 1);
             if (!tc_wait(&acce[b], ((uc >> 1) & 1) ^ 1, abort_flag, p)) break;
@@ -461,14 +510,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         uint32_t uc = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const TcUnit t = tc_unit<DOWN>(p, u, slot_e, slot_n, dm);
+            const TcUnit t = tc_unit(p, u, slot_e, slot_n, dm, ngu);
             if (t.n == 0 || t.nk == 0) continue;
             const int b = (int)(uc & 1);
             if (!tc_wait(&accf[b], (uc >> 1) & 1, abort_flag, p)) break;
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)b * kTcAccCols;
             const int np = (t.n + 15) & ~15;
-            if (!DOWN) {
+            if (!t.down) {
                 // lane l < 16: gate column pos+16q+l; lane l+16: the same up column
                 const int col = t.pos + 16 * q + (lane & 15);
                 __half *hrow = p.hs + (size_t)t.slot * p.npm * p.Imax + col;
@@ -485,6 +534,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(const __grid_constant
                         }
                     }
                 }
+                __threadfence();  // this lane's h stores, before the slot's ready count
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.ready + t.slot, 1u);
             } else {
                 const int hcol = t.pos + 32 * q + lane;  // output column of this lane
                 const TokEntry *ent = t.slot == 0 ? nullptr : p.tables[t.e].e;
@@ -648,13 +700,12 @@ size_t tc_scratch_bytes(int T, int H, int I, int E, int k, int I_s) {
     const size_t nslot = (size_t)(E < T * k ? E : T * k) + 1;
     const size_t npm = (size_t)((T + 15) & ~15);
     const size_t imax = (size_t)(I > I_s ? I : I_s);
-    return 1024 + nslot * npm * ((size_t)H + imax) * 2;
+    return 4096 + nslot * npm * ((size_t)H + imax) * 2;  // gate, ready counts, rows, h
 }
 
 int tc_preload() {
     const int sm = (int)kTcSmem;
-    if (cudaFuncSetAttribute(tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) != cudaSuccess)
+    if (cudaFuncSetAttribute(tc_mlp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) != cudaSuccess)
         return SPX_ERR_CUDA;
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, tc_gather_kernel) != cudaSuccess ||
@@ -680,7 +731,8 @@ int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl) {
     const int imax = I > I_s ? I : I_s;
     uint8_t *scr = static_cast<uint8_t *>(a.scratch);
     p.gam = reinterpret_cast<float *>(scr);
-    p.xs = reinterpret_cast<__half *>(scr + 1024);
+    p.ready = reinterpret_cast<uint32_t *>(scr + 1024);
+    p.xs = reinterpret_cast<__half *>(scr + 4096);
     p.hs = p.xs + (size_t)nslot * npm * H;
     bool ok = map_tiles(&p.tm_w, a.routed_tc, (uint64_t)E * tc_tiles(H, I)) &&
               map_rows(&p.tm_xs, p.xs, H, (uint64_t)nslot * npm, 16) &&
@@ -712,9 +764,7 @@ int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl) {
     int st = record_launch(cudaLaunchKernelEx(&cfg, tc_gather_kernel, p, nslot));
     if (st) return st;
     cfg = tc_config(dim3(nsm), kTcThreads, kTcSmem, s, true, attr);
-    st = record_launch(cudaLaunchKernelEx(&cfg, tc_kernel<false>, p));
-    if (st) return st;
-    st = record_launch(cudaLaunchKernelEx(&cfg, tc_kernel<true>, p));
+    st = record_launch(cudaLaunchKernelEx(&cfg, tc_mlp_kernel, p));
     if (st) return st;
     cfg = tc_config(dim3(4 * nsm), 256, 0, s, true, attr);
     return record_launch(cudaLaunchKernelEx(&cfg, tc_out_kernel, p));

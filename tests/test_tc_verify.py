@@ -76,12 +76,13 @@ def test_tc_verify_no_shared_expert():
 
 
 @pytest.mark.parametrize("name,T", [("phi35_moe", 33), ("phi35_moe", 17), ("deepseek_v2_lite", 33),
-                                    ("qwen15_moe", 33), ("deepseek_v2_lite", 17)])
+                                    ("qwen15_moe", 33), ("deepseek_v2_lite", 17), ("qwen15_moe", 9),
+                                    ("deepseek_v2_lite", 5)])
 def test_tc_verify_full_size(name, T):
-    """Full-size layers on the tensor-memory launches: at 33 tokens through the
-    automatic choice (Phi-3.5-MoE at 33 tokens has no expert-launch geometry),
-    at 17 forced."""
-    _check(W.CONFIGS[name], T, step=260 + T, launch=0 if T >= 25 else 2)
+    """Full-size layers on the tensor-memory launches: from 9 tokens through
+    the automatic choice (Phi-3.5-MoE at 33 tokens has no expert-launch
+    geometry), at 5 forced."""
+    _check(W.CONFIGS[name], T, step=260 + T, launch=0 if T >= 9 else 2)
 
 
 def test_tc_verify_invalid_calls():
@@ -90,7 +91,7 @@ def test_tc_verify_invalid_calls():
     misaligned pack is an invalid argument."""
     spx, gh = _spx(), _gh()
     s = W.scaled(W.CONFIGS["deepseek_v2_lite"], I=256, E=16, I_s=512)
-    T = 9  # below the automatic choice: spx_workspace_size leaves the tensor-memory scratch out
+    T = 5  # below the automatic choice: spx_workspace_size leaves the tensor-memory scratch out
     x = W.gen_x(s, T, step=270)
     lay = gh.Layer(s, needed=list(range(s.E)), draft=False, verify=True)
     routing = spx.Routing.empty(T, s.E, s.k)
