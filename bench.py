@@ -50,11 +50,10 @@ KERNEL_SOURCES = {
     "verify": ["spx_tc.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "tc_kernel<0> + tc_kernel<1>",
-               "dram_bytes": 452_486_400 + 3_636_736 + 226_958_336 + 2_780_672,
-               "algorithmic_bytes": 674_897_920, "source_sha": "832f3b8be5e311a7"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 203_520, "algorithmic_bytes": 61_374_720,
-              "source_sha": "f69c7bd963540eb8"},
+    "verify": {"kernel": "tc_mlp_kernel", "dram_bytes": 677_525_248 + 4_071_680,
+               "algorithmic_bytes": 674_897_920, "source_sha": "41122d04f99e7f41"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_648 + 278_272, "algorithmic_bytes": 61_374_720,
+              "source_sha": "fbf1bc63f78240c9"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
@@ -449,9 +448,8 @@ def run_mine(args):
                      "launch_us": round(d_us, 2), "bytes_per_launch": int(draft_bytes / n_draft),
                      "timing": f"CUDA events around the draft phase of every timed cycle ({n_draft} launches back "
                                f"to back on the launching stream), median over cycles / {n_draft}"},
-        "verify_roofline": {"bound": "hbm", "kernel": "route_kernel + tc_gather_kernel + tc_kernel<0> (tcgen05 "
-                                                      "gate/up) + tc_kernel<1> (tcgen05 down) + tc_out_kernel "
-                                                      "(verify layer)",
+        "verify_roofline": {"bound": "hbm", "kernel": "route_kernel + tc_gather_kernel + tc_mlp_kernel (tcgen05 "
+                                                      "gate/up and down) + tc_out_kernel (verify layer)",
                             "achieved": round(verify_bytes / L / (v_us * 1e-6) / 1e9, 1), "peak": peak,
                             "unit": "GB/s", "frac": round(verify_bytes / L / (v_us * 1e-6) / 1e9 / peak, 3),
                             "layer_us": round(v_us, 2), "bytes_per_layer": int(verify_bytes / L),
@@ -460,9 +458,9 @@ def run_mine(args):
         "clocks": clocks,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        # per cycle: K*L draft launches; per verify layer a routing launch and the four tensor-memory
-        # launches (gather, gate/up, down, output)
-        "gpu_launches": (n_draft + 5 * L) * args.steps,
+        # per cycle: K*L draft launches; per verify layer a routing launch and the three tensor-memory
+        # launches (gather, gate/up + down, output)
+        "gpu_launches": (n_draft + 4 * L) * args.steps,
     }
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s)
@@ -541,8 +539,8 @@ def layer_figures(s, sets, torch, spx, stream, peak, n_batches=10):
         if mode == "verify":
             # the library's automatic choice (every shape here has its tile packs)
             tc = sets[0]["f16"].tc is not None and T >= 9
-            out[mode]["launches"] = ("routing + tensor-memory launches (gather, tcgen05 gate/up, tcgen05 down, "
-                                     "output)" if tc else "routing + expert launch")
+            out[mode]["launches"] = ("routing + tensor-memory launches (gather, tcgen05 gate/up + down, output)"
+                                     if tc else "routing + expert launch")
     return out
 
 
