@@ -70,6 +70,15 @@ def test_tc_verify_small_shared_gate_and_router():
     _check(W.scaled(W.CONFIGS["qwen15_moe"], I=384, E=12, I_s=640), 40, step=240)
 
 
+@pytest.mark.parametrize("E,k,T,I_s", [(256, 8, 64, 192), (8, 8, 33, 0), (16, 4, 9, 320)])
+def test_tc_verify_slot_extremes(E, k, T, I_s):
+    """Slot-table extremes of the tensor-memory launches: 257 slots (256
+    experts, top-8 of 64 tokens), every expert selected (k = E), and shared
+    experts whose k range is not a multiple of the routed one (uneven down
+    pieces), at the automatic token threshold."""
+    _check(W.scaled(W.CONFIGS["deepseek_v2_lite"], H=256, I=128, E=E, k=k, I_s=I_s), T, step=280 + T)
+
+
 def test_tc_verify_no_shared_expert():
     """Phi-shaped (no shared expert, renormalised top-2), small, 33 tokens."""
     _check(W.scaled(W.CONFIGS["phi35_moe"], H=1024, I=512), 33, step=250)
