@@ -391,6 +391,35 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
     const bool via_draft = !cache_aware && draft_supported(T, H, I, S, I_s, E, k, kq);
     if (gguf && !via_draft && !engine_fits(T, H, gguf_fmt(a->gguf), 16)) return SPX_ERR_UNSUPPORTED;
     if (zeros && !via_draft && !engine_fits(T, H, kFmtW4Z, S)) return SPX_ERR_UNSUPPORTED;
+    // the tensor-memory launches' parameters (their tensor maps checked) before anything is enqueued
+    TcPlan tc_storage;
+    TcPlan *tc = nullptr;
+    if (use_tc) {
+        TcArgs t{};
+        t.x = reinterpret_cast<const __half *>(a->x);
+        t.T = T;
+        t.H = H;
+        t.E = E;
+        t.I = I;
+        t.k = k;
+        t.I_s = I_s;
+        t.routed_tc = a->f16->tc_packed;
+        if (a->shared) {
+            t.shared_tc = a->shared->tc_packed;
+            t.w_sgate = reinterpret_cast<const __half *>(a->shared->w_sgate);
+        }
+        t.active = a->active;
+        t.n_active = a->n_active;
+        t.tables = ws_tables(a->ws, T, H);
+        t.scratch = static_cast<uint8_t *>(a->ws) + ws_tc_offset(T, H);
+        t.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
+        t.out = reinterpret_cast<__half *>(a->out);
+        t.hdr = static_cast<WsHeader *>(a->ws);
+        t.wait_budget_ns = budget;
+        st = tc_plan(t, &tc_storage);
+        if (st) return st;
+        tc = &tc_storage;
+    }
     // every check has passed: only now may the caller's scratch be cleared
     if (clear) {
         const cudaError_t ce = cudaMemsetAsync(clear, 0, clear_bytes, s);
@@ -471,30 +500,9 @@ int spx::moe_layer(const spx_layer_args *a, cudaStream_t s, void *clear, size_t 
     if (st) return st;
 
     if (use_tc) {
-        TcArgs t{};
-        t.x = reinterpret_cast<const __half *>(a->x);
-        t.T = T;
-        t.H = H;
-        t.E = E;
-        t.I = I;
-        t.k = k;
-        t.I_s = I_s;
-        t.routed_tc = a->f16->tc_packed;
-        if (a->shared) {
-            t.shared_tc = a->shared->tc_packed;
-            t.w_sgate = reinterpret_cast<const __half *>(a->shared->w_sgate);
-        }
-        t.active = a->active;
-        t.n_active = a->n_active;
-        t.tables = ws_tables(a->ws, T, H);
-        t.scratch = static_cast<uint8_t *>(a->ws) + ws_tc_offset(T, H);
-        t.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(a->ws) + kWsAccOffset);
-        t.out = reinterpret_cast<__half *>(a->out);
-        t.hdr = static_cast<WsHeader *>(a->ws);
-        t.wait_budget_ns = budget;
         if (a->ev_experts_begin && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_begin), s) != cudaSuccess)
             return SPX_ERR_CUDA;
-        st = launch_tc_verify(t, s, !timed);
+        st = launch_tc_plan(*tc, s, !timed);
         if (st) return st;
         if (a->ev_experts_end && cudaEventRecord(static_cast<cudaEvent_t>(a->ev_experts_end), s) != cudaSuccess)
             return SPX_ERR_CUDA;

@@ -489,7 +489,13 @@ size_t tc_scratch_bytes(int T, int H, int I, int E, int k, int I_s);
 size_t tc_tiles(int H, int I);  // 16 KB tiles of one expert's pack
 int launch_tc_repack(const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, int E, int H, int I, void *dst,
                      cudaStream_t s);
-int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl);
+// The launches' parameters (tensor maps encoded, every pointer checked): made
+// before anything of the call is enqueued, launched after the routing launch.
+struct alignas(128) TcPlan {
+    unsigned char bytes[2048];
+};
+int tc_plan(const TcArgs &a, TcPlan *plan);
+int launch_tc_plan(const TcPlan &plan, cudaStream_t s, bool pdl);
 int tc_preload();
 
 // -------------------------------------------------------- host helpers --

@@ -82,7 +82,9 @@ struct TcParams {
     WsHeader *hdr;
     uint64_t budget;
     int T, H, E, I, I_s, npm, Imax, has_shared;
+    int nslot;  // 1 + min(E, T*k)
 };
+static_assert(sizeof(TcParams) <= sizeof(TcPlan) && alignof(TcParams) <= alignof(TcPlan), "a plan holds the params");
 
 // ------------------------------------------------------------- PTX ----
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y, uint64_t *bar,
@@ -714,7 +716,7 @@ int tc_preload() {
     return encode_fn() ? SPX_OK : SPX_ERR_UNSUPPORTED;
 }
 
-int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl) {
+int tc_plan(const TcArgs &a, TcPlan *plan) {
     static thread_local int loaded_dev = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SPX_ERR_CUDA;
@@ -756,12 +758,18 @@ int launch_tc_verify(const TcArgs &a, cudaStream_t s, bool pdl) {
     p.npm = npm;
     p.Imax = imax;
     p.has_shared = I_s > 0;
+    p.nslot = nslot;
+    memcpy(plan->bytes, &p, sizeof(p));
+    return SPX_OK;
+}
 
+int launch_tc_plan(const TcPlan &plan, cudaStream_t s, bool pdl) {
+    const TcParams &p = *reinterpret_cast<const TcParams *>(plan.bytes);
     const int nsm = device_sm_count();
     cudaLaunchAttribute attr[1];
-    const int gwarps = (nslot + 1) * T;  // slot rows, then the gate's tokens
+    const int gwarps = (p.nslot + 1) * p.T;  // slot rows, then the gate's tokens
     cudaLaunchConfig_t cfg = tc_config(dim3((gwarps + 7) / 8), 256, 0, s, pdl, attr);
-    int st = record_launch(cudaLaunchKernelEx(&cfg, tc_gather_kernel, p, nslot));
+    int st = record_launch(cudaLaunchKernelEx(&cfg, tc_gather_kernel, p, p.nslot));
     if (st) return st;
     cfg = tc_config(dim3(nsm), kTcThreads, kTcSmem, s, true, attr);
     st = record_launch(cudaLaunchKernelEx(&cfg, tc_mlp_kernel, p));
