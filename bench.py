@@ -50,10 +50,10 @@ KERNEL_SOURCES = {
     "verify": ["spx_tc.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "tc_mlp_kernel", "dram_bytes": 677_525_248 + 4_071_680,
-               "algorithmic_bytes": 674_897_920, "source_sha": "41122d04f99e7f41"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_648 + 278_272, "algorithmic_bytes": 61_374_720,
-              "source_sha": "fbf1bc63f78240c9"},
+    "verify": {"kernel": "tc_mlp_kernel", "dram_bytes": 677_603_840 + 3_597_568,
+               "algorithmic_bytes": 674_897_920, "source_sha": "60bb6eede37c1726"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_392 + 211_456, "algorithmic_bytes": 61_374_720,
+              "source_sha": "525706840b0f860e"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16
