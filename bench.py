@@ -52,8 +52,8 @@ KERNEL_SOURCES = {
 PROFILED_TRAFFIC = {
     "verify": {"kernel": "tc_mlp_kernel", "dram_bytes": 677_603_840 + 3_597_568,
                "algorithmic_bytes": 674_897_920, "source_sha": "60bb6eede37c1726"},
-    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_499_392 + 211_456, "algorithmic_bytes": 61_374_720,
-              "source_sha": "525706840b0f860e"},
+    "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 238_848, "algorithmic_bytes": 61_374_720,
+              "source_sha": "b75136a8eb199793"},
 }
 NSETS = 8  # default; --sets overrides (profiling captures use fewer)
 NINPUTS = 16

@@ -440,7 +440,8 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L,
         return true;
     };
     // Issues fills 0..n-1 of the unit (lane j holds fill j), in rounds of at
-    // most wmax lanes whose stages are all free.
+    // most wmax lanes (distinct stages); within a round each lane issues its
+    // fill as soon as its own stage is free.
     auto issue_fills = [&](const DFill &f, int n) -> bool {
         __syncwarp();  // lanes that finished describing their fill early wait here
         for (int base = 0; base < n; base += wmax) {
@@ -450,48 +451,64 @@ __device__ void dk_producer(const DkParams &p, uint8_t *smem, const DkLayout &L,
             const int st = mine ? (int)(fi % (uint32_t)nst) : 0;
             const uint32_t par = ((fi / (uint32_t)nst) & 1u) ^ 1u;
             const uint32_t tr_w = TR_NOW();
-            bool free_ = !mine || mbar_try_wait(&empty[st], par);
-            if (!__all_sync(kAll, free_)) {
-                const uint64_t t0 = global_timer_ns();
-                while (true) {
-                    if (!free_) free_ = mbar_try_wait_sleep(&empty[st], par, kDkSleepNs);
-                    if (__all_sync(kAll, free_)) break;
-                    if (rd0(misc)) {
-                        ok = false;
-                        return false;
+            bool done = !mine;
+            uint64_t t0 = 0;
+            bool waited = false;
+            while (true) {
+                const bool go = !done && (waited ? mbar_try_wait_sleep(&empty[st], par, kDkSleepNs)
+                                                 : mbar_try_wait(&empty[st], par));
+                const bool hs = go && f.hs_bytes;
+                if (go) {
+                    DHeader h = f.h;
+                    h.seq = (int)fi;
+                    h.hpar = (int)((hpar_bits >> st) & 1u);
+                    hdrs[st] = h;
+                    uint8_t *dst = ring + (size_t)st * L.stage;
+                    mbar_arrive_expect_tx(&full[st], f.bytes + f.zbytes);
+                    if (f.bytes) bulk_g2s(dst, f.src, f.bytes, &full[st], pol);
+                    if (f.zbytes) bulk_g2s(dst + f.zoff, f.zsrc, f.zbytes, &full[st], pol);
+                    if (hs) {
+                        mbar_arrive_expect_tx(&hfull[st], f.hs_bytes);  // completed by the poller's copy
+                        pend[st].src = f.hsrc;
+                        pend[st].rdy = f.rdy;
+                        pend[st].target = f.target;
+                        pend[st].bytes = f.hs_bytes;
+                        pend[st].t_reg = TL_NOW();
                     }
-                    if (expired(t0)) {
-                        timed_out(SITE_STAGE);
-                        return false;
+                    done = true;
+                }
+                const uint32_t hmask = __reduce_or_sync(kAll, hs ? (1u << st) : 0u);
+                if (hmask) {
+                    __threadfence_block();  // the pending entries before their flags
+                    if (hs) pstate[st] = 1;
+                    hpar_bits ^= hmask;
+                }
+                if (__all_sync(kAll, done)) break;
+                if (!waited) {
+                    waited = true;
+                    t0 = global_timer_ns();
+                }
+                // giving up: the fills this round did issue land (bounded) before the block may exit
+                auto drain_round = [&]() {
+                    if (mine && done) {
+                        const uint64_t td = global_timer_ns();
+                        while (!mbar_try_wait(&full[st], (fi / (uint32_t)nst) & 1u) &&
+                               global_timer_ns() - td < 100000000ull) {
+                        }
                     }
+                };
+                if (rd0(misc)) {
+                    drain_round();
+                    ok = false;
+                    return false;
+                }
+                if (expired(t0)) {
+                    timed_out(SITE_STAGE);
+                    drain_round();
+                    return false;
                 }
             }
             const uint32_t tr_r = TR_NOW();
-            const bool hs = mine && f.hs_bytes;
-            if (mine) {
-                DHeader h = f.h;
-                h.seq = (int)fi;
-                h.hpar = (int)((hpar_bits >> st) & 1u);
-                hdrs[st] = h;
-                uint8_t *dst = ring + (size_t)st * L.stage;
-                mbar_arrive_expect_tx(&full[st], f.bytes + f.zbytes);
-                if (f.bytes) bulk_g2s(dst, f.src, f.bytes, &full[st], pol);
-                if (f.zbytes) bulk_g2s(dst + f.zoff, f.zsrc, f.zbytes, &full[st], pol);
-                if (hs) {
-                    mbar_arrive_expect_tx(&hfull[st], f.hs_bytes);  // completed by the poller's copy
-                    pend[st].src = f.hsrc;
-                    pend[st].rdy = f.rdy;
-                    pend[st].target = f.target;
-                    pend[st].bytes = f.hs_bytes;
-                    pend[st].t_reg = TL_NOW();
-                }
-            }
-            const uint32_t hmask = __reduce_or_sync(kAll, hs ? (1u << st) : 0u);
-            if (hmask) {
-                __threadfence_block();  // the pending entries before their flags
-                if (hs) pstate[st] = 1;
-                hpar_bits ^= hmask;
-            }
 #if TL_ON
             if (mine && TR_ON() && fi < (uint32_t)kTrFills) {
                 s_tr.fill[fi][0] = tr_w;
