@@ -158,3 +158,37 @@ def test_draft_format_sizes_and_validation(lib):
     g = spx.GgufExperts(256, 8, 256, 512, 9)
     assert lib.spx_moe_draft_gguf(fake, 4, C.byref(g), 2, fake, fake, fake, fake, fake, None, 0, None) == \
         spx.SPX_ERR_WORKSPACE
+
+
+def test_verify_launch_choice_validation(lib):
+    """The layer call's checks of the tensor-memory verify arguments happen on
+    the host, before any CUDA call: an unknown verify_launch, a misaligned tile
+    pack, a forced call without tile packs, and a forced call whose workspace
+    lacks the tensor-memory scratch."""
+    from quantized_expert_gb300 import spx
+    fake = 1 << 20  # aligned, never dereferenced
+    T, H, E, k, I, I_s = 5, 2048, 64, 6, 1408, 2816
+    f16 = spx.F16Experts(fake, E, H, I, None)
+    sh = spx.Shared(fake, None, H, I_s, None)
+
+    def args(verify_launch, tc_packed=None, sh_tc=None, ws_bytes=None):
+        a = spx.LayerArgs()
+        a.mode, a.T, a.H, a.E, a.k = 1, T, H, E, k
+        a.x = a.logits = a.topk_ids = a.topk_w = fake
+        a.counts = a.offsets = a.sorted_slots = a.active = a.n_active = a.out = a.ws = fake
+        a.ws_bytes = ws_bytes if ws_bytes is not None else lib.spx_workspace_size(T, H, I, E, k, I_s)
+        f16.tc_packed = tc_packed
+        sh.tc_packed = sh_tc
+        a.f16 = C.pointer(f16)
+        a.shared = C.pointer(sh)
+        a.verify_launch = verify_launch
+        return a
+
+    assert lib.spx_moe_layer(C.byref(args(3)), None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_moe_layer(C.byref(args(-1)), None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_moe_layer(C.byref(args(2, tc_packed=fake + 8, sh_tc=fake)), None) == spx.SPX_ERR_INVALID_ARG
+    assert lib.spx_moe_layer(C.byref(args(2)), None) == spx.SPX_ERR_UNSUPPORTED
+    assert lib.spx_moe_layer(C.byref(args(2, tc_packed=fake)), None) == spx.SPX_ERR_UNSUPPORTED  # shared lacks one
+    # T = 5: the default workspace has no tensor-memory scratch, a forced call needs spx_workspace_size_tc
+    assert lib.spx_workspace_size_tc(T, H, I, E, k, I_s) > lib.spx_workspace_size(T, H, I, E, k, I_s)
+    assert lib.spx_moe_layer(C.byref(args(2, tc_packed=fake, sh_tc=fake)), None) == spx.SPX_ERR_WORKSPACE
