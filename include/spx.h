@@ -443,10 +443,14 @@ typedef struct {
 /* One layer.  Draft calls with T <= 5 (and no cache-aware options) are one
  * launch that routes its tokens in every block (after a router-product launch
  * when w_router is given); other calls are a routing launch (router product,
- * softmax, top-k, counters, counting sort, token tables) and one persistent
- * expert launch that streams the shared expert first, then every active
- * expert's units, and writes out[] from its last blocks.  Every launch of the
- * call may begin while the one before it on the stream finishes (programmatic
+ * softmax, top-k, counters, counting sort, token tables) and then either one
+ * persistent expert launch that streams the shared expert first, then every
+ * active expert's units, and writes out[] from its last blocks, or (verify
+ * calls of 9+ tokens with the tile packs, see verify_launch) the
+ * tensor-memory launches: a gather of each expert's token rows, one
+ * persistent tcgen05 launch for every expert's gate/up and then down products
+ * [P1 Key Contributions 4], and an output launch.  Every launch of the call
+ * may begin while the one before it on the stream finishes (programmatic
  * dependent launch): it reads nothing that launch writes before it has
  * completed. */
 SPX_API int spx_moe_layer(const spx_layer_args *args, spx_stream_t stream);
