@@ -86,11 +86,11 @@ def test_tc_verify_no_shared_expert():
 
 @pytest.mark.parametrize("name,T", [("phi35_moe", 33), ("phi35_moe", 17), ("deepseek_v2_lite", 33),
                                     ("qwen15_moe", 33), ("deepseek_v2_lite", 17), ("qwen15_moe", 9),
-                                    ("deepseek_v2_lite", 5)])
+                                    ("deepseek_v2_lite", 5), ("deepseek_v2_lite", 64), ("phi35_moe", 64)])
 def test_tc_verify_full_size(name, T):
     """Full-size layers on the tensor-memory launches: from 9 tokens through
     the automatic choice (Phi-3.5-MoE at 33 tokens has no expert-launch
-    geometry), at 5 forced."""
+    geometry; 64 tokens is the maximum call), at 5 forced."""
     _check(W.CONFIGS[name], T, step=260 + T, launch=0 if T >= 9 else 2)
 
 
