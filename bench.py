@@ -50,8 +50,8 @@ KERNEL_SOURCES = {
     "verify": ["spx_tc.cu", "spx_route.cu", "spx_routing.cuh", "spx_internal.cuh"],
 }
 PROFILED_TRAFFIC = {
-    "verify": {"kernel": "tc_mlp_kernel", "dram_bytes": 677_603_840 + 3_597_568,
-               "algorithmic_bytes": 674_897_920, "source_sha": "60bb6eede37c1726"},
+    "verify": {"kernel": "tc_mlp_kernel", "dram_bytes": 677_542_912 + 3_924_480,
+               "algorithmic_bytes": 674_897_920, "source_sha": "09a4a987efe1e0e7"},
     "draft": {"kernel": "draft_kernel<2,0>", "dram_bytes": 61_500_160 + 238_848, "algorithmic_bytes": 61_374_720,
               "source_sha": "b75136a8eb199793"},
 }

@@ -1,14 +1,15 @@
 // spx_tc.cu -- verify experts on the fifth-generation tensor cores: tcgen05
 // products with accumulators in tensor memory, operands staged by TMA tensor
-// copies, for verify calls whose experts hold many tokens.
+// copies; the layer call takes this path for verify calls of 9 tokens or more.
 //
 // [P1 Key Contributions 4: expert-wise verification reordering turns the
 // per-token expert GEMVs into one dense product per expert over the tokens it
 // holds.]  The expert launch (spx_engine.cu) keeps every activation row of the
-// call in shared memory and issues mma.sync tiles of 8 tokens; above ~24
-// tokens that geometry runs out of shared memory.  This path instead streams
-// activation tiles next to the weight tiles, so its shared memory does not
-// grow with the token count:
+// call in shared memory and issues mma.sync tiles of 8 tokens, so its weight
+// ring shrinks as the token count grows and above ~24 tokens (4096-wide: ~17)
+// its geometry runs out.  This path streams activation tiles next to the
+// weight tiles, so its shared memory does not grow with the token count, and
+// one thread issues the products, leaving the other warps to the epilogue:
 //
 //   gather launch   x rows of each active expert (and every token for the
 //                   shared expert) copied into one block of rows per expert
