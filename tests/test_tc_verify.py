@@ -127,3 +127,36 @@ def test_tc_verify_invalid_calls():
     assert call(lay.f16, ws, launch=3) == spx.SPX_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert spx.spx_workspace_status(ws) == 0
+
+
+def test_tile_pack_layout_matches_the_header():
+    """spx_f16_tc_repack writes the layout include/spx.h documents: per expert,
+    gate/up tiles (unit u, k-chunk kc) then down tiles (block hb, k-chunk kc),
+    128 rows x 64 fp16 each; gate/up tile row 32q + i is gate column
+    64u + 16q + i (i < 16) or up column 64u + 16q + i - 16.  Checked element by
+    element against the layout built with numpy from the canonical tensors."""
+    spx = _spx()
+    E, H, I = 2, 256, 192
+    rng = np.random.default_rng(5)
+    wg, wu = rng.standard_normal((E, I, H)).astype(np.float16), rng.standard_normal((E, I, H)).astype(np.float16)
+    wd = rng.standard_normal((E, H, I)).astype(np.float16)
+    dev = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
+    buf = spx.spx_f16_tc_repack(dev(wg), dev(wu), dev(wd))
+    torch.cuda.synchronize()
+    got = buf.cpu().numpy().view(np.float16)
+    tiles = []
+    for e in range(E):
+        for u in range(I // 64):
+            for kc in range(H // 64):
+                t = np.empty((128, 64), np.float16)
+                for q in range(4):
+                    cols = 64 * u + 16 * q + np.arange(16)
+                    t[32 * q:32 * q + 16] = wg[e, cols, 64 * kc:64 * kc + 64]
+                    t[32 * q + 16:32 * q + 32] = wu[e, cols, 64 * kc:64 * kc + 64]
+                tiles.append(t)
+        for hb in range(H // 128):
+            for kc in range(I // 64):
+                tiles.append(wd[e, 128 * hb:128 * hb + 128, 64 * kc:64 * kc + 64])
+    want = np.stack(tiles).reshape(-1)
+    assert got.shape == want.shape
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
